@@ -1,0 +1,342 @@
+"""Pins for the fp64 oracle: checks against things other than the oracle itself.
+
+Each test names what fixes the expected value: a closed form, a library
+routine on a special case, brute force, the merged-weight identity
+(W + s B A) x - W x = s B (A x) from the multi-LoRA serving note ("direct
+answer", "interviewer follow-ups": merging gives the same model), or an
+invariant the pages state (None / -1 rows run the base model, zero rank
+padding from the TGI page's "weight preprocessing" section leaves results
+unchanged).  A plausible slip in the oracle -- a dropped term, a wrong sign,
+a transposed operand, a wrong row index, a double rounding -- fails at least
+one of these.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+
+
+def _bits_of(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def _rand_bf16(gen, shape, std=1.0):
+    t = (torch.randn(*shape, generator=gen, dtype=torch.float32) * std).to(torch.bfloat16)
+    return _bits_of(t)
+
+
+# ---------------------------------------------------------------- bf16 ----
+
+def test_bf16_roundtrip_exhaustive():
+    """Every finite bf16 pattern survives bf16 -> double -> bf16 unchanged."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = O.bf16_to_f64(bits)
+    finite = np.isfinite(vals)
+    back = O.f64_to_bf16(vals[finite])
+    np.testing.assert_array_equal(back, bits[finite])
+    # bf16 -> double agrees with the hardware view of bf16 as the top half of binary32
+    ref = (bits[finite].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    np.testing.assert_array_equal(vals[finite], ref)
+
+
+def test_bf16_rne_matches_library_on_binary32_values():
+    """On values exactly representable in binary32 there is no double rounding,
+    so one RNE step to bf16 must agree with torch's binary32 -> bf16 (RNE)."""
+    g = torch.Generator().manual_seed(123)
+    f = torch.cat([
+        torch.randn(200000, generator=g) * 3.0,
+        torch.randn(20000, generator=g) * 1e-38,       # subnormal range
+        torch.randn(20000, generator=g) * 1e38,        # near overflow
+        torch.tensor([3.3961e38, -3.3961e38, 3.39e38, 1e-45, -1e-45, 0.0, -0.0]),
+    ]).to(torch.float32)
+    ref = _bits_of(f.to(torch.bfloat16))
+    got = O.f64_to_bf16(f.numpy().astype(np.float64))
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_bf16_ties_to_even_and_single_rounding():
+    # 1 + 2^-8 lies half-way between 1 and 1 + 2^-7: ties go to the even 1.0.
+    assert O.f64_to_bf16([1 + 2.0 ** -8])[0] == 0x3F80
+    # 1 + 3*2^-8 lies half-way between 1+2^-7 (odd) and 1+2^-6 (even).
+    assert O.f64_to_bf16([1 + 3 * 2.0 ** -8])[0] == 0x3F82
+    # Just above a tie must round up.  Going through binary32 first would lose
+    # the 2^-40 and then round the resulting tie down to 1.0 (double rounding).
+    assert O.f64_to_bf16([1 + 2.0 ** -8 + 2.0 ** -40])[0] == 0x3F81
+    assert O.f64_to_bf16([-(1 + 2.0 ** -8 + 2.0 ** -40)])[0] == 0xBF81
+    # smallest subnormal 2^-133; half of it is a tie that goes to +0
+    assert O.f64_to_bf16([2.0 ** -133])[0] == 0x0001
+    assert O.f64_to_bf16([2.0 ** -134])[0] == 0x0000
+    assert O.f64_to_bf16([1.5 * 2.0 ** -133])[0] == 0x0002
+    # largest finite (2 - 2^-7) 2^127; the tie above it overflows to inf
+    assert O.f64_to_bf16([(2 - 2.0 ** -7) * 2.0 ** 127])[0] == 0x7F7F
+    assert O.f64_to_bf16([(2 - 2.0 ** -8) * 2.0 ** 127])[0] == 0x7F80
+    assert O.f64_to_bf16([float("inf")])[0] == 0x7F80
+    assert O.f64_to_bf16([float("-inf")])[0] == 0xFF80
+    assert (O.f64_to_bf16([float("nan")])[0] & 0x7F80) == 0x7F80
+
+
+def test_bf16_rne_is_nearest_on_doubles():
+    """Definition of round-to-nearest on arbitrary doubles: the result is at
+    least as close as both bf16 neighbours."""
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal(50000) * np.exp(rng.uniform(-20, 20, 50000))
+    b = O.f64_to_bf16(x)
+    r = O.bf16_to_f64(b)
+    up = O.bf16_to_f64((b.astype(np.int32) + 1).astype(np.uint16))
+    dn = O.bf16_to_f64((b.astype(np.int32) - 1).astype(np.uint16))
+    err = np.abs(r - x)
+    assert np.all(err <= np.abs(up - x))
+    assert np.all(err <= np.abs(dn - x))
+    assert np.all(err <= np.abs(x) * 2.0 ** -8)
+
+
+# ------------------------------------------------------------ scaling ----
+
+@pytest.mark.parametrize("alpha,r,rs,expect", [
+    (16, 8, False, 2.0),     # the tiny workload: lora_alpha 16, rank 8
+    (32, 16, False, 2.0),    # the 3B decode workload: alpha 32, rank 16
+    (16, 64, False, 0.25),
+    (16, 64, True, 2.0),     # rsLoRA: alpha / sqrt(r) = 16 / 8
+    (16, 16, True, 4.0),
+])
+def test_scale_closed_form(alpha, r, rs, expect):
+    assert O.scale(alpha, r, rs) == expect
+
+
+def test_scale_rslora_defining_property():
+    for r in (8, 32, 128):
+        s = O.scale(16.0, r, True)
+        assert abs(s * s * r - 256.0) < 1e-12
+        assert O.scale(16.0, r, False) * r == 16.0
+
+
+def test_fold_power_of_two_is_exponent_shift():
+    """Scaling normal bf16 values by 2 (or 1/4) adds 1 (or -2) to the binary
+    exponent field and leaves sign and mantissa bits unchanged."""
+    g = torch.Generator().manual_seed(7)
+    B = _rand_bf16(g, (64, 16), std=0.02)
+    B = B[(B & 0x7F80) > (3 << 7)].reshape(-1, 1)  # normal, away from subnormals
+    np.testing.assert_array_equal(O.fold_B(B, 2.0), B + np.uint16(1 << 7))
+    np.testing.assert_array_equal(O.fold_B(B, 0.25), B - np.uint16(2 << 7))
+
+
+def test_fold_generic_scale_is_single_nearest_rounding():
+    g = torch.Generator().manual_seed(8)
+    B = _rand_bf16(g, (128, 8), std=0.02)
+    s = 16 / math.sqrt(8)
+    Bp = O.bf16_to_f64(O.fold_B(B, s))
+    exact = s * O.bf16_to_f64(B)
+    # bf16 keeps 8 significant bits: unit roundoff u = 2^-8
+    assert np.all(np.abs(Bp - exact) <= np.abs(exact) * 2.0 ** -8 * (1 + 1e-12))
+    # and the rounding actually happened at bf16 precision (not a no-op)
+    assert np.any(Bp != exact)
+
+
+# ----------------------------------------------------- delta: helpers ----
+
+def _tiny_problem(seed, T=11, h_in=24, w=40, ranks=(4, 8, 3), with_base=True):
+    g = torch.Generator().manual_seed(seed)
+    n = len(ranks)
+    A = [_rand_bf16(g, (r, h_in), 0.3) for r in ranks]
+    B = [_rand_bf16(g, (w, r), 0.3) for r in ranks]
+    alphas = [2.0 * r for r in ranks]
+    scales = [O.scale(a, r, False) for a, r in zip(alphas, ranks)]
+    x = _rand_bf16(g, (T, h_in))
+    lo = -1 if with_base else 0
+    ids = torch.randint(lo, n, (T,), generator=g).numpy().astype(np.int32)
+    return A, B, scales, x, ids
+
+
+def test_merged_weight_identity():
+    """(W + B'A) x - W x equals the oracle's delta B'(A x) for every row."""
+    for seed in range(4):
+        A, B, scales, x, ids = _tiny_problem(seed)
+        ad = O.Adapters(A, B, scales)
+        d = O.delta(ids, x, ad)
+        xd = O.bf16_to_f64(x)
+        rng = np.random.default_rng(seed)
+        W = rng.standard_normal((ad.w, ad.h_in))
+        for t in range(len(ids)):
+            k = ids[t]
+            if k < 0:
+                np.testing.assert_array_equal(d[t], 0.0)
+                continue
+            Bp = O.bf16_to_f64(O.fold_B(B[k], scales[k]))
+            merged = W + Bp @ O.bf16_to_f64(A[k])
+            ref = merged @ xd[t] - W @ xd[t]
+            tol = 1e-12 * (np.abs(W) @ np.abs(xd[t]) + np.abs(Bp) @ np.abs(O.bf16_to_f64(A[k])) @ np.abs(xd[t]))
+            assert np.all(np.abs(d[t] - ref) <= tol), (seed, t)
+
+
+def test_brute_force_triple_loop():
+    """Delta W = B'A formed entry by entry in plain Python, then Delta W x."""
+    A, B, scales, x, ids = _tiny_problem(11, T=5, h_in=8, w=6, ranks=(2, 3))
+    ad = O.Adapters(A, B, scales)
+    d = O.delta(ids, x, ad)
+    xd = O.bf16_to_f64(x)
+    for t in range(len(ids)):
+        k = ids[t]
+        if k < 0:
+            assert all(v == 0.0 for v in d[t])
+            continue
+        Ak = O.bf16_to_f64(A[k]).tolist()
+        Bk = O.bf16_to_f64(B[k]).tolist()
+        r = len(Ak)
+        dW = [[0.0] * 8 for _ in range(6)]
+        for c in range(6):
+            for i in range(8):
+                acc = 0.0
+                for j in range(r):
+                    # fold s into B' by the definition bf16_rne(s * B)
+                    bp = float(O.bf16_to_f64(O.f64_to_bf16([scales[k] * Bk[c][j]]))[0])
+                    acc += bp * Ak[j][i]
+                dW[c][i] = acc
+        for c in range(6):
+            ref = sum(dW[c][i] * float(xd[t][i]) for i in range(8))
+            assert abs(d[t][c] - ref) <= 1e-12 * (1 + abs(ref))
+
+
+def test_zero_padding_invariance_bit_exact():
+    """Zero-padding A's rows and B's columns to a slot rank gives bit-identical
+    results (the scale still uses the true rank)."""
+    A, B, scales, x, ids = _tiny_problem(21)
+    r_slot = 8
+    Ap = [np.vstack([a, np.zeros((r_slot - a.shape[0], a.shape[1]), np.uint16)]) for a in A]
+    Bpd = [np.hstack([b, np.zeros((b.shape[0], r_slot - b.shape[1]), np.uint16)]) for b in B]
+    d0 = O.delta(ids, x, O.Adapters(A, B, scales))
+    d1 = O.delta(ids, x, O.Adapters(Ap, Bpd, scales))
+    np.testing.assert_array_equal(d0, d1)
+    g = torch.Generator().manual_seed(3)
+    y = _rand_bf16(g, (len(ids), 50))
+    np.testing.assert_array_equal(O.apply_projection(ids, x, y, 6, O.Adapters(A, B, scales)),
+                                  O.apply_projection(ids, x, y, 6, O.Adapters(Ap, Bpd, scales)))
+
+
+def test_base_rows_untouched_and_slice_only():
+    A, B, scales, x, ids = _tiny_problem(31)
+    ids[::3] = -1
+    g = torch.Generator().manual_seed(4)
+    y = _rand_bf16(g, (len(ids), 64))
+    out = O.apply_projection(ids, x, y, 8, O.Adapters(A, B, scales))
+    base = ids < 0
+    np.testing.assert_array_equal(out[base], y[base])
+    np.testing.assert_array_equal(out[:, :8], y[:, :8])
+    np.testing.assert_array_equal(out[:, 48:], y[:, 48:])
+    assert np.any(out[~base, 8:48] != y[~base, 8:48])
+
+
+def test_apply_is_one_rounding_of_y_plus_delta():
+    A, B, scales, x, ids = _tiny_problem(41)
+    ad = O.Adapters(A, B, scales)
+    g = torch.Generator().manual_seed(5)
+    y = _rand_bf16(g, (len(ids), 40))
+    out = O.apply_projection(ids, x, y, 0, ad)
+    d = O.delta(ids, x, ad)
+    act = ids >= 0
+    ref = O.f64_to_bf16(O.bf16_to_f64(y[act]) + d[act])
+    np.testing.assert_array_equal(out[act], ref)
+
+
+def test_expand_of_shrink_equals_apply():
+    A, B, scales, x, ids = _tiny_problem(51)
+    ad = O.Adapters(A, B, scales)
+    v = O.shrink(ids, x, ad)
+    g = torch.Generator().manual_seed(6)
+    y = _rand_bf16(g, (len(ids), 40))
+    np.testing.assert_array_equal(O.expand(ids, v, y, 0, ad), O.apply_projection(ids, x, y, 0, ad))
+
+
+def test_single_adapter_reduces_to_matmul():
+    """All rows on one adapter: delta = X A^T B'^T, a plain library matmul."""
+    A, B, scales, x, _ = _tiny_problem(61, T=9, ranks=(8,))
+    ids = np.zeros(9, np.int32)
+    ad = O.Adapters(A, B, scales)
+    d = O.delta(ids, x, ad)
+    Bp = O.bf16_to_f64(O.fold_B(B[0], scales[0]))
+    ref = (O.bf16_to_f64(x) @ O.bf16_to_f64(A[0]).T) @ Bp.T
+    np.testing.assert_allclose(d, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_row_permutation_equivariance_exact():
+    A, B, scales, x, ids = _tiny_problem(71, T=17)
+    ad = O.Adapters(A, B, scales)
+    d = O.delta(ids, x, ad)
+    p = np.random.default_rng(0).permutation(len(ids))
+    dp = O.delta(ids[p], x[p], ad)
+    np.testing.assert_array_equal(dp, d[p])
+
+
+def test_rank_index_not_swapped():
+    """A delta built only from rank component j must use row j of A with
+    column j of B (an index swap between them changes the answer)."""
+    h_in, w, r = 4, 3, 2
+    A = np.zeros((r, h_in), np.uint16)
+    B = np.zeros((w, r), np.uint16)
+    one = O.f64_to_bf16([1.0])[0]
+    two = O.f64_to_bf16([2.0])[0]
+    A[0, 1] = one          # v0 = x1
+    A[1, 2] = two          # v1 = 2 x2
+    B[0, 0] = one          # d0 = v0
+    B[2, 1] = one          # d2 = v1
+    x = O.f64_to_bf16([[3.0, 5.0, 7.0, 11.0]])
+    d = O.delta(np.array([0], np.int32), x, O.Adapters([A], [B], [1.0]))
+    np.testing.assert_array_equal(d, [[5.0, 0.0, 14.0]])
+
+
+# ----------------------------------------------------------- metadata ----
+
+def _meta_brute(ids, P, n_slots):
+    seg_starts, seg_slot = [], []
+    pos = 0
+    for key, grp in itertools.groupby(ids[:P].tolist()):
+        seg_starts.append(pos)
+        seg_slot.append(key)
+        pos += len(list(grp))
+    seg_starts.append(P)
+    dec = list(range(P, len(ids)))
+    order = sorted(dec, key=lambda row: (ids[row] == -1, ids[row], row))
+    gseg_starts, gseg_slot = [], []
+    for i, row in enumerate(order):
+        if i == 0 or ids[row] != ids[order[i - 1]]:
+            gseg_starts.append(i)
+            gseg_slot.append(int(ids[row]))
+    gseg_starts.append(len(order))
+    return seg_starts, seg_slot, order, gseg_starts, gseg_slot
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_metadata_matches_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    n_slots = int(rng.integers(1, 9))
+    T = int(rng.integers(0, 60))
+    P = int(rng.integers(0, T + 1))
+    ids = rng.integers(-1, n_slots, T).astype(np.int32)
+    if seed % 3 == 0 and P > 0:  # long runs, as prefill segments have
+        ids[:P] = np.repeat(rng.integers(-1, n_slots, 4), (P + 3) // 4)[:P]
+    got = O.build_metadata(ids, P, n_slots)
+    ref = _meta_brute(ids, P, n_slots)
+    for a, b in zip(got, ref):
+        np.testing.assert_array_equal(a, np.array(b, np.int32).reshape(a.shape))
+
+
+def test_metadata_tiny_workload_layout():
+    """Three prefill segments of 5/17/32 rows with ids 0/2/-1, then six decode
+    rows with ids [1,3,3,0,-1,2] over 4 slots."""
+    ids = np.array([0] * 5 + [2] * 17 + [-1] * 32 + [1, 3, 3, 0, -1, 2], np.int32)
+    seg_starts, seg_slot, perm, gs, gslot = O.build_metadata(ids, 54, 4)
+    np.testing.assert_array_equal(seg_starts, [0, 5, 22, 54])
+    np.testing.assert_array_equal(seg_slot, [0, 2, -1])
+    np.testing.assert_array_equal(perm, [57, 54, 59, 55, 56, 58])
+    np.testing.assert_array_equal(gs, [0, 1, 2, 3, 5, 6])
+    np.testing.assert_array_equal(gslot, [0, 1, 2, 3, -1])
+
+
+def test_metadata_rejects_out_of_range_ids():
+    with pytest.raises(ValueError):
+        O.build_metadata(np.array([0, 4], np.int32), 1, 4)
+    with pytest.raises(ValueError):
+        O.build_metadata(np.array([-2], np.int32), 0, 4)
