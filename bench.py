@@ -1,0 +1,473 @@
+#!/usr/bin/env python3
+"""Benchmark of the multi-LoRA delta hot path on GB300.
+
+One step = one pass of the LoRA delta over every layer instance of the
+workload for one batch: for the default Llama-3.2-3B-shaped decode workload
+(64 decode tokens, 8 adapter slots of rank 16) that is 28 layers x
+(fused q/k/v call + o call) through ``lora_apply``, replayed as a CUDA graph.
+Throughput counts a token once per layer call: value = tokens x layers /
+step time, which equals tokens / (time of one layer's q/k/v + o delta).
+
+L2 honesty: the step's inputs (adapter stores, x, y) are replicated into
+enough rotating sets that consecutive steps touch more than 4x the L2 size.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+(plain fp64 C, the correctness reference) on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import signal
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "llama3b_decode"
+LAYERS = {"llama3b_decode": 28}  # Llama-3.2-3B has 28 decoder layers
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--layers", type=int, default=None)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------- ranks ----
+
+def dist_setup(backend: str):
+    import torch.distributed as dist
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+    return rank, local, ws
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, ws: int, device="cpu") -> float:
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, ws: int, device="cpu") -> float:
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------ accounting ----
+
+def algorithmic_bytes(wl, group) -> int:
+    """Compulsory bytes of one lora_apply call: each distinct adapter slot used
+    by an active row read once (A and B' at the slot rank), x of the active
+    rows read, y slices of the active rows read and written, plus the ids."""
+    act = wl.ids >= 0
+    n_act = int(act.sum())
+    n_adapters = int(np.unique(wl.ids[act]).size)
+    w_bytes = sum(wl.r_slot * (group.h_in + w) * 2 for _, w in group.projs)
+    return n_adapters * w_bytes + n_act * group.h_in * 2 + n_act * group.ld_y * 2 * 2 + wl.n_rows * 4
+
+
+def useful_flops(wl, group) -> int:
+    act = wl.ids >= 0
+    r = wl.ranks[wl.ids[act]].astype(np.int64)
+    return int(sum(2 * (r * (group.h_in + w)).sum() for _, w in group.projs))
+
+
+def src_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "lora_serving_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# DRAM traffic per launch of the dominant kernel from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload; valid
+# only while the kernel sources hash to `src`.  Summaries live in profiles/.
+NCU_TRAFFIC = {}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.send_signal(signal.SIGTERM)
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------ CPU oracle ----
+
+def cpu_oracle_rate(wl_name: str, budget_s: float, layers: int):
+    """Times the fp64 oracle (as it stands) on layer calls of the workload,
+    rows split across all host cores; returns (tokens/s per layer call, info)."""
+    import concurrent.futures as cf
+    import oracle as O
+    from lora_serving_gb300 import synth
+
+    wl = synth.get(wl_name).materialise("delta")
+    cores = os.cpu_count() or 1
+    ads = {}
+    for g in wl.groups:
+        for pname, _ in g.projs:
+            A = [wl.A[(g.name, pname, k)] for k in range(wl.n_slots)]
+            B = [wl.B[(g.name, pname, k)] for k in range(wl.n_slots)]
+            sc = [O.scale(float(wl.alphas[k]), int(wl.ranks[k]), bool(wl.rslora[k])) for k in range(wl.n_slots)]
+            ads[(g.name, pname)] = O.Adapters(A, B, sc)
+    # rows per layer call: all of them for small batches, a row block for large ones
+    T = wl.n_rows
+    blocks = np.array_split(np.arange(T), min(T, cores)) if T else []
+
+    def run_block(rows):
+        for g in wl.groups:
+            y = wl.y[g.name][rows].copy()
+            for (pname, _), off in zip(g.projs, g.offsets):
+                y = O.apply_projection(wl.ids[rows], wl.x[g.name][rows], y, off, ads[(g.name, pname)])
+        return len(rows)
+
+    # warm (builds the oracle library) then time whole layer calls until the budget
+    run_block(blocks[0][:1])
+    done_rows = 0
+    calls = 0
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        if T <= 4096:
+            while True:
+                done_rows += sum(ex.map(run_block, blocks))
+                calls += 1
+                if time.perf_counter() - t0 >= budget_s:
+                    break
+            sample = f"{calls} layer call(s) of all {T} rows (all groups of one layer)"
+        else:
+            # large batches: a random subset of rows, one block per core
+            rng = np.random.default_rng(0)
+            sub = np.sort(rng.choice(T, min(T, 64 * cores), replace=False))
+            done_rows = sum(ex.map(run_block, np.array_split(sub, cores)))
+            sample = f"{sub.size} sampled rows of {T} (all groups of one layer), scaled per row"
+    dt = time.perf_counter() - t0
+    rate = done_rows / dt
+    return rate, {"cores": cores, "sample": sample, "seconds": round(dt, 3)}
+
+
+# --------------------------------------------------------- GPU arm ----
+
+class Instance:
+    """Device inputs of one layer instance: stores, x and y per group."""
+
+    def __init__(self, wl, store_mod, to_dev):
+        self.stores = {g.name: store_mod.GroupStore.from_workload(wl, g.name) for g in wl.groups}
+        self.x = {g.name: to_dev(wl.x[g.name]) for g in wl.groups}
+        self.y = {g.name: to_dev(wl.y[g.name]) for g in wl.groups}
+
+    def nbytes(self):
+        n = 0
+        for st in self.stores.values():
+            n += sum(a.numel() * 2 for a in st.A) + sum(b.numel() * 2 for b in st.B)
+        n += sum(t.numel() * 2 for t in self.x.values()) + sum(t.numel() * 2 for t in self.y.values())
+        return n
+
+
+def run_ours(args, rank, local, ws):
+    import torch
+    from lora_serving_gb300 import abi, build, store, synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        build()
+    barrier(ws)
+    build()
+    lib = abi.load()
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    name = args.workload
+    layers = args.layers or LAYERS.get(name, 1)
+    base = synth.get(name)
+    # host inputs of every layer instance (weights differ per layer)
+    host = []
+    for l in range(layers):
+        wl = synth.get(name)
+        wl.materialise("accumulate", layer=l)
+        host.append(wl)
+    meta = store.BatchMeta(base.ids, base.n_prefill, base.n_slots, device=dev)
+    ws_buf = {g.name: store.workspace_for(base.n_rows, len(g.projs), base.r_slot, device=dev) for g in base.groups}
+    inst0 = [Instance(h, store, to_dev) for h in host]
+    set_bytes = sum(i.nbytes() for i in inst0)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_sets = max(1, math.ceil(4 * l2 / set_bytes))
+    sets = [inst0] + [[Instance(h, store, to_dev) for h in host] for _ in range(n_sets - 1)]
+
+    calls_per_step = layers * len(base.groups)
+
+    def step(s):
+        for inst in sets[s]:
+            for g in base.groups:
+                store.apply(inst.y[g.name], inst.x[g.name], inst.stores[g.name], meta, ws_buf[g.name])
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for s in range(n_sets):  # eager warm-up (first-call attributes) before capture
+            step(s)
+    torch.cuda.synchronize()
+    graphs = []
+    l0 = lib.lora_kernel_launch_count() if hasattr(lib, "lora_kernel_launch_count") else None
+    for s in range(n_sets):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(s)
+        graphs.append(g)
+    launches_per_step = None
+    if l0 is not None:
+        launches_per_step = (lib.lora_kernel_launch_count() - l0) // n_sets
+    torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        graphs[i % n_sets].replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    e0.record(cur)
+    for i in range(args.steps):
+        graphs[(args.warmup + i) % n_sets].replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    barrier(ws)
+    ms_local = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    ms = max_over_ranks(ms_local, ws, device=dev if ws > 1 else "cpu")
+    ms_per_step = ms / args.steps
+    tokens = base.n_rows
+    units_local = tokens * layers * args.steps
+    units = sum_over_ranks(units_local, ws, device=dev if ws > 1 else "cpu")
+    value = units / (ms / 1e3)
+
+    # dominant kernel roofline: every launch in the step is the delta kernel
+    bytes_call = [algorithmic_bytes(base, g) for g in base.groups]
+    bytes_per_launch_avg = sum(bytes_call) / len(bytes_call)
+    call_ms = ms_local / (args.steps * calls_per_step)
+    achieved = bytes_per_launch_avg / (call_ms / 1e3) / 1e9
+    peak, peak_kind = peaks()
+    digest = src_digest()
+    tr = NCU_TRAFFIC.get(name)
+    traffic = tr["bytes_per_launch"] if tr and tr.get("src") == digest else None
+
+    out = {
+        "metric": "SGMV/BGMV LoRA-delta tokens/s (token x layer calls per second)",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)", "data": "synthetic",
+        "config": {
+            "workload": name, "tokens": tokens, "n_prefill": base.n_prefill, "layers": layers,
+            "groups": {g.name: [w for _, w in g.projs] for g in base.groups},
+            "hidden": base.groups[0].h_in, "n_slots": base.n_slots, "r_slot": base.r_slot,
+            "active_rows": int((base.ids >= 0).sum()),
+            "l2": f"{n_sets} rotating input sets x {set_bytes / 1e6:.0f} MB (L2 {l2 / 1e6:.0f} MB)",
+            "timing": "CUDA graph of the step replayed; CUDA events on the launching stream",
+            "parallelism": f"replicas x{ws}",
+        },
+        "roofline": {
+            "kernel": "lora_apply decode/prefill delta (per call)", "bound": "hbm",
+            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
+            "bytes_per_launch": round(bytes_per_launch_avg), "launch_us": round(call_ms * 1e3, 3),
+            "traffic": traffic,
+        },
+        "clocks": clk,
+        "gpu_launches": (launches_per_step * args.steps) if launches_per_step is not None else None,
+    }
+
+    if not args.no_e2e:
+        out["e2e"] = run_e2e(args, base, host, sets[0], meta, ws_buf, store, dev, layers)
+
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        rate, info = cpu_oracle_rate(name, args.cpu_seconds, layers)
+        out["cpu_baseline"] = {"value": round(rate, 2), "unit": "tokens/s", "cores": info["cores"],
+                               "kind": "oracle", "sample": info["sample"]}
+    return out
+
+
+def run_e2e(args, base, host, inst, meta, ws_buf, store, dev, layers):
+    """Same metric through the public call with host buffers: per step the
+    pinned x and y_in of every layer call go host->device, lora_apply runs,
+    and every y comes back device->host."""
+    import torch
+    hx = {(l, g.name): torch.from_numpy(host[l].x[g.name].view(np.int16)).view(torch.bfloat16).pin_memory()
+          for l in range(layers) for g in base.groups}
+    hy = {(l, g.name): torch.from_numpy(host[l].y[g.name].view(np.int16)).view(torch.bfloat16).pin_memory()
+          for l in range(layers) for g in base.groups}
+    hout = {k: torch.empty_like(v).pin_memory() for k, v in hy.items()}
+    h_ids = torch.from_numpy(base.ids.copy()).pin_memory()
+    h2d = sum(t.numel() * 2 for t in hx.values()) + sum(t.numel() * 2 for t in hy.values()) + h_ids.numel() * 4
+    d2h = sum(t.numel() * 2 for t in hout.values())
+
+    def step():
+        meta.ids.copy_(h_ids, non_blocking=True)
+        for l in range(layers):
+            i = inst[l]
+            for g in base.groups:
+                i.x[g.name].copy_(hx[(l, g.name)], non_blocking=True)
+                i.y[g.name].copy_(hy[(l, g.name)], non_blocking=True)
+                store.apply(i.y[g.name], i.x[g.name], i.stores[g.name], meta, ws_buf[g.name])
+                hout[(l, g.name)].copy_(i.y[g.name], non_blocking=True)
+
+    n = max(3, min(args.steps, 20))
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    return {"value": round(base.n_rows * layers * n / (ms / 1e3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n,
+            "ms_per_step": round(ms / n, 4)}
+
+
+def run_reference(args, rank, ws):
+    """The CPU oracle timed on the machine's host cores, as the reference arm."""
+    if rank != 0:
+        return None
+    name = args.workload
+    layers = args.layers or LAYERS.get(name, 1)
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
+    vals = []
+    info = None
+    t0 = time.perf_counter()
+    cpu_oracle_rate(name, 0.0, layers)  # warm-up: builds the oracle, one layer call
+    for _ in range(args.steps):
+        rate, info = cpu_oracle_rate(name, per_step, layers)
+        vals.append(rate)
+    total = time.perf_counter() - t0
+    value = statistics.median(vals)
+    from lora_serving_gb300 import synth
+    base = synth.get(name)
+    return {
+        "impl": "reference",
+        "metric": "SGMV/BGMV LoRA-delta tokens/s (token x layer calls per second)",
+        "value": round(value, 2), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * base.n_rows * layers / value, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, "tokens": base.n_rows, "layers": layers, "n_slots": base.n_slots,
+                   "r_slot": base.r_slot},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": info["cores"], "kind": "oracle",
+                         "sample": info["sample"]},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "seconds": round(total, 2),
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        rank, local, ws = dist_setup("gloo")
+        out = run_reference(args, rank, ws)
+        if rank == 0 and out is not None:
+            print(json.dumps(out), flush=True)
+        return 0
+    rank, local, ws = dist_setup("nccl")
+    out = run_ours(args, rank, local, ws)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

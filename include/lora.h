@@ -1,0 +1,247 @@
+/*
+ * lora.h -- C ABI of the GB300 multi-LoRA delta library (liblora.so).
+ *
+ * The library adds, for every row t of a batch, the low-rank delta of the
+ * adapter that row names to a shared base-layer output:
+ *
+ *     y[t, off : off+w] += B'_id(t) ( A_id(t) x_t )        (id(t) >= 0)
+ *
+ * and leaves rows whose id is -1 (base model only) untouched.
+ *
+ * Sources (page title, section):
+ *   [MLS]  "Multi-LoRA serving: one base, many adapters" -- "direct answer":
+ *          Delta W = B A with B in R^{d x r}, A in R^{r x k}; the base GEMM
+ *          runs once for the batch and each row's B(Ax) is added by a grouped
+ *          kernel keyed by adapter id (SGMV/BGMV).
+ *   [TGI]  "Text Generation Inference multi-LoRA adapter serving in
+ *          practice" -- "implementation 3. weight preprocessing" (scale
+ *          lora_alpha/r or rsLoRA lora_alpha/sqrt(r) folded into lora_B; rank
+ *          padded to the kernel's vector width), "4. SGMV and BGMV at
+ *          inference" (SGMV for prefill segments or ranks above the BGMV cap,
+ *          BGMV token by token otherwise), "5. tensor parallelism" (slicing
+ *          for uneven q/k/v widths, fused gate_up), and the backend note
+ *          naming bgmv_shrink / bgmv_expand / sgmv_shrink / sgmv_expand.
+ *   [VLLM] "How vLLM attaches a different LoRA adapter per request in
+ *          offline inference" -- step 2 (max_loras slots, max_lora_rank =
+ *          the largest rank in use), step 3 (None runs the base model) and
+ *          "limits" (invalid requests are rejected before submission).
+ *
+ * Conventions for every entry point:
+ *   - bf16 values are passed as their 16-bit patterns (lora_bf16_t).
+ *   - Device pointers (marked [dev]) are owned by the caller; the library
+ *     allocates no memory on any of these paths and keeps no state between
+ *     calls except what the caller passes.  Host pointers are marked [host].
+ *   - Kernel entry points validate their arguments on the host, enqueue on
+ *     `stream` and return without synchronising.  A host-detectable error
+ *     returns a non-OK status BEFORE anything is enqueued.
+ *   - Device-detected faults (an adapter id >= n_slots, a segment table that
+ *     does not cover its rows) never trap: the row is skipped and a bit is
+ *     OR-ed into *dev_status (LORA_DEV_*), which may be NULL to ignore them.
+ *     Kernels contain no spin-waits and no device printf.
+ *   - Alignment: every bf16/fp32 matrix pointer is 16-byte aligned, and all
+ *     leading dimensions, widths, column offsets and h_in are multiples of 8
+ *     elements (one 128-bit vector of bf16); r_slot is a multiple of 8.
+ *   - Row-major everywhere.  Adapter stores keep the peft orientation [MLS]:
+ *       A store: [n_slots][r_slot][h_in]      (lora_A, K-major)
+ *       B store: [n_slots][width][r_slot]     (scaled lora_B, K-major)
+ *     The intermediate v is fp32 [n_rows][ld_v] and is never rounded to bf16.
+ */
+#ifndef LORA_GB300_H
+#define LORA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t lora_bf16_t;           /* bf16 bit pattern */
+typedef struct CUstream_st* lora_stream_t; /* same handle as cudaStream_t */
+
+typedef enum {
+    LORA_OK = 0,
+    LORA_ERR_INVALID_ARG = 1,       /* NULL pointer, negative size, n_proj out of range */
+    LORA_ERR_SHAPE = 2,             /* leading dimension too small, slice outside the row */
+    LORA_ERR_RANK_EXCEEDS_SLOT = 3, /* adapter rank > r_slot, or r_slot > LORA_MAX_RANK */
+    LORA_ERR_SLOT_RANGE = 4,        /* host-visible adapter id outside [-1, n_slots) */
+    LORA_ERR_ALIGNMENT = 5,         /* pointer or size violates the 16-byte rule above */
+    LORA_ERR_METADATA = 6,          /* segment table inconsistent with the row counts */
+    LORA_ERR_WORKSPACE = 7,         /* workspace NULL or smaller than required */
+    LORA_ERR_CUDA = 8               /* a CUDA call failed (launch, copy, attribute) */
+} lora_status_t;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define LORA_DEV_SLOT_OUT_OF_RANGE 0x1 /* a row named an id >= n_slots or < -1; row skipped */
+#define LORA_DEV_BAD_SEGMENT 0x2       /* a segment/perm entry fell outside its rows; skipped */
+
+/* Largest r_slot (rank of one projection's slot) the kernels accept. */
+#define LORA_MAX_RANK 128
+/* BGMV cap: decode rows use BGMV when r_slot <= this, SGMV otherwise [TGI 4].
+ * The page does not print the cap; 32 is this library's choice. */
+#define LORA_BGMV_MAX_RANK 32
+/* Most projections one fused lora_apply call handles (q/k/v: 3, gate/up: 2). */
+#define LORA_MAX_PROJ 4
+
+/* ------------------------------------------------------------------ *
+ *  Kernel entry points (device pointers, asynchronous on `stream`)
+ * ------------------------------------------------------------------ */
+
+/*
+ * BGMV shrink [TGI 4, decode, token by token]:
+ *   v[t][j] = sum_i A[id_t][j][i] * x[t][i]      for j < r_slot, id_t >= 0
+ * x        [dev] bf16 [n_rows][ld_x], ld_x >= h_in
+ * A        [dev] bf16 [n_slots][r_slot][h_in] (for q/k/v stacked along rank,
+ *                pass the stacked store and r_slot = n_proj * slot rank)
+ * lora_ids [dev] int32 [n_rows], -1 = base (v row not written)
+ * v        [dev] fp32 [n_rows][ld_v], ld_v >= r_slot; fp32 accumulation
+ * n_rows == 0 is a no-op.
+ */
+lora_status_t lora_bgmv_shrink(float* v, int ld_v, const lora_bf16_t* x, int ld_x,
+                               const lora_bf16_t* A, const int32_t* lora_ids, int n_rows,
+                               int h_in, int r_slot, int n_slots, int32_t* dev_status,
+                               lora_stream_t stream);
+
+/*
+ * BGMV expand [TGI 4; slicing per TGI 5]:
+ *   y[t][y_off+c] = bf16_rne( y[t][y_off+c] + sum_j B[id_t][c][j] * v[t][j] )
+ * for c < width, id_t >= 0; rows with id -1 are never written.
+ * y        [dev] bf16 [n_rows][ld_y], y_off + width <= ld_y
+ * v        [dev] fp32 [n_rows][ld_v] (pass v + p*r_slot for projection p of
+ *                a stacked shrink), ld_v >= r_slot
+ * B        [dev] bf16 [n_slots][width][r_slot], already scaled (B')
+ */
+lora_status_t lora_bgmv_expand(lora_bf16_t* y, int ld_y, int y_off, int width,
+                               const float* v, int ld_v, const lora_bf16_t* B,
+                               const int32_t* lora_ids, int n_rows, int r_slot, int n_slots,
+                               int32_t* dev_status, lora_stream_t stream);
+
+/*
+ * SGMV shrink [TGI 4, prefill, "variable-length segments"]:
+ * segment s covers positions [seg_starts[s], seg_starts[s+1]) and uses slot
+ * seg_slot[s] (-1: skipped).  Position p maps to row row_perm[p], or to row p
+ * when row_perm is NULL (contiguous segments).  For every covered row:
+ *   v[row][j] = sum_i A[slot][j][i] * x[row][i]       j < r_slot
+ * seg_starts [dev] int32 [n_segs+1], non-decreasing, seg_starts[0] == 0,
+ *            seg_starts[n_segs] == n_pos
+ * seg_slot   [dev] int32 [n_segs]
+ * row_perm   [dev] int32 [n_pos] or NULL; every entry in [0, n_rows)
+ * n_rows     rows of x / v (bounds for the row indices)
+ * max_seg_len  [host] an upper bound on the longest segment (0 = unknown);
+ *              only used to pick the kernel variant.
+ */
+lora_status_t lora_sgmv_shrink(float* v, int ld_v, const lora_bf16_t* x, int ld_x,
+                               const lora_bf16_t* A, const int32_t* seg_starts,
+                               const int32_t* seg_slot, int n_segs, const int32_t* row_perm,
+                               int n_pos, int n_rows, int max_seg_len, int h_in, int r_slot,
+                               int n_slots, int32_t* dev_status, lora_stream_t stream);
+
+/*
+ * SGMV expand: for every row covered by a segment with slot >= 0,
+ *   y[row][y_off+c] = bf16_rne( y[row][y_off+c] + sum_j B[slot][c][j] * v[row][j] )
+ * Arguments as in lora_sgmv_shrink and lora_bgmv_expand.
+ */
+lora_status_t lora_sgmv_expand(lora_bf16_t* y, int ld_y, int y_off, int width,
+                               const float* v, int ld_v, const lora_bf16_t* B,
+                               const int32_t* seg_starts, const int32_t* seg_slot, int n_segs,
+                               const int32_t* row_perm, int n_pos, int n_rows, int max_seg_len,
+                               int r_slot, int n_slots, int32_t* dev_status,
+                               lora_stream_t stream);
+
+/* One projection of a fused call: its own A/B stores and its output slice. */
+typedef struct {
+    const lora_bf16_t* A; /* [dev] [n_slots][r_slot][h_in] */
+    const lora_bf16_t* B; /* [dev] [n_slots][width][r_slot], scaled */
+    int out_off;          /* first column of this projection in y */
+    int width;            /* its number of output columns (uneven for GQA k/v) */
+} lora_proj_t;
+
+/*
+ * Batch metadata as built by lora_build_metadata and copied to the device.
+ * Rows [0, n_prefill) are prefill rows, rows [n_prefill, n_rows) decode rows.
+ */
+typedef struct {
+    const int32_t* lora_ids;    /* [dev] [n_rows], -1 = base */
+    int n_rows;
+    int n_prefill;
+    const int32_t* seg_starts;  /* [dev] [n_segs+1] prefill segments over [0, n_prefill) */
+    const int32_t* seg_slot;    /* [dev] [n_segs] */
+    int n_segs;
+    int max_seg_len;            /* longest prefill segment (host value) */
+    const int32_t* perm;        /* [dev] [n_rows-n_prefill] decode rows sorted by slot */
+    const int32_t* gseg_starts; /* [dev] [n_gsegs+1] groups over positions of perm */
+    const int32_t* gseg_slot;   /* [dev] [n_gsegs] */
+    int n_gsegs;
+    int max_gseg_len;           /* largest decode group (host value) */
+} lora_meta_t;
+
+/*
+ * Fused LoRA delta for n_proj projections that share the input x (q/k/v or
+ * gate/up) [TGI 4, 5]:
+ *   - prefill rows: SGMV over meta->seg_*;
+ *   - decode rows: BGMV when r_slot <= LORA_BGMV_MAX_RANK, otherwise SGMV
+ *     over the gather groups meta->perm / gseg_* [TGI 4].
+ * Each projection p adds its delta into y[:, projs[p].out_off + (0..width)).
+ * workspace [dev] at least lora_apply_workspace_bytes(n_rows, n_proj, r_slot)
+ *           bytes, 256-byte aligned; its contents are scratch.
+ */
+lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_x, int h_in,
+                         const lora_proj_t* projs, int n_proj, int r_slot, int n_slots,
+                         const lora_meta_t* meta, void* workspace, size_t ws_bytes,
+                         int32_t* dev_status, lora_stream_t stream);
+
+size_t lora_apply_workspace_bytes(int n_rows, int n_proj, int r_slot);
+
+/* ------------------------------------------------------------------ *
+ *  Host helpers (host pointers, synchronous)
+ * ------------------------------------------------------------------ */
+
+/*
+ * Batch metadata [TGI 4; VLLM step 3]:
+ *   (i) prefill segments = maximal runs of equal id over rows [0, n_prefill)
+ *       in row order; runs of -1 are kept with slot -1;
+ *  (ii) decode gather form = decode rows sorted by slot ascending, ties in
+ *       row order, -1 rows last, one group per distinct id present; perm
+ *       holds absolute row indices.
+ * Capacities: seg_starts n_prefill+1, seg_slot n_prefill,
+ * perm n_rows-n_prefill, gseg_starts n_slots+2, gseg_slot n_slots+1.
+ * max_seg_len / max_gseg_len may be NULL.
+ * Returns LORA_ERR_SLOT_RANGE if an id lies outside [-1, n_slots).
+ */
+lora_status_t lora_build_metadata(const int32_t* ids, int n_rows, int n_prefill, int n_slots,
+                                  int32_t* seg_starts, int32_t* seg_slot, int* n_segs,
+                                  int* max_seg_len, int32_t* perm, int32_t* gseg_starts,
+                                  int32_t* gseg_slot, int* n_gsegs, int* max_gseg_len);
+
+/*
+ * Adapter store preparation [TGI 3]:
+ *   s = alpha / r, or alpha / sqrt(r) when use_rslora (computed in double);
+ *   B_slot[c][j] = bf16_rne(s * B[c][j]) for j < r, 0 for r <= j < r_slot;
+ *   A_slot[j][i] = A[j][i] for j < r, 0 for r <= j < r_slot.
+ * A [host] bf16 [r][h_in]; B [host] bf16 [out][r] (peft lora_A / lora_B);
+ * A_slot_out [host] [r_slot][h_in]; B_slot_out [host] [out][r_slot].
+ * Returns LORA_ERR_RANK_EXCEEDS_SLOT if r > r_slot [VLLM limits].
+ */
+lora_status_t lora_prepare_adapter(const lora_bf16_t* A, const lora_bf16_t* B, int r, int h_in,
+                                   int out, double alpha, int use_rslora, int r_slot,
+                                   lora_bf16_t* A_slot_out, lora_bf16_t* B_slot_out);
+
+/* Slot rank for a set of adapter ranks: the largest rank [VLLM step 2],
+ * rounded up to a multiple of 8 (the kernels' 128-bit vector of bf16). */
+int lora_slot_rank(const int* ranks, int n);
+
+/* Copies *dev_status to *out (host) on `stream` and waits for it. */
+lora_status_t lora_read_device_status(const int32_t* dev_status, int32_t* out,
+                                      lora_stream_t stream);
+
+const char* lora_status_string(lora_status_t status);
+
+/* Number of kernels this library has launched from the host since it was
+ * loaded (a diagnostic; replays of a captured CUDA graph are not counted). */
+uint64_t lora_kernel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_GB300_H */

@@ -1,0 +1,279 @@
+// abi.cu -- C ABI entry points: host-side validation and dispatch.
+//
+// Every entry point checks its arguments before enqueueing anything and
+// returns a status code (vLLM offline LoRA page, "limits": invalid requests
+// are rejected at submission, not silently ignored).  The route rule of
+// lora_apply follows the TGI page, "4. SGMV and BGMV at inference": SGMV for
+// prefill rows or when the rank exceeds the BGMV cap, BGMV otherwise.
+
+#include <atomic>
+#include <cstdint>
+
+#include "launch.h"
+
+namespace lora {
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace lora
+
+using lora::bf16_t;
+using lora::ProjSet;
+using lora::RowMap;
+
+namespace {
+
+constexpr int kMaxHin = 65536;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+lora_status_t check_common(int n_rows, int r_slot, int n_slots)
+{
+    if (n_rows < 0 || n_slots <= 0 || r_slot <= 0) return LORA_ERR_INVALID_ARG;
+    if (r_slot > LORA_MAX_RANK) return LORA_ERR_RANK_EXCEEDS_SLOT;
+    if (r_slot % 8 != 0) return LORA_ERR_ALIGNMENT;
+    return LORA_OK;
+}
+
+lora_status_t check_x(const bf16_t* x, int ld_x, int h_in)
+{
+    if (!x || h_in <= 0) return LORA_ERR_INVALID_ARG;
+    if (h_in > kMaxHin || ld_x < h_in) return LORA_ERR_SHAPE;
+    if (!aligned16(x) || h_in % 8 != 0 || ld_x % 8 != 0) return LORA_ERR_ALIGNMENT;
+    return LORA_OK;
+}
+
+lora_status_t check_y(const bf16_t* y, int ld_y, int y_off, int width)
+{
+    if (!y || width <= 0 || y_off < 0) return LORA_ERR_INVALID_ARG;
+    if (y_off + width > ld_y) return LORA_ERR_SHAPE;
+    if (!aligned16(y) || ld_y % 8 != 0 || y_off % 8 != 0 || width % 8 != 0) return LORA_ERR_ALIGNMENT;
+    return LORA_OK;
+}
+
+lora_status_t check_v(const float* v, int ld_v, int cols)
+{
+    if (!v) return LORA_ERR_INVALID_ARG;
+    if (ld_v < cols) return LORA_ERR_SHAPE;
+    if (!aligned16(v) || ld_v % 4 != 0) return LORA_ERR_ALIGNMENT;
+    return LORA_OK;
+}
+
+lora_status_t check_store(const bf16_t* s)
+{
+    if (!s) return LORA_ERR_INVALID_ARG;
+    if (!aligned16(s)) return LORA_ERR_ALIGNMENT;
+    return LORA_OK;
+}
+
+lora_status_t check_segments(const int32_t* seg_starts, const int32_t* seg_slot, int n_segs,
+                             int n_pos, int n_rows, const int32_t* perm)
+{
+    if (n_segs < 0 || n_pos < 0 || n_rows < 0) return LORA_ERR_INVALID_ARG;
+    if (n_pos == 0) return LORA_OK;
+    if (n_segs == 0 || !seg_starts || !seg_slot) return LORA_ERR_METADATA;
+    if (!perm && n_pos > n_rows) return LORA_ERR_METADATA;
+    return LORA_OK;
+}
+
+#define LORA_TRY(expr)                          \
+    do {                                        \
+        lora_status_t _st = (expr);             \
+        if (_st != LORA_OK) return _st;         \
+    } while (0)
+
+inline lora_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
+
+RowMap ids_map(const int32_t* ids, int row_base, int n_pos, int n_rows, int n_slots)
+{
+    RowMap m{};
+    m.ids = ids;
+    m.row_base = row_base;
+    m.n_pos = n_pos;
+    m.n_rows = n_rows;
+    m.n_slots = n_slots;
+    return m;
+}
+
+RowMap seg_map(const int32_t* seg_starts, const int32_t* seg_slot, int n_segs,
+               const int32_t* perm, int n_pos, int n_rows, int n_slots)
+{
+    RowMap m{};
+    m.seg_starts = seg_starts;
+    m.seg_slot = seg_slot;
+    m.n_segs = n_segs;
+    m.perm = perm;
+    m.n_pos = n_pos;
+    m.n_rows = n_rows;
+    m.n_slots = n_slots;
+    return m;
+}
+
+ProjSet single_proj(const bf16_t* A, const bf16_t* B, int y_off, int width, int r_slot)
+{
+    ProjSet ps{};
+    ps.A[0] = A;
+    ps.B[0] = B;
+    ps.out_off[0] = y_off;
+    ps.width[0] = width;
+    ps.n_proj = 1;
+    ps.r_slot = r_slot;
+    return ps;
+}
+
+}  // namespace
+
+extern "C" {
+
+lora_status_t lora_bgmv_shrink(float* v, int ld_v, const lora_bf16_t* x, int ld_x,
+                               const lora_bf16_t* A, const int32_t* lora_ids, int n_rows,
+                               int h_in, int r_slot, int n_slots, int32_t* dev_status,
+                               lora_stream_t stream)
+{
+    // The shrink accepts a rank-stacked A (n_proj * slot rank rows), so its
+    // bound is the fused limit rather than one slot's LORA_MAX_RANK.
+    if (n_rows < 0 || n_slots <= 0 || r_slot <= 0) return LORA_ERR_INVALID_ARG;
+    if (r_slot > LORA_MAX_RANK * LORA_MAX_PROJ) return LORA_ERR_RANK_EXCEEDS_SLOT;
+    if (r_slot % 8 != 0) return LORA_ERR_ALIGNMENT;
+    if (n_rows == 0) return LORA_OK;
+    if (!lora_ids) return LORA_ERR_INVALID_ARG;
+    LORA_TRY(check_x(x, ld_x, h_in));
+    LORA_TRY(check_store(A));
+    LORA_TRY(check_v(v, ld_v, r_slot));
+    ProjSet ps = single_proj(A, nullptr, 0, 0, r_slot);
+    RowMap m = ids_map(lora_ids, 0, n_rows, n_rows, n_slots);
+    return cuda_status(lora::launch_shrink_rowwise(v, ld_v, x, ld_x, h_in, ps, m, dev_status,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_bgmv_expand(lora_bf16_t* y, int ld_y, int y_off, int width,
+                               const float* v, int ld_v, const lora_bf16_t* B,
+                               const int32_t* lora_ids, int n_rows, int r_slot, int n_slots,
+                               int32_t* dev_status, lora_stream_t stream)
+{
+    LORA_TRY(check_common(n_rows, r_slot, n_slots));
+    if (n_rows == 0) return LORA_OK;
+    if (!lora_ids) return LORA_ERR_INVALID_ARG;
+    LORA_TRY(check_y(y, ld_y, y_off, width));
+    LORA_TRY(check_store(B));
+    LORA_TRY(check_v(v, ld_v, r_slot));
+    ProjSet ps = single_proj(nullptr, B, y_off, width, r_slot);
+    RowMap m = ids_map(lora_ids, 0, n_rows, n_rows, n_slots);
+    return cuda_status(lora::launch_expand_rowwise(y, ld_y, v, ld_v, ps, m, dev_status,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_sgmv_shrink(float* v, int ld_v, const lora_bf16_t* x, int ld_x,
+                               const lora_bf16_t* A, const int32_t* seg_starts,
+                               const int32_t* seg_slot, int n_segs, const int32_t* row_perm,
+                               int n_pos, int n_rows, int max_seg_len, int h_in, int r_slot,
+                               int n_slots, int32_t* dev_status, lora_stream_t stream)
+{
+    (void)max_seg_len;
+    if (n_rows < 0 || n_slots <= 0 || r_slot <= 0) return LORA_ERR_INVALID_ARG;
+    if (r_slot > LORA_MAX_RANK * LORA_MAX_PROJ) return LORA_ERR_RANK_EXCEEDS_SLOT;
+    if (r_slot % 8 != 0) return LORA_ERR_ALIGNMENT;
+    LORA_TRY(check_segments(seg_starts, seg_slot, n_segs, n_pos, n_rows, row_perm));
+    if (n_pos == 0) return LORA_OK;
+    LORA_TRY(check_x(x, ld_x, h_in));
+    LORA_TRY(check_store(A));
+    LORA_TRY(check_v(v, ld_v, r_slot));
+    ProjSet ps = single_proj(A, nullptr, 0, 0, r_slot);
+    RowMap m = seg_map(seg_starts, seg_slot, n_segs, row_perm, n_pos, n_rows, n_slots);
+    return cuda_status(lora::launch_shrink_rowwise(v, ld_v, x, ld_x, h_in, ps, m, dev_status,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+lora_status_t lora_sgmv_expand(lora_bf16_t* y, int ld_y, int y_off, int width,
+                               const float* v, int ld_v, const lora_bf16_t* B,
+                               const int32_t* seg_starts, const int32_t* seg_slot, int n_segs,
+                               const int32_t* row_perm, int n_pos, int n_rows, int max_seg_len,
+                               int r_slot, int n_slots, int32_t* dev_status,
+                               lora_stream_t stream)
+{
+    (void)max_seg_len;
+    LORA_TRY(check_common(n_rows, r_slot, n_slots));
+    LORA_TRY(check_segments(seg_starts, seg_slot, n_segs, n_pos, n_rows, row_perm));
+    if (n_pos == 0) return LORA_OK;
+    LORA_TRY(check_y(y, ld_y, y_off, width));
+    LORA_TRY(check_store(B));
+    LORA_TRY(check_v(v, ld_v, r_slot));
+    ProjSet ps = single_proj(nullptr, B, y_off, width, r_slot);
+    RowMap m = seg_map(seg_starts, seg_slot, n_segs, row_perm, n_pos, n_rows, n_slots);
+    return cuda_status(lora::launch_expand_rowwise(y, ld_y, v, ld_v, ps, m, dev_status,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t lora_apply_workspace_bytes(int n_rows, int n_proj, int r_slot)
+{
+    if (n_rows <= 0 || n_proj <= 0 || r_slot <= 0) return 0;
+    return static_cast<size_t>(n_rows) * n_proj * r_slot * sizeof(float);
+}
+
+lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_x, int h_in,
+                         const lora_proj_t* projs, int n_proj, int r_slot, int n_slots,
+                         const lora_meta_t* meta, void* workspace, size_t ws_bytes,
+                         int32_t* dev_status, lora_stream_t stream)
+{
+    if (!projs || !meta || n_proj <= 0 || n_proj > LORA_MAX_PROJ) return LORA_ERR_INVALID_ARG;
+    const int T = meta->n_rows, P = meta->n_prefill;
+    LORA_TRY(check_common(T, r_slot, n_slots));
+    if (P < 0 || P > T) return LORA_ERR_METADATA;
+    if (T == 0) return LORA_OK;
+    LORA_TRY(check_x(x, ld_x, h_in));
+    ProjSet ps{};
+    ps.n_proj = n_proj;
+    ps.r_slot = r_slot;
+    for (int p = 0; p < n_proj; ++p) {
+        LORA_TRY(check_y(y, ld_y, projs[p].out_off, projs[p].width));
+        LORA_TRY(check_store(projs[p].A));
+        LORA_TRY(check_store(projs[p].B));
+        ps.A[p] = projs[p].A;
+        ps.B[p] = projs[p].B;
+        ps.out_off[p] = projs[p].out_off;
+        ps.width[p] = projs[p].width;
+    }
+    const int R = n_proj * r_slot;
+    if (!workspace) return LORA_ERR_WORKSPACE;
+    if (ws_bytes < lora_apply_workspace_bytes(T, n_proj, r_slot)) return LORA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LORA_ERR_ALIGNMENT;
+    float* v = static_cast<float*>(workspace);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int D = T - P;
+    if (P > 0) LORA_TRY(check_segments(meta->seg_starts, meta->seg_slot, meta->n_segs, P, T, nullptr));
+    if (D > 0) {
+        if (!meta->lora_ids) return LORA_ERR_INVALID_ARG;
+        if (r_slot > LORA_BGMV_MAX_RANK) {
+            if (!meta->perm) return LORA_ERR_METADATA;
+            LORA_TRY(check_segments(meta->gseg_starts, meta->gseg_slot, meta->n_gsegs, D, T, meta->perm));
+        }
+    }
+
+    if (P > 0) {
+        RowMap m = seg_map(meta->seg_starts, meta->seg_slot, meta->n_segs, nullptr, P, T, n_slots);
+        LORA_TRY(cuda_status(lora::launch_shrink_rowwise(v, R, x, ld_x, h_in, ps, m, dev_status, s)));
+        LORA_TRY(cuda_status(lora::launch_expand_rowwise(y, ld_y, v, R, ps, m, dev_status, s)));
+    }
+    if (D > 0) {
+        RowMap m = r_slot <= LORA_BGMV_MAX_RANK
+                       ? ids_map(meta->lora_ids, P, D, T, n_slots)
+                       : seg_map(meta->gseg_starts, meta->gseg_slot, meta->n_gsegs, meta->perm, D, T, n_slots);
+        LORA_TRY(cuda_status(lora::launch_shrink_rowwise(v, R, x, ld_x, h_in, ps, m, dev_status, s)));
+        LORA_TRY(cuda_status(lora::launch_expand_rowwise(y, ld_y, v, R, ps, m, dev_status, s)));
+    }
+    return LORA_OK;
+}
+
+uint64_t lora_kernel_launch_count(void) { return lora::g_launches.load(std::memory_order_relaxed); }
+
+lora_status_t lora_read_device_status(const int32_t* dev_status, int32_t* out, lora_stream_t stream)
+{
+    if (!dev_status || !out) return LORA_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(out, dev_status, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return cuda_status(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,24 @@
+// launch.h -- internal kernel launchers (C++; not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace lora {
+
+// Counts every kernel launch the library issues (see lora_kernel_launch_count).
+void note_launch();
+
+// One position per CTA, CUDA cores: v[row][p*r_slot + j] = A_p[slot][j] . x[row].
+cudaError_t launch_shrink_rowwise(float* v, int ld_v, const bf16_t* x, int ld_x, int h_in,
+                                  const ProjSet& ps, const RowMap& map, int32_t* status,
+                                  cudaStream_t stream);
+
+// One position per CTA, CUDA cores:
+// y[row][out_off_p + c] = bf16(y + B_p[slot][c] . v[row][p*r_slot ...]).
+cudaError_t launch_expand_rowwise(bf16_t* y, int ld_y, const float* v, int ld_v,
+                                  const ProjSet& ps, const RowMap& map, int32_t* status,
+                                  cudaStream_t stream);
+
+}  // namespace lora

@@ -1,0 +1,186 @@
+"""CPU tests of the C library's host side: exports, store preparation,
+metadata builder, slot rank and argument validation (no kernel launches)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from lora_serving_gb300 import abi, build, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build()
+    return abi.load()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "lora.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(lora_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(_lib):
+    declared = _declared_functions()
+    assert set(declared) == set(abi.EXPORTS)
+    for name in declared:
+        assert hasattr(_lib, name), name
+
+
+def test_status_strings(_lib):
+    for code, name in abi.STATUS.items():
+        assert abi.lora_status_string(code).startswith(name)
+
+
+def _bits(t):
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("r,r_slot,alpha,rs", [(8, 8, 16, False), (16, 16, 32, False),
+                                               (8, 64, 16, True), (32, 64, 16, True),
+                                               (64, 64, 16, False), (5, 16, 7.0, False)])
+def test_prepare_adapter_bit_exact_vs_oracle(r, r_slot, alpha, rs):
+    g = torch.Generator().manual_seed(r * 100 + r_slot)
+    h_in, out = 48, 40
+    A = _bits((torch.randn(r, h_in, generator=g) * 0.02).to(torch.bfloat16))
+    B = _bits((torch.randn(out, r, generator=g) * 0.02).to(torch.bfloat16))
+    A_s, B_s = abi.lora_prepare_adapter(A, B, alpha, rs, r_slot)
+    np.testing.assert_array_equal(A_s[:r], A)
+    np.testing.assert_array_equal(A_s[r:], 0)
+    np.testing.assert_array_equal(B_s[:, :r], O.fold_B(B, O.scale(alpha, r, rs)))
+    np.testing.assert_array_equal(B_s[:, r:], 0)
+
+
+def test_prepare_adapter_rounding_edge_cases():
+    """Values whose scaled product sits on or next to a bf16 rounding tie, and
+    subnormal/overflow products, fold exactly as the oracle's rounding."""
+    vals = O.f64_to_bf16(np.array([1.0, 1 + 2 ** -7, -3.0, 1e-38, 3e38, 2 ** -126, 0.0, -0.0]))
+    B = np.tile(vals, (3, 1)).T.copy()  # [8][3]
+    A = np.zeros((3, 8), np.uint16)
+    for alpha, rs in [(1.5, False), (3 * 1.0000001, True), (2.0 ** -10, False), (1e5, False)]:
+        _, B_s = abi.lora_prepare_adapter(A, B, alpha, rs, 8)
+        np.testing.assert_array_equal(B_s[:, :3], O.fold_B(B, O.scale(alpha, 3, rs)))
+
+
+def test_prepare_adapter_rejects():
+    A = np.zeros((16, 8), np.uint16)
+    B = np.zeros((8, 16), np.uint16)
+    with pytest.raises(abi.LoraError) as e:
+        abi.lora_prepare_adapter(A, B, 32, False, 8)   # rank 16 > slot rank 8
+    assert e.value.name == "LORA_ERR_RANK_EXCEEDS_SLOT"
+    with pytest.raises(abi.LoraError) as e:
+        abi.lora_prepare_adapter(A, B, 32, False, 20)  # slot rank not a multiple of 8
+    assert e.value.name == "LORA_ERR_ALIGNMENT"
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_metadata_bit_exact_vs_oracle(seed):
+    rng = np.random.default_rng(1000 + seed)
+    n_slots = int(rng.integers(1, 12))
+    T = int(rng.integers(0, 300))
+    P = int(rng.integers(0, T + 1))
+    ids = rng.integers(-1, n_slots, T).astype(np.int32)
+    if seed % 2 and P:
+        ids[:P] = np.repeat(rng.integers(-1, n_slots, 6), (P + 5) // 6)[:P]
+    m = abi.lora_build_metadata(ids, P, n_slots)
+    ref = O.build_metadata(ids, P, n_slots)
+    for key, r in zip(("seg_starts", "seg_slot", "perm", "gseg_starts", "gseg_slot"), ref):
+        np.testing.assert_array_equal(m[key], r, err_msg=key)
+    lens = np.diff(ref[0])
+    assert m["max_seg_len"] == (lens.max() if lens.size else 0)
+    glens = np.diff(ref[3])
+    assert m["max_gseg_len"] == (glens.max() if glens.size else 0)
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3b_decode", "mistral7b_prefill", "mixed", "stress70b"])
+def test_metadata_workloads_bit_exact(name):
+    wl = synth.get(name)
+    m = abi.lora_build_metadata(wl.ids, wl.n_prefill, wl.n_slots)
+    ref = O.build_metadata(wl.ids, wl.n_prefill, wl.n_slots)
+    for key, r in zip(("seg_starts", "seg_slot", "perm", "gseg_starts", "gseg_slot"), ref):
+        np.testing.assert_array_equal(m[key], r, err_msg=key)
+
+
+def test_metadata_rejects_bad_ids():
+    with pytest.raises(abi.LoraError) as e:
+        abi.lora_build_metadata(np.array([0, 5], np.int32), 1, 4)
+    assert e.value.name == "LORA_ERR_SLOT_RANGE"
+
+
+def _golden(name):
+    rows = []
+    for line in open(os.path.join(ROOT, "tests", "golden", name)):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            rows.append(line)
+    return rows
+
+
+def test_golden_slot_rank():
+    """vLLM page, step 2: adapters of rank 16/32/64 -> max_lora_rank 64."""
+    for row in _golden("slot_rank.txt"):
+        lhs, rhs = row.split("->")
+        assert abi.lora_slot_rank([int(v) for v in lhs.split()]) == int(rhs)
+    assert abi.lora_slot_rank([5, 3]) == 8      # rounded up to the 8-wide vector
+    assert abi.lora_slot_rank([]) == 0
+
+
+def test_golden_param_count_closed_form():
+    """Interview note: d*k -> r*(d+k) parameters per matrix, about 100x fewer.
+    The store slot of one projection holds exactly r_slot*(h_in + out) values."""
+    from lora_serving_gb300.store import GroupStore
+    for row in _golden("param_count.txt"):
+        d, k, r = (int(v) for v in row.split())
+        st = GroupStore.__new__(GroupStore)
+        st.h_in, st.r_slot, st.projs = k, r, [("p", d)]
+        assert st.nbytes_slot() == 2 * r * (d + k)
+        ratio = (d * k) / (r * (d + k))
+        assert 30 <= ratio <= 300
+
+
+def _null_stream():
+    return 0
+
+
+def test_kernel_entry_points_validate_before_launch():
+    """Host-detectable errors come back before anything is enqueued, so these
+    calls are safe without a GPU."""
+    lib = abi.load()
+    buf = (ctypes.c_uint8 * 4096)()
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    ids = base
+    # NULL x
+    assert lib.lora_bgmv_shrink(base, 16, 0, 64, base, ids, 4, 64, 16, 2, 0, 0) == 1
+    # h_in not a multiple of 8
+    assert lib.lora_bgmv_shrink(base, 16, base, 64, base, ids, 4, 60, 16, 2, 0, 0) == 5
+    # r_slot beyond the fused limit
+    assert lib.lora_bgmv_shrink(base, 1024, base, 64, base, ids, 4, 64, 1024, 2, 0, 0) == 3
+    # misaligned y pointer
+    assert lib.lora_bgmv_expand(base + 2, 64, 0, 64, base, 16, base, ids, 4, 16, 2, 0, 0) == 5
+    # slice past the row
+    assert lib.lora_bgmv_expand(base, 64, 32, 64, base, 16, base, ids, 4, 16, 2, 0, 0) == 2
+    # r_slot above the per-slot maximum
+    assert lib.lora_bgmv_expand(base, 64, 0, 64, base, 256, base, ids, 4, 256, 2, 0, 0) == 3
+    # empty batches are a no-op
+    assert lib.lora_bgmv_shrink(base, 16, base, 64, base, ids, 0, 64, 16, 2, 0, 0) == 0
+    # SGMV with positions but no segments
+    assert lib.lora_sgmv_shrink(base, 16, base, 64, base, 0, 0, 0, 0, 4, 4, 0, 64, 16, 2, 0, 0) == 6
+    # lora_apply: no workspace
+    projs = abi.make_projs([(base, base, 0, 64)])
+    meta = abi.lora_meta_t()
+    meta.lora_ids, meta.n_rows, meta.n_prefill = ids, 4, 0
+    meta.perm, meta.gseg_starts, meta.gseg_slot, meta.n_gsegs = base, base, base, 1
+    st = lib.lora_apply(base, 64, base, 64, 64, ctypes.addressof(projs), 1, 16, 2,
+                        ctypes.addressof(meta), 0, 0, 0, 0)
+    assert st == 7
+    # lora_apply: too many projections
+    st = lib.lora_apply(base, 64, base, 64, 64, ctypes.addressof(projs), 5, 16, 2,
+                        ctypes.addressof(meta), base, 1 << 20, 0, 0)
+    assert st == 1
+    assert lib.lora_apply_workspace_bytes(10, 3, 16) == 10 * 3 * 16 * 4

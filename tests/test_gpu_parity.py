@@ -1,0 +1,301 @@
+"""GPU parity: every C-ABI kernel entry point against the fp64 oracle on the
+same seeded inputs (tolerances in helpers.py), on all five workloads, plus
+the edge cases the method has (empty batch, all-base batch, prefill-only,
+decode-only, ranks above the BGMV cap, malformed ids and segments)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from helpers import check_bf16, oracle_adapters, oracle_group, shrink_bound, to_dev, to_host
+from lora_serving_gb300 import abi, build, store, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build()
+    abi.load()
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def _seeded_v(T, cols, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(T, cols, generator=g, dtype=torch.float32)
+
+
+_CACHE = {}
+
+
+def _wl(name, mode="delta", **kw):
+    key = (name, mode, tuple(sorted(kw.items())))
+    if key not in _CACHE:
+        _CACHE.clear()
+        _CACHE[key] = synth.get(name, **kw).materialise(mode)
+    return _CACHE[key]
+
+
+# ------------------------------------------------- standalone kernels ----
+
+@pytest.mark.parametrize("name,group", [("tiny", "proj"), ("llama3b_decode", "qkv"), ("llama3b_decode", "o")])
+def test_bgmv_shrink_vs_oracle(name, group):
+    wl = _wl(name)
+    st = store.GroupStore.from_workload(wl, group)
+    g = next(g for g in wl.groups if g.name == group)
+    x = to_dev(wl.x[group])
+    ids = torch.from_numpy(wl.ids).cuda()
+    for p, (pname, _) in enumerate(g.projs):
+        v = torch.full((wl.n_rows, wl.r_slot), -7.0, device="cuda")
+        s = _status()
+        abi.lora_bgmv_shrink(v, x, st.A[p], ids, h_in=g.h_in, r_slot=wl.r_slot, n_slots=wl.n_slots, dev_status=s)
+        torch.cuda.synchronize()
+        assert abi.lora_read_device_status(s) == 0
+        got = v.cpu().numpy().astype(np.float64)
+        ad = oracle_adapters(wl, group, pname)
+        ref = O.shrink(wl.ids, wl.x[group], ad, v_cols=wl.r_slot)
+        bound = shrink_bound(wl.ids, wl.x[group], [wl.A[(group, pname, k)] for k in range(wl.n_slots)], g.h_in)
+        act = wl.ids >= 0
+        r = int(wl.ranks.max())
+        assert np.all(np.abs(got[act, :r] - ref[act, :r]) <= bound[act, :r])
+        assert np.all(got[~act] == -7.0), "base rows must not be written"
+
+
+def test_bgmv_shrink_stacked_qkv():
+    """q/k/v A stores stacked along rank give the three shrinks side by side."""
+    wl = _wl("llama3b_decode")
+    st = store.GroupStore.from_workload(wl, "qkv")
+    A_stack = torch.cat(st.A, dim=1).contiguous()  # [n][3*r][h]
+    x = to_dev(wl.x["qkv"])
+    ids = torch.from_numpy(wl.ids).cuda()
+    v = torch.zeros(wl.n_rows, 3 * wl.r_slot, device="cuda")
+    abi.lora_bgmv_shrink(v, x, A_stack, ids, h_in=3072, r_slot=3 * wl.r_slot, n_slots=wl.n_slots)
+    for p in range(3):
+        v1 = torch.zeros(wl.n_rows, wl.r_slot, device="cuda")
+        abi.lora_bgmv_shrink(v1, x, st.A[p], ids, h_in=3072, r_slot=wl.r_slot, n_slots=wl.n_slots)
+        torch.testing.assert_close(v[:, p * wl.r_slot:(p + 1) * wl.r_slot], v1, rtol=0, atol=0)
+
+
+@pytest.mark.parametrize("mode", ["delta", "accumulate"])
+@pytest.mark.parametrize("name,group", [("tiny", "proj"), ("llama3b_decode", "qkv"), ("llama3b_decode", "o")])
+def test_bgmv_expand_vs_oracle(name, group, mode):
+    wl = _wl(name, mode)
+    st = store.GroupStore.from_workload(wl, group)
+    g = next(g for g in wl.groups if g.name == group)
+    ids = torch.from_numpy(wl.ids).cuda()
+    vcpu = _seeded_v(wl.n_rows, wl.r_slot, 99)
+    v = vcpu.cuda()
+    y = to_dev(wl.y[group])
+    for p, ((pname, w), off) in enumerate(zip(g.projs, g.offsets)):
+        abi.lora_bgmv_expand(y, off, w, v, st.B[p], ids, r_slot=wl.r_slot, n_slots=wl.n_slots)
+    torch.cuda.synchronize()
+    ref = wl.y[group].copy()
+    for (pname, w), off in zip(g.projs, g.offsets):
+        ref = O.expand(wl.ids, vcpu.numpy().astype(np.float64), ref, off, oracle_adapters(wl, group, pname))
+    check_bf16(to_host(y), ref, wl.ids, wl.y[group], f"bgmv_expand {name}/{group}/{mode}")
+
+
+@pytest.mark.parametrize("gather", [False, True])
+def test_sgmv_shrink_expand_vs_oracle(gather):
+    """Contiguous prefill segments of the tiny workload, or all its rows in
+    the gather form (rows sorted by adapter through a permutation)."""
+    wl = _wl("tiny", "accumulate")
+    st = store.GroupStore.from_workload(wl, "proj")
+    x = to_dev(wl.x["proj"])
+    y = to_dev(wl.y["proj"])
+    if gather:
+        m = abi.lora_build_metadata(wl.ids, 0, wl.n_slots)
+        starts, slots, perm, n_pos = m["gseg_starts"], m["gseg_slot"], m["perm"], wl.n_rows
+        ng = m["n_gsegs"]
+    else:
+        m = abi.lora_build_metadata(wl.ids, wl.n_prefill, wl.n_slots)
+        starts, slots, perm, n_pos = m["seg_starts"], m["seg_slot"], None, wl.n_prefill
+        ng = m["n_segs"]
+    d_starts = torch.from_numpy(starts).cuda()
+    d_slots = torch.from_numpy(slots).cuda()
+    d_perm = torch.from_numpy(perm).cuda() if perm is not None else None
+    v = torch.zeros(wl.n_rows, wl.r_slot, device="cuda")
+    s = _status()
+    abi.lora_sgmv_shrink(v, x, st.A[0], d_starts, d_slots, ng, d_perm, n_pos, h_in=256,
+                         r_slot=wl.r_slot, n_slots=wl.n_slots, dev_status=s)
+    abi.lora_sgmv_expand(y, 0, 256, v, st.B[0], d_starts, d_slots, ng, d_perm, n_pos,
+                         r_slot=wl.r_slot, n_slots=wl.n_slots, dev_status=s)
+    torch.cuda.synchronize()
+    assert abi.lora_read_device_status(s) == 0
+    covered = np.zeros(wl.n_rows, bool)
+    covered[(perm if perm is not None else np.arange(n_pos))] = True
+    ids_eff = np.where(covered, wl.ids, -1).astype(np.int32)
+    ref = oracle_group(wl, "proj")
+    ref[~covered] = wl.y["proj"][~covered]
+    check_bf16(to_host(y), ref, ids_eff, wl.y["proj"], f"sgmv gather={gather}")
+
+
+# ---------------------------------------------------------- lora_apply ----
+
+def _run_apply(wl, group, meta=None, stat=None):
+    g = next(g for g in wl.groups if g.name == group)
+    st = store.GroupStore.from_workload(wl, group)
+    meta = meta or store.BatchMeta(wl.ids, wl.n_prefill, wl.n_slots)
+    ws = store.workspace_for(wl.n_rows, len(g.projs), wl.r_slot)
+    x = to_dev(wl.x[group])
+    y = to_dev(wl.y[group])
+    s = stat if stat is not None else _status()
+    store.apply(y, x, st, meta, ws, dev_status=s)
+    torch.cuda.synchronize()
+    assert abi.lora_read_device_status(s) == 0
+    return to_host(y)
+
+
+@pytest.mark.parametrize("mode", ["delta", "accumulate"])
+@pytest.mark.parametrize("name", ["tiny", "llama3b_decode", "mixed"])
+def test_apply_full_workload(name, mode):
+    wl = _wl(name, mode)
+    for g in wl.groups:
+        got = _run_apply(wl, g.name)
+        ref = oracle_group(wl, g.name)
+        check_bf16(got, ref, wl.ids, wl.y[g.name], f"{name}/{g.name}/{mode}")
+
+
+def _sample_rows(wl, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = set(rng.choice(wl.n_rows, min(n, wl.n_rows), replace=False).tolist())
+    # every segment's first and last row (ragged tile edges)
+    pos = 0
+    for L in wl.seg_lens:
+        rows.update([pos, pos + L - 1])
+        pos += L
+    rows.update([0, wl.n_rows - 1])
+    return np.array(sorted(rows))
+
+
+@pytest.mark.parametrize("mode", ["delta", "accumulate"])
+@pytest.mark.parametrize("name", ["mistral7b_prefill", "stress70b"])
+def test_apply_full_size_sampled(name, mode):
+    """Full sizes, all groups, in the launch configuration the benchmark
+    uses; the oracle recomputes a sample of rows one by one."""
+    wl = _wl(name, mode)
+    rows = _sample_rows(wl, 48, 5)
+    for g in wl.groups:
+        got = _run_apply(wl, g.name)
+        ref = oracle_group(wl, g.name, rows)
+        check_bf16(got[rows], ref, wl.ids[rows], wl.y[g.name][rows], f"{name}/{g.name}/{mode}")
+        # rows that are base-only must be untouched everywhere, not just in the sample
+        base = wl.ids < 0
+        np.testing.assert_array_equal(got[base], wl.y[g.name][base])
+
+
+# ---------------------------------------------------------- edge cases ----
+
+def _small(ids, n_prefill, n_slots=4, rank=8, h_in=64, widths=(64, 16, 16), seed=0, mode="accumulate",
+           r_slot=None):
+    ids = np.asarray(ids, np.int32)
+    r_slot = r_slot or ((rank + 7) // 8 * 8)
+    wl = synth.Workload("edge", seed, [synth.Group("g", h_in, [(f"p{i}", w) for i, w in enumerate(widths)])],
+                        np.full(n_slots, rank), np.full(n_slots, 2.0 * rank), np.zeros(n_slots, bool),
+                        r_slot, ids, n_prefill)
+    return wl.materialise(mode)
+
+
+def test_apply_empty_batch_is_noop():
+    wl = _small(np.zeros(0, np.int32), 0)
+    st = store.GroupStore.from_workload(wl, "g")
+    meta = store.BatchMeta(wl.ids, 0, wl.n_slots)
+    y = torch.zeros(1, 96, dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros(1, 64, dtype=torch.bfloat16, device="cuda")
+    store.apply(y, x, st, meta, store.workspace_for(1, 3, 8))
+    torch.cuda.synchronize()
+
+
+def test_apply_all_base_rows_bit_identical():
+    wl = _small([-1] * 7 + [-1] * 5, 7)
+    got = _run_apply(wl, "g")
+    np.testing.assert_array_equal(got, wl.y["g"])
+
+
+@pytest.mark.parametrize("n_prefill", [0, 40])
+def test_apply_decode_only_and_prefill_only(n_prefill):
+    rng = np.random.default_rng(n_prefill)
+    ids = rng.integers(-1, 4, 40).astype(np.int32)
+    wl = _small(ids, n_prefill)
+    got = _run_apply(wl, "g")
+    check_bf16(got, oracle_group(wl, "g"), wl.ids, wl.y["g"], f"P={n_prefill}")
+
+
+@pytest.mark.parametrize("rank", [40, 64, 128])
+def test_apply_rank_above_bgmv_cap_uses_gather(rank):
+    """Decode rows with r_slot > 32 take the SGMV gather route; up to the
+    largest slot rank the kernels accept."""
+    rng = np.random.default_rng(rank)
+    ids = np.concatenate([np.repeat([2, 0, -1, 1], [9, 1, 3, 17]), rng.integers(-1, 4, 33)]).astype(np.int32)
+    wl = _small(ids, 30, rank=rank, h_in=128, widths=(128, 24, 24))
+    got = _run_apply(wl, "g")
+    check_bf16(got, oracle_group(wl, "g"), wl.ids, wl.y["g"], f"rank={rank}")
+
+
+def test_zero_padding_bit_identical_on_gpu():
+    """The same adapters stored at slot rank 8 and 24 give identical bits."""
+    rng = np.random.default_rng(3)
+    ids = np.concatenate([np.repeat([1, 3], [12, 5]), rng.integers(-1, 4, 9)]).astype(np.int32)
+    a = _small(ids, 17, rank=5, r_slot=8)
+    b = _small(ids, 17, rank=5, r_slot=24)
+    np.testing.assert_array_equal(_run_apply(a, "g"), _run_apply(b, "g"))
+
+
+def test_bgmv_row_permutation_bit_exact():
+    wl = _wl("llama3b_decode", "accumulate")
+    p = np.random.default_rng(1).permutation(wl.n_rows)
+    base = _run_apply(wl, "qkv")
+    wl2 = synth.Workload(wl.name, wl.seed, wl.groups, wl.ranks, wl.alphas, wl.rslora, wl.r_slot,
+                         wl.ids[p].copy(), 0)
+    wl2.A, wl2.B = wl.A, wl.B
+    wl2.x = {"qkv": wl.x["qkv"][p].copy()}
+    wl2.y = {"qkv": wl.y["qkv"][p].copy()}
+    np.testing.assert_array_equal(_run_apply(wl2, "qkv"), base[p])
+
+
+def test_bad_slot_id_flagged_and_row_skipped():
+    ids = np.array([0, 1, 2, 3, 1, 0], np.int32)
+    wl = _small(ids, 0)
+    st = store.GroupStore.from_workload(wl, "g")
+    meta = store.BatchMeta(ids, 0, wl.n_slots)
+    meta.ids.copy_(torch.tensor([0, 1, 9, 3, -5, 0], dtype=torch.int32))  # device ids corrupted
+    ws = store.workspace_for(6, 3, 8)
+    y = to_dev(wl.y["g"])
+    s = _status()
+    store.apply(y, to_dev(wl.x["g"]), st, meta, ws, dev_status=s)
+    torch.cuda.synchronize()
+    assert abi.lora_read_device_status(s) & abi.LORA_DEV_SLOT_OUT_OF_RANGE
+    got = to_host(y)
+    np.testing.assert_array_equal(got[[2, 4]], wl.y["g"][[2, 4]])
+    ok = np.array([0, 1, 3, 5])
+    check_bf16(got[ok], oracle_group(wl, "g", ok), ids[ok], wl.y["g"][ok], "bad id")
+
+
+def test_bad_segment_table_flagged():
+    ids = np.repeat([0, 1], [6, 6]).astype(np.int32)
+    wl = _small(ids, 12)
+    st = store.GroupStore.from_workload(wl, "g")
+    meta = store.BatchMeta(ids, 12, wl.n_slots)
+    meta.seg_starts.copy_(torch.tensor([0, 6, 9], dtype=torch.int32))  # ends short of 12 rows
+    s = _status()
+    y = to_dev(wl.y["g"])
+    store.apply(y, to_dev(wl.x["g"]), st, meta, store.workspace_for(12, 3, 8), dev_status=s)
+    torch.cuda.synchronize()
+    assert abi.lora_read_device_status(s) & abi.LORA_DEV_BAD_SEGMENT
+    got = to_host(y)
+    np.testing.assert_array_equal(got[9:], wl.y["g"][9:])
+
+
+def test_host_rejects_before_enqueue():
+    wl = _small(np.zeros(4, np.int32), 0)
+    st = store.GroupStore.from_workload(wl, "g")
+    meta = store.BatchMeta(wl.ids, 0, wl.n_slots)
+    y = to_dev(wl.y["g"])
+    with pytest.raises(abi.LoraError) as e:
+        store.apply(y, to_dev(wl.x["g"]), st, meta, store.workspace_for(1, 1, 8)[:16])
+    assert e.value.name == "LORA_ERR_WORKSPACE"
+    np.testing.assert_array_equal(to_host(y), wl.y["g"])
