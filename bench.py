@@ -286,47 +286,61 @@ def run_ours(args, rank, local, ws):
 
     calls_per_step = layers * len(base.groups)
 
-    def step(s):
+    # Dependency model of the timed step: each call's y is treated as the
+    # output of the kernel just before it (as the base GEMM's output is in a
+    # model layer) and x as produced earlier (LORA_APPLY_X_READY).  The two
+    # other orderings are timed too and reported beside the headline.
+    variants = {"x_ready": abi.LORA_APPLY_X_READY, "default": 0, "no_pdl": abi.LORA_APPLY_NO_PDL}
+
+    def step(s, flags):
         for inst in sets[s]:
             for g in base.groups:
-                store.apply(inst.y[g.name], inst.x[g.name], inst.stores[g.name], meta, ws_buf[g.name])
+                store.apply(inst.y[g.name], inst.x[g.name], inst.stores[g.name], meta, ws_buf[g.name],
+                            flags=flags)
 
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
         for s in range(n_sets):  # eager warm-up (first-call attributes) before capture
-            step(s)
+            step(s, 0)
     torch.cuda.synchronize()
-    graphs = []
-    l0 = lib.lora_kernel_launch_count() if hasattr(lib, "lora_kernel_launch_count") else None
-    for s in range(n_sets):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            step(s)
-        graphs.append(g)
-    launches_per_step = None
-    if l0 is not None:
-        launches_per_step = (lib.lora_kernel_launch_count() - l0) // n_sets
+    graphs = {}
+    l0 = abi.lora_kernel_launch_count()
+    for name_v, fl in variants.items():
+        graphs[name_v] = []
+        for s in range(n_sets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(s, fl)
+            graphs[name_v].append(g)
+    launches_per_step = (abi.lora_kernel_launch_count() - l0) // (n_sets * len(variants))
     torch.cuda.synchronize()
 
-    for i in range(args.warmup):
-        graphs[i % n_sets].replay()
-    torch.cuda.synchronize()
+    def timed(gs, steps, warm):
+        for i in range(warm):
+            gs[i % n_sets].replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier(ws)
+        torch.cuda.synchronize()
+        cur = torch.cuda.current_stream()
+        e0.record(cur)
+        for i in range(steps):
+            gs[(warm + i) % n_sets].replay()
+        e1.record(cur)
+        torch.cuda.synchronize()
+        barrier(ws)
+        return e0.elapsed_time(e1)
+
+    other = {}
+    for name_v in ("default", "no_pdl"):
+        n_v = max(10, args.steps // 4)
+        other[name_v] = round(timed(graphs[name_v], n_v, args.warmup) / n_v, 5)
 
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    barrier(ws)
-    torch.cuda.synchronize()
-    cur = torch.cuda.current_stream()
-    e0.record(cur)
-    for i in range(args.steps):
-        graphs[(args.warmup + i) % n_sets].replay()
-    e1.record(cur)
-    torch.cuda.synchronize()
-    barrier(ws)
-    ms_local = e0.elapsed_time(e1)
+    ms_local = timed(graphs["x_ready"], args.steps, args.warmup)
     clk = clocks.stop()
     ms = max_over_ranks(ms_local, ws, device=dev if ws > 1 else "cpu")
     ms_per_step = ms / args.steps
@@ -357,17 +371,19 @@ def run_ours(args, rank, local, ws):
             "active_rows": int((base.ids >= 0).sum()),
             "l2": f"{n_sets} rotating input sets x {set_bytes / 1e6:.0f} MB (L2 {l2 / 1e6:.0f} MB)",
             "timing": "CUDA graph of the step replayed; CUDA events on the launching stream",
+            "dependency": "x_ready: each call's y treated as the preceding kernel's output, x as earlier",
+            "ms_per_step_other_orderings": other,
             "parallelism": f"replicas x{ws}",
         },
         "roofline": {
-            "kernel": "lora_apply decode/prefill delta (per call)", "bound": "hbm",
+            "kernel": "lora_apply decode delta (bgmv_fused_kernel, one launch per call)", "bound": "hbm",
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
             "bytes_per_launch": round(bytes_per_launch_avg), "launch_us": round(call_ms * 1e3, 3),
             "traffic": traffic,
         },
         "clocks": clk,
-        "gpu_launches": (launches_per_step * args.steps) if launches_per_step is not None else None,
+        "gpu_launches": launches_per_step * args.steps,
     }
 
     if not args.no_e2e:
@@ -385,6 +401,7 @@ def run_e2e(args, base, host, inst, meta, ws_buf, store, dev, layers):
     pinned x and y_in of every layer call go host->device, lora_apply runs,
     and every y comes back device->host."""
     import torch
+    from lora_serving_gb300 import abi
     hx = {(l, g.name): torch.from_numpy(host[l].x[g.name].view(np.int16)).view(torch.bfloat16).pin_memory()
           for l in range(layers) for g in base.groups}
     hy = {(l, g.name): torch.from_numpy(host[l].y[g.name].view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -401,7 +418,8 @@ def run_e2e(args, base, host, inst, meta, ws_buf, store, dev, layers):
             for g in base.groups:
                 i.x[g.name].copy_(hx[(l, g.name)], non_blocking=True)
                 i.y[g.name].copy_(hy[(l, g.name)], non_blocking=True)
-                store.apply(i.y[g.name], i.x[g.name], i.stores[g.name], meta, ws_buf[g.name])
+                store.apply(i.y[g.name], i.x[g.name], i.stores[g.name], meta, ws_buf[g.name],
+                            flags=abi.LORA_APPLY_X_READY)
                 hout[(l, g.name)].copy_(i.y[g.name], non_blocking=True)
 
     n = max(3, min(args.steps, 20))

@@ -175,6 +175,20 @@ typedef struct {
     int max_gseg_len;           /* largest decode group (host value) */
 } lora_meta_t;
 
+/* lora_apply flags.
+ * Ordering against the kernel enqueued just before the call: lora_apply's
+ * decode kernel uses programmatic dependent launch, so it may start while
+ * that kernel is still running.  It reads the adapter store and the batch
+ * metadata at once (neither may be written by that kernel; copies made with
+ * cudaMemcpyAsync are ordered as usual), and touches y and dev_status only
+ * after that kernel has completed.  It also never completes before it.
+ *   LORA_APPLY_X_READY: x is not written by the kernel just before the call
+ *     (in a model layer x comes from earlier than the base GEMM that writes
+ *     y), so the shrink may read x before that kernel completes.
+ *   LORA_APPLY_NO_PDL: plain stream ordering, nothing starts early. */
+#define LORA_APPLY_X_READY 0x1u
+#define LORA_APPLY_NO_PDL 0x2u
+
 /*
  * Fused LoRA delta for n_proj projections that share the input x (q/k/v or
  * gate/up) [TGI 4, 5]:
@@ -184,11 +198,12 @@ typedef struct {
  * Each projection p adds its delta into y[:, projs[p].out_off + (0..width)).
  * workspace [dev] at least lora_apply_workspace_bytes(n_rows, n_proj, r_slot)
  *           bytes, 256-byte aligned; its contents are scratch.
+ * flags     LORA_APPLY_* above (0 = default ordering).
  */
 lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_x, int h_in,
                          const lora_proj_t* projs, int n_proj, int r_slot, int n_slots,
                          const lora_meta_t* meta, void* workspace, size_t ws_bytes,
-                         int32_t* dev_status, lora_stream_t stream);
+                         uint32_t flags, int32_t* dev_status, lora_stream_t stream);
 
 size_t lora_apply_workspace_bytes(int n_rows, int n_proj, int r_slot);
 

@@ -21,6 +21,8 @@ LORA_BGMV_MAX_RANK = 32
 LORA_MAX_PROJ = 4
 LORA_DEV_SLOT_OUT_OF_RANGE = 0x1
 LORA_DEV_BAD_SEGMENT = 0x2
+LORA_APPLY_X_READY = 0x1
+LORA_APPLY_NO_PDL = 0x2
 
 STATUS = {
     0: "LORA_OK", 1: "LORA_ERR_INVALID_ARG", 2: "LORA_ERR_SHAPE",
@@ -75,7 +77,7 @@ def load(path: str | None = None):
         "lora_bgmv_expand": [P, i32, i32, i32, P, i32, P, P, i32, i32, i32, P, P],
         "lora_sgmv_shrink": [P, i32, P, i32, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, P, P],
         "lora_sgmv_expand": [P, i32, i32, i32, P, i32, P, P, P, i32, P, i32, i32, i32, i32, i32, P, P],
-        "lora_apply": [P, i32, P, i32, i32, P, i32, i32, i32, P, P, sz, P, P],
+        "lora_apply": [P, i32, P, i32, i32, P, i32, i32, i32, P, P, sz, ctypes.c_uint32, P, P],
         "lora_apply_workspace_bytes": [i32, i32, i32],
         "lora_build_metadata": [P, i32, i32, i32, P, P, P, P, P, P, P, P, P],
         "lora_prepare_adapter": [P, P, i32, i32, i32, ctypes.c_double, i32, i32, P, P],
@@ -167,13 +169,14 @@ def make_projs(projs):
     return arr
 
 
-def lora_apply(y, x, h_in, projs, r_slot, n_slots, meta, workspace, *, dev_status=None,
+def lora_apply(y, x, h_in, projs, r_slot, n_slots, meta, workspace, *, flags=0, dev_status=None,
                stream=None):
-    """projs: ctypes array from make_projs(); meta: lora_meta_t; workspace: device tensor."""
+    """projs: ctypes array from make_projs(); meta: lora_meta_t; workspace: device tensor;
+    flags: LORA_APPLY_* bits."""
     ws_bytes = workspace.numel() * workspace.element_size()
     _check("lora_apply", load().lora_apply(
         _p(y), _ld(y), _p(x), _ld(x), h_in, ctypes.addressof(projs), len(projs), r_slot, n_slots,
-        ctypes.addressof(meta), _p(workspace), ws_bytes, _p(dev_status), _stream(stream)))
+        ctypes.addressof(meta), _p(workspace), ws_bytes, int(flags), _p(dev_status), _stream(stream)))
 
 
 def lora_apply_workspace_bytes(n_rows, n_proj, r_slot) -> int:

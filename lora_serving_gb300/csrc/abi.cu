@@ -214,7 +214,7 @@ size_t lora_apply_workspace_bytes(int n_rows, int n_proj, int r_slot)
 lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_x, int h_in,
                          const lora_proj_t* projs, int n_proj, int r_slot, int n_slots,
                          const lora_meta_t* meta, void* workspace, size_t ws_bytes,
-                         int32_t* dev_status, lora_stream_t stream)
+                         uint32_t flags, int32_t* dev_status, lora_stream_t stream)
 {
     if (!projs || !meta || n_proj <= 0 || n_proj > LORA_MAX_PROJ) return LORA_ERR_INVALID_ARG;
     const int T = meta->n_rows, P = meta->n_prefill;
@@ -256,11 +256,19 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
         LORA_TRY(cuda_status(lora::launch_expand_rowwise(y, ld_y, v, R, ps, m, dev_status, s)));
     }
     if (D > 0) {
-        RowMap m = r_slot <= LORA_BGMV_MAX_RANK
-                       ? ids_map(meta->lora_ids, P, D, T, n_slots)
-                       : seg_map(meta->gseg_starts, meta->gseg_slot, meta->n_gsegs, meta->perm, D, T, n_slots);
-        LORA_TRY(cuda_status(lora::launch_shrink_rowwise(v, R, x, ld_x, h_in, ps, m, dev_status, s)));
-        LORA_TRY(cuda_status(lora::launch_expand_rowwise(y, ld_y, v, R, ps, m, dev_status, s)));
+        const bool gathered = meta->perm && meta->gseg_starts && meta->gseg_slot && meta->n_gsegs > 0;
+        if (r_slot <= LORA_BGMV_MAX_RANK && gathered && lora::fused_decode_supported(n_proj, r_slot)) {
+            // BGMV route, one launch: rows grouped by adapter, cluster split-K.
+            LORA_TRY(cuda_status(lora::launch_bgmv_fused(y, ld_y, x, ld_x, h_in, ps, meta->perm,
+                                                         meta->gseg_starts, meta->gseg_slot, meta->n_gsegs,
+                                                         D, T, n_slots, flags, dev_status, s)));
+        } else {
+            RowMap m = r_slot <= LORA_BGMV_MAX_RANK
+                           ? ids_map(meta->lora_ids, P, D, T, n_slots)
+                           : seg_map(meta->gseg_starts, meta->gseg_slot, meta->n_gsegs, meta->perm, D, T, n_slots);
+            LORA_TRY(cuda_status(lora::launch_shrink_rowwise(v, R, x, ld_x, h_in, ps, m, dev_status, s)));
+            LORA_TRY(cuda_status(lora::launch_expand_rowwise(y, ld_y, v, R, ps, m, dev_status, s)));
+        }
     }
     return LORA_OK;
 }

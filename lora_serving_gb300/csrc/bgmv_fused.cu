@@ -1,0 +1,513 @@
+// bgmv_fused.cu -- decode-row LoRA delta in one launch (the BGMV route of
+// lora_apply): shrink, reduction of the fp32 intermediate and expand.
+//
+// TGI multi-LoRA page, "4. SGMV and BGMV at inference": decode tokens take
+// BGMV, each token applying its own adapter.  Here the decode rows arrive
+// grouped by adapter (the gather form of the batch metadata), so a unit of
+// work is (adapter, up to 16 of its rows), and every adapter's weights are
+// streamed from HBM once per call instead of once per token.
+//
+// Per unit, a thread-block cluster of CS CTAs splits the shrink's K = h_in:
+//   CTA c computes partial v_c[t][j] = sum_{k in chunk c} A[j][k] x[t][k]
+//   with mma.sync m16n8k16 (bf16 in, fp32 out: 16 rows x 8 ranks tiles).
+// The partials meet in distributed shared memory: after a cluster barrier
+// every CTA sums v = sum_c v_c in a fixed order (deterministic, fp32, never
+// rounded to bf16) and forms the delta of its own slice of output columns
+//   d[t][col] = sum_j B'_p[col][j] v[t][p*r + j]
+// in registers; the only step left is y[t][off_p + col] = bf16_rne(y + d).
+//
+// Latency (programmatic dependent launch): metadata and weights are read
+// before griddepcontrol.wait, so they stream in while the preceding kernel
+// on the stream is still running.  With LORA_APPLY_X_READY the shrink, the
+// cluster reduction and the delta are formed before the wait as well, and
+// only the read-modify-write of y follows it.  All waits are hardware waits
+// (cp.async groups, cluster barriers, grid dependency); no spin loops.
+
+#include <cstdlib>
+
+#include "launch.h"
+
+namespace lora {
+
+namespace {
+
+constexpr int kRB = 16;       // rows per unit (the mma M)
+constexpr int kKT = 128;      // K elements per pipeline stage
+constexpr int kPad = 8;       // bf16 padding per smem row: conflict-free ldmatrix
+constexpr int kLds = kKT + kPad;
+constexpr int kTC = 512;      // expand columns per tile
+constexpr int kChunksTile = kTC / 8;
+constexpr int kThreads = 256;
+constexpr int kPairs = kRB * kChunksTile / kThreads;  // (row, chunk) pairs per thread per tile
+
+struct FusedParams {
+    ProjSet ps;
+    const bf16_t* x;
+    int ld_x;
+    int h_in;
+    bf16_t* y;
+    int ld_y;
+    const int32_t* perm;      // absolute rows, grouped by slot
+    const int32_t* gstarts;   // [n_groups+1] over positions of perm
+    const int32_t* gslot;     // [n_groups]
+    int n_groups;
+    int n_pos;                // positions covered by perm
+    int n_slots;
+    int n_rows;
+    int kc;                   // K elements per cluster rank (multiple of 16)
+    int n_parts;              // column parts per unit
+    int cs;                   // cluster size
+    int x_ready;              // x may be read before the grid dependency resolves
+    int32_t* status;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid)
+{
+    const int n = valid ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t map_rank(uint32_t local_addr, uint32_t rank)
+{
+    uint32_t remote;
+    asm("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    return remote;
+}
+// Plain (non-volatile) DSMEM load: ordering against the partials' writes is
+// given by the cluster barrier, so independent loads may be issued together.
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t remote)
+{
+    float4 v;
+    asm("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(remote));
+    return v;
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x2(uint32_t addr, uint32_t& r0, uint32_t& r1)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];\n" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Unit u -> (group, first position, rows).  Uniform across the cluster.
+// Groups whose bounds fall outside [0, n_pos) are skipped (bad set), so perm
+// is never read out of range.
+__device__ __forceinline__ bool find_unit(const FusedParams& p, int u, int& g, int& pos0, int& nrows, bool& bad)
+{
+    int acc = 0;
+    for (int i = 0; i < p.n_groups; ++i) {
+        const int s = __ldg(p.gstarts + i), e = __ldg(p.gstarts + i + 1);
+        const bool sane = s >= 0 && e <= p.n_pos && s <= e;
+        bad |= !sane;
+        const int n = sane ? (e - s + kRB - 1) / kRB : 0;
+        if (u < acc + n) {
+            g = i;
+            pos0 = s + (u - acc) * kRB;
+            nrows = min(kRB, e - pos0);
+            return true;
+        }
+        acc += n;
+    }
+    return false;
+}
+
+// Output chunk (8 columns) -> projection and column within it.
+__device__ __forceinline__ void chunk_proj(const ProjSet& ps, int ch, int& p, int& col0)
+{
+    p = 0;
+    while (p < ps.n_proj - 1 && ch >= (ps.width[p] >> 3)) {
+        ch -= ps.width[p] >> 3;
+        ++p;
+    }
+    col0 = ch << 3;
+}
+
+__global__ void __launch_bounds__(kThreads)
+bgmv_fused_kernel(FusedParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int R = p.ps.n_proj * p.ps.r_slot;
+    const int r_slot = p.ps.r_slot;
+    bf16_t* sA = reinterpret_cast<bf16_t*>(smem);                    // [2][R][kLds]
+    bf16_t* sX = sA + 2 * R * kLds;                                  // [2][kRB][kLds]
+    float* vpart = reinterpret_cast<float*>(sX + 2 * kRB * kLds);    // [kRB][R]
+    float* vfull = vpart + kRB * R;                                  // [kRB][R]
+    bf16_t* sB = reinterpret_cast<bf16_t*>(vfull + kRB * R);         // [kChunksTile][8*r_slot], swizzled
+    __shared__ int s_rows[kRB];
+
+    grid_dep_launch();
+
+    const int tid = threadIdx.x;
+    const int crank = static_cast<int>(cluster_rank());
+    const int cluster = blockIdx.x / p.cs;
+    const int unit = cluster / p.n_parts;
+    const int part = cluster - unit * p.n_parts;
+
+    // Every exit path waits for the preceding grid first, so this grid never
+    // completes before it (stream order stays transitive under PDL), and
+    // status flags are written only after the wait.
+    int g, pos0, nrows;
+    bool bad_group = false;
+    if (!find_unit(p, unit, g, pos0, nrows, bad_group)) {   // whole cluster exits together
+        grid_dep_wait();
+        if (bad_group && crank == 0 && tid == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
+        return;
+    }
+    const int slot = __ldg(p.gslot + g);
+    if (slot == -1) {                                  // base-only rows: untouched
+        grid_dep_wait();
+        return;
+    }
+    if (slot < -1 || slot >= p.n_slots) {
+        grid_dep_wait();
+        if (crank == 0 && part == 0 && tid == 0) flag(p.status, LORA_DEV_SLOT_OUT_OF_RANGE);
+        return;
+    }
+    bool bad_row = false;
+    if (tid < kRB) {
+        int r = 0;
+        if (tid < nrows) {
+            r = __ldg(p.perm + pos0 + tid);
+            if (r < 0 || r >= p.n_rows) { bad_row = true; r = 0; }
+        }
+        s_rows[tid] = r;
+    }
+    if (__syncthreads_or(bad_row)) {
+        // A malformed permutation: flag it and leave this unit's rows alone.
+        // Every CTA of the cluster reads the same entries, so all return here.
+        grid_dep_wait();
+        if (tid == 0 && crank == 0 && part == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
+        return;
+    }
+
+    // ---- this CTA's K range and output chunks ----
+    const int k_begin = crank * p.kc;
+    const int k_end = min(p.h_in, k_begin + p.kc);
+    const int n_kt = k_end > k_begin ? (k_end - k_begin + kKT - 1) / kKT : 0;
+    int total_ch = 0;
+    for (int q = 0; q < p.ps.n_proj; ++q) total_ch += p.ps.width[q] >> 3;
+    const int q_idx = part * p.cs + crank, q_n = p.n_parts * p.cs;
+    const int ch_begin = static_cast<int>((static_cast<long long>(total_ch) * q_idx) / q_n);
+    const int ch_end = static_cast<int>((static_cast<long long>(total_ch) * (q_idx + 1)) / q_n);
+
+    auto load_A = [&](int kt, int buf) {
+        const int k0 = k_begin + kt * kKT;
+        for (int i = tid; i < R * (kKT / 8); i += kThreads) {
+            const int j = i / (kKT / 8), u = i - j * (kKT / 8);
+            const int k = k0 + u * 8;
+            const int pj = j / r_slot, jj = j - pj * r_slot;
+            const bool ok = k < k_end;
+            const bf16_t* src = p.ps.A[pj] + (static_cast<size_t>(slot) * r_slot + jj) * p.h_in + (ok ? k : 0);
+            cp_async16(smem_u32(sA + (buf * R + j) * kLds + u * 8), src, ok);
+        }
+    };
+    auto load_X = [&](int kt, int buf) {
+        const int k0 = k_begin + kt * kKT;
+        for (int i = tid; i < kRB * (kKT / 8); i += kThreads) {
+            const int t = i / (kKT / 8), u = i - t * (kKT / 8);
+            const int k = k0 + u * 8;
+            const bool ok = t < nrows && k < k_end;
+            const bf16_t* src = p.x + (ok ? static_cast<size_t>(s_rows[t]) * p.ld_x + k : 0);
+            cp_async16(smem_u32(sX + (buf * kRB + t) * kLds + u * 8), src, ok);
+        }
+    };
+    auto load_B = [&](int c0, int c1) {
+        // chunk = 8 output columns x r_slot ranks = r_slot 16-byte units,
+        // stored with the unit index XOR (chunk & 7) to spread smem banks
+        for (int i = tid; i < (c1 - c0) * r_slot; i += kThreads) {
+            const int ci = i / r_slot, u = i - ci * r_slot;
+            int pj, col0;
+            chunk_proj(p.ps, c0 + ci, pj, col0);
+            const bf16_t* src = p.ps.B[pj] + (static_cast<size_t>(slot) * p.ps.width[pj] + col0) * r_slot + u * 8;
+            cp_async16(smem_u32(sB + ci * 8 * r_slot + (u ^ (ci & 7)) * 8), src, true);
+        }
+    };
+
+    // ---- weights first: they do not depend on the preceding kernel ----
+    const int tile0_end = min(ch_end, ch_begin + kChunksTile);
+    if (n_kt > 0) load_A(0, 0);
+    if (ch_end > ch_begin) load_B(ch_begin, tile0_end);
+    cp_async_commit();
+    if (n_kt > 1) load_A(1, 1);
+    cp_async_commit();
+
+    bool waited = false;
+    if (!p.x_ready) {
+        grid_dep_wait();
+        waited = true;
+    }
+    if (n_kt > 0) load_X(0, 0);
+    cp_async_commit();
+    if (n_kt > 1) load_X(1, 1);
+    cp_async_commit();
+
+    // ---- shrink: 16 rows x R ranks x this CTA's K range on tensor cores ----
+    const int warp = tid >> 5, lane = tid & 31;
+    const int n_tiles = R / 8;                  // 8 ranks per mma tile; <= 16
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    for (int kt = 0; kt < n_kt; ++kt) {
+        // groups so far: {A0,B0} {A1} {X0} {X1} then one per stage; waiting
+        // for all but the newest group leaves exactly stage kt resident
+        cp_async_wait<1>();
+        __syncthreads();
+        const int buf = kt & 1;
+        const bf16_t* xs = sX + buf * kRB * kLds;
+        const bf16_t* as = sA + buf * R * kLds;
+#pragma unroll
+        for (int ks = 0; ks < kKT / 16; ++ks) {
+            const int mi = lane >> 3, mr = lane & 7;
+            uint32_t a0, a1, a2, a3;
+            ldmatrix_x4(smem_u32(xs + ((mi & 1) * 8 + mr) * kLds + ks * 16 + (mi >> 1) * 8), a0, a1, a2, a3);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int tile = warp + nt * 8;
+                if (tile < n_tiles) {
+                    uint32_t b0, b1;
+                    const int l = lane & 15;
+                    ldmatrix_x2(smem_u32(as + (tile * 8 + (l & 7)) * kLds + ks * 16 + (l >> 3) * 8), b0, b1);
+                    mma_bf16_16816(acc[nt], a0, a1, a2, a3, b0, b1);
+                }
+            }
+        }
+        __syncthreads();
+        if (kt + 2 < n_kt) {
+            load_A(kt + 2, buf);
+            load_X(kt + 2, buf);
+        }
+        cp_async_commit();
+    }
+    {
+        const int gr = lane >> 2, q2 = (lane & 3) * 2;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int tile = warp + nt * 8;
+            if (tile < n_tiles) {
+                const int j = tile * 8 + q2;
+                vpart[gr * R + j] = acc[nt][0];
+                vpart[gr * R + j + 1] = acc[nt][1];
+                vpart[(gr + 8) * R + j] = acc[nt][2];
+                vpart[(gr + 8) * R + j + 1] = acc[nt][3];
+            }
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // ---- cluster reduction of the fp32 partials through DSMEM ----
+    cluster_arrive();
+    cluster_wait();
+    {
+        const int n4 = nrows * R / 4;
+        const uint32_t base = smem_u32(vpart);
+        for (int i = tid; i < n4; i += kThreads) {
+            float4 part4[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                if (c < p.cs) part4[c] = ld_dsmem_f4(map_rank(base + i * 16, c));
+            float4 s = part4[0];
+#pragma unroll
+            for (int c = 1; c < 16; ++c) {
+                if (c < p.cs) {
+                    s.x += part4[c].x;
+                    s.y += part4[c].y;
+                    s.z += part4[c].z;
+                    s.w += part4[c].w;
+                }
+            }
+            reinterpret_cast<float4*>(vfull)[i] = s;
+        }
+    }
+    cluster_arrive();   // this CTA no longer reads its peers' partials
+    __syncthreads();
+
+    // ---- expand: delta in registers, then the read-modify-write of y ----
+    const int upr = r_slot >> 3;   // 16-byte units per B row
+    for (int c0 = ch_begin; c0 < ch_end; c0 += kChunksTile) {
+        const int c1 = min(ch_end, c0 + kChunksTile);
+        const int nch = c1 - c0;
+        if (c0 != ch_begin) {
+            __syncthreads();
+            load_B(c0, c1);
+            cp_async_commit();
+            cp_async_wait<0>();
+            __syncthreads();
+        }
+        float d[kPairs][8];
+#pragma unroll
+        for (int q = 0; q < kPairs; ++q) {
+            const int i = tid + q * kThreads;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) d[q][e] = 0.f;
+            if (i < nrows * nch) {
+                const int t = i / nch, ci = i - t * nch;
+                int pj, col0;
+                chunk_proj(p.ps, c0 + ci, pj, col0);
+                const float* vt = vfull + t * R + pj * r_slot;
+                const bf16_t* bc = sB + ci * 8 * r_slot;
+                for (int jj = 0; jj < upr; ++jj) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int u = e * upr + jj;
+                        const uint4 bv = *reinterpret_cast<const uint4*>(bc + (u ^ (ci & 7)) * 8);
+                        d[q][e] = dot8f(bv, vt + jj * 8, d[q][e]);
+                    }
+                }
+            }
+        }
+        if (!waited) {
+            grid_dep_wait();   // y may be the preceding kernel's output
+            waited = true;
+        }
+        uint4 yo[kPairs];
+        bf16_t* yp[kPairs];
+#pragma unroll
+        for (int q = 0; q < kPairs; ++q) {
+            const int i = tid + q * kThreads;
+            yp[q] = nullptr;
+            if (i < nrows * nch) {
+                const int t = i / nch, ci = i - t * nch;
+                int pj, col0;
+                chunk_proj(p.ps, c0 + ci, pj, col0);
+                yp[q] = p.y + static_cast<size_t>(s_rows[t]) * p.ld_y + p.ps.out_off[pj] + col0;
+                yo[q] = *reinterpret_cast<const uint4*>(yp[q]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kPairs; ++q)
+            if (yp[q]) *reinterpret_cast<uint4*>(yp[q]) = add_round8(yo[q], d[q]);
+    }
+    if (!waited) grid_dep_wait();
+    if (bad_group && crank == 0 && part == 0 && tid == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
+    cluster_wait();     // peers are done reading this CTA's partials
+}
+
+size_t fused_smem_bytes(int R, int r_slot)
+{
+    return sizeof(bf16_t) * (2 * R * kLds + 2 * kRB * kLds) + sizeof(float) * 2 * kRB * R +
+           sizeof(bf16_t) * kChunksTile * 8 * r_slot;
+}
+
+int env_int(const char* name, int dflt)
+{
+    const char* e = std::getenv(name);
+    return (e && *e) ? std::atoi(e) : dflt;
+}
+
+}  // namespace
+
+bool fused_decode_supported(int n_proj, int r_slot)
+{
+    return r_slot <= LORA_BGMV_MAX_RANK && n_proj * r_slot <= 2 * 8 * 8 && r_slot % 8 == 0;
+}
+
+cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
+                              const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
+                              int n_pos, int n_rows, int n_slots, unsigned flags, int32_t* status,
+                              cudaStream_t stream)
+{
+    if (n_pos <= 0 || n_groups <= 0) return cudaSuccess;
+    const int R = ps.n_proj * ps.r_slot;
+    const size_t smem = fused_smem_bytes(R, ps.r_slot);
+    static int configured_device = -1;
+    static int n_sms = 148;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(bgmv_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(bgmv_fused_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    // Cluster size: split K as far as 16 CTAs while each keeps >= one stage.
+    int cs = 1;
+    while (cs < 16 && h_in / (cs * 2) >= kKT) cs *= 2;
+    cs = env_int("LORA_FUSED_CS", cs);
+    const int max_units = n_groups + n_pos / kRB;
+    // Column parts: enough clusters to give every SM about one CTA.
+    int parts = 1;
+    while (parts < 4 && max_units * cs * parts * 2 <= n_sms) parts *= 2;
+    parts = env_int("LORA_FUSED_PARTS", parts);
+
+    FusedParams p{};
+    p.ps = ps;
+    p.x = x;
+    p.ld_x = ld_x;
+    p.h_in = h_in;
+    p.y = y;
+    p.ld_y = ld_y;
+    p.perm = perm;
+    p.gstarts = gstarts;
+    p.gslot = gslot;
+    p.n_groups = n_groups;
+    p.n_pos = n_pos;
+    p.n_slots = n_slots;
+    p.n_rows = n_rows;
+    p.kc = ((h_in + cs - 1) / cs + 15) / 16 * 16;
+    p.n_parts = parts;
+    p.cs = cs;
+    p.x_ready = (flags & LORA_APPLY_X_READY) ? 1 : 0;
+    p.status = status;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(max_units * parts * cs));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    attrs[na].id = cudaLaunchAttributeClusterDimension;
+    attrs[na].val.clusterDim.x = cs;
+    attrs[na].val.clusterDim.y = 1;
+    attrs[na].val.clusterDim.z = 1;
+    ++na;
+    if (!(flags & LORA_APPLY_NO_PDL)) {
+        attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    e = cudaLaunchKernelEx(&cfg, bgmv_fused_kernel, p);
+    note_launch();
+    return e;
+}
+
+}  // namespace lora

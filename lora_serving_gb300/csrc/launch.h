@@ -21,4 +21,14 @@ cudaError_t launch_expand_rowwise(bf16_t* y, int ld_y, const float* v, int ld_v,
                                   const ProjSet& ps, const RowMap& map, int32_t* status,
                                   cudaStream_t stream);
 
+// Whether the fused decode kernel handles this projection set.
+bool fused_decode_supported(int n_proj, int r_slot);
+
+// Decode rows in gather form (perm / gstarts / gslot over n_pos positions):
+// shrink + cluster reduction + expand in one launch, no workspace.
+cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
+                              const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
+                              int n_pos, int n_rows, int n_slots, unsigned flags, int32_t* status,
+                              cudaStream_t stream);
+
 }  // namespace lora

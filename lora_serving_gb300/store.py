@@ -122,7 +122,7 @@ def workspace_for(n_rows: int, n_proj: int, r_slot: int, device="cuda") -> torch
 
 
 def apply(y: torch.Tensor, x: torch.Tensor, store: GroupStore, meta: BatchMeta,
-          workspace: torch.Tensor, dev_status=None, stream=None):
+          workspace: torch.Tensor, dev_status=None, stream=None, flags: int = 0):
     """One fused lora_apply call: y[:, slices] += delta of every projection."""
     abi.lora_apply(y, x, store.h_in, store.c_projs(), store.r_slot, store.n_slots, meta.c,
-                   workspace, dev_status=dev_status, stream=stream)
+                   workspace, flags=flags, dev_status=dev_status, stream=stream)

@@ -177,10 +177,10 @@ def test_kernel_entry_points_validate_before_launch():
     meta.lora_ids, meta.n_rows, meta.n_prefill = ids, 4, 0
     meta.perm, meta.gseg_starts, meta.gseg_slot, meta.n_gsegs = base, base, base, 1
     st = lib.lora_apply(base, 64, base, 64, 64, ctypes.addressof(projs), 1, 16, 2,
-                        ctypes.addressof(meta), 0, 0, 0, 0)
+                        ctypes.addressof(meta), 0, 0, 0, 0, 0)
     assert st == 7
     # lora_apply: too many projections
     st = lib.lora_apply(base, 64, base, 64, 64, ctypes.addressof(projs), 5, 16, 2,
-                        ctypes.addressof(meta), base, 1 << 20, 0, 0)
+                        ctypes.addressof(meta), base, 1 << 20, 0, 0, 0)
     assert st == 1
     assert lib.lora_apply_workspace_bytes(10, 3, 16) == 10 * 3 * 16 * 4

@@ -257,12 +257,14 @@ def test_bgmv_row_permutation_bit_exact():
     np.testing.assert_array_equal(_run_apply(wl2, "qkv"), base[p])
 
 
-def test_bad_slot_id_flagged_and_row_skipped():
+def test_bad_slot_in_gather_groups_flagged_and_rows_skipped():
+    """lora_apply's decode route reads the gather groups: a group naming a
+    slot >= n_slots is flagged and its rows are left alone."""
     ids = np.array([0, 1, 2, 3, 1, 0], np.int32)
     wl = _small(ids, 0)
     st = store.GroupStore.from_workload(wl, "g")
     meta = store.BatchMeta(ids, 0, wl.n_slots)
-    meta.ids.copy_(torch.tensor([0, 1, 9, 3, -5, 0], dtype=torch.int32))  # device ids corrupted
+    meta.gseg_slot.copy_(torch.tensor([0, 1, 9, 3], dtype=torch.int32))  # slot 2's group corrupted
     ws = store.workspace_for(6, 3, 8)
     y = to_dev(wl.y["g"])
     s = _status()
@@ -270,9 +272,57 @@ def test_bad_slot_id_flagged_and_row_skipped():
     torch.cuda.synchronize()
     assert abi.lora_read_device_status(s) & abi.LORA_DEV_SLOT_OUT_OF_RANGE
     got = to_host(y)
+    np.testing.assert_array_equal(got[2], wl.y["g"][2])
+    ok = np.array([0, 1, 3, 4, 5])
+    check_bf16(got[ok], oracle_group(wl, "g", ok), ids[ok], wl.y["g"][ok], "bad group slot")
+
+
+def test_bad_row_id_flagged_in_per_token_kernels():
+    """The per-token BGMV entry points read lora_ids: ids outside [-1, n_slots)
+    are flagged and those rows skipped."""
+    ids = np.array([0, 1, 2, 3, 1, 0], np.int32)
+    wl = _small(ids, 0, widths=(64,))
+    st = store.GroupStore.from_workload(wl, "g")
+    bad = torch.tensor([0, 1, 9, 3, -5, 0], dtype=torch.int32, device="cuda")
+    v = torch.zeros(6, 8, device="cuda")
+    y = to_dev(wl.y["g"])
+    s = _status()
+    abi.lora_bgmv_shrink(v, to_dev(wl.x["g"]), st.A[0], bad, h_in=64, r_slot=8, n_slots=4, dev_status=s)
+    abi.lora_bgmv_expand(y, 0, 64, v, st.B[0], bad, r_slot=8, n_slots=4, dev_status=s)
+    torch.cuda.synchronize()
+    assert abi.lora_read_device_status(s) & abi.LORA_DEV_SLOT_OUT_OF_RANGE
+    got = to_host(y)
     np.testing.assert_array_equal(got[[2, 4]], wl.y["g"][[2, 4]])
     ok = np.array([0, 1, 3, 5])
     check_bf16(got[ok], oracle_group(wl, "g", ok), ids[ok], wl.y["g"][ok], "bad id")
+
+
+@pytest.mark.parametrize("flags", [0, abi.LORA_APPLY_X_READY, abi.LORA_APPLY_NO_PDL,
+                                   abi.LORA_APPLY_X_READY | abi.LORA_APPLY_NO_PDL])
+def test_apply_orderings_give_identical_bits(flags):
+    """The launch-ordering flags change when work may start, never the result;
+    a chain of calls with PDL matches the same chain with plain ordering."""
+    wl = _wl("llama3b_decode", "accumulate")
+    base = _run_apply(wl, "qkv")
+    g = wl.groups[0]
+    st = store.GroupStore.from_workload(wl, g.name)
+    meta = store.BatchMeta(wl.ids, 0, wl.n_slots)
+    ws = store.workspace_for(wl.n_rows, 3, wl.r_slot)
+    x = to_dev(wl.x[g.name])
+    y = to_dev(wl.y[g.name])
+    ys = [y.clone() for _ in range(4)]
+    for yy in ys:  # back-to-back dependent-free calls, then one call that re-reads its own output
+        store.apply(yy, x, st, meta, ws, flags=flags)
+    store.apply(ys[0], x, st, meta, ws, flags=flags)
+    torch.cuda.synchronize()
+    for yy in ys[1:]:
+        np.testing.assert_array_equal(to_host(yy), base)
+    twice = _run_apply(wl, "qkv")  # fresh: one application
+    st2 = store.GroupStore.from_workload(wl, g.name)
+    y2 = to_dev(twice)
+    store.apply(y2, x, st2, meta, ws, flags=abi.LORA_APPLY_NO_PDL)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_host(ys[0]), to_host(y2))
 
 
 def test_bad_segment_table_flagged():
@@ -299,3 +349,35 @@ def test_host_rejects_before_enqueue():
         store.apply(y, to_dev(wl.x["g"]), st, meta, store.workspace_for(1, 1, 8)[:16])
     assert e.value.name == "LORA_ERR_WORKSPACE"
     np.testing.assert_array_equal(to_host(y), wl.y["g"])
+
+
+@pytest.mark.parametrize("h_in,widths,rank,T,n_slots", [
+    (4096, (4096, 1024, 1024, 1024), 32, 200, 8),   # 4 projections x rank 32: 128 ranks per row
+    (28672, (8192,), 16, 40, 4),                    # long K: the cluster's K chunks pipeline in stages
+    (3072, (3072,), 8, 100, 2),                     # ~50 rows per adapter: several 16-row units each
+    (256, (256, 64, 64), 16, 7, 3),                 # fewer rows than one unit
+])
+def test_apply_decode_fused_shapes(h_in, widths, rank, T, n_slots):
+    rng = np.random.default_rng(h_in + T)
+    ids = rng.integers(-1, n_slots, T).astype(np.int32)
+    wl = _small(ids, 0, n_slots=n_slots, rank=rank, h_in=h_in, widths=widths, seed=T)
+    got = _run_apply(wl, "g")
+    check_bf16(got, oracle_group(wl, "g"), wl.ids, wl.y["g"], f"fused h_in={h_in} R={rank * len(widths)}")
+
+
+def test_apply_decode_bad_permutation_flagged():
+    """A corrupted gather permutation is flagged and its group's rows skipped."""
+    ids = np.array([0, 1, 0, 1, 0, 1], np.int32)
+    wl = _small(ids, 0)
+    st = store.GroupStore.from_workload(wl, "g")
+    meta = store.BatchMeta(ids, 0, wl.n_slots)
+    meta.perm.copy_(torch.tensor([0, 2, 77, 1, 3, 5], dtype=torch.int32))  # slot 0's group has row 77
+    s = _status()
+    y = to_dev(wl.y["g"])
+    store.apply(y, to_dev(wl.x["g"]), st, meta, store.workspace_for(6, 3, 8), dev_status=s)
+    torch.cuda.synchronize()
+    assert abi.lora_read_device_status(s) & abi.LORA_DEV_BAD_SEGMENT
+    got = to_host(y)
+    np.testing.assert_array_equal(got[[0, 2, 4]], wl.y["g"][[0, 2, 4]])
+    ok = np.array([1, 3, 5])
+    check_bf16(got[ok], oracle_group(wl, "g", ok), ids[ok], wl.y["g"][ok], "slot 1 rows")
