@@ -123,26 +123,93 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Unit u -> (group, first position, rows).  Uniform across the cluster.
-// Groups whose bounds fall outside [0, n_pos) are skipped (bad set), so perm
-// is never read out of range.
-__device__ __forceinline__ bool find_unit(const FusedParams& p, int u, int& g, int& pos0, int& nrows, bool& bad)
+// Units of group i: ceil(len / 16), or 0 (and bad) when its bounds fall
+// outside [0, n_pos) -- so perm is never read out of range.
+__device__ __forceinline__ int group_units(int s, int e, int n_pos, bool& bad)
 {
-    int acc = 0;
-    for (int i = 0; i < p.n_groups; ++i) {
-        const int s = __ldg(p.gstarts + i), e = __ldg(p.gstarts + i + 1);
-        const bool sane = s >= 0 && e <= p.n_pos && s <= e;
-        bad |= !sane;
-        const int n = sane ? (e - s + kRB - 1) / kRB : 0;
-        if (u < acc + n) {
-            g = i;
-            pos0 = s + (u - acc) * kRB;
-            nrows = min(kRB, e - pos0);
-            return true;
-        }
-        acc += n;
+    const bool sane = s >= 0 && e <= n_pos && s <= e;
+    bad |= !sane;
+    return sane ? (e - s + kRB - 1) / kRB : 0;
+}
+
+struct UnitInfo {
+    int g, pos0, nrows, slot, found, bad;
+};
+
+// Unit u -> (group, first position, rows, slot).  Every thread of the CTA
+// takes part; the answer is uniform across the cluster (all CTAs of a
+// cluster map to the same unit).  Tables of up to kThreads groups are
+// scanned in parallel (one group per thread, block-wide prefix sum); larger
+// tables fall back to a serial scan.
+__device__ __forceinline__ UnitInfo find_unit(const FusedParams& p, int u)
+{
+    __shared__ int s_warp[kThreads / 32];
+    __shared__ UnitInfo s_info;
+    __shared__ int s_bad;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        s_info.found = 0;
+        s_bad = 0;
     }
-    return false;
+    if (p.n_groups <= kThreads) {
+        int s = 0, e = 0, sl = -1;
+        bool bad = false;
+        int n = 0;
+        if (tid < p.n_groups) {   // one parallel round trip for the whole table
+            s = __ldg(p.gstarts + tid);
+            e = __ldg(p.gstarts + tid + 1);
+            sl = __ldg(p.gslot + tid);
+            n = group_units(s, e, p.n_pos, bad);
+        }
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        if (lane == 31) s_warp[warp] = incl;
+        __syncthreads();
+        int before = 0;
+        for (int w = 0; w < warp; ++w) before += s_warp[w];
+        incl += before;
+        const int excl = incl - n;
+        if (bad) atomicOr(&s_bad, 1);
+        if (tid < p.n_groups && u >= excl && u < incl) {
+            UnitInfo info;
+            info.g = tid;
+            info.pos0 = s + (u - excl) * kRB;
+            info.nrows = min(kRB, e - info.pos0);
+            info.slot = sl;
+            info.found = 1;
+            info.bad = 0;
+            s_info = info;
+        }
+        __syncthreads();
+    } else {
+        __syncthreads();
+        if (tid == 0) {
+            int acc = 0;
+            bool bad = false;
+            for (int i = 0; i < p.n_groups; ++i) {
+                const int s = __ldg(p.gstarts + i), e = __ldg(p.gstarts + i + 1);
+                const int n = group_units(s, e, p.n_pos, bad);
+                if (u < acc + n) {
+                    s_info.g = i;
+                    s_info.pos0 = s + (u - acc) * kRB;
+                    s_info.nrows = min(kRB, e - s_info.pos0);
+                    s_info.slot = __ldg(p.gslot + i);
+                    s_info.found = 1;
+                    break;
+                }
+                acc += n;
+            }
+            s_bad = bad;
+        }
+        __syncthreads();
+    }
+    UnitInfo r = s_info;
+    r.bad = s_bad;
+    return r;
 }
 
 // Output chunk (8 columns) -> projection and column within it.
@@ -156,7 +223,7 @@ __device__ __forceinline__ void chunk_proj(const ProjSet& ps, int ch, int& p, in
     col0 = ch << 3;
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 bgmv_fused_kernel(FusedParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -177,19 +244,16 @@ bgmv_fused_kernel(FusedParams p)
     const int unit = cluster / p.n_parts;
     const int part = cluster - unit * p.n_parts;
 
-    // Every exit path waits for the preceding grid first, so this grid never
-    // completes before it (stream order stays transitive under PDL), and
-    // status flags are written only after the wait.
-    int g, pos0, nrows;
-    bool bad_group = false;
-    if (!find_unit(p, unit, g, pos0, nrows, bad_group)) {   // whole cluster exits together
-        grid_dep_wait();
-        if (bad_group && crank == 0 && tid == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
-        return;
-    }
-    const int slot = __ldg(p.gslot + g);
-    if (slot == -1) {                                  // base-only rows: untouched
-        grid_dep_wait();
+    // Exits: CTA 0 of the grid always waits for the preceding grid before it
+    // leaves, so this grid never completes before that one (stream order
+    // stays transitive under PDL); status flags are written only after a
+    // wait.  Clusters without work leave at once and free their SM slots.
+    const UnitInfo ui = find_unit(p, unit);     // uniform across the cluster
+    const bool bad_group = ui.bad;
+    const int pos0 = ui.pos0, nrows = ui.nrows, slot = ui.slot;
+    if (!ui.found || slot == -1) {              // nothing to do (or base-only rows)
+        if (blockIdx.x == 0 || bad_group) grid_dep_wait();
+        if (bad_group && crank == 0 && part == 0 && tid == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
         return;
     }
     if (slot < -1 || slot >= p.n_slots) {
@@ -205,13 +269,6 @@ bgmv_fused_kernel(FusedParams p)
             if (r < 0 || r >= p.n_rows) { bad_row = true; r = 0; }
         }
         s_rows[tid] = r;
-    }
-    if (__syncthreads_or(bad_row)) {
-        // A malformed permutation: flag it and leave this unit's rows alone.
-        // Every CTA of the cluster reads the same entries, so all return here.
-        grid_dep_wait();
-        if (tid == 0 && crank == 0 && part == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
-        return;
     }
 
     // ---- this CTA's K range and output chunks ----
@@ -264,6 +321,16 @@ bgmv_fused_kernel(FusedParams p)
     cp_async_commit();
     if (n_kt > 1) load_A(1, 1);
     cp_async_commit();
+
+    if (__syncthreads_or(bad_row)) {
+        // A malformed permutation: flag it and leave this unit's rows alone.
+        // Every CTA of the cluster reads the same entries, so all return here
+        // (after their own copies into shared memory have landed).
+        cp_async_wait<0>();
+        grid_dep_wait();
+        if (tid == 0 && crank == 0 && part == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
+        return;
+    }
 
     bool waited = false;
     if (!p.x_ready) {
@@ -436,8 +503,8 @@ bool fused_decode_supported(int n_proj, int r_slot)
 
 cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
                               const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
-                              int n_pos, int n_rows, int n_slots, unsigned flags, int32_t* status,
-                              cudaStream_t stream)
+                              int n_pos, int max_group_len, int n_rows, int n_slots, unsigned flags,
+                              int32_t* status, cudaStream_t stream)
 {
     if (n_pos <= 0 || n_groups <= 0) return cudaSuccess;
     const int R = ps.n_proj * ps.r_slot;
@@ -460,11 +527,12 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     int cs = 1;
     while (cs < 16 && h_in / (cs * 2) >= kKT) cs *= 2;
     cs = env_int("LORA_FUSED_CS", cs);
-    const int max_units = n_groups + n_pos / kRB;
-    // Column parts: enough clusters to give every SM about one CTA.
-    int parts = 1;
-    while (parts < 4 && max_units * cs * parts * 2 <= n_sms) parts *= 2;
-    parts = env_int("LORA_FUSED_PARTS", parts);
+    // Units of <= 16 rows: at most ceil(longest group / 16) per group.
+    int max_units = n_groups + n_pos / kRB;
+    if (max_group_len > 0) max_units = min(max_units, n_groups * ((max_group_len + kRB - 1) / kRB));
+    // Column parts per unit (more clusters, each recomputing the shrink);
+    // one part measured best on the decode shapes here.
+    const int parts = env_int("LORA_FUSED_PARTS", 1);
 
     FusedParams p{};
     p.ps = ps;

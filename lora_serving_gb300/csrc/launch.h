@@ -28,7 +28,7 @@ bool fused_decode_supported(int n_proj, int r_slot);
 // shrink + cluster reduction + expand in one launch, no workspace.
 cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
                               const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
-                              int n_pos, int n_rows, int n_slots, unsigned flags, int32_t* status,
-                              cudaStream_t stream);
+                              int n_pos, int max_group_len, int n_rows, int n_slots, unsigned flags,
+                              int32_t* status, cudaStream_t stream);
 
 }  // namespace lora
