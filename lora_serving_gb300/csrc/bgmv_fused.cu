@@ -11,10 +11,12 @@
 //   CTA c computes partial v_c[t][j] = sum_{k in chunk c} A[j][k] x[t][k]
 //   with mma.sync m16n8k16 (bf16 in, fp32 out: 16 rows x 8 ranks tiles).
 // The partials meet in distributed shared memory: after a cluster barrier
-// every CTA sums v = sum_c v_c in a fixed order (deterministic, fp32, never
-// rounded to bf16) and forms the delta of its own slice of output columns
-//   d[t][col] = sum_j B'_p[col][j] v[t][p*r + j]
-// in registers; the only step left is y[t][off_p + col] = bf16_rne(y + d).
+// every CTA sums v = sum_c v_c in a fixed order (deterministic, fp32).  The
+// expand of the CTA's own output columns runs on the tensor cores as well:
+// v is split into v_hi = bf16(v) and v_lo = bf16(v - v_hi), so
+//   d[t][col] = sum_j B'[col][j] (v_hi + v_lo)[t][j]
+// carries v to ~2^-17 relative (v itself is never rounded to one bf16), and
+// the last step is y[t][off_p + col] = bf16_rne(y + d).
 //
 // Latency (programmatic dependent launch): metadata and weights are read
 // before griddepcontrol.wait, so they stream in while the preceding kernel
@@ -35,10 +37,11 @@ constexpr int kRB = 16;       // rows per unit (the mma M)
 constexpr int kKT = 128;      // K elements per pipeline stage
 constexpr int kPad = 8;       // bf16 padding per smem row: conflict-free ldmatrix
 constexpr int kLds = kKT + kPad;
-constexpr int kTC = 512;      // expand columns per tile
-constexpr int kChunksTile = kTC / 8;
+constexpr int kMaxChunks = 64;     // output chunks (8 columns) per CTA and tile
 constexpr int kThreads = 256;
-constexpr int kPairs = kRB * kChunksTile / kThreads;  // (row, chunk) pairs per thread per tile
+constexpr int kWarps = kThreads / 32;
+constexpr int kChunksPerWarp = kMaxChunks / kWarps;
+constexpr int kPermStage = 4096;   // decode positions staged in smem with the group table
 
 struct FusedParams {
     ProjSet ps;
@@ -57,6 +60,7 @@ struct FusedParams {
     int kc;                   // K elements per cluster rank (multiple of 16)
     int n_parts;              // column parts per unit
     int cs;                   // cluster size
+    int r_pad;                // r_slot rounded up to 16 (expand mma K)
     int x_ready;              // x may be read before the grid dependency resolves
     int32_t* status;
 };
@@ -95,11 +99,10 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t local_addr, uint32_t rank)
 }
 // Plain (non-volatile) DSMEM load: ordering against the partials' writes is
 // given by the cluster barrier, so independent loads may be issued together.
-__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t remote)
+__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t remote)
 {
-    float4 v;
-    asm("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
-        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(remote));
+    float2 v;
+    asm("ld.shared::cluster.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(remote));
     return v;
 }
 
@@ -123,7 +126,17 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Units of group i: ceil(len / 16), or 0 (and bad) when its bounds fall
+// v (two fp32 values) -> packed bf16 hi pair and bf16 lo pair (v ~= hi + lo).
+__device__ __forceinline__ void split_hi_lo(float a, float b, uint32_t& hi, uint32_t& lo)
+{
+    const __nv_bfloat16 ah = __float2bfloat16_rn(a), bh = __float2bfloat16_rn(b);
+    const __nv_bfloat16 al = __float2bfloat16_rn(a - __bfloat162float(ah));
+    const __nv_bfloat16 bl = __float2bfloat16_rn(b - __bfloat162float(bh));
+    hi = static_cast<uint32_t>(__bfloat16_as_ushort(ah)) | (static_cast<uint32_t>(__bfloat16_as_ushort(bh)) << 16);
+    lo = static_cast<uint32_t>(__bfloat16_as_ushort(al)) | (static_cast<uint32_t>(__bfloat16_as_ushort(bl)) << 16);
+}
+
+// Units of a group: ceil(len / 16), or 0 (and bad) when its bounds fall
 // outside [0, n_pos) -- so perm is never read out of range.
 __device__ __forceinline__ int group_units(int s, int e, int n_pos, bool& bad)
 {
@@ -138,12 +151,12 @@ struct UnitInfo {
 
 // Unit u -> (group, first position, rows, slot).  Every thread of the CTA
 // takes part; the answer is uniform across the cluster (all CTAs of a
-// cluster map to the same unit).  Tables of up to kThreads groups are
-// scanned in parallel (one group per thread, block-wide prefix sum); larger
-// tables fall back to a serial scan.
-__device__ __forceinline__ UnitInfo find_unit(const FusedParams& p, int u)
+// cluster map to the same unit).  The group table is read in one parallel
+// round trip (one group per thread, block-wide prefix sum), together with
+// the permutation when it fits in s_perm; larger tables take a serial scan.
+__device__ __forceinline__ UnitInfo find_unit(const FusedParams& p, int u, int* s_perm, bool stage_perm)
 {
-    __shared__ int s_warp[kThreads / 32];
+    __shared__ int s_warp[kWarps];
     __shared__ UnitInfo s_info;
     __shared__ int s_bad;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -151,11 +164,13 @@ __device__ __forceinline__ UnitInfo find_unit(const FusedParams& p, int u)
         s_info.found = 0;
         s_bad = 0;
     }
+    if (stage_perm)
+        for (int i = tid; i < p.n_pos; i += kThreads) s_perm[i] = __ldg(p.perm + i);
     if (p.n_groups <= kThreads) {
         int s = 0, e = 0, sl = -1;
         bool bad = false;
         int n = 0;
-        if (tid < p.n_groups) {   // one parallel round trip for the whole table
+        if (tid < p.n_groups) {
             s = __ldg(p.gstarts + tid);
             e = __ldg(p.gstarts + tid + 1);
             sl = __ldg(p.gslot + tid);
@@ -229,26 +244,33 @@ bgmv_fused_kernel(FusedParams p)
     extern __shared__ __align__(128) unsigned char smem[];
     const int R = p.ps.n_proj * p.ps.r_slot;
     const int r_slot = p.ps.r_slot;
+    const int r_pad = p.r_pad;
+    const int lds_b = r_pad + 8;                                     // B row stride (bf16)
     bf16_t* sA = reinterpret_cast<bf16_t*>(smem);                    // [2][R][kLds]
     bf16_t* sX = sA + 2 * R * kLds;                                  // [2][kRB][kLds]
     float* vpart = reinterpret_cast<float*>(sX + 2 * kRB * kLds);    // [kRB][R]
     float* vfull = vpart + kRB * R;                                  // [kRB][R]
-    bf16_t* sB = reinterpret_cast<bf16_t*>(vfull + kRB * R);         // [kChunksTile][8*r_slot], swizzled
+    bf16_t* sB = reinterpret_cast<bf16_t*>(vfull + kRB * R);         // [kMaxChunks*8][lds_b]
+    int* s_perm = reinterpret_cast<int*>(sB + kMaxChunks * 8 * lds_b);
     __shared__ int s_rows[kRB];
+    __shared__ int s_cp[kMaxChunks];      // chunk -> projection
+    __shared__ int s_ccol[kMaxChunks];    // chunk -> first column within its projection
 
     grid_dep_launch();
 
     const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
     const int crank = static_cast<int>(cluster_rank());
     const int cluster = blockIdx.x / p.cs;
     const int unit = cluster / p.n_parts;
     const int part = cluster - unit * p.n_parts;
+    const bool stage_perm = p.n_pos <= kPermStage;
 
     // Exits: CTA 0 of the grid always waits for the preceding grid before it
     // leaves, so this grid never completes before that one (stream order
     // stays transitive under PDL); status flags are written only after a
     // wait.  Clusters without work leave at once and free their SM slots.
-    const UnitInfo ui = find_unit(p, unit);     // uniform across the cluster
+    const UnitInfo ui = find_unit(p, unit, s_perm, stage_perm);   // uniform across the cluster
     const bool bad_group = ui.bad;
     const int pos0 = ui.pos0, nrows = ui.nrows, slot = ui.slot;
     if (!ui.found || slot == -1) {              // nothing to do (or base-only rows)
@@ -265,7 +287,7 @@ bgmv_fused_kernel(FusedParams p)
     if (tid < kRB) {
         int r = 0;
         if (tid < nrows) {
-            r = __ldg(p.perm + pos0 + tid);
+            r = stage_perm ? s_perm[pos0 + tid] : __ldg(p.perm + pos0 + tid);
             if (r < 0 || r >= p.n_rows) { bad_row = true; r = 0; }
         }
         s_rows[tid] = r;
@@ -281,6 +303,14 @@ bgmv_fused_kernel(FusedParams p)
     const int ch_begin = static_cast<int>((static_cast<long long>(total_ch) * q_idx) / q_n);
     const int ch_end = static_cast<int>((static_cast<long long>(total_ch) * (q_idx + 1)) / q_n);
 
+    auto map_chunks = [&](int c0, int c1) {
+        for (int ci = tid; ci < c1 - c0; ci += kThreads) {
+            int pj, col0;
+            chunk_proj(p.ps, c0 + ci, pj, col0);
+            s_cp[ci] = pj;
+            s_ccol[ci] = col0;
+        }
+    };
     auto load_A = [&](int kt, int buf) {
         const int k0 = k_begin + kt * kKT;
         for (int i = tid; i < R * (kKT / 8); i += kThreads) {
@@ -302,22 +332,26 @@ bgmv_fused_kernel(FusedParams p)
             cp_async16(smem_u32(sX + (buf * kRB + t) * kLds + u * 8), src, ok);
         }
     };
+    // B' rows (one per output column) for chunks [c0, c1): r_pad bf16 each,
+    // zero past r_slot; rows padded to lds_b for conflict-free ldmatrix.
+    // Needs s_cp / s_ccol of the same chunks (after a __syncthreads).
     auto load_B = [&](int c0, int c1) {
-        // chunk = 8 output columns x r_slot ranks = r_slot 16-byte units,
-        // stored with the unit index XOR (chunk & 7) to spread smem banks
-        for (int i = tid; i < (c1 - c0) * r_slot; i += kThreads) {
-            const int ci = i / r_slot, u = i - ci * r_slot;
-            int pj, col0;
-            chunk_proj(p.ps, c0 + ci, pj, col0);
-            const bf16_t* src = p.ps.B[pj] + (static_cast<size_t>(slot) * p.ps.width[pj] + col0) * r_slot + u * 8;
-            cp_async16(smem_u32(sB + ci * 8 * r_slot + (u ^ (ci & 7)) * 8), src, true);
+        const int upr = r_pad >> 3;
+        for (int i = tid; i < (c1 - c0) * 8 * upr; i += kThreads) {
+            const int row = i / upr, u = i - row * upr;
+            const int ci = row >> 3, e = row & 7;
+            const int pj = s_cp[ci];
+            const bool ok = u * 8 < r_slot;
+            const bf16_t* src = p.ps.B[pj] +
+                                (ok ? (static_cast<size_t>(slot) * p.ps.width[pj] + s_ccol[ci] + e) * r_slot + u * 8 : 0);
+            cp_async16(smem_u32(sB + row * lds_b + u * 8), src, ok);
         }
     };
 
     // ---- weights first: they do not depend on the preceding kernel ----
-    const int tile0_end = min(ch_end, ch_begin + kChunksTile);
+    const int tile0_end = min(ch_end, ch_begin + kMaxChunks);
+    map_chunks(ch_begin, tile0_end);
     if (n_kt > 0) load_A(0, 0);
-    if (ch_end > ch_begin) load_B(ch_begin, tile0_end);
     cp_async_commit();
     if (n_kt > 1) load_A(1, 1);
     cp_async_commit();
@@ -331,6 +365,9 @@ bgmv_fused_kernel(FusedParams p)
         if (tid == 0 && crank == 0 && part == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
         return;
     }
+    // s_cp / s_ccol are visible after the barrier above
+    if (ch_end > ch_begin) load_B(ch_begin, tile0_end);
+    cp_async_commit();
 
     bool waited = false;
     if (!p.x_ready) {
@@ -343,11 +380,10 @@ bgmv_fused_kernel(FusedParams p)
     cp_async_commit();
 
     // ---- shrink: 16 rows x R ranks x this CTA's K range on tensor cores ----
-    const int warp = tid >> 5, lane = tid & 31;
     const int n_tiles = R / 8;                  // 8 ranks per mma tile; <= 16
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     for (int kt = 0; kt < n_kt; ++kt) {
-        // groups so far: {A0,B0} {A1} {X0} {X1} then one per stage; waiting
+        // groups so far: {A0} {A1} {B0} {X0} {X1} then one per stage; waiting
         // for all but the newest group leaves exactly stage kt resident
         cp_async_wait<1>();
         __syncthreads();
@@ -398,59 +434,79 @@ bgmv_fused_kernel(FusedParams p)
     cluster_arrive();
     cluster_wait();
     {
-        const int n4 = nrows * R / 4;
+        const int n2 = kRB * R / 2;   // all 16 rows: rows past nrows sum to zero
         const uint32_t base = smem_u32(vpart);
-        for (int i = tid; i < n4; i += kThreads) {
-            float4 part4[16];
+        for (int i = tid; i < n2; i += kThreads) {
+            float2 part2[16];         // all peers' loads in flight, then a fixed-order sum
 #pragma unroll
             for (int c = 0; c < 16; ++c)
-                if (c < p.cs) part4[c] = ld_dsmem_f4(map_rank(base + i * 16, c));
-            float4 s = part4[0];
+                if (c < p.cs) part2[c] = ld_dsmem_f2(map_rank(base + i * 8, c));
+            float2 s = part2[0];
 #pragma unroll
             for (int c = 1; c < 16; ++c) {
                 if (c < p.cs) {
-                    s.x += part4[c].x;
-                    s.y += part4[c].y;
-                    s.z += part4[c].z;
-                    s.w += part4[c].w;
+                    s.x += part2[c].x;
+                    s.y += part2[c].y;
                 }
             }
-            reinterpret_cast<float4*>(vfull)[i] = s;
+            reinterpret_cast<float2*>(vfull)[i] = s;
         }
     }
     cluster_arrive();   // this CTA no longer reads its peers' partials
     __syncthreads();
 
-    // ---- expand: delta in registers, then the read-modify-write of y ----
-    const int upr = r_slot >> 3;   // 16-byte units per B row
-    for (int c0 = ch_begin; c0 < ch_end; c0 += kChunksTile) {
-        const int c1 = min(ch_end, c0 + kChunksTile);
+    // ---- expand on tensor cores: d[16 rows][8 cols] per chunk ----
+    const int gr = lane >> 2, q2 = (lane & 3) * 2;
+    for (int c0 = ch_begin; c0 < ch_end; c0 += kMaxChunks) {
+        const int c1 = min(ch_end, c0 + kMaxChunks);
         const int nch = c1 - c0;
         if (c0 != ch_begin) {
+            __syncthreads();
+            map_chunks(c0, c1);
             __syncthreads();
             load_B(c0, c1);
             cp_async_commit();
             cp_async_wait<0>();
             __syncthreads();
         }
-        float d[kPairs][8];
+        float d[kChunksPerWarp][4];
+        int cur_p = -1;
+        uint32_t ahi[2][4], alo[2][4];   // v fragments of the current projection (r_pad <= 32)
 #pragma unroll
-        for (int q = 0; q < kPairs; ++q) {
-            const int i = tid + q * kThreads;
+        for (int w = 0; w < kChunksPerWarp; ++w) {
+            const int ci = warp + w * kWarps;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) d[q][e] = 0.f;
-            if (i < nrows * nch) {
-                const int t = i / nch, ci = i - t * nch;
-                int pj, col0;
-                chunk_proj(p.ps, c0 + ci, pj, col0);
-                const float* vt = vfull + t * R + pj * r_slot;
-                const bf16_t* bc = sB + ci * 8 * r_slot;
-                for (int jj = 0; jj < upr; ++jj) {
+            for (int e = 0; e < 4; ++e) d[w][e] = 0.f;
+            if (ci < nch) {
+                const int pj = s_cp[ci];
+                if (pj != cur_p) {
+                    cur_p = pj;
+                    const float* vp = vfull + pj * r_slot;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int u = e * upr + jj;
-                        const uint4 bv = *reinterpret_cast<const uint4*>(bc + (u ^ (ci & 7)) * 8);
-                        d[q][e] = dot8f(bv, vt + jj * 8, d[q][e]);
+                    for (int kk = 0; kk < 2; ++kk) {
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            // a0: (row g, k 2q..), a1: (row g+8, k 2q..), a2: (row g, k 2q+8..), a3: (row g+8, k 2q+8..)
+                            const int row = gr + (h & 1) * 8;
+                            const int k = kk * 16 + q2 + (h >> 1) * 8;
+                            float v0 = 0.f, v1 = 0.f;
+                            if (k < r_slot) {
+                                v0 = vp[row * R + k];
+                                v1 = vp[row * R + k + 1];
+                            }
+                            split_hi_lo(v0, v1, ahi[kk][h], alo[kk][h]);
+                        }
+                    }
+                }
+                const bf16_t* bc = sB + ci * 8 * lds_b;
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    if (kk * 16 < r_pad) {
+                        uint32_t b0, b1;
+                        const int l = lane & 15;
+                        ldmatrix_x2(smem_u32(bc + (l & 7) * lds_b + kk * 16 + (l >> 3) * 8), b0, b1);
+                        mma_bf16_16816(d[w], ahi[kk][0], ahi[kk][1], ahi[kk][2], ahi[kk][3], b0, b1);
+                        mma_bf16_16816(d[w], alo[kk][0], alo[kk][1], alo[kk][2], alo[kk][3], b0, b1);
                     }
                 }
             }
@@ -459,33 +515,43 @@ bgmv_fused_kernel(FusedParams p)
             grid_dep_wait();   // y may be the preceding kernel's output
             waited = true;
         }
-        uint4 yo[kPairs];
-        bf16_t* yp[kPairs];
+        // d[w]: (row g, cols 2q, 2q+1) and (row g+8, same cols) of chunk ci
+        uint32_t yo[kChunksPerWarp][2];
 #pragma unroll
-        for (int q = 0; q < kPairs; ++q) {
-            const int i = tid + q * kThreads;
-            yp[q] = nullptr;
-            if (i < nrows * nch) {
-                const int t = i / nch, ci = i - t * nch;
-                int pj, col0;
-                chunk_proj(p.ps, c0 + ci, pj, col0);
-                yp[q] = p.y + static_cast<size_t>(s_rows[t]) * p.ld_y + p.ps.out_off[pj] + col0;
-                yo[q] = *reinterpret_cast<const uint4*>(yp[q]);
+        for (int w = 0; w < kChunksPerWarp; ++w) {
+            const int ci = warp + w * kWarps;
+            if (ci < nch) {
+                const int pj = s_cp[ci];
+                const int col = p.ps.out_off[pj] + s_ccol[ci] + q2;
+                if (gr < nrows) yo[w][0] = *reinterpret_cast<const uint32_t*>(p.y + static_cast<size_t>(s_rows[gr]) * p.ld_y + col);
+                if (gr + 8 < nrows) yo[w][1] = *reinterpret_cast<const uint32_t*>(p.y + static_cast<size_t>(s_rows[gr + 8]) * p.ld_y + col);
             }
         }
 #pragma unroll
-        for (int q = 0; q < kPairs; ++q)
-            if (yp[q]) *reinterpret_cast<uint4*>(yp[q]) = add_round8(yo[q], d[q]);
+        for (int w = 0; w < kChunksPerWarp; ++w) {
+            const int ci = warp + w * kWarps;
+            if (ci < nch) {
+                const int pj = s_cp[ci];
+                const int col = p.ps.out_off[pj] + s_ccol[ci] + q2;
+                if (gr < nrows)
+                    *reinterpret_cast<uint32_t*>(p.y + static_cast<size_t>(s_rows[gr]) * p.ld_y + col) =
+                        pack_bf16x2(bf16_lo(yo[w][0]) + d[w][0], bf16_hi(yo[w][0]) + d[w][1]);
+                if (gr + 8 < nrows)
+                    *reinterpret_cast<uint32_t*>(p.y + static_cast<size_t>(s_rows[gr + 8]) * p.ld_y + col) =
+                        pack_bf16x2(bf16_lo(yo[w][1]) + d[w][2], bf16_hi(yo[w][1]) + d[w][3]);
+            }
+        }
     }
     if (!waited) grid_dep_wait();
     if (bad_group && crank == 0 && part == 0 && tid == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
     cluster_wait();     // peers are done reading this CTA's partials
 }
 
-size_t fused_smem_bytes(int R, int r_slot)
+size_t fused_smem_bytes(int R, int r_pad, int n_pos)
 {
+    const int perm = n_pos <= kPermStage ? n_pos : 0;
     return sizeof(bf16_t) * (2 * R * kLds + 2 * kRB * kLds) + sizeof(float) * 2 * kRB * R +
-           sizeof(bf16_t) * kChunksTile * 8 * r_slot;
+           sizeof(bf16_t) * kMaxChunks * 8 * (r_pad + 8) + sizeof(int) * perm;
 }
 
 int env_int(const char* name, int dflt)
@@ -508,18 +574,16 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
 {
     if (n_pos <= 0 || n_groups <= 0) return cudaSuccess;
     const int R = ps.n_proj * ps.r_slot;
-    const size_t smem = fused_smem_bytes(R, ps.r_slot);
+    const int r_pad = (ps.r_slot + 15) / 16 * 16;
+    const size_t smem = fused_smem_bytes(R, r_pad, n_pos);
     static int configured_device = -1;
-    static int n_sms = 148;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(bgmv_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+        e = cudaFuncSetAttribute(bgmv_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(bgmv_fused_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
@@ -551,6 +615,7 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     p.kc = ((h_in + cs - 1) / cs + 15) / 16 * 16;
     p.n_parts = parts;
     p.cs = cs;
+    p.r_pad = r_pad;
     p.x_ready = (flags & LORA_APPLY_X_READY) ? 1 : 0;
     p.status = status;
 
