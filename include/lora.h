@@ -74,6 +74,8 @@ typedef enum {
 /* Bits OR-ed into *dev_status by the kernels. */
 #define LORA_DEV_SLOT_OUT_OF_RANGE 0x1 /* a row named an id >= n_slots or < -1; row skipped */
 #define LORA_DEV_BAD_SEGMENT 0x2       /* a segment/perm entry fell outside its rows; skipped */
+#define LORA_DEV_TIMEOUT 0x4           /* an asynchronous copy did not land within 0.2 s; the
+                                          affected rows are left unwritten (never expected) */
 
 /* Largest r_slot (rank of one projection's slot) the kernels accept. */
 #define LORA_MAX_RANK 128

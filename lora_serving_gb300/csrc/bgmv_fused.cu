@@ -18,12 +18,18 @@
 // carries v to ~2^-17 relative (v itself is never rounded to one bf16), and
 // the last step is y[t][off_p + col] = bf16_rne(y + d).
 //
-// Latency (programmatic dependent launch): metadata and weights are read
+// Data movement: rows of A, x and the CTA's slice of B' arrive by bulk
+// asynchronous copies (cp.async.bulk, completion counted on mbarriers), so
+// a CTA issues a few hundred large copies instead of thousands of 16-byte
+// requests.  Waits on the mbarriers are bounded (0.2 s); a copy that does
+// not land sets LORA_DEV_TIMEOUT and the CTA leaves its rows unwritten,
+// while still taking part in every cluster barrier.
+//
+// Ordering (programmatic dependent launch): metadata and weights are read
 // before griddepcontrol.wait, so they stream in while the preceding kernel
 // on the stream is still running.  With LORA_APPLY_X_READY the shrink, the
 // cluster reduction and the delta are formed before the wait as well, and
-// only the read-modify-write of y follows it.  All waits are hardware waits
-// (cp.async groups, cluster barriers, grid dependency); no spin loops.
+// only the read-modify-write of y follows it.
 
 #include <cstdlib>
 
@@ -33,15 +39,17 @@ namespace lora {
 
 namespace {
 
-constexpr int kRB = 16;       // rows per unit (the mma M)
-constexpr int kKT = 128;      // K elements per pipeline stage
-constexpr int kPad = 8;       // bf16 padding per smem row: conflict-free ldmatrix
+constexpr int kRB = 16;            // rows per unit (the mma M)
+constexpr int kKT = 128;           // K elements per pipeline stage
+constexpr int kPad = 8;            // bf16 padding per smem row: conflict-free ldmatrix
 constexpr int kLds = kKT + kPad;
-constexpr int kMaxChunks = 64;     // output chunks (8 columns) per CTA and tile
+constexpr int kStages = 2;
+constexpr int kMaxChunks = 64;     // output chunks (8 columns) per expand tile
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kChunksPerWarp = kMaxChunks / kWarps;
 constexpr int kPermStage = 4096;   // decode positions staged in smem with the group table
+constexpr int kBSlack = 32;        // zeroed bf16 after B' so padded-K fragments stay finite
+constexpr unsigned long long kTimeoutNs = 200000000ull;
 
 struct FusedParams {
     ProjSet ps;
@@ -60,6 +68,7 @@ struct FusedParams {
     int kc;                   // K elements per cluster rank (multiple of 16)
     int n_parts;              // column parts per unit
     int cs;                   // cluster size
+    int nch_tile;             // chunks per expand tile (<= kMaxChunks)
     int r_pad;                // r_slot rounded up to 16 (expand mma K)
     int x_ready;              // x may be read before the grid dependency resolves
     int32_t* status;
@@ -70,14 +79,50 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid)
+__device__ __forceinline__ unsigned long long gtime()
 {
-    const int n = valid ? 16 : 0;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n) : "memory");
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect(uint64_t* bar, unsigned bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait on an mbarrier phase: false after kTimeoutNs without it.
+__device__ __noinline__ bool mbar_wait(uint64_t* bar, unsigned parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = gtime();
+    while (!mbar_try_wait(bar, parity))
+        if (gtime() - t0 > kTimeoutNs) return false;
+    return true;
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
@@ -238,20 +283,47 @@ __device__ __forceinline__ void chunk_proj(const ProjSet& ps, int ch, int& p, in
     col0 = ch << 3;
 }
 
-__global__ void __launch_bounds__(kThreads, 3)
+struct SmemLayout {
+    size_t a, x, vpart, vfull, b, perm, total;
+};
+
+__host__ __device__ inline size_t align128(size_t v) { return (v + 127) / 128 * 128; }
+
+// sA (the K stages) and sD (the delta tile, fp32) share the first region:
+// sD is written only after every stage has been consumed.
+__host__ __device__ inline SmemLayout smem_layout(int R, int r_slot, int nch_tile, int n_pos)
+{
+    SmemLayout L;
+    const size_t sa = sizeof(bf16_t) * kStages * R * kLds;
+    const size_t sd = sizeof(float) * kRB * nch_tile * 8;
+    L.a = 0;
+    L.x = align128(sa > sd ? sa : sd);
+    L.vpart = L.x + align128(sizeof(bf16_t) * kStages * kRB * kLds);
+    L.vfull = L.vpart + align128(sizeof(float) * kRB * R);
+    L.b = L.vfull + align128(sizeof(float) * kRB * R);
+    L.perm = L.b + align128(sizeof(bf16_t) * (nch_tile * 8 * r_slot + kBSlack));
+    L.total = L.perm + (n_pos <= kPermStage ? sizeof(int) * n_pos : 0);
+    return L;
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
 bgmv_fused_kernel(FusedParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     const int R = p.ps.n_proj * p.ps.r_slot;
     const int r_slot = p.ps.r_slot;
     const int r_pad = p.r_pad;
-    const int lds_b = r_pad + 8;                                     // B row stride (bf16)
-    bf16_t* sA = reinterpret_cast<bf16_t*>(smem);                    // [2][R][kLds]
-    bf16_t* sX = sA + 2 * R * kLds;                                  // [2][kRB][kLds]
-    float* vpart = reinterpret_cast<float*>(sX + 2 * kRB * kLds);    // [kRB][R]
-    float* vfull = vpart + kRB * R;                                  // [kRB][R]
-    bf16_t* sB = reinterpret_cast<bf16_t*>(vfull + kRB * R);         // [kMaxChunks*8][lds_b]
-    int* s_perm = reinterpret_cast<int*>(sB + kMaxChunks * 8 * lds_b);
+    const SmemLayout L = smem_layout(R, r_slot, p.nch_tile, p.n_pos);
+    bf16_t* sA = reinterpret_cast<bf16_t*>(smem + L.a);        // [kStages][R][kLds]
+    float* sD = reinterpret_cast<float*>(smem + L.a);          // [kRB][nch_tile*8], after the shrink
+    bf16_t* sX = reinterpret_cast<bf16_t*>(smem + L.x);        // [kStages][kRB][kLds]
+    float* vpart = reinterpret_cast<float*>(smem + L.vpart);   // [kRB][R]
+    float* vfull = reinterpret_cast<float*>(smem + L.vfull);   // [kRB][R]
+    bf16_t* sB = reinterpret_cast<bf16_t*>(smem + L.b);        // [nch_tile*8][r_slot] + slack
+    int* s_perm = reinterpret_cast<int*>(smem + L.perm);
+    __shared__ __align__(8) uint64_t s_barW[kStages];
+    __shared__ __align__(8) uint64_t s_barX[kStages];
+    __shared__ __align__(8) uint64_t s_barB;
     __shared__ int s_rows[kRB];
     __shared__ int s_cp[kMaxChunks];      // chunk -> projection
     __shared__ int s_ccol[kMaxChunks];    // chunk -> first column within its projection
@@ -302,7 +374,9 @@ bgmv_fused_kernel(FusedParams p)
     const int q_idx = part * p.cs + crank, q_n = p.n_parts * p.cs;
     const int ch_begin = static_cast<int>((static_cast<long long>(total_ch) * q_idx) / q_n);
     const int ch_end = static_cast<int>((static_cast<long long>(total_ch) * (q_idx + 1)) / q_n);
+    const int tile0_end = min(ch_end, ch_begin + p.nch_tile);
 
+    auto stage_klen = [&](int kt) { return min(kKT, k_end - (k_begin + kt * kKT)); };
     auto map_chunks = [&](int c0, int c1) {
         for (int ci = tid; ci < c1 - c0; ci += kThreads) {
             int pj, col0;
@@ -311,83 +385,102 @@ bgmv_fused_kernel(FusedParams p)
             s_ccol[ci] = col0;
         }
     };
-    auto load_A = [&](int kt, int buf) {
-        const int k0 = k_begin + kt * kKT;
-        for (int i = tid; i < R * (kKT / 8); i += kThreads) {
-            const int j = i / (kKT / 8), u = i - j * (kKT / 8);
-            const int k = k0 + u * 8;
+    // Bytes of B' for chunks [c0, c1): 8 columns x r_slot each.
+    auto b_bytes = [&](int c0, int c1) { return static_cast<unsigned>((c1 - c0) * 8 * r_slot * sizeof(bf16_t)); };
+    // One bulk copy per projection segment of chunks [c0, c1), issued by threads 0..n_proj-1.
+    auto copy_B = [&](int c0, int c1, uint64_t* bar) {
+        if (tid < p.ps.n_proj) {
+            int pc0 = 0;
+            for (int q = 0; q < tid; ++q) pc0 += p.ps.width[q] >> 3;
+            const int pc1 = pc0 + (p.ps.width[tid] >> 3);
+            const int s = max(c0, pc0), e = min(c1, pc1);
+            if (s < e) {
+                const bf16_t* src = p.ps.B[tid] + (static_cast<size_t>(slot) * p.ps.width[tid] + (s - pc0) * 8) * r_slot;
+                bulk_g2s(sB + static_cast<size_t>(s - c0) * 8 * r_slot, src, b_bytes(s, e), bar);
+            }
+        }
+    };
+    // Rows of A (weights) for stage kt into buffer buf: thread j copies rank row j.
+    auto copy_A = [&](int kt, int buf) {
+        const int k0 = k_begin + kt * kKT, klen = stage_klen(kt);
+        for (int j = tid; j < R; j += kThreads) {
             const int pj = j / r_slot, jj = j - pj * r_slot;
-            const bool ok = k < k_end;
-            const bf16_t* src = p.ps.A[pj] + (static_cast<size_t>(slot) * r_slot + jj) * p.h_in + (ok ? k : 0);
-            cp_async16(smem_u32(sA + (buf * R + j) * kLds + u * 8), src, ok);
+            const bf16_t* src = p.ps.A[pj] + (static_cast<size_t>(slot) * r_slot + jj) * p.h_in + k0;
+            bulk_g2s(sA + (buf * R + j) * kLds, src, klen * sizeof(bf16_t), &s_barW[buf]);
         }
     };
-    auto load_X = [&](int kt, int buf) {
-        const int k0 = k_begin + kt * kKT;
-        for (int i = tid; i < kRB * (kKT / 8); i += kThreads) {
-            const int t = i / (kKT / 8), u = i - t * (kKT / 8);
-            const int k = k0 + u * 8;
-            const bool ok = t < nrows && k < k_end;
-            const bf16_t* src = p.x + (ok ? static_cast<size_t>(s_rows[t]) * p.ld_x + k : 0);
-            cp_async16(smem_u32(sX + (buf * kRB + t) * kLds + u * 8), src, ok);
-        }
+    auto copy_X = [&](int kt, int buf) {
+        const int k0 = k_begin + kt * kKT, klen = stage_klen(kt);
+        if (tid < nrows)
+            bulk_g2s(sX + (buf * kRB + tid) * kLds, p.x + static_cast<size_t>(s_rows[tid]) * p.ld_x + k0,
+                     klen * sizeof(bf16_t), &s_barX[buf]);
     };
-    // B' rows (one per output column) for chunks [c0, c1): r_pad bf16 each,
-    // zero past r_slot; rows padded to lds_b for conflict-free ldmatrix.
-    // Needs s_cp / s_ccol of the same chunks (after a __syncthreads).
-    auto load_B = [&](int c0, int c1) {
-        const int upr = r_pad >> 3;
-        for (int i = tid; i < (c1 - c0) * 8 * upr; i += kThreads) {
-            const int row = i / upr, u = i - row * upr;
-            const int ci = row >> 3, e = row & 7;
-            const int pj = s_cp[ci];
-            const bool ok = u * 8 < r_slot;
-            const bf16_t* src = p.ps.B[pj] +
-                                (ok ? (static_cast<size_t>(slot) * p.ps.width[pj] + s_ccol[ci] + e) * r_slot + u * 8 : 0);
-            cp_async16(smem_u32(sB + row * lds_b + u * 8), src, ok);
+    // A partial last stage: zero the columns past klen (A rows and x rows).
+    auto zero_tail = [&](int kt, int buf) {
+        const int klen = stage_klen(kt);
+        if (klen == kKT) return;
+        const int w = (kKT - klen) / 8;   // 16-byte units past the copied part
+        for (int i = tid; i < (R + kRB) * w; i += kThreads) {
+            const int r = i / w, u = i - r * w;
+            bf16_t* row = r < R ? sA + (buf * R + r) * kLds : sX + (buf * kRB + (r - R)) * kLds;
+            *reinterpret_cast<uint4*>(row + klen + u * 8) = make_uint4(0, 0, 0, 0);
         }
     };
 
-    // ---- weights first: they do not depend on the preceding kernel ----
-    const int tile0_end = min(ch_end, ch_begin + kMaxChunks);
+    // ---- set-up: barriers, zero rows, chunk map ----
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&s_barW[s], 1);
+            mbar_init(&s_barX[s], 1);
+        }
+        mbar_init(&s_barB, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    for (int i = tid; i < kStages * kRB * (kLds / 8); i += kThreads) {   // x rows past nrows stay zero
+        const int row = i / (kLds / 8);
+        if ((row % kRB) >= nrows) reinterpret_cast<uint4*>(sX)[i] = make_uint4(0, 0, 0, 0);
+    }
+    for (int i = tid; i < kBSlack / 8; i += kThreads)
+        reinterpret_cast<uint4*>(sB + p.nch_tile * 8 * r_slot)[i] = make_uint4(0, 0, 0, 0);
     map_chunks(ch_begin, tile0_end);
-    if (n_kt > 0) load_A(0, 0);
-    cp_async_commit();
-    if (n_kt > 1) load_A(1, 1);
-    cp_async_commit();
-
+    for (int s = 0; s < kStages && s < n_kt; ++s) zero_tail(s, s);
     if (__syncthreads_or(bad_row)) {
         // A malformed permutation: flag it and leave this unit's rows alone.
-        // Every CTA of the cluster reads the same entries, so all return here
-        // (after their own copies into shared memory have landed).
-        cp_async_wait<0>();
+        // Every CTA of the cluster reads the same entries, so all return here.
         grid_dep_wait();
         if (tid == 0 && crank == 0 && part == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
         return;
     }
-    // s_cp / s_ccol are visible after the barrier above
-    if (ch_end > ch_begin) load_B(ch_begin, tile0_end);
-    cp_async_commit();
+
+    // ---- weights first: they do not depend on the preceding kernel ----
+    if (tid == 0) {
+        for (int s = 0; s < kStages && s < n_kt; ++s) {
+            const unsigned a = static_cast<unsigned>(R * stage_klen(s) * sizeof(bf16_t));
+            mbar_expect(&s_barW[s], a + (s == 0 && ch_end > ch_begin ? b_bytes(ch_begin, tile0_end) : 0u));
+            mbar_expect(&s_barX[s], static_cast<unsigned>(nrows * stage_klen(s) * sizeof(bf16_t)));
+        }
+        if (n_kt == 0 && ch_end > ch_begin) mbar_expect(&s_barW[0], b_bytes(ch_begin, tile0_end));
+    }
+    __syncthreads();
+    for (int s = 0; s < kStages && s < n_kt; ++s) copy_A(s, s);
+    if (ch_end > ch_begin) copy_B(ch_begin, tile0_end, &s_barW[0]);
 
     bool waited = false;
     if (!p.x_ready) {
         grid_dep_wait();
         waited = true;
     }
-    if (n_kt > 0) load_X(0, 0);
-    cp_async_commit();
-    if (n_kt > 1) load_X(1, 1);
-    cp_async_commit();
+    for (int s = 0; s < kStages && s < n_kt; ++s) copy_X(s, s);
 
     // ---- shrink: 16 rows x R ranks x this CTA's K range on tensor cores ----
     const int n_tiles = R / 8;                  // 8 ranks per mma tile; <= 16
+    bool failed = false;
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     for (int kt = 0; kt < n_kt; ++kt) {
-        // groups so far: {A0} {A1} {B0} {X0} {X1} then one per stage; waiting
-        // for all but the newest group leaves exactly stage kt resident
-        cp_async_wait<1>();
-        __syncthreads();
-        const int buf = kt & 1;
+        const int buf = kt % kStages;
+        const unsigned par = static_cast<unsigned>((kt / kStages) & 1);
+        if (!mbar_wait(&s_barW[buf], par)) failed = true;
+        if (!mbar_wait(&s_barX[buf], par)) failed = true;
         const bf16_t* xs = sX + buf * kRB * kLds;
         const bf16_t* as = sA + buf * R * kLds;
 #pragma unroll
@@ -406,13 +499,20 @@ bgmv_fused_kernel(FusedParams p)
                 }
             }
         }
-        __syncthreads();
-        if (kt + 2 < n_kt) {
-            load_A(kt + 2, buf);
-            load_X(kt + 2, buf);
+        __syncthreads();                        // every warp is done with this buffer
+        if (kt + kStages < n_kt) {              // refill it with stage kt + kStages
+            fence_proxy_async();
+            zero_tail(kt + kStages, buf);
+            if (tid == 0) {
+                mbar_expect(&s_barW[buf], static_cast<unsigned>(R * stage_klen(kt + kStages) * sizeof(bf16_t)));
+                mbar_expect(&s_barX[buf], static_cast<unsigned>(nrows * stage_klen(kt + kStages) * sizeof(bf16_t)));
+            }
+            __syncthreads();
+            copy_A(kt + kStages, buf);
+            copy_X(kt + kStages, buf);
         }
-        cp_async_commit();
     }
+    if (n_kt == 0 && ch_end > ch_begin && !mbar_wait(&s_barW[0], 0)) failed = true;
     {
         const int gr = lane >> 2, q2 = (lane & 3) * 2;
 #pragma unroll
@@ -427,12 +527,23 @@ bgmv_fused_kernel(FusedParams p)
             }
         }
     }
-    cp_async_wait<0>();
+    __shared__ int s_cta_fail, s_any_fail;
+    failed = __syncthreads_or(failed);
+    if (tid == 0) s_cta_fail = failed ? 1 : 0;
     __syncthreads();
 
     // ---- cluster reduction of the fp32 partials through DSMEM ----
     cluster_arrive();
     cluster_wait();
+    if (tid == 0) {   // a peer whose copies timed out has no valid partials
+        int any = 0;
+        for (int c = 0; c < p.cs; ++c) {
+            int f;
+            asm("ld.shared::cluster.b32 %0, [%1];\n" : "=r"(f) : "r"(map_rank(smem_u32(&s_cta_fail), c)));
+            any |= f;
+        }
+        s_any_fail = any;
+    }
     {
         const int n2 = kRB * R / 2;   // all 16 rows: rows past nrows sum to zero
         const uint32_t base = smem_u32(vpart);
@@ -454,104 +565,103 @@ bgmv_fused_kernel(FusedParams p)
     }
     cluster_arrive();   // this CTA no longer reads its peers' partials
     __syncthreads();
+    failed = s_any_fail != 0;
 
-    // ---- expand on tensor cores: d[16 rows][8 cols] per chunk ----
+    // ---- expand on tensor cores (16 rows x 8 columns per chunk), delta to sD ----
     const int gr = lane >> 2, q2 = (lane & 3) * 2;
-    for (int c0 = ch_begin; c0 < ch_end; c0 += kMaxChunks) {
-        const int c1 = min(ch_end, c0 + kMaxChunks);
+    unsigned b_phase = 0;
+    for (int c0 = ch_begin; c0 < ch_end; c0 += p.nch_tile) {
+        const int c1 = min(ch_end, c0 + p.nch_tile);
         const int nch = c1 - c0;
-        if (c0 != ch_begin) {
+        if (c0 != ch_begin) {                   // later tiles: fresh chunk map and B'
             __syncthreads();
             map_chunks(c0, c1);
+            fence_proxy_async();
+            if (tid == 0) mbar_expect(&s_barB, b_bytes(c0, c1));
             __syncthreads();
-            load_B(c0, c1);
-            cp_async_commit();
-            cp_async_wait<0>();
-            __syncthreads();
+            copy_B(c0, c1, &s_barB);
+            if (!mbar_wait(&s_barB, b_phase)) failed = true;
+            b_phase ^= 1u;
+            failed = __syncthreads_or(failed);
         }
-        float d[kChunksPerWarp][4];
         int cur_p = -1;
         uint32_t ahi[2][4], alo[2][4];   // v fragments of the current projection (r_pad <= 32)
-#pragma unroll
-        for (int w = 0; w < kChunksPerWarp; ++w) {
-            const int ci = warp + w * kWarps;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) d[w][e] = 0.f;
-            if (ci < nch) {
-                const int pj = s_cp[ci];
-                if (pj != cur_p) {
-                    cur_p = pj;
-                    const float* vp = vfull + pj * r_slot;
-#pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            // a0: (row g, k 2q..), a1: (row g+8, k 2q..), a2: (row g, k 2q+8..), a3: (row g+8, k 2q+8..)
-                            const int row = gr + (h & 1) * 8;
-                            const int k = kk * 16 + q2 + (h >> 1) * 8;
-                            float v0 = 0.f, v1 = 0.f;
-                            if (k < r_slot) {
-                                v0 = vp[row * R + k];
-                                v1 = vp[row * R + k + 1];
-                            }
-                            split_hi_lo(v0, v1, ahi[kk][h], alo[kk][h]);
-                        }
-                    }
-                }
-                const bf16_t* bc = sB + ci * 8 * lds_b;
+        for (int ci = warp; ci < nch; ci += kWarps) {
+            const int pj = s_cp[ci];
+            if (pj != cur_p) {
+                cur_p = pj;
+                const float* vp = vfull + pj * r_slot;
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) {
-                    if (kk * 16 < r_pad) {
-                        uint32_t b0, b1;
-                        const int l = lane & 15;
-                        ldmatrix_x2(smem_u32(bc + (l & 7) * lds_b + kk * 16 + (l >> 3) * 8), b0, b1);
-                        mma_bf16_16816(d[w], ahi[kk][0], ahi[kk][1], ahi[kk][2], ahi[kk][3], b0, b1);
-                        mma_bf16_16816(d[w], alo[kk][0], alo[kk][1], alo[kk][2], alo[kk][3], b0, b1);
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        // a0: (row g, k 2q..), a1: (row g+8, k 2q..), a2: (row g, k 2q+8..), a3: (row g+8, k 2q+8..)
+                        const int row = gr + (h & 1) * 8;
+                        const int k = kk * 16 + q2 + (h >> 1) * 8;
+                        float v0 = 0.f, v1 = 0.f;
+                        if (k < r_slot) {
+                            v0 = vp[row * R + k];
+                            v1 = vp[row * R + k + 1];
+                        }
+                        split_hi_lo(v0, v1, ahi[kk][h], alo[kk][h]);
                     }
                 }
             }
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            const bf16_t* bc = sB + ci * 8 * r_slot;
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                if (kk * 16 < r_pad) {
+                    uint32_t b0, b1;
+                    const int l = lane & 15;
+                    ldmatrix_x2(smem_u32(bc + (l & 7) * r_slot + kk * 16 + (l >> 3) * 8), b0, b1);
+                    mma_bf16_16816(d, ahi[kk][0], ahi[kk][1], ahi[kk][2], ahi[kk][3], b0, b1);
+                    mma_bf16_16816(d, alo[kk][0], alo[kk][1], alo[kk][2], alo[kk][3], b0, b1);
+                }
+            }
+            // d: (row g, cols 2q, 2q+1) and (row g+8, same cols) of chunk ci
+            const int ld_d = nch * 8;
+            *reinterpret_cast<float2*>(sD + gr * ld_d + ci * 8 + q2) = make_float2(d[0], d[1]);
+            *reinterpret_cast<float2*>(sD + (gr + 8) * ld_d + ci * 8 + q2) = make_float2(d[2], d[3]);
         }
+        __syncthreads();
         if (!waited) {
             grid_dep_wait();   // y may be the preceding kernel's output
             waited = true;
         }
-        // d[w]: (row g, cols 2q, 2q+1) and (row g+8, same cols) of chunk ci
-        uint32_t yo[kChunksPerWarp][2];
+        // ---- read-modify-write of y: 16-byte pieces, coalesced along each row ----
+        if (!failed) {
+            constexpr int kPairs = kRB * kMaxChunks / kThreads;
+            uint4 yo[kPairs];
 #pragma unroll
-        for (int w = 0; w < kChunksPerWarp; ++w) {
-            const int ci = warp + w * kWarps;
-            if (ci < nch) {
-                const int pj = s_cp[ci];
-                const int col = p.ps.out_off[pj] + s_ccol[ci] + q2;
-                if (gr < nrows) yo[w][0] = *reinterpret_cast<const uint32_t*>(p.y + static_cast<size_t>(s_rows[gr]) * p.ld_y + col);
-                if (gr + 8 < nrows) yo[w][1] = *reinterpret_cast<const uint32_t*>(p.y + static_cast<size_t>(s_rows[gr + 8]) * p.ld_y + col);
+            for (int q = 0; q < kPairs; ++q) {
+                const int i = tid + q * kThreads;
+                if (i < nrows * nch) {
+                    const int t = i / nch, ci = i - t * nch;
+                    yo[q] = *reinterpret_cast<const uint4*>(p.y + static_cast<size_t>(s_rows[t]) * p.ld_y +
+                                                            p.ps.out_off[s_cp[ci]] + s_ccol[ci]);
+                }
             }
-        }
 #pragma unroll
-        for (int w = 0; w < kChunksPerWarp; ++w) {
-            const int ci = warp + w * kWarps;
-            if (ci < nch) {
-                const int pj = s_cp[ci];
-                const int col = p.ps.out_off[pj] + s_ccol[ci] + q2;
-                if (gr < nrows)
-                    *reinterpret_cast<uint32_t*>(p.y + static_cast<size_t>(s_rows[gr]) * p.ld_y + col) =
-                        pack_bf16x2(bf16_lo(yo[w][0]) + d[w][0], bf16_hi(yo[w][0]) + d[w][1]);
-                if (gr + 8 < nrows)
-                    *reinterpret_cast<uint32_t*>(p.y + static_cast<size_t>(s_rows[gr + 8]) * p.ld_y + col) =
-                        pack_bf16x2(bf16_lo(yo[w][1]) + d[w][2], bf16_hi(yo[w][1]) + d[w][3]);
+            for (int q = 0; q < kPairs; ++q) {
+                const int i = tid + q * kThreads;
+                if (i < nrows * nch) {
+                    const int t = i / nch, ci = i - t * nch;
+                    const float4* dp = reinterpret_cast<const float4*>(sD + t * nch * 8 + ci * 8);
+                    const float4 d0 = dp[0], d1 = dp[1];
+                    const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+                    *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(s_rows[t]) * p.ld_y +
+                                              p.ps.out_off[s_cp[ci]] + s_ccol[ci]) = add_round8(yo[q], dd);
+                }
             }
         }
     }
     if (!waited) grid_dep_wait();
-    if (bad_group && crank == 0 && part == 0 && tid == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
+    if (tid == 0) {
+        if (bad_group && crank == 0 && part == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
+        if (failed) flag(p.status, LORA_DEV_TIMEOUT);
+    }
     cluster_wait();     // peers are done reading this CTA's partials
-}
-
-size_t fused_smem_bytes(int R, int r_pad, int n_pos)
-{
-    const int perm = n_pos <= kPermStage ? n_pos : 0;
-    return sizeof(bf16_t) * (2 * R * kLds + 2 * kRB * kLds) + sizeof(float) * 2 * kRB * R +
-           sizeof(bf16_t) * kMaxChunks * 8 * (r_pad + 8) + sizeof(int) * perm;
 }
 
 int env_int(const char* name, int dflt)
@@ -574,8 +684,6 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
 {
     if (n_pos <= 0 || n_groups <= 0) return cudaSuccess;
     const int R = ps.n_proj * ps.r_slot;
-    const int r_pad = (ps.r_slot + 15) / 16 * 16;
-    const size_t smem = fused_smem_bytes(R, r_pad, n_pos);
     static int configured_device = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -597,6 +705,10 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     // Column parts per unit (more clusters, each recomputing the shrink);
     // one part measured best on the decode shapes here.
     const int parts = env_int("LORA_FUSED_PARTS", 1);
+    int total_ch = 0;
+    for (int q = 0; q < ps.n_proj; ++q) total_ch += ps.width[q] / 8;
+    const int per_cta = (total_ch + cs * parts - 1) / (cs * parts);
+    const int nch_tile = min(kMaxChunks, max(1, per_cta));
 
     FusedParams p{};
     p.ps = ps;
@@ -615,14 +727,15 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     p.kc = ((h_in + cs - 1) / cs + 15) / 16 * 16;
     p.n_parts = parts;
     p.cs = cs;
-    p.r_pad = r_pad;
+    p.nch_tile = nch_tile;
+    p.r_pad = (ps.r_slot + 15) / 16 * 16;
     p.x_ready = (flags & LORA_APPLY_X_READY) ? 1 : 0;
     p.status = status;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(max_units * parts * cs));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = smem_layout(R, ps.r_slot, nch_tile, n_pos).total;
     cfg.stream = stream;
     cudaLaunchAttribute attrs[2];
     int na = 0;

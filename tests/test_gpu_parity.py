@@ -356,6 +356,8 @@ def test_host_rejects_before_enqueue():
     (28672, (8192,), 16, 40, 4),                    # long K: the cluster's K chunks pipeline in stages
     (3072, (3072,), 8, 100, 2),                     # ~50 rows per adapter: several 16-row units each
     (256, (256, 64, 64), 16, 7, 3),                 # fewer rows than one unit
+    (8192, (28672, 28672), 16, 20, 4),              # wide outputs: several expand tiles per CTA
+    (1024, (1024,), 24, 20, 4),                     # slot rank not a multiple of 16
 ])
 def test_apply_decode_fused_shapes(h_in, widths, rank, T, n_slots):
     rng = np.random.default_rng(h_in + T)
