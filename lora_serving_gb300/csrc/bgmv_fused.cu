@@ -124,6 +124,15 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid)
+{
+    const int n = valid ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
@@ -174,11 +183,11 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, uint32_t a0, uint32_t a
 // v (two fp32 values) -> packed bf16 hi pair and bf16 lo pair (v ~= hi + lo).
 __device__ __forceinline__ void split_hi_lo(float a, float b, uint32_t& hi, uint32_t& lo)
 {
-    const __nv_bfloat16 ah = __float2bfloat16_rn(a), bh = __float2bfloat16_rn(b);
-    const __nv_bfloat16 al = __float2bfloat16_rn(a - __bfloat162float(ah));
-    const __nv_bfloat16 bl = __float2bfloat16_rn(b - __bfloat162float(bh));
-    hi = static_cast<uint32_t>(__bfloat16_as_ushort(ah)) | (static_cast<uint32_t>(__bfloat16_as_ushort(bh)) << 16);
-    lo = static_cast<uint32_t>(__bfloat16_as_ushort(al)) | (static_cast<uint32_t>(__bfloat16_as_ushort(bl)) << 16);
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);   // .x = a (low half)
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 // Units of a group: ceil(len / 16), or 0 (and bad) when its bounds fall
@@ -321,8 +330,6 @@ bgmv_fused_kernel(FusedParams p)
     float* vfull = reinterpret_cast<float*>(smem + L.vfull);   // [kRB][R]
     bf16_t* sB = reinterpret_cast<bf16_t*>(smem + L.b);        // [nch_tile*8][r_slot] + slack
     int* s_perm = reinterpret_cast<int*>(smem + L.perm);
-    __shared__ __align__(8) uint64_t s_barW[kStages];
-    __shared__ __align__(8) uint64_t s_barX[kStages];
     __shared__ __align__(8) uint64_t s_barB;
     __shared__ int s_rows[kRB];
     __shared__ int s_cp[kMaxChunks];      // chunk -> projection
@@ -376,7 +383,6 @@ bgmv_fused_kernel(FusedParams p)
     const int ch_end = static_cast<int>((static_cast<long long>(total_ch) * (q_idx + 1)) / q_n);
     const int tile0_end = min(ch_end, ch_begin + p.nch_tile);
 
-    auto stage_klen = [&](int kt) { return min(kKT, k_end - (k_begin + kt * kKT)); };
     auto map_chunks = [&](int c0, int c1) {
         for (int ci = tid; ci < c1 - c0; ci += kThreads) {
             int pj, col0;
@@ -400,50 +406,39 @@ bgmv_fused_kernel(FusedParams p)
             }
         }
     };
-    // Rows of A (weights) for stage kt into buffer buf: thread j copies rank row j.
+    // A rows (weights) for stage kt into buffer buf, 16 bytes per cp.async;
+    // columns past k_end are zero-filled.
     auto copy_A = [&](int kt, int buf) {
-        const int k0 = k_begin + kt * kKT, klen = stage_klen(kt);
-        for (int j = tid; j < R; j += kThreads) {
+        const int k0 = k_begin + kt * kKT;
+        for (int i = tid; i < R * (kKT / 8); i += kThreads) {
+            const int j = i / (kKT / 8), u = i - j * (kKT / 8);
+            const int k = k0 + u * 8;
             const int pj = j / r_slot, jj = j - pj * r_slot;
-            const bf16_t* src = p.ps.A[pj] + (static_cast<size_t>(slot) * r_slot + jj) * p.h_in + k0;
-            bulk_g2s(sA + (buf * R + j) * kLds, src, klen * sizeof(bf16_t), &s_barW[buf]);
+            const bool ok = k < k_end;
+            const bf16_t* src = p.ps.A[pj] + (static_cast<size_t>(slot) * r_slot + jj) * p.h_in + (ok ? k : 0);
+            cp_async16(smem_u32(sA + (buf * R + j) * kLds + u * 8), src, ok);
         }
     };
+    // x rows (gathered through perm); rows past nrows and columns past k_end are zero-filled.
     auto copy_X = [&](int kt, int buf) {
-        const int k0 = k_begin + kt * kKT, klen = stage_klen(kt);
-        if (tid < nrows)
-            bulk_g2s(sX + (buf * kRB + tid) * kLds, p.x + static_cast<size_t>(s_rows[tid]) * p.ld_x + k0,
-                     klen * sizeof(bf16_t), &s_barX[buf]);
-    };
-    // A partial last stage: zero the columns past klen (A rows and x rows).
-    auto zero_tail = [&](int kt, int buf) {
-        const int klen = stage_klen(kt);
-        if (klen == kKT) return;
-        const int w = (kKT - klen) / 8;   // 16-byte units past the copied part
-        for (int i = tid; i < (R + kRB) * w; i += kThreads) {
-            const int r = i / w, u = i - r * w;
-            bf16_t* row = r < R ? sA + (buf * R + r) * kLds : sX + (buf * kRB + (r - R)) * kLds;
-            *reinterpret_cast<uint4*>(row + klen + u * 8) = make_uint4(0, 0, 0, 0);
+        const int k0 = k_begin + kt * kKT;
+        for (int i = tid; i < kRB * (kKT / 8); i += kThreads) {
+            const int t = i / (kKT / 8), u = i - t * (kKT / 8);
+            const int k = k0 + u * 8;
+            const bool ok = t < nrows && k < k_end;
+            const bf16_t* src = p.x + (ok ? static_cast<size_t>(s_rows[t]) * p.ld_x + k : 0);
+            cp_async16(smem_u32(sX + (buf * kRB + t) * kLds + u * 8), src, ok);
         }
     };
 
-    // ---- set-up: barriers, zero rows, chunk map ----
+    // ---- set-up: barrier, zero slack, chunk map ----
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&s_barW[s], 1);
-            mbar_init(&s_barX[s], 1);
-        }
         mbar_init(&s_barB, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    }
-    for (int i = tid; i < kStages * kRB * (kLds / 8); i += kThreads) {   // x rows past nrows stay zero
-        const int row = i / (kLds / 8);
-        if ((row % kRB) >= nrows) reinterpret_cast<uint4*>(sX)[i] = make_uint4(0, 0, 0, 0);
     }
     for (int i = tid; i < kBSlack / 8; i += kThreads)
         reinterpret_cast<uint4*>(sB + p.nch_tile * 8 * r_slot)[i] = make_uint4(0, 0, 0, 0);
     map_chunks(ch_begin, tile0_end);
-    for (int s = 0; s < kStages && s < n_kt; ++s) zero_tail(s, s);
     if (__syncthreads_or(bad_row)) {
         // A malformed permutation: flag it and leave this unit's rows alone.
         // Every CTA of the cluster reads the same entries, so all return here.
@@ -453,34 +448,36 @@ bgmv_fused_kernel(FusedParams p)
     }
 
     // ---- weights first: they do not depend on the preceding kernel ----
-    if (tid == 0) {
-        for (int s = 0; s < kStages && s < n_kt; ++s) {
-            const unsigned a = static_cast<unsigned>(R * stage_klen(s) * sizeof(bf16_t));
-            mbar_expect(&s_barW[s], a + (s == 0 && ch_end > ch_begin ? b_bytes(ch_begin, tile0_end) : 0u));
-            mbar_expect(&s_barX[s], static_cast<unsigned>(nrows * stage_klen(s) * sizeof(bf16_t)));
-        }
-        if (n_kt == 0 && ch_end > ch_begin) mbar_expect(&s_barW[0], b_bytes(ch_begin, tile0_end));
+    if (ch_end > ch_begin) {
+        if (tid == 0) mbar_expect(&s_barB, b_bytes(ch_begin, tile0_end));
+        __syncthreads();
+        copy_B(ch_begin, tile0_end, &s_barB);
     }
-    __syncthreads();
-    for (int s = 0; s < kStages && s < n_kt; ++s) copy_A(s, s);
-    if (ch_end > ch_begin) copy_B(ch_begin, tile0_end, &s_barW[0]);
+    if (n_kt > 0) copy_A(0, 0);
+    cp_async_commit();
+    if (n_kt > 1) copy_A(1, 1);
+    cp_async_commit();
 
     bool waited = false;
     if (!p.x_ready) {
         grid_dep_wait();
         waited = true;
     }
-    for (int s = 0; s < kStages && s < n_kt; ++s) copy_X(s, s);
+    if (n_kt > 0) copy_X(0, 0);
+    cp_async_commit();
+    if (n_kt > 1) copy_X(1, 1);
+    cp_async_commit();
 
     // ---- shrink: 16 rows x R ranks x this CTA's K range on tensor cores ----
     const int n_tiles = R / 8;                  // 8 ranks per mma tile; <= 16
     bool failed = false;
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     for (int kt = 0; kt < n_kt; ++kt) {
+        // groups so far: {A0} {A1} {X0} {X1} then one per stage; waiting
+        // for all but the newest group leaves exactly stage kt resident
+        cp_async_wait<1>();
+        __syncthreads();
         const int buf = kt % kStages;
-        const unsigned par = static_cast<unsigned>((kt / kStages) & 1);
-        if (!mbar_wait(&s_barW[buf], par)) failed = true;
-        if (!mbar_wait(&s_barX[buf], par)) failed = true;
         const bf16_t* xs = sX + buf * kRB * kLds;
         const bf16_t* as = sA + buf * R * kLds;
 #pragma unroll
@@ -501,18 +498,12 @@ bgmv_fused_kernel(FusedParams p)
         }
         __syncthreads();                        // every warp is done with this buffer
         if (kt + kStages < n_kt) {              // refill it with stage kt + kStages
-            fence_proxy_async();
-            zero_tail(kt + kStages, buf);
-            if (tid == 0) {
-                mbar_expect(&s_barW[buf], static_cast<unsigned>(R * stage_klen(kt + kStages) * sizeof(bf16_t)));
-                mbar_expect(&s_barX[buf], static_cast<unsigned>(nrows * stage_klen(kt + kStages) * sizeof(bf16_t)));
-            }
-            __syncthreads();
             copy_A(kt + kStages, buf);
             copy_X(kt + kStages, buf);
         }
+        cp_async_commit();
     }
-    if (n_kt == 0 && ch_end > ch_begin && !mbar_wait(&s_barW[0], 0)) failed = true;
+    cp_async_wait<0>();
     {
         const int gr = lane >> 2, q2 = (lane & 3) * 2;
 #pragma unroll
@@ -566,10 +557,12 @@ bgmv_fused_kernel(FusedParams p)
     cluster_arrive();   // this CTA no longer reads its peers' partials
     __syncthreads();
     failed = s_any_fail != 0;
+    if (ch_end > ch_begin && !mbar_wait(&s_barB, 0)) failed = true;   // B' of the first tile
+    failed = __syncthreads_or(failed);
 
     // ---- expand on tensor cores (16 rows x 8 columns per chunk), delta to sD ----
     const int gr = lane >> 2, q2 = (lane & 3) * 2;
-    unsigned b_phase = 0;
+    unsigned b_phase = 1;
     for (int c0 = ch_begin; c0 < ch_end; c0 += p.nch_tile) {
         const int c1 = min(ch_end, c0 + p.nch_tile);
         const int nch = c1 - c0;
