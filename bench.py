@@ -290,7 +290,8 @@ def run_ours(args, rank, local, ws):
     # output of the kernel just before it (as the base GEMM's output is in a
     # model layer) and x as produced earlier (LORA_APPLY_X_READY).  The two
     # other orderings are timed too and reported beside the headline.
-    variants = {"x_ready": abi.LORA_APPLY_X_READY, "default": 0, "no_pdl": abi.LORA_APPLY_NO_PDL}
+    variants = {"x_ready": abi.LORA_APPLY_X_READY, "default": 0, "no_pdl": abi.LORA_APPLY_NO_PDL,
+                "independent": abi.LORA_APPLY_X_READY | abi.LORA_APPLY_Y_READY}
 
     def step(s, flags):
         for inst in sets[s]:
@@ -333,7 +334,7 @@ def run_ours(args, rank, local, ws):
         return e0.elapsed_time(e1)
 
     other = {}
-    for name_v in ("default", "no_pdl"):
+    for name_v in ("default", "no_pdl", "independent"):
         n_v = max(10, args.steps // 4)
         other[name_v] = round(timed(graphs[name_v], n_v, args.warmup) / n_v, 5)
 

@@ -187,9 +187,14 @@ typedef struct {
  *   LORA_APPLY_X_READY: x is not written by the kernel just before the call
  *     (in a model layer x comes from earlier than the base GEMM that writes
  *     y), so the shrink may read x before that kernel completes.
+ *   LORA_APPLY_Y_READY: y is neither read nor written by the kernel just
+ *     before the call (e.g. the delta goes to a buffer of its own), so y may
+ *     be updated before that kernel completes; with X_READY as well, calls
+ *     that share no buffers overlap fully.
  *   LORA_APPLY_NO_PDL: plain stream ordering, nothing starts early. */
 #define LORA_APPLY_X_READY 0x1u
 #define LORA_APPLY_NO_PDL 0x2u
+#define LORA_APPLY_Y_READY 0x4u
 
 /*
  * Fused LoRA delta for n_proj projections that share the input x (q/k/v or

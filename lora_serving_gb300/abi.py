@@ -23,6 +23,8 @@ LORA_DEV_SLOT_OUT_OF_RANGE = 0x1
 LORA_DEV_BAD_SEGMENT = 0x2
 LORA_APPLY_X_READY = 0x1
 LORA_APPLY_NO_PDL = 0x2
+LORA_APPLY_Y_READY = 0x4
+LORA_DEV_TIMEOUT = 0x4
 
 STATUS = {
     0: "LORA_OK", 1: "LORA_ERR_INVALID_ARG", 2: "LORA_ERR_SHAPE",

@@ -71,6 +71,7 @@ struct FusedParams {
     int nch_tile;             // chunks per expand tile (<= kMaxChunks)
     int r_pad;                // r_slot rounded up to 16 (expand mma K)
     int x_ready;              // x may be read before the grid dependency resolves
+    int y_ready;              // y may be updated before it resolves
     int32_t* status;
 };
 
@@ -618,7 +619,7 @@ bgmv_fused_kernel(FusedParams p)
             *reinterpret_cast<float2*>(sD + (gr + 8) * ld_d + ci * 8 + q2) = make_float2(d[2], d[3]);
         }
         __syncthreads();
-        if (!waited) {
+        if (!waited && !p.y_ready) {
             grid_dep_wait();   // y may be the preceding kernel's output
             waited = true;
         }
@@ -649,7 +650,9 @@ bgmv_fused_kernel(FusedParams p)
             }
         }
     }
-    if (!waited) grid_dep_wait();
+    // With LORA_APPLY_Y_READY only CTA 0 (and CTAs with a flag to write) wait
+    // here: enough to keep this grid from completing before the preceding one.
+    if (!waited && (blockIdx.x == 0 || bad_group || failed)) grid_dep_wait();
     if (tid == 0) {
         if (bad_group && crank == 0 && part == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
         if (failed) flag(p.status, LORA_DEV_TIMEOUT);
@@ -688,9 +691,11 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    // Cluster size: split K as far as 16 CTAs while each keeps >= one stage.
+    // Cluster size: split K over up to 8 CTAs while each keeps >= one stage
+    // (8 measured faster than 16 on the 3B decode shapes: smaller grids let
+    // more consecutive calls be resident at once under PDL).
     int cs = 1;
-    while (cs < 16 && h_in / (cs * 2) >= kKT) cs *= 2;
+    while (cs < 8 && h_in / (cs * 2) >= kKT) cs *= 2;
     cs = env_int("LORA_FUSED_CS", cs);
     // Units of <= 16 rows: at most ceil(longest group / 16) per group.
     int max_units = n_groups + n_pos / kRB;
@@ -723,6 +728,7 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     p.nch_tile = nch_tile;
     p.r_pad = (ps.r_slot + 15) / 16 * 16;
     p.x_ready = (flags & LORA_APPLY_X_READY) ? 1 : 0;
+    p.y_ready = (flags & LORA_APPLY_Y_READY) ? 1 : 0;
     p.status = status;
 
     cudaLaunchConfig_t cfg = {};

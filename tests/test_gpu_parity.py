@@ -298,7 +298,8 @@ def test_bad_row_id_flagged_in_per_token_kernels():
 
 
 @pytest.mark.parametrize("flags", [0, abi.LORA_APPLY_X_READY, abi.LORA_APPLY_NO_PDL,
-                                   abi.LORA_APPLY_X_READY | abi.LORA_APPLY_NO_PDL])
+                                   abi.LORA_APPLY_X_READY | abi.LORA_APPLY_NO_PDL,
+                                   abi.LORA_APPLY_X_READY | abi.LORA_APPLY_Y_READY])
 def test_apply_orderings_give_identical_bits(flags):
     """The launch-ordering flags change when work may start, never the result;
     a chain of calls with PDL matches the same chain with plain ordering."""
