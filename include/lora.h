@@ -214,6 +214,34 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
 
 size_t lora_apply_workspace_bytes(int n_rows, int n_proj, int r_slot);
 
+/* Size of the scratch array built into the library for lora_apply_noalloc. */
+#define LORA_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * lora_apply for callers that cannot allocate device memory at call time
+ * (an engine that has reserved nearly all free HBM for its KV cache, a
+ * plug-in that may only use its host's memory pool, a loop that cannot
+ * afford cudaMalloc's device synchronisation).  The source pages have no
+ * counterpart to this entry point; it is a deployment convenience.
+ * Same arguments and results as lora_apply, minus the workspace: the fp32
+ * intermediate lives in a LORA_NOALLOC_SCRATCH_BYTES array compiled into
+ * the library, which every GPU that loads the library holds until exit.
+ *   - Returns LORA_ERR_WORKSPACE, before anything is enqueued, when
+ *     lora_apply_workspace_bytes(meta->n_rows, n_proj, r_slot) exceeds
+ *     LORA_NOALLOC_SCRATCH_BYTES (16 MiB: e.g. 32768 rows x 128 ranks).
+ *   - The first call on a device looks up the array's device address on
+ *     the current device (cudaGetSymbolAddress); make that first call
+ *     before any stream capture.  LORA_ERR_CUDA if the lookup fails.
+ *   - No allocation of any kind happens on this path.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (nothing in it needs to start at zero); calls that may overlap on the
+ *     GPU, e.g. on two streams, race on it.
+ */
+lora_status_t lora_apply_noalloc(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_x, int h_in,
+                                 const lora_proj_t* projs, int n_proj, int r_slot, int n_slots,
+                                 const lora_meta_t* meta, uint32_t flags, int32_t* dev_status,
+                                 lora_stream_t stream);
+
 /* ------------------------------------------------------------------ *
  *  Host helpers (host pointers, synchronous)
  * ------------------------------------------------------------------ */

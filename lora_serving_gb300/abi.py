@@ -37,8 +37,9 @@ EXPORTS = (
     "lora_bgmv_shrink", "lora_bgmv_expand", "lora_sgmv_shrink", "lora_sgmv_expand",
     "lora_apply", "lora_apply_workspace_bytes", "lora_build_metadata",
     "lora_prepare_adapter", "lora_slot_rank", "lora_read_device_status", "lora_status_string",
-    "lora_kernel_launch_count",
+    "lora_kernel_launch_count", "lora_apply_noalloc",
 )
+LORA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class LoraError(RuntimeError):
@@ -80,6 +81,7 @@ def load(path: str | None = None):
         "lora_sgmv_shrink": [P, i32, P, i32, P, P, P, i32, P, i32, i32, i32, i32, i32, i32, P, P],
         "lora_sgmv_expand": [P, i32, i32, i32, P, i32, P, P, P, i32, P, i32, i32, i32, i32, i32, P, P],
         "lora_apply": [P, i32, P, i32, i32, P, i32, i32, i32, P, P, sz, ctypes.c_uint32, P, P],
+        "lora_apply_noalloc": [P, i32, P, i32, i32, P, i32, i32, i32, P, ctypes.c_uint32, P, P],
         "lora_apply_workspace_bytes": [i32, i32, i32],
         "lora_build_metadata": [P, i32, i32, i32, P, P, P, P, P, P, P, P, P],
         "lora_prepare_adapter": [P, P, i32, i32, i32, ctypes.c_double, i32, i32, P, P],
@@ -179,6 +181,14 @@ def lora_apply(y, x, h_in, projs, r_slot, n_slots, meta, workspace, *, flags=0, 
     _check("lora_apply", load().lora_apply(
         _p(y), _ld(y), _p(x), _ld(x), h_in, ctypes.addressof(projs), len(projs), r_slot, n_slots,
         ctypes.addressof(meta), _p(workspace), ws_bytes, int(flags), _p(dev_status), _stream(stream)))
+
+
+def lora_apply_noalloc(y, x, h_in, projs, r_slot, n_slots, meta, *, flags=0, dev_status=None, stream=None):
+    """lora_apply with the library's built-in scratch instead of a workspace
+    (for callers that cannot allocate device memory when they call in)."""
+    _check("lora_apply_noalloc", load().lora_apply_noalloc(
+        _p(y), _ld(y), _p(x), _ld(x), h_in, ctypes.addressof(projs), len(projs), r_slot, n_slots,
+        ctypes.addressof(meta), int(flags), _p(dev_status), _stream(stream)))
 
 
 def lora_apply_workspace_bytes(n_rows, n_proj, r_slot) -> int:
