@@ -31,11 +31,51 @@ _CHUNK = 1 << 24
 
 
 def _seed_of(*key) -> int:
-    return int(np.random.SeedSequence([abs(int(k)) for k in key]).generate_state(1, np.uint64)[0] >> 1)
+    """63-bit seed from a tuple of integers (sha256: the same on every machine)."""
+    data = b"".join(int(k).to_bytes(16, "little", signed=True) for k in key)
+    return int.from_bytes(hashlib.sha256(data).digest()[:8], "little") >> 1
 
 
 def _tag(s: str) -> int:
     return int.from_bytes(hashlib.sha256(s.encode()).digest()[:8], "little") >> 1
+
+
+class _Stream:
+    """splitmix64 (Steele, Lea & Flood, "Fast splittable pseudorandom number
+    generators", 2014) for the batch-structure draws, so lengths and ids are
+    the same on every machine and numpy version."""
+
+    _M = (1 << 64) - 1
+
+    def __init__(self, seed: int):
+        self.s = int(seed) & self._M
+
+    def u64(self) -> int:
+        self.s = (self.s + 0x9E3779B97F4A7C15) & self._M
+        z = self.s
+        z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & self._M
+        z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & self._M
+        return z ^ (z >> 31)
+
+    def random(self, n: int) -> np.ndarray:
+        return np.array([(self.u64() >> 11) * 2.0 ** -53 for _ in range(n)])
+
+    def integers(self, lo: int, hi: int, n: int) -> np.ndarray:
+        """Uniform in [lo, hi) (rejection-free multiply-shift; bias < 2^-32)."""
+        span = hi - lo
+        return np.array([lo + ((self.u64() >> 32) * span >> 32) for _ in range(n)], np.int64)
+
+    def choice_p(self, p: np.ndarray, n: int) -> np.ndarray:
+        cdf = np.cumsum(p)
+        cdf[-1] = 1.0
+        return np.searchsorted(cdf, self.random(n), side="right").astype(np.int64)
+
+    def permutation(self, a: np.ndarray) -> np.ndarray:
+        a = np.array(a, copy=True)
+        for i in range(a.size - 1, 0, -1):   # Fisher-Yates
+            j = int(self.integers(0, i + 1, 1)[0])
+            a[i], a[j] = a[j], a[i]
+        return a
 
 
 def normal_bf16(shape, std: float, seed: int, tag: str) -> np.ndarray:
@@ -152,7 +192,7 @@ def llama3b_decode(n_tokens: int = 64) -> Workload:
     3072; 8 adapter slots, all rank 16, alpha 32; 64 decode tokens, each
     base-only with p = 0.1, else an adapter uniform over the 8; seed 1."""
     seed = 1
-    g = np.random.default_rng(_seed_of(seed, _tag("ids")))
+    g = _Stream(_seed_of(seed, _tag("ids")))
     base = g.random(n_tokens) < 0.1
     ids = np.where(base, -1, g.integers(0, 8, n_tokens)).astype(np.int32)
     groups = [Group("qkv", 3072, [("q", 3072), ("k", 1024), ("v", 1024)]),
@@ -168,8 +208,8 @@ def mistral7b_prefill(n_seqs: int = 32) -> Workload:
     all; 32 sequences of lengths uniform in [64, 2048], each on an adapter
     uniform over the 16; contiguous segments; no base-only rows; seed 2."""
     seed = 2
-    g = np.random.default_rng(_seed_of(seed, _tag("ids")))
-    ranks = g.choice(np.array([8, 16, 32, 64]), 16)
+    g = _Stream(_seed_of(seed, _tag("ids")))
+    ranks = np.array([8, 16, 32, 64])[g.integers(0, 4, 16)]
     lens = g.integers(64, 2049, n_seqs)
     seq_ids = g.integers(0, 16, n_seqs)
     ids = np.repeat(seq_ids, lens).astype(np.int32)
@@ -189,13 +229,13 @@ def mixed(n_decode: int = 256, n_prefill_segs: int = 8) -> Workload:
     p = 0.2, else its adapter follows Zipf(s = 1.1) over popularity ranks
     1..64 (id = rank - 1); seed 3."""
     seed = 3
-    g = np.random.default_rng(_seed_of(seed, _tag("ids")))
+    g = _Stream(_seed_of(seed, _tag("ids")))
     pz = 1.0 / np.arange(1, 65) ** 1.1
     pz /= pz.sum()
 
     def draw(n):
         base = g.random(n) < 0.2
-        return np.where(base, -1, g.choice(64, n, p=pz)).astype(np.int32)
+        return np.where(base, -1, g.choice_p(pz, n)).astype(np.int32)
 
     lens = g.integers(128, 1025, n_prefill_segs)
     pre = np.repeat(draw(n_prefill_segs), lens)
@@ -214,7 +254,7 @@ def stress70b(n_tokens: int = 512) -> Workload:
     128 ids repeated 4 times (512 tokens cannot all be distinct over 128
     adapters: every adapter is touched, by 4 scattered tokens); seed 4."""
     seed = 4
-    g = np.random.default_rng(_seed_of(seed, _tag("ids")))
+    g = _Stream(_seed_of(seed, _tag("ids")))
     ids = g.permutation(np.repeat(np.arange(128), n_tokens // 128)).astype(np.int32)
     groups = [Group("gate_up", 8192, [("gate", 28672), ("up", 28672)]),
               Group("down", 28672, [("down", 8192)])]
