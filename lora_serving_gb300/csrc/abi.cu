@@ -25,6 +25,9 @@ using lora::RowMap;
 namespace {
 
 constexpr int kMaxHin = 65536;
+// Segments at least this long send a prefill batch to the tensor-core SGMV
+// kernels (128-row tiles); shorter ones stay on the CUDA-core kernels.
+constexpr int kTcMinSegment = 64;
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -170,7 +173,6 @@ lora_status_t lora_sgmv_shrink(float* v, int ld_v, const lora_bf16_t* x, int ld_
                                int n_pos, int n_rows, int max_seg_len, int h_in, int r_slot,
                                int n_slots, int32_t* dev_status, lora_stream_t stream)
 {
-    (void)max_seg_len;
     if (n_rows < 0 || n_slots <= 0 || r_slot <= 0) return LORA_ERR_INVALID_ARG;
     if (r_slot > LORA_MAX_RANK * LORA_MAX_PROJ) return LORA_ERR_RANK_EXCEEDS_SLOT;
     if (r_slot % 8 != 0) return LORA_ERR_ALIGNMENT;
@@ -180,6 +182,10 @@ lora_status_t lora_sgmv_shrink(float* v, int ld_v, const lora_bf16_t* x, int ld_
     LORA_TRY(check_store(A));
     LORA_TRY(check_v(v, ld_v, r_slot));
     ProjSet ps = single_proj(A, nullptr, 0, 0, r_slot);
+    if (!row_perm && max_seg_len >= kTcMinSegment && lora::sgmv_tc_supported(1, r_slot, h_in))
+        return cuda_status(lora::launch_sgmv_shrink_tc(v, ld_v, nullptr, nullptr, x, ld_x, h_in, ps, seg_starts,
+                                                       seg_slot, n_segs, n_pos, n_rows, n_slots, dev_status,
+                                                       reinterpret_cast<cudaStream_t>(stream)));
     RowMap m = seg_map(seg_starts, seg_slot, n_segs, row_perm, n_pos, n_rows, n_slots);
     return cuda_status(lora::launch_shrink_rowwise(v, ld_v, x, ld_x, h_in, ps, m, dev_status,
                                                    reinterpret_cast<cudaStream_t>(stream)));
@@ -205,10 +211,17 @@ lora_status_t lora_sgmv_expand(lora_bf16_t* y, int ld_y, int y_off, int width,
                                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Workspace layout: [bf16 hi/lo planes of v for the tensor-core SGMV route]
+// [fp32 v for the other routes], each part 256-byte aligned.
+static size_t plane_region_bytes(int n_rows, int n_proj, int r_slot)
+{
+    return (lora::sgmv_tc_plane_bytes(n_rows, n_proj, r_slot) + 255) / 256 * 256;
+}
+
 size_t lora_apply_workspace_bytes(int n_rows, int n_proj, int r_slot)
 {
     if (n_rows <= 0 || n_proj <= 0 || r_slot <= 0) return 0;
-    return static_cast<size_t>(n_rows) * n_proj * r_slot * sizeof(float);
+    return plane_region_bytes(n_rows, n_proj, r_slot) + static_cast<size_t>(n_rows) * n_proj * r_slot * sizeof(float);
 }
 
 lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_x, int h_in,
@@ -238,7 +251,9 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
     if (!workspace) return LORA_ERR_WORKSPACE;
     if (ws_bytes < lora_apply_workspace_bytes(T, n_proj, r_slot)) return LORA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LORA_ERR_ALIGNMENT;
-    float* v = static_cast<float*>(workspace);
+    bf16_t* vh = static_cast<bf16_t*>(workspace);
+    bf16_t* vl = vh + plane_region_bytes(T, n_proj, r_slot) / 2 / sizeof(bf16_t);
+    float* v = reinterpret_cast<float*>(static_cast<char*>(workspace) + plane_region_bytes(T, n_proj, r_slot));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int D = T - P;
     if (P > 0) LORA_TRY(check_segments(meta->seg_starts, meta->seg_slot, meta->n_segs, P, T, nullptr));
@@ -251,9 +266,19 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
     }
 
     if (P > 0) {
-        RowMap m = seg_map(meta->seg_starts, meta->seg_slot, meta->n_segs, nullptr, P, T, n_slots);
-        LORA_TRY(cuda_status(lora::launch_shrink_rowwise(v, R, x, ld_x, h_in, ps, m, dev_status, s)));
-        LORA_TRY(cuda_status(lora::launch_expand_rowwise(y, ld_y, v, R, ps, m, dev_status, s)));
+        if (meta->max_seg_len >= kTcMinSegment && lora::sgmv_tc_supported(n_proj, r_slot, h_in)) {
+            // long segments: tensor-core shrink into the hi/lo planes, then expand
+            LORA_TRY(cuda_status(lora::launch_sgmv_shrink_tc(nullptr, 0, vh, vl, x, ld_x, h_in, ps,
+                                                             meta->seg_starts, meta->seg_slot, meta->n_segs, P,
+                                                             T, n_slots, dev_status, s)));
+            LORA_TRY(cuda_status(lora::launch_sgmv_expand_tc(y, ld_y, vh, vl, ps, meta->seg_starts,
+                                                             meta->seg_slot, meta->n_segs, P, T, n_slots,
+                                                             dev_status, s)));
+        } else {
+            RowMap m = seg_map(meta->seg_starts, meta->seg_slot, meta->n_segs, nullptr, P, T, n_slots);
+            LORA_TRY(cuda_status(lora::launch_shrink_rowwise(v, R, x, ld_x, h_in, ps, m, dev_status, s)));
+            LORA_TRY(cuda_status(lora::launch_expand_rowwise(y, ld_y, v, R, ps, m, dev_status, s)));
+        }
     }
     if (D > 0) {
         const bool gathered = meta->perm && meta->gseg_starts && meta->gseg_slot && meta->n_gsegs > 0;

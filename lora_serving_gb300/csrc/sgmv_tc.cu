@@ -1,0 +1,524 @@
+// sgmv_tc.cu -- SGMV on the 5th-generation tensor cores (tcgen05) for long
+// prefill segments.
+//
+// TGI multi-LoRA page, "4. SGMV and BGMV at inference": prefill rows come in
+// variable-length segments that share one adapter, so each segment's shrink
+// and expand are dense contractions:
+//   shrink  V[rows, 0:R]      = X[rows, :] . A_slot^T          (R = n_proj * r_slot)
+//   expand  Y[rows, off + c] += V[rows, p-slice] . B'_slot,p^T
+// Both run as 128-row tiles of one segment: TMA brings 128-byte-swizzled
+// bf16 tiles into shared memory, one thread issues tcgen05.mma with the fp32
+// accumulator in tensor memory, and the epilogue reads it back with
+// tcgen05.ld.  Rows of a tile past the segment's end are computed but never
+// written (they belong to the next segment or to no one).
+//
+// The intermediate never becomes a single bf16: the shrink writes it either
+// as fp32 (the lora_sgmv_shrink entry point) or as two bf16 planes
+// hi = bf16(v), lo = bf16(v - hi) (inside lora_apply), and the expand
+// multiplies both planes by B', carrying v to ~2^-17 relative.
+//
+// Every mbarrier wait is bounded (0.2 s); a timeout sets LORA_DEV_TIMEOUT,
+// skips the rest of the tile and still frees the tensor memory.
+
+#include "launch.h"
+#include "tc_common.cuh"
+#include "tmap.h"
+
+namespace lora {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kTileM = 128;
+constexpr int kKB = 64;                 // K elements per 128-byte swizzled row
+constexpr int kBoxBytes = kTileM * 128; // one 128-row x 64-element box
+constexpr int kShrinkThreads = 128;
+constexpr int kExpandThreads = 256;
+constexpr int kExpandN = 128;           // output columns per expand tile
+
+struct TileInfo {
+    int found, slot, row0, nrows, bad;
+};
+
+// Tile u of the segments' 128-row tiles (segments with slot -1 have none).
+// One parallel round trip over the segment table when it fits the block,
+// a serial scan otherwise.  Malformed entries (bounds outside [0, n_pos))
+// contribute no tiles and set bad.
+template <int kThreads>
+__device__ TileInfo find_tile(const int32_t* seg_starts, const int32_t* seg_slot, int n_segs, int n_pos, int u)
+{
+    __shared__ int s_warp[kThreads / 32];
+    __shared__ TileInfo s_info;
+    __shared__ int s_bad;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        s_info.found = 0;
+        s_bad = 0;
+    }
+    if (n_segs <= kThreads) {
+        int s = 0, e = 0, sl = -1, n = 0;
+        bool bad = false;
+        if (tid < n_segs) {
+            s = __ldg(seg_starts + tid);
+            e = __ldg(seg_starts + tid + 1);
+            sl = __ldg(seg_slot + tid);
+            const bool sane = s >= 0 && e <= n_pos && s <= e;
+            bad = !sane;
+            n = (sane && sl >= 0) ? (e - s + kTileM - 1) / kTileM : 0;
+        }
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        if (lane == 31) s_warp[warp] = incl;
+        __syncthreads();
+        int before = 0;
+        for (int w = 0; w < warp; ++w) before += s_warp[w];
+        incl += before;
+        const int excl = incl - n;
+        if (bad) atomicOr(&s_bad, 1);
+        if (tid < n_segs && u >= excl && u < incl) {
+            TileInfo t;
+            t.found = 1;
+            t.slot = sl;
+            t.row0 = s + (u - excl) * kTileM;
+            t.nrows = min(kTileM, e - t.row0);
+            t.bad = 0;
+            s_info = t;
+        }
+        __syncthreads();
+    } else {
+        __syncthreads();
+        if (tid == 0) {
+            int acc = 0;
+            bool bad = false;
+            for (int i = 0; i < n_segs; ++i) {
+                const int s = __ldg(seg_starts + i), e = __ldg(seg_starts + i + 1), sl = __ldg(seg_slot + i);
+                const bool sane = s >= 0 && e <= n_pos && s <= e;
+                bad |= !sane;
+                const int n = (sane && sl >= 0) ? (e - s + kTileM - 1) / kTileM : 0;
+                if (u < acc + n) {
+                    s_info.found = 1;
+                    s_info.slot = sl;
+                    s_info.row0 = s + (u - acc) * kTileM;
+                    s_info.nrows = min(kTileM, e - s_info.row0);
+                    break;
+                }
+                acc += n;
+            }
+            s_bad = bad;
+        }
+        __syncthreads();
+    }
+    TileInfo r = s_info;
+    r.bad = s_bad;
+    return r;
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p)
+{
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+// ------------------------------------------------------------- shrink ----
+
+struct ShrinkTcParams {
+    int n_proj, r_slot, R, h_in, n_slots;
+    const int32_t* seg_starts;
+    const int32_t* seg_slot;
+    int n_segs, n_pos, n_rows;
+    int stages;
+    int mode;            // 0: fp32 v [n_rows][ld_v]; 1: bf16 hi/lo planes [n_rows][ld_p]
+    float* v;
+    int ld_v;
+    bf16_t* vh;
+    bf16_t* vl;
+    int ld_p;            // plane row length: n_proj * r_pad64
+    int r_pad64;         // r_slot rounded up to 64 (plane columns per projection)
+    int32_t* status;
+};
+
+__global__ void __launch_bounds__(kShrinkThreads, 1)
+sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap ma0,
+                      const __grid_constant__ CUtensorMap ma1, const __grid_constant__ CUtensorMap ma2,
+                      const __grid_constant__ CUtensorMap ma3, ShrinkTcParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full[8], empty[8], done;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_fail;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    const TileInfo ti = find_tile<kShrinkThreads>(p.seg_starts, p.seg_slot, p.n_segs, p.n_pos, blockIdx.x);
+    if (!ti.found) {
+        if (ti.bad && blockIdx.x == 0 && tid == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
+        return;
+    }
+    if (ti.slot >= p.n_slots || ti.slot < -1) {
+        if (tid == 0) flag(p.status, LORA_DEV_SLOT_OUT_OF_RANGE);
+        return;
+    }
+    const CUtensorMap* amap[4] = {&ma0, &ma1, &ma2, &ma3};
+    const int S = p.stages;
+    const int stage_bytes = kBoxBytes + p.R * 128;
+    uint8_t* base = align1024(smem_raw);
+    const int n_kb = (p.h_in + kKB - 1) / kKB;
+
+    uint32_t ncols = 32;   // accumulator columns: a power of two >= R
+    while (ncols < static_cast<uint32_t>(p.R)) ncols <<= 1;
+    if (warp == 0) tmem_alloc(&s_tmem, ncols);
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(&done, 1);
+        mbar_init_fence();
+        s_fail = 0;
+        tma_prefetch_desc(&mx);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    if (warp == 0 && lane == 0) {
+        // producer: X box + one A box per projection per 64-element K block
+        for (int kb = 0; kb < n_kb; ++kb) {
+            const int s = kb % S;
+            if (kb >= S && !mbar_wait(&empty[s], ((kb / S) - 1) & 1)) {
+                s_fail = 1;
+                break;
+            }
+            uint8_t* st = base + s * stage_bytes;
+            mbar_expect_tx(&full[s], stage_bytes);
+            tma_load_2d(st, &mx, kb * kKB, ti.row0, &full[s]);
+            for (int q = 0; q < p.n_proj; ++q)
+                tma_load_2d(st + kBoxBytes + q * p.r_slot * 128, amap[q], kb * kKB, ti.slot * p.r_slot, &full[s]);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // MMA issuer: 4 x (128 x R x 16) per K block, accumulating in TMEM
+        const uint32_t idesc = idesc_bf16_f32(kTileM, p.R);
+        bool ok = true;
+        for (int kb = 0; kb < n_kb && ok; ++kb) {
+            const int s = kb % S;
+            if (!mbar_wait(&full[s], (kb / S) & 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t st = smem_u32(base + s * stage_bytes);
+#pragma unroll
+            for (int ks = 0; ks < kKB / 16; ++ks)
+                mma_bf16(tmem, sdesc_sw128(st + ks * 32), sdesc_sw128(st + kBoxBytes + ks * 32), idesc,
+                         (kb | ks) != 0);
+            mma_commit(&empty[s]);   // frees the stage once these MMAs have read it
+        }
+        if (!ok) s_fail = 1;
+        mma_commit(&done);
+    }
+    __syncwarp();
+
+    // ---- epilogue: TMEM row (lane) -> v ----
+    bool ok = mbar_wait(&done, 0);
+    tc_fence_after();
+    const int r = warp * 32 + lane;   // tile row = TMEM lane
+    const bool row_ok = r < ti.nrows;
+    const size_t row = static_cast<size_t>(ti.row0 + r);
+    for (int c = 0; c < p.R; c += 16) {
+        float v[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
+        if (!row_ok || !ok) continue;
+        if (p.mode == 0) {
+            float4* dst = reinterpret_cast<float4*>(p.v + row * p.ld_v + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        } else {
+            const int q = c / p.r_slot, jj = c - q * p.r_slot;
+            uint32_t hi[8], lo[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                const float2 hf = __bfloat1622float2(h);
+                const __nv_bfloat162 l = __floats2bfloat162_rn(v[2 * i] - hf.x, v[2 * i + 1] - hf.y);
+                hi[i] = *reinterpret_cast<const uint32_t*>(&h);
+                lo[i] = *reinterpret_cast<const uint32_t*>(&l);
+            }
+            const size_t off = row * p.ld_p + q * p.r_pad64 + jj;
+            uint4* dh = reinterpret_cast<uint4*>(p.vh + off);
+            uint4* dl = reinterpret_cast<uint4*>(p.vl + off);
+            dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+            dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+        }
+    }
+    if (p.mode == 1 && row_ok && ok && p.r_pad64 > p.r_slot) {   // zero the plane padding
+        for (int q = 0; q < p.n_proj; ++q)
+            for (int jj = p.r_slot; jj < p.r_pad64; jj += 8) {
+                const size_t off = row * p.ld_p + q * p.r_pad64 + jj;
+                *reinterpret_cast<uint4*>(p.vh + off) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(p.vl + off) = make_uint4(0, 0, 0, 0);
+            }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, ncols);
+    if (tid == 0 && (!ok || s_fail)) flag(p.status, LORA_DEV_TIMEOUT);
+    if (tid == 0 && ti.bad && blockIdx.x == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
+}
+
+// ------------------------------------------------------------- expand ----
+
+struct ExpandTcParams {
+    int n_proj, r_slot, r_pad64, n_slots;
+    int out_off[LORA_MAX_PROJ];
+    int width[LORA_MAX_PROJ];
+    int col_tiles[LORA_MAX_PROJ];   // ceil(width / 128) per projection
+    const int32_t* seg_starts;
+    const int32_t* seg_slot;
+    int n_segs, n_pos, n_rows;
+    bf16_t* y;
+    int ld_y;
+    int32_t* status;
+};
+
+__global__ void __launch_bounds__(kExpandThreads, 2)
+sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_constant__ CUtensorMap mvl,
+                      const __grid_constant__ CUtensorMap my, const __grid_constant__ CUtensorMap mb0,
+                      const __grid_constant__ CUtensorMap mb1, const __grid_constant__ CUtensorMap mb2,
+                      const __grid_constant__ CUtensorMap mb3, ExpandTcParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t loaded, done;
+    __shared__ uint32_t s_tmem;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    const TileInfo ti = find_tile<kExpandThreads>(p.seg_starts, p.seg_slot, p.n_segs, p.n_pos, blockIdx.x);
+    if (!ti.found) {
+        if (ti.bad && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
+        return;
+    }
+    if (ti.slot >= p.n_slots || ti.slot < -1) {
+        if (tid == 0 && blockIdx.y == 0) flag(p.status, LORA_DEV_SLOT_OUT_OF_RANGE);
+        return;
+    }
+    // column tile -> (projection, first column)
+    int q = 0, ct = blockIdx.y;
+    while (q < p.n_proj - 1 && ct >= p.col_tiles[q]) {
+        ct -= p.col_tiles[q];
+        ++q;
+    }
+    const int col0 = ct * kExpandN;
+    const CUtensorMap* bmap[4] = {&mb0, &mb1, &mb2, &mb3};
+    const int kbs = p.r_pad64 / kKB;                    // K blocks per plane
+    uint8_t* base = align1024(smem_raw);
+    uint8_t* sy = base;                                 // 2 boxes: 128 rows x 64 columns of y
+    uint8_t* svh = sy + 2 * kBoxBytes;                  // kbs boxes of v_hi
+    uint8_t* svl = svh + kbs * kBoxBytes;               // kbs boxes of v_lo
+    uint8_t* sb = svl + kbs * kBoxBytes;                // kbs boxes of B' (128 output columns x 64 ranks)
+
+    if (warp == 0) tmem_alloc(&s_tmem, kExpandN);
+    if (tid == 0) {
+        mbar_init(&loaded, 1);
+        mbar_init(&done, 1);
+        mbar_init_fence();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    if (tid == 0) {
+        mbar_expect_tx(&loaded, (2 + 3 * kbs) * kBoxBytes);
+        const int ycol = p.out_off[q] + col0;
+        tma_load_2d(sy, &my, ycol, ti.row0, &loaded);
+        tma_load_2d(sy + kBoxBytes, &my, ycol + kKB, ti.row0, &loaded);
+        for (int kb = 0; kb < kbs; ++kb) {
+            tma_load_2d(svh + kb * kBoxBytes, &mvh, q * p.r_pad64 + kb * kKB, ti.row0, &loaded);
+            tma_load_2d(svl + kb * kBoxBytes, &mvl, q * p.r_pad64 + kb * kKB, ti.row0, &loaded);
+            tma_load_2d(sb + kb * kBoxBytes, bmap[q], kb * kKB, ti.slot * p.width[q] + col0, &loaded);
+        }
+    }
+    bool ok = true;
+    if (warp == 1 && lane == 0) {
+        if (mbar_wait(&loaded, 0)) {
+            tc_fence_after();
+            const uint32_t idesc = idesc_bf16_f32(kTileM, kExpandN);
+            int n = 0;
+            for (int plane = 0; plane < 2; ++plane)
+                for (int kb = 0; kb < kbs; ++kb) {
+                    const uint32_t a = smem_u32((plane ? svl : svh) + kb * kBoxBytes);
+                    const uint32_t b = smem_u32(sb + kb * kBoxBytes);
+#pragma unroll
+                    for (int ks = 0; ks < kKB / 16; ++ks, ++n)
+                        mma_bf16(tmem, sdesc_sw128(a + ks * 32), sdesc_sw128(b + ks * 32), idesc, n != 0);
+                }
+        }
+        mma_commit(&done);   // arrives even if nothing was issued
+    }
+    __syncwarp();
+    ok = mbar_wait(&done, 0) && mbar_wait(&loaded, 0);
+    tc_fence_after();
+
+    // ---- epilogue: warp w reads rows 32*(w%4).. and columns 64*(w/4).. ----
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;
+    const bool row_ok = ok && r < ti.nrows;
+    const uint8_t* yrow = sy + half * kBoxBytes + r * 128;   // swizzled 128-byte row of y
+    bf16_t* yg = p.y + static_cast<size_t>(ti.row0 + r) * p.ld_y + p.out_off[q] + col0 + half * kKB;
+    const int cols_left = p.width[q] - col0 - half * kKB;    // valid columns of this half
+#pragma unroll
+    for (int c = 0; c < kKB; c += 16) {
+        float d[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * kKB + c, d);
+        if (!row_ok) continue;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int chunk = (c >> 3) + h;                     // 16-byte chunk of the 128-byte row
+            if (chunk * 8 >= cols_left) continue;
+            const uint4 yo = *reinterpret_cast<const uint4*>(yrow + ((chunk ^ (r & 7)) << 4));
+            *reinterpret_cast<uint4*>(yg + chunk * 8) = add_round8(yo, d + h * 8);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kExpandN);
+    if (tid == 0 && !ok) flag(p.status, LORA_DEV_TIMEOUT);
+}
+
+}  // namespace
+
+bool sgmv_tc_supported(int n_proj, int r_slot, int h_in)
+{
+    return r_slot % 16 == 0 && r_slot <= LORA_MAX_RANK && n_proj * r_slot <= 256 && h_in >= kKB;
+}
+
+size_t sgmv_tc_plane_bytes(int n_rows, int n_proj, int r_slot)
+{
+    const int r_pad64 = (r_slot + kKB - 1) / kKB * kKB;
+    return 2 * static_cast<size_t>(n_rows) * n_proj * r_pad64 * sizeof(bf16_t);
+}
+
+namespace {
+
+size_t shrink_smem(int stages, int R) { return static_cast<size_t>(stages) * (kBoxBytes + R * 128) + 1024; }
+
+int shrink_stages(int R)
+{
+    int s = 4;
+    while (s > 2 && shrink_smem(s, R) > 200 * 1024) --s;
+    return s;
+}
+
+bool configure_once(const void* fn, size_t smem, int& configured_device)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (configured_device == dev) return true;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
+        return false;
+    configured_device = dev;
+    return true;
+}
+
+}  // namespace
+
+cudaError_t launch_sgmv_shrink_tc(float* v, int ld_v, bf16_t* vh, bf16_t* vl, const bf16_t* x, int ld_x, int h_in,
+                                  const ProjSet& ps, const int32_t* seg_starts, const int32_t* seg_slot, int n_segs,
+                                  int n_pos, int n_rows, int n_slots, int32_t* status, cudaStream_t stream)
+{
+    if (n_pos <= 0 || n_segs <= 0) return cudaSuccess;
+    const int R = ps.n_proj * ps.r_slot;
+    CUtensorMap mx, ma[4];
+    if (!encode_tmap_bf16(&mx, x, n_rows, h_in, ld_x, kTileM, kKB, true)) return cudaErrorInvalidValue;
+    for (int q = 0; q < 4; ++q) {
+        const int src = q < ps.n_proj ? q : 0;
+        if (!encode_tmap_bf16(&ma[q], ps.A[src], static_cast<uint64_t>(n_slots) * ps.r_slot, h_in, h_in,
+                              ps.r_slot, kKB, true))
+            return cudaErrorInvalidValue;
+    }
+    ShrinkTcParams p{};
+    p.n_proj = ps.n_proj;
+    p.r_slot = ps.r_slot;
+    p.R = R;
+    p.h_in = h_in;
+    p.n_slots = n_slots;
+    p.seg_starts = seg_starts;
+    p.seg_slot = seg_slot;
+    p.n_segs = n_segs;
+    p.n_pos = n_pos;
+    p.n_rows = n_rows;
+    p.stages = shrink_stages(R);
+    p.mode = v ? 0 : 1;
+    p.v = v;
+    p.ld_v = ld_v;
+    p.vh = vh;
+    p.vl = vl;
+    p.r_pad64 = (ps.r_slot + kKB - 1) / kKB * kKB;
+    p.ld_p = ps.n_proj * p.r_pad64;
+    p.status = status;
+    const size_t smem = shrink_smem(p.stages, R);
+    static int configured = -1;
+    if (!configure_once(reinterpret_cast<const void*>(sgmv_shrink_tc_kernel), 200 * 1024, configured))
+        return cudaErrorInvalidValue;
+    const int tiles = (n_pos + kTileM - 1) / kTileM + n_segs;   // upper bound
+    sgmv_shrink_tc_kernel<<<tiles, kShrinkThreads, smem, stream>>>(mx, ma[0], ma[1], ma[2], ma[3], p);
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const bf16_t* vl, const ProjSet& ps,
+                                  const int32_t* seg_starts, const int32_t* seg_slot, int n_segs, int n_pos,
+                                  int n_rows, int n_slots, int32_t* status, cudaStream_t stream)
+{
+    if (n_pos <= 0 || n_segs <= 0) return cudaSuccess;
+    const int r_pad64 = (ps.r_slot + kKB - 1) / kKB * kKB;
+    const int ld_p = ps.n_proj * r_pad64;
+    CUtensorMap mvh, mvl, my, mb[4];
+    if (!encode_tmap_bf16(&mvh, vh, n_rows, ld_p, ld_p, kTileM, kKB, true) ||
+        !encode_tmap_bf16(&mvl, vl, n_rows, ld_p, ld_p, kTileM, kKB, true) ||
+        !encode_tmap_bf16(&my, y, n_rows, ld_y, ld_y, kTileM, kKB, true))
+        return cudaErrorInvalidValue;
+    ExpandTcParams p{};
+    int total_tiles = 0;
+    for (int q = 0; q < 4; ++q) {
+        const int src = q < ps.n_proj ? q : 0;
+        if (!encode_tmap_bf16(&mb[q], ps.B[src], static_cast<uint64_t>(n_slots) * ps.width[src], ps.r_slot,
+                              ps.r_slot, kExpandN, kKB, true))
+            return cudaErrorInvalidValue;
+        if (q < ps.n_proj) {
+            p.out_off[q] = ps.out_off[q];
+            p.width[q] = ps.width[q];
+            p.col_tiles[q] = (ps.width[q] + kExpandN - 1) / kExpandN;
+            total_tiles += p.col_tiles[q];
+        }
+    }
+    p.n_proj = ps.n_proj;
+    p.r_slot = ps.r_slot;
+    p.r_pad64 = r_pad64;
+    p.n_slots = n_slots;
+    p.seg_starts = seg_starts;
+    p.seg_slot = seg_slot;
+    p.n_segs = n_segs;
+    p.n_pos = n_pos;
+    p.n_rows = n_rows;
+    p.y = y;
+    p.ld_y = ld_y;
+    p.status = status;
+    const int kbs = r_pad64 / kKB;
+    const size_t smem = static_cast<size_t>(2 + 3 * kbs) * kBoxBytes + 1024;
+    static int configured = -1;
+    if (!configure_once(reinterpret_cast<const void*>(sgmv_expand_tc_kernel), 200 * 1024, configured))
+        return cudaErrorInvalidValue;
+    const dim3 grid((n_pos + kTileM - 1) / kTileM + n_segs, total_tiles);
+    sgmv_expand_tc_kernel<<<grid, kExpandThreads, smem, stream>>>(mvh, mvl, my, mb[0], mb[1], mb[2], mb[3], p);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace lora

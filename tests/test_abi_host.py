@@ -183,4 +183,6 @@ def test_kernel_entry_points_validate_before_launch():
     st = lib.lora_apply(base, 64, base, 64, 64, ctypes.addressof(projs), 5, 16, 2,
                         ctypes.addressof(meta), base, 1 << 20, 0, 0, 0)
     assert st == 1
-    assert lib.lora_apply_workspace_bytes(10, 3, 16) == 10 * 3 * 16 * 4
+    # bf16 hi/lo planes (rank padded to 64, region rounded to 256 B) + fp32 v
+    planes = (2 * 10 * 3 * 64 * 2 + 255) // 256 * 256
+    assert lib.lora_apply_workspace_bytes(10, 3, 16) == planes + 10 * 3 * 16 * 4

@@ -384,3 +384,52 @@ def test_apply_decode_bad_permutation_flagged():
     np.testing.assert_array_equal(got[[0, 2, 4]], wl.y["g"][[0, 2, 4]])
     ok = np.array([1, 3, 5])
     check_bf16(got[ok], oracle_group(wl, "g", ok), ids[ok], wl.y["g"][ok], "slot 1 rows")
+
+
+# ------------------------------------------- tensor-core SGMV (tcgen05) ----
+
+def _segments(lens, slots):
+    return np.concatenate([np.full(n, s, np.int32) for n, s in zip(lens, slots)])
+
+
+@pytest.mark.parametrize("h_in,widths,rank,lens,slots", [
+    (256, (256,), 16, [300, 5, 129, 64], [1, 2, -1, 3]),                 # tiles crossing segment ends
+    (512, (512, 128, 128), 32, [70, 200, 128], [0, 3, 1]),               # q/k/v stack: 96 ranks
+    (1024, (1024,), 64, [64, 640, 1], [2, 2, 0]),                        # same slot twice, 1-row segment
+    (320, (320, 40, 40), 16, [130, 90], [3, 0]),                         # widths not multiples of 128
+    (4096, (2048, 2048), 128, [256, 100], [1, 0]),                       # r_slot 128: two K blocks per plane
+    (8200, (4096,), 16, [200], [2]),                                     # h_in not a multiple of 64
+])
+@pytest.mark.parametrize("mode", ["delta", "accumulate"])
+def test_apply_prefill_tensor_core(h_in, widths, rank, lens, slots, mode):
+    """Prefill segments of >= 64 rows take the tcgen05 shrink/expand route."""
+    ids = _segments(lens, slots)
+    rng = np.random.default_rng(h_in)
+    ids = np.concatenate([ids, rng.integers(-1, 4, 9).astype(np.int32)])   # plus some decode rows
+    wl = _small(ids, int(sum(lens)), rank=rank, h_in=h_in, widths=widths, seed=rank, mode=mode)
+    got = _run_apply(wl, "g")
+    check_bf16(got, oracle_group(wl, "g"), wl.ids, wl.y["g"], f"tc h_in={h_in} rank={rank}")
+
+
+def test_sgmv_shrink_tensor_core_fp32():
+    """lora_sgmv_shrink on long contiguous segments (tensor-core route) gives
+    fp32 v within the fp32 accumulation bound of the oracle's."""
+    lens, slots = [150, 80, 300], [2, -1, 0]
+    ids = _segments(lens, slots)
+    wl = _small(ids, ids.size, rank=32, h_in=1024, widths=(64,), seed=9)
+    st = store.GroupStore.from_workload(wl, "g")
+    m = abi.lora_build_metadata(wl.ids, wl.n_prefill, wl.n_slots)
+    v = torch.full((wl.n_rows, 32), -3.0, device="cuda")
+    s = _status()
+    abi.lora_sgmv_shrink(v, to_dev(wl.x["g"]), st.A[0], torch.from_numpy(m["seg_starts"]).cuda(),
+                         torch.from_numpy(m["seg_slot"]).cuda(), m["n_segs"], None, wl.n_prefill, h_in=1024,
+                         r_slot=32, n_slots=wl.n_slots, max_seg_len=m["max_seg_len"], dev_status=s)
+    torch.cuda.synchronize()
+    assert abi.lora_read_device_status(s) == 0
+    got = v.cpu().numpy().astype(np.float64)
+    ad = oracle_adapters(wl, "g", "p0")
+    ref = O.shrink(wl.ids, wl.x["g"], ad, v_cols=32)
+    bound = shrink_bound(wl.ids, wl.x["g"], [wl.A[("g", "p0", k)] for k in range(wl.n_slots)], 1024)
+    act = wl.ids >= 0
+    assert np.all(np.abs(got[act] - ref[act]) <= bound[act])
+    assert np.all(got[~act] == -3.0), "rows of slot -1 segments must not be written"
