@@ -20,6 +20,8 @@
 // Every mbarrier wait is bounded (0.2 s); a timeout sets LORA_DEV_TIMEOUT,
 // skips the rest of the tile and still frees the tensor memory.
 
+#include <cstdlib>
+
 #include "launch.h"
 #include "tc_common.cuh"
 #include "tmap.h"
@@ -34,7 +36,6 @@ constexpr int kTileM = 128;
 constexpr int kKB = 64;                 // K elements per 128-byte swizzled row
 constexpr int kBoxBytes = kTileM * 128; // one 128-row x 64-element box
 constexpr int kShrinkThreads = 128;
-constexpr int kExpandThreads = 256;
 constexpr int kExpandN = 128;           // output columns per expand tile
 
 struct TileInfo {
@@ -272,12 +273,26 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
 }
 
 // ------------------------------------------------------------- expand ----
+//
+// One CTA owns a 128-row tile of a segment and a run of up to tiles_per_cta
+// 128-column output tiles of one projection.  Its v_hi / v_lo tile is loaded
+// once; B' and y tiles stream through a kStagesE-deep TMA ring; the fp32
+// accumulator is double-buffered in tensor memory, so the epilogue of tile i
+// (TMEM -> registers, + y from shared memory, round, store) overlaps the
+// loads and MMAs of tile i+1.
+//   warp 0: TMA producer      warp 1: MMA issuer      warps 2..9: epilogue
+
+constexpr int kStagesE = 3;
+constexpr int kEpiWarps = 8;
+constexpr int kExpandThreadsP = 32 * (2 + kEpiWarps);
 
 struct ExpandTcParams {
     int n_proj, r_slot, r_pad64, n_slots;
     int out_off[LORA_MAX_PROJ];
     int width[LORA_MAX_PROJ];
     int col_tiles[LORA_MAX_PROJ];   // ceil(width / 128) per projection
+    int chunks[LORA_MAX_PROJ];      // ceil(col_tiles / tiles_per_cta) per projection
+    int tiles_per_cta;
     const int32_t* seg_starts;
     const int32_t* seg_slot;
     int n_segs, n_pos, n_rows;
@@ -286,18 +301,19 @@ struct ExpandTcParams {
     int32_t* status;
 };
 
-__global__ void __launch_bounds__(kExpandThreads, 2)
+__global__ void __launch_bounds__(kExpandThreadsP, 1)
 sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_constant__ CUtensorMap mvl,
                       const __grid_constant__ CUtensorMap my, const __grid_constant__ CUtensorMap mb0,
                       const __grid_constant__ CUtensorMap mb1, const __grid_constant__ CUtensorMap mb2,
                       const __grid_constant__ CUtensorMap mb3, ExpandTcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t loaded, done;
+    __shared__ __align__(8) uint64_t vbar, full[kStagesE], empty[kStagesE], acc_full[2], acc_empty[2];
     __shared__ uint32_t s_tmem;
+    __shared__ volatile int s_fail;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    const TileInfo ti = find_tile<kExpandThreads>(p.seg_starts, p.seg_slot, p.n_segs, p.n_pos, blockIdx.x);
+    const TileInfo ti = find_tile<kExpandThreadsP>(p.seg_starts, p.seg_slot, p.n_segs, p.n_pos, blockIdx.x);
     if (!ti.found) {
         if (ti.bad && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
         return;
@@ -306,88 +322,132 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
         if (tid == 0 && blockIdx.y == 0) flag(p.status, LORA_DEV_SLOT_OUT_OF_RANGE);
         return;
     }
-    // column tile -> (projection, first column)
-    int q = 0, ct = blockIdx.y;
-    while (q < p.n_proj - 1 && ct >= p.col_tiles[q]) {
-        ct -= p.col_tiles[q];
+    // chunk -> (projection q, first column tile, number of tiles)
+    int q = 0, ch = blockIdx.y;
+    while (q < p.n_proj - 1 && ch >= p.chunks[q]) {
+        ch -= p.chunks[q];
         ++q;
     }
-    const int col0 = ct * kExpandN;
+    const int t_first = ch * p.tiles_per_cta;
+    const int n_tiles = min(p.tiles_per_cta, p.col_tiles[q] - t_first);
+    if (n_tiles <= 0) return;
     const CUtensorMap* bmap[4] = {&mb0, &mb1, &mb2, &mb3};
-    const int kbs = p.r_pad64 / kKB;                    // K blocks per plane
+    const int kbs = p.r_pad64 / kKB;                         // K blocks per plane
+    const int S = kbs == 1 ? kStagesE : 2;                   // ring depth that fits shared memory
+    const int stage_bytes = (kbs + 2) * kBoxBytes;           // B' (kbs boxes) + y (2 boxes)
     uint8_t* base = align1024(smem_raw);
-    uint8_t* sy = base;                                 // 2 boxes: 128 rows x 64 columns of y
-    uint8_t* svh = sy + 2 * kBoxBytes;                  // kbs boxes of v_hi
-    uint8_t* svl = svh + kbs * kBoxBytes;               // kbs boxes of v_lo
-    uint8_t* sb = svl + kbs * kBoxBytes;                // kbs boxes of B' (128 output columns x 64 ranks)
+    uint8_t* svh = base;                                     // kbs boxes of v_hi
+    uint8_t* svl = svh + kbs * kBoxBytes;                    // kbs boxes of v_lo
+    uint8_t* ring = svl + kbs * kBoxBytes;                   // kStagesE x [B' | y]
 
-    if (warp == 0) tmem_alloc(&s_tmem, kExpandN);
+    if (warp == 0) tmem_alloc(&s_tmem, 2 * kExpandN);
     if (tid == 0) {
-        mbar_init(&loaded, 1);
-        mbar_init(&done, 1);
+        mbar_init(&vbar, 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kEpiWarps);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], kEpiWarps);
+        }
         mbar_init_fence();
+        s_fail = 0;
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
-    if (tid == 0) {
-        mbar_expect_tx(&loaded, (2 + 3 * kbs) * kBoxBytes);
-        const int ycol = p.out_off[q] + col0;
-        tma_load_2d(sy, &my, ycol, ti.row0, &loaded);
-        tma_load_2d(sy + kBoxBytes, &my, ycol + kKB, ti.row0, &loaded);
-        for (int kb = 0; kb < kbs; ++kb) {
-            tma_load_2d(svh + kb * kBoxBytes, &mvh, q * p.r_pad64 + kb * kKB, ti.row0, &loaded);
-            tma_load_2d(svl + kb * kBoxBytes, &mvl, q * p.r_pad64 + kb * kKB, ti.row0, &loaded);
-            tma_load_2d(sb + kb * kBoxBytes, bmap[q], kb * kKB, ti.slot * p.width[q] + col0, &loaded);
-        }
-    }
-    bool ok = true;
-    if (warp == 1 && lane == 0) {
-        if (mbar_wait(&loaded, 0)) {
-            tc_fence_after();
-            const uint32_t idesc = idesc_bf16_f32(kTileM, kExpandN);
-            int n = 0;
-            for (int plane = 0; plane < 2; ++plane)
-                for (int kb = 0; kb < kbs; ++kb) {
-                    const uint32_t a = smem_u32((plane ? svl : svh) + kb * kBoxBytes);
-                    const uint32_t b = smem_u32(sb + kb * kBoxBytes);
-#pragma unroll
-                    for (int ks = 0; ks < kKB / 16; ++ks, ++n)
-                        mma_bf16(tmem, sdesc_sw128(a + ks * 32), sdesc_sw128(b + ks * 32), idesc, n != 0);
+    if (warp == 0) {
+        if (lane == 0) {   // ---- producer ----
+            mbar_expect_tx(&vbar, 2 * kbs * kBoxBytes);
+            for (int kb = 0; kb < kbs; ++kb) {
+                tma_load_2d(svh + kb * kBoxBytes, &mvh, q * p.r_pad64 + kb * kKB, ti.row0, &vbar);
+                tma_load_2d(svl + kb * kBoxBytes, &mvl, q * p.r_pad64 + kb * kKB, ti.row0, &vbar);
+            }
+            for (int i = 0; i < n_tiles && !s_fail; ++i) {
+                const int s = i % S;
+                if (i >= S && !mbar_wait(&empty[s], ((i / S) - 1) & 1)) {
+                    s_fail = 1;
+                    break;
                 }
+                uint8_t* st = ring + s * stage_bytes;
+                const int col0 = (t_first + i) * kExpandN;
+                mbar_expect_tx(&full[s], stage_bytes);
+                for (int kb = 0; kb < kbs; ++kb)
+                    tma_load_2d(st + kb * kBoxBytes, bmap[q], kb * kKB, ti.slot * p.width[q] + col0, &full[s]);
+                const int ycol = p.out_off[q] + col0;
+                tma_load_2d(st + kbs * kBoxBytes, &my, ycol, ti.row0, &full[s]);
+                tma_load_2d(st + (kbs + 1) * kBoxBytes, &my, ycol + kKB, ti.row0, &full[s]);
+            }
         }
-        mma_commit(&done);   // arrives even if nothing was issued
-    }
-    __syncwarp();
-    ok = mbar_wait(&done, 0) && mbar_wait(&loaded, 0);
-    tc_fence_after();
-
-    // ---- epilogue: warp w reads rows 32*(w%4).. and columns 64*(w/4).. ----
-    const int quarter = warp & 3, half = warp >> 2;
-    const int r = quarter * 32 + lane;
-    const bool row_ok = ok && r < ti.nrows;
-    const uint8_t* yrow = sy + half * kBoxBytes + r * 128;   // swizzled 128-byte row of y
-    bf16_t* yg = p.y + static_cast<size_t>(ti.row0 + r) * p.ld_y + p.out_off[q] + col0 + half * kKB;
-    const int cols_left = p.width[q] - col0 - half * kKB;    // valid columns of this half
+    } else if (warp == 1) {
+        if (lane == 0) {   // ---- MMA issuer ----
+            const uint32_t idesc = idesc_bf16_f32(kTileM, kExpandN);
+            bool ok = mbar_wait(&vbar, 0);
+            tc_fence_after();
+            for (int i = 0; i < n_tiles && ok && !s_fail; ++i) {
+                const int s = i % S, a = i & 1;
+                if (i >= 2 && !mbar_wait(&acc_empty[a], ((i >> 1) - 1) & 1)) { ok = false; break; }
+                if (!mbar_wait(&full[s], (i / S) & 1)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t bs = smem_u32(ring + s * stage_bytes);
+                const uint32_t d = tmem + a * kExpandN;
+                int n = 0;
+                for (int plane = 0; plane < 2; ++plane)
+                    for (int kb = 0; kb < kbs; ++kb) {
+                        const uint32_t av = smem_u32((plane ? svl : svh) + kb * kBoxBytes);
 #pragma unroll
-    for (int c = 0; c < kKB; c += 16) {
-        float d[16];
-        tmem_ld16(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * kKB + c, d);
-        if (!row_ok) continue;
+                        for (int ks = 0; ks < kKB / 16; ++ks, ++n)
+                            mma_bf16(d, sdesc_sw128(av + ks * 32), sdesc_sw128(bs + kb * kBoxBytes + ks * 32),
+                                     idesc, n != 0);
+                    }
+                mma_commit(&acc_full[a]);
+            }
+            if (!ok) s_fail = 1;
+        }
+    } else {   // ---- epilogue warps ----
+        const int e = warp - 2;
+        const int quarter = warp & 3;       // TMEM lanes this warp may read
+        const int half = e >> 2;            // which 64-column half of the tile
+        const int r = quarter * 32 + lane;  // tile row
+        const bool row_ok = r < ti.nrows;
+        bf16_t* yrow_g = p.y + static_cast<size_t>(ti.row0 + r) * p.ld_y + p.out_off[q];
+        for (int i = 0; i < n_tiles; ++i) {
+            const int s = i % S, a = i & 1;
+            const bool ok = !s_fail && mbar_wait(&acc_full[a], (i >> 1) & 1);
+            if (!ok) s_fail = 1;
+            tc_fence_after();
+            const uint8_t* sy = ring + s * stage_bytes + (kbs + half) * kBoxBytes + r * 128;   // swizzled row
+            const int col0 = (t_first + i) * kExpandN + half * kKB;
+            const int cols_left = p.width[q] - col0;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int chunk = (c >> 3) + h;                     // 16-byte chunk of the 128-byte row
-            if (chunk * 8 >= cols_left) continue;
-            const uint4 yo = *reinterpret_cast<const uint4*>(yrow + ((chunk ^ (r & 7)) << 4));
-            *reinterpret_cast<uint4*>(yg + chunk * 8) = add_round8(yo, d + h * 8);
+            for (int c = 0; c < kKB; c += 16) {
+                float d[16];
+                tmem_ld16(tmem + a * kExpandN + (static_cast<uint32_t>(quarter * 32) << 16) + half * kKB + c, d);
+                if (!ok || !row_ok) continue;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int chunk = (c >> 3) + h;
+                    if (chunk * 8 >= cols_left) continue;
+                    const uint4 yo = *reinterpret_cast<const uint4*>(sy + ((chunk ^ (r & 7)) << 4));
+                    *reinterpret_cast<uint4*>(yrow_g + col0 + chunk * 8) = add_round8(yo, d + h * 8);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&acc_empty[a]);   // this warp is done with accumulator a
+                mbar_arrive(&empty[s]);       // ... and with stage s (y tile; B' was read by the MMA)
+            }
+            if (!ok) break;
         }
     }
-    tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kExpandN);
-    if (tid == 0 && !ok) flag(p.status, LORA_DEV_TIMEOUT);
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 2 * kExpandN);
+    if (tid == 0 && s_fail) flag(p.status, LORA_DEV_TIMEOUT);
 }
 
 }  // namespace
@@ -424,6 +484,14 @@ bool configure_once(const void* fn, size_t smem, int& configured_device)
         return false;
     configured_device = dev;
     return true;
+}
+
+// Output tiles per expand CTA (LORA_TC_TILES_PER_CTA overrides; tuning aid).
+int tiles_per_cta_env()
+{
+    const char* e = std::getenv("LORA_TC_TILES_PER_CTA");
+    const int v = (e && *e) ? std::atoi(e) : 8;
+    return v > 0 ? v : 8;
 }
 
 }  // namespace
@@ -485,7 +553,8 @@ cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const b
         !encode_tmap_bf16(&my, y, n_rows, ld_y, ld_y, kTileM, kKB, true))
         return cudaErrorInvalidValue;
     ExpandTcParams p{};
-    int total_tiles = 0;
+    p.tiles_per_cta = tiles_per_cta_env();
+    int total_chunks = 0;
     for (int q = 0; q < 4; ++q) {
         const int src = q < ps.n_proj ? q : 0;
         if (!encode_tmap_bf16(&mb[q], ps.B[src], static_cast<uint64_t>(n_slots) * ps.width[src], ps.r_slot,
@@ -495,7 +564,8 @@ cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const b
             p.out_off[q] = ps.out_off[q];
             p.width[q] = ps.width[q];
             p.col_tiles[q] = (ps.width[q] + kExpandN - 1) / kExpandN;
-            total_tiles += p.col_tiles[q];
+            p.chunks[q] = (p.col_tiles[q] + p.tiles_per_cta - 1) / p.tiles_per_cta;
+            total_chunks += p.chunks[q];
         }
     }
     p.n_proj = ps.n_proj;
@@ -511,12 +581,13 @@ cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const b
     p.ld_y = ld_y;
     p.status = status;
     const int kbs = r_pad64 / kKB;
-    const size_t smem = static_cast<size_t>(2 + 3 * kbs) * kBoxBytes + 1024;
+    const int stages = kbs == 1 ? kStagesE : 2;
+    const size_t smem = static_cast<size_t>(2 * kbs + stages * (kbs + 2)) * kBoxBytes + 1024;
     static int configured = -1;
-    if (!configure_once(reinterpret_cast<const void*>(sgmv_expand_tc_kernel), 200 * 1024, configured))
+    if (!configure_once(reinterpret_cast<const void*>(sgmv_expand_tc_kernel), 227 * 1024, configured))
         return cudaErrorInvalidValue;
-    const dim3 grid((n_pos + kTileM - 1) / kTileM + n_segs, total_tiles);
-    sgmv_expand_tc_kernel<<<grid, kExpandThreads, smem, stream>>>(mvh, mvl, my, mb[0], mb[1], mb[2], mb[3], p);
+    const dim3 grid((n_pos + kTileM - 1) / kTileM + n_segs, total_chunks);
+    sgmv_expand_tc_kernel<<<grid, kExpandThreadsP, smem, stream>>>(mvh, mvl, my, mb[0], mb[1], mb[2], mb[3], p);
     note_launch();
     return cudaGetLastError();
 }
