@@ -474,15 +474,18 @@ int shrink_stages(int R)
     return s;
 }
 
-bool configure_once(const void* fn, size_t smem, int& configured_device)
+// Raises the kernel's dynamic shared-memory limit to at least smem on the
+// current device (the limit excludes the kernel's static shared memory).
+bool configure_once(const void* fn, size_t smem, int& configured_device, size_t& configured_bytes)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    if (configured_device == dev) return true;
+    if (configured_device == dev && configured_bytes >= smem) return true;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
         return false;
     configured_device = dev;
+    configured_bytes = smem;
     return true;
 }
 
@@ -532,7 +535,8 @@ cudaError_t launch_sgmv_shrink_tc(float* v, int ld_v, bf16_t* vh, bf16_t* vl, co
     p.status = status;
     const size_t smem = shrink_smem(p.stages, R);
     static int configured = -1;
-    if (!configure_once(reinterpret_cast<const void*>(sgmv_shrink_tc_kernel), 200 * 1024, configured))
+    static size_t configured_bytes = 0;
+    if (!configure_once(reinterpret_cast<const void*>(sgmv_shrink_tc_kernel), smem, configured, configured_bytes))
         return cudaErrorInvalidValue;
     const int tiles = (n_pos + kTileM - 1) / kTileM + n_segs;   // upper bound
     sgmv_shrink_tc_kernel<<<tiles, kShrinkThreads, smem, stream>>>(mx, ma[0], ma[1], ma[2], ma[3], p);
@@ -584,7 +588,8 @@ cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const b
     const int stages = kbs == 1 ? kStagesE : 2;
     const size_t smem = static_cast<size_t>(2 * kbs + stages * (kbs + 2)) * kBoxBytes + 1024;
     static int configured = -1;
-    if (!configure_once(reinterpret_cast<const void*>(sgmv_expand_tc_kernel), 227 * 1024, configured))
+    static size_t configured_bytes = 0;
+    if (!configure_once(reinterpret_cast<const void*>(sgmv_expand_tc_kernel), smem, configured, configured_bytes))
         return cudaErrorInvalidValue;
     const dim3 grid((n_pos + kTileM - 1) / kTileM + n_segs, total_chunks);
     sgmv_expand_tc_kernel<<<grid, kExpandThreadsP, smem, stream>>>(mvh, mvl, my, mb[0], mb[1], mb[2], mb[3], p);
