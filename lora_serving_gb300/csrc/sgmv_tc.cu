@@ -493,8 +493,8 @@ bool configure_once(const void* fn, size_t smem, int& configured_device, size_t&
 int tiles_per_cta_env()
 {
     const char* e = std::getenv("LORA_TC_TILES_PER_CTA");
-    const int v = (e && *e) ? std::atoi(e) : 8;
-    return v > 0 ? v : 8;
+    const int v = (e && *e) ? std::atoi(e) : 16;
+    return v > 0 ? v : 16;
 }
 
 }  // namespace
