@@ -280,10 +280,10 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
 // accumulator is double-buffered in tensor memory, so the epilogue of tile i
 // (TMEM -> registers, + y from shared memory, round, store) overlaps the
 // loads and MMAs of tile i+1.
-//   warp 0: TMA producer      warp 1: MMA issuer      warps 2..9: epilogue
+//   warp 0: TMA producer      warp 1: MMA issuer      warps 2..17: epilogue
 
 constexpr int kStagesE = 3;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;       // 4 per TMEM lane quarter, 32 columns each
 constexpr int kExpandThreadsP = 32 * (2 + kEpiWarps);
 
 struct ExpandTcParams {
@@ -345,11 +345,11 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
         mbar_init(&vbar, 1);
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kEpiWarps);
+            mbar_init(&empty[s], kEpiWarps / 2);   // released by the team that took the tile
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_empty[a], kEpiWarps);
+            mbar_init(&acc_empty[a], kEpiWarps / 2);
         }
         mbar_init_fence();
         s_fail = 0;
@@ -408,41 +408,68 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
             if (!ok) s_fail = 1;
         }
     } else {   // ---- epilogue warps ----
+        // Two teams of 8 warps take alternate tiles (team t: tiles i = t, t+2,
+        // ..., accumulator t), so two tiles' epilogues are in flight at once.
+        // Within a team, 2 warps per TMEM lane quarter, 64 columns each.
         const int e = warp - 2;
+        const int team = e >> 3, w8 = e & 7;
         const int quarter = warp & 3;       // TMEM lanes this warp may read
-        const int half = e >> 2;            // which 64-column half of the tile
+        const int hc = w8 >> 2;             // which 64-column half of the tile (one y box)
         const int r = quarter * 32 + lane;  // tile row
         const bool row_ok = r < ti.nrows;
         bf16_t* yrow_g = p.y + static_cast<size_t>(ti.row0 + r) * p.ld_y + p.out_off[q];
-        for (int i = 0; i < n_tiles; ++i) {
-            const int s = i % S, a = i & 1;
+        // Every warp of a team runs every one of the team's iterations and
+        // meets both named barriers whatever happened (after a timeout it
+        // only skips work), so a barrier never waits for a warp that has left.
+        for (int i = team; i < n_tiles; i += 2) {
+            const int s = i % S, a = team;
             const bool ok = !s_fail && mbar_wait(&acc_full[a], (i >> 1) & 1);
             if (!ok) s_fail = 1;
             tc_fence_after();
-            const uint8_t* sy = ring + s * stage_bytes + (kbs + half) * kBoxBytes + r * 128;   // swizzled row
-            const int col0 = (t_first + i) * kExpandN + half * kKB;
-            const int cols_left = p.width[q] - col0;
-#pragma unroll
-            for (int c = 0; c < kKB; c += 16) {
-                float d[16];
-                tmem_ld16(tmem + a * kExpandN + (static_cast<uint32_t>(quarter * 32) << 16) + half * kKB + c, d);
-                if (!ok || !row_ok) continue;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int chunk = (c >> 3) + h;
-                    if (chunk * 8 >= cols_left) continue;
-                    const uint4 yo = *reinterpret_cast<const uint4*>(sy + ((chunk ^ (r & 7)) << 4));
-                    *reinterpret_cast<uint4*>(yrow_g + col0 + chunk * 8) = add_round8(yo, d + h * 8);
-                }
-            }
+            float d[64];
+            const uint32_t tcol = tmem + a * kExpandN + (static_cast<uint32_t>(quarter * 32) << 16) + hc * kKB;
+            tmem_ld32(tcol, d);
+            tmem_ld32(tcol + 32, d + 32);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&acc_empty[a]);   // this warp is done with accumulator a
-                mbar_arrive(&empty[s]);       // ... and with stage s (y tile; B' was read by the MMA)
+            if (lane == 0) mbar_arrive(&acc_empty[a]);   // accumulator a may be overwritten now
+
+            uint8_t* ybox = ring + s * stage_bytes + (kbs + hc) * kBoxBytes;
+            uint8_t* sy = ybox + r * 128;
+            const int tile_col0 = (t_first + i) * kExpandN;
+            const int col0 = tile_col0 + hc * kKB;
+            const int cols_left = p.width[q] - col0;
+            // whole tile inside this segment's rows and this projection's columns:
+            // results go back into the staged tile and leave by TMA bulk stores
+            const bool whole = ti.nrows == kTileM && tile_col0 + kExpandN <= p.width[q];
+            if (ok && row_ok) {
+#pragma unroll
+                for (int chunk = 0; chunk < 8; ++chunk) {
+                    if (chunk * 8 >= cols_left) continue;
+                    uint4* slot8 = reinterpret_cast<uint4*>(sy + ((chunk ^ (r & 7)) << 4));
+                    const uint4 res = add_round8(*slot8, d + chunk * 8);
+                    if (whole) *slot8 = res;
+                    else *reinterpret_cast<uint4*>(yrow_g + col0 + chunk * 8) = res;
+                }
             }
-            if (!ok) break;
+            if (whole) {
+                fence_async_smem();
+                named_barrier(1 + team, 256);
+                if (w8 == 0 && lane == 0) {
+                    if (!s_fail) {
+                        uint8_t* y0 = ring + s * stage_bytes + kbs * kBoxBytes;
+                        tma_store_2d(&my, p.out_off[q] + tile_col0, ti.row0, y0);
+                        tma_store_2d(&my, p.out_off[q] + tile_col0 + kKB, ti.row0, y0 + kBoxBytes);
+                        bulk_commit();
+                    }
+                    bulk_wait_read();   // the stage may be refilled once the stores have read it
+                }
+                named_barrier(1 + team, 256);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);   // this warp is done with stage s
         }
+        if (w8 == 0 && lane == 0) bulk_wait_all();
     }
     __syncthreads();
     tc_fence_after();
