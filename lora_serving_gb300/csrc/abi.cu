@@ -282,8 +282,10 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
     }
     if (D > 0) {
         const bool gathered = meta->perm && meta->gseg_starts && meta->gseg_slot && meta->n_gsegs > 0;
-        if (r_slot <= LORA_BGMV_MAX_RANK && gathered && lora::fused_decode_supported(n_proj, r_slot)) {
-            // BGMV route, one launch: rows grouped by adapter, cluster split-K.
+        if (gathered && lora::fused_decode_supported(n_proj, r_slot)) {
+            // One launch over the decode rows grouped by adapter (cluster
+            // split-K): the BGMV route for r_slot <= LORA_BGMV_MAX_RANK, and
+            // the SGMV-over-gather-groups route above it (same grouping).
             LORA_TRY(cuda_status(lora::launch_bgmv_fused(y, ld_y, x, ld_x, h_in, ps, meta->perm,
                                                          meta->gseg_starts, meta->gseg_slot, meta->n_gsegs,
                                                          D, meta->max_gseg_len, T, n_slots, flags,

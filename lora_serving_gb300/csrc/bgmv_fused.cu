@@ -579,14 +579,14 @@ bgmv_fused_kernel(FusedParams p)
             failed = __syncthreads_or(failed);
         }
         int cur_p = -1;
-        uint32_t ahi[2][4], alo[2][4];   // v fragments of the current projection (r_pad <= 32)
+        uint32_t ahi[4][4], alo[4][4];   // v fragments of the current projection (r_pad <= 64)
         for (int ci = warp; ci < nch; ci += kWarps) {
             const int pj = s_cp[ci];
             if (pj != cur_p) {
                 cur_p = pj;
                 const float* vp = vfull + pj * r_slot;
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
+                for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
                         // a0: (row g, k 2q..), a1: (row g+8, k 2q..), a2: (row g, k 2q+8..), a3: (row g+8, k 2q+8..)
@@ -604,7 +604,7 @@ bgmv_fused_kernel(FusedParams p)
             float d[4] = {0.f, 0.f, 0.f, 0.f};
             const bf16_t* bc = sB + ci * 8 * r_slot;
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
+            for (int kk = 0; kk < 4; ++kk) {
                 if (kk * 16 < r_pad) {
                     uint32_t b0, b1;
                     const int l = lane & 15;
@@ -670,7 +670,8 @@ int env_int(const char* name, int dflt)
 
 bool fused_decode_supported(int n_proj, int r_slot)
 {
-    return r_slot <= LORA_BGMV_MAX_RANK && n_proj * r_slot <= 2 * 8 * 8 && r_slot % 8 == 0;
+    // <= 2 rank tiles of 8 per warp in the shrink; <= 4 K steps of 16 in the expand
+    return r_slot <= 64 && n_proj * r_slot <= 2 * 8 * 8 && r_slot % 8 == 0;
 }
 
 cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
@@ -693,18 +694,22 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     }
     // Cluster size: split K over up to 8 CTAs while each keeps >= one stage
     // (8 measured faster than 16 on the 3B decode shapes: smaller grids let
-    // more consecutive calls be resident at once under PDL).
+    // more consecutive calls be resident at once under PDL); 16 for long K.
     int cs = 1;
-    while (cs < 8 && h_in / (cs * 2) >= kKT) cs *= 2;
+    const int cs_max = h_in >= 8192 ? 16 : 8;
+    while (cs < cs_max && h_in / (cs * 2) >= kKT) cs *= 2;
     cs = env_int("LORA_FUSED_CS", cs);
     // Units of <= 16 rows: at most ceil(longest group / 16) per group.
     int max_units = n_groups + n_pos / kRB;
     if (max_group_len > 0) max_units = min(max_units, n_groups * ((max_group_len + kRB - 1) / kRB));
-    // Column parts per unit (more clusters, each recomputing the shrink);
-    // one part measured best on the decode shapes here.
-    const int parts = env_int("LORA_FUSED_PARTS", 1);
     int total_ch = 0;
     for (int q = 0; q < ps.n_proj; ++q) total_ch += ps.width[q] / 8;
+    // Column parts per unit (more clusters, each recomputing the shrink from
+    // L2): one for the decode shapes here; wide outputs get enough parts that
+    // each CTA expands at most two tiles of kMaxChunks chunks.
+    int parts = 1;
+    while (parts < 8 && (total_ch + cs * parts - 1) / (cs * parts) > 2 * kMaxChunks) parts *= 2;
+    parts = env_int("LORA_FUSED_PARTS", parts);
     const int per_cta = (total_ch + cs * parts - 1) / (cs * parts);
     const int nch_tile = min(kMaxChunks, max(1, per_cta));
 

@@ -359,6 +359,9 @@ def test_host_rejects_before_enqueue():
     (256, (256, 64, 64), 16, 7, 3),                 # fewer rows than one unit
     (8192, (28672, 28672), 16, 20, 4),              # wide outputs: several expand tiles per CTA
     (1024, (1024,), 24, 20, 4),                     # slot rank not a multiple of 16
+    (8192, (28672, 28672), 64, 12, 4),              # rank 64 above the BGMV cap: gather groups, column parts
+    (28672, (8192,), 64, 9, 3),                     # rank 64, long K (70B down projection shape)
+    (2048, (2048, 512, 512), 40, 25, 3),            # rank 40: K padded to 48 in the expand
 ])
 def test_apply_decode_fused_shapes(h_in, widths, rank, T, n_slots):
     rng = np.random.default_rng(h_in + T)
