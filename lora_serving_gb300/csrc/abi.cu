@@ -288,7 +288,7 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
             // the SGMV-over-gather-groups route above it (same grouping).
             LORA_TRY(cuda_status(lora::launch_bgmv_fused(y, ld_y, x, ld_x, h_in, ps, meta->perm,
                                                          meta->gseg_starts, meta->gseg_slot, meta->n_gsegs,
-                                                         D, meta->max_gseg_len, T, n_slots, flags,
+                                                         D, meta->max_gseg_len, T, n_slots, flags, v,
                                                          dev_status, s)));
         } else {
             RowMap m = r_slot <= LORA_BGMV_MAX_RANK

@@ -43,7 +43,9 @@ constexpr int kRB = 16;            // rows per unit (the mma M)
 constexpr int kKT = 128;           // K elements per pipeline stage
 constexpr int kPad = 8;            // bf16 padding per smem row: conflict-free ldmatrix
 constexpr int kLds = kKT + kPad;
-constexpr int kStages = 2;
+constexpr int kStages = 2;         // K stages of the one-launch form
+constexpr int kStagesShrink = 4;   // K stages of the shrink-only form
+constexpr double kSplitWeightBytes = 32.0 * (1 << 20);   // two launches from this many weight bytes per call
 constexpr int kMaxChunks = 64;     // output chunks (8 columns) per expand tile
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
@@ -72,6 +74,8 @@ struct FusedParams {
     int r_pad;                // r_slot rounded up to 16 (expand mma K)
     int x_ready;              // x may be read before the grid dependency resolves
     int y_ready;              // y may be updated before it resolves
+    float* v_out;             // shrink only: fp32 v rows go here, no expand
+    int ld_v;
     int32_t* status;
 };
 
@@ -205,13 +209,14 @@ struct UnitInfo {
 };
 
 // Unit u -> (group, first position, rows, slot).  Every thread of the CTA
-// takes part; the answer is uniform across the cluster (all CTAs of a
-// cluster map to the same unit).  The group table is read in one parallel
-// round trip (one group per thread, block-wide prefix sum), together with
-// the permutation when it fits in s_perm; larger tables take a serial scan.
-__device__ __forceinline__ UnitInfo find_unit(const FusedParams& p, int u, int* s_perm, bool stage_perm)
+// takes part and the answer is uniform across the CTA (and across a
+// cluster, whose CTAs all map to the same unit).  The group table is read
+// NT groups per round trip (one group per thread, block-wide prefix sum),
+// together with the permutation when it fits in s_perm.
+template <int NT, class Params>
+__device__ __forceinline__ UnitInfo find_unit(const Params& p, int u, int* s_perm, bool stage_perm)
 {
-    __shared__ int s_warp[kWarps];
+    __shared__ int s_warp[NT / 32];
     __shared__ UnitInfo s_info;
     __shared__ int s_bad;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -220,15 +225,17 @@ __device__ __forceinline__ UnitInfo find_unit(const FusedParams& p, int u, int* 
         s_bad = 0;
     }
     if (stage_perm)
-        for (int i = tid; i < p.n_pos; i += kThreads) s_perm[i] = __ldg(p.perm + i);
-    if (p.n_groups <= kThreads) {
+        for (int i = tid; i < p.n_pos; i += NT) s_perm[i] = __ldg(p.perm + i);
+    int base = 0;   // units in the groups of earlier rounds
+    for (int g0 = 0; g0 < p.n_groups; g0 += NT) {
+        const int gi = g0 + tid;
         int s = 0, e = 0, sl = -1;
         bool bad = false;
         int n = 0;
-        if (tid < p.n_groups) {
-            s = __ldg(p.gstarts + tid);
-            e = __ldg(p.gstarts + tid + 1);
-            sl = __ldg(p.gslot + tid);
+        if (gi < p.n_groups) {
+            s = __ldg(p.gstarts + gi);
+            e = __ldg(p.gstarts + gi + 1);
+            sl = __ldg(p.gslot + gi);
             n = group_units(s, e, p.n_pos, bad);
         }
         int incl = n;
@@ -239,14 +246,19 @@ __device__ __forceinline__ UnitInfo find_unit(const FusedParams& p, int u, int* 
         }
         if (lane == 31) s_warp[warp] = incl;
         __syncthreads();
-        int before = 0;
-        for (int w = 0; w < warp; ++w) before += s_warp[w];
-        incl += before;
+        int before = 0, total = 0;
+#pragma unroll
+        for (int w = 0; w < NT / 32; ++w) {
+            const int c = s_warp[w];
+            if (w < warp) before += c;
+            total += c;
+        }
+        incl += base + before;
         const int excl = incl - n;
         if (bad) atomicOr(&s_bad, 1);
-        if (tid < p.n_groups && u >= excl && u < incl) {
+        if (gi < p.n_groups && u >= excl && u < incl) {
             UnitInfo info;
-            info.g = tid;
+            info.g = gi;
             info.pos0 = s + (u - excl) * kRB;
             info.nrows = min(kRB, e - info.pos0);
             info.slot = sl;
@@ -254,29 +266,10 @@ __device__ __forceinline__ UnitInfo find_unit(const FusedParams& p, int u, int* 
             info.bad = 0;
             s_info = info;
         }
-        __syncthreads();
-    } else {
-        __syncthreads();
-        if (tid == 0) {
-            int acc = 0;
-            bool bad = false;
-            for (int i = 0; i < p.n_groups; ++i) {
-                const int s = __ldg(p.gstarts + i), e = __ldg(p.gstarts + i + 1);
-                const int n = group_units(s, e, p.n_pos, bad);
-                if (u < acc + n) {
-                    s_info.g = i;
-                    s_info.pos0 = s + (u - acc) * kRB;
-                    s_info.nrows = min(kRB, e - s_info.pos0);
-                    s_info.slot = __ldg(p.gslot + i);
-                    s_info.found = 1;
-                    break;
-                }
-                acc += n;
-            }
-            s_bad = bad;
-        }
-        __syncthreads();
+        base += total;
+        __syncthreads();   // s_warp is rewritten by the next round
     }
+    if (p.n_groups <= 0) __syncthreads();
     UnitInfo r = s_info;
     r.bad = s_bad;
     return r;
@@ -301,14 +294,14 @@ __host__ __device__ inline size_t align128(size_t v) { return (v + 127) / 128 * 
 
 // sA (the K stages) and sD (the delta tile, fp32) share the first region:
 // sD is written only after every stage has been consumed.
-__host__ __device__ inline SmemLayout smem_layout(int R, int r_slot, int nch_tile, int n_pos)
+__host__ __device__ inline SmemLayout smem_layout(int R, int r_slot, int nch_tile, int n_pos, int stages)
 {
     SmemLayout L;
-    const size_t sa = sizeof(bf16_t) * kStages * R * kLds;
+    const size_t sa = sizeof(bf16_t) * stages * R * kLds;
     const size_t sd = sizeof(float) * kRB * nch_tile * 8;
     L.a = 0;
     L.x = align128(sa > sd ? sa : sd);
-    L.vpart = L.x + align128(sizeof(bf16_t) * kStages * kRB * kLds);
+    L.vpart = L.x + align128(sizeof(bf16_t) * stages * kRB * kLds);
     L.vfull = L.vpart + align128(sizeof(float) * kRB * R);
     L.b = L.vfull + align128(sizeof(float) * kRB * R);
     L.perm = L.b + align128(sizeof(bf16_t) * (nch_tile * 8 * r_slot + kBSlack));
@@ -316,6 +309,7 @@ __host__ __device__ inline SmemLayout smem_layout(int R, int r_slot, int nch_til
     return L;
 }
 
+template <int S>   // K stages in flight
 __global__ void __launch_bounds__(kThreads, 2)
 bgmv_fused_kernel(FusedParams p)
 {
@@ -323,10 +317,10 @@ bgmv_fused_kernel(FusedParams p)
     const int R = p.ps.n_proj * p.ps.r_slot;
     const int r_slot = p.ps.r_slot;
     const int r_pad = p.r_pad;
-    const SmemLayout L = smem_layout(R, r_slot, p.nch_tile, p.n_pos);
-    bf16_t* sA = reinterpret_cast<bf16_t*>(smem + L.a);        // [kStages][R][kLds]
+    const SmemLayout L = smem_layout(R, r_slot, p.nch_tile, p.n_pos, S);
+    bf16_t* sA = reinterpret_cast<bf16_t*>(smem + L.a);        // [S][R][kLds]
     float* sD = reinterpret_cast<float*>(smem + L.a);          // [kRB][nch_tile*8], after the shrink
-    bf16_t* sX = reinterpret_cast<bf16_t*>(smem + L.x);        // [kStages][kRB][kLds]
+    bf16_t* sX = reinterpret_cast<bf16_t*>(smem + L.x);        // [S][kRB][kLds]
     float* vpart = reinterpret_cast<float*>(smem + L.vpart);   // [kRB][R]
     float* vfull = reinterpret_cast<float*>(smem + L.vfull);   // [kRB][R]
     bf16_t* sB = reinterpret_cast<bf16_t*>(smem + L.b);        // [nch_tile*8][r_slot] + slack
@@ -350,7 +344,7 @@ bgmv_fused_kernel(FusedParams p)
     // leaves, so this grid never completes before that one (stream order
     // stays transitive under PDL); status flags are written only after a
     // wait.  Clusters without work leave at once and free their SM slots.
-    const UnitInfo ui = find_unit(p, unit, s_perm, stage_perm);   // uniform across the cluster
+    const UnitInfo ui = find_unit<kThreads>(p, unit, s_perm, stage_perm);   // uniform across the cluster
     const bool bad_group = ui.bad;
     const int pos0 = ui.pos0, nrows = ui.nrows, slot = ui.slot;
     if (!ui.found || slot == -1) {              // nothing to do (or base-only rows)
@@ -377,8 +371,9 @@ bgmv_fused_kernel(FusedParams p)
     const int k_begin = crank * p.kc;
     const int k_end = min(p.h_in, k_begin + p.kc);
     const int n_kt = k_end > k_begin ? (k_end - k_begin + kKT - 1) / kKT : 0;
-    int total_ch = 0;
-    for (int q = 0; q < p.ps.n_proj; ++q) total_ch += p.ps.width[q] >> 3;
+    int total_ch = 0;   // none in the shrink-only form
+    if (!p.v_out)
+        for (int q = 0; q < p.ps.n_proj; ++q) total_ch += p.ps.width[q] >> 3;
     const int q_idx = part * p.cs + crank, q_n = p.n_parts * p.cs;
     const int ch_begin = static_cast<int>((static_cast<long long>(total_ch) * q_idx) / q_n);
     const int ch_end = static_cast<int>((static_cast<long long>(total_ch) * (q_idx + 1)) / q_n);
@@ -454,31 +449,33 @@ bgmv_fused_kernel(FusedParams p)
         __syncthreads();
         copy_B(ch_begin, tile0_end, &s_barB);
     }
-    if (n_kt > 0) copy_A(0, 0);
-    cp_async_commit();
-    if (n_kt > 1) copy_A(1, 1);
-    cp_async_commit();
+#pragma unroll
+    for (int st = 0; st < S; ++st) {
+        if (st < n_kt) copy_A(st, st);
+        cp_async_commit();
+    }
 
     bool waited = false;
     if (!p.x_ready) {
         grid_dep_wait();
         waited = true;
     }
-    if (n_kt > 0) copy_X(0, 0);
-    cp_async_commit();
-    if (n_kt > 1) copy_X(1, 1);
-    cp_async_commit();
+#pragma unroll
+    for (int st = 0; st < S; ++st) {
+        if (st < n_kt) copy_X(st, st);
+        cp_async_commit();
+    }
 
     // ---- shrink: 16 rows x R ranks x this CTA's K range on tensor cores ----
     const int n_tiles = R / 8;                  // 8 ranks per mma tile; <= 16
     bool failed = false;
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     for (int kt = 0; kt < n_kt; ++kt) {
-        // groups so far: {A0} {A1} {X0} {X1} then one per stage; waiting
-        // for all but the newest group leaves exactly stage kt resident
-        cp_async_wait<1>();
+        // groups so far: {A_0}..{A_S-1} {X_0}..{X_S-1}, then one per
+        // iteration; stage kt is complete once at most S-1 groups are pending
+        cp_async_wait<S - 1>();
         __syncthreads();
-        const int buf = kt % kStages;
+        const int buf = kt % S;
         const bf16_t* xs = sX + buf * kRB * kLds;
         const bf16_t* as = sA + buf * R * kLds;
 #pragma unroll
@@ -498,9 +495,9 @@ bgmv_fused_kernel(FusedParams p)
             }
         }
         __syncthreads();                        // every warp is done with this buffer
-        if (kt + kStages < n_kt) {              // refill it with stage kt + kStages
-            copy_A(kt + kStages, buf);
-            copy_X(kt + kStages, buf);
+        if (kt + S < n_kt) {                    // refill it with stage kt + S
+            copy_A(kt + S, buf);
+            copy_X(kt + S, buf);
         }
         cp_async_commit();
     }
@@ -536,7 +533,35 @@ bgmv_fused_kernel(FusedParams p)
         }
         s_any_fail = any;
     }
-    {
+    if (p.v_out) {
+        // Shrink only: the cluster's CTAs share the reduction of the unit's
+        // rows and store v (fp32) for the grouped expand that follows.  The
+        // store waits for the preceding grid, which may still read v.
+        __syncthreads();                        // s_any_fail
+        if (!waited) {
+            grid_dep_wait();
+            waited = true;
+        }
+        const bool ok = s_any_fail == 0;
+        const int n2 = nrows * R / 2;
+        const uint32_t base = smem_u32(vpart);
+        for (int i = crank * kThreads + tid; i < n2; i += kThreads * p.cs) {
+            float2 part2[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                if (c < p.cs) part2[c] = ld_dsmem_f2(map_rank(base + i * 8, c));
+            float2 s = part2[0];
+#pragma unroll
+            for (int c = 1; c < 16; ++c) {
+                if (c < p.cs) {
+                    s.x += part2[c].x;
+                    s.y += part2[c].y;
+                }
+            }
+            const int t = (2 * i) / R, j = 2 * i - t * R;
+            if (ok) *reinterpret_cast<float2*>(p.v_out + static_cast<size_t>(s_rows[t]) * p.ld_v + j) = s;
+        }
+    } else {
         const int n2 = kRB * R / 2;   // all 16 rows: rows past nrows sum to zero
         const uint32_t base = smem_u32(vpart);
         for (int i = tid; i < n2; i += kThreads) {
@@ -660,6 +685,253 @@ bgmv_fused_kernel(FusedParams p)
     cluster_wait();     // peers are done reading this CTA's partials
 }
 
+// ---- grouped expand (second half of the two-launch form) --------------------
+//
+// Wide outputs (more columns than one cluster expands in two tiles) take
+// two launches: the kernel above in its shrink-only form stores fp32 v per
+// decode row, then this kernel streams B' in blocks of kGxCols columns,
+// one CTA per (unit, block), many CTAs per SM.  A block of B'[slot] is
+// contiguous ([columns][r_slot] bf16): each warp's 64 columns land in
+// shared memory with one bulk copy, issued before the grid dependency
+// resolves, and the warp proceeds as soon as its own part has arrived.
+// The y pieces the warp will update are loaded while B' is in flight, so a
+// CTA waits on memory twice, not once per tile.
+//
+// Tensor-core form (mma.sync m16n8k16, fp32 accumulate), transposed so the
+// columns fill M and the rows N: d^T[col][t] = sum_j B'[col][j] v[t][j],
+// 16 columns x 8 rows per tile, v split into bf16 hi + lo as above.  K is
+// permuted: in step (h, e) lane quad q carries ranks 8(q + 4h) + 4e + 0..3
+// of both operands, so each lane reads whole 16-byte pieces of a B' row.
+
+constexpr int kGxThreads = 128;
+constexpr int kGxWarps = kGxThreads / 32;
+constexpr int kGxCols = 256;                          // output columns per block
+constexpr int kGxWarpCols = kGxCols / kGxWarps;       // 64: one bulk copy per warp
+constexpr int kGxTiles = kGxWarpCols / 16;            // 16-column tiles per warp
+constexpr int kGxLdD = 20;       // per-warp delta tile row stride (floats): conflict-free
+
+struct GexParams {
+    ProjSet ps;
+    const float* v;           // [n_rows][ld_v] fp32, projection p at p*r_slot
+    int ld_v;
+    bf16_t* y;
+    int ld_y;
+    const int32_t* perm;
+    const int32_t* gstarts;
+    const int32_t* gslot;
+    int n_groups;
+    int n_pos;
+    int n_slots;
+    int n_rows;
+    int n_blocks;             // column blocks per unit, over all projections
+    int upg;                  // > 0: unit = group * upg + sub (direct form); 0: scanned
+    int32_t* status;
+};
+
+// Column block b -> projection and its first column.
+__device__ __forceinline__ void block_proj(const ProjSet& ps, int b, int& pj, int& col0)
+{
+    pj = 0;
+    int nb = (ps.width[0] + kGxCols - 1) / kGxCols;
+    while (pj < ps.n_proj - 1 && b >= nb) {
+        b -= nb;
+        ++pj;
+        nb = (ps.width[pj] + kGxCols - 1) / kGxCols;
+    }
+    col0 = b * kGxCols;
+}
+
+__device__ __forceinline__ uint4 lds128(const bf16_t* p)
+{
+    return *reinterpret_cast<const uint4*>(p);
+}
+
+__global__ void __launch_bounds__(kGxThreads, 5)
+bgmv_group_expand_kernel(GexParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];   // B' block [ncols][r_slot]
+    __shared__ __align__(16) float s_d[kGxWarps][kRB * kGxLdD];
+    __shared__ __align__(8) uint64_t s_bar[kGxWarps];
+    __shared__ int s_rows[kRB];
+    const bf16_t* sB = reinterpret_cast<const bf16_t*>(smem);
+
+    grid_dep_launch();
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int unit = blockIdx.x / p.n_blocks;
+    const int blk = blockIdx.x - unit * p.n_blocks;
+    int pos0, nrows, slot;
+    bool bad;
+    if (p.upg > 0) {
+        // Direct form: the unit names its group; all threads read the same
+        // three words (one round trip, no block-wide scan).
+        const int g = unit / p.upg, sub = unit - g * p.upg;
+        const int s = __ldg(p.gstarts + g), e = __ldg(p.gstarts + g + 1);
+        slot = __ldg(p.gslot + g);
+        const bool sane = s >= 0 && e <= p.n_pos && s <= e && e - s <= p.upg * kRB;
+        bad = !sane && sub == 0;
+        pos0 = s + sub * kRB;
+        nrows = sane ? min(kRB, e - pos0) : 0;
+    } else {
+        const UnitInfo ui = find_unit<kGxThreads>(p, unit, nullptr, false);
+        bad = ui.bad;
+        pos0 = ui.pos0;
+        nrows = ui.found ? ui.nrows : 0;
+        slot = ui.slot;
+    }
+    const bool flagger = blk == 0 && tid == 0;   // one CTA per unit reports
+    if (nrows <= 0 || slot == -1) {
+        if (blockIdx.x == 0 || bad) grid_dep_wait();
+        if (bad && flagger) flag(p.status, LORA_DEV_BAD_SEGMENT);
+        return;
+    }
+    if (slot < -1 || slot >= p.n_slots) {
+        grid_dep_wait();
+        if (flagger) flag(p.status, LORA_DEV_SLOT_OUT_OF_RANGE);
+        return;
+    }
+    bool bad_row = false;
+    if (tid < kRB) {
+        int r = 0;
+        if (tid < nrows) {
+            r = __ldg(p.perm + pos0 + tid);
+            if (r < 0 || r >= p.n_rows) {
+                bad_row = true;
+                r = 0;
+            }
+        }
+        s_rows[tid] = r;
+    }
+    if (tid < kGxWarps) mbar_init(&s_bar[tid], 1);
+    if (tid == 0) asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    if (__syncthreads_or(bad_row)) {
+        grid_dep_wait();
+        if (flagger) flag(p.status, LORA_DEV_BAD_SEGMENT);
+        return;
+    }
+
+    int pj, col0;
+    block_proj(p.ps, blk, pj, col0);
+    const int width = p.ps.width[pj];
+    const int ncols = min(kGxCols, width - col0);          // a multiple of 8
+    const int r_slot = p.ps.r_slot;
+    const int wc0 = warp * kGxWarpCols;                    // this warp's first column in the block
+    const int wcols = max(0, min(kGxWarpCols, ncols - wc0));
+    if (wcols > 0 && lane == 0) {   // weights first: they do not depend on the preceding kernel
+        const unsigned bytes = static_cast<unsigned>(wcols * r_slot * sizeof(bf16_t));
+        mbar_expect(&s_bar[warp], bytes);
+        bulk_g2s(smem + sizeof(bf16_t) * wc0 * r_slot,
+                 p.ps.B[pj] + (static_cast<size_t>(slot) * width + col0 + wc0) * r_slot, bytes, &s_bar[warp]);
+    }
+
+    grid_dep_wait();   // v is the preceding kernel's output; y may be too
+    if (wcols == 0) return;
+
+    // y pieces this lane updates (tile i, row lane/2, columns 8*(lane&1)..+7),
+    // loaded now so they arrive together with B'
+    const int yt = lane >> 1, yh = lane & 1;
+    bf16_t* yrow = p.y + static_cast<size_t>(s_rows[yt]) * p.ld_y + p.ps.out_off[pj] + col0;
+    uint4 yv[kGxTiles];
+#pragma unroll
+    for (int i = 0; i < kGxTiles; ++i) {
+        const int c = wc0 + i * 16 + yh * 8;
+        yv[i] = (yt < nrows && c < ncols) ? *reinterpret_cast<const uint4*>(yrow + c) : make_uint4(0, 0, 0, 0);
+    }
+
+    // v fragments (the mma B operand), n-tile nt = rows 8nt..8nt+7:
+    // b0 <- v[t][k0], v[t][k0+1]; b1 <- v[t][k0+2], v[t][k0+3], k0 = 8(q+4h)+4e.
+    const int g = lane >> 2, q = lane & 3;
+    const int n_nt = (nrows + 7) / 8;
+    const int np = r_slot / 8;              // 16-byte pieces per B' row
+    const int H = (np + 3) / 4;             // pieces per lane
+    uint32_t bh[2][2][2][2], bl[2][2][2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int t = nt * 8 + g, k0 = 8 * (q + 4 * h) + 4 * e;
+                float4 vv = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (nt < n_nt && t < nrows && k0 < r_slot)
+                    vv = *reinterpret_cast<const float4*>(p.v + static_cast<size_t>(s_rows[t]) * p.ld_v +
+                                                          pj * r_slot + k0);
+                split_hi_lo(vv.x, vv.y, bh[nt][h][e][0], bl[nt][h][e][0]);
+                split_hi_lo(vv.z, vv.w, bh[nt][h][e][1], bl[nt][h][e][1]);
+            }
+
+    if (!mbar_wait(&s_bar[warp], 0)) {
+        // This warp's block never landed: wait once more (bounded) so no copy
+        // is in flight into shared memory when the CTA leaves, then report.
+        mbar_wait(&s_bar[warp], 0);
+        if (lane == 0) flag(p.status, LORA_DEV_TIMEOUT);
+        return;
+    }
+
+    // Odd rows read their second piece first when a lane holds two (rows
+    // 128 bytes apart would otherwise meet in the same banks).
+    const int swap = (H == 2) ? (g & 1) : 0;
+    float* sd = s_d[warp];
+#pragma unroll
+    for (int i = 0; i < kGxTiles; ++i) {
+        const int m0 = wc0 + i * 16;
+        if (m0 >= ncols) break;
+        const int ca = m0 + g, cb = ca + 8;
+        uint4 La[2], Lb[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int piece = q + 4 * (j ^ swap);
+            const bool okp = (j ^ swap) < H && piece < np;
+            La[j] = (okp && ca < ncols) ? lds128(sB + ca * r_slot + piece * 8) : make_uint4(0, 0, 0, 0);
+            Lb[j] = (okp && cb < ncols) ? lds128(sB + cb * r_slot + piece * 8) : make_uint4(0, 0, 0, 0);
+        }
+        const uint4 Pa0 = swap ? La[1] : La[0], Pa1 = swap ? La[0] : La[1];
+        const uint4 Pb0 = swap ? Lb[1] : Lb[0], Pb1 = swap ? Lb[0] : Lb[1];
+        float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (h < H) {
+                const uint4 A = h ? Pa1 : Pa0, B = h ? Pb1 : Pb0;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const uint32_t a0 = e ? A.z : A.x, a2 = e ? A.w : A.y;
+                    const uint32_t a1 = e ? B.z : B.x, a3 = e ? B.w : B.y;
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        if (nt < n_nt) {
+                            mma_bf16_16816(d[nt], a0, a1, a2, a3, bh[nt][h][e][0], bh[nt][h][e][1]);
+                            mma_bf16_16816(d[nt], a0, a1, a2, a3, bl[nt][h][e][0], bl[nt][h][e][1]);
+                        }
+                    }
+                }
+            }
+        }
+        // d[nt]: (column g, rows 8nt+2q, +1) and (column g+8, same rows)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            if (nt < n_nt) {
+                const int t = nt * 8 + 2 * q;
+                sd[t * kGxLdD + g] = d[nt][0];
+                sd[(t + 1) * kGxLdD + g] = d[nt][1];
+                sd[t * kGxLdD + g + 8] = d[nt][2];
+                sd[(t + 1) * kGxLdD + g + 8] = d[nt][3];
+            }
+        }
+        __syncwarp();
+        {
+            const int c = m0 + yh * 8;
+            if (yt < nrows && c < ncols) {
+                const float4* dp = reinterpret_cast<const float4*>(sd + yt * kGxLdD + yh * 8);
+                const float4 d0 = dp[0], d1 = dp[1];
+                const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+                *reinterpret_cast<uint4*>(yrow + c) = add_round8(yv[i], dd);
+            }
+        }
+        __syncwarp();
+    }
+    if (bad && flagger) flag(p.status, LORA_DEV_BAD_SEGMENT);
+}
+
 int env_int(const char* name, int dflt)
 {
     const char* e = std::getenv(name);
@@ -677,18 +949,23 @@ bool fused_decode_supported(int n_proj, int r_slot)
 cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
                               const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
                               int n_pos, int max_group_len, int n_rows, int n_slots, unsigned flags,
-                              int32_t* status, cudaStream_t stream)
+                              float* v_ws, int32_t* status, cudaStream_t stream)
 {
     if (n_pos <= 0 || n_groups <= 0) return cudaSuccess;
     const int R = ps.n_proj * ps.r_slot;
     static int configured_device = -1;
+    static int n_sms = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(bgmv_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(bgmv_fused_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        for (auto fn : {bgmv_fused_kernel<kStages>, bgmv_fused_kernel<kStagesShrink>}) {
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
+        e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
@@ -698,7 +975,8 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     int cs = 1;
     const int cs_max = h_in >= 8192 ? 16 : 8;
     while (cs < cs_max && h_in / (cs * 2) >= kKT) cs *= 2;
-    cs = env_int("LORA_FUSED_CS", cs);
+    const int cs_env = env_int("LORA_FUSED_CS", 0);
+    if (cs_env > 0) cs = cs_env;
     // Units of <= 16 rows: at most ceil(longest group / 16) per group.
     int max_units = n_groups + n_pos / kRB;
     if (max_group_len > 0) max_units = min(max_units, n_groups * ((max_group_len + kRB - 1) / kRB));
@@ -709,9 +987,26 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     // each CTA expands at most two tiles of kMaxChunks chunks.
     int parts = 1;
     while (parts < 8 && (total_ch + cs * parts - 1) / (cs * parts) > 2 * kMaxChunks) parts *= 2;
+    // Wider than that (and with a workspace for v): two launches, the
+    // shrink-only form of this kernel and the grouped expand.
+    // So do calls that stream many weights (the one-launch form keeps only
+    // two K stages in flight per CTA and expands in the same CTAs).
+    const double weight_bytes =
+        static_cast<double>(n_groups) * sizeof(bf16_t) * (static_cast<double>(R) * h_in + 8.0 * total_ch * ps.r_slot);
+    int split = env_int("LORA_FUSED_SPLIT", -1);
+    if (split < 0) split = (parts > 1 || weight_bytes >= kSplitWeightBytes) ? 1 : 0;
+    if (!v_ws) split = 0;
+    if (split) {
+        // The shrink-only clusters only need to cover the SMs once: fewer
+        // CTAs per unit each stream a longer K range through more stages.
+        parts = 1;
+        cs = 1;
+        while (cs < 16 && static_cast<long long>(max_units) * cs < n_sms && h_in / (cs * 2) >= kKT) cs *= 2;
+        if (cs_env > 0) cs = cs_env;
+    }
     parts = env_int("LORA_FUSED_PARTS", parts);
     const int per_cta = (total_ch + cs * parts - 1) / (cs * parts);
-    const int nch_tile = min(kMaxChunks, max(1, per_cta));
+    const int nch_tile = split ? 1 : min(kMaxChunks, max(1, per_cta));
 
     FusedParams p{};
     p.ps = ps;
@@ -734,12 +1029,16 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     p.r_pad = (ps.r_slot + 15) / 16 * 16;
     p.x_ready = (flags & LORA_APPLY_X_READY) ? 1 : 0;
     p.y_ready = (flags & LORA_APPLY_Y_READY) ? 1 : 0;
+    p.v_out = split ? v_ws : nullptr;
+    p.ld_v = R;
     p.status = status;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(max_units * parts * cs));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem_layout(R, ps.r_slot, nch_tile, n_pos).total;
+    const int stages = (split && env_int("LORA_SHRINK_STAGES", kStagesShrink) == kStagesShrink) ? kStagesShrink
+                                                                                                : kStages;
+    cfg.dynamicSmemBytes = smem_layout(R, ps.r_slot, nch_tile, n_pos, stages).total;
     cfg.stream = stream;
     cudaLaunchAttribute attrs[2];
     int na = 0;
@@ -755,7 +1054,45 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     }
     cfg.attrs = attrs;
     cfg.numAttrs = na;
-    e = cudaLaunchKernelEx(&cfg, bgmv_fused_kernel, p);
+    e = stages == kStagesShrink ? cudaLaunchKernelEx(&cfg, bgmv_fused_kernel<kStagesShrink>, p)
+                                : cudaLaunchKernelEx(&cfg, bgmv_fused_kernel<kStages>, p);
+    note_launch();
+    if (e != cudaSuccess || !split) return e;
+
+    GexParams gp{};
+    gp.ps = ps;
+    gp.v = v_ws;
+    gp.ld_v = R;
+    gp.y = y;
+    gp.ld_y = ld_y;
+    gp.perm = perm;
+    gp.gstarts = gstarts;
+    gp.gslot = gslot;
+    gp.n_groups = n_groups;
+    gp.n_pos = n_pos;
+    gp.n_slots = n_slots;
+    gp.n_rows = n_rows;
+    for (int q = 0; q < ps.n_proj; ++q) gp.n_blocks += (ps.width[q] + kGxCols - 1) / kGxCols;
+    gp.status = status;
+    // Direct unit numbering (group, sub-unit) unless the longest group makes
+    // that grid much larger than the scanned one.
+    const long long upg = max_group_len > 0 ? (max_group_len + kRB - 1) / kRB : 0;
+    const long long scanned_units = n_groups + n_pos / kRB;
+    gp.upg = (upg > 0 && n_groups * upg <= 2 * scanned_units) ? static_cast<int>(upg) : 0;
+    const long long units = gp.upg ? n_groups * upg : max_units;
+    const long long n_ctas = units * gp.n_blocks;
+    if (n_ctas > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t gcfg = {};
+    gcfg.gridDim = dim3(static_cast<unsigned>(n_ctas));
+    gcfg.blockDim = dim3(kGxThreads);
+    gcfg.dynamicSmemBytes = sizeof(bf16_t) * kGxCols * ps.r_slot;   // <= 32 KB
+    gcfg.stream = stream;
+    cudaLaunchAttribute gattr;
+    gattr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    gattr.val.programmaticStreamSerializationAllowed = 1;
+    gcfg.attrs = &gattr;
+    gcfg.numAttrs = (flags & LORA_APPLY_NO_PDL) ? 0 : 1;
+    e = cudaLaunchKernelEx(&gcfg, bgmv_group_expand_kernel, gp);
     note_launch();
     return e;
 }

@@ -37,10 +37,12 @@ cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const b
 bool fused_decode_supported(int n_proj, int r_slot);
 
 // Decode rows in gather form (perm / gstarts / gslot over n_pos positions):
-// shrink + cluster reduction + expand in one launch, no workspace.
+// shrink + cluster reduction + expand in one launch.  Outputs too wide for
+// one launch's clusters take two when v_ws ([n_rows][n_proj*r_slot] fp32)
+// is given: the shrink-only form stores v there, a grouped expand follows.
 cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
                               const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
                               int n_pos, int max_group_len, int n_rows, int n_slots, unsigned flags,
-                              int32_t* status, cudaStream_t stream);
+                              float* v_ws, int32_t* status, cudaStream_t stream);
 
 }  // namespace lora

@@ -371,6 +371,53 @@ def test_apply_decode_fused_shapes(h_in, widths, rank, T, n_slots):
     check_bf16(got, oracle_group(wl, "g"), wl.ids, wl.y["g"], f"fused h_in={h_in} R={rank * len(widths)}")
 
 
+@pytest.mark.parametrize("h_in,widths,rank,T,n_slots,n_prefill", [
+    (1024, (2056, 520), 8, 30, 3, 0),        # ragged last column block in both projections; rank 8
+    (512, (4096, 256, 264), 24, 70, 2, 0),   # three pieces of 16 bytes per B' row; >16 rows per adapter
+    (2048, (1536,), 40, 45, 4, 0),           # rank 40: the second piece of each lane half empty
+    (8192, (3072, 3072), 64, 26, 5, 0),      # rank 64: two pieces per lane, odd rows swapped
+    (256, (256, 64, 64), 16, 50, 3, 20),     # prefill rows (row-wise route) before the decode rows
+])
+def test_apply_decode_two_launch_form(h_in, widths, rank, T, n_slots, n_prefill, monkeypatch):
+    """The shrink-only grouped kernel followed by the grouped expand (the
+    form wide outputs take), forced on for shapes that span its edge cases."""
+    monkeypatch.setenv("LORA_FUSED_SPLIT", "1")
+    rng = np.random.default_rng(h_in + T + rank)
+    ids = rng.integers(-1, n_slots, T).astype(np.int32)
+    wl = _small(ids, n_prefill, n_slots=n_slots, rank=rank, h_in=h_in, widths=widths, seed=T)
+    got = _run_apply(wl, "g")
+    check_bf16(got, oracle_group(wl, "g"), wl.ids, wl.y["g"], f"split h_in={h_in} r={rank}")
+
+
+@pytest.mark.parametrize("flags", [0, abi.LORA_APPLY_X_READY, abi.LORA_APPLY_NO_PDL])
+def test_two_launch_form_chained_calls_share_workspace(flags, monkeypatch):
+    """Back-to-back calls on one workspace: each call's shrink stores v only
+    after the previous call's expand has finished reading it."""
+    monkeypatch.setenv("LORA_FUSED_SPLIT", "1")
+    rng = np.random.default_rng(7)
+    ids = rng.integers(-1, 4, 40).astype(np.int32)
+    wl = _small(ids, 0, n_slots=4, rank=16, h_in=1024, widths=(2048, 512), seed=3)
+    st = store.GroupStore.from_workload(wl, "g")
+    meta = store.BatchMeta(wl.ids, 0, wl.n_slots)
+    # distinct inputs per call (rows rotated), so a call that stored v too
+    # early would change another call's output
+    xs = [to_dev(np.roll(wl.x["g"], i, axis=0)) for i in range(6)]
+    refs = []
+    for xx in xs:
+        yy = to_dev(wl.y["g"])
+        store.apply(yy, xx, st, meta, store.workspace_for(wl.n_rows, 2, wl.r_slot))
+        torch.cuda.synchronize()
+        refs.append(to_host(yy))
+    ws = store.workspace_for(wl.n_rows, 2, wl.r_slot)
+    ys = [to_dev(wl.y["g"]) for _ in range(6)]
+    for xx, yy in zip(xs, ys):
+        store.apply(yy, xx, st, meta, ws, flags=flags)
+    torch.cuda.synchronize()
+    for yy, ref in zip(ys, refs):
+        np.testing.assert_array_equal(to_host(yy), ref)
+    check_bf16(refs[0], oracle_group(wl, "g"), wl.ids, wl.y["g"], "chained")
+
+
 def test_apply_decode_bad_permutation_flagged():
     """A corrupted gather permutation is flagged and its group's rows skipped."""
     ids = np.array([0, 1, 0, 1, 0, 1], np.int32)
