@@ -282,13 +282,21 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
     }
     if (D > 0) {
         const bool gathered = meta->perm && meta->gseg_starts && meta->gseg_slot && meta->n_gsegs > 0;
-        if (gathered && lora::fused_decode_supported(n_proj, r_slot)) {
-            // One launch over the decode rows grouped by adapter (cluster
-            // split-K): the BGMV route for r_slot <= LORA_BGMV_MAX_RANK, and
-            // the SGMV-over-gather-groups route above it (same grouping).
+        const bool fused_ok = gathered && lora::fused_decode_supported(n_proj, r_slot);
+        const bool grouped_ok = gathered && r_slot <= 64;
+        // Decode rows grouped by adapter: the BGMV route for r_slot <=
+        // LORA_BGMV_MAX_RANK and the SGMV-over-gather-groups route above it
+        // share one grouping.  One launch (cluster split-K) for small calls;
+        // two (grouped shrink, grouped expand) for wide or weight-heavy ones.
+        if (grouped_ok && (!fused_ok || lora::decode_two_launch(ps, h_in, meta->n_gsegs))) {
+            LORA_TRY(cuda_status(lora::launch_bgmv_grouped(y, ld_y, x, ld_x, h_in, ps, meta->perm,
+                                                           meta->gseg_starts, meta->gseg_slot, meta->n_gsegs, D,
+                                                           meta->max_gseg_len, T, n_slots, flags, v, dev_status,
+                                                           s)));
+        } else if (fused_ok) {
             LORA_TRY(cuda_status(lora::launch_bgmv_fused(y, ld_y, x, ld_x, h_in, ps, meta->perm,
                                                          meta->gseg_starts, meta->gseg_slot, meta->n_gsegs,
-                                                         D, meta->max_gseg_len, T, n_slots, flags, v,
+                                                         D, meta->max_gseg_len, T, n_slots, flags,
                                                          dev_status, s)));
         } else {
             RowMap m = r_slot <= LORA_BGMV_MAX_RANK

@@ -1,6 +1,8 @@
 // launch.h -- internal kernel launchers (C++; not part of the C ABI).
 #pragma once
 
+#include <cstdlib>
+
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -9,6 +11,13 @@ namespace lora {
 
 // Counts every kernel launch the library issues (see lora_kernel_launch_count).
 void note_launch();
+
+// Integer tuning override from the environment (dflt when unset or empty).
+inline int env_int(const char* name, int dflt)
+{
+    const char* e = std::getenv(name);
+    return (e && *e) ? std::atoi(e) : dflt;
+}
 
 // One position per CTA, CUDA cores: v[row][p*r_slot + j] = A_p[slot][j] . x[row].
 cudaError_t launch_shrink_rowwise(float* v, int ld_v, const bf16_t* x, int ld_x, int h_in,
@@ -37,12 +46,21 @@ cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const b
 bool fused_decode_supported(int n_proj, int r_slot);
 
 // Decode rows in gather form (perm / gstarts / gslot over n_pos positions):
-// shrink + cluster reduction + expand in one launch.  Outputs too wide for
-// one launch's clusters take two when v_ws ([n_rows][n_proj*r_slot] fp32)
-// is given: the shrink-only form stores v there, a grouped expand follows.
+// shrink + cluster reduction + expand in one launch, no workspace.
 cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
                               const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
                               int n_pos, int max_group_len, int n_rows, int n_slots, unsigned flags,
-                              float* v_ws, int32_t* status, cudaStream_t stream);
+                              int32_t* status, cudaStream_t stream);
+
+// Whether a decode call takes the two-launch form (wide outputs, or many
+// weight bytes streamed per call) rather than the one-launch kernel.
+bool decode_two_launch(const ProjSet& ps, int h_in, int n_groups);
+
+// The same rows in two launches: a grouped shrink that stores fp32 v in
+// v_ws ([n_rows][n_proj*r_slot]), then a grouped expand that streams B'.
+cudaError_t launch_bgmv_grouped(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
+                                const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
+                                int n_pos, int max_group_len, int n_rows, int n_slots, unsigned flags,
+                                float* v_ws, int32_t* status, cudaStream_t stream);
 
 }  // namespace lora

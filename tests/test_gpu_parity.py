@@ -371,29 +371,45 @@ def test_apply_decode_fused_shapes(h_in, widths, rank, T, n_slots):
     check_bf16(got, oracle_group(wl, "g"), wl.ids, wl.y["g"], f"fused h_in={h_in} R={rank * len(widths)}")
 
 
-@pytest.mark.parametrize("h_in,widths,rank,T,n_slots,n_prefill", [
-    (1024, (2056, 520), 8, 30, 3, 0),        # ragged last column block in both projections; rank 8
-    (512, (4096, 256, 264), 24, 70, 2, 0),   # three pieces of 16 bytes per B' row; >16 rows per adapter
-    (2048, (1536,), 40, 45, 4, 0),           # rank 40: the second piece of each lane half empty
-    (8192, (3072, 3072), 64, 26, 5, 0),      # rank 64: two pieces per lane, odd rows swapped
-    (256, (256, 64, 64), 16, 50, 3, 20),     # prefill rows (row-wise route) before the decode rows
+@pytest.mark.parametrize("h_in,widths,rank,T,n_slots,n_prefill,ks", [
+    (1024, (2056, 520), 8, 30, 3, 0, None),       # ragged last column block in both projections; rank 8
+    (512, (4096, 256, 264), 24, 70, 2, 0, None),  # three pieces of 16 bytes per B' row; >16 rows per adapter
+    (2048, (1536,), 40, 45, 4, 0, None),          # rank 40: the second piece of each lane half empty
+    (8192, (3072, 3072), 64, 26, 5, 0, None),     # rank 64: two pieces per lane, odd rows swapped
+    (256, (256, 64, 64), 16, 50, 3, 20, None),    # prefill rows (row-wise route) before the decode rows
+    (1032, (512,), 16, 30, 3, 0, None),           # K ends 8 elements into a stage: ragged last k-step
+    (4104, (1024, 1024), 32, 40, 6, 0, 4),        # K split over a 4-CTA cluster, ragged in the last CTA
+    (3072, (512, 512, 512), 16, 33, 4, 0, 2),     # 48 ranks: three 16-rank blocks, 2-CTA clusters
 ])
-def test_apply_decode_two_launch_form(h_in, widths, rank, T, n_slots, n_prefill, monkeypatch):
-    """The shrink-only grouped kernel followed by the grouped expand (the
-    form wide outputs take), forced on for shapes that span its edge cases."""
-    monkeypatch.setenv("LORA_FUSED_SPLIT", "1")
+def test_apply_decode_two_launch_form(h_in, widths, rank, T, n_slots, n_prefill, ks, monkeypatch):
+    """The grouped shrink followed by the grouped expand (the form wide or
+    weight-heavy calls take), forced on for shapes that span its edge cases."""
+    monkeypatch.setenv("LORA_DECODE_TWO_LAUNCH", "1")
+    if ks:
+        monkeypatch.setenv("LORA_GROUPED_KS", str(ks))
     rng = np.random.default_rng(h_in + T + rank)
     ids = rng.integers(-1, n_slots, T).astype(np.int32)
     wl = _small(ids, n_prefill, n_slots=n_slots, rank=rank, h_in=h_in, widths=widths, seed=T)
     got = _run_apply(wl, "g")
-    check_bf16(got, oracle_group(wl, "g"), wl.ids, wl.y["g"], f"split h_in={h_in} r={rank}")
+    check_bf16(got, oracle_group(wl, "g"), wl.ids, wl.y["g"], f"two-launch h_in={h_in} r={rank}")
+
+
+def test_two_launch_form_skewed_groups(monkeypatch):
+    """One adapter with 100 rows beside 30 with one row each: units are
+    numbered by the block-wide scan instead of (group, sub-unit)."""
+    monkeypatch.setenv("LORA_DECODE_TWO_LAUNCH", "1")
+    rng = np.random.default_rng(11)
+    ids = rng.permutation(np.concatenate([np.zeros(100), np.arange(1, 31)])).astype(np.int32)
+    wl = _small(ids, 0, n_slots=31, rank=16, h_in=1024, widths=(1024,), seed=5)
+    got = _run_apply(wl, "g")
+    check_bf16(got, oracle_group(wl, "g"), wl.ids, wl.y["g"], "skewed groups")
 
 
 @pytest.mark.parametrize("flags", [0, abi.LORA_APPLY_X_READY, abi.LORA_APPLY_NO_PDL])
 def test_two_launch_form_chained_calls_share_workspace(flags, monkeypatch):
     """Back-to-back calls on one workspace: each call's shrink stores v only
     after the previous call's expand has finished reading it."""
-    monkeypatch.setenv("LORA_FUSED_SPLIT", "1")
+    monkeypatch.setenv("LORA_DECODE_TWO_LAUNCH", "1")
     rng = np.random.default_rng(7)
     ids = rng.integers(-1, 4, 40).astype(np.int32)
     wl = _small(ids, 0, n_slots=4, rank=16, h_in=1024, widths=(2048, 512), seed=3)
