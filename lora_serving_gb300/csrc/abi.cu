@@ -291,8 +291,8 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
         if (grouped_ok && (!fused_ok || lora::decode_two_launch(ps, h_in, meta->n_gsegs))) {
             LORA_TRY(cuda_status(lora::launch_bgmv_grouped(y, ld_y, x, ld_x, h_in, ps, meta->perm,
                                                            meta->gseg_starts, meta->gseg_slot, meta->n_gsegs, D,
-                                                           meta->max_gseg_len, T, n_slots, flags, v, dev_status,
-                                                           s)));
+                                                           meta->max_gseg_len, T, n_slots, flags, vh, vl,
+                                                           dev_status, s)));
         } else if (fused_ok) {
             LORA_TRY(cuda_status(lora::launch_bgmv_fused(y, ld_y, x, ld_x, h_in, ps, meta->perm,
                                                          meta->gseg_starts, meta->gseg_slot, meta->n_gsegs,

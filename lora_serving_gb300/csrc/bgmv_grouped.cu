@@ -12,18 +12,21 @@
 // Grouped shrink: one CTA per (unit, block of 16 ranks) -- optionally a
 // cluster of CTAs splitting K -- computes
 //   v[t][j] = sum_k A_slot[j][k] x[t][k]      (fp32, mma.sync m16n8k16)
-// for the unit's rows t.  Each stage brings 512 K-elements of every one of
-// its 16 A rows and of the unit's x rows by 16-byte cp.async, a warp per
-// 512 contiguous bytes, into padded shared-memory rows (pitch 1040 bytes,
-// so ldmatrix is conflict-free), four stages deep.  (Bulk copies of 1 KB
-// pieces reach well under half the bandwidth of this form on GB300; bulk
-// copies pay off from about 4 KB, as in the expand below.)  Partial sums of the eight warps (and of the cluster's CTAs)
-// are added in a fixed order: the result does not depend on timing.
+// for the unit's rows t, with the ranks as the mma M and the rows as N (a
+// unit of <= 8 rows costs one mma per 16 ranks x 16 K).  Each stage brings
+// 512 K-elements of every one of its 16 A rows and of the unit's x rows by
+// 16-byte cp.async, a warp per 512 contiguous bytes, into padded shared
+// rows (pitch 1040 bytes, so ldmatrix is conflict-free), four stages deep.
+// (Bulk copies of 1 KB pieces reach well under half the bandwidth of this
+// form on GB300; bulk copies pay off from about 4 KB, as in the expand
+// below.)  Partial sums of the eight warps (and of the cluster's CTAs) are
+// added in a fixed order: the result does not depend on timing.
 //
 // Grouped expand: one CTA per (unit, block of 256 output columns); each warp
 // brings its 64 columns of B' (contiguous in [columns][r_slot] storage) with
-// one bulk copy issued before the grid dependency resolves, loads the y
-// pieces it will update while B' is in flight, and forms
+// one bulk copy, requested as soon as the adapter slot is known (before the
+// rows and the grid dependency resolve), loads the y pieces it will update
+// while B' is in flight, and forms
 //   d^T[col][t] = sum_j B'[col][j] (v_hi + v_lo)[t][j],   y <- bf16_rne(y + d)
 // with v split into bf16 hi and lo parts (v itself is never rounded to one
 // bf16; the split carries it to ~2^-17 relative).
@@ -105,8 +108,10 @@ struct GsParams {
     const bf16_t* x;
     int ld_x;
     int h_in;
-    float* v;                 // [n_rows][ld_v] fp32, projection p at p*r_slot
-    int ld_v;
+    bf16_t* vh;               // v = vh + vl: bf16 planes [n_rows][ld_p], projection p at p*r_pad64
+    bf16_t* vl;
+    int ld_p;
+    int r_pad64;
     const int32_t* perm;
     const int32_t* gstarts;
     const int32_t* gslot;
@@ -162,12 +167,6 @@ bgmv_group_shrink_kernel(GsParams p)
         if (flagger) flag(p.status, LORA_DEV_BAD_SEGMENT);
         return;
     }
-    if (__syncthreads_or(unit_rows(p.perm, pos0, nrows, p.n_rows, s_rows))) {
-        grid_dep_wait();   // same rows in every CTA of the cluster: all leave here
-        if (flagger) flag(p.status, LORA_DEV_BAD_SEGMENT);
-        return;
-    }
-
     const int R = p.ps.n_proj * p.ps.r_slot, r_slot = p.ps.r_slot;
     const int j0 = rb * kGsRanks, nj = min(kGsRanks, R - j0);   // 8 or 16
     const int k_begin = crank * p.kc;
@@ -180,7 +179,6 @@ bgmv_group_shrink_kernel(GsParams p)
     // k_end, and x rows past the unit's, are zero-filled.
     const int c16 = tid & 63, r4 = tid >> 6;
     const bf16_t* a_src[4];
-    const bf16_t* x_src[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int row = r4 + 4 * i;
@@ -193,7 +191,6 @@ bgmv_group_shrink_kernel(GsParams p)
             }
             a_src[i] = p.ps.A[pj] + (static_cast<size_t>(slot) * r_slot + jj) * p.h_in + k_begin + c16 * 8;
         }
-        x_src[i] = row < nrows ? p.x + static_cast<size_t>(s_rows[row]) * p.ld_x + k_begin + c16 * 8 : nullptr;
     }
     auto issue_A = [&](int kt, int b) {
         const int off = kt * kGsKT;
@@ -205,6 +202,27 @@ bgmv_group_shrink_kernel(GsParams p)
                 cp_async16(smem_u32(sA + (b * kGsRanks + row) * kGsPitch + c16 * 16), ok ? a_src[i] + off : p.x, ok);
         }
     };
+    // Weights first: A for the first stages is requested as soon as the
+    // slot is known, before the rows are resolved and before the grid
+    // dependency resolves.
+#pragma unroll
+    for (int st = 0; st < kGsStages; ++st) {
+        if (st < n_kt) issue_A(st, st);
+        cp_async_commit();
+    }
+
+    if (__syncthreads_or(unit_rows(p.perm, pos0, nrows, p.n_rows, s_rows))) {
+        cp_async_wait<0>();   // no copy may land after the CTA has left
+        grid_dep_wait();      // same rows in every CTA of the cluster: all leave here
+        if (flagger) flag(p.status, LORA_DEV_BAD_SEGMENT);
+        return;
+    }
+    const bf16_t* x_src[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int row = r4 + 4 * i;
+        x_src[i] = row < nrows ? p.x + static_cast<size_t>(s_rows[row]) * p.ld_x + k_begin + c16 * 8 : nullptr;
+    }
     auto issue_X = [&](int kt, int b) {
         const int off = kt * kGsKT;
         const bool ok = k_begin + off + c16 * 8 < k_end;
@@ -217,14 +235,7 @@ bgmv_group_shrink_kernel(GsParams p)
             }
         }
     };
-
-    // Weights first: A for the first stages streams in before the grid
-    // dependency resolves; x follows it unless the caller says x is ready.
-#pragma unroll
-    for (int st = 0; st < kGsStages; ++st) {
-        if (st < n_kt) issue_A(st, st);
-        cp_async_commit();
-    }
+    // x follows the grid dependency unless the caller says x is ready.
     bool waited = false;
     if (!p.x_ready) {
         grid_dep_wait();
@@ -237,9 +248,13 @@ bgmv_group_shrink_kernel(GsParams p)
     }
 
     // ---- K loop: warp w takes k-steps w, w+8, ... of each stage ----
+    // Transposed tile: the 16 ranks fill the mma M, the unit's rows the N
+    // (8 per n-tile), so units of <= 8 rows take one mma per k-step.
+    //   d[nt][0..1] = (rank g, rows 8nt+2q, +1), d[nt][2..3] = (rank g+8, same rows)
+    const int n_nt = (nrows + 7) / 8;
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     const int mi = lane >> 3, mr = lane & 7;
-    const int xrow = min((mi & 1) * 8 + mr, p.xr - 1);   // rows past the unit's are never stored
+    const int arow = (mi & 1) * 8 + mr;                // rank row of this lane's ldmatrix address
     const int l16 = lane & 15;
     for (int kt = 0; kt < n_kt; ++kt) {
         // groups so far: {A_0}..{A_S-1} {X_0}..{X_S-1}, then one per
@@ -252,13 +267,13 @@ bgmv_group_shrink_kernel(GsParams p)
         const unsigned char* as = sA + b * kGsRanks * kGsPitch;
         for (int ks = warp; ks < n_ks; ks += kGsWarps) {
             uint32_t a0, a1, a2, a3;
-            ldmatrix_x4(smem_u32(xs + xrow * kGsPitch + (ks * 16 + (mi >> 1) * 8) * 2), a0, a1, a2, a3);
+            ldmatrix_x4(smem_u32(as + arow * kGsPitch + (ks * 16 + (mi >> 1) * 8) * 2), a0, a1, a2, a3);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-                if (nt * 8 < nj) {
+                if (nt < n_nt) {
                     uint32_t b0, b1;
-                    ldmatrix_x2(smem_u32(as + (nt * 8 + (l16 & 7)) * kGsPitch + (ks * 16 + (l16 >> 3) * 8) * 2), b0,
-                                b1);
+                    const int xrow = min(nt * 8 + (l16 & 7), p.xr - 1);   // rows past the unit's: never stored
+                    ldmatrix_x2(smem_u32(xs + xrow * kGsPitch + (ks * 16 + (l16 >> 3) * 8) * 2), b0, b1);
                     mma_bf16_16816(acc[nt], a0, a1, a2, a3, b0, b1);
                 }
             }
@@ -275,14 +290,15 @@ bgmv_group_shrink_kernel(GsParams p)
 
     // ---- fixed-order reduction over the warps, then over the cluster ----
     {
-        const int gr = lane >> 2, q2 = (lane & 3) * 2;
-        float* rw = red + warp * kRB * kGsRanks;
+        const int g = lane >> 2, q2 = (lane & 3) * 2;
+        float* rw = red + warp * kRB * kGsRanks;   // [row t][rank j]
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            rw[gr * kGsRanks + nt * 8 + q2] = acc[nt][0];
-            rw[gr * kGsRanks + nt * 8 + q2 + 1] = acc[nt][1];
-            rw[(gr + 8) * kGsRanks + nt * 8 + q2] = acc[nt][2];
-            rw[(gr + 8) * kGsRanks + nt * 8 + q2 + 1] = acc[nt][3];
+            const int t = nt * 8 + q2;
+            rw[t * kGsRanks + g] = acc[nt][0];
+            rw[(t + 1) * kGsRanks + g] = acc[nt][1];
+            rw[t * kGsRanks + g + 8] = acc[nt][2];
+            rw[(t + 1) * kGsRanks + g + 8] = acc[nt][3];
         }
     }
     __syncthreads();
@@ -294,8 +310,16 @@ bgmv_group_shrink_kernel(GsParams p)
     }
     if (!waited) grid_dep_wait();   // v may still be read by the preceding grid
     const int t = tid >> 4, j = tid & 15;
+    // v (fp32) is stored split: vh = bf16(v), vl = bf16(v - vh), exact in fp32
+    auto store_v = [&](float v) {
+        const int jr = j0 + j, pj = jr / r_slot, jj = jr - pj * r_slot;
+        const size_t off = static_cast<size_t>(s_rows[t]) * p.ld_p + pj * p.r_pad64 + jj;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        p.vh[off] = __bfloat16_as_ushort(hi);
+        p.vl[off] = __bfloat16_as_ushort(__float2bfloat16_rn(v - __bfloat162float(hi)));
+    };
     if (p.ks == 1) {
-        if (t < nrows && j < nj) p.v[static_cast<size_t>(s_rows[t]) * p.ld_v + j0 + j] = s_vp[tid];
+        if (t < nrows && j < nj) store_v(s_vp[tid]);
         return;
     }
     cluster_arrive();
@@ -308,7 +332,7 @@ bgmv_group_shrink_kernel(GsParams p)
             asm("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(f) : "r"(map_rank(base, c)));
             s += f;
         }
-        p.v[static_cast<size_t>(s_rows[t]) * p.ld_v + j0 + j] = s;
+        store_v(s);
     }
     cluster_arrive();   // peers may leave once everyone has read their partials
     cluster_wait();
@@ -325,8 +349,10 @@ constexpr int kGxLdD = 20;       // per-warp delta tile row stride (floats): con
 
 struct GexParams {
     ProjSet ps;
-    const float* v;           // [n_rows][ld_v] fp32, projection p at p*r_slot
-    int ld_v;
+    const bf16_t* vh;         // v = vh + vl: bf16 planes [n_rows][ld_p], projection p at p*r_pad64
+    const bf16_t* vl;
+    int ld_p;
+    int r_pad64;
     bf16_t* y;
     int ld_y;
     const int32_t* perm;
@@ -387,15 +413,6 @@ bgmv_group_expand_kernel(GexParams p)
         if (flagger) flag(p.status, LORA_DEV_SLOT_OUT_OF_RANGE);
         return;
     }
-    const bool bad_row = unit_rows(p.perm, pos0, nrows, p.n_rows, s_rows);
-    if (tid < kGxWarps) mbar_init(&s_bar[tid], 1);
-    if (tid == 0) asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    if (__syncthreads_or(bad_row)) {
-        grid_dep_wait();
-        if (flagger) flag(p.status, LORA_DEV_BAD_SEGMENT);
-        return;
-    }
-
     int pj, col0;
     block_proj(p.ps, blk, pj, col0);
     const int width = p.ps.width[pj];
@@ -403,11 +420,22 @@ bgmv_group_expand_kernel(GexParams p)
     const int r_slot = p.ps.r_slot;
     const int wc0 = warp * kGxWarpCols;                    // this warp's first column in the block
     const int wcols = max(0, min(kGxWarpCols, ncols - wc0));
-    if (wcols > 0 && lane == 0) {   // weights first: they do not depend on the preceding kernel
+    if (wcols > 0 && lane == 0) {
+        // Weights first, as soon as the slot is known: lane 0 owns the warp's
+        // barrier (init, expect, copy), before the rows and the grid dependency.
         const unsigned bytes = static_cast<unsigned>(wcols * r_slot * sizeof(bf16_t));
+        mbar_init(&s_bar[warp], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
         mbar_expect(&s_bar[warp], bytes);
         bulk_g2s(smem + sizeof(bf16_t) * wc0 * r_slot,
                  p.ps.B[pj] + (static_cast<size_t>(slot) * width + col0 + wc0) * r_slot, bytes, &s_bar[warp]);
+    }
+    __syncwarp();
+    if (__syncthreads_or(unit_rows(p.perm, pos0, nrows, p.n_rows, s_rows))) {
+        if (wcols > 0 && lane == 0) mbar_wait(&s_bar[warp], 0);   // let the block land before leaving (bounded)
+        grid_dep_wait();
+        if (flagger) flag(p.status, LORA_DEV_BAD_SEGMENT);
+        return;
     }
 
     grid_dep_wait();   // v is the preceding kernel's output; y may be too
@@ -424,8 +452,9 @@ bgmv_group_expand_kernel(GexParams p)
         yv[i] = (yt < nrows && c < ncols) ? *reinterpret_cast<const uint4*>(yrow + c) : make_uint4(0, 0, 0, 0);
     }
 
-    // v fragments (the mma B operand), n-tile nt = rows 8nt..8nt+7:
-    // b0 <- v[t][k0], v[t][k0+1]; b1 <- v[t][k0+2], v[t][k0+3], k0 = 8(q+4h)+4e.
+    // v fragments (the mma B operand) straight from the hi/lo planes, n-tile
+    // nt = rows 8nt..8nt+7: b0 <- v[t][k0..k0+1], b1 <- v[t][k0+2..k0+3],
+    // k0 = 8(q+4h)+4e: one 8-byte load per plane.
     const int g = lane >> 2, q = lane & 3;
     const int n_nt = (nrows + 7) / 8;
     const int np = r_slot / 8;              // 16-byte pieces per B' row
@@ -438,12 +467,16 @@ bgmv_group_expand_kernel(GexParams p)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int t = nt * 8 + g, k0 = 8 * (q + 4 * h) + 4 * e;
-                float4 vv = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (nt < n_nt && t < nrows && k0 < r_slot)
-                    vv = *reinterpret_cast<const float4*>(p.v + static_cast<size_t>(s_rows[t]) * p.ld_v +
-                                                          pj * r_slot + k0);
-                split_hi_lo(vv.x, vv.y, bh[nt][h][e][0], bl[nt][h][e][0]);
-                split_hi_lo(vv.z, vv.w, bh[nt][h][e][1], bl[nt][h][e][1]);
+                uint2 hv = make_uint2(0, 0), lv = make_uint2(0, 0);
+                if (nt < n_nt && t < nrows && k0 < r_slot) {
+                    const size_t off = static_cast<size_t>(s_rows[t]) * p.ld_p + pj * p.r_pad64 + k0;
+                    hv = *reinterpret_cast<const uint2*>(p.vh + off);
+                    lv = *reinterpret_cast<const uint2*>(p.vl + off);
+                }
+                bh[nt][h][e][0] = hv.x;
+                bh[nt][h][e][1] = hv.y;
+                bl[nt][h][e][0] = lv.x;
+                bl[nt][h][e][1] = lv.y;
             }
 
     if (!mbar_wait(&s_bar[warp], 0)) {
@@ -523,10 +556,11 @@ bgmv_group_expand_kernel(GexParams p)
 cudaError_t launch_bgmv_grouped(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
                                 const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
                                 int n_pos, int max_group_len, int n_rows, int n_slots, unsigned flags,
-                                float* v_ws, int32_t* status, cudaStream_t stream)
+                                bf16_t* vh, bf16_t* vl, int32_t* status, cudaStream_t stream)
 {
     if (n_pos <= 0 || n_groups <= 0) return cudaSuccess;
-    if (!v_ws || ps.r_slot > 64 || ps.r_slot % 8 != 0) return cudaErrorInvalidValue;
+    if (!vh || !vl || ps.r_slot > 64 || ps.r_slot % 8 != 0) return cudaErrorInvalidValue;
+    const int r_pad64 = (ps.r_slot + 63) / 64 * 64, ld_p = ps.n_proj * r_pad64;
     const int R = ps.n_proj * ps.r_slot;
     static int configured_device = -1;
     static int n_sms = 0;
@@ -536,6 +570,9 @@ cudaError_t launch_bgmv_grouped(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, 
     if (configured_device != dev) {
         e = cudaFuncSetAttribute(bgmv_group_shrink_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(gs_smem_bytes(kRB)));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(bgmv_group_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(sizeof(bf16_t) * kGxCols * 64));
         if (e != cudaSuccess) return e;
         e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
@@ -558,8 +595,10 @@ cudaError_t launch_bgmv_grouped(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, 
     sp.x = x;
     sp.ld_x = ld_x;
     sp.h_in = h_in;
-    sp.v = v_ws;
-    sp.ld_v = R;
+    sp.vh = vh;
+    sp.vl = vl;
+    sp.ld_p = ld_p;
+    sp.r_pad64 = r_pad64;
     sp.perm = perm;
     sp.gstarts = gstarts;
     sp.gslot = gslot;
@@ -609,8 +648,10 @@ cudaError_t launch_bgmv_grouped(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, 
     // ---- grouped expand ----
     GexParams gp{};
     gp.ps = ps;
-    gp.v = v_ws;
-    gp.ld_v = R;
+    gp.vh = vh;
+    gp.vl = vl;
+    gp.ld_p = ld_p;
+    gp.r_pad64 = r_pad64;
     gp.y = y;
     gp.ld_y = ld_y;
     gp.perm = perm;

@@ -56,11 +56,12 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
 // weight bytes streamed per call) rather than the one-launch kernel.
 bool decode_two_launch(const ProjSet& ps, int h_in, int n_groups);
 
-// The same rows in two launches: a grouped shrink that stores fp32 v in
-// v_ws ([n_rows][n_proj*r_slot]), then a grouped expand that streams B'.
+// The same rows in two launches: a grouped shrink that stores v as bf16
+// hi/lo planes vh, vl ([n_rows][n_proj * r_pad64], the layout of the
+// tensor-core SGMV route), then a grouped expand that streams B'.
 cudaError_t launch_bgmv_grouped(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
                                 const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
                                 int n_pos, int max_group_len, int n_rows, int n_slots, unsigned flags,
-                                float* v_ws, int32_t* status, cudaStream_t stream);
+                                bf16_t* vh, bf16_t* vl, int32_t* status, cudaStream_t stream);
 
 }  // namespace lora
