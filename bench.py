@@ -109,18 +109,33 @@ def useful_flops(wl, group) -> int:
     return int(sum(2 * (r * (group.h_in + w)).sum() for _, w in group.projs))
 
 
-def src_digest() -> str:
+def src_digest(files) -> str:
+    """sha256 (16 hex digits) over the named kernel sources under csrc/."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "lora_serving_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
-# DRAM traffic per launch of the dominant kernel from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload; valid
-# only while the kernel sources hash to `src`.  Summaries live in profiles/.
-NCU_TRAFFIC = {}
+# Kernels a lora_apply call launches on each workload (the route of csrc/abi.cu).
+ROUTE_KERNELS = {
+    "tiny": "shrink_rowwise + expand_rowwise (prefill), bgmv_fused_kernel (decode)",
+    "llama3b_decode": "bgmv_fused_kernel",
+    "mistral7b_prefill": "sgmv_shrink_tc_kernel + sgmv_expand_tc_kernel",
+    "mixed": "sgmv_shrink_tc_kernel + sgmv_expand_tc_kernel (prefill), bgmv_fused_kernel (decode)",
+    "stress70b": "bgmv_group_shrink_kernel + bgmv_group_expand_kernel",
+}
+
+# DRAM traffic per lora_apply call from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum over the call's launches), keyed by workload; valid
+# only while the listed kernel sources hash to `src`.  Summaries in profiles/.
+NCU_TRAFFIC = {
+    "llama3b_decode": {"files": ['bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "35f8b683ba9da9fe",
+                       "bytes_per_call": 3436288},   # profiles/bgmv_fused_llama3b_decode.md
+    "stress70b": {"files": ['bgmv_grouped.cu', 'decode_common.cuh', 'common.cuh'], "src": "80c90b0a7b77bbd7",
+                  "bytes_per_call": 987868032},   # profiles/bgmv_grouped_stress70b.md
+}
 
 
 def peaks():
@@ -350,15 +365,15 @@ def run_ours(args, rank, local, ws):
     units = sum_over_ranks(units_local, ws, device=dev if ws > 1 else "cpu")
     value = units / (ms / 1e3)
 
-    # dominant kernel roofline: every launch in the step is the delta kernel
+    # roofline of the delta: every launch in the step belongs to a lora_apply
+    # call; algorithmic bytes per call / the call's share of the timed region
     bytes_call = [algorithmic_bytes(base, g) for g in base.groups]
-    bytes_per_launch_avg = sum(bytes_call) / len(bytes_call)
+    bytes_per_call = sum(bytes_call) / len(bytes_call)
     call_ms = ms_local / (args.steps * calls_per_step)
-    achieved = bytes_per_launch_avg / (call_ms / 1e3) / 1e9
+    achieved = bytes_per_call / (call_ms / 1e3) / 1e9
     peak, peak_kind = peaks()
-    digest = src_digest()
     tr = NCU_TRAFFIC.get(name)
-    traffic = tr["bytes_per_launch"] if tr and tr.get("src") == digest else None
+    traffic = tr["bytes_per_call"] if tr and tr.get("src") == src_digest(tr["files"]) else None
 
     out = {
         "metric": "SGMV/BGMV LoRA-delta tokens/s (token x layer calls per second)",
@@ -377,10 +392,11 @@ def run_ours(args, rank, local, ws):
             "parallelism": f"replicas x{ws}",
         },
         "roofline": {
-            "kernel": "lora_apply decode delta (bgmv_fused_kernel, one launch per call)", "bound": "hbm",
+            "kernel": ROUTE_KERNELS.get(name, "lora_apply"), "bound": "hbm",
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
-            "bytes_per_launch": round(bytes_per_launch_avg), "launch_us": round(call_ms * 1e3, 3),
+            "per": "lora_apply call", "launches_per_call": round(launches_per_step / calls_per_step, 3),
+            "bytes_per_call": round(bytes_per_call), "call_us": round(call_ms * 1e3, 3),
             "traffic": traffic,
         },
         "clocks": clk,

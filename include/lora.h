@@ -204,7 +204,10 @@ typedef struct {
  *     over the gather groups meta->perm / gseg_* [TGI 4].
  * Each projection p adds its delta into y[:, projs[p].out_off + (0..width)).
  * workspace [dev] at least lora_apply_workspace_bytes(n_rows, n_proj, r_slot)
- *           bytes, 256-byte aligned; its contents are scratch.
+ *           bytes, 256-byte aligned; its contents are scratch (the
+ *           intermediate v: fp32, and bf16 hi/lo planes for the kernels
+ *           whose expand runs on tensor cores), written only after the
+ *           kernel enqueued just before the call has completed.
  * flags     LORA_APPLY_* above (0 = default ordering).
  */
 lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_x, int h_in,
@@ -223,12 +226,14 @@ size_t lora_apply_workspace_bytes(int n_rows, int n_proj, int r_slot);
  * plug-in that may only use its host's memory pool, a loop that cannot
  * afford cudaMalloc's device synchronisation).  The source pages have no
  * counterpart to this entry point; it is a deployment convenience.
- * Same arguments and results as lora_apply, minus the workspace: the fp32
- * intermediate lives in a LORA_NOALLOC_SCRATCH_BYTES array compiled into
- * the library, which every GPU that loads the library holds until exit.
+ * Same arguments and results as lora_apply, minus the workspace: lora_apply's
+ * workspace (the intermediate v, fp32 and as bf16 hi/lo planes) lives in a
+ * LORA_NOALLOC_SCRATCH_BYTES array compiled into the library, which every
+ * GPU that loads the library holds until exit.
  *   - Returns LORA_ERR_WORKSPACE, before anything is enqueued, when
  *     lora_apply_workspace_bytes(meta->n_rows, n_proj, r_slot) exceeds
- *     LORA_NOALLOC_SCRATCH_BYTES (16 MiB: e.g. 32768 rows x 128 ranks).
+ *     LORA_NOALLOC_SCRATCH_BYTES (16 MiB: e.g. 16384 rows x 2 projections
+ *     of slot rank 64).
  *   - The first call on a device looks up the array's device address on
  *     the current device (cudaGetSymbolAddress); make that first call
  *     before any stream capture.  LORA_ERR_CUDA if the lookup fails.

@@ -5,9 +5,9 @@
 // pool (so a cudaMalloc would fail), or a plug-in hosted by an engine that
 // forbids allocations outside its own pool, or a latency-critical loop where
 // cudaMalloc's implicit device synchronisation is not acceptable.  For them,
-// lora_apply_noalloc keeps lora_apply's fp32 intermediate in a fixed
-// scratch array compiled into this library, instead of a workspace the
-// caller would have to allocate.
+// lora_apply_noalloc keeps lora_apply's workspace (the intermediate v, fp32
+// and as bf16 hi/lo planes) in a fixed scratch array compiled into this
+// library, instead of a workspace the caller would have to allocate.
 //
 // The array is a file-scope __device__ object: every GPU that loads the
 // library holds LORA_NOALLOC_SCRATCH_BYTES of it until the process exits.
