@@ -50,8 +50,6 @@ constexpr int kPad = 8;            // bf16 padding per smem row: conflict-free l
 constexpr int kLds = kKT + kPad;
 constexpr int kStages = 2;
 constexpr int kMaxChunks = 64;     // output chunks (8 columns) per expand tile
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
 constexpr int kPermStage = 4096;   // decode positions staged in smem with the group table
 constexpr int kBSlack = 32;        // zeroed bf16 after B' so padded-K fragments stay finite
 
@@ -113,9 +111,15 @@ __host__ __device__ inline SmemLayout smem_layout(int R, int r_slot, int nch_til
     return L;
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+// kThreads = 256 (2 CTAs per SM) for small calls, whose time is the chain
+// of dependent latencies of each CTA; 128 (4 per SM) for calls whose grid
+// exceeds the resident slots, which more CTAs in flight serve better.
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads, 512 / kThreads)
 bgmv_fused_kernel(FusedParams p)
 {
+    constexpr int kWarps = kThreads / 32;
+    constexpr int kTilesPerWarp = 16 / kWarps;   // shrink n-tiles of 8 ranks per warp (R <= 128)
     extern __shared__ __align__(128) unsigned char smem[];
     const int R = p.ps.n_proj * p.ps.r_slot;
     const int r_slot = p.ps.r_slot;
@@ -271,7 +275,7 @@ bgmv_fused_kernel(FusedParams p)
     // ---- shrink: 16 rows x R ranks x this CTA's K range on tensor cores ----
     const int n_tiles = R / 8;                  // 8 ranks per mma tile; <= 16
     bool failed = false;
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float acc[kTilesPerWarp][4] = {};
     for (int kt = 0; kt < n_kt; ++kt) {
         // groups so far: {A_0} {A_1} {X_0} {X_1}, then one per iteration;
         // stage kt is complete once at most one group is pending
@@ -286,8 +290,8 @@ bgmv_fused_kernel(FusedParams p)
             uint32_t a0, a1, a2, a3;
             ldmatrix_x4(smem_u32(xs + ((mi & 1) * 8 + mr) * kLds + ks * 16 + (mi >> 1) * 8), a0, a1, a2, a3);
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int tile = warp + nt * 8;
+            for (int nt = 0; nt < kTilesPerWarp; ++nt) {
+                const int tile = warp + nt * kWarps;
                 if (tile < n_tiles) {
                     uint32_t b0, b1;
                     const int l = lane & 15;
@@ -307,8 +311,8 @@ bgmv_fused_kernel(FusedParams p)
     {
         const int gr = lane >> 2, q2 = (lane & 3) * 2;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int tile = warp + nt * 8;
+        for (int nt = 0; nt < kTilesPerWarp; ++nt) {
+            const int tile = warp + nt * kWarps;
             if (tile < n_tiles) {
                 const int j = tile * 8 + q2;
                 vpart[gr * R + j] = acc[nt][0];
@@ -518,13 +522,18 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     if (n_pos <= 0 || n_groups <= 0) return cudaSuccess;
     const int R = ps.n_proj * ps.r_slot;
     static int configured_device = -1;
+    static int n_sms = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(bgmv_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(bgmv_fused_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        for (auto fn : {bgmv_fused_kernel<128>, bgmv_fused_kernel<256>}) {
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
+        e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
@@ -561,8 +570,10 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     p.status = status;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(max_units * parts * cs));
-    cfg.blockDim = dim3(kThreads);
+    const long long n_ctas = static_cast<long long>(max_units) * parts * cs;
+    const int threads = env_int("LORA_FUSED_THREADS", n_ctas > 2LL * n_sms ? 128 : 256) == 128 ? 128 : 256;
+    cfg.gridDim = dim3(static_cast<unsigned>(n_ctas));
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem_layout(R, ps.r_slot, nch_tile, n_pos).total;
     cfg.stream = stream;
     cudaLaunchAttribute attrs[2];
@@ -579,7 +590,8 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     }
     cfg.attrs = attrs;
     cfg.numAttrs = na;
-    e = cudaLaunchKernelEx(&cfg, bgmv_fused_kernel, p);
+    e = threads == 128 ? cudaLaunchKernelEx(&cfg, bgmv_fused_kernel<128>, p)
+                       : cudaLaunchKernelEx(&cfg, bgmv_fused_kernel<256>, p);
     note_launch();
     return e;
 }

@@ -59,13 +59,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity)
         : "memory");
     return ok != 0;
 }
+// The same test, letting the hardware suspend the thread for up to
+// kSuspendNs while the phase is incomplete (it resumes when the phase
+// completes): a waiting warp does not spin through issue slots.
+constexpr uint32_t kSuspendNs = 1000000u;
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, unsigned parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    return ok != 0;
+}
 // Waits for the phase with the given parity to complete; false after
 // kTimeoutNs (the caller flags the timeout and winds down).
 __device__ __noinline__ bool mbar_wait(uint64_t* bar, unsigned parity)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = gtime();
-    while (!mbar_try_wait(bar, parity))
+    while (!mbar_try_wait_suspend(bar, parity))
         if (gtime() - t0 > kTimeoutNs) return false;
     return true;
 }

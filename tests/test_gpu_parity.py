@@ -434,6 +434,24 @@ def test_two_launch_form_chained_calls_share_workspace(flags, monkeypatch):
     check_bf16(refs[0], oracle_group(wl, "g"), wl.ids, wl.y["g"], "chained")
 
 
+@pytest.mark.parametrize("threads", [128, 256])
+@pytest.mark.parametrize("h_in,widths,rank,T,n_slots", [
+    (4096, (4096, 1024, 1024, 1024), 32, 200, 8),   # 4 tiles of 8 ranks per warp at 128 threads
+    (1024, (1024,), 24, 20, 4),                     # slot rank not a multiple of 16
+    (8192, (28672,), 16, 40, 4),                    # long K, wide output (no column parts)
+])
+def test_apply_decode_fused_thread_counts(h_in, widths, rank, T, n_slots, threads, monkeypatch):
+    """The one-launch kernel in both CTA sizes (128 threads for large grids,
+    256 for small ones) on the same shapes."""
+    monkeypatch.setenv("LORA_DECODE_TWO_LAUNCH", "0")
+    monkeypatch.setenv("LORA_FUSED_THREADS", str(threads))
+    rng = np.random.default_rng(h_in + T + threads)
+    ids = rng.integers(-1, n_slots, T).astype(np.int32)
+    wl = _small(ids, 0, n_slots=n_slots, rank=rank, h_in=h_in, widths=widths, seed=T)
+    got = _run_apply(wl, "g")
+    check_bf16(got, oracle_group(wl, "g"), wl.ids, wl.y["g"], f"fused threads={threads} h_in={h_in}")
+
+
 def test_apply_decode_bad_permutation_flagged():
     """A corrupted gather permutation is flagged and its group's rows skipped."""
     ids = np.array([0, 1, 0, 1, 0, 1], np.int32)
