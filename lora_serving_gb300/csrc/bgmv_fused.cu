@@ -49,7 +49,9 @@ constexpr int kKT = 128;           // K elements per pipeline stage
 constexpr int kPad = 8;            // bf16 padding per smem row: conflict-free ldmatrix
 constexpr int kLds = kKT + kPad;
 constexpr int kStages = 2;
-constexpr int kMaxChunks = 64;     // output chunks (8 columns) per expand tile
+constexpr int kMaxChunks = 128;    // output chunks (8 columns) per expand tile, at most
+constexpr int kPartChunks = 64;    // column parts keep a CTA's chunks within two tiles of this
+constexpr int kTileBBytes = 32768; // B' bytes per expand tile, at most
 constexpr int kPermStage = 4096;   // decode positions staged in smem with the group table
 constexpr int kBSlack = 32;        // zeroed bf16 after B' so padded-K fragments stay finite
 
@@ -70,7 +72,7 @@ struct FusedParams {
     int kc;                   // K elements per cluster rank (multiple of 16)
     int n_parts;              // column parts per unit
     int cs;                   // cluster size
-    int nch_tile;             // chunks per expand tile (<= kMaxChunks)
+    int nch_tile;             // chunks per expand tile (<= kMaxChunks, B' <= kTileBBytes)
     int r_pad;                // r_slot rounded up to 16 (expand mma K)
     int x_ready;              // x may be read before the grid dependency resolves
     int y_ready;              // y may be updated before it resolves
@@ -106,7 +108,9 @@ __host__ __device__ inline SmemLayout smem_layout(int R, int r_slot, int nch_til
     L.vpart = L.x + align128(sizeof(bf16_t) * kStages * kRB * kLds);
     L.vfull = L.vpart + align128(sizeof(float) * kRB * R);
     L.b = L.vfull + align128(sizeof(float) * kRB * R);
-    L.perm = L.b + align128(sizeof(bf16_t) * (nch_tile * 8 * r_slot + kBSlack));
+    // the B' tile, and after the delta is formed, the y pieces being updated
+    const size_t sb = sizeof(bf16_t) * (nch_tile * 8 * r_slot + kBSlack), sy = 16 * kRB * nch_tile;
+    L.perm = L.b + align128(sb > sy ? sb : sy);
     L.total = L.perm + (n_pos <= kPermStage ? sizeof(int) * n_pos : 0);
     return L;
 }
@@ -426,30 +430,25 @@ bgmv_fused_kernel(FusedParams p)
             grid_dep_wait();   // y may be the preceding kernel's output
             waited = true;
         }
-        // ---- read-modify-write of y: 16-byte pieces, coalesced along each row ----
+        // ---- read-modify-write of y: 16-byte pieces, coalesced along each row.
+        // All of a thread's pieces are requested at once (cp.async into the
+        // B' region, free once the delta is formed): one round trip. ----
         if (!failed) {
-            constexpr int kPairs = kRB * kMaxChunks / kThreads;
-            uint4 yo[kPairs];
-#pragma unroll
-            for (int q = 0; q < kPairs; ++q) {
-                const int i = tid + q * kThreads;
-                if (i < nrows * nch) {
-                    const int t = i / nch, ci = i - t * nch;
-                    yo[q] = *reinterpret_cast<const uint4*>(p.y + static_cast<size_t>(s_rows[t]) * p.ld_y +
-                                                            p.ps.out_off[s_cp[ci]] + s_ccol[ci]);
-                }
+            uint4* sY = reinterpret_cast<uint4*>(sB);
+            for (int i = tid; i < nrows * nch; i += kThreads) {
+                const int t = i / nch, ci = i - t * nch;
+                cp_async16(smem_u32(sY + i),
+                           p.y + static_cast<size_t>(s_rows[t]) * p.ld_y + p.ps.out_off[s_cp[ci]] + s_ccol[ci], true);
             }
-#pragma unroll
-            for (int q = 0; q < kPairs; ++q) {
-                const int i = tid + q * kThreads;
-                if (i < nrows * nch) {
-                    const int t = i / nch, ci = i - t * nch;
-                    const float4* dp = reinterpret_cast<const float4*>(sD + t * nch * 8 + ci * 8);
-                    const float4 d0 = dp[0], d1 = dp[1];
-                    const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-                    *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(s_rows[t]) * p.ld_y +
-                                              p.ps.out_off[s_cp[ci]] + s_ccol[ci]) = add_round8(yo[q], dd);
-                }
+            cp_async_commit();
+            cp_async_wait<0>();   // each thread reads back only its own pieces
+            for (int i = tid; i < nrows * nch; i += kThreads) {
+                const int t = i / nch, ci = i - t * nch;
+                const float4* dp = reinterpret_cast<const float4*>(sD + t * nch * 8 + ci * 8);
+                const float4 d0 = dp[0], d1 = dp[1];
+                const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+                *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(s_rows[t]) * p.ld_y + p.ps.out_off[s_cp[ci]] +
+                                          s_ccol[ci]) = add_round8(sY[i], dd);
             }
         }
     }
@@ -483,11 +482,11 @@ int total_chunks(const ProjSet& ps)
 }
 
 // Column parts per unit (more clusters, each recomputing the shrink from
-// L2) so that each CTA expands at most two tiles of kMaxChunks chunks.
+// L2) so that each CTA expands at most two tiles of kPartChunks chunks.
 int fused_parts(int total_ch, int cs)
 {
     int parts = 1;
-    while (parts < 8 && (total_ch + cs * parts - 1) / (cs * parts) > 2 * kMaxChunks) parts *= 2;
+    while (parts < 8 && (total_ch + cs * parts - 1) / (cs * parts) > 2 * kPartChunks) parts *= 2;
     return env_int("LORA_FUSED_PARTS", parts);
 }
 
@@ -544,7 +543,14 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     const int total_ch = total_chunks(ps);
     const int parts = fused_parts(total_ch, cs);
     const int per_cta = (total_ch + cs * parts - 1) / (cs * parts);
-    const int nch_tile = min(kMaxChunks, max(1, per_cta));
+    const long long n_ctas = static_cast<long long>(max_units) * parts * cs;
+    const int threads = env_int("LORA_FUSED_THREADS", n_ctas > 2LL * n_sms ? 128 : 256) == 128 ? 128 : 256;
+    // Small calls (256 threads): one tile when the B' slice fits, since a
+    // second tile would put its B' copy and delta behind the grid
+    // dependency.  Large grids (128 threads): tiles of kPartChunks, so four
+    // CTAs' shared memory fits on an SM.
+    const int tile_cap = threads == 256 ? min(kMaxChunks, kTileBBytes / (16 * ps.r_slot)) : kPartChunks;
+    const int nch_tile = min(tile_cap, max(1, per_cta));
 
     FusedParams p{};
     p.ps = ps;
@@ -570,8 +576,6 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     p.status = status;
 
     cudaLaunchConfig_t cfg = {};
-    const long long n_ctas = static_cast<long long>(max_units) * parts * cs;
-    const int threads = env_int("LORA_FUSED_THREADS", n_ctas > 2LL * n_sms ? 128 : 256) == 128 ? 128 : 256;
     cfg.gridDim = dim3(static_cast<unsigned>(n_ctas));
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem_layout(R, ps.r_slot, nch_tile, n_pos).total;
