@@ -185,8 +185,9 @@ bgmv_fused_kernel(FusedParams p)
     int total_ch = 0;
     for (int q = 0; q < p.ps.n_proj; ++q) total_ch += p.ps.width[q] >> 3;
     const int q_idx = part * p.cs + crank, q_n = p.n_parts * p.cs;
-    const int ch_begin = static_cast<int>((static_cast<long long>(total_ch) * q_idx) / q_n);
-    const int ch_end = static_cast<int>((static_cast<long long>(total_ch) * (q_idx + 1)) / q_n);
+    // total_ch * q_n < 2^31: the launcher takes at most 2^24 chunks, q_n <= 128
+    const int ch_begin = (total_ch * q_idx) / q_n;
+    const int ch_end = (total_ch * (q_idx + 1)) / q_n;
     const int tile0_end = min(ch_end, ch_begin + p.nch_tile);
 
     auto map_chunks = [&](int c0, int c1) {
@@ -394,6 +395,7 @@ bgmv_fused_kernel(FusedParams p)
                 const float* vp = vfull + pj * r_slot;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
+                    if (kk * 16 >= r_pad) break;   // K steps past the slot rank are never used
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
                         // a0: (row g, k 2q..), a1: (row g+8, k 2q..), a2: (row g, k 2q+8..), a3: (row g+8, k 2q+8..)
@@ -519,6 +521,7 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
                               int32_t* status, cudaStream_t stream)
 {
     if (n_pos <= 0 || n_groups <= 0) return cudaSuccess;
+    if (total_chunks(ps) > (1 << 24)) return cudaErrorInvalidValue;   // > 128M output columns
     const int R = ps.n_proj * ps.r_slot;
     static int configured_device = -1;
     static int n_sms = 0;
