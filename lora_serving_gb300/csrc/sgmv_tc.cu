@@ -20,6 +20,7 @@
 // Every mbarrier wait is bounded (0.2 s); a timeout sets LORA_DEV_TIMEOUT,
 // skips the rest of the tile and still frees the tensor memory.
 
+#include <algorithm>
 #include <cstdlib>
 
 #include "launch.h"
@@ -274,25 +275,36 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
 
 // ------------------------------------------------------------- expand ----
 //
-// One CTA owns a 128-row tile of a segment and a run of up to tiles_per_cta
-// 128-column output tiles of one projection.  Its v_hi / v_lo tile is loaded
-// once; B' and y tiles stream through a kStagesE-deep TMA ring; the fp32
-// accumulator is double-buffered in tensor memory, so the epilogue of tile i
-// (TMEM -> registers, + y from shared memory, round, store) overlaps the
-// loads and MMAs of tile i+1.
+// Persistent: one CTA per SM walks work items -- (projection q, chunk of up
+// to p.chunk 128-column output tiles, 128-row tile u of the segments) -- taken
+// round-robin (item c, c + G, c + 2G, ... for CTA c of G), ordered with the
+// row tile fastest, so at any moment the CTAs work on the same chunk of B'
+// for different row tiles and B' is read from HBM about once.  The TMA ring
+// keeps streaming across items: no CTA pays a start-up and a drain per item.
+// The row tiles of a CTA's items are resolved once, at its start, into a
+// shared-memory table.  The v_hi / v_lo slice of an item (row tile,
+// projection) is loaded once into one of two buffers (one when r_pad64 > 64),
+// so the next item's slice loads while the current one's tiles finish; B'
+// and y tiles stream through a kStagesE-deep TMA ring; the fp32 accumulator
+// is double-buffered in tensor memory, so the epilogue of tile i (TMEM ->
+// registers, + y from shared memory, round, store) overlaps the loads and
+// MMAs of tile i+1.
 //   warp 0: TMA producer      warp 1: MMA issuer      warps 2..17: epilogue
 
 constexpr int kStagesE = 3;
 constexpr int kEpiWarps = 16;       // 4 per TMEM lane quarter, 32 columns each
 constexpr int kExpandThreadsP = 32 * (2 + kEpiWarps);
+constexpr int kChunkMax = 16;       // output tiles per work item, at most
+constexpr int kMaxItems = 64;       // work items per CTA (the launcher sizes the grid)
 
 struct ExpandTcParams {
     int n_proj, r_slot, r_pad64, n_slots;
     int out_off[LORA_MAX_PROJ];
     int width[LORA_MAX_PROJ];
     int col_tiles[LORA_MAX_PROJ];   // ceil(width / 128) per projection
-    int chunks[LORA_MAX_PROJ];      // ceil(col_tiles / tiles_per_cta) per projection
-    int tiles_per_cta;
+    int chunks[LORA_MAX_PROJ];      // ceil(col_tiles / chunk) per projection
+    int n_chunks;                   // sum of chunks
+    int chunk;                      // output tiles per work item
     const int32_t* seg_starts;
     const int32_t* seg_slot;
     int n_segs, n_pos, n_rows;
@@ -301,6 +313,97 @@ struct ExpandTcParams {
     int32_t* status;
 };
 
+struct RowTile {
+    int slot, row0, nrows;
+};
+
+// Walks this CTA's tiles: item k (global item c + k * G), tile ct of the
+// item's projection.  Divides once per item, never per tile.
+struct TileIter {
+    int k, q, ct, ct_end;
+    __device__ __forceinline__ void item(const ExpandTcParams& p, int n_rt)
+    {
+        const long long it = blockIdx.x + static_cast<long long>(k) * gridDim.x;
+        int ch = static_cast<int>(it / n_rt);   // chunk index over all projections
+        q = 0;
+        while (q < p.n_proj - 1 && ch >= p.chunks[q]) {
+            ch -= p.chunks[q];
+            ++q;
+        }
+        ct = ch * p.chunk;
+        ct_end = min(ct + p.chunk, p.col_tiles[q]);
+    }
+    __device__ __forceinline__ void init(const ExpandTcParams& p, int n_rt)
+    {
+        k = 0;
+        item(p, n_rt);
+    }
+    // false once past the CTA's last item
+    __device__ __forceinline__ bool next(const ExpandTcParams& p, int n_rt, int n_items)
+    {
+        if (++ct < ct_end) return true;
+        if (++k >= n_items) return false;
+        item(p, n_rt);
+        return true;
+    }
+};
+
+// Row tile u of item it (row tile fastest).
+__device__ __forceinline__ int item_row_tile(long long it, int n_rt) { return static_cast<int>(it % n_rt); }
+
+// One block-wide pass over the segment table, kExpandThreadsP segments per
+// round: row tiles per segment (slot -1 and malformed segments have none)
+// and their prefix sums.  With fill, the segment holding the row tile of
+// each of this CTA's n_items items writes s_rt[item].  Returns the total
+// number of row tiles.  Every thread of the block takes part.
+__device__ int scan_row_tiles(const ExpandTcParams& p, bool fill, int n_rt, int n_items, RowTile* s_rt, int* s_warp,
+                              int* s_bad)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int base = 0;
+    for (int g0 = 0; g0 < p.n_segs; g0 += kExpandThreadsP) {
+        const int gi = g0 + tid;
+        int n = 0, s = 0, e = 0, sl = -1;
+        if (gi < p.n_segs) {
+            s = __ldg(p.seg_starts + gi);
+            e = __ldg(p.seg_starts + gi + 1);
+            sl = __ldg(p.seg_slot + gi);
+            const bool sane = s >= 0 && e <= p.n_pos && s <= e;
+            if (!sane) atomicOr(s_bad, 1);
+            n = (sane && sl >= 0) ? (e - s + kTileM - 1) / kTileM : 0;
+        }
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        if (lane == 31) s_warp[warp] = incl;
+        __syncthreads();
+        int before = 0, total = 0;
+        for (int w = 0; w < kExpandThreadsP / 32; ++w) {
+            if (w < warp) before += s_warp[w];
+            total += s_warp[w];
+        }
+        if (fill && n > 0) {
+            const int excl = base + before + (incl - n);   // row tiles before this segment
+            for (int kk = 0; kk < n_items; ++kk) {
+                const int u = item_row_tile(blockIdx.x + static_cast<long long>(kk) * gridDim.x, n_rt);
+                if (u >= excl && u < excl + n) {
+                    RowTile rt;
+                    rt.slot = sl;
+                    rt.row0 = s + (u - excl) * kTileM;
+                    rt.nrows = min(kTileM, e - rt.row0);
+                    s_rt[kk] = rt;
+                }
+            }
+        }
+        base += total;
+        __syncthreads();   // s_warp is rewritten by the next round
+    }
+    return base;
+}
+
 __global__ void __launch_bounds__(kExpandThreadsP, 1)
 sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_constant__ CUtensorMap mvl,
                       const __grid_constant__ CUtensorMap my, const __grid_constant__ CUtensorMap mb0,
@@ -308,41 +411,46 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
                       const __grid_constant__ CUtensorMap mb3, ExpandTcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t vbar, full[kStagesE], empty[kStagesE], acc_full[2], acc_empty[2];
+    __shared__ __align__(8) uint64_t full[kStagesE], empty[kStagesE], acc_full[2], acc_empty[2];
+    __shared__ __align__(8) uint64_t v_full[2], v_empty[2];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_fail;
+    __shared__ RowTile s_rt[kMaxItems];
+    __shared__ int s_warp[kExpandThreadsP / 32];
+    __shared__ int s_bad;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    const TileInfo ti = find_tile<kExpandThreadsP>(p.seg_starts, p.seg_slot, p.n_segs, p.n_pos, blockIdx.x);
-    if (!ti.found) {
-        if (ti.bad && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
+    // ---- this CTA's items and their row tiles ----
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+    const int n_rt = scan_row_tiles(p, false, 1, 0, s_rt, s_warp, &s_bad);
+    const long long n_all = static_cast<long long>(n_rt) * p.n_chunks;
+    const int n_items = n_all > blockIdx.x ? static_cast<int>((n_all - 1 - blockIdx.x) / gridDim.x + 1) : 0;
+    if (n_items <= 0 || n_items > kMaxItems) {   // the launcher sizes the grid so the second cannot happen
+        if (tid == 0 && (n_items > 0 || (blockIdx.x == 0 && s_bad))) flag(p.status, LORA_DEV_BAD_SEGMENT);
         return;
     }
-    if (ti.slot >= p.n_slots || ti.slot < -1) {
-        if (tid == 0 && blockIdx.y == 0) flag(p.status, LORA_DEV_SLOT_OUT_OF_RANGE);
+    scan_row_tiles(p, true, n_rt, n_items, s_rt, s_warp, &s_bad);
+    for (int i = tid; i < n_items; i += kExpandThreadsP)
+        if (s_rt[i].slot >= p.n_slots || s_rt[i].slot < -1) atomicOr(&s_bad, 2);
+    __syncthreads();
+    if (tid == 0 && blockIdx.x == 0 && (s_bad & 1)) flag(p.status, LORA_DEV_BAD_SEGMENT);
+    if (s_bad & 2) {   // a slot out of range: flag it, leave this CTA's tiles alone
+        if (tid == 0) flag(p.status, LORA_DEV_SLOT_OUT_OF_RANGE);
         return;
     }
-    // chunk -> (projection q, first column tile, number of tiles)
-    int q = 0, ch = blockIdx.y;
-    while (q < p.n_proj - 1 && ch >= p.chunks[q]) {
-        ch -= p.chunks[q];
-        ++q;
-    }
-    const int t_first = ch * p.tiles_per_cta;
-    const int n_tiles = min(p.tiles_per_cta, p.col_tiles[q] - t_first);
-    if (n_tiles <= 0) return;
+
     const CUtensorMap* bmap[4] = {&mb0, &mb1, &mb2, &mb3};
     const int kbs = p.r_pad64 / kKB;                         // K blocks per plane
     const int S = kbs == 1 ? kStagesE : 2;                   // ring depth that fits shared memory
+    const int VB = kbs == 1 ? 2 : 1;                         // v slice buffers
     const int stage_bytes = (kbs + 2) * kBoxBytes;           // B' (kbs boxes) + y (2 boxes)
-    uint8_t* base = align1024(smem_raw);
-    uint8_t* svh = base;                                     // kbs boxes of v_hi
-    uint8_t* svl = svh + kbs * kBoxBytes;                    // kbs boxes of v_lo
-    uint8_t* ring = svl + kbs * kBoxBytes;                   // kStagesE x [B' | y]
+    const int vbuf_bytes = 2 * kbs * kBoxBytes;              // v_hi boxes, then v_lo boxes
+    uint8_t* vbufs = align1024(smem_raw);                    // VB x [v_hi | v_lo]
+    uint8_t* ring = vbufs + VB * vbuf_bytes;                 // S x [B' | y]
 
     if (warp == 0) tmem_alloc(&s_tmem, 2 * kExpandN);
     if (tid == 0) {
-        mbar_init(&vbar, 1);
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kEpiWarps / 2);   // released by the team that took the tile
@@ -350,6 +458,8 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
             mbar_init(&acc_empty[a], kEpiWarps / 2);
+            mbar_init(&v_full[a], 1);
+            mbar_init(&v_empty[a], 1);
         }
         mbar_init_fence();
         s_fail = 0;
@@ -361,49 +471,75 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
 
     if (warp == 0) {
         if (lane == 0) {   // ---- producer ----
-            mbar_expect_tx(&vbar, 2 * kbs * kBoxBytes);
-            for (int kb = 0; kb < kbs; ++kb) {
-                tma_load_2d(svh + kb * kBoxBytes, &mvh, q * p.r_pad64 + kb * kKB, ti.row0, &vbar);
-                tma_load_2d(svl + kb * kBoxBytes, &mvl, q * p.r_pad64 + kb * kKB, ti.row0, &vbar);
-            }
-            for (int i = 0; i < n_tiles && !s_fail; ++i) {
+            TileIter tr;
+            tr.init(p, n_rt);
+            int k_prev = -1;
+            for (int i = 0; !s_fail; ++i) {
+                const RowTile rt = s_rt[tr.k];
+                if (tr.k != k_prev) {   // a new item: its v slice into buffer k % VB
+                    k_prev = tr.k;
+                    const int vb = tr.k % VB;
+                    if (tr.k >= VB && !mbar_wait(&v_empty[vb], ((tr.k / VB) - 1) & 1)) {
+                        s_fail = 1;
+                        break;
+                    }
+                    uint8_t* vh = vbufs + vb * vbuf_bytes;
+                    mbar_expect_tx(&v_full[vb], vbuf_bytes);
+                    for (int kb = 0; kb < kbs; ++kb) {
+                        tma_load_2d(vh + kb * kBoxBytes, &mvh, tr.q * p.r_pad64 + kb * kKB, rt.row0, &v_full[vb]);
+                        tma_load_2d(vh + (kbs + kb) * kBoxBytes, &mvl, tr.q * p.r_pad64 + kb * kKB, rt.row0,
+                                    &v_full[vb]);
+                    }
+                }
                 const int s = i % S;
                 if (i >= S && !mbar_wait(&empty[s], ((i / S) - 1) & 1)) {
                     s_fail = 1;
                     break;
                 }
                 uint8_t* st = ring + s * stage_bytes;
-                const int col0 = (t_first + i) * kExpandN;
+                const int col0 = tr.ct * kExpandN;
                 mbar_expect_tx(&full[s], stage_bytes);
                 for (int kb = 0; kb < kbs; ++kb)
-                    tma_load_2d(st + kb * kBoxBytes, bmap[q], kb * kKB, ti.slot * p.width[q] + col0, &full[s]);
-                const int ycol = p.out_off[q] + col0;
-                tma_load_2d(st + kbs * kBoxBytes, &my, ycol, ti.row0, &full[s]);
-                tma_load_2d(st + (kbs + 1) * kBoxBytes, &my, ycol + kKB, ti.row0, &full[s]);
+                    tma_load_2d(st + kb * kBoxBytes, bmap[tr.q], kb * kKB, rt.slot * p.width[tr.q] + col0, &full[s]);
+                const int ycol = p.out_off[tr.q] + col0;
+                tma_load_2d(st + kbs * kBoxBytes, &my, ycol, rt.row0, &full[s]);
+                tma_load_2d(st + (kbs + 1) * kBoxBytes, &my, ycol + kKB, rt.row0, &full[s]);
+                if (!tr.next(p, n_rt, n_items)) break;
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {   // ---- MMA issuer ----
             const uint32_t idesc = idesc_bf16_f32(kTileM, kExpandN);
-            bool ok = mbar_wait(&vbar, 0);
-            tc_fence_after();
-            for (int i = 0; i < n_tiles && ok && !s_fail; ++i) {
+            bool ok = true;
+            TileIter tr;
+            tr.init(p, n_rt);
+            int k_prev = -1;
+            for (int i = 0; ok && !s_fail; ++i) {
+                const int k = tr.k;
+                if (k != k_prev) {
+                    k_prev = k;
+                    if (!mbar_wait(&v_full[k % VB], (k / VB) & 1)) { ok = false; break; }
+                }
                 const int s = i % S, a = i & 1;
                 if (i >= 2 && !mbar_wait(&acc_empty[a], ((i >> 1) - 1) & 1)) { ok = false; break; }
                 if (!mbar_wait(&full[s], (i / S) & 1)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t bs = smem_u32(ring + s * stage_bytes);
+                const uint32_t vs = smem_u32(vbufs + (k % VB) * vbuf_bytes);
                 const uint32_t d = tmem + a * kExpandN;
                 int n = 0;
                 for (int plane = 0; plane < 2; ++plane)
                     for (int kb = 0; kb < kbs; ++kb) {
-                        const uint32_t av = smem_u32((plane ? svl : svh) + kb * kBoxBytes);
+                        const uint32_t av = vs + (plane * kbs + kb) * kBoxBytes;
 #pragma unroll
                         for (int ks = 0; ks < kKB / 16; ++ks, ++n)
                             mma_bf16(d, sdesc_sw128(av + ks * 32), sdesc_sw128(bs + kb * kBoxBytes + ks * 32),
                                      idesc, n != 0);
                     }
                 mma_commit(&acc_full[a]);
+                const bool more = tr.next(p, n_rt, n_items);
+                if (!more || tr.k != k) mma_commit(&v_empty[k % VB]);   // the item's slice is free after these
+                if (!more) break;
             }
             if (!ok) s_fail = 1;
         }
@@ -416,12 +552,15 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
         const int quarter = warp & 3;       // TMEM lanes this warp may read
         const int hc = w8 >> 2;             // which 64-column half of the tile (one y box)
         const int r = quarter * 32 + lane;  // tile row
-        const bool row_ok = r < ti.nrows;
-        bf16_t* yrow_g = p.y + static_cast<size_t>(ti.row0 + r) * p.ld_y + p.out_off[q];
         // Every warp of a team runs every one of the team's iterations and
         // meets both named barriers whatever happened (after a timeout it
         // only skips work), so a barrier never waits for a warp that has left.
-        for (int i = team; i < n_tiles; i += 2) {
+        TileIter tr;
+        tr.init(p, n_rt);
+        bool more = true;
+        if (team == 1) more = tr.next(p, n_rt, n_items);
+        for (int i = team; more; i += 2) {
+            const RowTile rt = s_rt[tr.k];
             const int s = i % S, a = team;
             const bool ok = !s_fail && mbar_wait(&acc_full[a], (i >> 1) & 1);
             if (!ok) s_fail = 1;
@@ -436,13 +575,14 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
 
             uint8_t* ybox = ring + s * stage_bytes + (kbs + hc) * kBoxBytes;
             uint8_t* sy = ybox + r * 128;
-            const int tile_col0 = (t_first + i) * kExpandN;
+            const int tile_col0 = tr.ct * kExpandN;
             const int col0 = tile_col0 + hc * kKB;
-            const int cols_left = p.width[q] - col0;
-            // whole tile inside this segment's rows and this projection's columns:
+            const int cols_left = p.width[tr.q] - col0;
+            // whole tile inside the segment's rows and the projection's columns:
             // results go back into the staged tile and leave by TMA bulk stores
-            const bool whole = ti.nrows == kTileM && tile_col0 + kExpandN <= p.width[q];
-            if (ok && row_ok) {
+            const bool whole = rt.nrows == kTileM && tile_col0 + kExpandN <= p.width[tr.q];
+            if (ok && r < rt.nrows) {
+                bf16_t* yrow_g = p.y + static_cast<size_t>(rt.row0 + r) * p.ld_y + p.out_off[tr.q];
 #pragma unroll
                 for (int chunk = 0; chunk < 8; ++chunk) {
                     if (chunk * 8 >= cols_left) continue;
@@ -458,8 +598,8 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
                 if (w8 == 0 && lane == 0) {
                     if (!s_fail) {
                         uint8_t* y0 = ring + s * stage_bytes + kbs * kBoxBytes;
-                        tma_store_2d(&my, p.out_off[q] + tile_col0, ti.row0, y0);
-                        tma_store_2d(&my, p.out_off[q] + tile_col0 + kKB, ti.row0, y0 + kBoxBytes);
+                        tma_store_2d(&my, p.out_off[tr.q] + tile_col0, rt.row0, y0);
+                        tma_store_2d(&my, p.out_off[tr.q] + tile_col0 + kKB, rt.row0, y0 + kBoxBytes);
                         bulk_commit();
                     }
                     bulk_wait_read();   // the stage may be refilled once the stores have read it
@@ -468,6 +608,7 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);   // this warp is done with stage s
+            more = tr.next(p, n_rt, n_items) && tr.next(p, n_rt, n_items);
         }
         if (w8 == 0 && lane == 0) bulk_wait_all();
     }
@@ -517,12 +658,6 @@ bool configure_once(const void* fn, size_t smem, int& configured_device, size_t&
 }
 
 // Output tiles per expand CTA (LORA_TC_TILES_PER_CTA overrides; tuning aid).
-int tiles_per_cta_env()
-{
-    const char* e = std::getenv("LORA_TC_TILES_PER_CTA");
-    const int v = (e && *e) ? std::atoi(e) : 16;
-    return v > 0 ? v : 16;
-}
 
 }  // namespace
 
@@ -583,9 +718,21 @@ cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const b
         !encode_tmap_bf16(&mvl, vl, n_rows, ld_p, ld_p, kTileM, kKB, true) ||
         !encode_tmap_bf16(&my, y, n_rows, ld_y, ld_y, kTileM, kKB, true))
         return cudaErrorInvalidValue;
+    static int n_sms = 0, sms_device = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidValue;
+    if (sms_device != dev) {
+        if (cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return cudaErrorInvalidValue;
+        sms_device = dev;
+    }
     ExpandTcParams p{};
-    p.tiles_per_cta = tiles_per_cta_env();
-    int total_chunks = 0;
+    int tiles_per_row = 0;
+    for (int q = 0; q < ps.n_proj; ++q) tiles_per_row += (ps.width[q] + kExpandN - 1) / kExpandN;
+    // Work items of up to 16 output tiles; fewer for small calls, so that
+    // every SM gets about three items and the last ones end together.
+    const long long rt_bound = (n_pos + kTileM - 1) / kTileM + static_cast<long long>(n_segs);
+    p.chunk = static_cast<int>(std::max(4LL, std::min<long long>(kChunkMax, rt_bound * tiles_per_row / (3LL * n_sms))));
+    p.chunk = std::max(1, env_int("LORA_TC_EXPAND_CHUNK", p.chunk));
     for (int q = 0; q < 4; ++q) {
         const int src = q < ps.n_proj ? q : 0;
         if (!encode_tmap_bf16(&mb[q], ps.B[src], static_cast<uint64_t>(n_slots) * ps.width[src], ps.r_slot,
@@ -595,8 +742,8 @@ cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const b
             p.out_off[q] = ps.out_off[q];
             p.width[q] = ps.width[q];
             p.col_tiles[q] = (ps.width[q] + kExpandN - 1) / kExpandN;
-            p.chunks[q] = (p.col_tiles[q] + p.tiles_per_cta - 1) / p.tiles_per_cta;
-            total_chunks += p.chunks[q];
+            p.chunks[q] = (p.col_tiles[q] + p.chunk - 1) / p.chunk;
+            p.n_chunks += p.chunks[q];
         }
     }
     p.n_proj = ps.n_proj;
@@ -613,13 +760,21 @@ cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const b
     p.status = status;
     const int kbs = r_pad64 / kKB;
     const int stages = kbs == 1 ? kStagesE : 2;
-    const size_t smem = static_cast<size_t>(2 * kbs + stages * (kbs + 2)) * kBoxBytes + 1024;
+    const int vbufs = kbs == 1 ? 2 : 1;
+    const size_t smem = static_cast<size_t>(vbufs * 2 * kbs + stages * (kbs + 2)) * kBoxBytes + 1024;
     static int configured = -1;
     static size_t configured_bytes = 0;
     if (!configure_once(reinterpret_cast<const void*>(sgmv_expand_tc_kernel), smem, configured, configured_bytes))
         return cudaErrorInvalidValue;
-    const dim3 grid((n_pos + kTileM - 1) / kTileM + n_segs, total_chunks);
-    sgmv_expand_tc_kernel<<<grid, kExpandThreadsP, smem, stream>>>(mvh, mvl, my, mb[0], mb[1], mb[2], mb[3], p);
+    // One CTA per SM (the shared memory allows no more), and enough CTAs that
+    // none takes more than kMaxItems items.
+    const long long items_bound = rt_bound * p.n_chunks;
+    long long grid = env_int("LORA_TC_EXPAND_GRID", n_sms);
+    grid = std::max(grid, (items_bound + kMaxItems - 1) / kMaxItems);   // at most kMaxItems items per CTA
+    grid = std::min(grid, items_bound);
+    if (grid > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+    sgmv_expand_tc_kernel<<<static_cast<unsigned>(grid), kExpandThreadsP, smem, stream>>>(mvh, mvl, my, mb[0], mb[1],
+                                                                                          mb[2], mb[3], p);
     note_launch();
     return cudaGetLastError();
 }
