@@ -46,11 +46,12 @@ __device__ __forceinline__ float dot8f(const uint4& a, const float* f, float acc
     return acc;
 }
 
+// Two fp32 values -> packed bf16 pair (lo in the low half), each rounded to
+// nearest-even: one conversion instruction for the pair.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
-    const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-    const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-    return l | (h << 16);
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);   // .x = lo (low half), .y = hi
+    return *reinterpret_cast<const uint32_t*>(&h2);
 }
 
 // y8 <- bf16_rne(y8 + acc) for 8 packed bf16 values.

@@ -565,14 +565,7 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
             const bool ok = !s_fail && mbar_wait(&acc_full[a], (i >> 1) & 1);
             if (!ok) s_fail = 1;
             tc_fence_after();
-            float d[64];
             const uint32_t tcol = tmem + a * kExpandN + (static_cast<uint32_t>(quarter * 32) << 16) + hc * kKB;
-            tmem_ld32(tcol, d);
-            tmem_ld32(tcol + 32, d + 32);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[a]);   // accumulator a may be overwritten now
-
             uint8_t* ybox = ring + s * stage_bytes + (kbs + hc) * kBoxBytes;
             uint8_t* sy = ybox + r * 128;
             const int tile_col0 = tr.ct * kExpandN;
@@ -581,15 +574,29 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
             // whole tile inside the segment's rows and the projection's columns:
             // results go back into the staged tile and leave by TMA bulk stores
             const bool whole = rt.nrows == kTileM && tile_col0 + kExpandN <= p.width[tr.q];
-            if (ok && r < rt.nrows) {
-                bf16_t* yrow_g = p.y + static_cast<size_t>(rt.row0 + r) * p.ld_y + p.out_off[tr.q];
+            const bool mine = ok && r < rt.nrows;
+            bf16_t* yrow_g = p.y + static_cast<size_t>(rt.row0 + min(r, rt.nrows - 1)) * p.ld_y + p.out_off[tr.q];
+            // 32 accumulator columns at a time, so registers are left for the
+            // four 16-byte pieces of y in flight
 #pragma unroll
-                for (int chunk = 0; chunk < 8; ++chunk) {
-                    if (chunk * 8 >= cols_left) continue;
-                    uint4* slot8 = reinterpret_cast<uint4*>(sy + ((chunk ^ (r & 7)) << 4));
-                    const uint4 res = add_round8(*slot8, d + chunk * 8);
-                    if (whole) *slot8 = res;
-                    else *reinterpret_cast<uint4*>(yrow_g + col0 + chunk * 8) = res;
+            for (int half = 0; half < 2; ++half) {
+                float d[32];
+                tmem_ld32(tcol + half * 32, d);
+                if (half == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acc_empty[a]);   // accumulator a may be overwritten now
+                }
+                if (mine) {
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const int chunk = half * 4 + c4;
+                        if (chunk * 8 >= cols_left) continue;
+                        uint4* slot8 = reinterpret_cast<uint4*>(sy + ((chunk ^ (r & 7)) << 4));
+                        const uint4 res = add_round8(*slot8, d + c4 * 8);
+                        if (whole) *slot8 = res;
+                        else *reinterpret_cast<uint4*>(yrow_g + col0 + chunk * 8) = res;
+                    }
                 }
             }
             if (whole) {
