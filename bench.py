@@ -131,10 +131,14 @@ ROUTE_KERNELS = {
 # dram__bytes_write.sum over the call's launches), keyed by workload; valid
 # only while the listed kernel sources hash to `src`.  Summaries in profiles/.
 NCU_TRAFFIC = {
-    "llama3b_decode": {"files": ['bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "35f8b683ba9da9fe",
-                       "bytes_per_call": 3436288},   # profiles/bgmv_fused_llama3b_decode.md
-    "stress70b": {"files": ['bgmv_grouped.cu', 'decode_common.cuh', 'common.cuh'], "src": "80c90b0a7b77bbd7",
-                  "bytes_per_call": 987868032},   # profiles/bgmv_grouped_stress70b.md
+    "llama3b_decode": {"files": ['bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "3a350bbfe24a6d79",
+             "bytes_per_call": 3435680},   # profiles/bgmv_fused_llama3b_decode.md
+    "stress70b": {"files": ['bgmv_grouped.cu', 'decode_common.cuh', 'common.cuh'], "src": "39f626336a236965",
+             "bytes_per_call": 988240896},   # profiles/bgmv_grouped_stress70b.md
+    "mistral7b_prefill": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "5998f7be0360734f",
+             "bytes_per_call": 2060215616},   # profiles/sgmv_tc_mistral7b_prefill.md
+    "mixed": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "e3827a22ab74ebd8",
+             "bytes_per_call": 113042432},   # profiles/sgmv_tc_mistral7b_prefill.md
 }
 
 
