@@ -8,6 +8,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "cluster.cuh"
 #include "common.cuh"
 
 namespace lora {
@@ -92,30 +93,6 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
-
-__device__ __forceinline__ uint32_t cluster_rank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory"); }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory"); }
-
-__device__ __forceinline__ uint32_t map_rank(uint32_t local_addr, uint32_t rank)
-{
-    uint32_t remote;
-    asm("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(local_addr), "r"(rank));
-    return remote;
-}
-// Plain (non-volatile) DSMEM load: ordering against the partials' writes is
-// given by the cluster barrier, so independent loads may be issued together.
-__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t remote)
-{
-    float2 v;
-    asm("ld.shared::cluster.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(remote));
-    return v;
-}
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
 {

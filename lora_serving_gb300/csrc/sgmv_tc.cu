@@ -140,8 +140,48 @@ struct ShrinkTcParams {
     bf16_t* vl;
     int ld_p;            // plane row length: n_proj * r_pad64
     int r_pad64;         // r_slot rounded up to 64 (plane columns per projection)
+    int ks;              // CTAs per row tile (a cluster), each a slice of K
     int32_t* status;
 };
+
+// Rows of v for one tile row r (16 columns from c, fp32) -> the output form.
+__device__ __forceinline__ void store_v16(const ShrinkTcParams& p, size_t row, int c, const float* v)
+{
+    if (p.mode == 0) {
+        float4* dst = reinterpret_cast<float4*>(p.v + row * p.ld_v + c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        return;
+    }
+    const int q = c / p.r_slot, jj = c - q * p.r_slot;
+    uint32_t hi[8], lo[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+        const float2 hf = __bfloat1622float2(h);
+        const __nv_bfloat162 l = __floats2bfloat162_rn(v[2 * i] - hf.x, v[2 * i + 1] - hf.y);
+        hi[i] = *reinterpret_cast<const uint32_t*>(&h);
+        lo[i] = *reinterpret_cast<const uint32_t*>(&l);
+    }
+    const size_t off = row * p.ld_p + q * p.r_pad64 + jj;
+    uint4* dh = reinterpret_cast<uint4*>(p.vh + off);
+    uint4* dl = reinterpret_cast<uint4*>(p.vl + off);
+    dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+    dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+}
+
+// Zeroes the planes' columns past r_slot in one row (the expand's K runs to r_pad64).
+__device__ __forceinline__ void zero_plane_padding(const ShrinkTcParams& p, size_t row)
+{
+    for (int q = 0; q < p.n_proj; ++q)
+        for (int jj = p.r_slot; jj < p.r_pad64; jj += 8) {
+            const size_t off = row * p.ld_p + q * p.r_pad64 + jj;
+            *reinterpret_cast<uint4*>(p.vh + off) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(p.vl + off) = make_uint4(0, 0, 0, 0);
+        }
+}
 
 __global__ void __launch_bounds__(kShrinkThreads, 1)
 sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap ma0,
@@ -154,20 +194,26 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
     __shared__ int s_fail;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    const TileInfo ti = find_tile<kShrinkThreads>(p.seg_starts, p.seg_slot, p.n_segs, p.n_pos, blockIdx.x);
+    // With ks > 1 a cluster of ks CTAs shares a row tile, CTA c reducing K
+    // blocks [c n_kb / ks, (c+1) n_kb / ks); the fp32 partial accumulators
+    // meet in distributed shared memory and are summed in a fixed order.
+    const int crank = p.ks > 1 ? static_cast<int>(cluster_rank()) : 0;
+    const TileInfo ti = find_tile<kShrinkThreads>(p.seg_starts, p.seg_slot, p.n_segs, p.n_pos, blockIdx.x / p.ks);
     if (!ti.found) {
         if (ti.bad && blockIdx.x == 0 && tid == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
         return;
     }
     if (ti.slot >= p.n_slots || ti.slot < -1) {
-        if (tid == 0) flag(p.status, LORA_DEV_SLOT_OUT_OF_RANGE);
+        if (tid == 0 && crank == 0) flag(p.status, LORA_DEV_SLOT_OUT_OF_RANGE);
         return;
     }
     const CUtensorMap* amap[4] = {&ma0, &ma1, &ma2, &ma3};
     const int S = p.stages;
     const int stage_bytes = kBoxBytes + p.R * 128;
     uint8_t* base = align1024(smem_raw);
-    const int n_kb = (p.h_in + kKB - 1) / kKB;
+    const int n_kb_all = (p.h_in + kKB - 1) / kKB;
+    const int kb0 = crank * n_kb_all / p.ks;
+    const int n_kb = (crank + 1) * n_kb_all / p.ks - kb0;   // >= 1: the launcher keeps ks <= n_kb_all
 
     uint32_t ncols = 32;   // accumulator columns: a power of two >= R
     while (ncols < static_cast<uint32_t>(p.R)) ncols <<= 1;
@@ -197,9 +243,10 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
             }
             uint8_t* st = base + s * stage_bytes;
             mbar_expect_tx(&full[s], stage_bytes);
-            tma_load_2d(st, &mx, kb * kKB, ti.row0, &full[s]);
+            tma_load_2d(st, &mx, (kb0 + kb) * kKB, ti.row0, &full[s]);
             for (int q = 0; q < p.n_proj; ++q)
-                tma_load_2d(st + kBoxBytes + q * p.r_slot * 128, amap[q], kb * kKB, ti.slot * p.r_slot, &full[s]);
+                tma_load_2d(st + kBoxBytes + q * p.r_slot * 128, amap[q], (kb0 + kb) * kKB, ti.slot * p.r_slot,
+                            &full[s]);
         }
     } else if (warp == 1 && lane == 0) {
         // MMA issuer: 4 x (128 x R x 16) per K block, accumulating in TMEM
@@ -228,43 +275,57 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
     bool ok = mbar_wait(&done, 0);
     tc_fence_after();
     const int r = warp * 32 + lane;   // tile row = TMEM lane
-    const bool row_ok = r < ti.nrows;
-    const size_t row = static_cast<size_t>(ti.row0 + r);
-    for (int c = 0; c < p.R; c += 16) {
-        float v[16];
-        tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
-        if (!row_ok || !ok) continue;
-        if (p.mode == 0) {
-            float4* dst = reinterpret_cast<float4*>(p.v + row * p.ld_v + c);
+    if (p.ks == 1) {
+        const bool row_ok = r < ti.nrows;
+        const size_t row = static_cast<size_t>(ti.row0 + r);
+        for (int c = 0; c < p.R; c += 16) {
+            float v[16];
+            tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
+            if (row_ok && ok) store_v16(p, row, c, v);
+        }
+        if (p.mode == 1 && row_ok && ok && p.r_pad64 > p.r_slot) zero_plane_padding(p, row);
+    } else {
+        // partial accumulator -> shared memory (over the consumed ring), row
+        // pitch R + 4 floats: 16-byte stores from 8 consecutive rows meet no
+        // bank twice
+        float* red = reinterpret_cast<float*>(base);
+        const int pitch = p.R + 4;
+        for (int c = 0; c < p.R; c += 16) {
+            float v[16];
+            tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
+            float4* dst = reinterpret_cast<float4*>(red + r * pitch + c);
 #pragma unroll
             for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-        } else {
-            const int q = c / p.r_slot, jj = c - q * p.r_slot;
-            uint32_t hi[8], lo[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-                const float2 hf = __bfloat1622float2(h);
-                const __nv_bfloat162 l = __floats2bfloat162_rn(v[2 * i] - hf.x, v[2 * i + 1] - hf.y);
-                hi[i] = *reinterpret_cast<const uint32_t*>(&h);
-                lo[i] = *reinterpret_cast<const uint32_t*>(&l);
-            }
-            const size_t off = row * p.ld_p + q * p.r_pad64 + jj;
-            uint4* dh = reinterpret_cast<uint4*>(p.vh + off);
-            uint4* dl = reinterpret_cast<uint4*>(p.vl + off);
-            dh[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            dh[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-            dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
         }
-    }
-    if (p.mode == 1 && row_ok && ok && p.r_pad64 > p.r_slot) {   // zero the plane padding
-        for (int q = 0; q < p.n_proj; ++q)
-            for (int jj = p.r_slot; jj < p.r_pad64; jj += 8) {
-                const size_t off = row * p.ld_p + q * p.r_pad64 + jj;
-                *reinterpret_cast<uint4*>(p.vh + off) = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(p.vl + off) = make_uint4(0, 0, 0, 0);
+        __syncthreads();
+        cluster_arrive();
+        cluster_wait();
+        // CTA c sums rows [c * 128 / ks, (c + 1) * 128 / ks) over the cluster,
+        // 16 columns per item, peers in rank order
+        const int r_lo = crank * kTileM / p.ks, r_hi = (crank + 1) * kTileM / p.ks;
+        const int per_row = p.R / 16;
+        const uint32_t red_s = smem_u32(red);
+        for (int it = tid; it < (r_hi - r_lo) * per_row; it += kShrinkThreads) {
+            const int rr = r_lo + it / per_row, c = (it - (it / per_row) * per_row) * 16;
+            float v[16] = {};
+            for (int peer = 0; peer < p.ks; ++peer) {
+                const uint32_t src = map_rank(red_s + 4u * static_cast<uint32_t>(rr * pitch + c), peer);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 f = ld_dsmem_f4(src + 16u * i);
+                    v[4 * i] += f.x;
+                    v[4 * i + 1] += f.y;
+                    v[4 * i + 2] += f.z;
+                    v[4 * i + 3] += f.w;
+                }
             }
+            if (rr < ti.nrows && ok) store_v16(p, static_cast<size_t>(ti.row0 + rr), c, v);
+        }
+        if (p.mode == 1 && ok && p.r_pad64 > p.r_slot)
+            for (int rr = r_lo + tid; rr < min(r_hi, ti.nrows); rr += kShrinkThreads)
+                zero_plane_padding(p, static_cast<size_t>(ti.row0 + rr));
+        cluster_arrive();   // peers may leave once everyone has read their partials
+        cluster_wait();
     }
     tc_fence_before();
     __syncthreads();
@@ -702,15 +763,42 @@ cudaError_t launch_sgmv_shrink_tc(float* v, int ld_v, bf16_t* vh, bf16_t* vl, co
     p.r_pad64 = (ps.r_slot + kKB - 1) / kKB * kKB;
     p.ld_p = ps.n_proj * p.r_pad64;
     p.status = status;
-    const size_t smem = shrink_smem(p.stages, R);
+    // Few row tiles: split K over a cluster of ks CTAs per tile so that the
+    // grid covers the SMs (each CTA keeps at least two K blocks).
+    static int n_sms = 0, sms_device = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidValue;
+    if (sms_device != dev) {
+        if (cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return cudaErrorInvalidValue;
+        sms_device = dev;
+    }
+    const int tiles = (n_pos + kTileM - 1) / kTileM + n_segs;   // upper bound
+    const int n_kb = (h_in + kKB - 1) / kKB;
+    int ks = 1;
+    while (ks < 8 && static_cast<long long>(tiles) * ks < n_sms && n_kb >= 4 * ks) ks *= 2;
+    p.ks = std::max(1, std::min(env_int("LORA_TC_SHRINK_KS", ks), n_kb));
+    // the cluster's partials reuse the ring: 128 rows x (R + 4) fp32
+    const size_t red = p.ks > 1 ? static_cast<size_t>(kTileM) * (R + 4) * sizeof(float) + 1024 : 0;
+    const size_t smem = std::max(shrink_smem(p.stages, R), red);
     static int configured = -1;
     static size_t configured_bytes = 0;
     if (!configure_once(reinterpret_cast<const void*>(sgmv_shrink_tc_kernel), smem, configured, configured_bytes))
         return cudaErrorInvalidValue;
-    const int tiles = (n_pos + kTileM - 1) / kTileM + n_segs;   // upper bound
-    sgmv_shrink_tc_kernel<<<tiles, kShrinkThreads, smem, stream>>>(mx, ma[0], ma[1], ma[2], ma[3], p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles * p.ks));
+    cfg.blockDim = dim3(kShrinkThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = p.ks;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, sgmv_shrink_tc_kernel, mx, ma[0], ma[1], ma[2], ma[3], p);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const bf16_t* vl, const ProjSet& ps,

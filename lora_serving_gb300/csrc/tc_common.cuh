@@ -13,6 +13,8 @@
 #include <cuda.h>
 #include <stdint.h>
 
+#include "cluster.cuh"
+
 namespace lora {
 namespace tc {
 

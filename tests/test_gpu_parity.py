@@ -495,9 +495,28 @@ def test_apply_prefill_tensor_core(h_in, widths, rank, lens, slots, mode):
     check_bf16(got, oracle_group(wl, "g"), wl.ids, wl.y["g"], f"tc h_in={h_in} rank={rank}")
 
 
-def test_sgmv_shrink_tensor_core_fp32():
+@pytest.mark.parametrize("ks", [1, 2, 8])
+@pytest.mark.parametrize("h_in,widths,rank,lens,slots", [
+    (1024, (1024,), 64, [64, 640, 1], [2, 2, 0]),                        # 16 K blocks over the cluster
+    (8200, (4096,), 16, [200], [2]),                                     # ragged last K block, uneven split
+    (512, (512, 128, 128), 32, [70, 200, 128], [0, 3, 1]),               # 96 ranks: 6 column groups per row
+])
+def test_tensor_core_shrink_cluster_split(h_in, widths, rank, lens, slots, ks, monkeypatch):
+    """The tensor-core shrink with K split over a cluster of ks CTAs per row
+    tile (partials summed through distributed shared memory) and without."""
+    monkeypatch.setenv("LORA_TC_SHRINK_KS", str(ks))
+    ids = _segments(lens, slots)
+    wl = _small(ids, int(sum(lens)), rank=rank, h_in=h_in, widths=widths, seed=rank + ks, mode="accumulate")
+    got = _run_apply(wl, "g")
+    check_bf16(got, oracle_group(wl, "g"), wl.ids, wl.y["g"], f"tc ks={ks} h_in={h_in}")
+
+
+@pytest.mark.parametrize("ks", [1, 4])
+def test_sgmv_shrink_tensor_core_fp32(ks, monkeypatch):
     """lora_sgmv_shrink on long contiguous segments (tensor-core route) gives
-    fp32 v within the fp32 accumulation bound of the oracle's."""
+    fp32 v within the fp32 accumulation bound of the oracle's, with K whole
+    or split over a cluster."""
+    monkeypatch.setenv("LORA_TC_SHRINK_KS", str(ks))
     lens, slots = [150, 80, 300], [2, -1, 0]
     ids = _segments(lens, slots)
     wl = _small(ids, ids.size, rank=32, h_in=1024, widths=(64,), seed=9)
