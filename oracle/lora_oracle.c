@@ -297,3 +297,24 @@ void oracle_expand(int n_rows, const int32_t* ids, const double* v, int64_t ld_v
     add_round(n_rows, ids, d, w, y, ld_y, off, w);
     free(d);
 }
+
+/*
+ * Merged weight for single-tenant serving ([MLS], interviewer follow-ups:
+ * W' = W + B A gives the same model as the base plus the adapter's delta):
+ *     W'[o][k] = bf16_rne(W[o][k] + sign * sum_{j < r} B'[o][j] A[j][k])
+ * with sign = +1 (merge) or -1 (unmerge), the sum over the true rank r in
+ * double, and one rounding.  W is [out][ld_w], A [r][ld_a], B' [out][ld_b].
+ */
+void oracle_merge(const uint16_t* W, int64_t ld_w, int out, int h_in, const uint16_t* A, int64_t ld_a,
+                  const uint16_t* Bp, int64_t ld_b, int r, int sign, uint16_t* W_out)
+{
+    for (int o = 0; o < out; ++o) {
+        for (int k = 0; k < h_in; ++k) {
+            double d = 0.0;
+            for (int j = 0; j < r; ++j)
+                d += oracle_bf16_to_double(Bp[(int64_t)o * ld_b + j]) * oracle_bf16_to_double(A[(int64_t)j * ld_a + k]);
+            W_out[(int64_t)o * ld_w + k] =
+                oracle_double_to_bf16(oracle_bf16_to_double(W[(int64_t)o * ld_w + k]) + (double)sign * d);
+        }
+    }
+}

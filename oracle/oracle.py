@@ -26,7 +26,7 @@ _lib = None
 
 __all__ = [
     "build", "bf16_to_f64", "f64_to_bf16", "scale", "fold_B", "build_metadata",
-    "Adapters", "shrink", "delta", "apply_projection", "expand",
+    "Adapters", "shrink", "delta", "apply_projection", "expand", "merge",
 ]
 
 
@@ -65,6 +65,7 @@ def _load():
             lib.oracle_apply_projection.argtypes = [i32, P, P, i64, i32, P, i64, i32, i32,
                                                     P, P, P, P, P, P]
             lib.oracle_expand.argtypes = [i32, P, P, i64, P, i64, i32, i32, P, P, P, P]
+            lib.oracle_merge.argtypes = [P, i64, i32, i32, P, i64, P, i64, i32, i32, P]
             _lib = lib
     return _lib
 
@@ -205,3 +206,18 @@ def expand(ids, v, y_bits, off: int, ad: Adapters) -> np.ndarray:
     _load().oracle_expand(T, _ptr(ids), _ptr(v), v.shape[1], _ptr(y), y.shape[1], int(off),
                           ad.w, _ptr(ad.rp), _ptr(ad.scale), _ptr(ad.B_cat), _ptr(ad.B_off))
     return y
+
+
+def merge(W_bits, A_bits, Bp_bits, sign: int) -> np.ndarray:
+    """W' = bf16_rne(W + sign * B' A) (sign +1 merge, -1 unmerge); W [out][h_in],
+    A [r][h_in], B' [out][r], all bf16 bits; the true rank r is A's row count."""
+    lib = _load()
+    W = _c(W_bits, np.uint16)
+    A = _c(A_bits, np.uint16)
+    Bp = _c(Bp_bits, np.uint16)
+    out, h_in = W.shape
+    r = A.shape[0]
+    assert A.shape == (r, h_in) and Bp.shape == (out, r) and sign in (1, -1)
+    res = np.empty_like(W)
+    lib.oracle_merge(_ptr(W), h_in, out, h_in, _ptr(A), h_in, _ptr(Bp), r, r, sign, _ptr(res))
+    return res

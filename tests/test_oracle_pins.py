@@ -340,3 +340,72 @@ def test_metadata_rejects_out_of_range_ids():
         O.build_metadata(np.array([0, 4], np.int32), 1, 4)
     with pytest.raises(ValueError):
         O.build_metadata(np.array([-2], np.int32), 0, 4)
+
+
+# --------------------------------------------------------------- merge ----
+# The merged weight W' = bf16(W +/- B'A) ([MLS], interviewer follow-ups).
+
+def _small_ints_bf16(rng, shape, lo, hi):
+    """Small integers: exact in bf16, and every sum below stays exact too."""
+    return O.f64_to_bf16(rng.integers(lo, hi + 1, shape).astype(np.float64))
+
+
+def test_merge_zero_adapter_leaves_weight_bit_identical():
+    g = torch.Generator().manual_seed(21)
+    W = _rand_bf16(g, (24, 40))
+    A = _rand_bf16(g, (5, 40))
+    Bp = np.zeros((24, 5), np.uint16)
+    for sign in (1, -1):
+        np.testing.assert_array_equal(O.merge(W, A, Bp, sign), W)
+
+
+def test_merge_rank_one_closed_form():
+    """A = a e_i^T (one row), B' = b e_j: only W[j][i] moves, by sign * a * b, one rounding."""
+    g = torch.Generator().manual_seed(3)
+    W = _rand_bf16(g, (16, 32))
+    a, b, i, j = 0.71875, -1.40625, 9, 4   # both exact in bf16
+    A = np.zeros((1, 32), np.uint16)
+    A[0, i] = O.f64_to_bf16(np.array([a]))[0]
+    Bp = np.zeros((16, 1), np.uint16)
+    Bp[j, 0] = O.f64_to_bf16(np.array([b]))[0]
+    for sign in (1, -1):
+        got = O.merge(W, A, Bp, sign)
+        expect = W.copy()
+        expect[j, i] = O.f64_to_bf16(np.array([O.bf16_to_f64(W[j:j + 1, i])[0] + sign * a * b]))[0]
+        np.testing.assert_array_equal(got, expect)
+
+
+def test_merge_then_unmerge_restores_exact_weights():
+    """With small integers every value and sum is exact in bf16, so unmerge
+    undoes merge bit for bit (a swapped sign or operand would not)."""
+    rng = np.random.default_rng(11)
+    W = _small_ints_bf16(rng, (12, 20), -40, 40)
+    A = _small_ints_bf16(rng, (3, 20), -3, 3)
+    Bp = _small_ints_bf16(rng, (12, 3), -3, 3)
+    merged = O.merge(W, A, Bp, 1)
+    # spot value by hand: an integer sum
+    w = O.bf16_to_f64(W)
+    expect = w + O.bf16_to_f64(Bp) @ O.bf16_to_f64(A)
+    np.testing.assert_array_equal(O.bf16_to_f64(merged), expect)
+    np.testing.assert_array_equal(O.merge(merged, A, Bp, -1), W)
+
+
+def test_merged_weight_applied_equals_base_plus_delta():
+    """W' x = W x + B'(A x) up to W's one rounding: the merge checked against
+    the oracle's separate delta path (shrink then expand, per row)."""
+    for seed in range(3):
+        A, B, scales, x, ids = _tiny_problem(seed, ranks=(4, 8))
+        ad = O.Adapters(A, B, scales)
+        d = O.delta(ids, x, ad)
+        g = torch.Generator().manual_seed(100 + seed)
+        W = _rand_bf16(g, (ad.w, ad.h_in))
+        xd = O.bf16_to_f64(x)
+        for k in range(len(A)):
+            Bp = O.fold_B(B[k], scales[k])
+            merged = O.bf16_to_f64(O.merge(W, A[k], Bp, 1))
+            # one bf16 rounding per weight: |error| <= 2^-9 |w'| per element
+            for t in np.nonzero(ids == k)[0]:
+                lhs = merged @ xd[t]
+                rhs = O.bf16_to_f64(W) @ xd[t] + d[t]
+                bound = 2.0 ** -8 * (np.abs(merged) @ np.abs(xd[t])) + 1e-12
+                assert np.all(np.abs(lhs - rhs) <= bound), (seed, k, t)
