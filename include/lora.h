@@ -247,6 +247,28 @@ lora_status_t lora_apply_noalloc(lora_bf16_t* y, int ld_y, const lora_bf16_t* x,
                                  const lora_meta_t* meta, uint32_t flags, int32_t* dev_status,
                                  lora_stream_t stream);
 
+/*
+ * Merged weight for single-tenant serving [MLS, interviewer follow-ups:
+ * merging W' = W + B A gives the same model]:
+ *   W[o][k] <- bf16_rne(W[o][k] + sign * sum_j B[o][j] A[j][k])
+ * sign = +1 folds the adapter into the base weight, -1 takes it out again
+ * (W comes back to within one bf16 rounding per element; exactly when no
+ * rounding happened).  The sum runs in fp32 over the slot rank (padding
+ * ranks are zero).
+ *   W      [dev] [out][ld_w] bf16, updated in place (16-byte aligned,
+ *          ld_w >= h_in, both multiples of 8)
+ *   A      [dev] [r_slot][h_in]: one adapter slot of the A store
+ *          (the store pointer + slot * r_slot * h_in)
+ *   B      [dev] [out][r_slot]: the same slot of the scaled B store
+ * Errors (before anything is enqueued): LORA_ERR_INVALID_ARG (null pointer,
+ * non-positive size, sign not +1 or -1), LORA_ERR_SHAPE (ld_w < h_in, more
+ * than 4M rows), LORA_ERR_RANK_EXCEEDS_SLOT (r_slot > LORA_MAX_RANK),
+ * LORA_ERR_ALIGNMENT, LORA_ERR_CUDA (launch).  No device-side failure is
+ * possible: the kernel reads no indices.
+ */
+lora_status_t lora_merge(lora_bf16_t* W, int ld_w, int out, int h_in, const lora_bf16_t* A,
+                         const lora_bf16_t* B, int r_slot, int sign, lora_stream_t stream);
+
 /* ------------------------------------------------------------------ *
  *  Host helpers (host pointers, synchronous)
  * ------------------------------------------------------------------ */

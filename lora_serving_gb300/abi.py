@@ -37,7 +37,7 @@ EXPORTS = (
     "lora_bgmv_shrink", "lora_bgmv_expand", "lora_sgmv_shrink", "lora_sgmv_expand",
     "lora_apply", "lora_apply_workspace_bytes", "lora_build_metadata",
     "lora_prepare_adapter", "lora_slot_rank", "lora_read_device_status", "lora_status_string",
-    "lora_kernel_launch_count", "lora_apply_noalloc",
+    "lora_kernel_launch_count", "lora_apply_noalloc", "lora_merge",
 )
 LORA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -88,6 +88,7 @@ def load(path: str | None = None):
         "lora_slot_rank": [P, i32],
         "lora_read_device_status": [P, P, P],
         "lora_status_string": [i32],
+        "lora_merge": [P, i32, i32, i32, P, P, i32, i32, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -189,6 +190,16 @@ def lora_apply_noalloc(y, x, h_in, projs, r_slot, n_slots, meta, *, flags=0, dev
     _check("lora_apply_noalloc", load().lora_apply_noalloc(
         _p(y), _ld(y), _p(x), _ld(x), h_in, ctypes.addressof(projs), len(projs), r_slot, n_slots,
         ctypes.addressof(meta), int(flags), _p(dev_status), _stream(stream)))
+
+
+def lora_merge(W, A, B, sign, *, stream=None):
+    """W [out][h_in] (row stride ld) += sign * B A, one bf16 rounding; A is one
+    adapter slot [r_slot][h_in] of the A store, B the same slot [out][r_slot]
+    of the scaled B store; sign +1 merges, -1 unmerges."""
+    out, h_in = int(W.shape[0]), int(W.shape[1])
+    r_slot = int(A.shape[0])
+    _check("lora_merge", load().lora_merge(_p(W), _ld(W), out, h_in, _p(A), _p(B), r_slot, int(sign),
+                                           _stream(stream)))
 
 
 def lora_apply_workspace_bytes(n_rows, n_proj, r_slot) -> int:

@@ -309,6 +309,19 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
     return LORA_OK;
 }
 
+lora_status_t lora_merge(lora_bf16_t* W, int ld_w, int out, int h_in, const lora_bf16_t* A,
+                         const lora_bf16_t* B, int r_slot, int sign, lora_stream_t stream)
+{
+    if (!W || out <= 0 || h_in <= 0 || r_slot <= 0 || (sign != 1 && sign != -1)) return LORA_ERR_INVALID_ARG;
+    if (r_slot > LORA_MAX_RANK) return LORA_ERR_RANK_EXCEEDS_SLOT;
+    if (ld_w < h_in || out > (1 << 22)) return LORA_ERR_SHAPE;
+    if (!aligned16(W) || ld_w % 8 != 0 || h_in % 8 != 0 || r_slot % 8 != 0) return LORA_ERR_ALIGNMENT;
+    LORA_TRY(check_store(A));
+    LORA_TRY(check_store(B));
+    return cuda_status(lora::launch_merge(W, ld_w, out, h_in, A, B, r_slot, sign,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
 uint64_t lora_kernel_launch_count(void) { return lora::g_launches.load(std::memory_order_relaxed); }
 
 lora_status_t lora_read_device_status(const int32_t* dev_status, int32_t* out, lora_stream_t stream)

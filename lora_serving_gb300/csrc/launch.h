@@ -64,4 +64,8 @@ cudaError_t launch_bgmv_grouped(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, 
                                 int n_pos, int max_group_len, int n_rows, int n_slots, unsigned flags,
                                 bf16_t* vh, bf16_t* vl, int32_t* status, cudaStream_t stream);
 
+// W += sign * B A over one adapter slot (merge / unmerge), one rounding.
+cudaError_t launch_merge(bf16_t* W, int ld_w, int out, int h_in, const bf16_t* A, const bf16_t* B, int r_slot,
+                         int sign, cudaStream_t stream);
+
 }  // namespace lora

@@ -1,0 +1,154 @@
+// merge.cu -- fold one adapter into (or out of) a base weight, for serving a
+// single tenant at the base model's cost.
+//
+// Multi-LoRA serving note, "interviewer follow-ups": merging W' = W + B A
+// gives the same model as the base plus the adapter's delta.  Here
+//   W[o][k] <- bf16_rne(W[o][k] + sign * sum_j B'[o][j] A[j][k]),
+// sign = +1 (merge) or -1 (unmerge), B' the folded store (scale applied),
+// the sum in fp32 over the slot rank (padding ranks are zero).
+//
+// One CTA per 64 x 128 tile of W: the tile, its 64 rows of B' and 128
+// columns of A arrive by 16-byte cp.async; warp w forms rows 16w..16w+15 of
+// B'A on the tensor cores (mma.sync m16n8k16, fp32 accumulate; A enters as
+// the col-major operand through transposing ldmatrix); each thread adds
+// its accumulator fragments into the staged tile and rounds once; the tile
+// leaves by coalesced 16-byte stores.  HBM-bound: W is read and written
+// once, A and B' come from L2 after their first use.
+
+#include "decode_common.cuh"
+#include "launch.h"
+
+namespace lora {
+
+namespace {
+
+using namespace dec;
+
+constexpr int kMRows = 64;                 // W rows per CTA
+constexpr int kMCols = 128;                // W columns per CTA
+constexpr int kMThreads = 128;             // 4 warps, 16 rows each
+constexpr int kMPitch = kMCols + 8;        // bf16 pitch of the W and A tiles (conflict-free ldmatrix)
+
+__device__ __forceinline__ void ldmatrix_x2_trans(uint32_t addr, uint32_t& r0, uint32_t& r1)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];\n"
+                 : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
+struct MergeParams {
+    bf16_t* W;
+    int ld_w, out, h_in;
+    const bf16_t* A;   // [r_slot][h_in]
+    const bf16_t* B;   // [out][r_slot]
+    int r_slot, r_pad; // r_pad: r_slot rounded up to 16 (the mma K)
+    float sign;
+};
+
+__global__ void __launch_bounds__(kMThreads)
+merge_kernel(MergeParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int bp_pitch = p.r_pad + 8;
+    bf16_t* sW = reinterpret_cast<bf16_t*>(smem);                       // [64][kMPitch]
+    bf16_t* sB = sW + kMRows * kMPitch;                                 // [64][r_pad + 8]
+    bf16_t* sA = sB + kMRows * bp_pitch;                                // [r_pad][kMPitch]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int o0 = blockIdx.y * kMRows, k0 = blockIdx.x * kMCols;
+
+    // ---- stage the W tile, B' rows and A columns (zero outside the matrices) ----
+    for (int i = tid; i < kMRows * (kMCols / 8); i += kMThreads) {
+        const int r = i / (kMCols / 8), c = (i % (kMCols / 8)) * 8;
+        const bool ok = o0 + r < p.out && k0 + c < p.h_in;
+        cp_async16(smem_u32(sW + r * kMPitch + c),
+                   ok ? static_cast<const void*>(p.W + static_cast<size_t>(o0 + r) * p.ld_w + k0 + c) : p.W, ok);
+    }
+    const int bch = p.r_pad / 8;
+    for (int i = tid; i < kMRows * bch; i += kMThreads) {
+        const int r = i / bch, c = (i % bch) * 8;
+        const bool ok = o0 + r < p.out && c < p.r_slot;
+        cp_async16(smem_u32(sB + r * bp_pitch + c),
+                   ok ? static_cast<const void*>(p.B + static_cast<size_t>(o0 + r) * p.r_slot + c) : p.B, ok);
+    }
+    for (int i = tid; i < p.r_pad * (kMCols / 8); i += kMThreads) {
+        const int j = i / (kMCols / 8), c = (i % (kMCols / 8)) * 8;
+        const bool ok = j < p.r_slot && k0 + c < p.h_in;
+        cp_async16(smem_u32(sA + j * kMPitch + c),
+                   ok ? static_cast<const void*>(p.A + static_cast<size_t>(j) * p.h_in + k0 + c) : p.A, ok);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // ---- B'A for rows 16w..16w+15, all 128 columns (16 n-tiles of 8) ----
+    float acc[16][4] = {};
+    const int mi = lane >> 3, mr = lane & 7, l16 = lane & 15;
+    for (int kk = 0; kk < p.r_pad; kk += 16) {
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4(smem_u32(sB + (warp * 16 + (mi & 1) * 8 + mr) * bp_pitch + kk + (mi >> 1) * 8), a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+            uint32_t b0, b1;
+            ldmatrix_x2_trans(smem_u32(sA + (kk + l16) * kMPitch + nt * 8), b0, b1);
+            mma_bf16_16816(acc[nt], a0, a1, a2, a3, b0, b1);
+        }
+    }
+
+    // ---- W += sign * B'A at the fragment positions, one rounding ----
+    const int g = lane >> 2, q2 = (lane & 3) * 2;
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t* w2 = reinterpret_cast<uint32_t*>(sW + (warp * 16 + g + h * 8) * kMPitch + nt * 8 + q2);
+            const uint32_t old = *w2;
+            *w2 = pack_bf16x2(bf16_lo(old) + p.sign * acc[nt][2 * h], bf16_hi(old) + p.sign * acc[nt][2 * h + 1]);
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < kMRows * (kMCols / 8); i += kMThreads) {
+        const int r = i / (kMCols / 8), c = (i % (kMCols / 8)) * 8;
+        if (o0 + r < p.out && k0 + c < p.h_in)
+            *reinterpret_cast<uint4*>(p.W + static_cast<size_t>(o0 + r) * p.ld_w + k0 + c) =
+                *reinterpret_cast<const uint4*>(sW + r * kMPitch + c);
+    }
+}
+
+size_t merge_smem(int r_pad)
+{
+    return sizeof(bf16_t) * (static_cast<size_t>(kMRows) * kMPitch + static_cast<size_t>(kMRows) * (r_pad + 8) +
+                             static_cast<size_t>(r_pad) * kMPitch);
+}
+
+}  // namespace
+
+cudaError_t launch_merge(bf16_t* W, int ld_w, int out, int h_in, const bf16_t* A, const bf16_t* B, int r_slot,
+                         int sign, cudaStream_t stream)
+{
+    MergeParams p{};
+    p.W = W;
+    p.ld_w = ld_w;
+    p.out = out;
+    p.h_in = h_in;
+    p.A = A;
+    p.B = B;
+    p.r_slot = r_slot;
+    p.r_pad = (r_slot + 15) / 16 * 16;
+    p.sign = sign > 0 ? 1.f : -1.f;
+    const size_t smem = merge_smem(p.r_pad);
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(merge_smem((LORA_MAX_RANK + 15) / 16 * 16)));
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    const dim3 grid((h_in + kMCols - 1) / kMCols, (out + kMRows - 1) / kMRows);
+    merge_kernel<<<grid, kMThreads, smem, stream>>>(p);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace lora

@@ -536,3 +536,72 @@ def test_sgmv_shrink_tensor_core_fp32(ks, monkeypatch):
     act = wl.ids >= 0
     assert np.all(np.abs(got[act] - ref[act]) <= bound[act])
     assert np.all(got[~act] == -3.0), "rows of slot -1 segments must not be written"
+
+
+# ------------------------------------------------------ merge / unmerge ----
+
+def _merge_case(out, h_in, r, r_slot, seed, std_w=1.0):
+    g = torch.Generator().manual_seed(seed)
+    W = (torch.randn(out, h_in, generator=g) * std_w).to(torch.bfloat16)
+    A = torch.zeros(r_slot, h_in, dtype=torch.bfloat16)
+    A[:r] = (torch.randn(r, h_in, generator=g) * 0.05).to(torch.bfloat16)
+    Bp = torch.zeros(out, r_slot, dtype=torch.bfloat16)
+    Bp[:, :r] = (torch.randn(out, r, generator=g) * 0.05).to(torch.bfloat16)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    return W, A, Bp, bits(W), bits(A[:r]), bits(Bp[:, :r])
+
+
+@pytest.mark.parametrize("out,h_in,r,r_slot", [
+    (300, 520, 13, 16),      # ragged row and column tiles; padding ranks
+    (4096, 1024, 64, 64),    # full tiles, rank 64
+    (70, 136, 100, 128),     # rank above 64: eight K steps
+])
+@pytest.mark.parametrize("sign", [1, -1])
+def test_merge_vs_oracle(out, h_in, r, r_slot, sign):
+    """W' = bf16(W + sign B'A) against the fp64 oracle: the kernel's fp32 sum
+    may move a value across a rounding boundary, so elements agree within one
+    bf16 step and nearly all bit for bit."""
+    W, A, Bp, Wb, Ab, Bb = _merge_case(out, h_in, r, r_slot, seed=out + r)
+    ref = O.bf16_to_f64(O.merge(Wb, Ab, Bb, sign))
+    Wd = W.cuda()
+    abi.lora_merge(Wd, A.cuda(), Bp.cuda(), sign)
+    torch.cuda.synchronize()
+    got = O.bf16_to_f64(to_host(Wd))
+    # fp32 sum of r products plus W: error <= (r + 1) 2^-24 (sum |B'||A| + |W|);
+    # then the one rounding may land one bf16 step (<= 2^-7 |value|) apart
+    E = (r + 1) * 2.0 ** -24 * (np.abs(O.bf16_to_f64(Bb)) @ np.abs(O.bf16_to_f64(Ab)) + np.abs(O.bf16_to_f64(Wb)))
+    assert np.all(np.abs(got - ref) <= 2.0 ** -7 * (np.abs(ref) + E) + E)
+    assert (got != ref).mean() < 1e-3
+
+
+def test_merge_unmerge_round_trip_exact():
+    """Small integers: every value and sum is exact, so the merged weight
+    equals the oracle's bit for bit and unmerge restores W bit for bit."""
+    rng = np.random.default_rng(5)
+    out, h_in, r = 200, 264, 8
+    Wb = O.f64_to_bf16(rng.integers(-40, 41, (out, h_in)).astype(np.float64))
+    Ab = O.f64_to_bf16(rng.integers(-3, 4, (r, h_in)).astype(np.float64))
+    Bb = O.f64_to_bf16(rng.integers(-3, 4, (out, r)).astype(np.float64))
+    Wd, Ad, Bd = to_dev(Wb), to_dev(Ab), to_dev(Bb)
+    abi.lora_merge(Wd, Ad, Bd, 1)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_host(Wd), O.merge(Wb, Ab, Bb, 1))
+    abi.lora_merge(Wd, Ad, Bd, -1)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_host(Wd), Wb)
+
+
+def test_merge_rejects_bad_arguments_before_enqueue():
+    W = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
+    A = torch.zeros(16, 64, dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros(64, 16, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(abi.LoraError) as e:
+        abi.lora_merge(W, A, B, 0)
+    assert e.value.name == "LORA_ERR_INVALID_ARG"
+    with pytest.raises(abi.LoraError) as e:
+        abi.lora_merge(W[:, 1:], A[:, 1:], B, 1)    # unaligned W and h_in not a multiple of 8
+    assert e.value.name in ("LORA_ERR_ALIGNMENT", "LORA_ERR_SHAPE")
+    big = torch.zeros(136, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(abi.LoraError) as e:
+        abi.lora_merge(W, big, B, 1)               # slot rank above the limit
+    assert e.value.name == "LORA_ERR_RANK_EXCEEDS_SLOT"
