@@ -253,6 +253,130 @@ def cpu_oracle_rate(wl_name: str, budget_s: float, layers: int):
     return rate, {"cores": cores, "sample": sample, "seconds": round(dt, 3)}
 
 
+# ------------------------------------------------- merge / unmerge ----
+# Merged weights for single-tenant serving: W <- bf16(W +/- B'A) for every
+# projection weight of MERGE_LAYERS Mistral-7B-shaped layers, one adapter of
+# rank MERGE_RANK.  A step merges then unmerges every weight once.
+
+MERGE_WORKLOAD = "merge_mistral7b"
+MERGE_LAYERS = 4
+MERGE_RANK = 64
+MERGE_SHAPES = [("q", 4096, 4096), ("k", 1024, 4096), ("v", 1024, 4096), ("o", 4096, 4096),
+                ("gate", 14336, 4096), ("up", 14336, 4096), ("down", 4096, 14336)]   # (name, out, h_in)
+
+
+def merge_bytes(out: int, h_in: int, r: int) -> int:
+    """Algorithmic bytes of one merge: W read and written, A and B' read once."""
+    return 2 * 2 * out * h_in + 2 * r * (out + h_in)
+
+
+def cpu_oracle_merge_rate(budget_s: float):
+    """The fp64 oracle's merge on one q-shaped weight, row blocks over all cores."""
+    import concurrent.futures as cf
+    import oracle as O
+    rng = np.random.default_rng(0)
+    out, h_in, r = 4096, 4096, MERGE_RANK
+    W = O.f64_to_bf16(rng.standard_normal((out, h_in)))
+    A = O.f64_to_bf16(rng.standard_normal((r, h_in)) * 0.02)
+    Bp = O.f64_to_bf16(rng.standard_normal((out, r)) * 0.02)
+    cores = os.cpu_count() or 1
+    O.merge(W[:1], A, Bp[:1], 1)   # builds the library
+    rows = 0
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        start = 0
+        while time.perf_counter() - t0 < budget_s and start < out:
+            blocks = [(start + i * 8, start + (i + 1) * 8) for i in range(cores)]
+            rows += sum(ex.map(lambda b: O.merge(W[b[0]:b[1]], A, Bp[b[0]:b[1]], 1).shape[0], blocks))
+            start += 8 * cores
+    dt = time.perf_counter() - t0
+    return rows * h_in / dt, {"cores": cores, "sample": f"{rows} rows of a {out}x{h_in} weight, rank {r}",
+                              "seconds": round(dt, 3)}
+
+
+def run_merge(args, rank, local, ws):
+    import torch
+    from lora_serving_gb300 import abi, build
+    build()
+    abi.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    g = torch.Generator(device=dev).manual_seed(7 + rank)
+    r = MERGE_RANK
+    layers = args.layers or MERGE_LAYERS
+    weights = []
+    for _ in range(layers):
+        for name, out, h_in in MERGE_SHAPES:
+            W = torch.randn(out, h_in, generator=g, device=dev).to(torch.bfloat16)
+            A = (torch.randn(r, h_in, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+            B = (torch.randn(out, r, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+            weights.append((W, A, B))
+    elems = sum(W.numel() for W, _, _ in weights)
+    bytes_step = 2 * sum(merge_bytes(W.shape[0], W.shape[1], r) for W, _, _ in weights)
+
+    def step():
+        for W, A, B in weights:
+            abi.lora_merge(W, A, B, 1)
+        for W, A, B in weights:
+            abi.lora_merge(W, A, B, -1)
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    l0 = abi.lora_kernel_launch_count()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    launches_per_step = abi.lora_kernel_launch_count() - l0
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    e0.record(cur)
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    ms_local = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    barrier(ws)
+    ms = max_over_ranks(ms_local, ws, device=dev if ws > 1 else "cpu")
+    units = sum_over_ranks(2.0 * elems * args.steps, ws, device=dev if ws > 1 else "cpu")
+    peak, peak_kind = peaks()
+    achieved = bytes_step / (ms_local / args.steps / 1e3) / 1e9
+    out = {
+        "metric": "LoRA merge/unmerge: weight elements updated per second",
+        "value": round(units / (ms / 1e3), 1), "unit": "weights/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": MERGE_WORKLOAD, "layers": layers, "rank": r,
+                   "weights": {n: [o, h] for n, o, h in MERGE_SHAPES}, "elements": elems,
+                   "l2": f"{bytes_step / 2 / 1e9:.2f} GB of weights per pass (L2 "
+                         f"{torch.cuda.get_device_properties(dev).L2_cache_size / 1e6:.0f} MB)",
+                   "timing": "CUDA graph of merge then unmerge of every weight; CUDA events",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": {"kernel": "merge_kernel", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
+                     "per": "step", "bytes_per_step": bytes_step, "traffic": None},
+        "clocks": clk,
+        "gpu_launches": int(launches_per_step * args.steps),
+        "e2e": None,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        rate, info = cpu_oracle_merge_rate(args.cpu_seconds)
+        out["cpu_baseline"] = {"value": round(rate, 1), "unit": "weights/s", "cores": info["cores"],
+                               "kind": "oracle", "sample": info["sample"]}
+    return out
+
+
 # --------------------------------------------------------- GPU arm ----
 
 class Instance:
@@ -467,6 +591,23 @@ def run_reference(args, rank, ws):
     name = args.workload
     layers = args.layers or LAYERS.get(name, 1)
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
+    if name == MERGE_WORKLOAD:
+        vals, info = [], None
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            rate, info = cpu_oracle_merge_rate(per_step)
+            vals.append(rate)
+        value = statistics.median(vals)
+        return {
+            "impl": "reference", "metric": "LoRA merge/unmerge: weight elements updated per second",
+            "value": round(value, 1), "unit": "weights/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "config": {"workload": name, "rank": MERGE_RANK},
+            "cpu_baseline": {"value": round(value, 1), "unit": "weights/s", "cores": info["cores"], "kind": "oracle",
+                             "sample": info["sample"]},
+            "e2e": {"value": round(value, 1), "unit": "weights/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "seconds": round(time.perf_counter() - t0, 2),
+        }
     vals = []
     info = None
     t0 = time.perf_counter()
@@ -502,7 +643,7 @@ def main(argv=None):
             print(json.dumps(out), flush=True)
         return 0
     rank, local, ws = dist_setup("nccl")
-    out = run_ours(args, rank, local, ws)
+    out = run_merge(args, rank, local, ws) if args.workload == MERGE_WORKLOAD else run_ours(args, rank, local, ws)
     if rank == 0:
         print(json.dumps(out), flush=True)
     return 0
