@@ -64,7 +64,7 @@ typedef enum {
     LORA_ERR_INVALID_ARG = 1,       /* NULL pointer, negative size, n_proj out of range */
     LORA_ERR_SHAPE = 2,             /* leading dimension too small, slice outside the row */
     LORA_ERR_RANK_EXCEEDS_SLOT = 3, /* adapter rank > r_slot, or r_slot > LORA_MAX_RANK */
-    LORA_ERR_SLOT_RANGE = 4,        /* host-visible adapter id outside [-1, n_slots) */
+    LORA_ERR_SLOT_RANGE = 4,        /* adapter id outside [-1, n_slots); more adapters than slots */
     LORA_ERR_ALIGNMENT = 5,         /* pointer or size violates the 16-byte rule above */
     LORA_ERR_METADATA = 6,          /* segment table inconsistent with the row counts */
     LORA_ERR_WORKSPACE = 7,         /* workspace NULL or smaller than required */
@@ -268,6 +268,84 @@ lora_status_t lora_apply_noalloc(lora_bf16_t* y, int ld_y, const lora_bf16_t* x,
  */
 lora_status_t lora_merge(lora_bf16_t* W, int ld_w, int out, int h_in, const lora_bf16_t* A,
                          const lora_bf16_t* B, int r_slot, int sign, lora_stream_t stream);
+
+/* ------------------------------------------------------------------ *
+ *  Adapter slots: GPU slots fed from a host cache of prepared adapters
+ * ------------------------------------------------------------------ */
+
+/*
+ * [VLLM step 2]: max_loras adapters live in GPU slots at once, up to
+ * max_cpu_loras prepared adapters wait in host memory, and the slot rank is
+ * the largest rank served; [VLLM, limits]: an adapter of higher rank cannot
+ * load.  [TGI 3]: an adapter is prepared once -- scale folded into B, ranks
+ * zero-padded to the slot rank -- before it is used.
+ *
+ * The manager owns a host cache of up to max_cpu prepared adapters in pinned
+ * memory (least recently used evicted first) and assigns adapters to the
+ * n_slots slots of the caller's device stores (least recently used slot
+ * reused first, never one the current batch needs).  Loading an adapter
+ * into a slot is one cudaMemcpyAsync per projection for A and for B on the
+ * caller's stream: kernels enqueued on that stream after lora_slots_acquire
+ * see it, kernels enqueued before it have finished with the slot's old
+ * contents.  Use one stream for lora_slots_acquire and the kernels that read
+ * the stores.  Not thread-safe: one manager per serving thread.
+ *
+ * Without device stores the manager only tracks the assignment (no device
+ * memory, no copies): the policy on its own.
+ */
+typedef struct lora_slot_manager lora_slot_manager_t;
+
+typedef struct {
+    uint64_t registered;        /* adapters prepared into the host cache */
+    uint64_t host_evictions;    /* cached adapters dropped to make room */
+    uint64_t hits;              /* batch adapters already resident in a slot */
+    uint64_t loads;             /* adapters copied into a slot */
+    uint64_t slot_evictions;    /* resident adapters replaced by a load */
+} lora_slot_stats_t;
+
+/*
+ * Creates a manager for n_proj projections (1..16) of input widths h_in[p]
+ * (multiples of 8) and output widths width[p], with device stores
+ * A_stores[p] [n_slots][r_slot][h_in[p]] and B_stores[p]
+ * [n_slots][width[p]][r_slot] (both arrays NULL: policy only), and a host
+ * cache of max_cpu adapters (max_cpu >= n_slots).  Errors:
+ * LORA_ERR_INVALID_ARG, LORA_ERR_RANK_EXCEEDS_SLOT (r_slot > LORA_MAX_RANK),
+ * LORA_ERR_ALIGNMENT (r_slot or an h_in not a multiple of 8, a store not
+ * 16-byte aligned).
+ */
+lora_status_t lora_slots_create(int n_proj, const int* h_in, const int* width, lora_bf16_t* const* A_stores,
+                                lora_bf16_t* const* B_stores, int n_slots, int r_slot, int max_cpu,
+                                lora_slot_manager_t** out);
+void lora_slots_destroy(lora_slot_manager_t* m);
+
+/*
+ * Prepares adapter `adapter_id` (>= 0) into the host cache: A[p] host bf16
+ * [r][h_in[p]], B[p] host bf16 [width[p]][r] (peft orientation, unscaled),
+ * scale alpha/r (alpha/sqrt(r) with use_rslora) folded into B with one
+ * rounding, ranks padded to r_slot.  Re-registering an id replaces it (a
+ * resident copy is reloaded at its next acquire).  A full cache first drops
+ * its least recently used adapter that is not resident in a slot.
+ * Errors, all before anything changes: LORA_ERR_INVALID_ARG,
+ * LORA_ERR_RANK_EXCEEDS_SLOT (r > r_slot), LORA_ERR_SLOT_RANGE (cache full
+ * of resident adapters), LORA_ERR_CUDA (pinned allocation).
+ */
+lora_status_t lora_slots_register(lora_slot_manager_t* m, int64_t adapter_id, const lora_bf16_t* const* A,
+                                  const lora_bf16_t* const* B, int r, double alpha, int use_rslora);
+
+/*
+ * Maps a batch's adapter ids (n entries, -1 = base model) to slot ids in
+ * slots_out (-1 stays -1), loading the adapters that are not resident.
+ * Errors, before anything is enqueued or changed: LORA_ERR_INVALID_ARG (an
+ * id neither -1 nor registered), LORA_ERR_SLOT_RANGE (more distinct adapters
+ * than slots).  LORA_ERR_CUDA: a copy could not be enqueued; the slot it was
+ * meant for is left empty, adapters loaded before it stay loaded.
+ */
+lora_status_t lora_slots_acquire(lora_slot_manager_t* m, const int64_t* adapter_ids, int n, int32_t* slots_out,
+                                 lora_stream_t stream);
+
+/* Slot currently holding adapter_id, or -1. */
+int lora_slots_slot_of(const lora_slot_manager_t* m, int64_t adapter_id);
+lora_status_t lora_slots_stats(const lora_slot_manager_t* m, lora_slot_stats_t* out);
 
 /* ------------------------------------------------------------------ *
  *  Host helpers (host pointers, synchronous)

@@ -38,6 +38,8 @@ EXPORTS = (
     "lora_apply", "lora_apply_workspace_bytes", "lora_build_metadata",
     "lora_prepare_adapter", "lora_slot_rank", "lora_read_device_status", "lora_status_string",
     "lora_kernel_launch_count", "lora_apply_noalloc", "lora_merge",
+    "lora_slots_create", "lora_slots_destroy", "lora_slots_register", "lora_slots_acquire",
+    "lora_slots_slot_of", "lora_slots_stats",
 )
 LORA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -89,6 +91,11 @@ def load(path: str | None = None):
         "lora_read_device_status": [P, P, P],
         "lora_status_string": [i32],
         "lora_merge": [P, i32, i32, i32, P, P, i32, i32, P],
+        "lora_slots_create": [i32, P, P, P, P, i32, i32, i32, P],
+        "lora_slots_register": [P, ctypes.c_int64, P, P, i32, ctypes.c_double, i32],
+        "lora_slots_acquire": [P, P, i32, P, P],
+        "lora_slots_slot_of": [P, ctypes.c_int64],
+        "lora_slots_stats": [P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -98,6 +105,8 @@ def load(path: str | None = None):
     lib.lora_status_string.restype = ctypes.c_char_p
     lib.lora_kernel_launch_count.argtypes = []
     lib.lora_kernel_launch_count.restype = ctypes.c_uint64
+    lib.lora_slots_destroy.argtypes = [P]
+    lib.lora_slots_destroy.restype = None
     _lib = lib
     return lib
 
@@ -200,6 +209,70 @@ def lora_merge(W, A, B, sign, *, stream=None):
     r_slot = int(A.shape[0])
     _check("lora_merge", load().lora_merge(_p(W), _ld(W), out, h_in, _p(A), _p(B), r_slot, int(sign),
                                            _stream(stream)))
+
+
+class lora_slot_stats_t(ctypes.Structure):
+    _fields_ = [("registered", ctypes.c_uint64), ("host_evictions", ctypes.c_uint64), ("hits", ctypes.c_uint64),
+                ("loads", ctypes.c_uint64), ("slot_evictions", ctypes.c_uint64)]
+
+
+class SlotManager:
+    """The adapter slot manager (lora_slots_*): a host cache of prepared
+    adapters feeding the GPU slots of the stores.  A_stores / B_stores: one
+    device tensor per projection ([n_slots][r_slot][h_in], [n_slots][w][r_slot]),
+    or None for the policy alone."""
+
+    def __init__(self, h_in, width, n_slots, r_slot, max_cpu, A_stores=None, B_stores=None):
+        self.n_proj = len(h_in)
+        hi = (ctypes.c_int * self.n_proj)(*h_in)
+        wd = (ctypes.c_int * self.n_proj)(*width)
+        if A_stores is not None:
+            self._a = (ctypes.c_void_p * self.n_proj)(*[_p(t) for t in A_stores])
+            self._b = (ctypes.c_void_p * self.n_proj)(*[_p(t) for t in B_stores])
+            a, b = ctypes.addressof(self._a), ctypes.addressof(self._b)
+        else:
+            a = b = 0
+        self._h = ctypes.c_void_p()
+        _check("lora_slots_create", load().lora_slots_create(self.n_proj, ctypes.addressof(hi), ctypes.addressof(wd),
+                                                             a, b, n_slots, r_slot, max_cpu, ctypes.byref(self._h)))
+
+    def close(self):
+        if self._h:
+            load().lora_slots_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def register(self, adapter_id, A_list, B_list, r, alpha, use_rslora=False):
+        """A_list[p]: host uint16 bits [r][h_in_p]; B_list[p]: [w_p][r] (unscaled)."""
+        A = [np.ascontiguousarray(a, dtype=np.uint16) for a in A_list]
+        B = [np.ascontiguousarray(b, dtype=np.uint16) for b in B_list]
+        ap = (ctypes.c_void_p * self.n_proj)(*[a.ctypes.data for a in A])
+        bp = (ctypes.c_void_p * self.n_proj)(*[b.ctypes.data for b in B])
+        _check("lora_slots_register", load().lora_slots_register(self._h, int(adapter_id), ctypes.addressof(ap),
+                                                                 ctypes.addressof(bp), int(r), float(alpha),
+                                                                 int(bool(use_rslora))))
+
+    def acquire(self, adapter_ids, stream=0) -> np.ndarray:
+        """Adapter ids of a batch (-1 = base) -> slot ids, loading what is missing."""
+        ids = np.ascontiguousarray(adapter_ids, dtype=np.int64)
+        out = np.empty(ids.size, np.int32)
+        st = stream if isinstance(stream, int) else _stream(stream)
+        _check("lora_slots_acquire", load().lora_slots_acquire(self._h, ids.ctypes.data, int(ids.size),
+                                                               out.ctypes.data, st))
+        return out
+
+    def slot_of(self, adapter_id) -> int:
+        return int(load().lora_slots_slot_of(self._h, int(adapter_id)))
+
+    def stats(self) -> dict:
+        s = lora_slot_stats_t()
+        _check("lora_slots_stats", load().lora_slots_stats(self._h, ctypes.byref(s)))
+        return {f: int(getattr(s, f)) for f, _ in s._fields_}
 
 
 def lora_apply_workspace_bytes(n_rows, n_proj, r_slot) -> int:

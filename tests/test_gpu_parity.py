@@ -605,3 +605,46 @@ def test_merge_rejects_bad_arguments_before_enqueue():
     with pytest.raises(abi.LoraError) as e:
         abi.lora_merge(W, big, B, 1)               # slot rank above the limit
     assert e.value.name == "LORA_ERR_RANK_EXCEEDS_SLOT"
+
+
+# ------------------------------------------------------ adapter slots ----
+
+def test_slot_manager_feeds_the_stores_end_to_end():
+    """Six adapters through three GPU slots over several batches: the manager
+    maps each batch's adapter ids to slots, loading what is missing by async
+    copies on the stream, and lora_apply then matches the oracle computed
+    from the adapters by id (true ranks, unpadded, scale folded by the oracle)."""
+    h_in, projs, r_slot, n_slots = 128, [("q", 128), ("k", 32), ("v", 32)], 16, 3
+    ranks = [4, 8, 16, 12, 16, 8]
+    g = torch.Generator().manual_seed(12)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+    A = {(k, p): bits((torch.randn(r, h_in, generator=g) * 0.1).to(torch.bfloat16))
+         for k, r in enumerate(ranks) for p in range(len(projs))}
+    B = {(k, p): bits((torch.randn(w, r, generator=g) * 0.1).to(torch.bfloat16))
+         for k, r in enumerate(ranks) for p, (_, w) in enumerate(projs)}
+    st = store.GroupStore(h_in, projs, n_slots, r_slot)
+    m = abi.SlotManager([h_in] * len(projs), [w for _, w in projs], n_slots, r_slot, max_cpu=6,
+                        A_stores=st.A, B_stores=st.B)
+    for k, r in enumerate(ranks):
+        m.register(k, [A[k, p] for p in range(len(projs))], [B[k, p] for p in range(len(projs))], r, 2.0 * r,
+                   use_rslora=(k % 2 == 1))
+    ads = [O.Adapters([A[k, p] for k in range(len(ranks))], [B[k, p] for k in range(len(ranks))],
+                      [O.scale(2.0 * r, r, k % 2 == 1) for k, r in enumerate(ranks)]) for p in range(len(projs))]
+    batches = [[0, 1, 2, 0, -1, 1], [3, 0, 3, 3], [4, 5, 3, -1, 5], [1, 2, 1], [5, 4, 0, 0]]
+    stream = torch.cuda.current_stream()
+    for n, ids in enumerate(batches):
+        ids = np.array(ids, np.int32)
+        slots = m.acquire(ids, stream=stream)
+        x = bits((torch.randn(len(ids), h_in, generator=g)).to(torch.bfloat16))
+        y = bits((torch.randn(len(ids), st.ld_y, generator=g)).to(torch.bfloat16))
+        yd = to_dev(y)
+        meta = store.BatchMeta(slots, 0, n_slots)
+        store.apply(yd, to_dev(x), st, meta, store.workspace_for(len(ids), len(projs), r_slot), stream=stream)
+        torch.cuda.synchronize()
+        ref = y.copy()
+        for p, off in enumerate(st.offsets):
+            ref = O.apply_projection(ids, x, ref, off, ads[p])
+        check_bf16(to_host(yd), ref, ids, y, f"slot batch {n}")
+    s = m.stats()
+    assert s["loads"] == 10 and s["slot_evictions"] == 7 and s["hits"] == 3, s
+    m.close()
