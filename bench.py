@@ -377,6 +377,90 @@ def run_merge(args, rank, local, ws):
     return out
 
 
+# ---------------------------------------------------------- slots ----
+# Adapter slot manager: loading adapters into GPU slots.  Llama-3.2-3B q/k/v/o
+# adapters of rank 16 (640 KiB prepared), SLOTS_N slots, a pool of SLOTS_POOL
+# registered adapters; a step acquires a batch of SLOTS_N adapters none of
+# which is resident (every one a load), then a batch of resident ones (all hits).
+
+SLOTS_WORKLOAD = "slots_llama3b"
+SLOTS_N, SLOTS_POOL, SLOTS_RANK = 8, 64, 16
+SLOTS_PROJS = [(3072, 3072), (3072, 1024), (3072, 1024), (3072, 3072)]   # (h_in, width): q, k, v, o
+
+
+def run_slots(args, rank, local, ws):
+    import torch
+    from lora_serving_gb300 import abi, build
+    build()
+    abi.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    r_slot = SLOTS_RANK
+    A_st = [torch.zeros(SLOTS_N, r_slot, h, dtype=torch.bfloat16, device=dev) for h, _ in SLOTS_PROJS]
+    B_st = [torch.zeros(SLOTS_N, w, r_slot, dtype=torch.bfloat16, device=dev) for _, w in SLOTS_PROJS]
+    m = abi.SlotManager([h for h, _ in SLOTS_PROJS], [w for _, w in SLOTS_PROJS], SLOTS_N, r_slot, SLOTS_POOL,
+                        A_stores=A_st, B_stores=B_st)
+    rng = np.random.default_rng(3 + rank)
+    for k in range(SLOTS_POOL):
+        A = [(rng.standard_normal((SLOTS_RANK, h)) * 0.02).astype(np.float32).view(np.uint32) >> 16
+             for h, _ in SLOTS_PROJS]
+        B = [(rng.standard_normal((w, SLOTS_RANK)) * 0.02).astype(np.float32).view(np.uint32) >> 16
+             for _, w in SLOTS_PROJS]
+        m.register(k, [a.astype(np.uint16) for a in A], [b.astype(np.uint16) for b in B], SLOTS_RANK, 32.0)
+    stream = torch.cuda.current_stream(dev)
+    adapter_bytes = sum(2 * r_slot * (h + w) for h, w in SLOTS_PROJS)
+    batch = 0
+
+    def step():
+        nonlocal batch
+        ids = np.arange(batch * SLOTS_N, (batch + 1) * SLOTS_N) % SLOTS_POOL   # none resident
+        batch += 1
+        m.acquire(ids, stream=stream)
+        return ids
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    last = None
+    for _ in range(args.steps):
+        last = step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    ms_local = e0.elapsed_time(e1)
+    # host cost of a batch whose adapters are all resident (no copies)
+    t1 = time.perf_counter()
+    for _ in range(1000):
+        m.acquire(last, stream=stream)
+    hit_us = (time.perf_counter() - t1) / 1000 * 1e6
+    barrier(ws)
+    ms = max_over_ranks(ms_local, ws, device=dev if ws > 1 else "cpu")
+    loads = sum_over_ranks(float(SLOTS_N * args.steps), ws, device=dev if ws > 1 else "cpu")
+    st = m.stats()
+    m.close()
+    return {
+        "metric": "adapter loads into GPU slots per second", "value": round(loads / (ms / 1e3), 1),
+        "unit": "loads/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": SLOTS_WORKLOAD, "slots": SLOTS_N, "pool": SLOTS_POOL, "rank": SLOTS_RANK,
+                   "adapter_bytes": adapter_bytes, "projections": SLOTS_PROJS,
+                   "timing": "CUDA events around the acquires of a step's all-miss batches (H2D copies)",
+                   "parallelism": f"replicas x{ws}"},
+        "h2d": {"achieved_gbs": round(SLOTS_N * adapter_bytes * args.steps / (ms_local / 1e3) / 1e9, 1),
+                "copies_per_load": 2 * len(SLOTS_PROJS), "host_wall_ms_per_step": round(wall / args.steps * 1e3, 4)},
+        "acquire_all_hits_us": round(hit_us, 2),
+        "stats": st,
+        "gpu_launches": 0,
+        "e2e": None,
+    }
+
+
 # --------------------------------------------------------- GPU arm ----
 
 class Instance:
@@ -643,7 +727,12 @@ def main(argv=None):
             print(json.dumps(out), flush=True)
         return 0
     rank, local, ws = dist_setup("nccl")
-    out = run_merge(args, rank, local, ws) if args.workload == MERGE_WORKLOAD else run_ours(args, rank, local, ws)
+    if args.workload == MERGE_WORKLOAD:
+        out = run_merge(args, rank, local, ws)
+    elif args.workload == SLOTS_WORKLOAD:
+        out = run_slots(args, rank, local, ws)
+    else:
+        out = run_ours(args, rank, local, ws)
     if rank == 0:
         print(json.dumps(out), flush=True)
     return 0
