@@ -648,3 +648,46 @@ def test_slot_manager_feeds_the_stores_end_to_end():
     s = m.stats()
     assert s["loads"] == 10 and s["slot_evictions"] == 7 and s["hits"] == 3, s
     m.close()
+
+
+# ------------------------------------------------- tensor-parallel steps ----
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_tensor_parallel_kernel_steps_two_layouts(world):
+    """The sharded stores through the library's BGMV kernels (tp.kernel_steps),
+    with the ranks run one after another on this device and the exchange on
+    v done by a device concatenation (all_gather) or sum (all_reduce): both
+    layouts must match the oracle's unsharded delta."""
+    from lora_serving_gb300 import tp
+    h_in, w, r_slot, n_slots, T = 256, 128, 32, 4, 37     # a rank's slice of v: 32 / world >= 8 columns
+    ranks = [4, 32, 20, 8]
+    g = torch.Generator().manual_seed(21)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+    A = [bits((torch.randn(r, h_in, generator=g) * 0.1).to(torch.bfloat16)) for r in ranks]
+    B = [bits((torch.randn(w, r, generator=g) * 0.1).to(torch.bfloat16)) for r in ranks]
+    alphas = [2.0 * r for r in ranks]
+    st = store.GroupStore(h_in, [("q", w)], n_slots, r_slot).load_slots(
+        {k: [(A[k], B[k], alphas[k], False)] for k in range(n_slots)})
+    ids = torch.randint(-1, n_slots, (T,), generator=g, dtype=torch.int32)
+    x = bits(torch.randn(T, h_in, generator=g).to(torch.bfloat16))
+    y = bits(torch.randn(T, w, generator=g).to(torch.bfloat16))
+    ids_np = ids.numpy()
+    ref = O.apply_projection(ids_np, x, y, 0, O.Adapters(A, B, [O.scale(a, r, False) for a, r in zip(alphas, ranks)]))
+    s = _status()
+    shrink, expand = tp.kernel_steps(ids.cuda(), n_slots, dev_status=s)
+    xd, yd = to_dev(x), to_dev(y)
+
+    # column-parallel: each rank's slice of v, gathered in rank order
+    shards = [tp.shard_column(st.A[0], st.B[0], world, i) for i in range(world)]
+    v = torch.cat([shrink(xd, a) for a, _ in shards], dim=1)
+    cols = [tp._split(w, world, i) for i in range(world)]
+    y_col = torch.cat([expand(yd[:, c].contiguous(), v, b) for c, (_, b) in zip(cols, shards)], dim=1)
+    # row-parallel: partial v from each input slice, summed
+    ks = [tp._split(h_in, world, i) for i in range(world)]
+    rshards = [tp.shard_row(st.A[0], st.B[0], world, i) for i in range(world)]
+    v_sum = sum(shrink(xd[:, k].contiguous(), a) for k, (a, _) in zip(ks, rshards))
+    y_row = expand(yd.clone(), v_sum, rshards[0][1])
+    torch.cuda.synchronize()
+    assert abi.lora_read_device_status(s) == 0
+    check_bf16(to_host(y_col), ref, ids_np, y, f"column-parallel over {world}")
+    check_bf16(to_host(y_row), ref, ids_np, y, f"row-parallel over {world}")
