@@ -299,6 +299,37 @@ void oracle_expand(int n_rows, const int32_t* ids, const double* v, int64_t ld_v
 }
 
 /*
+ * One projection of the LoRA linear layer ([MLS], direct answer: the base
+ * product runs once for the whole batch and each row adds its own adapter's
+ * delta; [TGI], implementation: the LoRA layer adds the adapter output to
+ * the base layer's output):
+ *     y[t][off+c] = bf16_rne( sum_k x[t][k] W[c][k] + d[t][c] )
+ * with d the delta of oracle_delta (zero for base rows), the sum in double
+ * and ONE rounding.  W holds this projection's base weight as [w][ld_w];
+ * y_in is not read.
+ */
+void oracle_linear_projection(int n_rows, const int32_t* ids, const uint16_t* x, int64_t ld_x, int h_in,
+                              const uint16_t* W, int64_t ld_w, uint16_t* y, int64_t ld_y, int off, int w,
+                              const int* rp, const double* scale,
+                              const uint16_t* A_cat, const int64_t* A_off,
+                              const uint16_t* B_cat, const int64_t* B_off)
+{
+    double* d = (double*)malloc(sizeof(double) * (size_t)(n_rows > 0 ? n_rows : 1) * (size_t)(w > 0 ? w : 1));
+    oracle_delta(n_rows, ids, x, ld_x, h_in, w, rp, scale, A_cat, A_off, B_cat, B_off, d, w);
+    for (int t = 0; t < n_rows; ++t) {
+        const uint16_t* xt = x + (int64_t)t * ld_x;
+        for (int c = 0; c < w; ++c) {
+            const uint16_t* Wc = W + (int64_t)c * ld_w;
+            double base = 0.0;
+            for (int k = 0; k < h_in; ++k)
+                base += oracle_bf16_to_double(xt[k]) * oracle_bf16_to_double(Wc[k]);
+            y[(int64_t)t * ld_y + off + c] = oracle_double_to_bf16(base + d[(int64_t)t * w + c]);
+        }
+    }
+    free(d);
+}
+
+/*
  * Merged weight for single-tenant serving ([MLS], interviewer follow-ups:
  * W' = W + B A gives the same model as the base plus the adapter's delta):
  *     W'[o][k] = bf16_rne(W[o][k] + sign * sum_{j < r} B'[o][j] A[j][k])

@@ -26,7 +26,7 @@ _lib = None
 
 __all__ = [
     "build", "bf16_to_f64", "f64_to_bf16", "scale", "fold_B", "build_metadata",
-    "Adapters", "shrink", "delta", "apply_projection", "expand", "merge",
+    "Adapters", "shrink", "delta", "apply_projection", "expand", "merge", "linear_projection",
 ]
 
 
@@ -66,6 +66,8 @@ def _load():
                                                     P, P, P, P, P, P]
             lib.oracle_expand.argtypes = [i32, P, P, i64, P, i64, i32, i32, P, P, P, P]
             lib.oracle_merge.argtypes = [P, i64, i32, i32, P, i64, P, i64, i32, i32, P]
+            lib.oracle_linear_projection.argtypes = [i32, P, P, i64, i32, P, i64, P, i64, i32, i32,
+                                                     P, P, P, P, P, P]
             _lib = lib
     return _lib
 
@@ -205,6 +207,21 @@ def expand(ids, v, y_bits, off: int, ad: Adapters) -> np.ndarray:
     T = ids.size
     _load().oracle_expand(T, _ptr(ids), _ptr(v), v.shape[1], _ptr(y), y.shape[1], int(off),
                           ad.w, _ptr(ad.rp), _ptr(ad.scale), _ptr(ad.B_cat), _ptr(ad.B_off))
+    return y
+
+
+def linear_projection(ids, x_bits, W_bits, y_bits, off: int, ad: Adapters) -> np.ndarray:
+    """Returns a copy of y with bf16_rne(x W^T + delta) written into
+    [off, off+w); W is this projection's base weight [w][h_in] (bf16 bits)."""
+    ids = _c(ids, np.int32)
+    x_bits = _c(x_bits, np.uint16)
+    W = _c(W_bits, np.uint16)
+    assert W.shape == (ad.w, ad.h_in)
+    y = np.array(y_bits, dtype=np.uint16, copy=True, order="C")
+    _load().oracle_linear_projection(ids.size, _ptr(ids), _ptr(x_bits), x_bits.shape[1], ad.h_in, _ptr(W),
+                                     W.shape[1], _ptr(y), y.shape[1], int(off), ad.w, _ptr(ad.rp),
+                                     _ptr(ad.scale), _ptr(ad.A_cat), _ptr(ad.A_off), _ptr(ad.B_cat),
+                                     _ptr(ad.B_off))
     return y
 
 

@@ -409,3 +409,64 @@ def test_merged_weight_applied_equals_base_plus_delta():
                 rhs = O.bf16_to_f64(W) @ xd[t] + d[t]
                 bound = 2.0 ** -8 * (np.abs(merged) @ np.abs(xd[t])) + 1e-12
                 assert np.all(np.abs(lhs - rhs) <= bound), (seed, k, t)
+
+
+# ------------------------------------------------------ linear layer ----
+
+def test_linear_small_integers_equal_exact_integer_product():
+    """With small integers and scale 1 every product and sum is exact, so the
+    layer's output must equal x (W + B A)^T computed in integers for adapter
+    rows and x W^T for base rows (a dropped delta, a wrong slot, a transposed
+    operand or a sign slip would not)."""
+    rng = np.random.default_rng(17)
+    T, h_in, w, ranks = 11, 12, 9, (2, 3, 1)
+    x = rng.integers(-1, 2, (T, h_in))
+    W = rng.integers(-3, 4, (w, h_in))
+    A = [rng.integers(-2, 3, (r, h_in)) for r in ranks]
+    B = [rng.integers(-2, 3, (w, r)) for r in ranks]
+    ids = np.array([0, -1, 1, 2, 2, 0, -1, 1, 0, 2, 1], np.int32)
+    to_bits = lambda a: O.f64_to_bf16(a.astype(np.float64))
+    ad = O.Adapters([to_bits(a) for a in A], [to_bits(b) for b in B],
+                    [O.scale(float(r), r, False) for r in ranks])            # alpha = r: s = 1
+    y_in = np.full((T, w + 5), 0x7FC0, np.uint16)                             # NaN: must not be read
+    got = O.linear_projection(ids, to_bits(x), to_bits(W), y_in, 3, ad)
+    expect = np.empty((T, w), np.int64)
+    for t in range(T):
+        Wt = W + (B[ids[t]] @ A[ids[t]] if ids[t] >= 0 else 0)
+        expect[t] = Wt @ x[t]
+    assert np.abs(expect).max() < 256                                         # exact in bf16
+    np.testing.assert_array_equal(O.bf16_to_f64(got[:, 3:3 + w]), expect.astype(np.float64))
+    np.testing.assert_array_equal(got[:, :3], y_in[:, :3])                    # outside the slice untouched
+    np.testing.assert_array_equal(got[:, 3 + w:], y_in[:, 3 + w:])
+
+
+def test_linear_rounds_once():
+    """base = 1 + 2^-8 sits exactly halfway between two bf16 values; a delta
+    of 2^-10 tips the single rounding up to 1 + 2^-7, where rounding the base
+    first (ties to even: 1) and then adding the delta would give 1.  A base
+    row keeps the tie and rounds to even."""
+    one, eps8, eps10 = 1.0, 2.0 ** -8, 2.0 ** -10
+    x = O.f64_to_bf16(np.array([[one, one], [one, one]]))
+    W = O.f64_to_bf16(np.array([[one, eps8]]))
+    A = [O.f64_to_bf16(np.array([[1.0, 0.0]]))]
+    B = [O.f64_to_bf16(np.array([[eps10]]))]
+    ad = O.Adapters(A, B, [O.scale(1.0, 1, False)])
+    got = O.bf16_to_f64(O.linear_projection(np.array([0, -1], np.int32), x, W, np.zeros((2, 1), np.uint16), 0, ad))
+    assert got[0, 0] == 1.0 + 2.0 ** -7
+    assert got[1, 0] == 1.0
+
+
+def test_linear_base_rows_equal_rounded_plain_product():
+    """Rows with id -1 are bf16_rne of the plain product, checked against an
+    independent fp64 matrix product."""
+    g = torch.Generator().manual_seed(8)
+    T, h_in, w = 6, 40, 24
+    x, W = _rand_bf16(g, (T, h_in)), _rand_bf16(g, (w, h_in), 0.2)
+    A, B = [_rand_bf16(g, (4, h_in))], [_rand_bf16(g, (w, 4))]
+    ids = np.array([-1, 0, -1, -1, 0, -1], np.int32)
+    ad = O.Adapters(A, B, [O.scale(8.0, 4, False)])
+    got = O.linear_projection(ids, x, W, np.zeros((T, w), np.uint16), 0, ad)
+    plain = O.f64_to_bf16(O.bf16_to_f64(x) @ O.bf16_to_f64(W).T)
+    base = ids < 0
+    np.testing.assert_array_equal(got[base], plain[base])
+    assert (got[~base] != plain[~base]).any()                                 # adapter rows differ
