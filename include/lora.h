@@ -248,6 +248,36 @@ lora_status_t lora_apply_noalloc(lora_bf16_t* y, int ld_y, const lora_bf16_t* x,
                                  lora_stream_t stream);
 
 /*
+ * The LoRA linear layer [MLS, direct answer: the base product runs once for
+ * the whole batch and every row adds its own adapter's delta; TGI,
+ * implementation: the LoRA layer adds the adapter output to the base
+ * layer's output].  For every row t and every column c of projection p:
+ *   y[t][off_p + c] = bf16_rne( sum_k x[t][k] W[off_p + c][k]
+ *                               + sum_j B'_{p,id_t}[c][j] (A_{p,id_t} x_t)[j] )
+ * one rounding of the fp32 sum (base rows, id -1: the base product alone).
+ * y is written, not read.
+ *   W      [dev] [n_out][ld_w] bf16: the projections' base weights stacked,
+ *          rows [off_p, off_p + width_p) for projection p, where the
+ *          projections tile [0, n_out) in order (off_0 = 0, off_{p+1} =
+ *          off_p + width_p); 16-byte aligned, ld_w >= h_in, ld_w % 8 == 0
+ *   other arguments as lora_apply (the same stores, metadata and
+ *   workspace: lora_apply_workspace_bytes(n_rows, n_proj, r_slot)).
+ * Limits: r_slot <= 64 when the batch has decode rows; up to
+ * LORA_MAX_RANK for prefill-only batches whose r_slot is a multiple of 16
+ * with n_proj * r_slot <= 256.  Per-row ids are read from meta->lora_ids,
+ * which must name the same adapters as the segment and group tables.
+ * Errors (before anything is enqueued): as lora_apply, plus LORA_ERR_SHAPE
+ * when the projections do not tile [0, n_out) or ld_w < h_in, and
+ * LORA_ERR_RANK_EXCEEDS_SLOT beyond the limits above.  Device status: rows
+ * naming an id outside [-1, n_slots) keep the base product and set
+ * LORA_DEV_SLOT_OUT_OF_RANGE; LORA_DEV_TIMEOUT as lora_apply.
+ */
+lora_status_t lora_linear(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_x, int h_in,
+                          const lora_bf16_t* W, int ld_w, const lora_proj_t* projs, int n_proj, int r_slot,
+                          int n_slots, const lora_meta_t* meta, void* workspace, size_t workspace_bytes,
+                          int32_t* dev_status, lora_stream_t stream);
+
+/*
  * Merged weight for single-tenant serving [MLS, interviewer follow-ups:
  * merging W' = W + B A gives the same model]:
  *   W[o][k] <- bf16_rne(W[o][k] + sign * sum_j B[o][j] A[j][k])

@@ -37,7 +37,7 @@ EXPORTS = (
     "lora_bgmv_shrink", "lora_bgmv_expand", "lora_sgmv_shrink", "lora_sgmv_expand",
     "lora_apply", "lora_apply_workspace_bytes", "lora_build_metadata",
     "lora_prepare_adapter", "lora_slot_rank", "lora_read_device_status", "lora_status_string",
-    "lora_kernel_launch_count", "lora_apply_noalloc", "lora_merge",
+    "lora_kernel_launch_count", "lora_apply_noalloc", "lora_merge", "lora_linear",
     "lora_slots_create", "lora_slots_destroy", "lora_slots_register", "lora_slots_acquire",
     "lora_slots_slot_of", "lora_slots_stats",
 )
@@ -91,6 +91,7 @@ def load(path: str | None = None):
         "lora_read_device_status": [P, P, P],
         "lora_status_string": [i32],
         "lora_merge": [P, i32, i32, i32, P, P, i32, i32, P],
+        "lora_linear": [P, i32, P, i32, i32, P, i32, P, i32, i32, i32, P, P, sz, P, P],
         "lora_slots_create": [i32, P, P, P, P, i32, i32, i32, P],
         "lora_slots_register": [P, ctypes.c_int64, P, P, i32, ctypes.c_double, i32],
         "lora_slots_acquire": [P, P, i32, P, P],
@@ -199,6 +200,16 @@ def lora_apply_noalloc(y, x, h_in, projs, r_slot, n_slots, meta, *, flags=0, dev
     _check("lora_apply_noalloc", load().lora_apply_noalloc(
         _p(y), _ld(y), _p(x), _ld(x), h_in, ctypes.addressof(projs), len(projs), r_slot, n_slots,
         ctypes.addressof(meta), int(flags), _p(dev_status), _stream(stream)))
+
+
+def lora_linear(y, x, h_in, W, projs, r_slot, n_slots, meta, workspace, *, dev_status=None, stream=None):
+    """y[:, off_p + c] = bf16(x W^T + B'_p (A_p x)) for every projection of
+    projs (ctypes array from make_projs(), tiling W's rows in order); W is
+    the stacked base weight [n_out][h_in] (row stride ld); y is written."""
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("lora_linear", load().lora_linear(
+        _p(y), _ld(y), _p(x), _ld(x), h_in, _p(W), _ld(W), ctypes.addressof(projs), len(projs), r_slot,
+        n_slots, ctypes.addressof(meta), _p(workspace), ws_bytes, _p(dev_status), _stream(stream)))
 
 
 def lora_merge(W, A, B, sign, *, stream=None):

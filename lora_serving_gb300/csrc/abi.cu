@@ -309,6 +309,73 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
     return LORA_OK;
 }
 
+lora_status_t lora_linear(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_x, int h_in,
+                          const lora_bf16_t* W, int ld_w, const lora_proj_t* projs, int n_proj, int r_slot,
+                          int n_slots, const lora_meta_t* meta, void* workspace, size_t ws_bytes,
+                          int32_t* dev_status, lora_stream_t stream)
+{
+    if (!projs || !meta || !W || n_proj <= 0 || n_proj > LORA_MAX_PROJ) return LORA_ERR_INVALID_ARG;
+    const int T = meta->n_rows, P = meta->n_prefill, D = T - P;
+    LORA_TRY(check_common(T, r_slot, n_slots));
+    if (P < 0 || P > T) return LORA_ERR_METADATA;
+    if (T == 0) return LORA_OK;
+    LORA_TRY(check_x(x, ld_x, h_in));
+    if (ld_w < h_in) return LORA_ERR_SHAPE;
+    if (!aligned16(W) || ld_w % 8 != 0) return LORA_ERR_ALIGNMENT;
+    ProjSet ps{};
+    ps.n_proj = n_proj;
+    ps.r_slot = r_slot;
+    int n_out = 0;
+    for (int p = 0; p < n_proj; ++p) {
+        LORA_TRY(check_y(y, ld_y, projs[p].out_off, projs[p].width));
+        LORA_TRY(check_store(projs[p].A));
+        LORA_TRY(check_store(projs[p].B));
+        if (projs[p].out_off != n_out) return LORA_ERR_SHAPE;   // the projections tile [0, n_out)
+        n_out += projs[p].width;
+        ps.A[p] = projs[p].A;
+        ps.B[p] = projs[p].B;
+        ps.out_off[p] = projs[p].out_off;
+        ps.width[p] = projs[p].width;
+    }
+    const bool tc_shrink = lora::sgmv_tc_supported(n_proj, r_slot, h_in);
+    if (r_slot > 64 && (D > 0 || !tc_shrink)) return LORA_ERR_RANK_EXCEEDS_SLOT;
+    if (!meta->lora_ids) return LORA_ERR_INVALID_ARG;
+    if (!workspace) return LORA_ERR_WORKSPACE;
+    if (ws_bytes < lora_apply_workspace_bytes(T, n_proj, r_slot)) return LORA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LORA_ERR_ALIGNMENT;
+    if (P > 0) LORA_TRY(check_segments(meta->seg_starts, meta->seg_slot, meta->n_segs, P, T, nullptr));
+    if (D > 0) {
+        if (!meta->perm) return LORA_ERR_METADATA;
+        LORA_TRY(check_segments(meta->gseg_starts, meta->gseg_slot, meta->n_gsegs, D, T, meta->perm));
+    }
+    bf16_t* vh = static_cast<bf16_t*>(workspace);
+    bf16_t* vl = vh + plane_region_bytes(T, n_proj, r_slot) / 2 / sizeof(bf16_t);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    // v = A x into the hi/lo planes: tensor-core shrink over the prefill
+    // segments (grouped shrink over them where the tensor-core form does not
+    // apply), grouped shrink over the decode groups
+    if (P > 0 && meta->n_segs > 0) {
+        if (tc_shrink)
+            LORA_TRY(cuda_status(lora::launch_sgmv_shrink_tc(nullptr, 0, vh, vl, x, ld_x, h_in, ps, meta->seg_starts,
+                                                             meta->seg_slot, meta->n_segs, P, T, n_slots,
+                                                             dev_status, s)));
+        else
+            LORA_TRY(cuda_status(lora::launch_bgmv_grouped_shrink(x, ld_x, h_in, ps, nullptr, meta->seg_starts,
+                                                                  meta->seg_slot, meta->n_segs, P,
+                                                                  meta->max_seg_len, T, n_slots, LORA_APPLY_NO_PDL,
+                                                                  vh, vl, dev_status, s)));
+    }
+    if (D > 0 && meta->n_gsegs > 0)
+        LORA_TRY(cuda_status(lora::launch_bgmv_grouped_shrink(x, ld_x, h_in, ps, meta->perm, meta->gseg_starts,
+                                                              meta->gseg_slot, meta->n_gsegs, D, meta->max_gseg_len,
+                                                              T, n_slots, LORA_APPLY_NO_PDL, vh, vl, dev_status,
+                                                              s)));
+    // base product with the delta in the same accumulator
+    return cuda_status(lora::launch_linear_tc(y, ld_y, x, ld_x, h_in, W, ld_w, n_out, ps, vh, vl, meta->lora_ids, T,
+                                              n_slots, dev_status, s));
+}
+
 lora_status_t lora_merge(lora_bf16_t* W, int ld_w, int out, int h_in, const lora_bf16_t* A,
                          const lora_bf16_t* B, int r_slot, int sign, lora_stream_t stream)
 {

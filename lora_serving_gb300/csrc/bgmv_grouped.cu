@@ -75,7 +75,8 @@ __device__ __forceinline__ UnitInfo grouped_unit(const Params& p, int u)
     return ui;
 }
 
-// Rows of the unit through perm (threads 0..15); false when one is out of range.
+// Rows of the unit through perm (threads 0..15; no perm: the positions are
+// the rows); false when one is out of range.
 __device__ __forceinline__ bool unit_rows(const int32_t* perm, int pos0, int nrows, int n_rows, int* s_rows)
 {
     bool bad = false;
@@ -83,7 +84,7 @@ __device__ __forceinline__ bool unit_rows(const int32_t* perm, int pos0, int nro
     if (tid < kRB) {
         int r = 0;
         if (tid < nrows) {
-            r = __ldg(perm + pos0 + tid);
+            r = perm ? __ldg(perm + pos0 + tid) : pos0 + tid;
             if (r < 0 || r >= n_rows) {
                 bad = true;
                 r = 0;
@@ -553,15 +554,17 @@ bgmv_group_expand_kernel(GexParams p)
 
 }  // namespace
 
-cudaError_t launch_bgmv_grouped(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
-                                const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
-                                int n_pos, int max_group_len, int n_rows, int n_slots, unsigned flags,
-                                bf16_t* vh, bf16_t* vl, int32_t* status, cudaStream_t stream)
+namespace {
+
+// Launch geometry shared by the grouped shrink and expand of one call.
+struct GroupedPlan {
+    int r_pad64, ld_p, form_upg, xr, pdl, n_sms;
+    long long units;
+};
+
+cudaError_t grouped_plan(const ProjSet& ps, int n_groups, int n_pos, int max_group_len, unsigned flags,
+                         GroupedPlan& g)
 {
-    if (n_pos <= 0 || n_groups <= 0) return cudaSuccess;
-    if (!vh || !vl || ps.r_slot > 64 || ps.r_slot % 8 != 0) return cudaErrorInvalidValue;
-    const int r_pad64 = (ps.r_slot + 63) / 64 * 64, ld_p = ps.n_proj * r_pad64;
-    const int R = ps.n_proj * ps.r_slot;
     static int configured_device = -1;
     static int n_sms = 0;
     int dev = 0;
@@ -578,18 +581,28 @@ cudaError_t launch_bgmv_grouped(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, 
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
+    g.n_sms = n_sms;
+    g.r_pad64 = (ps.r_slot + 63) / 64 * 64;
+    g.ld_p = ps.n_proj * g.r_pad64;
     // Units: direct numbering (group, sub-unit) unless the longest group
     // makes that grid much larger than the scanned one.
     const long long upg = max_group_len > 0 ? (max_group_len + kRB - 1) / kRB : 0;
     const long long scanned_units = n_groups + n_pos / kRB;
     const long long direct_units = n_groups * upg;
-    const int form_upg = (upg > 0 && direct_units <= 2 * scanned_units) ? static_cast<int>(upg) : 0;
-    long long units = form_upg ? direct_units : scanned_units;
-    if (!form_upg && max_group_len > 0) units = std::min(units, direct_units);
-    const int xr = max_group_len > 0 ? std::min(kRB, max_group_len) : kRB;
-    const int pdl = (flags & LORA_APPLY_NO_PDL) ? 0 : 1;
+    g.form_upg = (upg > 0 && direct_units <= 2 * scanned_units) ? static_cast<int>(upg) : 0;
+    g.units = g.form_upg ? direct_units : scanned_units;
+    if (!g.form_upg && max_group_len > 0) g.units = std::min(g.units, direct_units);
+    g.xr = max_group_len > 0 ? std::min(kRB, max_group_len) : kRB;
+    g.pdl = (flags & LORA_APPLY_NO_PDL) ? 0 : 1;
+    return cudaSuccess;
+}
 
-    // ---- grouped shrink ----
+cudaError_t grouped_shrink(const GroupedPlan& g, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
+                           const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
+                           int n_pos, int n_rows, int n_slots, unsigned flags, bf16_t* vh, bf16_t* vl,
+                           int32_t* status, cudaStream_t stream)
+{
+    const int R = ps.n_proj * ps.r_slot;
     GsParams sp{};
     sp.ps = ps;
     sp.x = x;
@@ -597,8 +610,8 @@ cudaError_t launch_bgmv_grouped(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, 
     sp.h_in = h_in;
     sp.vh = vh;
     sp.vl = vl;
-    sp.ld_p = ld_p;
-    sp.r_pad64 = r_pad64;
+    sp.ld_p = g.ld_p;
+    sp.r_pad64 = g.r_pad64;
     sp.perm = perm;
     sp.gstarts = gstarts;
     sp.gslot = gslot;
@@ -607,23 +620,23 @@ cudaError_t launch_bgmv_grouped(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, 
     sp.n_slots = n_slots;
     sp.n_rows = n_rows;
     sp.n_rb = (R + kGsRanks - 1) / kGsRanks;
-    sp.upg = form_upg;
-    sp.xr = xr;
+    sp.upg = g.form_upg;
+    sp.xr = g.xr;
     // Split K over a cluster only when the (unit, rank block) CTAs would not
     // fill the GPU twice over, keeping at least two stages per CTA.
     int ks = 1;
-    while (ks < 8 && units * sp.n_rb * ks < 2LL * n_sms && h_in / (ks * 2) >= 2 * kGsKT) ks *= 2;
+    while (ks < 8 && g.units * sp.n_rb * ks < 2LL * g.n_sms && h_in / (ks * 2) >= 2 * kGsKT) ks *= 2;
     ks = env_int("LORA_GROUPED_KS", ks);
     sp.ks = ks;
     sp.kc = ((h_in + ks - 1) / ks + kGsKT - 1) / kGsKT * kGsKT;
     sp.x_ready = (flags & LORA_APPLY_X_READY) ? 1 : 0;
     sp.status = status;
-    const long long n_shrink = units * sp.n_rb * ks;
+    const long long n_shrink = g.units * sp.n_rb * ks;
     if (n_shrink > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(n_shrink));
     cfg.blockDim = dim3(kGsThreads);
-    cfg.dynamicSmemBytes = gs_smem_bytes(xr);
+    cfg.dynamicSmemBytes = gs_smem_bytes(g.xr);
     cfg.stream = stream;
     cudaLaunchAttribute attrs[2];
     int na = 0;
@@ -634,16 +647,49 @@ cudaError_t launch_bgmv_grouped(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, 
         attrs[na].val.clusterDim.z = 1;
         ++na;
     }
-    if (pdl) {
+    if (g.pdl) {
         attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attrs[na].val.programmaticStreamSerializationAllowed = 1;
         ++na;
     }
     cfg.attrs = attrs;
     cfg.numAttrs = na;
-    e = cudaLaunchKernelEx(&cfg, bgmv_group_shrink_kernel, sp);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, bgmv_group_shrink_kernel, sp);
     note_launch();
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_bgmv_grouped_shrink(const bf16_t* x, int ld_x, int h_in, const ProjSet& ps, const int32_t* perm,
+                                       const int32_t* gstarts, const int32_t* gslot, int n_groups, int n_pos,
+                                       int max_group_len, int n_rows, int n_slots, unsigned flags, bf16_t* vh,
+                                       bf16_t* vl, int32_t* status, cudaStream_t stream)
+{
+    if (n_pos <= 0 || n_groups <= 0) return cudaSuccess;
+    if (!vh || !vl || ps.r_slot > 64 || ps.r_slot % 8 != 0) return cudaErrorInvalidValue;
+    GroupedPlan g{};
+    const cudaError_t e = grouped_plan(ps, n_groups, n_pos, max_group_len, flags, g);
     if (e != cudaSuccess) return e;
+    return grouped_shrink(g, x, ld_x, h_in, ps, perm, gstarts, gslot, n_groups, n_pos, n_rows, n_slots, flags, vh,
+                          vl, status, stream);
+}
+
+cudaError_t launch_bgmv_grouped(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
+                                const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
+                                int n_pos, int max_group_len, int n_rows, int n_slots, unsigned flags,
+                                bf16_t* vh, bf16_t* vl, int32_t* status, cudaStream_t stream)
+{
+    if (n_pos <= 0 || n_groups <= 0) return cudaSuccess;
+    if (!vh || !vl || ps.r_slot > 64 || ps.r_slot % 8 != 0) return cudaErrorInvalidValue;
+    GroupedPlan g{};
+    cudaError_t e = grouped_plan(ps, n_groups, n_pos, max_group_len, flags, g);
+    if (e != cudaSuccess) return e;
+    e = grouped_shrink(g, x, ld_x, h_in, ps, perm, gstarts, gslot, n_groups, n_pos, n_rows, n_slots, flags, vh, vl,
+                       status, stream);
+    if (e != cudaSuccess) return e;
+    const int r_pad64 = g.r_pad64, ld_p = g.ld_p, form_upg = g.form_upg, pdl = g.pdl;
+    const long long units = g.units;
 
     // ---- grouped expand ----
     GexParams gp{};

@@ -64,6 +64,20 @@ cudaError_t launch_bgmv_grouped(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, 
                                 int n_pos, int max_group_len, int n_rows, int n_slots, unsigned flags,
                                 bf16_t* vh, bf16_t* vl, int32_t* status, cudaStream_t stream);
 
+// The grouped shrink alone (the planes, no expand); perm == nullptr takes
+// positions as rows (contiguous prefill segments as groups).
+cudaError_t launch_bgmv_grouped_shrink(const bf16_t* x, int ld_x, int h_in, const ProjSet& ps, const int32_t* perm,
+                                       const int32_t* gstarts, const int32_t* gslot, int n_groups, int n_pos,
+                                       int max_group_len, int n_rows, int n_slots, unsigned flags, bf16_t* vh,
+                                       bf16_t* vl, int32_t* status, cudaStream_t stream);
+
+// The LoRA linear layer: y[:, off_p + c] = bf16(x W^T + B'_p v_p) for every
+// row (ids per row, -1 = base only), W [n_out][ld_w] stacking the
+// projections' base weights, v from the bf16 hi/lo planes.
+cudaError_t launch_linear_tc(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int h_in, const bf16_t* W, int ld_w,
+                             int n_out, const ProjSet& ps, const bf16_t* vh, const bf16_t* vl,
+                             const int32_t* ids, int n_rows, int n_slots, int32_t* status, cudaStream_t stream);
+
 // W += sign * B A over one adapter slot (merge / unmerge), one rounding.
 cudaError_t launch_merge(bf16_t* W, int ld_w, int out, int h_in, const bf16_t* A, const bf16_t* B, int r_slot,
                          int sign, cudaStream_t stream);

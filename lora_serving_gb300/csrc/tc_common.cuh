@@ -77,7 +77,7 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, unsigned pa
 }
 // Waits for the phase with the given parity to complete; false after
 // kTimeoutNs (the caller flags the timeout and winds down).
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, unsigned parity)
+static __device__ __noinline__ bool mbar_wait(uint64_t* bar, unsigned parity)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = gtime();

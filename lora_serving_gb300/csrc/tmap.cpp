@@ -45,4 +45,19 @@ bool encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_
     return r == CUDA_SUCCESS;
 }
 
+bool encode_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t n0, uint64_t n1, uint64_t n2, uint64_t ld1,
+                         uint64_t ld2, uint32_t box0, uint32_t box2)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {n0, n1, n2};
+    const cuuint64_t strides[2] = {ld1 * 2, ld2 * 2};
+    const cuuint32_t box[3] = {box0, 1, box2};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                          elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace lora

@@ -15,4 +15,11 @@ namespace lora {
 bool encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
                       uint32_t box_rows, uint32_t box_cols, bool swizzle128);
 
+// A 3-D bf16 tensor [n2][n1][n0] (n0 innermost, strides ld1 and ld2
+// elements for dimensions 1 and 2) read in 128-byte-swizzled boxes of
+// box0 (= 64) x 1 x box2.  Elements past n0 read as zero, which pads a
+// short innermost extent inside a longer stored row.
+bool encode_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t n0, uint64_t n1, uint64_t n2, uint64_t ld1,
+                         uint64_t ld2, uint32_t box0, uint32_t box2);
+
 }  // namespace lora

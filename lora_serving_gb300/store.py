@@ -126,3 +126,11 @@ def apply(y: torch.Tensor, x: torch.Tensor, store: GroupStore, meta: BatchMeta,
     """One fused lora_apply call: y[:, slices] += delta of every projection."""
     abi.lora_apply(y, x, store.h_in, store.c_projs(), store.r_slot, store.n_slots, meta.c,
                    workspace, flags=flags, dev_status=dev_status, stream=stream)
+
+
+def linear(y: torch.Tensor, x: torch.Tensor, W: torch.Tensor, store: GroupStore, meta: BatchMeta,
+           workspace: torch.Tensor, dev_status=None, stream=None):
+    """One lora_linear call: y[:, slices] = bf16(x W^T + delta) of every
+    projection, W the group's stacked base weight [ld_y][h_in]."""
+    abi.lora_linear(y, x, store.h_in, W, store.c_projs(), store.r_slot, store.n_slots, meta.c, workspace,
+                    dev_status=dev_status, stream=stream)

@@ -10,6 +10,8 @@ Recipe (shapes follow the five workloads of the LoRA-serving pages' sizing):
     i.i.d. N(0, 0.02^2) rounded to bf16 (B is non-zero, unlike peft's init);
   * x: N(0, 1) rounded to bf16, one matrix per projection group;
   * y_in: zeros ("delta" mode) or N(0, 1) in bf16 ("accumulate" mode);
+  * base weights (the linear layer): the group's stacked W [out][h_in],
+    i.i.d. N(0, 1/h_in) in bf16, so that x W^T is of order one;
   * adapter ids: per workload, see the builders below.
 Draw order: batch structure (lengths, ids) -> adapters (slot, group,
 projection; A then B) -> x per group -> y_in per group.  Every tensor is
@@ -174,6 +176,12 @@ class Workload:
             else:
                 self.y[g.name] = normal_bf16((T, g.ld_y), 1.0, self.seed, f"y{g.name}{L}")
         return self
+
+    def base_weight(self, group: str, layer: int = 0) -> np.ndarray:
+        """The group's stacked base weight [sum of widths][h_in] (bf16 bits)."""
+        g = next(g for g in self.groups if g.name == group)
+        L = f"L{layer}" if layer else ""
+        return normal_bf16((g.ld_y, g.h_in), 1.0 / np.sqrt(g.h_in), self.seed, f"W{g.name}{L}")
 
 
 # ------------------------------------------------------------ workloads ----

@@ -1,0 +1,171 @@
+"""GPU parity of the LoRA linear layer (lora_linear): the base product and
+every row's delta in one fp32 accumulator, rounded once, against the oracle's
+linear projection, on prefill segments (tiles of one adapter and tiles across
+segment boundaries), decode rows (tiles mixing adapters), mixed batches,
+ragged shapes and the error paths."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from helpers import check_bf16, to_dev, to_host
+from lora_serving_gb300 import abi, build, store, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build()
+    abi.load()
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def _case(h_in, widths, ranks, r_slot, ids, n_prefill, seed=0, alpha_per_rank=2.0):
+    g = torch.Generator().manual_seed(seed)
+    n_slots = len(ranks)
+    projs = [(f"p{i}", w) for i, w in enumerate(widths)]
+    A = {(k, p): _bits((torch.randn(r, h_in, generator=g) * 0.05).to(torch.bfloat16))
+         for k, r in enumerate(ranks) for p in range(len(widths))}
+    B = {(k, p): _bits((torch.randn(w, r, generator=g) * 0.05).to(torch.bfloat16))
+         for k, r in enumerate(ranks) for p, w in enumerate(widths)}
+    st = store.GroupStore(h_in, projs, n_slots, r_slot).load_slots(
+        {k: [(A[k, p], B[k, p], alpha_per_rank * r, k % 2 == 1) for p in range(len(widths))]
+         for k, r in enumerate(ranks)})
+    T = len(ids)
+    x = _bits(torch.randn(T, h_in, generator=g).to(torch.bfloat16))
+    W = _bits((torch.randn(sum(widths), h_in, generator=g) / np.sqrt(h_in)).to(torch.bfloat16))
+    ads = [O.Adapters([A[k, p] for k in range(n_slots)], [B[k, p] for k in range(n_slots)],
+                      [O.scale(alpha_per_rank * r, r, k % 2 == 1) for k, r in enumerate(ranks)])
+           for p in range(len(widths))]
+    ids = np.asarray(ids, np.int32)
+    meta = store.BatchMeta(ids, n_prefill, n_slots)
+    return st, x, W, ads, ids, meta
+
+
+def _oracle(ids, x, W, ads, st):
+    ref = np.zeros((len(ids), st.ld_y), np.uint16)
+    for p, off in enumerate(st.offsets):
+        ref = O.linear_projection(ids, x, W[off:off + ads[p].w], ref, off, ads[p])
+    return ref
+
+
+def _run(st, x, W, meta, status=None):
+    T = x.shape[0]
+    y = torch.full((T, st.ld_y), float("nan"), dtype=torch.bfloat16, device="cuda")   # every element written
+    ws = store.workspace_for(T, len(st.projs), st.r_slot)
+    s = status if status is not None else torch.zeros(1, dtype=torch.int32, device="cuda")
+    store.linear(y, to_dev(x), to_dev(W), st, meta, ws, dev_status=s)
+    torch.cuda.synchronize()
+    return to_host(y), abi.lora_read_device_status(s)
+
+
+def _segments(lens, slots):
+    return np.concatenate([np.full(n, s, np.int32) for n, s in zip(lens, slots)])
+
+
+CASES = {
+    # prefill segments: whole tiles of one adapter, tiles across boundaries, a base segment
+    "prefill_qkv": dict(h_in=512, widths=(256, 128, 128), ranks=(8, 16, 12, 4), r_slot=16,
+                        ids=_segments([300, 128, 57, 200, 40], [0, 2, -1, 1, 3]), n_prefill=725),
+    # decode rows only: every tile mixes adapters
+    "decode": dict(h_in=384, widths=(512,), ranks=(32, 8, 24, 16, 32), r_slot=32,
+                   ids=np.array([(i * 7) % 6 - 1 for i in range(70)]), n_prefill=0),
+    # prefill then decode in one batch
+    "mixed": dict(h_in=256, widths=(256, 256), ranks=(16, 16, 16), r_slot=16,
+                  ids=np.concatenate([_segments([200, 200], [1, 0]), np.array([(i * 5) % 4 - 1 for i in range(60)])]),
+                  n_prefill=400),
+    # ragged: h_in not a multiple of 64, widths not multiples of 256, a 2-row last tile
+    "ragged": dict(h_in=200, widths=(136, 520), ranks=(8, 16), r_slot=16,
+                   ids=np.concatenate([_segments([130], [1]), np.array([0, -1])]), n_prefill=130),
+    # the largest slot ranks: two K blocks per plane in the prefill-only form
+    "rank64": dict(h_in=256, widths=(256, 256), ranks=(64, 40, 64), r_slot=64,
+                   ids=_segments([256, 100, 156], [0, 1, 2]), n_prefill=512),
+    "rank128": dict(h_in=256, widths=(384,), ranks=(128, 96), r_slot=128,
+                    ids=_segments([256, 130], [1, 0]), n_prefill=386),
+    # rank 8: the prefill shrink takes the grouped form
+    "rank8": dict(h_in=128, widths=(128, 64), ranks=(8, 8, 8), r_slot=8,
+                  ids=np.concatenate([_segments([150, 90], [2, 0]), np.array([1, 0, 2, -1, 1])]), n_prefill=240),
+    "all_base": dict(h_in=192, widths=(256,), ranks=(16, 16), r_slot=16,
+                     ids=np.concatenate([_segments([140], [-1]), np.full(9, -1)]), n_prefill=140),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_linear_vs_oracle(name):
+    st, x, W, ads, ids, meta = _case(**CASES[name], seed=list(CASES).index(name))
+    got, status = _run(st, x, W, meta)
+    assert status == 0
+    ref = _oracle(ids, x, W, ads, st)
+    # every row is written: compare all of them (none is left at y_in)
+    check_bf16(got, ref, np.zeros_like(ids), got, f"linear {name}")
+
+
+def test_linear_bad_row_id_keeps_base_product_and_is_flagged():
+    c = dict(CASES["decode"])
+    st, x, W, ads, ids, meta = _case(**c, seed=5)
+    bad = 13
+    assert ids[bad] >= 0
+    meta.ids[bad] = len(c["ranks"]) + 3          # the per-row id the layer reads; groups still valid
+    got, status = _run(st, x, W, meta)
+    assert status & abi.LORA_DEV_SLOT_OUT_OF_RANGE
+    ids_ref = ids.copy()
+    ids_ref[bad] = -1
+    ref = _oracle(ids_ref, x, W, ads, st)
+    check_bf16(got, ref, np.zeros_like(ids), got, "linear with a bad id")
+
+
+def test_linear_host_rejections():
+    st, x, W, ads, ids, meta = _case(**CASES["mixed"], seed=2)
+    T = x.shape[0]
+    y = torch.zeros(T, st.ld_y, dtype=torch.bfloat16, device="cuda")
+    ws = store.workspace_for(T, len(st.projs), st.r_slot)
+    xd, Wd = to_dev(x), to_dev(W)
+    gap = abi.make_projs([(st.A[0], st.B[0], 0, 256), (st.A[1], st.B[1], 264, 240)])   # not tiling [0, n_out)
+    with pytest.raises(abi.LoraError) as e:
+        abi.lora_linear(y, xd, st.h_in, Wd, gap, st.r_slot, st.n_slots, meta.c, ws)
+    assert e.value.name == "LORA_ERR_SHAPE"
+    with pytest.raises(abi.LoraError) as e:
+        abi.lora_linear(y, xd, st.h_in, Wd[:, 1:], st.c_projs(), st.r_slot, st.n_slots, meta.c, ws)
+    assert e.value.name in ("LORA_ERR_ALIGNMENT", "LORA_ERR_SHAPE")
+    with pytest.raises(abi.LoraError) as e:
+        abi.lora_linear(y, xd, st.h_in, Wd, st.c_projs(), st.r_slot, st.n_slots, meta.c, ws[:1024])
+    assert e.value.name == "LORA_ERR_WORKSPACE"
+    st128, x128, W128, _, _, meta128 = _case(h_in=128, widths=(128,), ranks=(128,), r_slot=128,
+                                             ids=np.array([0, 0, 0, 0]), n_prefill=2)   # decode rows above rank 64
+    with pytest.raises(abi.LoraError) as e:
+        abi.lora_linear(torch.zeros(4, 128, dtype=torch.bfloat16, device="cuda"), to_dev(x128), 128, to_dev(W128),
+                        st128.c_projs(), 128, 1, meta128.c, store.workspace_for(4, 1, 128))
+    assert e.value.name == "LORA_ERR_RANK_EXCEEDS_SLOT"
+    torch.cuda.synchronize()
+
+
+def test_linear_full_size_sampled_rows():
+    """The Mistral-7B-shaped prefill batch (about 34 K rows, 32 segments over
+    16 adapters of ranks 8-64) through the q/k/v group at full size, with the
+    oracle on a seeded sample of rows (the first and last of every segment
+    and random ones)."""
+    wl = synth.get("mistral7b_prefill")
+    wl.materialise("delta", groups=["qkv"])
+    g = next(g for g in wl.groups if g.name == "qkv")
+    st = store.GroupStore.from_workload(wl, "qkv")
+    W = wl.base_weight("qkv")
+    meta = store.BatchMeta(wl.ids, wl.n_prefill, wl.n_slots)
+    got, status = _run(st, wl.x["qkv"], W, meta)
+    assert status == 0
+    starts = np.cumsum([0] + wl.seg_lens)
+    rng = np.random.default_rng(4)
+    rows = np.unique(np.concatenate([starts[:-1], starts[1:] - 1, rng.integers(0, wl.n_rows, 16)]))
+    ids = wl.ids[rows]
+    ref = np.zeros((rows.size, st.ld_y), np.uint16)
+    for p, (pname, w) in enumerate(g.projs):
+        off = st.offsets[p]
+        ad = O.Adapters([wl.A[("qkv", pname, k)] for k in range(wl.n_slots)],
+                        [wl.B[("qkv", pname, k)] for k in range(wl.n_slots)],
+                        [O.scale(float(wl.alphas[k]), int(wl.ranks[k]), bool(wl.rslora[k])) for k in range(wl.n_slots)])
+        ref = O.linear_projection(ids, wl.x["qkv"][rows], W[off:off + w], ref, off, ad)
+    check_bf16(got[rows], ref, np.zeros_like(ids), got[rows], "linear full size, sampled rows")
