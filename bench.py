@@ -45,6 +45,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--layers", type=int, default=None)
+    ap.add_argument("--seqs", type=int, default=None,
+                    help="prefill sequences of the linear-layer workload (default 32; fewer for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget")
@@ -377,6 +379,228 @@ def run_merge(args, rank, local, ws):
     return out
 
 
+# ----------------------------------------------------- linear layer ----
+# The LoRA linear layer: one Mistral-7B-shaped layer of the prefill batch
+# (32 sequences of 64-2048 tokens over 16 adapters of ranks 8-64) through
+# lora_linear for the q/k/v, o, gate/up and down groups, the base product
+# and every row's delta in one accumulator.  Inputs: seeded bf16, base
+# weights N(0, 1/h_in) (the synthetic recipe).  Context numbers: the same
+# base products through cuBLAS (torch.matmul) without the delta, and cuBLAS
+# followed by lora_apply adding the delta in place (the unfused layer).
+
+LINEAR_WORKLOAD = "linear_mistral7b_prefill"
+LINEAR_BASE = "mistral7b_prefill"
+
+
+def linear_flops(wl, group) -> int:
+    """Algorithmic FLOPs of one lora_linear call: 2 T h_in n_out for the base
+    product plus 2 r (h_in + w) per active row and projection (true ranks)."""
+    return 2 * wl.n_rows * group.h_in * group.ld_y + useful_flops(wl, group)
+
+
+def tensor_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["bf16_tflops_sustained"]), float(d["bf16_tflops"]), "measured"
+    return 1700.0, 1900.0, "fallback"
+
+
+_LINEAR_CPU = None
+
+
+def cpu_oracle_linear_rate(budget_s: float):
+    """The fp64 oracle's linear layer (all four groups of one layer) on rows of
+    the prefill batch, row blocks over all host cores; returns rows per second."""
+    import concurrent.futures as cf
+    import oracle as O
+    from lora_serving_gb300 import synth
+    global _LINEAR_CPU
+    cores = os.cpu_count() or 1
+    if _LINEAR_CPU is None:   # inputs drawn once, outside the timed region
+        wl = synth.get(LINEAR_BASE)
+        rng = np.random.default_rng(0)
+        rows = np.sort(rng.choice(wl.n_rows, size=min(wl.n_rows, 4 * cores), replace=False))
+        wl.materialise("delta")
+        sub = {g.name: wl.x[g.name][rows] for g in wl.groups}
+        Ws = {g.name: wl.base_weight(g.name) for g in wl.groups}
+        ads = {}
+        for g in wl.groups:
+            for pname, _ in g.projs:
+                ads[(g.name, pname)] = O.Adapters(
+                    [wl.A[(g.name, pname, k)] for k in range(wl.n_slots)],
+                    [wl.B[(g.name, pname, k)] for k in range(wl.n_slots)],
+                    [O.scale(float(wl.alphas[k]), int(wl.ranks[k]), bool(wl.rslora[k])) for k in range(wl.n_slots)])
+        wl.x.clear()
+        _LINEAR_CPU = (wl, rows, sub, Ws, ads)
+    wl, rows, sub, Ws, ads = _LINEAR_CPU
+
+    def run_rows(idx):
+        for g in wl.groups:
+            y = np.zeros((len(idx), g.ld_y), np.uint16)
+            for (pname, w), off in zip(g.projs, g.offsets):
+                y = O.linear_projection(wl.ids[rows[idx]], sub[g.name][idx], Ws[g.name][off:off + w], y, off,
+                                        ads[(g.name, pname)])
+        return len(idx)
+
+    done = 0
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        pos = 0
+        while time.perf_counter() - t0 < budget_s and pos < rows.size:
+            blocks = [np.arange(i, min(i + 1, rows.size)) for i in range(pos, min(pos + cores, rows.size))]
+            done += sum(ex.map(run_rows, blocks))
+            pos += len(blocks)
+    dt = time.perf_counter() - t0
+    return done / dt, {"cores": cores, "sample": f"{done} rows of the {wl.n_rows}-row prefill batch, all four "
+                                                 f"groups of one layer", "seconds": round(dt, 3)}
+
+
+def run_linear(args, rank, local, ws):
+    import torch
+    from lora_serving_gb300 import abi, build, store, synth
+    build()
+    abi.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = synth.get(LINEAR_BASE, **({"n_seqs": args.seqs} if args.seqs else {}))
+    wl.materialise("delta")
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    meta = store.BatchMeta(wl.ids, wl.n_prefill, wl.n_slots, device=dev)
+    groups = {}
+    for g in wl.groups:
+        groups[g.name] = {
+            "st": store.GroupStore.from_workload(wl, g.name, device=dev),
+            "x": to_dev(wl.x[g.name]), "W": to_dev(wl.base_weight(g.name)),
+            "y": torch.empty(wl.n_rows, g.ld_y, dtype=torch.bfloat16, device=dev),
+            "ws": store.workspace_for(wl.n_rows, len(g.projs), wl.r_slot, device=dev)}
+    flops_call = {g.name: linear_flops(wl, g) for g in wl.groups}
+    flops_step = sum(flops_call.values())
+
+    def fused():
+        for g in wl.groups:
+            d = groups[g.name]
+            store.linear(d["y"], d["x"], d["W"], d["st"], meta, d["ws"])
+
+    def cublas_base():
+        for g in wl.groups:
+            d = groups[g.name]
+            torch.matmul(d["x"], d["W"].t(), out=d["y"])
+
+    def unfused():
+        for g in wl.groups:
+            d = groups[g.name]
+            torch.matmul(d["x"], d["W"].t(), out=d["y"])
+            store.apply(d["y"], d["x"], d["st"], meta, d["ws"])
+
+    stream = torch.cuda.Stream(device=dev)
+    graphs = {}
+    l0 = None
+    for name_v, fn in (("fused", fused), ("cublas_base", cublas_base), ("unfused", unfused)):
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        if name_v == "fused":
+            l0 = abi.lora_kernel_launch_count()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            fn()
+        if name_v == "fused":
+            launches_per_step = abi.lora_kernel_launch_count() - l0
+        graphs[name_v] = gr
+    torch.cuda.synchronize()
+
+    def timed(gr, steps, warm):
+        for _ in range(warm):
+            gr.replay()
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        cur = torch.cuda.current_stream()
+        torch.cuda.synchronize()
+        e0.record(cur)
+        for _ in range(steps):
+            gr.replay()
+        e1.record(cur)
+        torch.cuda.synchronize()
+        barrier(ws)
+        return e0.elapsed_time(e1)
+
+    other = {}
+    for name_v in ("cublas_base", "unfused"):
+        n_v = max(5, args.steps // 4)
+        other[name_v] = round(timed(graphs[name_v], n_v, args.warmup) / n_v, 4)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ms_local = timed(graphs["fused"], args.steps, args.warmup)
+    clk = clocks.stop()
+    ms = max_over_ranks(ms_local, ws, device=dev if ws > 1 else "cpu")
+    units = sum_over_ranks(float(wl.n_rows * args.steps), ws, device=dev if ws > 1 else "cpu")
+    sustained, burst, kind = tensor_peaks()
+    achieved = flops_step / (ms_local / args.steps / 1e3) / 1e12
+    out = {
+        "metric": "LoRA linear layer tokens/s (base product + per-row delta, one Mistral-7B layer)",
+        "value": round(units / (ms / 1e3), 1), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)", "data": "synthetic",
+        "config": {
+            "workload": LINEAR_WORKLOAD, "tokens": wl.n_rows, "segments": len(wl.seg_lens), "n_slots": wl.n_slots,
+            "r_slot": wl.r_slot, "groups": {g.name: [g.h_in, g.ld_y] for g in wl.groups},
+            "l2": "inputs larger than L2 (x, W and y of a group are 0.3-2 GB each)",
+            "timing": "CUDA graph of the four lora_linear calls of one layer; CUDA events",
+            "ms_per_step_context": {"cublas_base_only": other["cublas_base"],
+                                    "cublas_base_then_lora_apply": other["unfused"]},
+            "parallelism": f"replicas x{ws}",
+        },
+        "roofline": {"kernel": "linear_tc_kernel (+ sgmv_shrink_tc_kernel per call)", "bound": "tensor",
+                     "achieved": round(achieved, 1), "peak": sustained, "unit": "TFLOP/s",
+                     "frac": round(achieved / sustained, 4), "frac_of_burst": round(achieved / burst, 4),
+                     "peak_source": f"{kind} bf16_tflops_sustained (burst {burst})", "per": "step",
+                     "flops_per_step": flops_step, "traffic": None},
+        "clocks": clk,
+        "gpu_launches": int(launches_per_step * args.steps),
+    }
+    if not args.no_e2e:
+        hx = {g.name: torch.from_numpy(wl.x[g.name].view(np.int16)).view(torch.bfloat16).pin_memory()
+              for g in wl.groups}
+        hy = {g.name: torch.empty(wl.n_rows, g.ld_y, dtype=torch.bfloat16).pin_memory() for g in wl.groups}
+        h_ids = torch.from_numpy(wl.ids.copy()).pin_memory()
+
+        def e2e_step():
+            meta.ids.copy_(h_ids, non_blocking=True)
+            for g in wl.groups:
+                d = groups[g.name]
+                d["x"].copy_(hx[g.name], non_blocking=True)
+                store.linear(d["y"], d["x"], d["W"], d["st"], meta, d["ws"])
+                hy[g.name].copy_(d["y"], non_blocking=True)
+
+        n = max(3, min(args.steps, 10))
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        out["e2e"] = {"value": round(wl.n_rows * n / (ems / 1e3), 1), "unit": "tokens/s",
+                      "h2d_bytes_per_step": int(sum(t.numel() * 2 for t in hx.values()) + h_ids.numel() * 4),
+                      "d2h_bytes_per_step": int(sum(t.numel() * 2 for t in hy.values())), "steps": n,
+                      "ms_per_step": round(ems / n, 4)}
+    if args.seqs:
+        out["config"]["seqs"] = args.seqs
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        rate, info = cpu_oracle_linear_rate(args.cpu_seconds)
+        out["cpu_baseline"] = {"value": round(rate, 2), "unit": "tokens/s", "cores": info["cores"],
+                               "kind": "oracle", "sample": info["sample"]}
+    return out
+
+
 # ---------------------------------------------------------- slots ----
 # Adapter slot manager: loading adapters into GPU slots.  Llama-3.2-3B q/k/v/o
 # adapters of rank 16 (640 KiB prepared), SLOTS_N slots, a pool of SLOTS_POOL
@@ -675,6 +899,24 @@ def run_reference(args, rank, ws):
     name = args.workload
     layers = args.layers or LAYERS.get(name, 1)
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
+    if name == LINEAR_WORKLOAD:
+        vals, info = [], None
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            rate, info = cpu_oracle_linear_rate(per_step)
+            vals.append(rate)
+        value = statistics.median(vals)
+        return {
+            "impl": "reference",
+            "metric": "LoRA linear layer tokens/s (base product + per-row delta, one Mistral-7B layer)",
+            "value": round(value, 2), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "config": {"workload": name},
+            "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": info["cores"], "kind": "oracle",
+                             "sample": info["sample"]},
+            "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "seconds": round(time.perf_counter() - t0, 2),
+        }
     if name == MERGE_WORKLOAD:
         vals, info = [], None
         t0 = time.perf_counter()
@@ -729,6 +971,8 @@ def main(argv=None):
     rank, local, ws = dist_setup("nccl")
     if args.workload == MERGE_WORKLOAD:
         out = run_merge(args, rank, local, ws)
+    elif args.workload == LINEAR_WORKLOAD:
+        out = run_linear(args, rank, local, ws)
     elif args.workload == SLOTS_WORKLOAD:
         out = run_slots(args, rank, local, ws)
     else:

@@ -12,21 +12,28 @@
 //                               + sum_j B'_{p,id_t}[c][j] v_{p,t}[j] )
 // with v = A x from the shrink kernels, stored as bf16 planes v_hi + v_lo.
 //
-// Persistent tcgen05 GEMM, one CTA per SM, tiles of 128 rows x 256 output
+// Persistent tcgen05 GEMM, one CTA per SM, tiles of 256 rows x 256 output
 // columns of one projection, visited in groups of kGroupM row tiles so that
-// the x and W tiles in flight at once fit in L2.  Per tile the K loop is
-// ceil(h_in / 64) base steps (an x box and a W box) followed, when every row
-// of the tile carries the same adapter (the common case inside a prefill
-// segment), by 2 * ceil(r_slot / 64) LoRA steps (a v_hi or v_lo box and a
-// box of B') into the same accumulator: the delta is a K extension of the
-// GEMM.  In tiles whose rows mix adapters (segment boundaries, decode rows)
-// the epilogue adds each row's delta on the CUDA cores from the planes and
-// B' before rounding.
+// the x and W tiles in flight at once fit in L2.  A tile is two 128-row
+// halves, each an M = 128 MMA into its own 256 columns of tensor memory,
+// sharing every W box: 64 bytes of operands per 1024 MMA cycles.  Per tile
+// the K loop is ceil(h_in / 64) base steps (a 256-row x box and a W box)
+// followed by ceil(r_slot / 64) LoRA steps (the half's v_hi and v_lo boxes
+// and a box of B') per adapter of each half, into the half's accumulator:
+// the delta is a K extension of the GEMM.  A half whose rows all carry one
+// adapter (the common case inside a prefill segment) takes one extension;
+// a half with up to four adapters (a segment boundary, base rows) takes one
+// per adapter, the v rows of the other rows zeroed in shared memory by a
+// mask warp first; with more adapters than that (decode rows) the epilogue
+// adds each row's delta on the CUDA cores from the planes and B' before
+// rounding.  The LoRA boxes of a tile are prefetched into L2 when the
+// tile starts.
 //   warp 0: TMA producer   warp 1: MMA issuer   warps 2..17: epilogue
-// The fp32 accumulator is double-buffered in tensor memory (2 x 256
-// columns), so the epilogue of one tile overlaps the K loop of the next.
-// Every wait is bounded (0.2 s); a timeout sets LORA_DEV_TIMEOUT and the
-// CTA winds down, freeing its tensor memory.
+//   warp 18: masks v in the LoRA steps of halves that mix adapters
+// The accumulator fills all 512 tensor-memory columns, so a tile's MMAs
+// start once the epilogue has read the previous tile out (a few percent of
+// a tile's K loop).  Every wait is bounded (0.2 s); a timeout sets
+// LORA_DEV_TIMEOUT and the CTA winds down, freeing its tensor memory.
 
 #include <algorithm>
 
@@ -40,15 +47,18 @@ namespace {
 
 using namespace tc;
 
-constexpr int kLM = 128;                      // rows per tile
+constexpr int kLH = 128;                      // rows per MMA (one tensor-memory lane each)
+constexpr int kLM = 2 * kLH;                  // rows per tile
 constexpr int kLN = 256;                      // output columns per tile
 constexpr int kLK = 64;                       // K elements per step (one 128-byte swizzled row)
-constexpr int kLStages = 4;
-constexpr int kABytes = kLM * 128;            // x or v box
+constexpr int kLStages = 3;
+constexpr int kABytes = kLM * 128;            // x box (256 rows); a v box uses the first half
 constexpr int kBBytes = kLN * 128;            // W or B' box
+constexpr int kHalfBytes = kLH * 128;
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kLEpiWarps = 16;                // 4 per tensor-memory lane quarter, 64 columns each
-constexpr int kLThreads = 32 * (2 + kLEpiWarps);
+constexpr int kLMaskWarp = 2 + kLEpiWarps;    // zeroes v rows of other adapters in masked LoRA steps
+constexpr int kLThreads = 32 * (3 + kLEpiWarps);
 constexpr int kGroupM = 16;                   // row tiles per raster group
 
 struct LinearParams {
@@ -90,19 +100,92 @@ __device__ __forceinline__ LTile tile_of(const LinearParams& P, int t)
     return T;
 }
 
-// The adapter slot shared by every row of row tile m, or -1 when the rows
-// mix adapters, include base rows or name an id outside [0, n_slots).
-// Whole warp; the answer is the same in every warp that asks.
-__device__ __forceinline__ int uniform_slot(const LinearParams& P, int m)
+constexpr int kMaxSlotsHalf = 4;   // adapters per half taken on the tensor cores
+
+// How the delta of one 128-row half is formed.
+enum HalfKind { kNone = 0, kUniform = 1, kMasked = 2, kRows = 3 };
+
+// Plans half h of row tile m (whole warp; every warp that asks gets the
+// same answer).  Each lane holds the ids of rows lane, lane+32, lane+64,
+// lane+96 of the half (-1 past the last row).  The half's distinct valid
+// adapters, in order of first claim, go to sl[]:
+//   kNone     no row has an adapter;
+//   kUniform  every row has the same adapter: one K extension;
+//   kMasked   up to kMaxSlotsHalf adapters (a segment boundary, base rows):
+//             one K extension per adapter, with the v rows of the other
+//             rows zeroed in shared memory before the MMA;
+//   kRows     more adapters than that (decode rows): the epilogue adds
+//             each row's delta on the CUDA cores.
+// Ids outside [-1, n_slots) take no delta (the epilogue flags them).
+__device__ __forceinline__ int plan_half(const LinearParams& P, int m, int h, int* sl, int& nsl, int* myid)
 {
     const int lane = threadIdx.x & 31;
-    const int row0 = m * kLM, nr = min(kLM, P.n_rows - row0);
-    const int first = __ldg(P.ids + row0);
-    bool same = true;
-    for (int i = lane; i < nr; i += 32) same &= __ldg(P.ids + row0 + i) == first;
-    same = __all_sync(0xFFFFFFFFu, same);
-    return (same && first >= 0 && first < P.n_slots) ? first : -1;
+    const int row0 = m * kLM + h * kLH, nr = min(kLH, P.n_rows - row0);
+    unsigned open = 0;   // this lane's rows with a valid adapter not yet listed
+    bool all_valid = true;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = lane + 32 * i;
+        myid[i] = r < nr ? __ldg(P.ids + row0 + r) : -1;
+        const bool v = myid[i] >= 0 && myid[i] < P.n_slots;
+        if (v) open |= 1u << i;
+        if (r < nr && !v) all_valid = false;
+    }
+    all_valid = __all_sync(0xFFFFFFFFu, all_valid);
+    nsl = 0;
+    for (;;) {
+        const unsigned ball = __ballot_sync(0xFFFFFFFFu, open != 0);
+        if (ball == 0) break;
+        if (nsl == kMaxSlotsHalf) return kRows;
+        int cand = -1;
+#pragma unroll
+        for (int i = 3; i >= 0; --i)
+            if (open & (1u << i)) cand = myid[i];
+        cand = __shfl_sync(0xFFFFFFFFu, cand, __ffs(ball) - 1);
+        sl[nsl++] = cand;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (myid[i] == cand) open &= ~(1u << i);
+    }
+    if (nsl == 0) return kNone;
+    return (nsl == 1 && all_valid) ? kUniform : kMasked;
 }
+
+// A tile's K steps: the base steps, then kbs LoRA steps for each adapter
+// of each half planned onto the tensor cores (half 0 first).  A LoRA step
+// carries the v_hi and v_lo boxes of the half (the A region) and one box
+// of B' (the B region): two MMAs per K slice on the same B'.
+struct Plan {
+    int kind[2];
+    int nsl[2];
+    int sl[2][kMaxSlotsHalf];
+    int myid[2][4];
+    int live[2];   // the half has rows
+    int n_ks;
+    __device__ __forceinline__ void make(const LinearParams& P, int m)
+    {
+        live[0] = 1;
+        live[1] = m * kLM + kLH < P.n_rows;
+        int n_ext = 0;
+        for (int h = 0; h < 2; ++h) {
+            kind[h] = plan_half(P, m, h, sl[h], nsl[h], myid[h]);
+            if (kind[h] == kUniform || kind[h] == kMasked) n_ext += nsl[h];
+            else nsl[h] = 0;
+        }
+        n_ks = P.n_kb + P.kbs * n_ext;
+    }
+    // LoRA step l (0-based after the base steps) -> half, adapter index, K block
+    __device__ __forceinline__ void lora(const LinearParams& P, int l, int& h, int& j, int& kb) const
+    {
+        j = l / P.kbs;
+        kb = l - j * P.kbs;
+        h = 0;
+        if (j >= nsl[0]) {
+            j -= nsl[0];
+            h = 1;
+        }
+    }
+};
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar)
 {
@@ -111,6 +194,21 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         "[%5];\n" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
         : "memory");
+}
+
+// L2 prefetches of a box (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n" ::"l"(reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
 }
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p)
@@ -179,7 +277,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
                  const __grid_constant__ CUtensorMap mb2, const __grid_constant__ CUtensorMap mb3, LinearParams P)
 {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full[kLStages], empty[kLStages], acc_full[2], acc_empty[2];
+    __shared__ __align__(8) uint64_t full[kLStages], empty[kLStages], mask_req[kLStages], masked[kLStages];
+    __shared__ __align__(8) uint64_t acc_full, acc_empty;
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_fail;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -191,11 +290,11 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
         for (int s = 0; s < kLStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);   // released by the MMA commit of the stage's last read
+            mbar_init(&mask_req[s], 1);  // the MMA asks for a masked LoRA step's v rows to be zeroed
+            mbar_init(&masked[s], 1);    // ... and they are
         }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_empty[a], kLEpiWarps);
-        }
+        mbar_init(&acc_full, 1);
+        mbar_init(&acc_empty, kLEpiWarps);
         mbar_init_fence();
         s_fail = 0;
     }
@@ -204,29 +303,41 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
-    if (warp == 0) {   // ---- producer (lane 0 issues; the warp decides each tile's kind) ----
+    if (warp == 0) {   // ---- producer (lane 0 issues; the warp plans each tile) ----
         int it = 0;
         for (int t = blockIdx.x; t < P.n_tiles && !s_fail; t += gridDim.x) {
             const LTile T = tile_of(P, t);
-            const int us = uniform_slot(P, T.m);
-            const int n_ks = P.n_kb + (us >= 0 ? 2 * P.kbs : 0);
+            Plan pl;
+            pl.make(P, T.m);
             if (lane == 0) {
-                for (int k = 0; k < n_ks; ++k, ++it) {
+                // the LoRA boxes come after the whole base K loop: start them
+                // towards L2 now so that those steps do not wait on DRAM
+                for (int l = 0; l < pl.n_ks - P.n_kb; ++l) {
+                    int h, j, kb;
+                    pl.lora(P, l, h, j, kb);
+                    tma_prefetch_3d(&mvh, kb * kLK, T.p, T.m * kLM + h * kLH);
+                    tma_prefetch_3d(&mvl, kb * kLK, T.p, T.m * kLM + h * kLH);
+                    tma_prefetch_2d(bmap[T.p], kb * kLK, pl.sl[h][j] * P.width[T.p] + T.col0);
+                }
+                for (int k = 0; k < pl.n_ks; ++k, ++it) {
                     const int s = it % kLStages;
-                    if (it >= kLStages && !mbar_wait(&empty[s], ((it / kLStages) - 1) & 1)) {
+                    if (it >= kLStages && !mbar_wait_spin(&empty[s], ((it / kLStages) - 1) & 1)) {
                         s_fail = 1;
                         break;
                     }
                     uint8_t* a = ring + s * kStageBytes;
                     uint8_t* b = a + kABytes;
-                    mbar_expect_tx(&full[s], kStageBytes);
                     if (k < P.n_kb) {
+                        mbar_expect_tx(&full[s], kStageBytes);
                         tma_load_2d(a, &mx, k * kLK, T.m * kLM, &full[s]);
                         tma_load_2d(b, &mw, k * kLK, P.out_off[T.p] + T.col0, &full[s]);
                     } else {
-                        const int l = k - P.n_kb, plane = l / P.kbs, kb = l - plane * P.kbs;
-                        tma_load_3d(a, plane ? &mvl : &mvh, kb * kLK, T.p, T.m * kLM, &full[s]);
-                        tma_load_2d(b, bmap[T.p], kb * kLK, us * P.width[T.p] + T.col0, &full[s]);
+                        int h, j, kb;
+                        pl.lora(P, k - P.n_kb, h, j, kb);
+                        mbar_expect_tx(&full[s], kStageBytes);
+                        tma_load_3d(a, &mvh, kb * kLK, T.p, T.m * kLM + h * kLH, &full[s]);
+                        tma_load_3d(a + kHalfBytes, &mvl, kb * kLK, T.p, T.m * kLM + h * kLH, &full[s]);
+                        tma_load_2d(b, bmap[T.p], kb * kLK, pl.sl[h][j] * P.width[T.p] + T.col0, &full[s]);
                     }
                 }
             }
@@ -235,78 +346,175 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
         }
     } else if (warp == 1) {   // ---- MMA issuer ----
         int it = 0, ti = 0, ok = 1;
+        int mc[kLStages] = {};   // masked steps seen per stage (the phase of masked[s])
         for (int t = blockIdx.x; ok && t < P.n_tiles && !s_fail; t += gridDim.x, ++ti) {
             const LTile T = tile_of(P, t);
-            const int us = uniform_slot(P, T.m);
-            const int n_ks = P.n_kb + (us >= 0 ? 2 * P.kbs : 0);
+            Plan pl;
+            pl.make(P, T.m);
             if (lane == 0) {
-                const int a = ti & 1;
-                const uint32_t idesc = idesc_bf16_f32(kLM, (T.ncols + 15) / 16 * 16);
-                if (ti >= 2 && !mbar_wait(&acc_empty[a], ((ti >> 1) - 1) & 1)) ok = 0;
+                const uint32_t idesc = idesc_bf16_f32(kLH, (T.ncols + 15) / 16 * 16);
+                const bool live1 = pl.live[1];
+                if (ti >= 1 && !mbar_wait_spin(&acc_empty, (ti - 1) & 1)) ok = 0;
                 tc_fence_after();
-                const uint32_t d = tmem + a * kLN;
-                for (int k = 0; ok && k < n_ks; ++k, ++it) {
+                for (int k = 0; ok && k < pl.n_ks; ++k, ++it) {
                     const int s = it % kLStages;
-                    if (!mbar_wait(&full[s], (it / kLStages) & 1)) {
+                    if (!mbar_wait_spin(&full[s], (it / kLStages) & 1)) {
                         ok = 0;
                         break;
                     }
-                    tc_fence_after();
                     const uint32_t as = smem_u32(ring + s * kStageBytes), bs = as + kABytes;
+                    if (k < P.n_kb) {
+                        tc_fence_after();
 #pragma unroll
-                    for (int ks = 0; ks < kLK / 16; ++ks)
-                        mma_bf16(d, sdesc_sw128(as + ks * 32), sdesc_sw128(bs + ks * 32), idesc, k > 0 || ks > 0);
+                        for (int ks = 0; ks < kLK / 16; ++ks)
+                            mma_bf16(tmem, sdesc_sw128(as + ks * 32), sdesc_sw128(bs + ks * 32), idesc, k > 0 || ks > 0);
+                        if (live1) {
+#pragma unroll
+                            for (int ks = 0; ks < kLK / 16; ++ks)
+                                mma_bf16(tmem + kLN, sdesc_sw128(as + kHalfBytes + ks * 32), sdesc_sw128(bs + ks * 32),
+                                         idesc, k > 0 || ks > 0);
+                        }
+                    } else {
+                        int h, j, kb;
+                        pl.lora(P, k - P.n_kb, h, j, kb);
+                        if (pl.kind[h] == kMasked) {
+                            // the mask warp zeroes the other adapters' rows of this v box first;
+                            // requests and replies alternate, so each stage's phases pair up
+                            mbar_arrive(&mask_req[s]);
+                            if (!mbar_wait_spin(&masked[s], (mc[s]++) & 1)) {
+                                ok = 0;
+                                break;
+                            }
+                        }
+                        tc_fence_after();
+                        for (int plane = 0; plane < 2; ++plane) {   // v_hi, then v_lo, on the same B'
+#pragma unroll
+                            for (int ks = 0; ks < kLK / 16; ++ks)
+                                mma_bf16(tmem + h * kLN, sdesc_sw128(as + plane * kHalfBytes + ks * 32),
+                                         sdesc_sw128(bs + ks * 32), idesc, true);
+                        }
+                    }
                     mma_commit(&empty[s]);   // the stage is free once these MMAs have read it
                 }
-                if (ok) mma_commit(&acc_full[a]);
+                if (ok) mma_commit(&acc_full);
             }
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             it = __shfl_sync(0xFFFFFFFFu, it, 0);
+        }
+        if (!ok) s_fail = 1;
+    } else if (warp == kLMaskWarp) {   // ---- v masking for halves that mix adapters ----
+        int it = 0, ok = 1;
+        int mr[kLStages] = {};   // requests served per stage (the phase of mask_req[s])
+        for (int t = blockIdx.x; ok && t < P.n_tiles && !s_fail; t += gridDim.x) {
+            const LTile T = tile_of(P, t);
+            Plan pl;
+            pl.make(P, T.m);
+            for (int k = P.n_kb; ok && k < pl.n_ks; ++k) {
+                const int step = it + k, s = step % kLStages;
+                int h, j, kb;
+                pl.lora(P, k - P.n_kb, h, j, kb);
+                if (pl.kind[h] != kMasked) continue;
+                // the request comes after the stage has landed and before it can be
+                // refilled, so the stage's fill phase is exactly this step's
+                if (lane == 0 && (!mbar_wait_spin(&mask_req[s], (mr[s]++) & 1) ||
+                                  !mbar_wait_spin(&full[s], (step / kLStages) & 1)))
+                    ok = 0;
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                if (!ok) break;
+                uint8_t* vbox = ring + s * kStageBytes;   // v_hi box, then the v_lo box
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (pl.myid[h][i] != pl.sl[h][j]) {
+#pragma unroll
+                        for (int plane = 0; plane < 2; ++plane) {
+                            uint4* row = reinterpret_cast<uint4*>(vbox + plane * kHalfBytes + (lane + 32 * i) * 128);
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                }
+                fence_async_smem();   // the tensor cores read what these generic stores wrote
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&masked[s]);
+            }
+            it += pl.n_ks;
         }
         if (!ok) s_fail = 1;
     } else {   // ---- epilogue ----
         const int e = warp - 2;
         const int quarter = warp & 3;        // tensor-memory lanes this warp may read
         const int cs = (e >> 2) * 64;        // its 64 columns of the tile
-        const int r = quarter * 32 + lane;   // its row of the tile
         int ti = 0;
         for (int t = blockIdx.x; t < P.n_tiles; t += gridDim.x, ++ti) {
             const LTile T = tile_of(P, t);
-            const int us = uniform_slot(P, T.m);
-            const int a = ti & 1;
-            if (s_fail || !mbar_wait(&acc_full[a], (ti >> 1) & 1)) {
+            Plan pl;
+            pl.make(P, T.m);
+            if (s_fail || !mbar_wait(&acc_full, ti & 1)) {
                 s_fail = 1;
                 break;
             }
             tc_fence_after();
-            const uint32_t tcol = tmem + a * kLN + (static_cast<uint32_t>(quarter * 32) << 16) + cs;
-            const int row = T.m * kLM + r;
-            const bool live = row < P.n_rows;
-            int id = -1;
-            if (live && us < 0) {
-                id = __ldg(P.ids + row);
-                if (id < -1 || id >= P.n_slots) {
-                    flag(P.status, LORA_DEV_SLOT_OUT_OF_RANGE);   // the row keeps its base value
-                    id = -1;
+            const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + cs;
+            if (pl.kind[0] != kRows && pl.kind[1] != kRows) {
+                // no per-row delta: read the warp's four 32-column pieces,
+                // round them into registers, hand the accumulator back to the
+                // MMA at once, then store
+                uint32_t pk[4][16];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                    for (int g = 0; g < 2; ++g) {   // 16 columns per read keeps the registers in bounds
+                        float d[16];
+                        tmem_ld16(tbase + (q >> 1) * kLN + (q & 1) * 32 + g * 16, d);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) pk[q][8 * g + i] = pack_bf16x2(d[2 * i], d[2 * i + 1]);
+                    }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int h = q >> 1, c0 = cs + (q & 1) * 32;
+                    const int row = T.m * kLM + h * kLH + quarter * 32 + lane;
+                    if (row < P.n_rows && c0 < T.ncols) {
+                        const int id = quarter == 0 ? pl.myid[h][0] : quarter == 1 ? pl.myid[h][1]
+                                     : quarter == 2 ? pl.myid[h][2] : pl.myid[h][3];
+                        if ((id < -1 || id >= P.n_slots) && (q & 1) == 0 && c0 == 0)
+                            flag(P.status, LORA_DEV_SLOT_OUT_OF_RANGE);   // the row keeps its base value
+                        uint4* yp = reinterpret_cast<uint4*>(P.y + static_cast<size_t>(row) * P.ld_y + P.out_off[T.p] +
+                                                             T.col0 + c0);
+#pragma unroll
+                        for (int c8 = 0; c8 < 4; ++c8)
+                            if (c8 * 8 < T.ncols - c0)
+                                yp[c8] = make_uint4(pk[q][4 * c8], pk[q][4 * c8 + 1], pk[q][4 * c8 + 2], pk[q][4 * c8 + 3]);
+                    }
+                }
+                continue;
             }
-            bf16_t* yrow = P.y + static_cast<size_t>(min(row, P.n_rows - 1)) * P.ld_y + P.out_off[T.p] + T.col0;
-            // 32 accumulator columns at a time; the accumulator is handed back
-            // to the MMA after the second read (it is next needed two tiles on)
+            // a half adds per-row deltas on the CUDA cores: 32 accumulator
+            // columns at a time (half h, piece c): read, add the row's delta,
+            // round and store; the accumulator goes back after the last read
 #pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
+            for (int q = 0; q < 4; ++q) {
+                const int h = q >> 1, c0 = cs + (q & 1) * 32;
                 float d[32];
-                tmem_ld32(tcol + h * 32, d);
-                if (h == 1) {
+                tmem_ld32(tbase + h * kLN + (q & 1) * 32, d);
+                if (q == 3) {
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&acc_empty[a]);
+                    if (lane == 0) mbar_arrive(&acc_empty);
                 }
-                const int c0 = cs + h * 32;   // first column of this piece in the tile
-                if (live && c0 < T.ncols) {
-                    // rows that mix adapters add their own delta here
-                    if (id >= 0) add_row_delta(P, T.p, id, row, T.col0 + c0, d);
-                    store_row32(yrow + c0, T.ncols - c0, d);
+                const int row = T.m * kLM + h * kLH + quarter * 32 + lane;
+                if (row < P.n_rows && c0 < T.ncols) {
+                    const int id = pl.myid[h][quarter];   // the id of this lane's row (row = quarter * 32 + lane)
+                    if (id >= 0 && id < P.n_slots) {
+                        if (pl.kind[h] == kRows) add_row_delta(P, T.p, id, row, T.col0 + c0, d);
+                    } else if (id != -1 && (q & 1) == 0 && c0 == 0) {
+                        flag(P.status, LORA_DEV_SLOT_OUT_OF_RANGE);   // the row keeps its base value
+                    }
+                    store_row32(P.y + static_cast<size_t>(row) * P.ld_y + P.out_off[T.p] + T.col0 + c0,
+                                T.ncols - c0, d);
                 }
             }
         }
@@ -345,8 +553,8 @@ cudaError_t launch_linear_tc(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int
     CUtensorMap mx, mw, mvh, mvl, mb[4];
     if (!encode_tmap_bf16(&mx, x, n_rows, h_in, ld_x, kLM, kLK, true) ||
         !encode_tmap_bf16(&mw, W, n_out, h_in, ld_w, kLN, kLK, true) ||
-        !encode_tmap_bf16_3d(&mvh, vh, ps.r_slot, ps.n_proj, n_rows, P.r_pad64, P.ld_p, kLK, kLM) ||
-        !encode_tmap_bf16_3d(&mvl, vl, ps.r_slot, ps.n_proj, n_rows, P.r_pad64, P.ld_p, kLK, kLM))
+        !encode_tmap_bf16_3d(&mvh, vh, ps.r_slot, ps.n_proj, n_rows, P.r_pad64, P.ld_p, kLK, kLH) ||
+        !encode_tmap_bf16_3d(&mvl, vl, ps.r_slot, ps.n_proj, n_rows, P.r_pad64, P.ld_p, kLK, kLH))
         return cudaErrorInvalidValue;
     for (int q = 0; q < 4; ++q) {
         const int src = q < ps.n_proj ? q : 0;

@@ -86,6 +86,30 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, unsigned parity)
     return true;
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, unsigned parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// The same bounded wait by polling, never suspending: for the single
+// threads that feed the tensor cores, where a late wake-up leaves the
+// pipeline idle.  false after kTimeoutNs.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, unsigned parity)
+{
+    if (mbar_test_wait(bar, parity)) return true;
+    const unsigned long long t0 = gtime();
+    for (unsigned n = 1;; ++n) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((n & 255u) == 0 && gtime() - t0 > kTimeoutNs) return false;
+    }
+}
+
 // ---- TMA ----------------------------------------------------------------
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map)

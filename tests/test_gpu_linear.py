@@ -90,6 +90,11 @@ CASES = {
     # rank 8: the prefill shrink takes the grouped form
     "rank8": dict(h_in=128, widths=(128, 64), ranks=(8, 8, 8), r_slot=8,
                   ids=np.concatenate([_segments([150, 90], [2, 0]), np.array([1, 0, 2, -1, 1])]), n_prefill=240),
+    # one half with exactly four adapters (tensor-core masked extensions) and with five (CUDA-core rows)
+    "four_in_half": dict(h_in=256, widths=(256,), ranks=(16, 8, 16, 12), r_slot=16,
+                         ids=np.array([i % 4 for i in range(100)]), n_prefill=0),
+    "five_in_half": dict(h_in=256, widths=(256,), ranks=(16, 8, 16, 12, 4), r_slot=16,
+                         ids=np.array([i % 5 for i in range(100)]), n_prefill=0),
     "all_base": dict(h_in=192, widths=(256,), ranks=(16, 16), r_slot=16,
                      ids=np.concatenate([_segments([140], [-1]), np.full(9, -1)]), n_prefill=140),
 }
@@ -105,10 +110,12 @@ def test_linear_vs_oracle(name):
     check_bf16(got, ref, np.zeros_like(ids), got, f"linear {name}")
 
 
-def test_linear_bad_row_id_keeps_base_product_and_is_flagged():
-    c = dict(CASES["decode"])
+@pytest.mark.parametrize("name,bad", [("decode", 13), ("mixed", 407)])
+def test_linear_bad_row_id_keeps_base_product_and_is_flagged(name, bad):
+    """A row whose id is out of range, in a half handled on the CUDA cores
+    (decode) and in one handled by masked tensor-core extensions (mixed)."""
+    c = dict(CASES[name])
     st, x, W, ads, ids, meta = _case(**c, seed=5)
-    bad = 13
     assert ids[bad] >= 0
     meta.ids[bad] = len(c["ranks"]) + 3          # the per-row id the layer reads; groups still valid
     got, status = _run(st, x, W, meta)
