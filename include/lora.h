@@ -311,13 +311,14 @@ lora_status_t lora_merge(lora_bf16_t* W, int ld_w, int out, int h_in, const lora
  * zero-padded to the slot rank -- before it is used.
  *
  * The manager owns a host cache of up to max_cpu prepared adapters in pinned
- * memory (least recently used evicted first) and assigns adapters to the
- * n_slots slots of the caller's device stores (least recently used slot
- * reused first, never one the current batch needs).  Loading an adapter
- * into a slot is one cudaMemcpyAsync per projection for A and for B on the
- * caller's stream: kernels enqueued on that stream after lora_slots_acquire
- * see it, kernels enqueued before it have finished with the slot's old
- * contents.  Use one stream for lora_slots_acquire and the kernels that read
+ * memory mapped into the device's address space (least recently used
+ * evicted first) and assigns adapters to the n_slots slots of the caller's
+ * device stores (least recently used slot reused first, never one the
+ * current batch needs).  The adapters a batch loads are gathered from the
+ * host cache into their slots by one kernel launch (per 64 pieces; a piece
+ * is one projection's A or B) on the caller's stream: kernels enqueued on
+ * that stream after lora_slots_acquire see them, kernels enqueued before it
+ * have finished with the slots' old contents.  Use one stream for lora_slots_acquire and the kernels that read
  * the stores.  Not thread-safe: one manager per serving thread.
  *
  * Without device stores the manager only tracks the assignment (no device
@@ -367,8 +368,8 @@ lora_status_t lora_slots_register(lora_slot_manager_t* m, int64_t adapter_id, co
  * slots_out (-1 stays -1), loading the adapters that are not resident.
  * Errors, before anything is enqueued or changed: LORA_ERR_INVALID_ARG (an
  * id neither -1 nor registered), LORA_ERR_SLOT_RANGE (more distinct adapters
- * than slots).  LORA_ERR_CUDA: a copy could not be enqueued; the slot it was
- * meant for is left empty, adapters loaded before it stay loaded.
+ * than slots).  LORA_ERR_CUDA: the load could not be enqueued; the slots
+ * meant for this batch's loads are left empty (resident adapters stay).
  */
 lora_status_t lora_slots_acquire(lora_slot_manager_t* m, const int64_t* adapter_ids, int n, int32_t* slots_out,
                                  lora_stream_t stream);

@@ -10,13 +10,15 @@
 // Policy: the host cache drops its least recently used adapter that is not
 // resident in a slot; a batch's adapters that are not resident go to free
 // slots first, then to the least recently used slots the batch does not
-// need.  Loads are cudaMemcpyAsync calls (one per projection for A and for
-// B) from pinned host memory on the caller's stream; an event after an
-// adapter's last load guards its host buffers against being overwritten or
-// freed while a copy is still in flight.
+// need.  The host cache is pinned and mapped into the device's address
+// space, and one gather kernel per batch (slot_copy.cu) moves every piece
+// of every adapter the batch loads, on the caller's stream; an event after
+// it guards those host buffers against being overwritten or freed while the
+// copy is still in flight.
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 #include <limits>
 #include <new>
@@ -24,10 +26,12 @@
 #include <vector>
 
 #include "lora.h"
+#include "slot_copy.h"
 
 struct lora_slot_manager {
     struct Entry {
         std::vector<lora_bf16_t*> A, B;   // prepared [r_slot][h_in] and [width][r_slot], host
+        std::vector<const void*> dA, dB;  // the same buffers' device addresses (device mode)
         uint64_t used = 0;                // last batch (tick) that named it
         int slot = -1;                    // resident slot, or -1
         bool stale = false;               // replaced while resident: reload at the next acquire
@@ -64,6 +68,8 @@ struct lora_slot_manager {
             }
         e.A.clear();
         e.B.clear();
+        e.dA.clear();
+        e.dB.clear();
         if (e.copied) cudaEventDestroy(e.copied);
         e.copied = nullptr;
     }
@@ -75,10 +81,15 @@ struct lora_slot_manager {
             for (int ab = 0; ab < 2; ++ab) {
                 const size_t n = ab == 0 ? a_elems(p) : b_elems(p);
                 lora_bf16_t* b = nullptr;
+                void* db = nullptr;
                 if (device()) {
-                    if (cudaHostAlloc(reinterpret_cast<void**>(&b), n * sizeof(lora_bf16_t), cudaHostAllocDefault) !=
+                    if (cudaHostAlloc(reinterpret_cast<void**>(&b), n * sizeof(lora_bf16_t), cudaHostAllocMapped) !=
                         cudaSuccess)
                         b = nullptr;
+                    else if (cudaHostGetDevicePointer(&db, b, 0) != cudaSuccess) {
+                        cudaFreeHost(b);
+                        b = nullptr;
+                    }
                 } else {
                     b = new (std::nothrow) lora_bf16_t[n];
                 }
@@ -87,6 +98,7 @@ struct lora_slot_manager {
                     return false;
                 }
                 (ab == 0 ? e.A : e.B).push_back(b);
+                (ab == 0 ? e.dA : e.dB).push_back(db);
             }
         }
         if (device() && cudaEventCreateWithFlags(&e.copied, cudaEventDisableTiming) != cudaSuccess) {
@@ -238,22 +250,38 @@ lora_status_t lora_slots_acquire(lora_slot_manager_t* m, const int64_t* adapter_
             m->slot_used[slot] = tick;
             e.slot = slot;
         }
-        if (m->device()) {
+    }
+    if (m->device() && !need.empty()) {
+        // every piece of every adapter to load, gathered by one kernel per
+        // kMaxCopySegs pieces; then one event per adapter
+        std::vector<lora::CopySeg> segs;
+        segs.reserve(need.size() * 2 * m->n_proj);
+        for (int64_t id : need) {
+            const auto& e = m->cache[id];
             for (int p = 0; p < m->n_proj; ++p) {
-                cudaError_t ce = cudaMemcpyAsync(m->A_st[p] + static_cast<size_t>(slot) * m->a_elems(p), e.A[p],
-                                                 m->a_elems(p) * sizeof(lora_bf16_t), cudaMemcpyHostToDevice, s);
-                if (ce == cudaSuccess)
-                    ce = cudaMemcpyAsync(m->B_st[p] + static_cast<size_t>(slot) * m->b_elems(p), e.B[p],
-                                         m->b_elems(p) * sizeof(lora_bf16_t), cudaMemcpyHostToDevice, s);
-                if (ce == cudaSuccess) ce = cudaEventRecord(e.copied, s);
-                if (ce != cudaSuccess) {   // leave the slot empty rather than half loaded
-                    m->slot_owner[slot] = -1;
-                    e.slot = -1;
-                    return LORA_ERR_CUDA;
-                }
+                segs.push_back({e.dA[p], m->A_st[p] + static_cast<size_t>(e.slot) * m->a_elems(p),
+                                m->a_elems(p) * sizeof(lora_bf16_t)});
+                segs.push_back({e.dB[p], m->B_st[p] + static_cast<size_t>(e.slot) * m->b_elems(p),
+                                m->b_elems(p) * sizeof(lora_bf16_t)});
             }
         }
-        e.stale = false;
+        cudaError_t ce = cudaSuccess;
+        for (size_t i = 0; ce == cudaSuccess && i < segs.size(); i += lora::kMaxCopySegs)
+            ce = lora::launch_slot_copy(segs.data() + i,
+                                        static_cast<int>(std::min<size_t>(lora::kMaxCopySegs, segs.size() - i)), s);
+        for (int64_t id : need)
+            if (ce == cudaSuccess) ce = cudaEventRecord(m->cache[id].copied, s);
+        if (ce != cudaSuccess) {   // leave the slots empty rather than half loaded
+            for (int64_t id : need) {
+                auto& e = m->cache[id];
+                if (e.slot >= 0) m->slot_owner[e.slot] = -1;
+                e.slot = -1;
+            }
+            return LORA_ERR_CUDA;
+        }
+    }
+    for (int64_t id : need) {
+        m->cache[id].stale = false;
         ++m->stats.loads;
     }
     for (int i = 0; i < n; ++i)
