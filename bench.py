@@ -133,8 +133,8 @@ ROUTE_KERNELS = {
 # dram__bytes_write.sum over the call's launches), keyed by workload; valid
 # only while the listed kernel sources hash to `src`.  Summaries in profiles/.
 NCU_TRAFFIC = {
-    "llama3b_decode": {"files": ['bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "3a350bbfe24a6d79",
-             "bytes_per_call": 3435680},   # profiles/bgmv_fused_llama3b_decode.md
+    "llama3b_decode": {"files": ['bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "731e6e18209c2843",
+             "bytes_per_call": 3435520},   # profiles/bgmv_fused_llama3b_decode.md
     "stress70b": {"files": ['bgmv_grouped.cu', 'decode_common.cuh', 'common.cuh'], "src": "d9f12af3b4f26b87",
              "bytes_per_call": 987882112},   # profiles/bgmv_grouped_stress70b.md
     "mistral7b_prefill": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "ee03036539001160",

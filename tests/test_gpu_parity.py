@@ -691,3 +691,37 @@ def test_tensor_parallel_kernel_steps_two_layouts(world):
     assert abi.lora_read_device_status(s) == 0
     check_bf16(to_host(y_col), ref, ids_np, y, f"column-parallel over {world}")
     check_bf16(to_host(y_row), ref, ids_np, y, f"row-parallel over {world}")
+
+
+def test_slot_loads_spanning_several_gather_launches_land_exactly():
+    """Twelve adapters of four projections loaded by one acquire: 96 pieces,
+    so the gather takes two launches.  Every slot must then hold exactly the
+    prepared adapter (scale folded, ranks padded), bit for bit, and slots
+    the batch did not load keep their previous contents."""
+    projs = [(128, 96), (64, 40), (256, 128), (72, 24)]   # (h_in, width): uneven sizes, multiples of 8
+    n_slots, r_slot, n_ad = 14, 16, 12
+    A_st = [torch.full((n_slots, r_slot, h), 7.0, dtype=torch.bfloat16, device="cuda") for h, _ in projs]
+    B_st = [torch.full((n_slots, w, r_slot), 7.0, dtype=torch.bfloat16, device="cuda") for _, w in projs]
+    m = abi.SlotManager([h for h, _ in projs], [w for _, w in projs], n_slots, r_slot, max_cpu=n_slots,
+                        A_stores=A_st, B_stores=B_st)
+    g = torch.Generator().manual_seed(31)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16).copy()
+    ranks = [4 + (k % 4) * 4 for k in range(n_ad)]
+    prepared = {}
+    for k, r in enumerate(ranks):
+        A = [bits(torch.randn(r, h, generator=g).to(torch.bfloat16)) for h, _ in projs]
+        B = [bits(torch.randn(w, r, generator=g).to(torch.bfloat16)) for _, w in projs]
+        m.register(k, A, B, r, 2.0 * r, use_rslora=(k % 3 == 0))
+        prepared[k] = [abi.lora_prepare_adapter(A[p], B[p], 2.0 * r, k % 3 == 0, r_slot) for p in range(len(projs))]
+    slots = m.acquire(np.arange(n_ad), stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert len(set(slots.tolist())) == n_ad and m.stats()["loads"] == n_ad
+    for k in range(n_ad):
+        for p in range(len(projs)):
+            np.testing.assert_array_equal(to_host(A_st[p][slots[k]]), prepared[k][p][0], err_msg=f"A adapter {k} proj {p}")
+            np.testing.assert_array_equal(to_host(B_st[p][slots[k]]), prepared[k][p][1], err_msg=f"B adapter {k} proj {p}")
+    untouched = sorted(set(range(n_slots)) - set(slots.tolist()))
+    for p in range(len(projs)):
+        for sl in untouched:
+            assert bool((A_st[p][sl] == 7.0).all()) and bool((B_st[p][sl] == 7.0).all())
+    m.close()
