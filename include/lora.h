@@ -179,18 +179,19 @@ typedef struct {
 
 /* lora_apply flags.
  * Ordering against the kernel enqueued just before the call: lora_apply's
- * decode kernel uses programmatic dependent launch, so it may start while
- * that kernel is still running.  It reads the adapter store and the batch
- * metadata at once (neither may be written by that kernel; copies made with
- * cudaMemcpyAsync are ordered as usual), and touches y and dev_status only
- * after that kernel has completed.  It also never completes before it.
+ * kernels (decode rows first, then prefill rows) use programmatic dependent
+ * launch, so each may start while the kernel before it is still running.
+ * They read the adapter store and the batch metadata at once (neither may
+ * be written by that kernel; copies made with cudaMemcpyAsync are ordered
+ * as usual), and touch y, the workspace and dev_status only after that
+ * kernel has completed.  None completes before the kernel before it.
  *   LORA_APPLY_X_READY: x is not written by the kernel just before the call
  *     (in a model layer x comes from earlier than the base GEMM that writes
- *     y), so the shrink may read x before that kernel completes.
+ *     y), so the shrinks may read x before that kernel completes.
  *   LORA_APPLY_Y_READY: y is neither read nor written by the kernel just
- *     before the call (e.g. the delta goes to a buffer of its own), so y may
- *     be updated before that kernel completes; with X_READY as well, calls
- *     that share no buffers overlap fully.
+ *     before the call (e.g. the delta goes to a buffer of its own), so the
+ *     decode kernel may update y before that kernel completes; with X_READY
+ *     as well, calls that share no buffers overlap fully.
  *   LORA_APPLY_NO_PDL: plain stream ordering, nothing starts early. */
 #define LORA_APPLY_X_READY 0x1u
 #define LORA_APPLY_NO_PDL 0x2u

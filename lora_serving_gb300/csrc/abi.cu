@@ -184,8 +184,8 @@ lora_status_t lora_sgmv_shrink(float* v, int ld_v, const lora_bf16_t* x, int ld_
     ProjSet ps = single_proj(A, nullptr, 0, 0, r_slot);
     if (!row_perm && max_seg_len >= kTcMinSegment && lora::sgmv_tc_supported(1, r_slot, h_in))
         return cuda_status(lora::launch_sgmv_shrink_tc(v, ld_v, nullptr, nullptr, x, ld_x, h_in, ps, seg_starts,
-                                                       seg_slot, n_segs, n_pos, n_rows, n_slots, dev_status,
-                                                       reinterpret_cast<cudaStream_t>(stream)));
+                                                       seg_slot, n_segs, n_pos, n_rows, n_slots, LORA_APPLY_NO_PDL,
+                                                       dev_status, reinterpret_cast<cudaStream_t>(stream)));
     RowMap m = seg_map(seg_starts, seg_slot, n_segs, row_perm, n_pos, n_rows, n_slots);
     return cuda_status(lora::launch_shrink_rowwise(v, ld_v, x, ld_x, h_in, ps, m, dev_status,
                                                    reinterpret_cast<cudaStream_t>(stream)));
@@ -265,21 +265,9 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
         }
     }
 
-    if (P > 0) {
-        if (meta->max_seg_len >= kTcMinSegment && lora::sgmv_tc_supported(n_proj, r_slot, h_in)) {
-            // long segments: tensor-core shrink into the hi/lo planes, then expand
-            LORA_TRY(cuda_status(lora::launch_sgmv_shrink_tc(nullptr, 0, vh, vl, x, ld_x, h_in, ps,
-                                                             meta->seg_starts, meta->seg_slot, meta->n_segs, P,
-                                                             T, n_slots, dev_status, s)));
-            LORA_TRY(cuda_status(lora::launch_sgmv_expand_tc(y, ld_y, vh, vl, ps, meta->seg_starts,
-                                                             meta->seg_slot, meta->n_segs, P, T, n_slots,
-                                                             dev_status, s)));
-        } else {
-            RowMap m = seg_map(meta->seg_starts, meta->seg_slot, meta->n_segs, nullptr, P, T, n_slots);
-            LORA_TRY(cuda_status(lora::launch_shrink_rowwise(v, R, x, ld_x, h_in, ps, m, dev_status, s)));
-            LORA_TRY(cuda_status(lora::launch_expand_rowwise(y, ld_y, v, R, ps, m, dev_status, s)));
-        }
-    }
+    // Decode rows first: their kernel is short and latency-bound, and the
+    // prefill shrink that follows (programmatic dependent launch) can run
+    // beside it -- the two touch disjoint rows of y and of the workspace.
     if (D > 0) {
         const bool gathered = meta->perm && meta->gseg_starts && meta->gseg_slot && meta->n_gsegs > 0;
         const bool fused_ok = gathered && lora::fused_decode_supported(n_proj, r_slot);
@@ -302,6 +290,21 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
             RowMap m = r_slot <= LORA_BGMV_MAX_RANK
                            ? ids_map(meta->lora_ids, P, D, T, n_slots)
                            : seg_map(meta->gseg_starts, meta->gseg_slot, meta->n_gsegs, meta->perm, D, T, n_slots);
+            LORA_TRY(cuda_status(lora::launch_shrink_rowwise(v, R, x, ld_x, h_in, ps, m, dev_status, s)));
+            LORA_TRY(cuda_status(lora::launch_expand_rowwise(y, ld_y, v, R, ps, m, dev_status, s)));
+        }
+    }
+    if (P > 0) {
+        if (meta->max_seg_len >= kTcMinSegment && lora::sgmv_tc_supported(n_proj, r_slot, h_in)) {
+            // long segments: tensor-core shrink into the hi/lo planes, then expand
+            LORA_TRY(cuda_status(lora::launch_sgmv_shrink_tc(nullptr, 0, vh, vl, x, ld_x, h_in, ps,
+                                                             meta->seg_starts, meta->seg_slot, meta->n_segs, P,
+                                                             T, n_slots, flags, dev_status, s)));
+            LORA_TRY(cuda_status(lora::launch_sgmv_expand_tc(y, ld_y, vh, vl, ps, meta->seg_starts,
+                                                             meta->seg_slot, meta->n_segs, P, T, n_slots, flags,
+                                                             dev_status, s)));
+        } else {
+            RowMap m = seg_map(meta->seg_starts, meta->seg_slot, meta->n_segs, nullptr, P, T, n_slots);
             LORA_TRY(cuda_status(lora::launch_shrink_rowwise(v, R, x, ld_x, h_in, ps, m, dev_status, s)));
             LORA_TRY(cuda_status(lora::launch_expand_rowwise(y, ld_y, v, R, ps, m, dev_status, s)));
         }
@@ -359,7 +362,7 @@ lora_status_t lora_linear(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld
         if (tc_shrink)
             LORA_TRY(cuda_status(lora::launch_sgmv_shrink_tc(nullptr, 0, vh, vl, x, ld_x, h_in, ps, meta->seg_starts,
                                                              meta->seg_slot, meta->n_segs, P, T, n_slots,
-                                                             dev_status, s)));
+                                                             LORA_APPLY_NO_PDL, dev_status, s)));
         else
             LORA_TRY(cuda_status(lora::launch_bgmv_grouped_shrink(x, ld_x, h_in, ps, nullptr, meta->seg_starts,
                                                                   meta->seg_slot, meta->n_segs, P,

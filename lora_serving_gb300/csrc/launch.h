@@ -35,12 +35,15 @@ cudaError_t launch_expand_rowwise(bf16_t* y, int ld_y, const float* v, int ld_v,
 // the expand reads the planes.
 bool sgmv_tc_supported(int n_proj, int r_slot, int h_in);
 size_t sgmv_tc_plane_bytes(int n_rows, int n_proj, int r_slot);
+// Both take lora_apply's ordering flags (programmatic dependent launch unless
+// LORA_APPLY_NO_PDL; the shrink reads x before the wait with X_READY).
 cudaError_t launch_sgmv_shrink_tc(float* v, int ld_v, bf16_t* vh, bf16_t* vl, const bf16_t* x, int ld_x, int h_in,
                                   const ProjSet& ps, const int32_t* seg_starts, const int32_t* seg_slot, int n_segs,
-                                  int n_pos, int n_rows, int n_slots, int32_t* status, cudaStream_t stream);
+                                  int n_pos, int n_rows, int n_slots, unsigned flags, int32_t* status,
+                                  cudaStream_t stream);
 cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const bf16_t* vl, const ProjSet& ps,
                                   const int32_t* seg_starts, const int32_t* seg_slot, int n_segs, int n_pos,
-                                  int n_rows, int n_slots, int32_t* status, cudaStream_t stream);
+                                  int n_rows, int n_slots, unsigned flags, int32_t* status, cudaStream_t stream);
 
 // Whether the fused decode kernel handles this projection set.
 bool fused_decode_supported(int n_proj, int r_slot);

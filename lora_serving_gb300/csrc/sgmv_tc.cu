@@ -141,6 +141,7 @@ struct ShrinkTcParams {
     int ld_p;            // plane row length: n_proj * r_pad64
     int r_pad64;         // r_slot rounded up to 64 (plane columns per projection)
     int ks;              // CTAs per row tile (a cluster), each a slice of K
+    int x_ready;         // x is not written by the preceding kernel: read it before the wait
     int32_t* status;
 };
 
@@ -197,13 +198,22 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
     // With ks > 1 a cluster of ks CTAs shares a row tile, CTA c reducing K
     // blocks [c n_kb / ks, (c+1) n_kb / ks); the fp32 partial accumulators
     // meet in distributed shared memory and are summed in a fixed order.
+    //
+    // Under programmatic dependent launch the segment table and A are read
+    // at once, x too when it is ready (LORA_APPLY_X_READY); everything this
+    // grid writes (v, the planes, status) waits for the preceding grid, and
+    // every CTA waits before it leaves, so this grid never completes before
+    // that one.
+    grid_dep_launch();
     const int crank = p.ks > 1 ? static_cast<int>(cluster_rank()) : 0;
     const TileInfo ti = find_tile<kShrinkThreads>(p.seg_starts, p.seg_slot, p.n_segs, p.n_pos, blockIdx.x / p.ks);
     if (!ti.found) {
+        grid_dep_wait();
         if (ti.bad && blockIdx.x == 0 && tid == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
         return;
     }
     if (ti.slot >= p.n_slots || ti.slot < -1) {
+        grid_dep_wait();
         if (tid == 0 && crank == 0) flag(p.status, LORA_DEV_SLOT_OUT_OF_RANGE);
         return;
     }
@@ -232,6 +242,7 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
+    if (!p.x_ready) grid_dep_wait();   // x may be the preceding kernel's output
 
     if (warp == 0 && lane == 0) {
         // producer: X box + one A box per projection per 64-element K block
@@ -274,6 +285,7 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
     // ---- epilogue: TMEM row (lane) -> v ----
     bool ok = mbar_wait(&done, 0);
     tc_fence_after();
+    grid_dep_wait();   // the preceding kernel may still read the buffers written below
     const int r = warp * 32 + lane;   // tile row = TMEM lane
     if (p.ks == 1) {
         const bool row_ok = r < ti.nrows;
@@ -482,12 +494,17 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // ---- this CTA's items and their row tiles ----
+    // Under programmatic dependent launch the segment table is read at once;
+    // v and y are touched only after the preceding grid has completed, and
+    // every CTA waits before it leaves.
+    grid_dep_launch();
     if (tid == 0) s_bad = 0;
     __syncthreads();
     const int n_rt = scan_row_tiles(p, false, 1, 0, s_rt, s_warp, &s_bad);
     const long long n_all = static_cast<long long>(n_rt) * p.n_chunks;
     const int n_items = n_all > blockIdx.x ? static_cast<int>((n_all - 1 - blockIdx.x) / gridDim.x + 1) : 0;
     if (n_items <= 0 || n_items > kMaxItems) {   // the launcher sizes the grid so the second cannot happen
+        grid_dep_wait();
         if (tid == 0 && (n_items > 0 || (blockIdx.x == 0 && s_bad))) flag(p.status, LORA_DEV_BAD_SEGMENT);
         return;
     }
@@ -495,6 +512,7 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
     for (int i = tid; i < n_items; i += kExpandThreadsP)
         if (s_rt[i].slot >= p.n_slots || s_rt[i].slot < -1) atomicOr(&s_bad, 2);
     __syncthreads();
+    grid_dep_wait();
     if (tid == 0 && blockIdx.x == 0 && (s_bad & 1)) flag(p.status, LORA_DEV_BAD_SEGMENT);
     if (s_bad & 2) {   // a slot out of range: flag it, leave this CTA's tiles alone
         if (tid == 0) flag(p.status, LORA_DEV_SLOT_OUT_OF_RANGE);
@@ -731,7 +749,8 @@ bool configure_once(const void* fn, size_t smem, int& configured_device, size_t&
 
 cudaError_t launch_sgmv_shrink_tc(float* v, int ld_v, bf16_t* vh, bf16_t* vl, const bf16_t* x, int ld_x, int h_in,
                                   const ProjSet& ps, const int32_t* seg_starts, const int32_t* seg_slot, int n_segs,
-                                  int n_pos, int n_rows, int n_slots, int32_t* status, cudaStream_t stream)
+                                  int n_pos, int n_rows, int n_slots, unsigned flags, int32_t* status,
+                                  cudaStream_t stream)
 {
     if (n_pos <= 0 || n_segs <= 0) return cudaSuccess;
     const int R = ps.n_proj * ps.r_slot;
@@ -762,6 +781,7 @@ cudaError_t launch_sgmv_shrink_tc(float* v, int ld_v, bf16_t* vh, bf16_t* vl, co
     p.vl = vl;
     p.r_pad64 = (ps.r_slot + kKB - 1) / kKB * kKB;
     p.ld_p = ps.n_proj * p.r_pad64;
+    p.x_ready = (flags & LORA_APPLY_X_READY) ? 1 : 0;
     p.status = status;
     // Few row tiles: split K over a cluster of ks CTAs per tile so that the
     // grid covers the SMs (each CTA keeps at least two K blocks).
@@ -789,13 +809,15 @@ cudaError_t launch_sgmv_shrink_tc(float* v, int ld_v, bf16_t* vh, bf16_t* vl, co
     cfg.blockDim = dim3(kShrinkThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = p.ks;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.ks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (flags & LORA_APPLY_NO_PDL) ? 1 : 2;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, sgmv_shrink_tc_kernel, mx, ma[0], ma[1], ma[2], ma[3], p);
     note_launch();
     return e;
@@ -803,7 +825,7 @@ cudaError_t launch_sgmv_shrink_tc(float* v, int ld_v, bf16_t* vh, bf16_t* vl, co
 
 cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const bf16_t* vl, const ProjSet& ps,
                                   const int32_t* seg_starts, const int32_t* seg_slot, int n_segs, int n_pos,
-                                  int n_rows, int n_slots, int32_t* status, cudaStream_t stream)
+                                  int n_rows, int n_slots, unsigned flags, int32_t* status, cudaStream_t stream)
 {
     if (n_pos <= 0 || n_segs <= 0) return cudaSuccess;
     const int r_pad64 = (ps.r_slot + kKB - 1) / kKB * kKB;
@@ -868,10 +890,19 @@ cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const b
     grid = std::max(grid, (items_bound + kMaxItems - 1) / kMaxItems);   // at most kMaxItems items per CTA
     grid = std::min(grid, items_bound);
     if (grid > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
-    sgmv_expand_tc_kernel<<<static_cast<unsigned>(grid), kExpandThreadsP, smem, stream>>>(mvh, mvl, my, mb[0], mb[1],
-                                                                                          mb[2], mb[3], p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kExpandThreadsP);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = (flags & LORA_APPLY_NO_PDL) ? 0 : 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, sgmv_expand_tc_kernel, mvh, mvl, my, mb[0], mb[1], mb[2], mb[3], p);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace lora

@@ -110,6 +110,11 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, unsigned parity)
     }
 }
 
+// ---- programmatic dependent launch ------------------------------------
+// (no-ops in a grid launched without the attribute)
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
 // ---- TMA ----------------------------------------------------------------
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map)
