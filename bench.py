@@ -137,10 +137,10 @@ NCU_TRAFFIC = {
              "bytes_per_call": 3435520},   # profiles/bgmv_fused_llama3b_decode.md
     "stress70b": {"files": ['bgmv_grouped.cu', 'decode_common.cuh', 'common.cuh'], "src": "d9f12af3b4f26b87",
              "bytes_per_call": 987882112},   # profiles/bgmv_grouped_stress70b.md
-    "mistral7b_prefill": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "ee03036539001160",
-             "bytes_per_call": 2059358976},   # profiles/sgmv_tc_mistral7b_prefill.md
-    "mixed": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "a05b7715974c7861",
-             "bytes_per_call": 113070720},   # profiles/sgmv_tc_mistral7b_prefill.md
+    "mistral7b_prefill": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "e1e55b430f7ab83b",
+             "bytes_per_call": 2060608192},   # profiles/sgmv_tc_mistral7b_prefill.md
+    "mixed": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "e6a0a932989ee2f2",
+             "bytes_per_call": 113061248},   # profiles/sgmv_tc_mistral7b_prefill.md
 }
 
 
