@@ -176,3 +176,17 @@ def test_linear_full_size_sampled_rows():
                         [O.scale(float(wl.alphas[k]), int(wl.ranks[k]), bool(wl.rslora[k])) for k in range(wl.n_slots)])
         ref = O.linear_projection(ids, wl.x["qkv"][rows], W[off:off + w], ref, off, ad)
     check_bf16(got[rows], ref, np.zeros_like(ids), got[rows], "linear full size, sampled rows")
+
+
+@pytest.mark.parametrize("grid", [1, 3])
+@pytest.mark.parametrize("name", ["prefill_qkv", "mixed", "rank64"])
+def test_linear_few_ctas_walk_many_tiles(name, grid, monkeypatch):
+    """A persistent grid of one or three CTAs walks every tile: the stage
+    ring, the accumulator hand-back and the mask warp's request/reply pairs
+    wrap around many times and must stay in step."""
+    monkeypatch.setenv("LORA_LINEAR_GRID", str(grid))
+    st, x, W, ads, ids, meta = _case(**CASES[name], seed=7 + grid)
+    got, status = _run(st, x, W, meta)
+    assert status == 0
+    ref = _oracle(ids, x, W, ads, st)
+    check_bf16(got, ref, np.zeros_like(ids), got, f"linear {name} on {grid} CTAs")

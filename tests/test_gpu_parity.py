@@ -511,6 +511,20 @@ def test_tensor_core_shrink_cluster_split(h_in, widths, rank, lens, slots, ks, m
     check_bf16(got, oracle_group(wl, "g"), wl.ids, wl.y["g"], f"tc ks={ks} h_in={h_in}")
 
 
+@pytest.mark.parametrize("grid,chunk", [(1, 2), (3, 1), (5, 4)])
+def test_tensor_core_expand_few_ctas_walk_many_items(grid, chunk, monkeypatch):
+    """The persistent expand on one, three or five CTAs with short work items:
+    the TMA ring, the v-slice buffers and both accumulators wrap around many
+    times and must stay in step (segments of several row tiles, base rows,
+    widths that leave partial output tiles)."""
+    monkeypatch.setenv("LORA_TC_EXPAND_GRID", str(grid))
+    monkeypatch.setenv("LORA_TC_EXPAND_CHUNK", str(chunk))
+    ids = _segments([300, 5, 129, 260, 64], [1, 2, -1, 3, 0])
+    wl = _small(ids, int(ids.size), rank=32, h_in=256, widths=(384, 72, 72), seed=grid, mode="accumulate")
+    got = _run_apply(wl, "g")
+    check_bf16(got, oracle_group(wl, "g"), wl.ids, wl.y["g"], f"tc expand grid={grid} chunk={chunk}")
+
+
 @pytest.mark.parametrize("ks", [1, 4])
 def test_sgmv_shrink_tensor_core_fp32(ks, monkeypatch):
     """lora_sgmv_shrink on long contiguous segments (tensor-core route) gives
