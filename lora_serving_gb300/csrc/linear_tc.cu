@@ -12,6 +12,11 @@
 //                               + sum_j B'_{p,id_t}[c][j] v_{p,t}[j] )
 // with v = A x from the shrink kernels, stored as bf16 planes v_hi + v_lo.
 //
+// Batches of at most 128 rows with few column tiles split K instead: a
+// cluster of up to 8 CTAs per tile, each streaming a slice of K (rank 0
+// also the LoRA steps); the fp32 partials meet in distributed shared memory
+// and each CTA sums, rounds and stores its share of the tile's columns.
+//
 // Persistent tcgen05 GEMM, one CTA per SM, tiles of 256 rows x 256 output
 // columns of one projection, visited in groups of kGroupM row tiles so that
 // the x and W tiles in flight at once fit in L2.  A tile is two 128-row
@@ -60,6 +65,8 @@ constexpr int kLEpiWarps = 16;                // 4 per tensor-memory lane quarte
 constexpr int kLMaskWarp = 2 + kLEpiWarps;    // zeroes v rows of other adapters in masked LoRA steps
 constexpr int kLThreads = 32 * (3 + kLEpiWarps);
 constexpr int kGroupM = 16;                   // row tiles per raster group
+constexpr int kPartPitch = kLN + 4;           // fp32 pitch of the split-K partial sums (conflict-free float4 rows)
+constexpr int kMaxSplit = 8;                  // split-K cluster size, at most (portable)
 
 struct LinearParams {
     int n_proj, r_slot, r_pad64, n_slots, n_rows;
@@ -68,6 +75,8 @@ struct LinearParams {
     int ntiles[LORA_MAX_PROJ];   // 256-column tiles per projection
     const bf16_t* B[LORA_MAX_PROJ];
     int n_tm, n_tn, n_tiles, n_kb, kbs;
+    int cs;                      // split-K cluster size (1: persistent tiles)
+    int x_box_bytes;             // bytes of one x box (fewer rows when the batch is one short tile)
     const int32_t* ids;
     const bf16_t* vh;
     const bf16_t* vl;
@@ -161,18 +170,23 @@ struct Plan {
     int sl[2][kMaxSlotsHalf];
     int myid[2][4];
     int live[2];   // the half has rows
+    int kb_lo, nb; // base K blocks [kb_lo, kb_lo + nb)
     int n_ks;
-    __device__ __forceinline__ void make(const LinearParams& P, int m)
+    // The tile's plan; with split K (cluster size P.cs) this CTA takes the
+    // K blocks of its cluster rank, and rank 0 alone the LoRA steps.
+    __device__ __forceinline__ void make(const LinearParams& P, int m, int crank)
     {
         live[0] = 1;
         live[1] = m * kLM + kLH < P.n_rows;
         int n_ext = 0;
         for (int h = 0; h < 2; ++h) {
             kind[h] = plan_half(P, m, h, sl[h], nsl[h], myid[h]);
-            if (kind[h] == kUniform || kind[h] == kMasked) n_ext += nsl[h];
+            if ((kind[h] == kUniform || kind[h] == kMasked) && crank == 0) n_ext += nsl[h];
             else nsl[h] = 0;
         }
-        n_ks = P.n_kb + P.kbs * n_ext;
+        kb_lo = crank * P.n_kb / P.cs;
+        nb = (crank + 1) * P.n_kb / P.cs - kb_lo;
+        n_ks = nb + P.kbs * n_ext;
     }
     // LoRA step l (0-based after the base steps) -> half, adapter index, K block
     __device__ __forceinline__ void lora(const LinearParams& P, int l, int& h, int& j, int& kb) const
@@ -254,6 +268,35 @@ __device__ __forceinline__ void add_row_delta(const LinearParams& P, int p, int 
     }
 }
 
+// acc[c] += B'_{p,slot}[col0 + c] . (v_hi + v_lo)[row] for 8 columns col0 .. col0 + 7
+// (all inside the width: widths are multiples of 8).
+__device__ __forceinline__ void add_row_delta8(const LinearParams& P, int p, int slot, int row, int col0, float* acc)
+{
+    const size_t vo = static_cast<size_t>(row) * P.ld_p + p * P.r_pad64;
+    const bf16_t* Bp = P.B[p] + (static_cast<size_t>(slot) * P.width[p] + col0) * P.r_slot;
+    for (int j8 = 0; j8 < P.r_slot; j8 += 8) {
+        const uint4 h = __ldg(reinterpret_cast<const uint4*>(P.vh + vo + j8));
+        const uint4 l = __ldg(reinterpret_cast<const uint4*>(P.vl + vo + j8));
+        const float v[8] = {bf16_lo(h.x) + bf16_lo(l.x), bf16_hi(h.x) + bf16_hi(l.x), bf16_lo(h.y) + bf16_lo(l.y),
+                            bf16_hi(h.y) + bf16_hi(l.y), bf16_lo(h.z) + bf16_lo(l.z), bf16_hi(h.z) + bf16_hi(l.z),
+                            bf16_lo(h.w) + bf16_lo(l.w), bf16_hi(h.w) + bf16_hi(l.w)};
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 b = __ldg(reinterpret_cast<const uint4*>(Bp + static_cast<size_t>(c) * P.r_slot + j8));
+            float s = acc[c];
+            s = fmaf(bf16_lo(b.x), v[0], s);
+            s = fmaf(bf16_hi(b.x), v[1], s);
+            s = fmaf(bf16_lo(b.y), v[2], s);
+            s = fmaf(bf16_hi(b.y), v[3], s);
+            s = fmaf(bf16_lo(b.z), v[4], s);
+            s = fmaf(bf16_hi(b.z), v[5], s);
+            s = fmaf(bf16_lo(b.w), v[6], s);
+            s = fmaf(bf16_hi(b.w), v[7], s);
+            acc[c] = s;
+        }
+    }
+}
+
 // Rounds 32 accumulator columns to bf16 and stores those inside the width.
 __device__ __forceinline__ void store_row32(bf16_t* yrow, int ncols_left, const float* acc)
 {
@@ -267,6 +310,44 @@ __device__ __forceinline__ void store_row32(bf16_t* yrow, int ncols_left, const 
             o.w = pack_bf16x2(acc[c8 * 8 + 6], acc[c8 * 8 + 7]);
             *reinterpret_cast<uint4*>(yrow + c8 * 8) = o;
         }
+    }
+}
+
+// Split K, after the cluster barrier: the 8-column groups of this CTA's
+// share of the tile summed over the cluster's partials (rank order), the
+// per-row deltas of a half that mixes many adapters added, rounded, stored.
+// Whole CTA (the plan's warp votes).
+__device__ __noinline__ void splitk_reduce(const LinearParams& P, int t, int crank, float* part)
+{
+    const int tid = threadIdx.x;
+    const LTile T = tile_of(P, t);
+    Plan pl;
+    pl.make(P, T.m, 0);
+    const int n_g = (T.ncols + 7) / 8;   // 8-column groups of the tile
+    const int g_lo = crank * n_g / P.cs, g_hi = (crank + 1) * n_g / P.cs;
+    const int per_row = g_hi - g_lo;
+    const uint32_t part_s = smem_u32(part);
+    for (int it = tid; it < P.n_rows * per_row; it += kLThreads) {
+        const int row = it / per_row, c0 = (g_lo + it - row * per_row) * 8;
+        float acc[8] = {};
+        for (int peer = 0; peer < P.cs; ++peer) {
+            const uint32_t src = map_rank(part_s + 4u * static_cast<uint32_t>(row * kPartPitch + c0), peer);
+            const float4 a = ld_dsmem_f4(src), b = ld_dsmem_f4(src + 16u);
+            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+        }
+        const int id = __ldg(P.ids + row);
+        if (id >= 0 && id < P.n_slots) {
+            if (pl.kind[0] == kRows) add_row_delta8(P, T.p, id, row, T.col0 + c0, acc);
+        } else if (id != -1 && c0 == 0) {
+            flag(P.status, LORA_DEV_SLOT_OUT_OF_RANGE);   // the row keeps its base value
+        }
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        *reinterpret_cast<uint4*>(P.y + static_cast<size_t>(row) * P.ld_y + P.out_off[T.p] + T.col0 + c0) = o;
     }
 }
 
@@ -302,17 +383,22 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
+    // persistent: tiles blockIdx.x, + gridDim.x, ...; split K: the cluster's one tile
+    const int crank = P.cs > 1 ? static_cast<int>(cluster_rank()) : 0;
+    const int t_first = P.cs > 1 ? static_cast<int>(blockIdx.x) / P.cs : static_cast<int>(blockIdx.x);
+    const int t_step = P.cs > 1 ? P.n_tiles : static_cast<int>(gridDim.x);
+    float* part = reinterpret_cast<float*>(ring);   // split K: this CTA's partial sums, after its K loop
 
     if (warp == 0) {   // ---- producer (lane 0 issues; the warp plans each tile) ----
         int it = 0;
-        for (int t = blockIdx.x; t < P.n_tiles && !s_fail; t += gridDim.x) {
+        for (int t = t_first; t < P.n_tiles && !s_fail; t += t_step) {
             const LTile T = tile_of(P, t);
             Plan pl;
-            pl.make(P, T.m);
+            pl.make(P, T.m, crank);
             if (lane == 0) {
                 // the LoRA boxes come after the whole base K loop: start them
                 // towards L2 now so that those steps do not wait on DRAM
-                for (int l = 0; l < pl.n_ks - P.n_kb; ++l) {
+                for (int l = 0; l < pl.n_ks - pl.nb; ++l) {
                     int h, j, kb;
                     pl.lora(P, l, h, j, kb);
                     tma_prefetch_3d(&mvh, kb * kLK, T.p, T.m * kLM + h * kLH);
@@ -327,13 +413,14 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
                     }
                     uint8_t* a = ring + s * kStageBytes;
                     uint8_t* b = a + kABytes;
-                    if (k < P.n_kb) {
-                        mbar_expect_tx(&full[s], kStageBytes);
-                        tma_load_2d(a, &mx, k * kLK, T.m * kLM, &full[s]);
-                        tma_load_2d(b, &mw, k * kLK, P.out_off[T.p] + T.col0, &full[s]);
+                    if (k < pl.nb) {
+                        const int kc = (pl.kb_lo + k) * kLK;
+                        mbar_expect_tx(&full[s], P.x_box_bytes + kBBytes);
+                        tma_load_2d(a, &mx, kc, T.m * kLM, &full[s]);
+                        tma_load_2d(b, &mw, kc, P.out_off[T.p] + T.col0, &full[s]);
                     } else {
                         int h, j, kb;
-                        pl.lora(P, k - P.n_kb, h, j, kb);
+                        pl.lora(P, k - pl.nb, h, j, kb);
                         mbar_expect_tx(&full[s], kStageBytes);
                         tma_load_3d(a, &mvh, kb * kLK, T.p, T.m * kLM + h * kLH, &full[s]);
                         tma_load_3d(a + kHalfBytes, &mvl, kb * kLK, T.p, T.m * kLM + h * kLH, &full[s]);
@@ -347,10 +434,10 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
     } else if (warp == 1) {   // ---- MMA issuer ----
         int it = 0, ti = 0, ok = 1;
         int mc[kLStages] = {};   // masked steps seen per stage (the phase of masked[s])
-        for (int t = blockIdx.x; ok && t < P.n_tiles && !s_fail; t += gridDim.x, ++ti) {
+        for (int t = t_first; ok && t < P.n_tiles && !s_fail; t += t_step, ++ti) {
             const LTile T = tile_of(P, t);
             Plan pl;
-            pl.make(P, T.m);
+            pl.make(P, T.m, crank);
             if (lane == 0) {
                 const uint32_t idesc = idesc_bf16_f32(kLH, (T.ncols + 15) / 16 * 16);
                 const bool live1 = pl.live[1];
@@ -363,7 +450,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
                         break;
                     }
                     const uint32_t as = smem_u32(ring + s * kStageBytes), bs = as + kABytes;
-                    if (k < P.n_kb) {
+                    if (k < pl.nb) {
                         tc_fence_after();
 #pragma unroll
                         for (int ks = 0; ks < kLK / 16; ++ks)
@@ -376,7 +463,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
                         }
                     } else {
                         int h, j, kb;
-                        pl.lora(P, k - P.n_kb, h, j, kb);
+                        pl.lora(P, k - pl.nb, h, j, kb);
                         if (pl.kind[h] == kMasked) {
                             // the mask warp zeroes the other adapters' rows of this v box first;
                             // requests and replies alternate, so each stage's phases pair up
@@ -405,14 +492,14 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
     } else if (warp == kLMaskWarp) {   // ---- v masking for halves that mix adapters ----
         int it = 0, ok = 1;
         int mr[kLStages] = {};   // requests served per stage (the phase of mask_req[s])
-        for (int t = blockIdx.x; ok && t < P.n_tiles && !s_fail; t += gridDim.x) {
+        for (int t = t_first; ok && t < P.n_tiles && !s_fail; t += t_step) {
             const LTile T = tile_of(P, t);
             Plan pl;
-            pl.make(P, T.m);
-            for (int k = P.n_kb; ok && k < pl.n_ks; ++k) {
+            pl.make(P, T.m, crank);
+            for (int k = pl.nb; ok && k < pl.n_ks; ++k) {
                 const int step = it + k, s = step % kLStages;
                 int h, j, kb;
-                pl.lora(P, k - P.n_kb, h, j, kb);
+                pl.lora(P, k - pl.nb, h, j, kb);
                 if (pl.kind[h] != kMasked) continue;
                 // the request comes after the stage has landed and before it can be
                 // refilled, so the stage's fill phase is exactly this step's
@@ -445,16 +532,31 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
         const int quarter = warp & 3;        // tensor-memory lanes this warp may read
         const int cs = (e >> 2) * 64;        // its 64 columns of the tile
         int ti = 0;
-        for (int t = blockIdx.x; t < P.n_tiles; t += gridDim.x, ++ti) {
+        for (int t = t_first; t < P.n_tiles; t += t_step, ++ti) {
             const LTile T = tile_of(P, t);
             Plan pl;
-            pl.make(P, T.m);
+            pl.make(P, T.m, crank);
             if (s_fail || !mbar_wait(&acc_full, ti & 1)) {
                 s_fail = 1;
                 break;
             }
             tc_fence_after();
             const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + cs;
+            if (P.cs > 1) {
+                // split K (at most 128 rows: half 0): the partial sums go to
+                // shared memory, where the cluster adds them up below
+                float* prow = part + (quarter * 32 + lane) * kPartPitch + cs;
+#pragma unroll 1
+                for (int q = 0; q < 2; ++q) {
+                    float d[32];
+                    tmem_ld32(tbase + q * 32, d);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        *reinterpret_cast<float4*>(prow + q * 32 + 4 * i) =
+                            make_float4(d[4 * i], d[4 * i + 1], d[4 * i + 2], d[4 * i + 3]);
+                }
+                continue;
+            }
             if (pl.kind[0] != kRows && pl.kind[1] != kRows) {
                 // no per-row delta: read the warp's four 32-column pieces,
                 // round them into registers, hand the accumulator back to the
@@ -520,6 +622,16 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
         }
     }
     __syncthreads();
+    if (P.cs > 1) {
+        // ---- split K: sum the cluster's partials, add per-row deltas, round, store ----
+        // Every thread of every CTA of the cluster meets both barriers (a CTA
+        // that timed out still takes part; its status flag tells the caller).
+        cluster_arrive();
+        cluster_wait();
+        splitk_reduce(P, t_first, crank, part);
+        cluster_arrive();   // the peers have read this CTA's partials
+        cluster_wait();
+    }
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, 2 * kLN);
     if (tid == 0 && s_fail) flag(P.status, LORA_DEV_TIMEOUT);
@@ -550,8 +662,13 @@ cudaError_t launch_linear_tc(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int
     P.status = status;
     P.n_kb = (h_in + kLK - 1) / kLK;
     P.n_tm = (n_rows + kLM - 1) / kLM;
+    // A batch of one row tile loads only its rows of x (rounded up to 8):
+    // the other rows of the A operand are left over from earlier steps and
+    // only feed accumulator rows that are never stored.
+    const int x_rows = P.n_tm == 1 ? std::min(kLM, (n_rows + 7) / 8 * 8) : kLM;
+    P.x_box_bytes = x_rows * 128;
     CUtensorMap mx, mw, mvh, mvl, mb[4];
-    if (!encode_tmap_bf16(&mx, x, n_rows, h_in, ld_x, kLM, kLK, true) ||
+    if (!encode_tmap_bf16(&mx, x, n_rows, h_in, ld_x, x_rows, kLK, true) ||
         !encode_tmap_bf16(&mw, W, n_out, h_in, ld_w, kLN, kLK, true) ||
         !encode_tmap_bf16_3d(&mvh, vh, ps.r_slot, ps.n_proj, n_rows, P.r_pad64, P.ld_p, kLK, kLH) ||
         !encode_tmap_bf16_3d(&mvl, vl, ps.r_slot, ps.n_proj, n_rows, P.r_pad64, P.ld_p, kLK, kLH))
@@ -585,11 +702,42 @@ cudaError_t launch_linear_tc(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    const int grid = static_cast<int>(std::min<long long>(env_int("LORA_LINEAR_GRID", n_sms), n_tiles));
-    linear_tc_kernel<<<grid, kLThreads, linear_tc_smem(), stream>>>(mx, mw, mvh, mvl, mb[0], mb[1], mb[2], mb[3],
-                                                                    P);
+    // Few rows (one half of one row tile) and few column tiles: split K over
+    // a cluster per tile so that the weight streams through most SMs.
+    // The largest cluster for which every tile's cluster is resident at once
+    // (clusters must fit inside a GPC, so fewer than n_sms / cs may be).
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kLThreads);
+    cfg.dynamicSmemBytes = linear_tc_smem();
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    int cs = 1;
+    if (P.n_tm == 1 && n_rows <= kLH && 2 * P.n_tiles <= n_sms) {
+        for (int c = std::min(kMaxSplit, P.n_kb); c >= 2 && cs == 1; --c) {
+            attr.val.clusterDim.x = c;
+            cfg.gridDim = dim3(static_cast<unsigned>(P.n_tiles * c));
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            int active = 0;
+            if (cudaOccupancyMaxActiveClusters(&active, linear_tc_kernel, &cfg) == cudaSuccess && active >= P.n_tiles)
+                cs = c;
+        }
+        (void)cudaGetLastError();
+    }
+    cs = std::max(1, std::min({env_int("LORA_LINEAR_SPLIT", cs), kMaxSplit, P.n_kb}));
+    if (n_rows > kLH || P.n_tm != 1) cs = 1;
+    P.cs = cs;
+    cfg.gridDim = dim3(static_cast<unsigned>(cs > 1 ? P.n_tiles * cs
+                                                    : std::min<long long>(env_int("LORA_LINEAR_GRID", n_sms), n_tiles)));
+    attr.val.clusterDim.x = cs;
+    cfg.attrs = &attr;
+    cfg.numAttrs = cs > 1 ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, linear_tc_kernel, mx, mw, mvh, mvl, mb[0], mb[1], mb[2], mb[3], P);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace lora

@@ -190,3 +190,43 @@ def test_linear_few_ctas_walk_many_tiles(name, grid, monkeypatch):
     assert status == 0
     ref = _oracle(ids, x, W, ads, st)
     check_bf16(got, ref, np.zeros_like(ids), got, f"linear {name} on {grid} CTAs")
+
+
+SPLIT_CASES = {
+    # decode rows over five adapters: the reduction adds each row's delta
+    "decode": CASES["decode"],
+    # every row on one adapter: rank 0's K extension
+    "uniform": dict(h_in=512, widths=(256, 128), ranks=(16, 8), r_slot=16, ids=np.full(40, 1), n_prefill=0),
+    # three adapters and base rows in the half: masked extensions on rank 0
+    "masked": dict(h_in=384, widths=(128, 384), ranks=(16, 16, 8), r_slot=16,
+                   ids=np.array([(i * 3) % 4 - 1 for i in range(77)]), n_prefill=0),
+    # 128 rows exactly, a width that leaves a partial column tile
+    "full_half": dict(h_in=256, widths=(392,), ranks=(32, 24), r_slot=32,
+                      ids=np.array([i % 2 for i in range(128)]), n_prefill=0),
+}
+
+
+@pytest.mark.parametrize("split", [1, 2, 5, 8])
+@pytest.mark.parametrize("name", list(SPLIT_CASES))
+def test_linear_split_k_small_batches(name, split, monkeypatch):
+    """Batches of at most 128 rows with K split over a cluster of 2-8 CTAs
+    (partials summed through distributed shared memory) and without."""
+    monkeypatch.setenv("LORA_LINEAR_SPLIT", str(split))
+    st, x, W, ads, ids, meta = _case(**SPLIT_CASES[name], seed=40 + split)
+    got, status = _run(st, x, W, meta)
+    assert status == 0
+    ref = _oracle(ids, x, W, ads, st)
+    check_bf16(got, ref, np.zeros_like(ids), got, f"linear split {split} {name}")
+
+
+def test_linear_split_k_bad_row_id_flagged():
+    c = dict(SPLIT_CASES["decode"])
+    st, x, W, ads, ids, meta = _case(**c, seed=9)
+    bad = 21
+    assert ids[bad] >= 0
+    meta.ids[bad] = len(c["ranks"]) + 1
+    got, status = _run(st, x, W, meta)
+    assert status & abi.LORA_DEV_SLOT_OUT_OF_RANGE
+    ids_ref = ids.copy()
+    ids_ref[bad] = -1
+    check_bf16(got, _oracle(ids_ref, x, W, ads, st), np.zeros_like(ids), got, "split K with a bad id")
