@@ -67,6 +67,7 @@ constexpr int kLThreads = 32 * (3 + kLEpiWarps);
 constexpr int kGroupM = 16;                   // row tiles per raster group
 constexpr int kPartPitch = kLN + 4;           // fp32 pitch of the split-K partial sums (conflict-free float4 rows)
 constexpr int kMaxSplit = 8;                  // split-K cluster size, at most (portable)
+constexpr int kSplitCacheTiles = 160;         // tile counts whose split-K choice is remembered
 
 struct LinearParams {
     int n_proj, r_slot, r_pad64, n_slots, n_rows;
@@ -714,18 +715,35 @@ cudaError_t launch_linear_tc(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.y = 1;
     attr.val.clusterDim.z = 1;
+    // (the answer depends only on the tile count and the K blocks: kept per
+    // device in a small table, so repeated calls skip the occupancy queries)
+    static int split_dev = -1;
+    static signed char split_cache[kSplitCacheTiles][kMaxSplit + 1];
+    if (split_dev != dev) {
+        for (auto& row : split_cache)
+            for (auto& c : row) c = -1;
+        split_dev = dev;
+    }
     int cs = 1;
     if (P.n_tm == 1 && n_rows <= kLH && 2 * P.n_tiles <= n_sms) {
-        for (int c = std::min(kMaxSplit, P.n_kb); c >= 2 && cs == 1; --c) {
-            attr.val.clusterDim.x = c;
-            cfg.gridDim = dim3(static_cast<unsigned>(P.n_tiles * c));
-            cfg.attrs = &attr;
-            cfg.numAttrs = 1;
-            int active = 0;
-            if (cudaOccupancyMaxActiveClusters(&active, linear_tc_kernel, &cfg) == cudaSuccess && active >= P.n_tiles)
-                cs = c;
+        const int c_max = std::min(kMaxSplit, P.n_kb);
+        signed char* cached = P.n_tiles < kSplitCacheTiles ? &split_cache[P.n_tiles][c_max] : nullptr;
+        if (cached && *cached >= 0) {
+            cs = *cached;
+        } else {
+            for (int c = c_max; c >= 2 && cs == 1; --c) {
+                attr.val.clusterDim.x = c;
+                cfg.gridDim = dim3(static_cast<unsigned>(P.n_tiles * c));
+                cfg.attrs = &attr;
+                cfg.numAttrs = 1;
+                int active = 0;
+                if (cudaOccupancyMaxActiveClusters(&active, linear_tc_kernel, &cfg) == cudaSuccess &&
+                    active >= P.n_tiles)
+                    cs = c;
+            }
+            (void)cudaGetLastError();
+            if (cached) *cached = static_cast<signed char>(cs);
         }
-        (void)cudaGetLastError();
     }
     cs = std::max(1, std::min({env_int("LORA_LINEAR_SPLIT", cs), kMaxSplit, P.n_kb}));
     if (n_rows > kLH || P.n_tm != 1) cs = 1;
