@@ -316,11 +316,11 @@ def run_merge(args, rank, local, ws):
     elems = sum(W.numel() for W, _, _ in weights)
     bytes_step = 2 * sum(merge_bytes(W.shape[0], W.shape[1], r) for W, _, _ in weights)
 
+    Ws, As, Bs = [w for w, _, _ in weights], [a for _, a, _ in weights], [b for _, _, b in weights]
+
     def step():
-        for W, A, B in weights:
-            abi.lora_merge(W, A, B, 1)
-        for W, A, B in weights:
-            abi.lora_merge(W, A, B, -1)
+        abi.lora_merge_batch(Ws, As, Bs, 1)
+        abi.lora_merge_batch(Ws, As, Bs, -1)
 
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
@@ -363,9 +363,9 @@ def run_merge(args, rank, local, ws):
                    "weights": {n: [o, h] for n, o, h in MERGE_SHAPES}, "elements": elems,
                    "l2": f"{bytes_step / 2 / 1e9:.2f} GB of weights per pass (L2 "
                          f"{torch.cuda.get_device_properties(dev).L2_cache_size / 1e6:.0f} MB)",
-                   "timing": "CUDA graph of merge then unmerge of every weight; CUDA events",
+                   "timing": "CUDA graph of one batched merge then one batched unmerge of every weight; CUDA events",
                    "parallelism": f"replicas x{ws}"},
-        "roofline": {"kernel": "merge_kernel", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+        "roofline": {"kernel": "merge_batch_kernel", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
                      "per": "step", "bytes_per_step": bytes_step, "traffic": None},
         "clocks": clk,

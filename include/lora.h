@@ -300,6 +300,19 @@ lora_status_t lora_linear(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld
 lora_status_t lora_merge(lora_bf16_t* W, int ld_w, int out, int h_in, const lora_bf16_t* A,
                          const lora_bf16_t* B, int r_slot, int sign, lora_stream_t stream);
 
+/*
+ * lora_merge over n weights in one launch (per 32 weights): W[i], ld_w[i],
+ * out[i], h_in[i], A[i], B[i] as in lora_merge, all with the same r_slot
+ * and sign (e.g. one adapter folded into every projection of a model).
+ * The arrays are host memory; the pointers in them are device memory.
+ * Same result, bit for bit, as n calls of lora_merge.  Errors (before
+ * anything is enqueued): as lora_merge for any weight, LORA_ERR_INVALID_ARG
+ * for n < 0 or a NULL array.
+ */
+lora_status_t lora_merge_batch(int n, lora_bf16_t* const* W, const int* ld_w, const int* out, const int* h_in,
+                               const lora_bf16_t* const* A, const lora_bf16_t* const* B, int r_slot, int sign,
+                               lora_stream_t stream);
+
 /* ------------------------------------------------------------------ *
  *  Adapter slots: GPU slots fed from a host cache of prepared adapters
  * ------------------------------------------------------------------ */

@@ -37,7 +37,7 @@ EXPORTS = (
     "lora_bgmv_shrink", "lora_bgmv_expand", "lora_sgmv_shrink", "lora_sgmv_expand",
     "lora_apply", "lora_apply_workspace_bytes", "lora_build_metadata",
     "lora_prepare_adapter", "lora_slot_rank", "lora_read_device_status", "lora_status_string",
-    "lora_kernel_launch_count", "lora_apply_noalloc", "lora_merge", "lora_linear",
+    "lora_kernel_launch_count", "lora_apply_noalloc", "lora_merge", "lora_merge_batch", "lora_linear",
     "lora_slots_create", "lora_slots_destroy", "lora_slots_register", "lora_slots_acquire",
     "lora_slots_slot_of", "lora_slots_stats",
 )
@@ -91,6 +91,7 @@ def load(path: str | None = None):
         "lora_read_device_status": [P, P, P],
         "lora_status_string": [i32],
         "lora_merge": [P, i32, i32, i32, P, P, i32, i32, P],
+        "lora_merge_batch": [i32, P, P, P, P, P, P, i32, i32, P],
         "lora_linear": [P, i32, P, i32, i32, P, i32, P, i32, i32, i32, P, P, sz, P, P],
         "lora_slots_create": [i32, P, P, P, P, i32, i32, i32, P],
         "lora_slots_register": [P, ctypes.c_int64, P, P, i32, ctypes.c_double, i32],
@@ -220,6 +221,23 @@ def lora_merge(W, A, B, sign, *, stream=None):
     r_slot = int(A.shape[0])
     _check("lora_merge", load().lora_merge(_p(W), _ld(W), out, h_in, _p(A), _p(B), r_slot, int(sign),
                                            _stream(stream)))
+
+
+def lora_merge_batch(Ws, As, Bs, sign, *, stream=None):
+    """lora_merge over every (W, A, B) of the lists in one launch (per 32);
+    all A share the slot rank (their row count)."""
+    n = len(Ws)
+    P = ctypes.c_void_p
+    arr_w, arr_a, arr_b = (P * max(1, n))(), (P * max(1, n))(), (P * max(1, n))()
+    ld = (ctypes.c_int * max(1, n))()
+    out = (ctypes.c_int * max(1, n))()
+    h_in = (ctypes.c_int * max(1, n))()
+    for i, (W, A, B) in enumerate(zip(Ws, As, Bs)):
+        arr_w[i], arr_a[i], arr_b[i] = _p(W), _p(A), _p(B)
+        ld[i], out[i], h_in[i] = _ld(W), int(W.shape[0]), int(W.shape[1])
+    r_slot = int(As[0].shape[0]) if n else 8
+    _check("lora_merge_batch", load().lora_merge_batch(n, arr_w, ld, out, h_in, arr_a, arr_b, r_slot, int(sign),
+                                                       _stream(stream)))
 
 
 class lora_slot_stats_t(ctypes.Structure):

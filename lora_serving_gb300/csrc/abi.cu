@@ -392,6 +392,26 @@ lora_status_t lora_merge(lora_bf16_t* W, int ld_w, int out, int h_in, const lora
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+lora_status_t lora_merge_batch(int n, lora_bf16_t* const* W, const int* ld_w, const int* out, const int* h_in,
+                               const lora_bf16_t* const* A, const lora_bf16_t* const* B, int r_slot, int sign,
+                               lora_stream_t stream)
+{
+    if (n < 0 || (n > 0 && (!W || !ld_w || !out || !h_in || !A || !B))) return LORA_ERR_INVALID_ARG;
+    if (r_slot <= 0 || (sign != 1 && sign != -1)) return LORA_ERR_INVALID_ARG;
+    if (r_slot > LORA_MAX_RANK) return LORA_ERR_RANK_EXCEEDS_SLOT;
+    if (r_slot % 8 != 0) return LORA_ERR_ALIGNMENT;
+    for (int i = 0; i < n; ++i) {
+        if (!W[i] || out[i] <= 0 || h_in[i] <= 0) return LORA_ERR_INVALID_ARG;
+        if (ld_w[i] < h_in[i] || out[i] > (1 << 22)) return LORA_ERR_SHAPE;
+        if (!aligned16(W[i]) || ld_w[i] % 8 != 0 || h_in[i] % 8 != 0) return LORA_ERR_ALIGNMENT;
+        LORA_TRY(check_store(A[i]));
+        LORA_TRY(check_store(B[i]));
+    }
+    if (n == 0) return LORA_OK;
+    return cuda_status(lora::launch_merge_batch(n, W, ld_w, out, h_in, A, B, r_slot, sign,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
 uint64_t lora_kernel_launch_count(void) { return lora::g_launches.load(std::memory_order_relaxed); }
 
 lora_status_t lora_read_device_status(const int32_t* dev_status, int32_t* out, lora_stream_t stream)

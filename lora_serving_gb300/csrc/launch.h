@@ -84,5 +84,9 @@ cudaError_t launch_linear_tc(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int
 // W += sign * B A over one adapter slot (merge / unmerge), one rounding.
 cudaError_t launch_merge(bf16_t* W, int ld_w, int out, int h_in, const bf16_t* A, const bf16_t* B, int r_slot,
                          int sign, cudaStream_t stream);
+// The same over n weights (host arrays of device pointers), one launch per 32.
+cudaError_t launch_merge_batch(int n, bf16_t* const* W, const int* ld_w, const int* out, const int* h_in,
+                               const bf16_t* const* A, const bf16_t* const* B, int r_slot, int sign,
+                               cudaStream_t stream);
 
 }  // namespace lora

@@ -15,6 +15,8 @@
 // leaves by coalesced 16-byte stores.  HBM-bound: W is read and written
 // once, A and B' come from L2 after their first use.
 
+#include <algorithm>
+
 #include "decode_common.cuh"
 #include "launch.h"
 
@@ -28,6 +30,7 @@ constexpr int kMRows = 64;                 // W rows per CTA
 constexpr int kMCols = 128;                // W columns per CTA
 constexpr int kMThreads = 128;             // 4 warps, 16 rows each
 constexpr int kMPitch = kMCols + 8;        // bf16 pitch of the W and A tiles (conflict-free ldmatrix)
+constexpr int kMaxMergeWeights = 32;       // weights per batch launch
 
 __device__ __forceinline__ void ldmatrix_x2_trans(uint32_t addr, uint32_t& r0, uint32_t& r1)
 {
@@ -35,45 +38,55 @@ __device__ __forceinline__ void ldmatrix_x2_trans(uint32_t addr, uint32_t& r0, u
                  : "=r"(r0), "=r"(r1) : "r"(addr));
 }
 
-struct MergeParams {
+// One weight to merge: W [out][ld_w], its adapter slot's A [r_slot][h_in]
+// and B' [out][r_slot].
+struct MergeWeight {
     bf16_t* W;
+    const bf16_t* A;
+    const bf16_t* B;
     int ld_w, out, h_in;
-    const bf16_t* A;   // [r_slot][h_in]
-    const bf16_t* B;   // [out][r_slot]
-    int r_slot, r_pad; // r_pad: r_slot rounded up to 16 (the mma K)
+    int col_tiles;       // ceil(h_in / 128)
+    long long first;     // first tile of this weight in the batch's tile order
+};
+
+struct MergeParams {
+    MergeWeight w[kMaxMergeWeights];
+    int n;               // weights
+    long long n_tiles;   // all weights' tiles
+    int r_slot, r_pad;   // r_pad: r_slot rounded up to 16 (the mma K)
     float sign;
 };
 
-__global__ void __launch_bounds__(kMThreads)
-merge_kernel(MergeParams p)
+// W[o0 .. o0+63][k0 .. k0+127] += sign * B'A, one rounding.  Whole CTA;
+// the caller synchronises before smem is reused.
+__device__ __forceinline__ void merge_tile(const MergeWeight& m, const MergeParams& p, int o0, int k0,
+                                           unsigned char* smem)
 {
-    extern __shared__ __align__(128) unsigned char smem[];
     const int bp_pitch = p.r_pad + 8;
     bf16_t* sW = reinterpret_cast<bf16_t*>(smem);                       // [64][kMPitch]
     bf16_t* sB = sW + kMRows * kMPitch;                                 // [64][r_pad + 8]
     bf16_t* sA = sB + kMRows * bp_pitch;                                // [r_pad][kMPitch]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int o0 = blockIdx.y * kMRows, k0 = blockIdx.x * kMCols;
 
     // ---- stage the W tile, B' rows and A columns (zero outside the matrices) ----
     for (int i = tid; i < kMRows * (kMCols / 8); i += kMThreads) {
         const int r = i / (kMCols / 8), c = (i % (kMCols / 8)) * 8;
-        const bool ok = o0 + r < p.out && k0 + c < p.h_in;
+        const bool ok = o0 + r < m.out && k0 + c < m.h_in;
         cp_async16(smem_u32(sW + r * kMPitch + c),
-                   ok ? static_cast<const void*>(p.W + static_cast<size_t>(o0 + r) * p.ld_w + k0 + c) : p.W, ok);
+                   ok ? static_cast<const void*>(m.W + static_cast<size_t>(o0 + r) * m.ld_w + k0 + c) : m.W, ok);
     }
     const int bch = p.r_pad / 8;
     for (int i = tid; i < kMRows * bch; i += kMThreads) {
         const int r = i / bch, c = (i % bch) * 8;
-        const bool ok = o0 + r < p.out && c < p.r_slot;
+        const bool ok = o0 + r < m.out && c < p.r_slot;
         cp_async16(smem_u32(sB + r * bp_pitch + c),
-                   ok ? static_cast<const void*>(p.B + static_cast<size_t>(o0 + r) * p.r_slot + c) : p.B, ok);
+                   ok ? static_cast<const void*>(m.B + static_cast<size_t>(o0 + r) * p.r_slot + c) : m.B, ok);
     }
     for (int i = tid; i < p.r_pad * (kMCols / 8); i += kMThreads) {
         const int j = i / (kMCols / 8), c = (i % (kMCols / 8)) * 8;
-        const bool ok = j < p.r_slot && k0 + c < p.h_in;
+        const bool ok = j < p.r_slot && k0 + c < m.h_in;
         cp_async16(smem_u32(sA + j * kMPitch + c),
-                   ok ? static_cast<const void*>(p.A + static_cast<size_t>(j) * p.h_in + k0 + c) : p.A, ok);
+                   ok ? static_cast<const void*>(m.A + static_cast<size_t>(j) * m.h_in + k0 + c) : m.A, ok);
     }
     cp_async_commit();
     cp_async_wait<0>();
@@ -107,9 +120,36 @@ merge_kernel(MergeParams p)
     __syncthreads();
     for (int i = tid; i < kMRows * (kMCols / 8); i += kMThreads) {
         const int r = i / (kMCols / 8), c = (i % (kMCols / 8)) * 8;
-        if (o0 + r < p.out && k0 + c < p.h_in)
-            *reinterpret_cast<uint4*>(p.W + static_cast<size_t>(o0 + r) * p.ld_w + k0 + c) =
+        if (o0 + r < m.out && k0 + c < m.h_in)
+            *reinterpret_cast<uint4*>(m.W + static_cast<size_t>(o0 + r) * m.ld_w + k0 + c) =
                 *reinterpret_cast<const uint4*>(sW + r * kMPitch + c);
+    }
+}
+
+// One weight: one CTA per tile (blockIdx.x = column block, blockIdx.y = row block).
+__global__ void __launch_bounds__(kMThreads)
+merge_kernel(const __grid_constant__ MergeParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    merge_tile(p.w[0], p, blockIdx.y * kMRows, blockIdx.x * kMCols, smem);
+}
+
+// Several weights in one launch: the CTAs walk the weights' tiles in order
+// (tile c, c + gridDim.x, ...), so no weight leaves a partial last wave and
+// there is one launch for all.  Within a weight, column block fastest: the
+// CTAs in flight together share B' rows and read neighbouring A columns.
+__global__ void __launch_bounds__(kMThreads)
+merge_batch_kernel(const __grid_constant__ MergeParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    int q = 0;
+    for (long long t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
+        while (q + 1 < p.n && t >= p.w[q + 1].first) ++q;
+        const MergeWeight& m = p.w[q];
+        const long long local = t - m.first;
+        const int rb = static_cast<int>(local / m.col_tiles), cb = static_cast<int>(local - static_cast<long long>(rb) * m.col_tiles);
+        merge_tile(m, p, rb * kMRows, cb * kMCols, smem);
+        __syncthreads();   // the next tile reuses the staging buffers
     }
 }
 
@@ -121,34 +161,81 @@ size_t merge_smem(int r_pad)
 
 }  // namespace
 
-cudaError_t launch_merge(bf16_t* W, int ld_w, int out, int h_in, const bf16_t* A, const bf16_t* B, int r_slot,
-                         int sign, cudaStream_t stream)
+namespace {
+
+cudaError_t configure_merge(int& n_sms)
 {
-    MergeParams p{};
-    p.W = W;
-    p.ld_w = ld_w;
-    p.out = out;
-    p.h_in = h_in;
-    p.A = A;
-    p.B = B;
-    p.r_slot = r_slot;
-    p.r_pad = (r_slot + 15) / 16 * 16;
-    p.sign = sign > 0 ? 1.f : -1.f;
-    const size_t smem = merge_smem(p.r_pad);
-    static int configured_device = -1;
+    static int configured_device = -1, sms = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(merge_smem((LORA_MAX_RANK + 15) / 16 * 16)));
+        const int max_smem = static_cast<int>(merge_smem((LORA_MAX_RANK + 15) / 16 * 16));
+        e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(merge_batch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
+    n_sms = sms;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_merge(bf16_t* W, int ld_w, int out, int h_in, const bf16_t* A, const bf16_t* B, int r_slot,
+                         int sign, cudaStream_t stream)
+{
+    MergeParams p{};
+    p.n = 1;
+    p.w[0] = MergeWeight{W, A, B, ld_w, out, h_in, (h_in + kMCols - 1) / kMCols, 0};
+    p.r_slot = r_slot;
+    p.r_pad = (r_slot + 15) / 16 * 16;
+    p.sign = sign > 0 ? 1.f : -1.f;
+    int n_sms = 0;
+    const cudaError_t e = configure_merge(n_sms);
+    if (e != cudaSuccess) return e;
     const dim3 grid((h_in + kMCols - 1) / kMCols, (out + kMRows - 1) / kMRows);
-    merge_kernel<<<grid, kMThreads, smem, stream>>>(p);
+    merge_kernel<<<grid, kMThreads, merge_smem(p.r_pad), stream>>>(p);
     note_launch();
     return cudaGetLastError();
+}
+
+cudaError_t launch_merge_batch(int n, bf16_t* const* W, const int* ld_w, const int* out, const int* h_in,
+                               const bf16_t* const* A, const bf16_t* const* B, int r_slot, int sign,
+                               cudaStream_t stream)
+{
+    int n_sms = 0;
+    cudaError_t e = configure_merge(n_sms);
+    if (e != cudaSuccess) return e;
+    const size_t smem = merge_smem((r_slot + 15) / 16 * 16);
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, merge_batch_kernel, kMThreads, smem);
+    if (e != cudaSuccess) return e;
+    for (int i0 = 0; i0 < n; i0 += kMaxMergeWeights) {
+        MergeParams p{};
+        p.n = std::min(kMaxMergeWeights, n - i0);
+        p.r_slot = r_slot;
+        p.r_pad = (r_slot + 15) / 16 * 16;
+        p.sign = sign > 0 ? 1.f : -1.f;
+        long long tiles = 0;
+        for (int q = 0; q < p.n; ++q) {
+            const int i = i0 + q;
+            const int ct = (h_in[i] + kMCols - 1) / kMCols;
+            p.w[q] = MergeWeight{W[i], A[i], B[i], ld_w[i], out[i], h_in[i], ct, tiles};
+            tiles += static_cast<long long>(ct) * ((out[i] + kMRows - 1) / kMRows);
+        }
+        p.n_tiles = tiles;
+        const long long grid = std::min<long long>(tiles, static_cast<long long>(std::max(1, per_sm)) * n_sms);
+        if (grid <= 0) continue;
+        merge_batch_kernel<<<static_cast<unsigned>(grid), kMThreads, smem, stream>>>(p);
+        note_launch();
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace lora

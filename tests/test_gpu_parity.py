@@ -605,6 +605,52 @@ def test_merge_unmerge_round_trip_exact():
     np.testing.assert_array_equal(to_host(Wd), Wb)
 
 
+@pytest.mark.parametrize("n", [5, 37])
+def test_merge_batch_equals_single_merges_and_oracle(n):
+    """n weights of assorted shapes (37: two launches) folded in one call:
+    bit for bit what n single lora_merge calls give, and within the single
+    kernel's bound of the oracle; a repeat with sign -1 takes them back
+    out the same way."""
+    rng = np.random.default_rng(n)
+    shapes = [(int(rng.integers(1, 40)) * 8, int(rng.integers(1, 50)) * 8) for _ in range(n)]
+    r, r_slot = 12, 16
+    cases = [_merge_case(o, h, r, r_slot, seed=100 + i) for i, (o, h) in enumerate(shapes)]
+    Wb_dev = [c[0].cuda() for c in cases]
+    Ws_dev = [c[0].cuda() for c in cases]
+    As = [c[1].cuda() for c in cases]
+    Bs = [c[2].cuda() for c in cases]
+    for sign in (1, -1):
+        abi.lora_merge_batch(Wb_dev, As, Bs, sign)
+        for W, A, B in zip(Ws_dev, As, Bs):
+            abi.lora_merge(W, A, B, sign)
+        torch.cuda.synchronize()
+        for i in range(n):
+            np.testing.assert_array_equal(to_host(Wb_dev[i]), to_host(Ws_dev[i]), err_msg=f"weight {i} sign {sign}")
+    # the first merge against the oracle
+    Wd = [c[0].cuda() for c in cases]
+    abi.lora_merge_batch(Wd, As, Bs, 1)
+    torch.cuda.synchronize()
+    for i, (W, A, Bp, Wb, Ab, Bb) in enumerate(cases):
+        ref = O.bf16_to_f64(O.merge(Wb, Ab, Bb, 1))
+        got = O.bf16_to_f64(to_host(Wd[i]))
+        E = (r + 1) * 2.0 ** -24 * (np.abs(O.bf16_to_f64(Bb)) @ np.abs(O.bf16_to_f64(Ab)) + np.abs(O.bf16_to_f64(Wb)))
+        assert np.all(np.abs(got - ref) <= 2.0 ** -7 * (np.abs(ref) + E) + E), i
+
+
+def test_merge_batch_rejects_before_enqueue():
+    W, A, Bp, *_ = _merge_case(64, 128, 8, 16, seed=1)
+    Wd, Ad, Bd = W.cuda(), A.cuda(), Bp.cuda()
+    keep = to_host(Wd).copy()
+    with pytest.raises(abi.LoraError) as e:
+        abi.lora_merge_batch([Wd, Wd[:, 1:]], [Ad, Ad[:, 1:]], [Bd, Bd], 1)   # second weight misaligned
+    assert e.value.name in ("LORA_ERR_ALIGNMENT", "LORA_ERR_SHAPE")
+    with pytest.raises(abi.LoraError) as e:
+        abi.lora_merge_batch([Wd], [Ad], [Bd], 2)
+    assert e.value.name == "LORA_ERR_INVALID_ARG"
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_host(Wd), keep)   # nothing ran
+
+
 def test_merge_rejects_bad_arguments_before_enqueue():
     W = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
     A = torch.zeros(16, 64, dtype=torch.bfloat16, device="cuda")
