@@ -130,8 +130,9 @@ ROUTE_KERNELS = {
 }
 
 # DRAM traffic per lora_apply call from an ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum over the call's launches), keyed by workload; valid
-# only while the listed kernel sources hash to `src`.  Summaries in profiles/.
+# dram__bytes_write.sum over the call's launches), keyed by workload; per
+# step for the merge and linear-layer workloads; valid only while the listed
+# kernel sources hash to `src`.  Summaries in profiles/.
 NCU_TRAFFIC = {
     "llama3b_decode": {"files": ['bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "731e6e18209c2843",
              "bytes_per_call": 3435520},   # profiles/bgmv_fused_llama3b_decode.md
@@ -139,9 +140,24 @@ NCU_TRAFFIC = {
              "bytes_per_call": 987882112},   # profiles/bgmv_grouped_stress70b.md
     "mistral7b_prefill": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "e1e55b430f7ab83b",
              "bytes_per_call": 2060608192},   # profiles/sgmv_tc_mistral7b_prefill.md
+    "merge_mistral7b": {"files": ['merge.cu', 'decode_common.cuh', 'common.cuh'], "src": "23de5092951a476a",
+             "bytes_per_step": 6953849856},   # profiles/merge_mistral7b.md
+    "linear_mistral7b_prefill": {"files": ['linear_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "f9a71240bbae42de",
+             "bytes_per_step": 19274225664},   # profiles/linear_tc_mistral7b_prefill.md (linear_tc_kernel only)
     "mixed": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "e6a0a932989ee2f2",
              "bytes_per_call": 113061248},   # profiles/sgmv_tc_mistral7b_prefill.md
 }
+
+
+def recorded_traffic(name, layers=None):
+    """Recorded DRAM bytes per step of a merge or linear-layer workload, or
+    None once its kernel sources have changed (or for another layer count)."""
+    tr = NCU_TRAFFIC.get(name)
+    if not tr or tr.get("src") != src_digest(tr["files"]):
+        return None
+    if layers is not None and layers != MERGE_LAYERS:
+        return None
+    return tr["bytes_per_step"]
 
 
 def peaks():
@@ -367,7 +383,7 @@ def run_merge(args, rank, local, ws):
                    "parallelism": f"replicas x{ws}"},
         "roofline": {"kernel": "merge_batch_kernel", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
-                     "per": "step", "bytes_per_step": bytes_step, "traffic": None},
+                     "per": "step", "bytes_per_step": bytes_step, "traffic": recorded_traffic(MERGE_WORKLOAD, layers)},
         "clocks": clk,
         "gpu_launches": int(launches_per_step * args.steps),
         "e2e": None,
@@ -558,7 +574,8 @@ def run_linear(args, rank, local, ws):
                      "achieved": round(achieved, 1), "peak": sustained, "unit": "TFLOP/s",
                      "frac": round(achieved / sustained, 4), "frac_of_burst": round(achieved / burst, 4),
                      "peak_source": f"{kind} bf16_tflops_sustained (burst {burst})", "per": "step",
-                     "flops_per_step": flops_step, "traffic": None},
+                     "flops_per_step": flops_step,
+                     "traffic": recorded_traffic(LINEAR_WORKLOAD) if not args.seqs else None},
         "clocks": clk,
         "gpu_launches": int(launches_per_step * args.steps),
     }
