@@ -12,11 +12,6 @@
 //                               + sum_j B'_{p,id_t}[c][j] v_{p,t}[j] )
 // with v = A x from the shrink kernels, stored as bf16 planes v_hi + v_lo.
 //
-// Batches of at most 128 rows with few column tiles split K instead: a
-// cluster of up to 8 CTAs per tile, each streaming a slice of K (rank 0
-// also the LoRA steps); the fp32 partials meet in distributed shared memory
-// and each CTA sums, rounds and stores its share of the tile's columns.
-//
 // Persistent tcgen05 GEMM, one CTA per SM, tiles of 256 rows x 256 output
 // columns of one projection, visited in groups of kGroupM row tiles so that
 // the x and W tiles in flight at once fit in L2.  A tile is two 128-row
@@ -39,6 +34,13 @@
 // start once the epilogue has read the previous tile out (a few percent of
 // a tile's K loop).  Every wait is bounded (0.2 s); a timeout sets
 // LORA_DEV_TIMEOUT and the CTA winds down, freeing its tensor memory.
+//
+// Batches of at most 128 rows with few column tiles split K instead: a
+// cluster of up to 8 CTAs per tile (the largest size whose clusters are all
+// resident at once), each streaming a slice of K (rank 0 also the LoRA
+// steps); the fp32 partials meet in distributed shared memory and each CTA
+// sums, adds per-row deltas, rounds and stores its share of the tile's
+// columns.  Such a batch loads only its own rows of x.
 
 #include <algorithm>
 
