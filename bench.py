@@ -142,7 +142,7 @@ NCU_TRAFFIC = {
              "bytes_per_call": 2060608192},   # profiles/sgmv_tc_mistral7b_prefill.md
     "merge_mistral7b": {"files": ['merge.cu', 'decode_common.cuh', 'common.cuh'], "src": "23de5092951a476a",
              "bytes_per_step": 6953849856},   # profiles/merge_mistral7b.md
-    "linear_mistral7b_prefill": {"files": ['linear_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "f9a71240bbae42de",
+    "linear_mistral7b_prefill": {"files": ['linear_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "f52cc27e446ec6c9",
              "bytes_per_step": 19274225664},   # profiles/linear_tc_mistral7b_prefill.md (linear_tc_kernel only)
     "mixed": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "e6a0a932989ee2f2",
              "bytes_per_call": 113061248},   # profiles/sgmv_tc_mistral7b_prefill.md
