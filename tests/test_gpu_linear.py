@@ -95,6 +95,13 @@ CASES = {
                          ids=np.array([i % 4 for i in range(100)]), n_prefill=0),
     "five_in_half": dict(h_in=256, widths=(256,), ranks=(16, 8, 16, 12, 4), r_slot=16,
                          ids=np.array([i % 5 for i in range(100)]), n_prefill=0),
+    # four projections (the most one call takes), widths leaving partial column tiles
+    "four_proj": dict(h_in=320, widths=(200, 72, 72, 264), ranks=(16, 8, 12), r_slot=16,
+                      ids=np.concatenate([_segments([150, 131], [2, 0]), np.array([1, -1, 2, 0, 1])]),
+                      n_prefill=281),
+    # one row past a 256-row tile: a last tile with a single live row
+    "rows_257": dict(h_in=256, widths=(256,), ranks=(16, 16), r_slot=16,
+                     ids=_segments([257], [1]), n_prefill=257),
     "all_base": dict(h_in=192, widths=(256,), ranks=(16, 16), r_slot=16,
                      ids=np.concatenate([_segments([140], [-1]), np.full(9, -1)]), n_prefill=140),
 }
