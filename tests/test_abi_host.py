@@ -186,3 +186,48 @@ def test_kernel_entry_points_validate_before_launch():
     # bf16 hi/lo planes (rank padded to 64, region rounded to 256 B) + fp32 v
     planes = (2 * 10 * 3 * 64 * 2 + 255) // 256 * 256
     assert lib.lora_apply_workspace_bytes(10, 3, 16) == planes + 10 * 3 * 16 * 4
+
+
+def test_linear_and_merge_batch_validate_before_launch():
+    """lora_linear and lora_merge_batch reject host-detectable errors before
+    any CUDA call, so these run without a GPU."""
+    lib = abi.load()
+    buf = (ctypes.c_uint8 * 8192)()
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    meta = abi.lora_meta_t()
+    meta.lora_ids, meta.n_rows, meta.n_prefill = base, 4, 4
+    meta.seg_starts, meta.seg_slot, meta.n_segs = base, base, 1
+    tiles = abi.make_projs([(base, base, 0, 64), (base, base, 64, 64)])
+    gap = abi.make_projs([(base, base, 0, 64), (base, base, 72, 56)])   # column 64..71 uncovered
+    P = ctypes.addressof
+    # projections that do not tile [0, n_out)
+    assert lib.lora_linear(base, 128, base, 64, 64, base, 64, P(gap), 2, 16, 2, P(meta), base, 1 << 20, 0, 0) == 2
+    # ld_w below h_in
+    assert lib.lora_linear(base, 128, base, 64, 64, base, 32, P(tiles), 2, 16, 2, P(meta), base, 1 << 20, 0, 0) == 2
+    # misaligned W
+    assert lib.lora_linear(base, 128, base, 64, 64, base + 2, 64, P(tiles), 2, 16, 2, P(meta), base, 1 << 20,
+                           0, 0) == 5
+    # slot rank above 64 with decode rows
+    meta.n_prefill = 2
+    assert lib.lora_linear(base, 128, base, 64, 64, base, 64, P(tiles), 2, 128, 2, P(meta), base, 1 << 20,
+                           0, 0) == 3
+    meta.n_prefill = 4
+    # no workspace
+    assert lib.lora_linear(base, 128, base, 64, 64, base, 64, P(tiles), 2, 16, 2, P(meta), 0, 0, 0, 0) == 7
+    # NULL W
+    assert lib.lora_linear(base, 128, base, 64, 64, 0, 64, P(tiles), 2, 16, 2, P(meta), base, 1 << 20, 0, 0) == 1
+
+    Ws = (ctypes.c_void_p * 2)(base, base + 2)
+    As = (ctypes.c_void_p * 2)(base, base)
+    Bs = (ctypes.c_void_p * 2)(base, base)
+    ld = (ctypes.c_int * 2)(64, 64)
+    out = (ctypes.c_int * 2)(32, 32)
+    h_in = (ctypes.c_int * 2)(64, 64)
+    # the second weight misaligned
+    assert lib.lora_merge_batch(2, Ws, ld, out, h_in, As, Bs, 16, 1, 0) == 5
+    # bad sign, NULL arrays, slot rank above the maximum
+    assert lib.lora_merge_batch(1, Ws, ld, out, h_in, As, Bs, 16, 0, 0) == 1
+    assert lib.lora_merge_batch(1, None, ld, out, h_in, As, Bs, 16, 1, 0) == 1
+    assert lib.lora_merge_batch(1, Ws, ld, out, h_in, As, Bs, 136, 1, 0) == 3
+    # nothing to do
+    assert lib.lora_merge_batch(0, None, None, None, None, None, None, 16, 1, 0) == 0
