@@ -472,6 +472,85 @@ def cpu_oracle_linear_rate(budget_s: float):
                                                  f"groups of one layer", "seconds": round(dt, 3)}
 
 
+def linear_e2e(args, wl, groups, store, dev):
+    """The linear layer through the public call with host buffers: per step
+    one host->device copy of every group's x (staged in one pinned buffer)
+    and of the ids, the four lora_linear calls, and one device->host copy of
+    every y; each step a CUDA graph, steps alternating over two streams with
+    their own buffers, workspaces and metadata."""
+    import torch
+    names = [g.name for g in wl.groups]
+    sizes_x = {n: wl.x[n].size for n in names}
+    sizes_y = {g.name: wl.n_rows * g.ld_y for g in wl.groups}
+    n_x, n_y = sum(sizes_x.values()), sum(sizes_y.values())
+    h_x = torch.empty(n_x, dtype=torch.bfloat16).pin_memory()
+    flat = h_x.view(torch.int16).numpy()
+    off = 0
+    for n in names:
+        flat[off:off + sizes_x[n]] = wl.x[n].reshape(-1).view(np.int16)
+        off += sizes_x[n]
+    h_ids = torch.from_numpy(wl.ids.copy()).pin_memory()
+    lanes = []
+    for _ in range(2):
+        dx = torch.empty(n_x, dtype=torch.bfloat16, device=dev)
+        dy = torch.empty(n_y, dtype=torch.bfloat16, device=dev)
+        xv, yv, ox, oy = {}, {}, 0, 0
+        for g in wl.groups:
+            xv[g.name] = dx[ox:ox + sizes_x[g.name]].view(wl.n_rows, g.h_in)
+            yv[g.name] = dy[oy:oy + sizes_y[g.name]].view(wl.n_rows, g.ld_y)
+            ox += sizes_x[g.name]
+            oy += sizes_y[g.name]
+        lanes.append({"stream": torch.cuda.Stream(device=dev), "dx": dx, "dy": dy, "x": xv, "y": yv,
+                      "out": torch.empty(n_y, dtype=torch.bfloat16).pin_memory(),
+                      "meta": store.BatchMeta(wl.ids, wl.n_prefill, wl.n_slots, device=dev),
+                      "ws": {g.name: store.workspace_for(wl.n_rows, len(g.projs), wl.r_slot, device=dev)
+                             for g in wl.groups}})
+
+    def step(ln):
+        ln["meta"].ids.copy_(h_ids, non_blocking=True)
+        ln["dx"].copy_(h_x, non_blocking=True)
+        for g in wl.groups:
+            store.linear(ln["y"][g.name], ln["x"][g.name], groups[g.name]["W"], groups[g.name]["st"], ln["meta"],
+                         ln["ws"][g.name])
+        ln["out"].copy_(ln["dy"], non_blocking=True)
+
+    graphs = []
+    for ln in lanes:
+        with torch.cuda.stream(ln["stream"]):
+            step(ln)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=ln["stream"]):
+            step(ln)
+        graphs.append(gr)
+    torch.cuda.synchronize()
+
+    def run(count):
+        for i in range(count):
+            with torch.cuda.stream(lanes[i % 2]["stream"]):
+                graphs[i % 2].replay()
+
+    n = max(4, min(args.steps, 10))
+    run(2)
+    torch.cuda.synchronize()
+    main = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(main)
+    for ln in lanes:
+        ln["stream"].wait_event(e0)
+    run(n)
+    for ln in lanes:
+        main.wait_stream(ln["stream"])
+    e1.record(main)
+    torch.cuda.synchronize()
+    ems = e0.elapsed_time(e1)
+    return {"value": round(wl.n_rows * n / (ems / 1e3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(n_x * 2 + h_ids.numel() * 4), "d2h_bytes_per_step": int(n_y * 2),
+            "steps": n, "ms_per_step": round(ems / n, 4), "copies_per_step": 3, "streams": 2,
+            "timing": "each step's copies and calls as a CUDA graph; steps alternate over two streams"}
+
+
 def run_linear(args, rank, local, ws):
     import torch
     from lora_serving_gb300 import abi, build, store, synth
@@ -580,35 +659,7 @@ def run_linear(args, rank, local, ws):
         "gpu_launches": int(launches_per_step * args.steps),
     }
     if not args.no_e2e:
-        hx = {g.name: torch.from_numpy(wl.x[g.name].view(np.int16)).view(torch.bfloat16).pin_memory()
-              for g in wl.groups}
-        hy = {g.name: torch.empty(wl.n_rows, g.ld_y, dtype=torch.bfloat16).pin_memory() for g in wl.groups}
-        h_ids = torch.from_numpy(wl.ids.copy()).pin_memory()
-
-        def e2e_step():
-            meta.ids.copy_(h_ids, non_blocking=True)
-            for g in wl.groups:
-                d = groups[g.name]
-                d["x"].copy_(hx[g.name], non_blocking=True)
-                store.linear(d["y"], d["x"], d["W"], d["st"], meta, d["ws"])
-                hy[g.name].copy_(d["y"], non_blocking=True)
-
-        n = max(3, min(args.steps, 10))
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(n):
-            e2e_step()
-        e1.record()
-        torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1)
-        out["e2e"] = {"value": round(wl.n_rows * n / (ems / 1e3), 1), "unit": "tokens/s",
-                      "h2d_bytes_per_step": int(sum(t.numel() * 2 for t in hx.values()) + h_ids.numel() * 4),
-                      "d2h_bytes_per_step": int(sum(t.numel() * 2 for t in hy.values())), "steps": n,
-                      "ms_per_step": round(ems / n, 4)}
+        out["e2e"] = linear_e2e(args, wl, groups, store, dev)
     if args.seqs:
         out["config"]["seqs"] = args.seqs
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
