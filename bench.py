@@ -1037,6 +1037,37 @@ def run_reference(args, rank, ws):
     name = args.workload
     layers = args.layers or LAYERS.get(name, 1)
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
+    if name == SLOTS_WORKLOAD:
+        # the slot manager moves bytes, it computes nothing: the host-side
+        # counterpart is the same adapter loads done by memory copies
+        rng = np.random.default_rng(3)
+        adapter_elems = [SLOTS_RANK * h for h, _ in SLOTS_PROJS] + [w * SLOTS_RANK for _, w in SLOTS_PROJS]
+        pool = [[rng.integers(0, 1 << 16, n, dtype=np.uint16) for n in adapter_elems] for _ in range(SLOTS_POOL)]
+        slots = [[np.empty(n, np.uint16) for n in adapter_elems] for _ in range(SLOTS_N)]
+        vals = []
+        t0 = time.perf_counter()
+        batch = 0
+        for _ in range(args.steps):
+            loads = 0
+            ts = time.perf_counter()
+            while time.perf_counter() - ts < per_step:
+                for k in range(SLOTS_N):
+                    for dst, src in zip(slots[k], pool[(batch * SLOTS_N + k) % SLOTS_POOL]):
+                        np.copyto(dst, src)
+                    loads += 1
+                batch += 1
+            vals.append(loads / (time.perf_counter() - ts))
+        value = statistics.median(vals)
+        return {
+            "impl": "reference", "metric": "adapter loads into GPU slots per second",
+            "value": round(value, 1), "unit": "loads/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic", "config": {"workload": name, "slots": SLOTS_N, "rank": SLOTS_RANK},
+            "cpu_baseline": {"value": round(value, 1), "unit": "loads/s", "cores": 1, "kind": "host memory copies",
+                             "sample": f"batches of {SLOTS_N} adapter loads for {per_step:.1f} s per step"},
+            "e2e": {"value": round(value, 1), "unit": "loads/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "seconds": round(time.perf_counter() - t0, 2),
+        }
     if name == LINEAR_WORKLOAD:
         vals, info = [], None
         t0 = time.perf_counter()
