@@ -115,11 +115,14 @@ __host__ __device__ inline SmemLayout smem_layout(int R, int r_slot, int nch_til
     return L;
 }
 
-// kThreads = 256 (2 CTAs per SM) for small calls, whose time is the chain
-// of dependent latencies of each CTA; 128 (4 per SM) for calls whose grid
-// exceeds the resident slots, which more CTAs in flight serve better.
+// kThreads = 256 for small calls, whose time is the chain of dependent
+// latencies of each CTA; 128 for calls whose grid exceeds the resident
+// slots, which more CTAs in flight serve better.  Registers are held to 64
+// per thread (1024 threads per SM): in a chain of calls the next call's
+// CTAs then find room beside the running ones (shared memory permitting:
+// four CTAs of a 48 KB o-projection call), without spilling.
 template <int kThreads>
-__global__ void __launch_bounds__(kThreads, 512 / kThreads)
+__global__ void __launch_bounds__(kThreads, 1024 / kThreads)
 bgmv_fused_kernel(FusedParams p)
 {
     constexpr int kWarps = kThreads / 32;
