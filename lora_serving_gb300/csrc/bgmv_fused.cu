@@ -96,16 +96,18 @@ struct SmemLayout {
 
 __host__ __device__ inline size_t align128(size_t v) { return (v + 127) / 128 * 128; }
 
-// sA (the K stages) and sD (the delta tile, fp32) share the first region:
-// sD is written only after every stage has been consumed.
+// sD (the delta tile, fp32) overlays the K stages of A and x: it is written
+// only after every stage has been consumed.  Keeping the overlay tight lets
+// three CTAs of a 3B-shaped q/k/v call (80 chunks, rank 16) share an SM.
 __host__ __device__ inline SmemLayout smem_layout(int R, int r_slot, int nch_tile, int n_pos)
 {
     SmemLayout L;
-    const size_t sa = sizeof(bf16_t) * kStages * R * kLds;
-    const size_t sd = sizeof(float) * kRB * nch_tile * 8;
+    const size_t sa = align128(sizeof(bf16_t) * kStages * R * kLds);
+    const size_t sx = align128(sizeof(bf16_t) * kStages * kRB * kLds);
+    const size_t sd = align128(sizeof(float) * kRB * nch_tile * 8);
     L.a = 0;
-    L.x = align128(sa > sd ? sa : sd);
-    L.vpart = L.x + align128(sizeof(bf16_t) * kStages * kRB * kLds);
+    L.x = sa;
+    L.vpart = sa + sx > sd ? sa + sx : sd;
     L.vfull = L.vpart + align128(sizeof(float) * kRB * R);
     L.b = L.vfull + align128(sizeof(float) * kRB * R);
     // the B' tile, and after the delta is formed, the y pieces being updated
