@@ -21,6 +21,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import signal
 import statistics
 import subprocess
@@ -220,9 +221,11 @@ class ClockSampler:
 
 # ------------------------------------------------------ CPU oracle ----
 
-def cpu_oracle_rate(wl_name: str, budget_s: float, layers: int):
+def cpu_oracle_rate(wl_name: str, budget_s: float, layers: int, single_core: bool = True):
     """Times the fp64 oracle (as it stands) on layer calls of the workload,
-    rows split across all host cores; returns (tokens/s per layer call, info)."""
+    rows split across all host cores; returns (tokens/s per layer call, info).
+    With `single_core`, info also holds the rate of the same oracle on one
+    core (timed over a quarter of the budget) and the host CPU's model."""
     import concurrent.futures as cf
     import oracle as O
     from lora_serving_gb300 import synth
@@ -268,7 +271,37 @@ def cpu_oracle_rate(wl_name: str, budget_s: float, layers: int):
             sample = f"{sub.size} sampled rows of {T} (all groups of one layer), scaled per row"
     dt = time.perf_counter() - t0
     rate = done_rows / dt
-    return rate, {"cores": cores, "sample": sample, "seconds": round(dt, 3)}
+    if not single_core:
+        return rate, {"cores": cores, "sample": sample, "seconds": round(dt, 3)}
+    # the same oracle on one core, over a quarter of the budget (at most 64 rows per pass)
+    one = (np.arange(T) if T <= 4096 else sub)[:64]
+    n1, t1 = 0, time.perf_counter()
+    while True:
+        n1 += run_block(one)
+        if time.perf_counter() - t1 >= budget_s / 4:
+            break
+    rate1 = n1 / (time.perf_counter() - t1)
+    return rate, {"cores": cores, "sample": sample, "seconds": round(dt, 3),
+                  "single_core_value": round(rate1, 2), "cpu_model": host_cpu_model()}
+
+
+def host_cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
 
 
 # ------------------------------------------------- merge / unmerge ----
@@ -932,7 +965,8 @@ def run_ours(args, rank, local, ws):
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         rate, info = cpu_oracle_rate(name, args.cpu_seconds, layers)
         out["cpu_baseline"] = {"value": round(rate, 2), "unit": "tokens/s", "cores": info["cores"],
-                               "kind": "oracle", "sample": info["sample"]}
+                               "kind": "oracle", "sample": info["sample"],
+                               "single_core_value": info["single_core_value"], "cpu_model": info["cpu_model"]}
     return out
 
 
@@ -1106,9 +1140,9 @@ def run_reference(args, rank, ws):
     vals = []
     info = None
     t0 = time.perf_counter()
-    cpu_oracle_rate(name, 0.0, layers)  # warm-up: builds the oracle, one layer call
+    cpu_oracle_rate(name, 0.0, layers, single_core=False)  # warm-up: builds the oracle, one layer call
     for _ in range(args.steps):
-        rate, info = cpu_oracle_rate(name, per_step, layers)
+        rate, info = cpu_oracle_rate(name, per_step, layers, single_core=False)
         vals.append(rate)
     total = time.perf_counter() - t0
     value = statistics.median(vals)
@@ -1123,7 +1157,7 @@ def run_reference(args, rank, ws):
         "config": {"workload": name, "tokens": base.n_rows, "layers": layers, "n_slots": base.n_slots,
                    "r_slot": base.r_slot},
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": info["cores"], "kind": "oracle",
-                         "sample": info["sample"]},
+                         "sample": info["sample"], "cpu_model": host_cpu_model()},
         "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "seconds": round(total, 2),
     }

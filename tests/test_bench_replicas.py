@@ -58,3 +58,13 @@ def test_single_process_needs_no_process_group():
     assert bench.max_over_ranks(3.0, 1) == 3.0
     assert bench.sum_over_ranks(7.0, 1) == 7.0
     bench.barrier(1)
+
+
+def test_cpu_baseline_reports_single_core_rate_and_cpu_model():
+    """The oracle's host timing names the CPU and gives the one-core rate beside the all-cores one."""
+    rate, info = bench.cpu_oracle_rate("tiny", 0.2, 1)
+    assert rate > 0 and info["cores"] >= 1
+    assert info["single_core_value"] > 0
+    assert isinstance(info["cpu_model"], str) and info["cpu_model"]
+    _, info2 = bench.cpu_oracle_rate("tiny", 0.0, 1, single_core=False)
+    assert "single_core_value" not in info2
