@@ -134,21 +134,47 @@ merge_kernel(const __grid_constant__ MergeParams p)
     merge_tile(p.w[0], p, blockIdx.y * kMRows, blockIdx.x * kMCols, smem);
 }
 
+// Tile t of the batch: its weight (q advances monotonically) and its corner.
+__device__ __forceinline__ void locate_tile(const MergeParams& p, long long t, int& q, int& o0, int& k0)
+{
+    while (q + 1 < p.n && t >= p.w[q + 1].first) ++q;
+    const MergeWeight& m = p.w[q];
+    const long long local = t - m.first;
+    const int rb = static_cast<int>(local / m.col_tiles);
+    o0 = rb * kMRows;
+    k0 = static_cast<int>(local - static_cast<long long>(rb) * m.col_tiles) * kMCols;
+}
+
+// One 128-byte line of a W tile per thread (64 rows x 2 lines) into L2.
+__device__ __forceinline__ void prefetch_tile_l2(const MergeWeight& m, int o0, int k0)
+{
+    const int r = threadIdx.x >> 1, c = k0 + (threadIdx.x & 1) * 64;
+    if (o0 + r < m.out && c < m.h_in)
+        asm volatile("prefetch.global.L2 [%0];\n" ::"l"(m.W + static_cast<size_t>(o0 + r) * m.ld_w + c));
+}
+
 // Several weights in one launch: the CTAs walk the weights' tiles in order
 // (tile c, c + gridDim.x, ...), so no weight leaves a partial last wave and
 // there is one launch for all.  Within a weight, column block fastest: the
 // CTAs in flight together share B' rows and read neighbouring A columns.
+// Each CTA requests its next tile's W into L2 before it works on the current
+// one, so the HBM reads of the next tile overlap this tile's compute and
+// stores instead of following them.
 __global__ void __launch_bounds__(kMThreads)
 merge_batch_kernel(const __grid_constant__ MergeParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    int q = 0;
+    static_assert(kMThreads == 2 * kMRows && kMCols * sizeof(bf16_t) == 2 * 128, "one L2 line per thread");
+    int q = 0, qn = 0, o0 = 0, k0 = 0;
+    if (blockIdx.x < p.n_tiles) locate_tile(p, blockIdx.x, qn, o0, k0);
     for (long long t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
-        while (q + 1 < p.n && t >= p.w[q + 1].first) ++q;
-        const MergeWeight& m = p.w[q];
-        const long long local = t - m.first;
-        const int rb = static_cast<int>(local / m.col_tiles), cb = static_cast<int>(local - static_cast<long long>(rb) * m.col_tiles);
-        merge_tile(m, p, rb * kMRows, cb * kMCols, smem);
+        q = qn;
+        const int to0 = o0, tk0 = k0;
+        if (t + gridDim.x < p.n_tiles) {
+            locate_tile(p, t + gridDim.x, qn, o0, k0);
+            prefetch_tile_l2(p.w[qn], o0, k0);
+        }
+        merge_tile(p.w[q], p, to0, tk0, smem);
         __syncthreads();   // the next tile reuses the staging buffers
     }
 }
