@@ -141,8 +141,8 @@ NCU_TRAFFIC = {
              "bytes_per_call": 987882112},   # profiles/bgmv_grouped_stress70b.md
     "mistral7b_prefill": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "e1e55b430f7ab83b",
              "bytes_per_call": 2060608192},   # profiles/sgmv_tc_mistral7b_prefill.md
-    "merge_mistral7b": {"files": ['merge.cu', 'decode_common.cuh', 'common.cuh'], "src": "511bb61086f954f4",
-             "bytes_per_step": 6988235520},   # profiles/merge_mistral7b.md
+    "merge_mistral7b": {"files": ['merge.cu', 'decode_common.cuh', 'common.cuh'], "src": "9deb0307ba91937a",
+             "bytes_per_step": 6994243328},   # profiles/merge_mistral7b.md
     "linear_mistral7b_prefill": {"files": ['linear_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "f52cc27e446ec6c9",
              "bytes_per_step": 19274225664},   # profiles/linear_tc_mistral7b_prefill.md (linear_tc_kernel only)
     "mixed": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "95f06cb49eae61ed",

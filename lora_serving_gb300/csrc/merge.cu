@@ -7,13 +7,15 @@
 // sign = +1 (merge) or -1 (unmerge), B' the folded store (scale applied),
 // the sum in fp32 over the slot rank (padding ranks are zero).
 //
-// One CTA per 64 x 128 tile of W: the tile, its 64 rows of B' and 128
-// columns of A arrive by 16-byte cp.async; warp w forms rows 16w..16w+15 of
-// B'A on the tensor cores (mma.sync m16n8k16, fp32 accumulate; A enters as
-// the col-major operand through transposing ldmatrix); each thread adds
-// its accumulator fragments into the staged tile and rounds once; the tile
-// leaves by coalesced 16-byte stores.  HBM-bound: W is read and written
-// once, A and B' come from L2 after their first use.
+// One CTA per 128 x 128 tile of W: its 128 rows of B' and 128 columns of A
+// arrive by 16-byte cp.async, then the tile itself (a second group, needed
+// only by the epilogue, so it lands while the MMAs run); warp w forms rows
+// 16w..16w+15 of B'A on the tensor cores (mma.sync m16n8k16, fp32
+// accumulate; A enters as the col-major operand through transposing
+// ldmatrix); each thread adds its accumulator fragments into the staged
+// tile and rounds once; the tile leaves by coalesced 16-byte stores.
+// HBM-bound: W is read and written once, A and B' come from L2 after their
+// first use.
 
 #include <algorithm>
 
@@ -26,9 +28,9 @@ namespace {
 
 using namespace dec;
 
-constexpr int kMRows = 64;                 // W rows per CTA
+constexpr int kMRows = 128;                // W rows per CTA
 constexpr int kMCols = 128;                // W columns per CTA
-constexpr int kMThreads = 128;             // 4 warps, 16 rows each
+constexpr int kMThreads = 256;             // 8 warps, 16 rows each
 constexpr int kMPitch = kMCols + 8;        // bf16 pitch of the W and A tiles (conflict-free ldmatrix)
 constexpr int kMaxMergeWeights = 32;       // weights per batch launch
 
@@ -57,24 +59,19 @@ struct MergeParams {
     float sign;
 };
 
-// W[o0 .. o0+63][k0 .. k0+127] += sign * B'A, one rounding.  Whole CTA;
+// W[o0 .. o0+127][k0 .. k0+127] += sign * B'A, one rounding.  Whole CTA;
 // the caller synchronises before smem is reused.
 __device__ __forceinline__ void merge_tile(const MergeWeight& m, const MergeParams& p, int o0, int k0,
                                            unsigned char* smem)
 {
     const int bp_pitch = p.r_pad + 8;
-    bf16_t* sW = reinterpret_cast<bf16_t*>(smem);                       // [64][kMPitch]
-    bf16_t* sB = sW + kMRows * kMPitch;                                 // [64][r_pad + 8]
+    bf16_t* sW = reinterpret_cast<bf16_t*>(smem);                       // [kMRows][kMPitch]
+    bf16_t* sB = sW + kMRows * kMPitch;                                 // [kMRows][r_pad + 8]
     bf16_t* sA = sB + kMRows * bp_pitch;                                // [r_pad][kMPitch]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // ---- stage the W tile, B' rows and A columns (zero outside the matrices) ----
-    for (int i = tid; i < kMRows * (kMCols / 8); i += kMThreads) {
-        const int r = i / (kMCols / 8), c = (i % (kMCols / 8)) * 8;
-        const bool ok = o0 + r < m.out && k0 + c < m.h_in;
-        cp_async16(smem_u32(sW + r * kMPitch + c),
-                   ok ? static_cast<const void*>(m.W + static_cast<size_t>(o0 + r) * m.ld_w + k0 + c) : m.W, ok);
-    }
+    // ---- stage B' rows and A columns (the MMA's operands), then the W tile
+    // (needed only by the epilogue); zero outside the matrices ----
     const int bch = p.r_pad / 8;
     for (int i = tid; i < kMRows * bch; i += kMThreads) {
         const int r = i / bch, c = (i % bch) * 8;
@@ -89,7 +86,14 @@ __device__ __forceinline__ void merge_tile(const MergeWeight& m, const MergePara
                    ok ? static_cast<const void*>(m.A + static_cast<size_t>(j) * m.h_in + k0 + c) : m.A, ok);
     }
     cp_async_commit();
-    cp_async_wait<0>();
+    for (int i = tid; i < kMRows * (kMCols / 8); i += kMThreads) {
+        const int r = i / (kMCols / 8), c = (i % (kMCols / 8)) * 8;
+        const bool ok = o0 + r < m.out && k0 + c < m.h_in;
+        cp_async16(smem_u32(sW + r * kMPitch + c),
+                   ok ? static_cast<const void*>(m.W + static_cast<size_t>(o0 + r) * m.ld_w + k0 + c) : m.W, ok);
+    }
+    cp_async_commit();
+    cp_async_wait<1>();
     __syncthreads();
 
     // ---- B'A for rows 16w..16w+15, all 128 columns (16 n-tiles of 8) ----
@@ -105,6 +109,9 @@ __device__ __forceinline__ void merge_tile(const MergeWeight& m, const MergePara
             mma_bf16_16816(acc[nt], a0, a1, a2, a3, b0, b1);
         }
     }
+
+    cp_async_wait<0>();
+    __syncthreads();
 
     // ---- W += sign * B'A at the fragment positions, one rounding ----
     const int g = lane >> 2, q2 = (lane & 3) * 2;
@@ -145,7 +152,7 @@ __device__ __forceinline__ void locate_tile(const MergeParams& p, long long t, i
     k0 = static_cast<int>(local - static_cast<long long>(rb) * m.col_tiles) * kMCols;
 }
 
-// One 128-byte line of a W tile per thread (64 rows x 2 lines) into L2.
+// One 128-byte line of a W tile per thread (128 rows x 2 lines) into L2.
 __device__ __forceinline__ void prefetch_tile_l2(const MergeWeight& m, int o0, int k0)
 {
     const int r = threadIdx.x >> 1, c = k0 + (threadIdx.x & 1) * 64;
@@ -159,8 +166,9 @@ __device__ __forceinline__ void prefetch_tile_l2(const MergeWeight& m, int o0, i
 // CTAs in flight together share B' rows and read neighbouring A columns.
 // Each CTA requests its next tile's W into L2 before it works on the current
 // one, so the HBM reads of the next tile overlap this tile's compute and
-// stores instead of following them.
-__global__ void __launch_bounds__(kMThreads)
+// stores instead of following them.  Three CTAs per SM (shared memory
+// allows three at slot rank 64), registers held to match.
+__global__ void __launch_bounds__(kMThreads, 3)
 merge_batch_kernel(const __grid_constant__ MergeParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
