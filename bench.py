@@ -135,18 +135,18 @@ ROUTE_KERNELS = {
 # step for the merge and linear-layer workloads; valid only while the listed
 # kernel sources hash to `src`.  Summaries in profiles/.
 NCU_TRAFFIC = {
-    "llama3b_decode": {"files": ['bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "0854a474f6bf61da",
-             "bytes_per_call": 3439008},   # profiles/bgmv_fused_llama3b_decode.md
-    "stress70b": {"files": ['bgmv_grouped.cu', 'decode_common.cuh', 'common.cuh'], "src": "d9f12af3b4f26b87",
-             "bytes_per_call": 987882112},   # profiles/bgmv_grouped_stress70b.md
+    "llama3b_decode": {"files": ['bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "010059f8745e9b90",
+             "bytes_per_call": 3438272},   # profiles/bgmv_fused_llama3b_decode.md
+    "stress70b": {"files": ['bgmv_grouped.cu', 'decode_common.cuh', 'common.cuh'], "src": "0d1b3c3b8322d136",
+             "bytes_per_call": 988209024},   # profiles/bgmv_grouped_stress70b.md
     "mistral7b_prefill": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "e1e55b430f7ab83b",
              "bytes_per_call": 2060608192},   # profiles/sgmv_tc_mistral7b_prefill.md
-    "merge_mistral7b": {"files": ['merge.cu', 'decode_common.cuh', 'common.cuh'], "src": "9deb0307ba91937a",
-             "bytes_per_step": 6994243328},   # profiles/merge_mistral7b.md
+    "merge_mistral7b": {"files": ['merge.cu', 'decode_common.cuh', 'common.cuh'], "src": "64c410c3e24d8148",
+             "bytes_per_step": 6994841856},   # profiles/merge_mistral7b.md
     "linear_mistral7b_prefill": {"files": ['linear_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "f52cc27e446ec6c9",
              "bytes_per_step": 19274225664},   # profiles/linear_tc_mistral7b_prefill.md (linear_tc_kernel only)
-    "mixed": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "95f06cb49eae61ed",
-             "bytes_per_call": 113031616},   # profiles/sgmv_tc_mistral7b_prefill.md
+    "mixed": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "304df0d5fa9a8122",
+             "bytes_per_call": 113018240},   # profiles/sgmv_tc_mistral7b_prefill.md
 }
 
 

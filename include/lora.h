@@ -73,7 +73,8 @@ typedef enum {
 
 /* Bits OR-ed into *dev_status by the kernels. */
 #define LORA_DEV_SLOT_OUT_OF_RANGE 0x1 /* a row named an id >= n_slots or < -1; row skipped */
-#define LORA_DEV_BAD_SEGMENT 0x2       /* a segment/perm entry fell outside its rows; skipped */
+#define LORA_DEV_BAD_SEGMENT 0x2       /* a segment/perm entry fell outside its rows, or a
+                                          group outgrew meta->max_gseg_len; rows skipped */
 #define LORA_DEV_TIMEOUT 0x4           /* an asynchronous copy did not land within 0.2 s; the
                                           affected rows are left unwritten (never expected) */
 
@@ -169,12 +170,19 @@ typedef struct {
     const int32_t* seg_starts;  /* [dev] [n_segs+1] prefill segments over [0, n_prefill) */
     const int32_t* seg_slot;    /* [dev] [n_segs] */
     int n_segs;
-    int max_seg_len;            /* longest prefill segment (host value) */
+    int max_seg_len;            /* longest prefill segment (host value; an upper bound,
+                                   0 = unknown).  It picks the kernel form; where
+                                   lora_linear's grouped shrink takes the segments, it
+                                   also sizes that grid, as max_gseg_len below. */
     const int32_t* perm;        /* [dev] [n_rows-n_prefill] decode rows sorted by slot */
     const int32_t* gseg_starts; /* [dev] [n_gsegs+1] groups over positions of perm */
     const int32_t* gseg_slot;   /* [dev] [n_gsegs] */
     int n_gsegs;
-    int max_gseg_len;           /* largest decode group (host value) */
+    int max_gseg_len;           /* largest decode group (host value; an upper bound,
+                                   0 = unknown).  The decode kernels size their grids
+                                   from it: a value below the true largest group leaves
+                                   rows without their delta and sets
+                                   LORA_DEV_BAD_SEGMENT. */
 } lora_meta_t;
 
 /* lora_apply flags.
@@ -203,7 +211,8 @@ typedef struct {
  *   - prefill rows: SGMV over meta->seg_*;
  *   - decode rows: BGMV when r_slot <= LORA_BGMV_MAX_RANK, otherwise SGMV
  *     over the gather groups meta->perm / gseg_* [TGI 4].
- * Each projection p adds its delta into y[:, projs[p].out_off + (0..width)).
+ * Each projection p adds its delta into y[:, projs[p].out_off + (0..width));
+ * the projections' column ranges must not overlap (LORA_ERR_SHAPE).
  * workspace [dev] at least lora_apply_workspace_bytes(n_rows, n_proj, r_slot)
  *           bytes, 256-byte aligned; its contents are scratch (the
  *           intermediate v: fp32, and bf16 hi/lo planes for the kernels

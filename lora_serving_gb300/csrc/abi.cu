@@ -50,7 +50,7 @@ lora_status_t check_x(const bf16_t* x, int ld_x, int h_in)
 lora_status_t check_y(const bf16_t* y, int ld_y, int y_off, int width)
 {
     if (!y || width <= 0 || y_off < 0) return LORA_ERR_INVALID_ARG;
-    if (y_off + width > ld_y) return LORA_ERR_SHAPE;
+    if (static_cast<long long>(y_off) + width > ld_y) return LORA_ERR_SHAPE;
     if (!aligned16(y) || ld_y % 8 != 0 || y_off % 8 != 0 || width % 8 != 0) return LORA_ERR_ALIGNMENT;
     return LORA_OK;
 }
@@ -77,6 +77,19 @@ lora_status_t check_segments(const int32_t* seg_starts, const int32_t* seg_slot,
     if (n_pos == 0) return LORA_OK;
     if (n_segs == 0 || !seg_starts || !seg_slot) return LORA_ERR_METADATA;
     if (!perm && n_pos > n_rows) return LORA_ERR_METADATA;
+    return LORA_OK;
+}
+
+// Projections of one call update disjoint column ranges of y: two kernels'
+// read-modify-writes of one element would race.
+lora_status_t check_disjoint(const lora_proj_t* projs, int n_proj)
+{
+    for (int p = 0; p < n_proj; ++p)
+        for (int q = 0; q < p; ++q) {
+            const long long a0 = projs[p].out_off, a1 = a0 + projs[p].width;
+            const long long b0 = projs[q].out_off, b1 = b0 + projs[q].width;
+            if (a0 < b1 && b0 < a1) return LORA_ERR_SHAPE;
+        }
     return LORA_OK;
 }
 
@@ -247,6 +260,7 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
         ps.out_off[p] = projs[p].out_off;
         ps.width[p] = projs[p].width;
     }
+    LORA_TRY(check_disjoint(projs, n_proj));
     const int R = n_proj * r_slot;
     if (!workspace) return LORA_ERR_WORKSPACE;
     if (ws_bytes < lora_apply_workspace_bytes(T, n_proj, r_slot)) return LORA_ERR_WORKSPACE;

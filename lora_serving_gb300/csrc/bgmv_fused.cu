@@ -160,7 +160,8 @@ bgmv_fused_kernel(FusedParams p)
     // leaves, so this grid never completes before that one (stream order
     // stays transitive under PDL); status flags are written only after a
     // wait.  Clusters without work leave at once and free their SM slots.
-    const UnitInfo ui = find_unit<kThreads>(p, unit, s_perm, stage_perm);   // uniform across the cluster
+    const int grid_units = static_cast<int>(gridDim.x) / (p.cs * p.n_parts);
+    const UnitInfo ui = find_unit<kThreads>(p, unit, s_perm, stage_perm, grid_units);   // uniform across the cluster
     const bool bad_group = ui.bad;
     const int pos0 = ui.pos0, nrows = ui.nrows, slot = ui.slot;
     if (!ui.found || slot == -1) {              // nothing to do (or base-only rows)

@@ -38,6 +38,7 @@
 // Waits on mbarriers are bounded (0.2 s) and end in LORA_DEV_TIMEOUT.
 
 #include <algorithm>
+#include <climits>
 
 #include "decode_common.cuh"
 #include "launch.h"
@@ -55,7 +56,7 @@ using namespace dec;
 // group whose bounds are not sane is reported by its first unit.  Scanned
 // form (upg == 0): units are numbered over all groups by a prefix sum.
 template <int NT, class Params>
-__device__ __forceinline__ UnitInfo grouped_unit(const Params& p, int u)
+__device__ __forceinline__ UnitInfo grouped_unit(const Params& p, int u, int grid_units)
 {
     if (p.upg > 0) {
         UnitInfo ui;
@@ -70,7 +71,7 @@ __device__ __forceinline__ UnitInfo grouped_unit(const Params& p, int u)
         ui.found = ui.nrows > 0;
         return ui;
     }
-    UnitInfo ui = find_unit<NT>(p, u, nullptr, false);
+    UnitInfo ui = find_unit<NT>(p, u, nullptr, false, grid_units);
     if (!ui.found) ui.nrows = 0;
     return ui;
 }
@@ -150,12 +151,16 @@ bgmv_group_shrink_kernel(GsParams p)
     const int crank = p.ks > 1 ? static_cast<int>(cluster_rank()) : 0;
     const int cl = blockIdx.x / p.ks;
     const int unit = cl / p.n_rb, rb = cl - unit * p.n_rb;
-    const UnitInfo ui = grouped_unit<kGsThreads>(p, unit);   // uniform across the cluster
+    const int grid_units = static_cast<int>(gridDim.x) / (p.ks * p.n_rb);
+    const UnitInfo ui = grouped_unit<kGsThreads>(p, unit, grid_units);   // uniform across the cluster
     const int pos0 = ui.pos0, nrows = ui.nrows, slot = ui.slot;
     const bool flagger = rb == 0 && crank == 0 && tid == 0;
+    if (ui.bad) {   // flagged, and a unit that was found is still done
+        grid_dep_wait();
+        if (flagger) flag(p.status, LORA_DEV_BAD_SEGMENT);
+    }
     if (nrows <= 0 || slot == -1) {
-        if (blockIdx.x == 0 || ui.bad) grid_dep_wait();
-        if (ui.bad && flagger) flag(p.status, LORA_DEV_BAD_SEGMENT);
+        if (blockIdx.x == 0) grid_dep_wait();
         return;
     }
     if (slot < -1 || slot >= p.n_slots) {
@@ -400,7 +405,7 @@ bgmv_group_expand_kernel(GexParams p)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.x / p.n_blocks;
     const int blk = blockIdx.x - unit * p.n_blocks;
-    const UnitInfo ui = grouped_unit<kGxThreads>(p, unit);
+    const UnitInfo ui = grouped_unit<kGxThreads>(p, unit, INT_MAX);   // unit count: checked by the shrink
     const int pos0 = ui.pos0, nrows = ui.nrows, slot = ui.slot;
     const bool bad = ui.bad;
     const bool flagger = blk == 0 && tid == 0;   // one CTA per unit reports

@@ -141,9 +141,12 @@ struct UnitInfo {
 // takes part and the answer is uniform across the CTA (and across a
 // cluster, whose CTAs all map to the same unit).  The group table is read
 // NT groups per round trip (one group per thread, block-wide prefix sum),
-// together with the permutation when it fits in s_perm.
+// together with the permutation when it fits in s_perm.  `bad` is set for
+// a malformed table, and when the table holds more units than the grid's
+// grid_units (the host's bound on the longest group was understated, so
+// some rows have no CTA): every CTA sees the same total and reports it.
 template <int NT, class Params>
-__device__ __forceinline__ UnitInfo find_unit(const Params& p, int u, int* s_perm, bool stage_perm)
+__device__ __forceinline__ UnitInfo find_unit(const Params& p, int u, int* s_perm, bool stage_perm, int grid_units)
 {
     __shared__ int s_warp[NT / 32];
     __shared__ UnitInfo s_info;
@@ -200,7 +203,7 @@ __device__ __forceinline__ UnitInfo find_unit(const Params& p, int u, int* s_per
     }
     if (p.n_groups <= 0) __syncthreads();
     UnitInfo r = s_info;
-    r.bad = s_bad;
+    r.bad = s_bad || base > grid_units;
     return r;
 }
 

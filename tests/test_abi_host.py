@@ -183,6 +183,13 @@ def test_kernel_entry_points_validate_before_launch():
     st = lib.lora_apply(base, 64, base, 64, 64, ctypes.addressof(projs), 5, 16, 2,
                         ctypes.addressof(meta), base, 1 << 20, 0, 0, 0)
     assert st == 1
+    # lora_apply: projection slices that overlap in y
+    both = abi.make_projs([(base, base, 0, 64), (base, base, 56, 64)])
+    st = lib.lora_apply(base, 128, base, 64, 64, ctypes.addressof(both), 2, 16, 2,
+                        ctypes.addressof(meta), base, 1 << 20, 0, 0, 0)
+    assert st == 2
+    # a slice whose end overflows int is past the row, not wrapped around
+    assert lib.lora_bgmv_expand(base, 64, 2**31 - 8, 64, base, 16, base, ids, 4, 16, 2, 0, 0) == 2
     # bf16 hi/lo planes (rank padded to 64, region rounded to 256 B) + fp32 v
     planes = (2 * 10 * 3 * 64 * 2 + 255) // 256 * 256
     assert lib.lora_apply_workspace_bytes(10, 3, 16) == planes + 10 * 3 * 16 * 4

@@ -452,6 +452,35 @@ def test_apply_decode_fused_thread_counts(h_in, widths, rank, T, n_slots, thread
     check_bf16(got, oracle_group(wl, "g"), wl.ids, wl.y["g"], f"fused threads={threads} h_in={h_in}")
 
 
+@pytest.mark.parametrize("two_launch", ["0", "1"])
+def test_apply_decode_understated_longest_group_flagged(two_launch, monkeypatch):
+    """The grids of the decode kernels are sized from the host's bound on the
+    longest group.  Understated, some rows get no CTA: the call flags it (and
+    the rows it did cover are still right)."""
+    monkeypatch.setenv("LORA_DECODE_TWO_LAUNCH", two_launch)
+    ids = np.concatenate([np.zeros(40), [1, 2, 3]]).astype(np.int32)   # 40 rows on slot 0: three units
+    wl = _small(ids, 0)
+    st = store.GroupStore.from_workload(wl, "g")
+    meta = store.BatchMeta(ids, 0, wl.n_slots)
+    assert meta.c.max_gseg_len == 40
+    meta.c.max_gseg_len = 1                                            # grid of 4 units for 6
+    s = _status()
+    y = to_dev(wl.y["g"])
+    store.apply(y, to_dev(wl.x["g"]), st, meta, store.workspace_for(43, 3, 8), dev_status=s)
+    torch.cuda.synchronize()
+    assert abi.lora_read_device_status(s) & abi.LORA_DEV_BAD_SEGMENT
+    if two_launch == "0":   # the scan numbers slot 0's units first: all 40 rows are covered
+        got = to_host(y)
+        ok = np.arange(40)
+        check_bf16(got[ok], oracle_group(wl, "g", ok), ids[ok], wl.y["g"][ok], "covered rows")
+    # a correct bound: no flag
+    meta.c.max_gseg_len = 40
+    s2 = _status()
+    store.apply(to_dev(wl.y["g"]), to_dev(wl.x["g"]), st, meta, store.workspace_for(43, 3, 8), dev_status=s2)
+    torch.cuda.synchronize()
+    assert abi.lora_read_device_status(s2) == 0
+
+
 def test_apply_decode_bad_permutation_flagged():
     """A corrupted gather permutation is flagged and its group's rows skipped."""
     ids = np.array([0, 1, 0, 1, 0, 1], np.int32)
