@@ -133,6 +133,27 @@ def _ld(t) -> int:
     return int(t.stride(0))
 
 
+_DTYPES = {"bf16": "torch.bfloat16", "f32": "torch.float32", "i32": "torch.int32"}
+
+
+def _dev(t, name: str, dtype: str | None = None, mat: bool = False) -> int:
+    """Device pointer of a kernel argument, after the checks the C ABI cannot
+    make: a torch tensor on a CUDA device (a host pointer handed to a kernel
+    is an illegal address), of the element type the kernel reads, and for
+    row-major operands (mat) 2-D with unit column stride, so that the row
+    stride is the leading dimension.  None (NULL) and raw integer pointers
+    pass unchecked."""
+    if t is None or isinstance(t, int):
+        return _p(t)
+    if not getattr(t, "is_cuda", False):
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and str(t.dtype) != _DTYPES[dtype]:
+        raise ValueError(f"{name} must be {_DTYPES[dtype]}, got {t.dtype}")
+    if mat and (t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1)):
+        raise ValueError(f"{name} must be 2-D with unit column stride")
+    return t.data_ptr()
+
+
 def _stream(stream) -> int:
     if stream is None:
         import torch
@@ -147,34 +168,38 @@ def _stream(stream) -> int:
 def lora_bgmv_shrink(v, x, A, lora_ids, *, h_in, r_slot, n_slots, dev_status=None, stream=None):
     n_rows = int(lora_ids.numel())
     _check("lora_bgmv_shrink", load().lora_bgmv_shrink(
-        _p(v), _ld(v), _p(x), _ld(x), _p(A), _p(lora_ids), n_rows, h_in, r_slot, n_slots,
-        _p(dev_status), _stream(stream)))
+        _dev(v, "v", "f32", True), _ld(v), _dev(x, "x", "bf16", True), _ld(x), _dev(A, "A", "bf16"),
+        _dev(lora_ids, "lora_ids", "i32"), n_rows, h_in, r_slot, n_slots, _dev(dev_status, "dev_status", "i32"),
+        _stream(stream)))
 
 
 def lora_bgmv_expand(y, y_off, width, v, B, lora_ids, *, r_slot, n_slots, dev_status=None,
                      stream=None, v_col=0):
     n_rows = int(lora_ids.numel())
-    vp = _p(v) + 4 * v_col
+    vp = _dev(v, "v", "f32", True) + 4 * v_col
     _check("lora_bgmv_expand", load().lora_bgmv_expand(
-        _p(y), _ld(y), y_off, width, vp, _ld(v), _p(B), _p(lora_ids), n_rows, r_slot, n_slots,
-        _p(dev_status), _stream(stream)))
+        _dev(y, "y", "bf16", True), _ld(y), y_off, width, vp, _ld(v), _dev(B, "B", "bf16"),
+        _dev(lora_ids, "lora_ids", "i32"), n_rows, r_slot, n_slots, _dev(dev_status, "dev_status", "i32"),
+        _stream(stream)))
 
 
 def lora_sgmv_shrink(v, x, A, seg_starts, seg_slot, n_segs, row_perm, n_pos, *, h_in, r_slot,
                      n_slots, max_seg_len=0, dev_status=None, stream=None):
     _check("lora_sgmv_shrink", load().lora_sgmv_shrink(
-        _p(v), _ld(v), _p(x), _ld(x), _p(A), _p(seg_starts), _p(seg_slot), n_segs, _p(row_perm),
-        n_pos, int(x.shape[0]), max_seg_len, h_in, r_slot, n_slots, _p(dev_status),
-        _stream(stream)))
+        _dev(v, "v", "f32", True), _ld(v), _dev(x, "x", "bf16", True), _ld(x), _dev(A, "A", "bf16"),
+        _dev(seg_starts, "seg_starts", "i32"), _dev(seg_slot, "seg_slot", "i32"), n_segs,
+        _dev(row_perm, "row_perm", "i32"), n_pos, int(x.shape[0]), max_seg_len, h_in, r_slot, n_slots,
+        _dev(dev_status, "dev_status", "i32"), _stream(stream)))
 
 
 def lora_sgmv_expand(y, y_off, width, v, B, seg_starts, seg_slot, n_segs, row_perm, n_pos, *,
                      r_slot, n_slots, max_seg_len=0, dev_status=None, stream=None, v_col=0):
-    vp = _p(v) + 4 * v_col
+    vp = _dev(v, "v", "f32", True) + 4 * v_col
     _check("lora_sgmv_expand", load().lora_sgmv_expand(
-        _p(y), _ld(y), y_off, width, vp, _ld(v), _p(B), _p(seg_starts), _p(seg_slot), n_segs,
-        _p(row_perm), n_pos, int(y.shape[0]), max_seg_len, r_slot, n_slots, _p(dev_status),
-        _stream(stream)))
+        _dev(y, "y", "bf16", True), _ld(y), y_off, width, vp, _ld(v), _dev(B, "B", "bf16"),
+        _dev(seg_starts, "seg_starts", "i32"), _dev(seg_slot, "seg_slot", "i32"), n_segs,
+        _dev(row_perm, "row_perm", "i32"), n_pos, int(y.shape[0]), max_seg_len, r_slot, n_slots,
+        _dev(dev_status, "dev_status", "i32"), _stream(stream)))
 
 
 def make_projs(projs):
@@ -191,16 +216,18 @@ def lora_apply(y, x, h_in, projs, r_slot, n_slots, meta, workspace, *, flags=0, 
     flags: LORA_APPLY_* bits."""
     ws_bytes = workspace.numel() * workspace.element_size()
     _check("lora_apply", load().lora_apply(
-        _p(y), _ld(y), _p(x), _ld(x), h_in, ctypes.addressof(projs), len(projs), r_slot, n_slots,
-        ctypes.addressof(meta), _p(workspace), ws_bytes, int(flags), _p(dev_status), _stream(stream)))
+        _dev(y, "y", "bf16", True), _ld(y), _dev(x, "x", "bf16", True), _ld(x), h_in, ctypes.addressof(projs),
+        len(projs), r_slot, n_slots, ctypes.addressof(meta), _dev(workspace, "workspace"), ws_bytes, int(flags),
+        _dev(dev_status, "dev_status", "i32"), _stream(stream)))
 
 
 def lora_apply_noalloc(y, x, h_in, projs, r_slot, n_slots, meta, *, flags=0, dev_status=None, stream=None):
     """lora_apply with the library's built-in scratch instead of a workspace
     (for callers that cannot allocate device memory when they call in)."""
     _check("lora_apply_noalloc", load().lora_apply_noalloc(
-        _p(y), _ld(y), _p(x), _ld(x), h_in, ctypes.addressof(projs), len(projs), r_slot, n_slots,
-        ctypes.addressof(meta), int(flags), _p(dev_status), _stream(stream)))
+        _dev(y, "y", "bf16", True), _ld(y), _dev(x, "x", "bf16", True), _ld(x), h_in, ctypes.addressof(projs),
+        len(projs), r_slot, n_slots, ctypes.addressof(meta), int(flags), _dev(dev_status, "dev_status", "i32"),
+        _stream(stream)))
 
 
 def lora_linear(y, x, h_in, W, projs, r_slot, n_slots, meta, workspace, *, dev_status=None, stream=None):
@@ -209,8 +236,9 @@ def lora_linear(y, x, h_in, W, projs, r_slot, n_slots, meta, workspace, *, dev_s
     the stacked base weight [n_out][h_in] (row stride ld); y is written."""
     ws_bytes = workspace.numel() * workspace.element_size()
     _check("lora_linear", load().lora_linear(
-        _p(y), _ld(y), _p(x), _ld(x), h_in, _p(W), _ld(W), ctypes.addressof(projs), len(projs), r_slot,
-        n_slots, ctypes.addressof(meta), _p(workspace), ws_bytes, _p(dev_status), _stream(stream)))
+        _dev(y, "y", "bf16", True), _ld(y), _dev(x, "x", "bf16", True), _ld(x), h_in, _dev(W, "W", "bf16", True),
+        _ld(W), ctypes.addressof(projs), len(projs), r_slot, n_slots, ctypes.addressof(meta),
+        _dev(workspace, "workspace"), ws_bytes, _dev(dev_status, "dev_status", "i32"), _stream(stream)))
 
 
 def lora_merge(W, A, B, sign, *, stream=None):
@@ -219,8 +247,8 @@ def lora_merge(W, A, B, sign, *, stream=None):
     of the scaled B store; sign +1 merges, -1 unmerges."""
     out, h_in = int(W.shape[0]), int(W.shape[1])
     r_slot = int(A.shape[0])
-    _check("lora_merge", load().lora_merge(_p(W), _ld(W), out, h_in, _p(A), _p(B), r_slot, int(sign),
-                                           _stream(stream)))
+    _check("lora_merge", load().lora_merge(_dev(W, "W", "bf16", True), _ld(W), out, h_in, _dev(A, "A", "bf16", True),
+                                           _dev(B, "B", "bf16", True), r_slot, int(sign), _stream(stream)))
 
 
 def lora_merge_batch(Ws, As, Bs, sign, *, stream=None):
@@ -233,7 +261,8 @@ def lora_merge_batch(Ws, As, Bs, sign, *, stream=None):
     out = (ctypes.c_int * max(1, n))()
     h_in = (ctypes.c_int * max(1, n))()
     for i, (W, A, B) in enumerate(zip(Ws, As, Bs)):
-        arr_w[i], arr_a[i], arr_b[i] = _p(W), _p(A), _p(B)
+        arr_w[i] = _dev(W, f"Ws[{i}]", "bf16", True)
+        arr_a[i], arr_b[i] = _dev(A, f"As[{i}]", "bf16", True), _dev(B, f"Bs[{i}]", "bf16", True)
         ld[i], out[i], h_in[i] = _ld(W), int(W.shape[0]), int(W.shape[1])
     r_slot = int(As[0].shape[0]) if n else 8
     _check("lora_merge_batch", load().lora_merge_batch(n, arr_w, ld, out, h_in, arr_a, arr_b, r_slot, int(sign),
@@ -256,8 +285,8 @@ class SlotManager:
         hi = (ctypes.c_int * self.n_proj)(*h_in)
         wd = (ctypes.c_int * self.n_proj)(*width)
         if A_stores is not None:
-            self._a = (ctypes.c_void_p * self.n_proj)(*[_p(t) for t in A_stores])
-            self._b = (ctypes.c_void_p * self.n_proj)(*[_p(t) for t in B_stores])
+            self._a = (ctypes.c_void_p * self.n_proj)(*[_dev(t, "A_stores", "bf16") for t in A_stores])
+            self._b = (ctypes.c_void_p * self.n_proj)(*[_dev(t, "B_stores", "bf16") for t in B_stores])
             a, b = ctypes.addressof(self._a), ctypes.addressof(self._b)
         else:
             a = b = 0
@@ -311,7 +340,7 @@ def lora_apply_workspace_bytes(n_rows, n_proj, r_slot) -> int:
 def lora_read_device_status(dev_status, stream=None) -> int:
     out = ctypes.c_int32(0)
     _check("lora_read_device_status", load().lora_read_device_status(
-        _p(dev_status), ctypes.addressof(out), _stream(stream)))
+        _dev(dev_status, "dev_status", "i32"), ctypes.addressof(out), _stream(stream)))
     return out.value
 
 

@@ -238,3 +238,18 @@ def test_linear_and_merge_batch_validate_before_launch():
     assert lib.lora_merge_batch(1, Ws, ld, out, h_in, As, Bs, 136, 1, 0) == 3
     # nothing to do
     assert lib.lora_merge_batch(0, None, None, None, None, None, None, 16, 1, 0) == 0
+
+
+def test_binding_refuses_host_tensors_for_kernel_arguments():
+    """A host pointer handed to a kernel would be an illegal device address:
+    the binding refuses host tensors before calling into the library."""
+    import torch
+    v = torch.zeros(4, 16)
+    x = torch.zeros(4, 64, dtype=torch.bfloat16)
+    A = torch.zeros(2, 16, 64, dtype=torch.bfloat16)
+    ids = torch.zeros(4, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        abi.lora_bgmv_shrink(v, x, A, ids, h_in=64, r_slot=16, n_slots=2, stream=0)
+    W = torch.zeros(64, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        abi.lora_merge(W, A[0], torch.zeros(64, 16, dtype=torch.bfloat16), 1, stream=0)

@@ -680,6 +680,24 @@ def test_merge_batch_rejects_before_enqueue():
     np.testing.assert_array_equal(to_host(Wd), keep)   # nothing ran
 
 
+def test_binding_checks_dtype_and_layout():
+    """Arguments of the wrong element type, or operands whose columns are not
+    contiguous, are refused by the binding before any launch."""
+    wl = _small(np.array([0, 1, 0, 1], np.int32), 0, widths=(64,))
+    st = store.GroupStore.from_workload(wl, "g")
+    x = to_dev(wl.x["g"])
+    ids = torch.from_numpy(wl.ids).cuda()
+    v = torch.zeros(4, 8, device="cuda")
+    with pytest.raises(ValueError, match="float32"):
+        abi.lora_bgmv_shrink(v.double(), x, st.A[0], ids, h_in=64, r_slot=8, n_slots=4)
+    with pytest.raises(ValueError, match="int32"):
+        abi.lora_bgmv_shrink(v, x, st.A[0], ids.long(), h_in=64, r_slot=8, n_slots=4)
+    with pytest.raises(ValueError, match="unit column stride"):
+        abi.lora_bgmv_shrink(v, x.t(), st.A[0], ids, h_in=64, r_slot=8, n_slots=4)
+    torch.cuda.synchronize()
+    assert torch.all(v == 0)
+
+
 def test_merge_rejects_bad_arguments_before_enqueue():
     W = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
     A = torch.zeros(16, 64, dtype=torch.bfloat16, device="cuda")
