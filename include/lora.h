@@ -28,16 +28,18 @@
  *
  * Conventions for every entry point:
  *   - bf16 values are passed as their 16-bit patterns (lora_bf16_t).
- *   - Device pointers (marked [dev]) are owned by the caller; the library
- *     allocates no memory on any of these paths and keeps no state between
- *     calls except what the caller passes.  Host pointers are marked [host].
+ *   - Device pointers (marked [dev]) are owned by the caller; the kernel
+ *     entry points allocate no memory and keep no state between calls
+ *     except what the caller passes (the slot manager, below, owns a pinned
+ *     host cache).  Host pointers are marked [host].
  *   - Kernel entry points validate their arguments on the host, enqueue on
  *     `stream` and return without synchronising.  A host-detectable error
  *     returns a non-OK status BEFORE anything is enqueued.
  *   - Device-detected faults (an adapter id >= n_slots, a segment table that
  *     does not cover its rows) never trap: the row is skipped and a bit is
  *     OR-ed into *dev_status (LORA_DEV_*), which may be NULL to ignore them.
- *     Kernels contain no spin-waits and no device printf.
+ *     Kernels contain no device printf and no unbounded wait: a wait for an
+ *     asynchronous copy gives up after 0.2 s and sets LORA_DEV_TIMEOUT.
  *   - Alignment: every bf16/fp32 matrix pointer is 16-byte aligned, and all
  *     leading dimensions, widths, column offsets and h_in are multiples of 8
  *     elements (one 128-bit vector of bf16); r_slot is a multiple of 8.
@@ -219,6 +221,13 @@ typedef struct {
  *           whose expand runs on tensor cores), written only after the
  *           kernel enqueued just before the call has completed.
  * flags     LORA_APPLY_* above (0 = default ordering).
+ * Errors (before anything is enqueued): LORA_ERR_INVALID_ARG (NULL projs,
+ * meta, x or lora_ids; n_proj outside 1..LORA_MAX_PROJ), LORA_ERR_SHAPE (a
+ * slice past ld_y, overlapping slices, ld_x < h_in), LORA_ERR_ALIGNMENT,
+ * LORA_ERR_RANK_EXCEEDS_SLOT (r_slot > LORA_MAX_RANK), LORA_ERR_METADATA
+ * (n_prefill outside [0, n_rows], missing segment or group tables),
+ * LORA_ERR_WORKSPACE, LORA_ERR_CUDA (a launch failed; kernels enqueued
+ * before it stay enqueued).  Device status: LORA_DEV_* above.
  */
 lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_x, int h_in,
                          const lora_proj_t* projs, int n_proj, int r_slot, int n_slots,
