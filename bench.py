@@ -143,7 +143,7 @@ NCU_TRAFFIC = {
              "bytes_per_call": 2060608192},   # profiles/sgmv_tc_mistral7b_prefill.md
     "merge_mistral7b": {"files": ['merge.cu', 'decode_common.cuh', 'common.cuh'], "src": "64c410c3e24d8148",
              "bytes_per_step": 6994841856},   # profiles/merge_mistral7b.md
-    "linear_mistral7b_prefill": {"files": ['linear_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "f52cc27e446ec6c9",
+    "linear_mistral7b_prefill": {"files": ['linear_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "f502730f1fa519ab",
              "bytes_per_step": 19274225664},   # profiles/linear_tc_mistral7b_prefill.md (linear_tc_kernel only)
     "mixed": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "304df0d5fa9a8122",
              "bytes_per_call": 113018240},   # profiles/sgmv_tc_mistral7b_prefill.md

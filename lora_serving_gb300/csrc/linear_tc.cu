@@ -16,7 +16,7 @@
 // columns of one projection, visited in groups of kGroupM row tiles so that
 // the x and W tiles in flight at once fit in L2.  A tile is two 128-row
 // halves, each an M = 128 MMA into its own 256 columns of tensor memory,
-// sharing every W box: 64 bytes of operands per 1024 MMA cycles.  Per tile
+// sharing every W box: 64 KB of operands per 1024 MMA cycles.  Per tile
 // the K loop is ceil(h_in / 64) base steps (a 256-row x box and a W box)
 // followed by ceil(r_slot / 64) LoRA steps (the half's v_hi and v_lo boxes
 // and a box of B') per adapter of each half, into the half's accumulator:
