@@ -2,7 +2,8 @@
  * lora_oracle.c -- plain, slow, fp64 CPU oracle for the multi-LoRA delta.
  *
  * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
- * baseline leg of the benchmark may load this library.  It shares no code,
+ * legs of the benchmark (its host baseline and its reference arm) may load
+ * this library.  It shares no code,
  * header, table or helper with the CUDA library under lora_serving_gb300/,
  * and it must never sit on the product path.
  *
