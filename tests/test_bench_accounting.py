@@ -61,3 +61,24 @@ def test_merge_bytes_equal_brute_force():
     touched |= {("A", j, k, b) for j in range(r) for k in range(h_in) for b in range(2)}
     touched |= {("B", o, j, b) for o in range(out) for j in range(r) for b in range(2)}
     assert bench.merge_bytes(out, h_in, r) == len(touched)
+
+
+def test_linear_flops_equal_counted_multiply_adds():
+    """Base product for every row and output column, then the delta of each
+    active row at its adapter's true rank: two flops per multiply-add."""
+    ids = np.array([0, 1, -1, 1, 2], np.int32)
+    ranks = np.array([8, 4, 16])
+    wl = synth.Workload("acct", 0, [synth.Group("g", 16, [("q", 16), ("k", 8)])],
+                        ranks, 2.0 * ranks, np.zeros(3, bool), 16, ids, 0)
+    g = wl.groups[0]
+    macs = 0
+    for t in range(wl.n_rows):
+        for _o in range(g.ld_y):
+            for _k in range(g.h_in):
+                macs += 1
+        if ids[t] >= 0:
+            r = int(ranks[ids[t]])
+            for _, w in g.projs:
+                macs += r * g.h_in      # shrink
+                macs += w * r           # expand
+    assert bench.linear_flops(wl, g) == 2 * macs
