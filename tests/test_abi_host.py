@@ -253,3 +253,20 @@ def test_binding_refuses_host_tensors_for_kernel_arguments():
     W = torch.zeros(64, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA tensor"):
         abi.lora_merge(W, A[0], torch.zeros(64, 16, dtype=torch.bfloat16), 1, stream=0)
+
+
+def test_noalloc_rejects_before_any_cuda_call():
+    """lora_apply_noalloc refuses a batch too large for its built-in scratch,
+    and bad counts, before it looks up the scratch on a device."""
+    lib = abi.load()
+    buf = (ctypes.c_uint8 * 4096)()
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    projs = abi.make_projs([(base, base, 0, 64)])
+    meta = abi.lora_meta_t()
+    rows = abi.LORA_NOALLOC_SCRATCH_BYTES // (64 * 4) + 1   # fp32 v alone exceeds the scratch
+    meta.lora_ids, meta.n_rows, meta.n_prefill = base, rows, 0
+    P = ctypes.addressof
+    assert lib.lora_apply_noalloc(base, 64, base, 64, 64, P(projs), 1, 64, 2, P(meta), 0, 0, 0) == 7
+    assert lib.lora_apply_noalloc(base, 64, base, 64, 64, P(projs), 0, 64, 2, P(meta), 0, 0, 0) == 1
+    meta.n_rows = -1
+    assert lib.lora_apply_noalloc(base, 64, base, 64, 64, P(projs), 1, 64, 2, P(meta), 0, 0, 0) == 1
