@@ -234,6 +234,9 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
                          const lora_meta_t* meta, void* workspace, size_t ws_bytes,
                          uint32_t flags, int32_t* dev_status, lora_stream_t stream);
 
+/* Workspace bytes lora_apply needs for n_rows rows, n_proj projections of
+ * slot rank r_slot; 0 for counts lora_apply rejects (a non-positive count,
+ * n_proj > LORA_MAX_PROJ, r_slot > LORA_MAX_RANK). */
 size_t lora_apply_workspace_bytes(int n_rows, int n_proj, int r_slot);
 
 /* Size of the scratch array built into the library for lora_apply_noalloc. */
@@ -255,7 +258,12 @@ size_t lora_apply_workspace_bytes(int n_rows, int n_proj, int r_slot);
  *     of slot rank 64).
  *   - The first call on a device looks up the array's device address on
  *     the current device (cudaGetSymbolAddress); make that first call
- *     before any stream capture.  LORA_ERR_CUDA if the lookup fails.
+ *     before any stream capture.  LORA_ERR_CUDA if the lookup fails.  The
+ *     address is kept for the life of the process: after a device reset
+ *     (cudaDeviceReset, or a reset of the primary context) it may be stale,
+ *     so do not call this entry point again on that device.
+ *   - n_slots, r_slot and the row count are checked as lora_apply checks
+ *     them before the size test, so a bad rank gives lora_apply's status.
  *   - No allocation of any kind happens on this path.
  *   - All calls share the one array and it keeps the last call's contents
  *     (nothing in it needs to start at zero); calls that may overlap on the

@@ -234,6 +234,7 @@ static size_t plane_region_bytes(int n_rows, int n_proj, int r_slot)
 size_t lora_apply_workspace_bytes(int n_rows, int n_proj, int r_slot)
 {
     if (n_rows <= 0 || n_proj <= 0 || r_slot <= 0) return 0;
+    if (n_proj > LORA_MAX_PROJ || r_slot > LORA_MAX_RANK) return 0;   // lora_apply rejects these
     return plane_region_bytes(n_rows, n_proj, r_slot) + static_cast<size_t>(n_rows) * n_proj * r_slot * sizeof(float);
 }
 

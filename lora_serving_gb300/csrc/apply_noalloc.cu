@@ -14,7 +14,10 @@
 // Host code cannot use the array's name as a device address (on the host
 // it is only a stand-in), so the first call on each device looks the
 // address up with cudaGetSymbolAddress, with that device current, and keeps
-// it.  Nothing in the array needs to start at zero: within one call, every
+// it for the life of the process; a device reset (cudaDeviceReset, or a
+// reset of the primary context) reloads the module and may move the array,
+// after which the kept address is stale and this entry point must not be
+// called again on that device.  Nothing in the array needs to start at zero: within one call, every
 // element the expand reads has been written by that call's shrink.  All
 // calls share the one array, so calls that may run at the same time on the
 // GPU (on different streams, say) race on it.
@@ -55,7 +58,11 @@ extern "C" lora_status_t lora_apply_noalloc(lora_bf16_t* y, int ld_y, const lora
                                             lora_stream_t stream)
 {
     if (!projs || !meta || n_proj <= 0 || n_proj > LORA_MAX_PROJ) return LORA_ERR_INVALID_ARG;
-    if (meta->n_rows < 0 || r_slot <= 0) return LORA_ERR_INVALID_ARG;
+    // The counts lora_apply checks first, so a bad rank reports what
+    // lora_apply would report rather than a scratch-size failure.
+    if (meta->n_rows < 0 || n_slots <= 0 || r_slot <= 0) return LORA_ERR_INVALID_ARG;
+    if (r_slot > LORA_MAX_RANK) return LORA_ERR_RANK_EXCEEDS_SLOT;
+    if (r_slot % 8 != 0) return LORA_ERR_ALIGNMENT;
     if (lora_apply_workspace_bytes(meta->n_rows, n_proj, r_slot) > LORA_NOALLOC_SCRATCH_BYTES)
         return LORA_ERR_WORKSPACE;   // batch too large for the built-in scratch
     void* scratch = nullptr;

@@ -270,3 +270,11 @@ def test_noalloc_rejects_before_any_cuda_call():
     assert lib.lora_apply_noalloc(base, 64, base, 64, 64, P(projs), 0, 64, 2, P(meta), 0, 0, 0) == 1
     meta.n_rows = -1
     assert lib.lora_apply_noalloc(base, 64, base, 64, 64, P(projs), 1, 64, 2, P(meta), 0, 0, 0) == 1
+    # a bad rank is reported as lora_apply reports it, not as a scratch-size
+    # failure (and the size arithmetic never sees a huge rank)
+    meta.n_rows = rows
+    assert lib.lora_apply_noalloc(base, 64, base, 64, 64, P(projs), 1, 2**31 - 1, 2, P(meta), 0, 0, 0) == 3
+    assert lib.lora_apply_noalloc(base, 64, base, 64, 64, P(projs), 1, 12, 2, P(meta), 0, 0, 0) == 5
+    assert lib.lora_apply_noalloc(base, 64, base, 64, 64, P(projs), 1, 64, 0, P(meta), 0, 0, 0) == 1
+    assert lib.lora_apply_workspace_bytes(rows, 1, 2**31 - 1) == 0
+    assert lib.lora_apply_workspace_bytes(rows, 5, 64) == 0

@@ -62,6 +62,35 @@ def test_no_alloc_matches_workspace_entry_point_twice():
         np.testing.assert_array_equal(got, ref)   # same kernels, same order: same bits
 
 
+def test_no_alloc_back_to_back_on_one_stream():
+    """The mixed and the tiny batch enqueued one after the other on one
+    stream with no synchronisation between them: the second call's kernels
+    may start early (programmatic dependent launch) while the first call
+    still uses the shared scratch, and must still see only their own
+    intermediate values.  Both results match the workspace entry point bit
+    for bit."""
+    probs = [_problem("mixed", "accumulate"), _problem("tiny", "delta")]
+    refs = [_with_workspace(*p) for p in probs]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ys = []
+    for flags in (0, abi.LORA_APPLY_X_READY):
+        outs = []
+        for wl, g, st, meta in probs:
+            y = to_dev(wl.y[g.name])
+            x = to_dev(wl.x[g.name])
+            outs.append((y, x))
+        torch.cuda.synchronize()
+        for (wl, g, st, meta), (y, x) in zip(probs, outs):
+            abi.lora_apply_noalloc(y, x, g.h_in, st.c_projs(), st.r_slot, st.n_slots, meta.c, flags=flags,
+                                   dev_status=status)
+        torch.cuda.synchronize()
+        ys.append([to_host(y) for y, _ in outs])
+    assert abi.lora_read_device_status(status) == 0
+    for got in ys:
+        for (wl, g, _, _), out, ref in zip(probs, got, refs):
+            np.testing.assert_array_equal(out, ref, err_msg=f"back-to-back no-alloc call, {wl.name}")
+
+
 def test_no_alloc_rejects_batches_beyond_its_scratch():
     rows = abi.LORA_NOALLOC_SCRATCH_BYTES // (3 * 64 * 4) + 1
     ids = np.zeros(rows, np.int32)
