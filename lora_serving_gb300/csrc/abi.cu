@@ -16,6 +16,7 @@ namespace {
 std::atomic<uint64_t> g_launches{0};
 }
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+unsigned test_stall_bytes(int kernel) { return env_int("LORA_TEST_STALL", 0) == kernel ? 16u : 0u; }
 }  // namespace lora
 
 using lora::bf16_t;

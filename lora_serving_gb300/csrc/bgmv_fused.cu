@@ -76,6 +76,7 @@ struct FusedParams {
     int r_pad;                // r_slot rounded up to 16 (expand mma K)
     int x_ready;              // x may be read before the grid dependency resolves
     int y_ready;              // y may be updated before it resolves
+    unsigned stall_tx;        // test hook: extra bytes expected on the first B' tile (0 normally)
     int32_t* status;
 };
 
@@ -262,7 +263,7 @@ bgmv_fused_kernel(FusedParams p)
 
     // ---- weights first: they do not depend on the preceding kernel ----
     if (ch_end > ch_begin) {
-        if (tid == 0) mbar_expect(&s_barB, b_bytes(ch_begin, tile0_end));
+        if (tid == 0) mbar_expect(&s_barB, b_bytes(ch_begin, tile0_end) + p.stall_tx);
         __syncthreads();
         copy_B(ch_begin, tile0_end, &s_barB);
     }
@@ -381,6 +382,10 @@ bgmv_fused_kernel(FusedParams p)
     for (int c0 = ch_begin; c0 < ch_end; c0 += p.nch_tile) {
         const int c1 = min(ch_end, c0 + p.nch_tile);
         const int nch = c1 - c0;
+        // After a timeout the barrier's phase never completed: it is not armed
+        // again, and this CTA's remaining tiles are left alone (failed is
+        // uniform across the CTA here).
+        if (failed) break;
         if (c0 != ch_begin) {                   // later tiles: fresh chunk map and B'
             __syncthreads();
             map_chunks(c0, c1);
@@ -582,6 +587,7 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     p.r_pad = (ps.r_slot + 15) / 16 * 16;
     p.x_ready = (flags & LORA_APPLY_X_READY) ? 1 : 0;
     p.y_ready = (flags & LORA_APPLY_Y_READY) ? 1 : 0;
+    p.stall_tx = test_stall_bytes(kStallFusedDecode);
     p.status = status;
 
     cudaLaunchConfig_t cfg = {};

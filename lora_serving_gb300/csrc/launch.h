@@ -12,6 +12,14 @@ namespace lora {
 // Counts every kernel launch the library issues (see lora_kernel_launch_count).
 void note_launch();
 
+// Test hook for the bounded waits: LORA_TEST_STALL names one kernel
+// (kStallShrinkTc, kStallExpandTc or kStallFusedDecode) whose first copy
+// barrier is armed for 16 bytes more than its copies deliver, so that wait
+// runs out and the kernel takes its timeout path (LORA_DEV_TIMEOUT).  The
+// copies themselves complete as usual.  Unset outside the tests.
+constexpr int kStallShrinkTc = 1, kStallExpandTc = 2, kStallFusedDecode = 3;
+unsigned test_stall_bytes(int kernel);
+
 // Integer tuning override from the environment (dflt when unset or empty).
 inline int env_int(const char* name, int dflt)
 {

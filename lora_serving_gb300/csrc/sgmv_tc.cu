@@ -18,7 +18,11 @@
 // multiplies both planes by B', carrying v to ~2^-17 relative.
 //
 // Every mbarrier wait is bounded (0.2 s); a timeout sets LORA_DEV_TIMEOUT,
-// skips the rest of the tile and still frees the tensor memory.
+// skips the rest of the tile and still frees the tensor memory.  The shrink
+// then stores a zero intermediate for the tile's rows (so the expand adds
+// nothing to them) and the expand writes nothing; before a CTA leaves, its
+// producer waits (bounded) for every copy it issued, so no copy into the
+// CTA's shared memory is still in flight when the CTA's resources go back.
 
 #include <algorithm>
 #include <cstdlib>
@@ -142,6 +146,7 @@ struct ShrinkTcParams {
     int r_pad64;         // r_slot rounded up to 64 (plane columns per projection)
     int ks;              // CTAs per row tile (a cluster), each a slice of K
     int x_ready;         // x is not written by the preceding kernel: read it before the wait
+    unsigned stall_tx;   // test hook: extra bytes expected on the first stage (0 normally)
     int32_t* status;
 };
 
@@ -192,7 +197,7 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full[8], empty[8], done;
     __shared__ uint32_t s_tmem;
-    __shared__ int s_fail;
+    __shared__ volatile int s_fail;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // With ks > 1 a cluster of ks CTAs shares a row tile, CTA c reducing K
@@ -246,19 +251,27 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
 
     if (warp == 0 && lane == 0) {
         // producer: X box + one A box per projection per 64-element K block
+        int issued = 0;
         for (int kb = 0; kb < n_kb; ++kb) {
             const int s = kb % S;
+            // a stage is re-armed only once the MMAs have consumed it (its
+            // previous phase complete)
             if (kb >= S && !mbar_wait(&empty[s], ((kb / S) - 1) & 1)) {
                 s_fail = 1;
                 break;
             }
             uint8_t* st = base + s * stage_bytes;
-            mbar_expect_tx(&full[s], stage_bytes);
+            mbar_expect_tx(&full[s], stage_bytes + (kb == 0 ? p.stall_tx : 0u));
             tma_load_2d(st, &mx, (kb0 + kb) * kKB, ti.row0, &full[s]);
             for (int q = 0; q < p.n_proj; ++q)
                 tma_load_2d(st + kBoxBytes + q * p.r_slot * 128, amap[q], (kb0 + kb) * kKB, ti.slot * p.r_slot,
                             &full[s]);
+            issued = kb + 1;
         }
+        // Every copy issued has landed before the CTA moves on (after a normal
+        // run the MMA thread has already seen each of these phases complete).
+        for (int kb = issued > S ? issued - S : 0; kb < issued; ++kb)
+            if (!mbar_wait(&full[kb % S], (kb / S) & 1)) s_fail = 1;
     } else if (warp == 1 && lane == 0) {
         // MMA issuer: 4 x (128 x R x 16) per K block, accumulating in TMEM
         const uint32_t idesc = idesc_bf16_f32(kTileM, p.R);
@@ -283,8 +296,13 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
     __syncwarp();
 
     // ---- epilogue: TMEM row (lane) -> v ----
+    // A tile whose copies or MMAs did not complete stores a zero intermediate
+    // for its rows (the expand then adds nothing to them) and reports the
+    // timeout; s_fail is final once every thread has passed the barrier
+    // below (the producer and MMA threads have left their loops).
     bool ok = mbar_wait(&done, 0);
     tc_fence_after();
+    ok = __syncthreads_and(ok && !s_fail);
     grid_dep_wait();   // the preceding kernel may still read the buffers written below
     const int r = warp * 32 + lane;   // tile row = TMEM lane
     if (p.ks == 1) {
@@ -293,9 +311,12 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
         for (int c = 0; c < p.R; c += 16) {
             float v[16];
             tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
-            if (row_ok && ok) store_v16(p, row, c, v);
+            if (!ok)
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = 0.f;
+            if (row_ok) store_v16(p, row, c, v);
         }
-        if (p.mode == 1 && row_ok && ok && p.r_pad64 > p.r_slot) zero_plane_padding(p, row);
+        if (p.mode == 1 && row_ok && p.r_pad64 > p.r_slot) zero_plane_padding(p, row);
     } else {
         // partial accumulator -> shared memory (over the consumed ring), row
         // pitch R + 4 floats: 16-byte stores from 8 consecutive rows meet no
@@ -309,9 +330,20 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
 #pragma unroll
             for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
         }
+        if (tid == 0) s_fail = ok ? 0 : 1;   // this CTA's partials are valid unless it failed
         __syncthreads();
         cluster_arrive();
         cluster_wait();
+        // a peer whose copies timed out has no valid partials: the whole
+        // tile then gets a zero intermediate
+        for (int peer = 0; peer < p.ks; ++peer) {
+            int f;
+            asm volatile("ld.shared::cluster.b32 %0, [%1];\n"
+                         : "=r"(f)
+                         : "r"(map_rank(smem_u32(const_cast<int*>(&s_fail)), peer))
+                         : "memory");
+            if (f) ok = false;
+        }
         // CTA c sums rows [c * 128 / ks, (c + 1) * 128 / ks) over the cluster,
         // 16 columns per item, peers in rank order
         const int r_lo = crank * kTileM / p.ks, r_hi = (crank + 1) * kTileM / p.ks;
@@ -331,9 +363,12 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
                     v[4 * i + 3] += f.w;
                 }
             }
-            if (rr < ti.nrows && ok) store_v16(p, static_cast<size_t>(ti.row0 + rr), c, v);
+            if (!ok)
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = 0.f;
+            if (rr < ti.nrows) store_v16(p, static_cast<size_t>(ti.row0 + rr), c, v);
         }
-        if (p.mode == 1 && ok && p.r_pad64 > p.r_slot)
+        if (p.mode == 1 && p.r_pad64 > p.r_slot)
             for (int rr = r_lo + tid; rr < min(r_hi, ti.nrows); rr += kShrinkThreads)
                 zero_plane_padding(p, static_cast<size_t>(ti.row0 + rr));
         cluster_arrive();   // peers may leave once everyone has read their partials
@@ -342,7 +377,7 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, ncols);
-    if (tid == 0 && (!ok || s_fail)) flag(p.status, LORA_DEV_TIMEOUT);
+    if (tid == 0 && !ok) flag(p.status, LORA_DEV_TIMEOUT);
     if (tid == 0 && ti.bad && blockIdx.x == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
 }
 
@@ -383,6 +418,7 @@ struct ExpandTcParams {
     int n_segs, n_pos, n_rows;
     bf16_t* y;
     int ld_y;
+    unsigned stall_tx;              // test hook: extra bytes expected on the first ring stage (0 normally)
     int32_t* status;
 };
 
@@ -553,6 +589,7 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
             TileIter tr;
             tr.init(p, n_rt);
             int k_prev = -1;
+            int issued = 0, v_issued = 0;   // ring stages and v slices armed so far
             for (int i = 0; !s_fail; ++i) {
                 const RowTile rt = s_rt[tr.k];
                 if (tr.k != k_prev) {   // a new item: its v slice into buffer k % VB
@@ -569,22 +606,34 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
                         tma_load_2d(vh + (kbs + kb) * kBoxBytes, &mvl, tr.q * p.r_pad64 + kb * kKB, rt.row0,
                                     &v_full[vb]);
                     }
+                    v_issued = tr.k + 1;
                 }
                 const int s = i % S;
                 if (i >= S && !mbar_wait(&empty[s], ((i / S) - 1) & 1)) {
                     s_fail = 1;
                     break;
                 }
+                // The epilogue releases a stage after a failure too (setting
+                // s_fail first): re-arm it only while nothing has failed, so a
+                // stage whose previous phase never completed is never armed again.
+                if (s_fail) break;
                 uint8_t* st = ring + s * stage_bytes;
                 const int col0 = tr.ct * kExpandN;
-                mbar_expect_tx(&full[s], stage_bytes);
+                mbar_expect_tx(&full[s], stage_bytes + (i == 0 ? p.stall_tx : 0u));
                 for (int kb = 0; kb < kbs; ++kb)
                     tma_load_2d(st + kb * kBoxBytes, bmap[tr.q], kb * kKB, rt.slot * p.width[tr.q] + col0, &full[s]);
                 const int ycol = p.out_off[tr.q] + col0;
                 tma_load_2d(st + kbs * kBoxBytes, &my, ycol, rt.row0, &full[s]);
                 tma_load_2d(st + (kbs + 1) * kBoxBytes, &my, ycol + kKB, rt.row0, &full[s]);
+                issued = i + 1;
                 if (!tr.next(p, n_rt, n_items)) break;
             }
+            // Every copy issued has landed before the CTA moves on (after a
+            // normal run the MMA thread has seen each of these phases complete).
+            for (int i = issued > S ? issued - S : 0; i < issued; ++i)
+                if (!mbar_wait(&full[i % S], (i / S) & 1)) s_fail = 1;
+            for (int k = v_issued > VB ? v_issued - VB : 0; k < v_issued; ++k)
+                if (!mbar_wait(&v_full[k % VB], (k / VB) & 1)) s_fail = 1;
         }
     } else if (warp == 1) {
         if (lane == 0) {   // ---- MMA issuer ----
@@ -782,6 +831,7 @@ cudaError_t launch_sgmv_shrink_tc(float* v, int ld_v, bf16_t* vh, bf16_t* vl, co
     p.r_pad64 = (ps.r_slot + kKB - 1) / kKB * kKB;
     p.ld_p = ps.n_proj * p.r_pad64;
     p.x_ready = (flags & LORA_APPLY_X_READY) ? 1 : 0;
+    p.stall_tx = test_stall_bytes(kStallShrinkTc);
     p.status = status;
     // Few row tiles: split K over a cluster of ks CTAs per tile so that the
     // grid covers the SMs (each CTA keeps at least two K blocks).
@@ -874,6 +924,7 @@ cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const b
     p.n_rows = n_rows;
     p.y = y;
     p.ld_y = ld_y;
+    p.stall_tx = test_stall_bytes(kStallExpandTc);
     p.status = status;
     const int kbs = r_pad64 / kKB;
     const int stages = kbs == 1 ? kStagesE : 2;
