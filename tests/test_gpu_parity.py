@@ -7,7 +7,8 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import check_bf16, oracle_adapters, oracle_group, shrink_bound, to_dev, to_host
+from helpers import (check_bf16, oracle_adapters, oracle_group, oracle_group_all_rows, shrink_bound, to_dev,
+                     to_host)
 from lora_serving_gb300 import abi, build, store, synth
 
 pytestmark = pytest.mark.gpu
@@ -160,32 +161,21 @@ def test_apply_full_workload(name, mode):
         check_bf16(got, ref, wl.ids, wl.y[g.name], f"{name}/{g.name}/{mode}")
 
 
-def _sample_rows(wl, n, seed):
-    rng = np.random.default_rng(seed)
-    rows = set(rng.choice(wl.n_rows, min(n, wl.n_rows), replace=False).tolist())
-    # every segment's first and last row (ragged tile edges)
-    pos = 0
-    for L in wl.seg_lens:
-        rows.update([pos, pos + L - 1])
-        pos += L
-    rows.update([0, wl.n_rows - 1])
-    return np.array(sorted(rows))
-
-
 @pytest.mark.parametrize("mode", ["delta", "accumulate"])
 @pytest.mark.parametrize("name", ["mistral7b_prefill", "stress70b"])
-def test_apply_full_size_sampled(name, mode):
+def test_apply_full_size_all_rows(name, mode):
     """Full sizes, all groups, in the launch configuration the benchmark
-    uses; the oracle recomputes a sample of rows one by one."""
+    uses (the tensor-core SGMV kernels for the prefill batch, the two-launch
+    grouped kernels for the stress batch): every element of every row is
+    compared with the oracle, which runs over row blocks on all host cores."""
     wl = _wl(name, mode)
-    rows = _sample_rows(wl, 48, 5)
     for g in wl.groups:
         got = _run_apply(wl, g.name)
-        ref = oracle_group(wl, g.name, rows)
-        check_bf16(got[rows], ref, wl.ids[rows], wl.y[g.name][rows], f"{name}/{g.name}/{mode}")
-        # rows that are base-only must be untouched everywhere, not just in the sample
-        base = wl.ids < 0
-        np.testing.assert_array_equal(got[base], wl.y[g.name][base])
+        ref = oracle_group_all_rows(wl, g.name)
+        r = check_bf16(got, ref, wl.ids, wl.y[g.name], f"{name}/{g.name}/{mode}")
+        assert r["n"] == int((wl.ids >= 0).sum()) * g.ld_y
+        print(f"{name}/{g.name}/{mode}: {r['n']} elements, rel-L2 {r['rel_l2']:.2e}, max-abs "
+              f"{r['max_abs']:.3g}, one bf16 step off where the step exceeds 3e-2: {r['n_big_step']}")
 
 
 # ---------------------------------------------------------- edge cases ----
