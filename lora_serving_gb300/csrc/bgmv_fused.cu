@@ -30,9 +30,10 @@
 //
 // Ordering (programmatic dependent launch): metadata and weights are read
 // before griddepcontrol.wait, so they stream in while the preceding kernel
-// on the stream is still running.  With LORA_APPLY_X_READY the shrink, the
-// cluster reduction and the delta are formed before the wait as well, and
-// only the read-modify-write of y follows it.
+// on the stream is still running, and the CTA's y lines are prefetched into
+// L2.  With LORA_APPLY_X_READY the shrink, the cluster reduction and the
+// delta are formed before the wait as well, and only the read-modify-write
+// of y follows it.
 
 #include <cstdlib>
 
@@ -271,6 +272,18 @@ bgmv_fused_kernel(FusedParams p)
     for (int st = 0; st < kStages; ++st) {
         if (st < n_kt) copy_A(st, st);
         cp_async_commit();
+    }
+    // The first tile's y lines go into L2 now: their addresses do not depend
+    // on the preceding kernel and L2 is coherent with its writes, so the
+    // read-modify-write after the grid dependency finds them there.  One
+    // request per 128-byte line of each row (a 16-byte piece never spans two).
+    {
+        const int nch0 = tile0_end - ch_begin;
+        for (int i = tid; i < nrows * nch0; i += kThreads) {
+            const int t = i / nch0, ci = i - t * nch0;
+            const bf16_t* yp = p.y + static_cast<size_t>(s_rows[t]) * p.ld_y + p.ps.out_off[s_cp[ci]] + s_ccol[ci];
+            if (ci == 0 || (reinterpret_cast<uintptr_t>(yp) & 127) == 0) prefetch_l2(yp);
+        }
     }
 
     bool waited = false;
