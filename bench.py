@@ -1,15 +1,20 @@
 #!/usr/bin/env python3
 """Benchmark of the multi-LoRA delta hot path on GB300.
 
-One step = one pass of the LoRA delta over every layer instance of the
-workload for one batch: for the default Llama-3.2-3B-shaped decode workload
-(64 decode tokens, 8 adapter slots of rank 16) that is 28 layers x
-(fused q/k/v call + o call) through ``lora_apply``, replayed as a CUDA graph.
-Throughput counts a token once per layer call: value = tokens x layers /
-step time, which equals tokens / (time of one layer's q/k/v + o delta).
+One step = one pass of the LoRA delta over every layer instance of a
+workload for one batch, replayed as a CUDA graph.  The default run measures
+all five workloads in one process: the headline line is the largest
+single-GPU one (Mistral-7B-shaped prefill, about 33.8k rows through the
+seven projections of one layer), and ``per_config`` carries the other four
+(tiny; Llama-3.2-3B-shaped decode as a 28-layer graph; the mixed continuous
+batch as a 32-layer graph; the 70B-shaped stress batch).  Throughput counts
+a token once per layer call: value = tokens x layers / step time.
 
-L2 honesty: the step's inputs (adapter stores, x, y) are replicated into
-enough rotating sets that consecutive steps touch more than 4x the L2 size.
+Timing: W untimed replays, then K timed replays with a CUDA event between
+consecutive replays; ``ms_per_step`` is the median replay (``ms_per_step_mean``
+the mean over the K).  L2 honesty: the step's inputs (adapter stores, x, y)
+are replicated into enough rotating sets that consecutive steps touch more
+than 4x the L2 size (one set suffices when a step alone is that large).
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 (plain fp64 C, the correctness reference) on a bounded sample instead.
@@ -34,8 +39,15 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "llama3b_decode"
-LAYERS = {"llama3b_decode": 28}  # Llama-3.2-3B has 28 decoder layers
+DEFAULT_WORKLOAD = "all"
+HEADLINE = "mistral7b_prefill"            # the largest workload that fits one GPU
+PER_CONFIG = ["tiny", "llama3b_decode", "mixed", "stress70b"]
+# layer instances per step: Llama-3.2-3B has 28 decoder layers; the mixed
+# batch is Mistral-7B-shaped (32 layers)
+LAYERS = {"llama3b_decode": 28, "mixed": 32}
+# workloads whose rows are decode tokens: their chain of calls is also timed
+# behind a base GEMM per call
+DECODE_WORKLOADS = ("llama3b_decode", "mixed")
 
 
 def parse_args(argv=None):
@@ -132,21 +144,22 @@ ROUTE_KERNELS = {
 
 # DRAM traffic per lora_apply call from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum over the call's launches), keyed by workload; per
-# step for the merge and linear-layer workloads; valid only while the listed
-# kernel sources hash to `src`.  Summaries in profiles/.
+# step for the merge and linear-layer workloads (linear_tc_kernel's launches
+# only for the linear layer); valid only while the listed kernel sources
+# hash to `src`.
 NCU_TRAFFIC = {
     "llama3b_decode": {"files": ['bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "010059f8745e9b90",
-             "bytes_per_call": 3438272},   # profiles/bgmv_fused_llama3b_decode.md
+             "bytes_per_call": 3438272},
     "stress70b": {"files": ['bgmv_grouped.cu', 'decode_common.cuh', 'common.cuh'], "src": "0d1b3c3b8322d136",
-             "bytes_per_call": 988209024},   # profiles/bgmv_grouped_stress70b.md
+             "bytes_per_call": 988209024},
     "mistral7b_prefill": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "e1e55b430f7ab83b",
-             "bytes_per_call": 2060608192},   # profiles/sgmv_tc_mistral7b_prefill.md
+             "bytes_per_call": 2060608192},
     "merge_mistral7b": {"files": ['merge.cu', 'decode_common.cuh', 'common.cuh'], "src": "64c410c3e24d8148",
-             "bytes_per_step": 6994841856},   # profiles/merge_mistral7b.md
+             "bytes_per_step": 6994841856},
     "linear_mistral7b_prefill": {"files": ['linear_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "f502730f1fa519ab",
-             "bytes_per_step": 19274225664},   # profiles/linear_tc_mistral7b_prefill.md (linear_tc_kernel only)
+             "bytes_per_step": 19274225664},
     "mixed": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "304df0d5fa9a8122",
-             "bytes_per_call": 113018240},   # profiles/sgmv_tc_mistral7b_prefill.md
+             "bytes_per_call": 113018240},
 }
 
 
@@ -221,6 +234,9 @@ class ClockSampler:
 
 # ------------------------------------------------------ CPU oracle ----
 
+_ORACLE_INPUTS = {}
+
+
 def cpu_oracle_rate(wl_name: str, budget_s: float, layers: int, single_core: bool = True):
     """Times the fp64 oracle (as it stands) on layer calls of the workload,
     rows split across all host cores; returns (tokens/s per layer call, info).
@@ -230,15 +246,20 @@ def cpu_oracle_rate(wl_name: str, budget_s: float, layers: int, single_core: boo
     import oracle as O
     from lora_serving_gb300 import synth
 
-    wl = synth.get(wl_name).materialise("delta")
     cores = os.cpu_count() or 1
-    ads = {}
-    for g in wl.groups:
-        for pname, _ in g.projs:
-            A = [wl.A[(g.name, pname, k)] for k in range(wl.n_slots)]
-            B = [wl.B[(g.name, pname, k)] for k in range(wl.n_slots)]
-            sc = [O.scale(float(wl.alphas[k]), int(wl.ranks[k]), bool(wl.rslora[k])) for k in range(wl.n_slots)]
-            ads[(g.name, pname)] = O.Adapters(A, B, sc)
+    if _ORACLE_INPUTS.get("name") != wl_name:   # inputs drawn once per workload, outside the timing
+        wl = synth.get(wl_name).materialise("delta")
+        ads = {}
+        for g in wl.groups:
+            for pname, _ in g.projs:
+                A = [wl.A[(g.name, pname, k)] for k in range(wl.n_slots)]
+                B = [wl.B[(g.name, pname, k)] for k in range(wl.n_slots)]
+                sc = [O.scale(float(wl.alphas[k]), int(wl.ranks[k]), bool(wl.rslora[k]))
+                      for k in range(wl.n_slots)]
+                ads[(g.name, pname)] = O.Adapters(A, B, sc)
+        _ORACLE_INPUTS.clear()
+        _ORACLE_INPUTS.update(name=wl_name, wl=wl, ads=ads)
+    wl, ads = _ORACLE_INPUTS["wl"], _ORACLE_INPUTS["ads"]
     # rows per layer call: all of them for small batches, a row block for large ones
     T = wl.n_rows
     blocks = np.array_split(np.arange(T), min(T, cores)) if T else []
@@ -823,23 +844,42 @@ class Instance:
         return n
 
 
-def run_ours(args, rank, local, ws):
+def time_replays(run_step, steps, warm, ws):
+    """W untimed steps, then K timed ones with a CUDA event between
+    consecutive steps, bracketed by a barrier and a synchronise on both
+    sides.  Returns (total ms, per-step ms list)."""
     import torch
-    from lora_serving_gb300 import abi, build, store, synth
-
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if rank == 0:
-        build()
+    for i in range(warm):
+        run_step(i)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     barrier(ws)
-    build()
-    lib = abi.load()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    ev[0].record(cur)
+    for i in range(steps):
+        run_step(warm + i)
+        ev[i + 1].record(cur)
+    torch.cuda.synchronize()
+    barrier(ws)
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    return ev[0].elapsed_time(ev[steps]), per
+
+
+def measure_delta(name, args, rank, local, ws, *, with_e2e=True, cpu_seconds=None, layers=None,
+                  sample_clocks=True):
+    """The LoRA delta of one workload through lora_apply: one line's worth of
+    figures (value, roofline, orderings, clocks, and optionally e2e and the
+    oracle's host rate)."""
+    import torch
+    from lora_serving_gb300 import abi, store, synth
+
+    dev = torch.device("cuda", local)
 
     def to_dev(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
 
-    name = args.workload
-    layers = args.layers or LAYERS.get(name, 1)
+    layers = layers or LAYERS.get(name, 1)
     base = synth.get(name)
     # host inputs of every layer instance (weights differ per layer)
     host = []
@@ -854,12 +894,14 @@ def run_ours(args, rank, local, ws):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     n_sets = max(1, math.ceil(4 * l2 / set_bytes))
     sets = [inst0] + [[Instance(h, store, to_dev) for h in host] for _ in range(n_sets - 1)]
+    if not with_e2e:
+        host = None
 
     calls_per_step = layers * len(base.groups)
 
     # Dependency model of the timed step: each call's y is treated as the
     # output of the kernel just before it (as the base GEMM's output is in a
-    # model layer) and x as produced earlier (LORA_APPLY_X_READY).  The two
+    # model layer) and x as produced earlier (LORA_APPLY_X_READY).  The
     # other orderings are timed too and reported beside the headline.
     variants = {"x_ready": abi.LORA_APPLY_X_READY, "default": 0, "no_pdl": abi.LORA_APPLY_NO_PDL,
                 "independent": abi.LORA_APPLY_X_READY | abi.LORA_APPLY_Y_READY}
@@ -887,45 +929,41 @@ def run_ours(args, rank, local, ws):
     launches_per_step = (abi.lora_kernel_launch_count() - l0) // (n_sets * len(variants))
     torch.cuda.synchronize()
 
-    def timed(gs, steps, warm):
-        for i in range(warm):
-            gs[i % n_sets].replay()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        barrier(ws)
-        torch.cuda.synchronize()
-        cur = torch.cuda.current_stream()
-        e0.record(cur)
-        for i in range(steps):
-            gs[(warm + i) % n_sets].replay()
-        e1.record(cur)
-        torch.cuda.synchronize()
-        barrier(ws)
-        return e0.elapsed_time(e1)
+    def replay(gs):
+        return lambda i: gs[i % n_sets].replay()
 
     other = {}
+    n_other = max(10, args.steps // 2)
     for name_v in ("default", "no_pdl", "independent"):
-        n_v = max(10, args.steps // 4)
-        other[name_v] = round(timed(graphs[name_v], n_v, args.warmup) / n_v, 5)
+        _, per = time_replays(replay(graphs[name_v]), n_other, args.warmup, ws)
+        other[name_v] = round(statistics.median(per), 5)
+    del graphs["default"], graphs["no_pdl"], graphs["independent"]
 
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    ms_local = timed(graphs["x_ready"], args.steps, args.warmup)
-    clk = clocks.stop()
-    ms = max_over_ranks(ms_local, ws, device=dev if ws > 1 else "cpu")
-    ms_per_step = ms / args.steps
+    # A model layer puts a base GEMM (x W^T, here cuBLAS) before each delta:
+    # the chain timed with and without the delta gives the delta's marginal
+    # cost per call behind a kernel that does not start it early.
+    gemm_ctx = floor = None
+    if name in DECODE_WORKLOADS:
+        gemm_ctx = gemm_chain(base, sets[0], meta, ws_buf, store, abi, dev, args, ws, stream)
+        floor = y_rmw_chain(base, sets, n_sets, args, ws, stream)
+
+    clocks = ClockSampler(local) if sample_clocks else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    total_ms, per = time_replays(replay(graphs["x_ready"]), args.steps, args.warmup, ws)
+    clk = clocks.stop() if clocks else None
+    med_local = statistics.median(per)
+    med = max_over_ranks(med_local, ws, device=dev if ws > 1 else "cpu")
     tokens = base.n_rows
-    units_local = tokens * layers * args.steps
-    units = sum_over_ranks(units_local, ws, device=dev if ws > 1 else "cpu")
-    value = units / (ms / 1e3)
+    units = sum_over_ranks(float(tokens * layers), ws, device=dev if ws > 1 else "cpu")
+    value = units / (med / 1e3)
 
     # roofline of the delta: every launch in the step belongs to a lora_apply
-    # call; algorithmic bytes per call / the call's share of the timed region
+    # call; algorithmic bytes per call / the call's share of the step
     bytes_call = [algorithmic_bytes(base, g) for g in base.groups]
     bytes_per_call = sum(bytes_call) / len(bytes_call)
-    call_ms = ms_local / (args.steps * calls_per_step)
+    call_ms = med_local / calls_per_step
     achieved = bytes_per_call / (call_ms / 1e3) / 1e9
     peak, peak_kind = peaks()
     tr = NCU_TRAFFIC.get(name)
@@ -934,15 +972,18 @@ def run_ours(args, rank, local, ws):
     out = {
         "metric": "SGMV/BGMV LoRA-delta tokens/s (token x layer calls per second)",
         "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)", "data": "synthetic",
+        "warmup": args.warmup, "ms_per_step": round(med, 5),
+        "ms_per_step_mean": round(max_over_ranks(total_ms, ws, device=dev if ws > 1 else "cpu") / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)",
+        "data": "synthetic",
         "config": {
             "workload": name, "tokens": tokens, "n_prefill": base.n_prefill, "layers": layers,
             "groups": {g.name: [w for _, w in g.projs] for g in base.groups},
             "hidden": base.groups[0].h_in, "n_slots": base.n_slots, "r_slot": base.r_slot,
             "active_rows": int((base.ids >= 0).sum()),
-            "l2": f"{n_sets} rotating input sets x {set_bytes / 1e6:.0f} MB (L2 {l2 / 1e6:.0f} MB)",
-            "timing": "CUDA graph of the step replayed; CUDA events on the launching stream",
+            "l2": f"{n_sets} rotating input set(s) x {set_bytes / 1e6:.0f} MB (L2 {l2 / 1e6:.0f} MB)",
+            "timing": "CUDA graph of the step replayed; a CUDA event between replays on the launching stream; "
+                      "median replay",
             "dependency": "x_ready: each call's y treated as the preceding kernel's output, x as earlier",
             "ms_per_step_other_orderings": other,
             "parallelism": f"replicas x{ws}",
@@ -958,16 +999,133 @@ def run_ours(args, rank, local, ws):
         "clocks": clk,
         "gpu_launches": launches_per_step * args.steps,
     }
+    if gemm_ctx:
+        out["config"]["behind_base_gemm"] = gemm_ctx
+    if floor:
+        out["config"]["chain_floor"] = floor
 
-    if not args.no_e2e:
+    if with_e2e:
         out["e2e"] = run_e2e(args, base, host, sets[0], meta, ws_buf, store, dev, layers)
 
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        rate, info = cpu_oracle_rate(name, args.cpu_seconds, layers)
+    if rank == 0 and ws == 1 and cpu_seconds:
+        rate, info = cpu_oracle_rate(name, cpu_seconds, layers)
         out["cpu_baseline"] = {"value": round(rate, 2), "unit": "tokens/s", "cores": info["cores"],
                                "kind": "oracle", "sample": info["sample"],
                                "single_core_value": info["single_core_value"], "cpu_model": info["cpu_model"]}
+    del sets, inst0, graphs, ws_buf
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     return out
+
+
+def gemm_chain(base, inst, meta, ws_buf, store, abi, dev, args, ws, stream):
+    """Each layer call behind a base GEMM that writes its y (cuBLAS, x W^T):
+    the step with the GEMMs alone, and with lora_apply (X_READY) after each
+    GEMM.  The difference per call is the delta's marginal cost in a layer."""
+    import torch
+    g_w = torch.Generator(device=dev).manual_seed(11)
+    Ws = [{g.name: (torch.randn(g.ld_y, g.h_in, generator=g_w, device=dev) / math.sqrt(g.h_in)).to(torch.bfloat16)
+           for g in base.groups} for _ in inst]
+
+    def step(with_delta):
+        for li, it in enumerate(inst):
+            for g in base.groups:
+                torch.matmul(it.x[g.name], Ws[li][g.name].t(), out=it.y[g.name])
+                if with_delta:
+                    store.apply(it.y[g.name], it.x[g.name], it.stores[g.name], meta, ws_buf[g.name],
+                                flags=abi.LORA_APPLY_X_READY)
+
+    graphs = {}
+    for key in (False, True):
+        with torch.cuda.stream(stream):
+            step(key)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            step(key)
+        graphs[key] = gr
+    n = max(10, args.steps // 2)
+    _, per0 = time_replays(lambda i: graphs[False].replay(), n, args.warmup, ws)
+    _, per1 = time_replays(lambda i: graphs[True].replay(), n, args.warmup, ws)
+    calls = len(inst) * len(base.groups)
+    t0, t1 = statistics.median(per0), statistics.median(per1)
+    del graphs, Ws
+    return {"ms_per_step_gemm_only": round(t0, 5), "ms_per_step_gemm_then_delta": round(t1, 5),
+            "delta_us_per_call": round((t1 - t0) / calls * 1e3, 3),
+            "note": "cuBLAS x W^T writes y, then lora_apply (X_READY) adds the delta; weights of "
+                    f"{len(inst)} layer instance(s), one input set"}
+
+
+def y_rmw_chain(base, sets, n_sets, args, ws, stream):
+    """Context for a chain of dependent calls: the same step with each call
+    replaced by one plain torch kernel that reads and writes the call's y
+    (y *= 1, in place) -- what any design with one kernel per call pays
+    before it does any LoRA work."""
+    import torch
+
+    def step(s):
+        for inst in sets[s]:
+            for g in base.groups:
+                inst.y[g.name].mul_(1)
+
+    graphs = []
+    for s in range(n_sets):
+        with torch.cuda.stream(stream):
+            step(s)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            step(s)
+        graphs.append(gr)
+    n = max(10, args.steps // 2)
+    _, per = time_replays(lambda i: graphs[i % n_sets].replay(), n, args.warmup, ws)
+    calls = len(sets[0]) * len(base.groups)
+    t = statistics.median(per)
+    del graphs
+    return {"ms_per_step_y_rmw_only": round(t, 5), "us_per_call": round(t / calls * 1e3, 3),
+            "note": "each call replaced by torch's in-place y *= 1 over the call's whole y (all rows): "
+                    "a dependent chain of one plain read-modify-write kernel per call"}
+
+
+def run_all(args, rank, local, ws):
+    """The default line: the headline workload in full (e2e, oracle
+    baseline), the other four workloads in per_config."""
+    import torch
+    from lora_serving_gb300 import abi, build
+    torch.cuda.set_device(local)
+    if rank == 0:
+        build()
+    barrier(ws)
+    build()
+    abi.load()
+    cpu = None if args.no_cpu_baseline else args.cpu_seconds
+    out = measure_delta(HEADLINE, args, rank, local, ws, with_e2e=not args.no_e2e, cpu_seconds=cpu)
+    per = {}
+    keep = ("value", "unit", "ms_per_step", "ms_per_step_mean", "roofline", "clocks", "gpu_launches",
+            "cpu_baseline")
+    for name in PER_CONFIG:
+        line = measure_delta(name, args, rank, local, ws, with_e2e=False,
+                             cpu_seconds=None if cpu is None else max(1.0, cpu / 4))
+        d = {k: line[k] for k in keep if k in line}
+        d["config"] = line["config"]
+        per[name] = d
+    out["per_config"] = per
+    out["gpu_launches"] = out["gpu_launches"] + sum(d["gpu_launches"] for d in per.values())
+    out["gpu_launches_note"] = "timed launches of the headline and of every per_config line"
+    return out
+
+
+def run_ours(args, rank, local, ws):
+    import torch
+    from lora_serving_gb300 import abi, build
+    torch.cuda.set_device(local)
+    if rank == 0:
+        build()
+    barrier(ws)
+    build()
+    abi.load()
+    return measure_delta(args.workload, args, rank, local, ws, with_e2e=not args.no_e2e,
+                         cpu_seconds=None if args.no_cpu_baseline else args.cpu_seconds, layers=args.layers)
 
 
 def run_e2e(args, base, host, inst, meta, ws_buf, store, dev, layers):
@@ -1068,7 +1226,7 @@ def run_reference(args, rank, ws):
     """The CPU oracle timed on the machine's host cores, as the reference arm."""
     if rank != 0:
         return None
-    name = args.workload
+    name = HEADLINE if args.workload == "all" else args.workload
     layers = args.layers or LAYERS.get(name, 1)
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
     if name == SLOTS_WORKLOAD:
@@ -1178,6 +1336,8 @@ def main(argv=None):
         out = run_linear(args, rank, local, ws)
     elif args.workload == SLOTS_WORKLOAD:
         out = run_slots(args, rank, local, ws)
+    elif args.workload == "all":
+        out = run_all(args, rank, local, ws)
     else:
         out = run_ours(args, rank, local, ws)
     if rank == 0:
