@@ -135,8 +135,12 @@ lora_status_t lora_bgmv_expand(lora_bf16_t* y, int ld_y, int y_off, int width,
  * seg_slot   [dev] int32 [n_segs]
  * row_perm   [dev] int32 [n_pos] or NULL; every entry in [0, n_rows)
  * n_rows     rows of x / v (bounds for the row indices)
- * max_seg_len  [host] an upper bound on the longest segment (0 = unknown);
- *              only used to pick the kernel variant.
+ * max_seg_len  [host] an upper bound on the longest segment (0 = unknown).
+ *              It picks the kernel form (tensor cores for contiguous
+ *              segments of 64 rows or more; otherwise, for r_slot <= 64, the
+ *              grouped kernels, whose grid it sizes: a value below the true
+ *              longest segment leaves rows without their result and sets
+ *              LORA_DEV_BAD_SEGMENT).
  */
 lora_status_t lora_sgmv_shrink(float* v, int ld_v, const lora_bf16_t* x, int ld_x,
                                const lora_bf16_t* A, const int32_t* seg_starts,
@@ -147,7 +151,8 @@ lora_status_t lora_sgmv_shrink(float* v, int ld_v, const lora_bf16_t* x, int ld_
 /*
  * SGMV expand: for every row covered by a segment with slot >= 0,
  *   y[row][y_off+c] = bf16_rne( y[row][y_off+c] + sum_j B[slot][c][j] * v[row][j] )
- * Arguments as in lora_sgmv_shrink and lora_bgmv_expand.
+ * Arguments as in lora_sgmv_shrink and lora_bgmv_expand (max_seg_len sizes
+ * the grouped kernels' grid for r_slot <= 64, as in lora_sgmv_shrink).
  */
 lora_status_t lora_sgmv_expand(lora_bf16_t* y, int ld_y, int y_off, int width,
                                const float* v, int ld_v, const lora_bf16_t* B,

@@ -200,6 +200,13 @@ lora_status_t lora_sgmv_shrink(float* v, int ld_v, const lora_bf16_t* x, int ld_
         return cuda_status(lora::launch_sgmv_shrink_tc(v, ld_v, nullptr, nullptr, x, ld_x, h_in, ps, seg_starts,
                                                        seg_slot, n_segs, n_pos, n_rows, n_slots, LORA_APPLY_NO_PDL,
                                                        dev_status, reinterpret_cast<cudaStream_t>(stream)));
+    // Short segments and gathered rows: the segments as groups of the
+    // grouped shrink (units of 16 rows, each adapter's A streamed once per
+    // unit), for ranks the grouped kernels take.
+    if (r_slot <= 64)
+        return cuda_status(lora::launch_group_shrink_f32(v, ld_v, x, ld_x, h_in, ps, row_perm, seg_starts, seg_slot,
+                                                         n_segs, n_pos, max_seg_len, n_rows, n_slots, dev_status,
+                                                         reinterpret_cast<cudaStream_t>(stream)));
     RowMap m = seg_map(seg_starts, seg_slot, n_segs, row_perm, n_pos, n_rows, n_slots);
     return cuda_status(lora::launch_shrink_rowwise(v, ld_v, x, ld_x, h_in, ps, m, dev_status,
                                                    reinterpret_cast<cudaStream_t>(stream)));
@@ -212,7 +219,6 @@ lora_status_t lora_sgmv_expand(lora_bf16_t* y, int ld_y, int y_off, int width,
                                int r_slot, int n_slots, int32_t* dev_status,
                                lora_stream_t stream)
 {
-    (void)max_seg_len;
     LORA_TRY(check_common(n_rows, r_slot, n_slots));
     LORA_TRY(check_segments(seg_starts, seg_slot, n_segs, n_pos, n_rows, row_perm));
     if (n_pos == 0) return LORA_OK;
@@ -220,6 +226,12 @@ lora_status_t lora_sgmv_expand(lora_bf16_t* y, int ld_y, int y_off, int width,
     LORA_TRY(check_store(B));
     LORA_TRY(check_v(v, ld_v, r_slot));
     ProjSet ps = single_proj(nullptr, B, y_off, width, r_slot);
+    // The segments as groups of the grouped expand (each unit's B' columns
+    // brought by bulk copies, the tensor cores on v split hi/lo).
+    if (r_slot <= 64)
+        return cuda_status(lora::launch_group_expand_f32(y, ld_y, v, ld_v, ps, row_perm, seg_starts, seg_slot, n_segs,
+                                                         n_pos, max_seg_len, n_rows, n_slots, dev_status,
+                                                         reinterpret_cast<cudaStream_t>(stream)));
     RowMap m = seg_map(seg_starts, seg_slot, n_segs, row_perm, n_pos, n_rows, n_slots);
     return cuda_status(lora::launch_expand_rowwise(y, ld_y, v, ld_v, ps, m, dev_status,
                                                    reinterpret_cast<cudaStream_t>(stream)));
@@ -319,6 +331,12 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
             LORA_TRY(cuda_status(lora::launch_sgmv_expand_tc(y, ld_y, vh, vl, ps, meta->seg_starts,
                                                              meta->seg_slot, meta->n_segs, P, T, n_slots, flags,
                                                              dev_status, s)));
+        } else if (r_slot <= 64) {
+            // short segments: the segments as groups of the grouped pair (no
+            // permutation: a segment's positions are its rows)
+            LORA_TRY(cuda_status(lora::launch_bgmv_grouped(y, ld_y, x, ld_x, h_in, ps, nullptr, meta->seg_starts,
+                                                           meta->seg_slot, meta->n_segs, P, meta->max_seg_len, T,
+                                                           n_slots, flags, vh, vl, dev_status, s)));
         } else {
             RowMap m = seg_map(meta->seg_starts, meta->seg_slot, meta->n_segs, nullptr, P, T, n_slots);
             LORA_TRY(cuda_status(lora::launch_shrink_rowwise(v, R, x, ld_x, h_in, ps, m, dev_status, s)));

@@ -53,7 +53,8 @@ using namespace dec;
 
 // Unit u of the grid.  Direct form (upg > 0): u = group * upg + sub, rows
 // [gstarts[group] + 16 sub, ...): one round trip, no block-wide scan; a
-// group whose bounds are not sane is reported by its first unit.  Scanned
+// group whose bounds are not sane is reported by its first unit, and a
+// table that does not cover [0, n_pos) by unit 0.  Scanned
 // form (upg == 0): units are numbered over all groups by a prefix sum.
 template <int NT, class Params>
 __device__ __forceinline__ UnitInfo grouped_unit(const Params& p, int u, int grid_units)
@@ -65,7 +66,9 @@ __device__ __forceinline__ UnitInfo grouped_unit(const Params& p, int u, int gri
         const int s = __ldg(p.gstarts + ui.g), e = __ldg(p.gstarts + ui.g + 1);
         ui.slot = __ldg(p.gslot + ui.g);
         const bool sane = s >= 0 && e <= p.n_pos && s <= e && e - s <= p.upg * kRB;
-        ui.bad = !sane && sub == 0;
+        // the first unit also checks that the table covers [0, n_pos)
+        const bool covers = u != 0 || (__ldg(p.gstarts) == 0 && __ldg(p.gstarts + p.n_groups) == p.n_pos);
+        ui.bad = (!sane && sub == 0) || !covers;
         ui.pos0 = s + sub * kRB;
         ui.nrows = sane ? min(kRB, e - ui.pos0) : 0;
         ui.found = ui.nrows > 0;
@@ -114,6 +117,8 @@ struct GsParams {
     bf16_t* vl;
     int ld_p;
     int r_pad64;
+    float* v;                 // or, when not null, fp32 v [n_rows][ld_v] (rank j at column j)
+    int ld_v;
     const int32_t* perm;
     const int32_t* gstarts;
     const int32_t* gslot;
@@ -316,9 +321,13 @@ bgmv_group_shrink_kernel(GsParams p)
     }
     if (!waited) grid_dep_wait();   // v may still be read by the preceding grid
     const int t = tid >> 4, j = tid & 15;
-    // v (fp32) is stored split: vh = bf16(v), vl = bf16(v - vh), exact in fp32
+    // v (fp32) is stored as it is, or split: vh = bf16(v), vl = bf16(v - vh), exact in fp32
     auto store_v = [&](float v) {
         const int jr = j0 + j, pj = jr / r_slot, jj = jr - pj * r_slot;
+        if (p.v) {
+            p.v[static_cast<size_t>(s_rows[t]) * p.ld_v + jr] = v;
+            return;
+        }
         const size_t off = static_cast<size_t>(s_rows[t]) * p.ld_p + pj * p.r_pad64 + jj;
         const __nv_bfloat16 hi = __float2bfloat16_rn(v);
         p.vh[off] = __bfloat16_as_ushort(hi);
@@ -359,6 +368,8 @@ struct GexParams {
     const bf16_t* vl;
     int ld_p;
     int r_pad64;
+    const float* v;           // or, when not null, fp32 v [n_rows][ld_v], projection p at p*r_slot,
+    int ld_v;                 //   split into the same hi/lo parts as it is read
     bf16_t* y;
     int ld_y;
     const int32_t* perm;
@@ -475,9 +486,16 @@ bgmv_group_expand_kernel(GexParams p)
                 const int t = nt * 8 + g, k0 = 8 * (q + 4 * h) + 4 * e;
                 uint2 hv = make_uint2(0, 0), lv = make_uint2(0, 0);
                 if (nt < n_nt && t < nrows && k0 < r_slot) {
-                    const size_t off = static_cast<size_t>(s_rows[t]) * p.ld_p + pj * p.r_pad64 + k0;
-                    hv = *reinterpret_cast<const uint2*>(p.vh + off);
-                    lv = *reinterpret_cast<const uint2*>(p.vl + off);
+                    if (p.v) {
+                        const float4 f = *reinterpret_cast<const float4*>(
+                            p.v + static_cast<size_t>(s_rows[t]) * p.ld_v + pj * r_slot + k0);
+                        split_hi_lo(f.x, f.y, hv.x, lv.x);
+                        split_hi_lo(f.z, f.w, hv.y, lv.y);
+                    } else {
+                        const size_t off = static_cast<size_t>(s_rows[t]) * p.ld_p + pj * p.r_pad64 + k0;
+                        hv = *reinterpret_cast<const uint2*>(p.vh + off);
+                        lv = *reinterpret_cast<const uint2*>(p.vl + off);
+                    }
                 }
                 bh[nt][h][e][0] = hv.x;
                 bh[nt][h][e][1] = hv.y;
@@ -602,10 +620,11 @@ cudaError_t grouped_plan(const ProjSet& ps, int n_groups, int n_pos, int max_gro
     return cudaSuccess;
 }
 
+// v goes to the planes vh/vl, or as fp32 to v (ld_v) when v is not null.
 cudaError_t grouped_shrink(const GroupedPlan& g, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
                            const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
                            int n_pos, int n_rows, int n_slots, unsigned flags, bf16_t* vh, bf16_t* vl,
-                           int32_t* status, cudaStream_t stream)
+                           float* v, int ld_v, int32_t* status, cudaStream_t stream)
 {
     const int R = ps.n_proj * ps.r_slot;
     GsParams sp{};
@@ -615,6 +634,8 @@ cudaError_t grouped_shrink(const GroupedPlan& g, const bf16_t* x, int ld_x, int 
     sp.h_in = h_in;
     sp.vh = vh;
     sp.vl = vl;
+    sp.v = v;
+    sp.ld_v = ld_v;
     sp.ld_p = g.ld_p;
     sp.r_pad64 = g.r_pad64;
     sp.perm = perm;
@@ -664,6 +685,49 @@ cudaError_t grouped_shrink(const GroupedPlan& g, const bf16_t* x, int ld_x, int 
     return e;
 }
 
+// v from the planes vh/vl, or as fp32 from v (ld_v) when v is not null.
+cudaError_t grouped_expand(const GroupedPlan& g, bf16_t* y, int ld_y, const ProjSet& ps, const int32_t* perm,
+                           const int32_t* gstarts, const int32_t* gslot, int n_groups, int n_pos, int n_rows,
+                           int n_slots, const bf16_t* vh, const bf16_t* vl, const float* v, int ld_v,
+                           int32_t* status, cudaStream_t stream)
+{
+    GexParams gp{};
+    gp.ps = ps;
+    gp.vh = vh;
+    gp.vl = vl;
+    gp.ld_p = g.ld_p;
+    gp.r_pad64 = g.r_pad64;
+    gp.v = v;
+    gp.ld_v = ld_v;
+    gp.y = y;
+    gp.ld_y = ld_y;
+    gp.perm = perm;
+    gp.gstarts = gstarts;
+    gp.gslot = gslot;
+    gp.n_groups = n_groups;
+    gp.n_pos = n_pos;
+    gp.n_slots = n_slots;
+    gp.n_rows = n_rows;
+    for (int q = 0; q < ps.n_proj; ++q) gp.n_blocks += (ps.width[q] + kGxCols - 1) / kGxCols;
+    gp.upg = g.form_upg;
+    gp.status = status;
+    const long long n_expand = g.units * gp.n_blocks;
+    if (n_expand > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t gcfg = {};
+    gcfg.gridDim = dim3(static_cast<unsigned>(n_expand));
+    gcfg.blockDim = dim3(kGxThreads);
+    gcfg.dynamicSmemBytes = sizeof(bf16_t) * kGxCols * ps.r_slot;   // <= 32 KB
+    gcfg.stream = stream;
+    cudaLaunchAttribute gattr;
+    gattr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    gattr.val.programmaticStreamSerializationAllowed = 1;
+    gcfg.attrs = &gattr;
+    gcfg.numAttrs = g.pdl;
+    const cudaError_t e = cudaLaunchKernelEx(&gcfg, bgmv_group_expand_kernel, gp);
+    note_launch();
+    return e;
+}
+
 }  // namespace
 
 cudaError_t launch_bgmv_grouped_shrink(const bf16_t* x, int ld_x, int h_in, const ProjSet& ps, const int32_t* perm,
@@ -677,7 +741,7 @@ cudaError_t launch_bgmv_grouped_shrink(const bf16_t* x, int ld_x, int h_in, cons
     const cudaError_t e = grouped_plan(ps, n_groups, n_pos, max_group_len, flags, g);
     if (e != cudaSuccess) return e;
     return grouped_shrink(g, x, ld_x, h_in, ps, perm, gstarts, gslot, n_groups, n_pos, n_rows, n_slots, flags, vh,
-                          vl, status, stream);
+                          vl, nullptr, 0, status, stream);
 }
 
 cudaError_t launch_bgmv_grouped(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
@@ -691,45 +755,38 @@ cudaError_t launch_bgmv_grouped(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, 
     cudaError_t e = grouped_plan(ps, n_groups, n_pos, max_group_len, flags, g);
     if (e != cudaSuccess) return e;
     e = grouped_shrink(g, x, ld_x, h_in, ps, perm, gstarts, gslot, n_groups, n_pos, n_rows, n_slots, flags, vh, vl,
-                       status, stream);
+                       nullptr, 0, status, stream);
     if (e != cudaSuccess) return e;
-    const int r_pad64 = g.r_pad64, ld_p = g.ld_p, form_upg = g.form_upg, pdl = g.pdl;
-    const long long units = g.units;
+    return grouped_expand(g, y, ld_y, ps, perm, gstarts, gslot, n_groups, n_pos, n_rows, n_slots, vh, vl, nullptr, 0,
+                          status, stream);
+}
 
-    // ---- grouped expand ----
-    GexParams gp{};
-    gp.ps = ps;
-    gp.vh = vh;
-    gp.vl = vl;
-    gp.ld_p = ld_p;
-    gp.r_pad64 = r_pad64;
-    gp.y = y;
-    gp.ld_y = ld_y;
-    gp.perm = perm;
-    gp.gstarts = gstarts;
-    gp.gslot = gslot;
-    gp.n_groups = n_groups;
-    gp.n_pos = n_pos;
-    gp.n_slots = n_slots;
-    gp.n_rows = n_rows;
-    for (int q = 0; q < ps.n_proj; ++q) gp.n_blocks += (ps.width[q] + kGxCols - 1) / kGxCols;
-    gp.upg = form_upg;
-    gp.status = status;
-    const long long n_expand = units * gp.n_blocks;
-    if (n_expand > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
-    cudaLaunchConfig_t gcfg = {};
-    gcfg.gridDim = dim3(static_cast<unsigned>(n_expand));
-    gcfg.blockDim = dim3(kGxThreads);
-    gcfg.dynamicSmemBytes = sizeof(bf16_t) * kGxCols * ps.r_slot;   // <= 32 KB
-    gcfg.stream = stream;
-    cudaLaunchAttribute gattr;
-    gattr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    gattr.val.programmaticStreamSerializationAllowed = 1;
-    gcfg.attrs = &gattr;
-    gcfg.numAttrs = pdl;
-    e = cudaLaunchKernelEx(&gcfg, bgmv_group_expand_kernel, gp);
-    note_launch();
-    return e;
+cudaError_t launch_group_shrink_f32(float* v, int ld_v, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
+                                    const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
+                                    int n_pos, int max_group_len, int n_rows, int n_slots, int32_t* status,
+                                    cudaStream_t stream)
+{
+    if (n_pos <= 0 || n_groups <= 0) return cudaSuccess;
+    if (!v || ps.r_slot > 64 || ps.r_slot % 8 != 0) return cudaErrorInvalidValue;
+    GroupedPlan g{};
+    const cudaError_t e = grouped_plan(ps, n_groups, n_pos, max_group_len, LORA_APPLY_NO_PDL, g);
+    if (e != cudaSuccess) return e;
+    return grouped_shrink(g, x, ld_x, h_in, ps, perm, gstarts, gslot, n_groups, n_pos, n_rows, n_slots,
+                          LORA_APPLY_NO_PDL, nullptr, nullptr, v, ld_v, status, stream);
+}
+
+cudaError_t launch_group_expand_f32(bf16_t* y, int ld_y, const float* v, int ld_v, const ProjSet& ps,
+                                    const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
+                                    int n_pos, int max_group_len, int n_rows, int n_slots, int32_t* status,
+                                    cudaStream_t stream)
+{
+    if (n_pos <= 0 || n_groups <= 0) return cudaSuccess;
+    if (!v || ps.r_slot > 64 || ps.r_slot % 8 != 0) return cudaErrorInvalidValue;
+    GroupedPlan g{};
+    const cudaError_t e = grouped_plan(ps, n_groups, n_pos, max_group_len, LORA_APPLY_NO_PDL, g);
+    if (e != cudaSuccess) return e;
+    return grouped_expand(g, y, ld_y, ps, perm, gstarts, gslot, n_groups, n_pos, n_rows, n_slots, nullptr, nullptr,
+                          v, ld_v, status, stream);
 }
 
 }  // namespace lora

@@ -148,7 +148,8 @@ struct UnitInfo {
 // cluster, whose CTAs all map to the same unit).  The group table is read
 // NT groups per round trip (one group per thread, block-wide prefix sum),
 // together with the permutation when it fits in s_perm.  `bad` is set for
-// a malformed table, and when the table holds more units than the grid's
+// a malformed table (a group outside [0, n_pos), or a table that does not
+// start at 0 and end at n_pos), and when the table holds more units than the grid's
 // grid_units (the host's bound on the longest group was understated, so
 // some rows have no CTA): every CTA sees the same total and reports it.
 template <int NT, class Params>
@@ -160,7 +161,8 @@ __device__ __forceinline__ UnitInfo find_unit(const Params& p, int u, int* s_per
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
         s_info.found = 0;
-        s_bad = 0;
+        // the table must cover [0, n_pos): its first entry 0, its last n_pos
+        s_bad = p.n_groups > 0 && (__ldg(p.gstarts) != 0 || __ldg(p.gstarts + p.n_groups) != p.n_pos);
     }
     if (stage_perm)
         for (int i = tid; i < p.n_pos; i += NT) s_perm[i] = __ldg(p.perm + i);

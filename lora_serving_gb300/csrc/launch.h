@@ -82,6 +82,17 @@ cudaError_t launch_bgmv_grouped_shrink(const bf16_t* x, int ld_x, int h_in, cons
                                        int max_group_len, int n_rows, int n_slots, unsigned flags, bf16_t* vh,
                                        bf16_t* vl, int32_t* status, cudaStream_t stream);
 
+// The grouped pair with an fp32 intermediate (the standalone SGMV calls):
+// v[row][j] (ld_v) instead of the planes; r_slot <= 64.  Plain stream order.
+cudaError_t launch_group_shrink_f32(float* v, int ld_v, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
+                                    const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
+                                    int n_pos, int max_group_len, int n_rows, int n_slots, int32_t* status,
+                                    cudaStream_t stream);
+cudaError_t launch_group_expand_f32(bf16_t* y, int ld_y, const float* v, int ld_v, const ProjSet& ps,
+                                    const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
+                                    int n_pos, int max_group_len, int n_rows, int n_slots, int32_t* status,
+                                    cudaStream_t stream);
+
 // The LoRA linear layer: y[:, off_p + c] = bf16(x W^T + B'_p v_p) for every
 // row (ids per row, -1 = base only), W [n_out][ld_w] stacking the
 // projections' base weights, v from the bf16 hi/lo planes.

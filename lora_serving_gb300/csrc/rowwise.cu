@@ -9,7 +9,13 @@
 //                                     (TGI page, "5. tensor parallelism":
 //                                      uneven q/k/v slices)
 // Loads are 128-bit (8 bf16) and coalesced across the warp; x is staged in
-// shared memory once per row and reused by every rank.
+// shared memory once per row and reused by every rank of the CTA.  A second
+// grid dimension splits a row's work over several CTAs (blocks of ranks for
+// the shrink, blocks of output columns for the expand), so that a decode
+// batch of a few dozen rows still covers every SM; the adapter rows a
+// position reads are shared by the positions of the same adapter through L2.
+
+#include <algorithm>
 
 #include "launch.h"
 
@@ -33,7 +39,10 @@ shrink_rowwise_kernel(float* __restrict__ v, int ld_v, const bf16_t* __restrict_
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int R = ps.n_proj * ps.r_slot;
-    for (int j = warp; j < R; j += kThreads / 32) {
+    // ranks [j0, j1) of this CTA's block
+    const int per = (R + gridDim.y - 1) / gridDim.y;
+    const int j0 = blockIdx.y * per, j1 = min(R, j0 + per);
+    for (int j = j0 + warp; j < j1; j += kThreads / 32) {
         const int pj = j / ps.r_slot, jj = j - pj * ps.r_slot;
         const uint4* a = reinterpret_cast<const uint4*>(
             ps.A[pj] + (static_cast<size_t>(slot) * ps.r_slot + jj) * h_in);
@@ -58,7 +67,7 @@ expand_rowwise_kernel(bf16_t* __restrict__ y, int ld_y, const float* __restrict_
     int total = 0;
     for (int p = 0; p < ps.n_proj; ++p) total += ps.width[p] >> 3;
     bf16_t* yrow = y + static_cast<size_t>(row) * ld_y;
-    for (int c = threadIdx.x; c < total; c += kThreads) {
+    for (int c = blockIdx.y * kThreads + threadIdx.x; c < total; c += kThreads * gridDim.y) {
         int p = 0, q = c;
         while (q >= (ps.width[p] >> 3)) { q -= ps.width[p] >> 3; ++p; }
         const int col0 = q << 3;
@@ -77,6 +86,19 @@ expand_rowwise_kernel(bf16_t* __restrict__ y, int ld_y, const float* __restrict_
     }
 }
 
+// Multiprocessors of the current device (queried once per device).
+int sm_count()
+{
+    static int n_sms = 0, sms_device = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+    if (sms_device != dev) {
+        if (cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 152;
+        sms_device = dev;
+    }
+    return n_sms;
+}
+
 }  // namespace
 
 cudaError_t launch_shrink_rowwise(float* v, int ld_v, const bf16_t* x, int ld_x, int h_in,
@@ -92,7 +114,13 @@ cudaError_t launch_shrink_rowwise(float* v, int ld_v, const bf16_t* x, int ld_x,
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    shrink_rowwise_kernel<<<map.n_pos, kThreads, smem, stream>>>(v, ld_v, x, ld_x, h_in, ps, map, status);
+    // Rank blocks of at least 8 ranks (one per warp), enough of them that
+    // the grid covers the SMs about twice.
+    const int R = ps.n_proj * ps.r_slot;
+    const int want = (2 * sm_count() + map.n_pos - 1) / map.n_pos;
+    const int blocks = std::max(1, std::min(want, (R + 7) / 8));
+    shrink_rowwise_kernel<<<dim3(map.n_pos, blocks), kThreads, smem, stream>>>(v, ld_v, x, ld_x, h_in, ps, map,
+                                                                               status);
     note_launch();
     return cudaGetLastError();
 }
@@ -102,7 +130,13 @@ cudaError_t launch_expand_rowwise(bf16_t* y, int ld_y, const float* v, int ld_v,
                                   cudaStream_t stream)
 {
     if (map.n_pos <= 0) return cudaSuccess;
-    expand_rowwise_kernel<<<map.n_pos, kThreads, 0, stream>>>(y, ld_y, v, ld_v, ps, map, status);
+    // Column blocks of kThreads 8-column chunks, enough that the grid covers
+    // the SMs about twice.
+    int total = 0;
+    for (int p = 0; p < ps.n_proj; ++p) total += ps.width[p] >> 3;
+    const int want = (2 * sm_count() + map.n_pos - 1) / map.n_pos;
+    const int blocks = std::max(1, std::min(want, (total + kThreads - 1) / kThreads));
+    expand_rowwise_kernel<<<dim3(map.n_pos, blocks), kThreads, 0, stream>>>(y, ld_y, v, ld_v, ps, map, status);
     note_launch();
     return cudaGetLastError();
 }

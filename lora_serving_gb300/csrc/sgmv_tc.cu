@@ -50,7 +50,8 @@ struct TileInfo {
 // Tile u of the segments' 128-row tiles (segments with slot -1 have none).
 // One parallel round trip over the segment table when it fits the block,
 // a serial scan otherwise.  Malformed entries (bounds outside [0, n_pos))
-// contribute no tiles and set bad.
+// contribute no tiles and set bad, as does a table that does not cover
+// [0, n_pos).
 template <int kThreads>
 __device__ TileInfo find_tile(const int32_t* seg_starts, const int32_t* seg_slot, int n_segs, int n_pos, int u)
 {
@@ -60,7 +61,8 @@ __device__ TileInfo find_tile(const int32_t* seg_starts, const int32_t* seg_slot
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) {
         s_info.found = 0;
-        s_bad = 0;
+        // the table must cover [0, n_pos): its first entry 0, its last n_pos
+        s_bad = n_segs > 0 && (__ldg(seg_starts) != 0 || __ldg(seg_starts + n_segs) != n_pos);
     }
     if (n_segs <= kThreads) {
         int s = 0, e = 0, sl = -1, n = 0;
@@ -115,7 +117,7 @@ __device__ TileInfo find_tile(const int32_t* seg_starts, const int32_t* seg_slot
                 }
                 acc += n;
             }
-            s_bad = bad;
+            s_bad |= bad;
         }
         __syncthreads();
     }
@@ -534,7 +536,8 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
     // v and y are touched only after the preceding grid has completed, and
     // every CTA waits before it leaves.
     grid_dep_launch();
-    if (tid == 0) s_bad = 0;
+    if (tid == 0)   // the table must cover [0, n_pos): its first entry 0, its last n_pos
+        s_bad = p.n_segs > 0 && (__ldg(p.seg_starts) != 0 || __ldg(p.seg_starts + p.n_segs) != p.n_pos);
     __syncthreads();
     const int n_rt = scan_row_tiles(p, false, 1, 0, s_rt, s_warp, &s_bad);
     const long long n_all = static_cast<long long>(n_rt) * p.n_chunks;
