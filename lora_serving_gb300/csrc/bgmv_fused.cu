@@ -49,12 +49,13 @@ using namespace dec;
 constexpr int kKT = 128;           // K elements per pipeline stage
 constexpr int kPad = 8;            // bf16 padding per smem row: conflict-free ldmatrix
 constexpr int kLds = kKT + kPad;
-constexpr int kStages = 2;
+constexpr int kMaxStages = 3;      // K stages in flight: 2, or 3 for small calls whose K slice is 3 stages
 constexpr int kMaxChunks = 128;    // output chunks (8 columns) per expand tile, at most
 constexpr int kPartChunks = 64;    // column parts keep a CTA's chunks within two tiles of this
 constexpr int kTileBBytes = 32768; // B' bytes per expand tile, at most
 constexpr int kPermStage = 4096;   // decode positions staged in smem with the group table
 constexpr int kBSlack = 32;        // zeroed bf16 after B' so padded-K fragments stay finite
+constexpr int kDPad = 8;           // fp32 padding per delta-tile row: rows 8 banks apart
 
 struct FusedParams {
     ProjSet ps;
@@ -101,12 +102,12 @@ __host__ __device__ inline size_t align128(size_t v) { return (v + 127) / 128 * 
 // sD (the delta tile, fp32) overlays the K stages of A and x: it is written
 // only after every stage has been consumed.  Keeping the overlay tight lets
 // three CTAs of a 3B-shaped q/k/v call (80 chunks, rank 16) share an SM.
-__host__ __device__ inline SmemLayout smem_layout(int R, int r_slot, int nch_tile, int n_pos)
+__host__ __device__ inline SmemLayout smem_layout(int R, int r_slot, int nch_tile, int n_pos, int stages)
 {
     SmemLayout L;
-    const size_t sa = align128(sizeof(bf16_t) * kStages * R * kLds);
-    const size_t sx = align128(sizeof(bf16_t) * kStages * kRB * kLds);
-    const size_t sd = align128(sizeof(float) * kRB * nch_tile * 8);
+    const size_t sa = align128(sizeof(bf16_t) * stages * R * kLds);
+    const size_t sx = align128(sizeof(bf16_t) * stages * kRB * kLds);
+    const size_t sd = align128(sizeof(float) * kRB * (nch_tile * 8 + kDPad));
     L.a = 0;
     L.x = sa;
     L.vpart = sa + sx > sd ? sa + sx : sd;
@@ -125,7 +126,7 @@ __host__ __device__ inline SmemLayout smem_layout(int R, int r_slot, int nch_til
 // per thread (1024 threads per SM): in a chain of calls the next call's
 // CTAs then find room beside the running ones (shared memory permitting:
 // four CTAs of a 48 KB o-projection call), without spilling.
-template <int kThreads>
+template <int kThreads, int kStages>
 __global__ void __launch_bounds__(kThreads, 1024 / kThreads)
 bgmv_fused_kernel(FusedParams p)
 {
@@ -135,9 +136,9 @@ bgmv_fused_kernel(FusedParams p)
     const int R = p.ps.n_proj * p.ps.r_slot;
     const int r_slot = p.ps.r_slot;
     const int r_pad = p.r_pad;
-    const SmemLayout L = smem_layout(R, r_slot, p.nch_tile, p.n_pos);
+    const SmemLayout L = smem_layout(R, r_slot, p.nch_tile, p.n_pos, kStages);
     bf16_t* sA = reinterpret_cast<bf16_t*>(smem + L.a);        // [kStages][R][kLds]
-    float* sD = reinterpret_cast<float*>(smem + L.a);          // [kRB][nch_tile*8], after the shrink
+    float* sD = reinterpret_cast<float*>(smem + L.a);          // [kRB][nch_tile*8 + kDPad], after the shrink
     bf16_t* sX = reinterpret_cast<bf16_t*>(smem + L.x);        // [kStages][kRB][kLds]
     float* vpart = reinterpret_cast<float*>(smem + L.vpart);   // [kRB][R]
     float* vfull = reinterpret_cast<float*>(smem + L.vfull);   // [kRB][R]
@@ -162,6 +163,10 @@ bgmv_fused_kernel(FusedParams p)
     // leaves, so this grid never completes before that one (stream order
     // stays transitive under PDL); status flags are written only after a
     // wait.  Clusters without work leave at once and free their SM slots.
+    if (tid == 0) {   // the B' barrier, initialised while the group table is in flight
+        mbar_init(&s_barB, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
     const int grid_units = static_cast<int>(gridDim.x) / (p.cs * p.n_parts);
     const UnitInfo ui = find_unit<kThreads>(p, unit, s_perm, stage_perm, grid_units);   // uniform across the cluster
     const bool bad_group = ui.bad;
@@ -176,16 +181,6 @@ bgmv_fused_kernel(FusedParams p)
         if (crank == 0 && part == 0 && tid == 0) flag(p.status, LORA_DEV_SLOT_OUT_OF_RANGE);
         return;
     }
-    bool bad_row = false;
-    if (tid < kRB) {
-        int r = 0;
-        if (tid < nrows) {
-            r = stage_perm ? s_perm[pos0 + tid] : __ldg(p.perm + pos0 + tid);
-            if (r < 0 || r >= p.n_rows) { bad_row = true; r = 0; }
-        }
-        s_rows[tid] = r;
-    }
-
     // ---- this CTA's K range and output chunks ----
     const int k_begin = crank * p.kc;
     const int k_end = min(p.h_in, k_begin + p.kc);
@@ -208,16 +203,20 @@ bgmv_fused_kernel(FusedParams p)
     };
     // Bytes of B' for chunks [c0, c1): 8 columns x r_slot each.
     auto b_bytes = [&](int c0, int c1) { return static_cast<unsigned>((c1 - c0) * 8 * r_slot * sizeof(bf16_t)); };
-    // One bulk copy per projection segment of chunks [c0, c1), issued by threads 0..n_proj-1.
-    auto copy_B = [&](int c0, int c1, uint64_t* bar) {
-        if (tid < p.ps.n_proj) {
+    // The expected bytes, then one bulk copy per projection segment of
+    // chunks [c0, c1), all from thread 0 (no barrier needed between them).
+    auto copy_B = [&](int c0, int c1, uint64_t* bar, unsigned extra) {
+        if (tid == 0) {
+            mbar_expect(bar, b_bytes(c0, c1) + extra);
             int pc0 = 0;
-            for (int q = 0; q < tid; ++q) pc0 += p.ps.width[q] >> 3;
-            const int pc1 = pc0 + (p.ps.width[tid] >> 3);
-            const int s = max(c0, pc0), e = min(c1, pc1);
-            if (s < e) {
-                const bf16_t* src = p.ps.B[tid] + (static_cast<size_t>(slot) * p.ps.width[tid] + (s - pc0) * 8) * r_slot;
-                bulk_g2s(sB + static_cast<size_t>(s - c0) * 8 * r_slot, src, b_bytes(s, e), bar);
+            for (int q = 0; q < p.ps.n_proj; ++q) {
+                const int pc1 = pc0 + (p.ps.width[q] >> 3);
+                const int s = max(c0, pc0), e = min(c1, pc1);
+                if (s < e) {
+                    const bf16_t* src = p.ps.B[q] + (static_cast<size_t>(slot) * p.ps.width[q] + (s - pc0) * 8) * r_slot;
+                    bulk_g2s(sB + static_cast<size_t>(s - c0) * 8 * r_slot, src, b_bytes(s, e), bar);
+                }
+                pc0 = pc1;
             }
         }
     };
@@ -246,32 +245,37 @@ bgmv_fused_kernel(FusedParams p)
         }
     };
 
-    // ---- set-up: barrier, zero slack, chunk map ----
-    if (tid == 0) {
-        mbar_init(&s_barB, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    // ---- weights first, as soon as the slot is known: they depend neither
+    // on the rows nor on the preceding kernel ----
+    if (ch_end > ch_begin) copy_B(ch_begin, tile0_end, &s_barB, p.stall_tx);
+#pragma unroll
+    for (int st = 0; st < kStages; ++st) {
+        if (st < n_kt) copy_A(st, st);
+        cp_async_commit();
+    }
+
+    // ---- rows, zero slack, chunk map ----
+    bool bad_row = false;
+    if (tid < kRB) {
+        int r = 0;
+        if (tid < nrows) {
+            r = stage_perm ? s_perm[pos0 + tid] : __ldg(p.perm + pos0 + tid);
+            if (r < 0 || r >= p.n_rows) { bad_row = true; r = 0; }
+        }
+        s_rows[tid] = r;
     }
     for (int i = tid; i < kBSlack / 8; i += kThreads)
         reinterpret_cast<uint4*>(sB + p.nch_tile * 8 * r_slot)[i] = make_uint4(0, 0, 0, 0);
     map_chunks(ch_begin, tile0_end);
     if (__syncthreads_or(bad_row)) {
         // A malformed permutation: flag it and leave this unit's rows alone.
-        // Every CTA of the cluster reads the same entries, so all return here.
+        // Every CTA of the cluster reads the same entries, so all return here,
+        // once the copies already issued have landed (bounded wait for B').
+        cp_async_wait<0>();
+        if (tid == 0 && ch_end > ch_begin) mbar_wait(&s_barB, 0);
         grid_dep_wait();
         if (tid == 0 && crank == 0 && part == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
         return;
-    }
-
-    // ---- weights first: they do not depend on the preceding kernel ----
-    if (ch_end > ch_begin) {
-        if (tid == 0) mbar_expect(&s_barB, b_bytes(ch_begin, tile0_end) + p.stall_tx);
-        __syncthreads();
-        copy_B(ch_begin, tile0_end, &s_barB);
-    }
-#pragma unroll
-    for (int st = 0; st < kStages; ++st) {
-        if (st < n_kt) copy_A(st, st);
-        cp_async_commit();
     }
     // The first tile's y lines go into L2 now: their addresses do not depend
     // on the preceding kernel and L2 is coherent with its writes, so the
@@ -299,7 +303,6 @@ bgmv_fused_kernel(FusedParams p)
 
     // ---- shrink: 16 rows x R ranks x this CTA's K range on tensor cores ----
     const int n_tiles = R / 8;                  // 8 ranks per mma tile; <= 16
-    bool failed = false;
     float acc[kTilesPerWarp][4] = {};
     for (int kt = 0; kt < n_kt; ++kt) {
         // groups so far: {A_0} {A_1} {X_0} {X_1}, then one per iteration;
@@ -347,45 +350,45 @@ bgmv_fused_kernel(FusedParams p)
             }
         }
     }
-    __shared__ int s_cta_fail, s_any_fail;
-    failed = __syncthreads_or(failed);
-    if (tid == 0) s_cta_fail = failed ? 1 : 0;
     __syncthreads();
 
     // ---- cluster reduction of the fp32 partials through DSMEM ----
+    // (the shrink's copies are cp.async, whose waits always complete: every
+    // peer's partials are valid here)
     cluster_arrive();
     cluster_wait();
-    if (tid == 0) {   // a peer whose copies timed out has no valid partials
-        int any = 0;
-        for (int c = 0; c < p.cs; ++c) {
-            int f;
-            asm("ld.shared::cluster.b32 %0, [%1];\n" : "=r"(f) : "r"(map_rank(smem_u32(&s_cta_fail), c)));
-            any |= f;
-        }
-        s_any_fail = any;
-    }
     {
-        const int n2 = kRB * R / 2;   // all 16 rows: rows past nrows sum to zero
+        // 16-byte pieces (R is a multiple of 8): with R <= 64 every thread
+        // has at most one piece, so the peers' loads make one round trip;
+        // eight peers' loads in flight at a time, summed in rank order.
+        const int n4 = kRB * R / 4;   // all 16 rows: rows past nrows sum to zero
         const uint32_t base = smem_u32(vpart);
-        for (int i = tid; i < n2; i += kThreads) {
-            float2 part2[16];         // all peers' loads in flight, then a fixed-order sum
+        for (int i = tid; i < n4; i += kThreads) {
+            float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int c0 = 0; c0 < p.cs; c0 += 8) {
+                float4 part4[8];
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
-                if (c < p.cs) part2[c] = ld_dsmem_f2(map_rank(base + i * 8, c));
-            float2 s = part2[0];
+                for (int c = 0; c < 8; ++c)
+                    if (c0 + c < p.cs) part4[c] = ld_dsmem_f4(map_rank(base + i * 16, c0 + c));
 #pragma unroll
-            for (int c = 1; c < 16; ++c) {
-                if (c < p.cs) {
-                    s.x += part2[c].x;
-                    s.y += part2[c].y;
+                for (int c = 0; c < 8; ++c) {
+                    if (c0 + c < p.cs) {
+                        if (c0 + c == 0) {
+                            s = part4[0];
+                        } else {
+                            s.x += part4[c].x;
+                            s.y += part4[c].y;
+                            s.z += part4[c].z;
+                            s.w += part4[c].w;
+                        }
+                    }
                 }
             }
-            reinterpret_cast<float2*>(vfull)[i] = s;
+            reinterpret_cast<float4*>(vfull)[i] = s;
         }
     }
     cluster_arrive();   // this CTA no longer reads its peers' partials
-    __syncthreads();
-    failed = s_any_fail != 0;
+    bool failed = false;
     if (ch_end > ch_begin && !mbar_wait(&s_barB, 0)) failed = true;   // B' of the first tile
     failed = __syncthreads_or(failed);
 
@@ -403,9 +406,8 @@ bgmv_fused_kernel(FusedParams p)
             __syncthreads();
             map_chunks(c0, c1);
             fence_proxy_async();
-            if (tid == 0) mbar_expect(&s_barB, b_bytes(c0, c1));
             __syncthreads();
-            copy_B(c0, c1, &s_barB);
+            copy_B(c0, c1, &s_barB, 0u);
             if (!mbar_wait(&s_barB, b_phase)) failed = true;
             b_phase ^= 1u;
             failed = __syncthreads_or(failed);
@@ -447,7 +449,7 @@ bgmv_fused_kernel(FusedParams p)
                 }
             }
             // d: (row g, cols 2q, 2q+1) and (row g+8, same cols) of chunk ci
-            const int ld_d = nch * 8;
+            const int ld_d = nch * 8 + kDPad;
             *reinterpret_cast<float2*>(sD + gr * ld_d + ci * 8 + q2) = make_float2(d[0], d[1]);
             *reinterpret_cast<float2*>(sD + (gr + 8) * ld_d + ci * 8 + q2) = make_float2(d[2], d[3]);
         }
@@ -470,7 +472,7 @@ bgmv_fused_kernel(FusedParams p)
             cp_async_wait<0>();   // each thread reads back only its own pieces
             for (int i = tid; i < nrows * nch; i += kThreads) {
                 const int t = i / nch, ci = i - t * nch;
-                const float4* dp = reinterpret_cast<const float4*>(sD + t * nch * 8 + ci * 8);
+                const float4* dp = reinterpret_cast<const float4*>(sD + t * (nch * 8 + kDPad) + ci * 8);
                 const float4 d0 = dp[0], d1 = dp[1];
                 const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
                 *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(s_rows[t]) * p.ld_y + p.ps.out_off[s_cp[ci]] +
@@ -553,7 +555,7 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        for (auto fn : {bgmv_fused_kernel<128>, bgmv_fused_kernel<256>}) {
+        for (auto fn : {bgmv_fused_kernel<128, 2>, bgmv_fused_kernel<256, 2>, bgmv_fused_kernel<256, 3>}) {
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
             if (e != cudaSuccess) return e;
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -578,6 +580,14 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     // CTAs' shared memory fits on an SM.
     const int tile_cap = threads == 256 ? min(kMaxChunks, kTileBBytes / (16 * ps.r_slot)) : kPartChunks;
     const int nch_tile = min(tile_cap, max(1, per_cta));
+    const int kc = ((h_in + cs - 1) / cs + 15) / 16 * 16;
+    // Two K stages in flight.  Three (the whole K slice of a 3B-shaped call
+    // in one round trip) shorten one call alone a little, but the larger
+    // shared-memory footprint lets fewer CTAs of consecutive calls overlap
+    // (LORA_FUSED_STAGES=3 selects it for small calls).
+    const int n_kt = (kc + kKT - 1) / kKT;
+    const int stages = env_int("LORA_FUSED_STAGES", 2) == kMaxStages && threads == 256 && n_kt <= kMaxStages
+                           ? kMaxStages : 2;
 
     FusedParams p{};
     p.ps = ps;
@@ -593,7 +603,7 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     p.n_pos = n_pos;
     p.n_slots = n_slots;
     p.n_rows = n_rows;
-    p.kc = ((h_in + cs - 1) / cs + 15) / 16 * 16;
+    p.kc = kc;
     p.n_parts = parts;
     p.cs = cs;
     p.nch_tile = nch_tile;
@@ -606,7 +616,7 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(n_ctas));
     cfg.blockDim = dim3(threads);
-    cfg.dynamicSmemBytes = smem_layout(R, ps.r_slot, nch_tile, n_pos).total;
+    cfg.dynamicSmemBytes = smem_layout(R, ps.r_slot, nch_tile, n_pos, stages).total;
     cfg.stream = stream;
     cudaLaunchAttribute attrs[2];
     int na = 0;
@@ -622,8 +632,9 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
     }
     cfg.attrs = attrs;
     cfg.numAttrs = na;
-    e = threads == 128 ? cudaLaunchKernelEx(&cfg, bgmv_fused_kernel<128>, p)
-                       : cudaLaunchKernelEx(&cfg, bgmv_fused_kernel<256>, p);
+    e = threads == 128  ? cudaLaunchKernelEx(&cfg, bgmv_fused_kernel<128, 2>, p)
+        : stages == 2   ? cudaLaunchKernelEx(&cfg, bgmv_fused_kernel<256, 2>, p)
+                        : cudaLaunchKernelEx(&cfg, bgmv_fused_kernel<256, 3>, p);
     note_launch();
     return e;
 }
