@@ -826,6 +826,128 @@ def run_slots(args, rank, local, ws):
     }
 
 
+# ------------------------------------------------- standalone calls ----
+# The four standalone entry points on the Llama-3.2-3B-shaped decode batch:
+# per layer and group, one shrink over the group's rank-stacked A store (v
+# fp32 [T][n_proj * r_slot]) then one expand per projection.  BGMV takes the
+# per-token ids; SGMV the gather form (rows grouped by adapter through a
+# permutation).  28 layer instances per step, as the decode workload.
+
+STANDALONE_WORKLOAD = "standalone_llama3b"
+
+
+def run_standalone(args, rank, local, ws):
+    import torch
+    from lora_serving_gb300 import abi, build, store, synth
+    torch.cuda.set_device(local)
+    build()
+    abi.load()
+    dev = torch.device("cuda", local)
+    name = "llama3b_decode"
+    layers = args.layers or LAYERS[name]
+    base = synth.get(name)
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    host = []
+    for l in range(layers):
+        wl = synth.get(name)
+        wl.materialise("accumulate", layer=l)
+        host.append(wl)
+    meta = store.BatchMeta(base.ids, 0, base.n_slots, device=dev)
+    m = meta.host
+    inst0 = [Instance(h, store, to_dev) for h in host]
+    set_bytes = sum(i.nbytes() for i in inst0)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_sets = max(1, math.ceil(4 * l2 / set_bytes))
+    sets = [inst0] + [[Instance(h, store, to_dev) for h in host] for _ in range(n_sets - 1)]
+    stacked = [[{g.name: torch.cat(inst.stores[g.name].A, dim=1).contiguous() for g in base.groups} for inst in st]
+               for st in sets]
+    T, r = base.n_rows, base.r_slot
+    v = {g.name: torch.empty(T, len(g.projs) * r, dtype=torch.float32, device=dev) for g in base.groups}
+
+    def step(s, form):
+        for inst, A_st in zip(sets[s], stacked[s]):
+            for g in base.groups:
+                R = len(g.projs) * r
+                st = inst.stores[g.name]
+                if form == "bgmv":
+                    abi.lora_bgmv_shrink(v[g.name], inst.x[g.name], A_st[g.name], meta.ids, h_in=g.h_in, r_slot=R,
+                                         n_slots=base.n_slots)
+                else:
+                    abi.lora_sgmv_shrink(v[g.name], inst.x[g.name], A_st[g.name], meta.gseg_starts, meta.gseg_slot,
+                                         m["n_gsegs"], meta.perm, T, h_in=g.h_in, r_slot=R, n_slots=base.n_slots,
+                                         max_seg_len=m["max_gseg_len"])
+                for pj, ((_, w), off) in enumerate(zip(g.projs, g.offsets)):
+                    if form == "bgmv":
+                        abi.lora_bgmv_expand(inst.y[g.name], off, w, v[g.name], st.B[pj], meta.ids, r_slot=r,
+                                             n_slots=base.n_slots, v_col=pj * r)
+                    else:
+                        abi.lora_sgmv_expand(inst.y[g.name], off, w, v[g.name], st.B[pj], meta.gseg_starts,
+                                             meta.gseg_slot, m["n_gsegs"], meta.perm, T, r_slot=r,
+                                             n_slots=base.n_slots, max_seg_len=m["max_gseg_len"], v_col=pj * r)
+
+    stream = torch.cuda.Stream(device=dev)
+    res = {}
+    clk = None
+    for form in ("sgmv", "bgmv"):
+        with torch.cuda.stream(stream):
+            for s_ in range(n_sets):
+                step(s_, form)
+        torch.cuda.synchronize()
+        l0 = abi.lora_kernel_launch_count()
+        gs = []
+        for s_ in range(n_sets):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                step(s_, form)
+            gs.append(gr)
+        launches = (abi.lora_kernel_launch_count() - l0) // n_sets
+        clocks = ClockSampler(local) if form == "bgmv" else None
+        if clocks:
+            clocks.start()
+            time.sleep(0.3)
+        _, per = time_replays(lambda i: gs[i % n_sets].replay(), args.steps, args.warmup, ws)
+        if clocks:
+            clk = clocks.stop()
+        res[form] = (statistics.median(per), launches)
+        del gs
+    calls = layers * len(base.groups)
+    act = int((base.ids >= 0).sum())
+    # a call's algorithmic bytes: the lora_apply bytes plus the fp32 v the
+    # standalone form writes and reads back
+    bytes_call = [algorithmic_bytes(base, g) + 2 * act * len(g.projs) * r * 4 for g in base.groups]
+    bpc = sum(bytes_call) / len(bytes_call)
+    peak, peak_kind = peaks()
+    med, launches = res["bgmv"]
+    med = max_over_ranks(med, ws, device=dev if ws > 1 else "cpu")
+    call_ms = med / calls
+    achieved = bpc / (call_ms / 1e3) / 1e9
+    sg_ms, sg_launches = res["sgmv"]
+    units = sum_over_ranks(float(T * layers), ws, device=dev if ws > 1 else "cpu")
+    return {
+        "metric": "standalone BGMV shrink+expand tokens/s (token x layer calls per second)",
+        "value": round(units / (med / 1e3), 1), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(med, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": STANDALONE_WORKLOAD, "tokens": T, "layers": layers, "r_slot": r,
+                   "groups": {g.name: [w for _, w in g.projs] for g in base.groups},
+                   "calls": "per group: one shrink over the rank-stacked A, one expand per projection",
+                   "l2": f"{n_sets} rotating input set(s) x {set_bytes / 1e6:.0f} MB (L2 {l2 / 1e6:.0f} MB)",
+                   "timing": "CUDA graph of the step; median replay",
+                   "sgmv_gather_form": {"ms_per_step": round(sg_ms, 5),
+                                        "us_per_call": round(sg_ms / calls * 1e3, 3),
+                                        "frac": round(bpc / (sg_ms / calls / 1e3) / 1e9 / peak, 4),
+                                        "launches_per_step": sg_launches},
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": {"kernel": "lora_bgmv_shrink + lora_bgmv_expand kernels", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} hbm_gbs", "per": "group call (shrink + expands)",
+                     "bytes_per_call": round(bpc), "call_us": round(call_ms * 1e3, 3), "traffic": None},
+        "clocks": clk,
+        "gpu_launches": int(launches * args.steps),
+        "e2e": None,
+    }
+
+
 # --------------------------------------------------------- GPU arm ----
 
 class Instance:
@@ -1227,6 +1349,8 @@ def run_reference(args, rank, ws):
     if rank != 0:
         return None
     name = HEADLINE if args.workload == "all" else args.workload
+    if name == STANDALONE_WORKLOAD:   # the same delta, through the oracle's per-row path
+        name = "llama3b_decode"
     layers = args.layers or LAYERS.get(name, 1)
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
     if name == SLOTS_WORKLOAD:
@@ -1336,6 +1460,8 @@ def main(argv=None):
         out = run_linear(args, rank, local, ws)
     elif args.workload == SLOTS_WORKLOAD:
         out = run_slots(args, rank, local, ws)
+    elif args.workload == STANDALONE_WORKLOAD:
+        out = run_standalone(args, rank, local, ws)
     elif args.workload == "all":
         out = run_all(args, rank, local, ws)
     else:
