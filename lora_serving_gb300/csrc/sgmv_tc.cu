@@ -395,13 +395,13 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
 // shared-memory table.  The v_hi / v_lo slice of an item (row tile,
 // projection) is loaded once into one of two buffers (one when r_pad64 > 64),
 // so the next item's slice loads while the current one's tiles finish; B'
-// and y tiles stream through a kStagesE-deep TMA ring; the fp32 accumulator
+// and y tiles stream through a TMA ring of up to kStagesE stages; the fp32 accumulator
 // is double-buffered in tensor memory, so the epilogue of tile i (TMEM ->
 // registers, + y from shared memory, round, store) overlaps the loads and
 // MMAs of tile i+1.
 //   warp 0: TMA producer      warp 1: MMA issuer      warps 2..17: epilogue
 
-constexpr int kStagesE = 3;
+constexpr int kStagesE = 4;        // ring stages, at most (the launcher picks 3 or 4, or 2 for r_pad64 = 128)
 constexpr int kEpiWarps = 16;       // 4 per TMEM lane quarter, 32 columns each
 constexpr int kExpandThreadsP = 32 * (2 + kEpiWarps);
 constexpr int kChunkMax = 16;       // output tiles per work item, at most
@@ -420,6 +420,8 @@ struct ExpandTcParams {
     int n_segs, n_pos, n_rows;
     bf16_t* y;
     int ld_y;
+    int stages;                     // ring stages (<= kStagesE)
+    int vbufs;                      // v slice buffers (1 or 2)
     unsigned stall_tx;              // test hook: extra bytes expected on the first ring stage (0 normally)
     int32_t* status;
 };
@@ -560,8 +562,8 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
 
     const CUtensorMap* bmap[4] = {&mb0, &mb1, &mb2, &mb3};
     const int kbs = p.r_pad64 / kKB;                         // K blocks per plane
-    const int S = kbs == 1 ? kStagesE : 2;                   // ring depth that fits shared memory
-    const int VB = kbs == 1 ? 2 : 1;                         // v slice buffers
+    const int S = p.stages;                                  // ring depth (shared memory permitting)
+    const int VB = p.vbufs;                                  // v slice buffers
     const int stage_bytes = (kbs + 2) * kBoxBytes;           // B' (kbs boxes) + y (2 boxes)
     const int vbuf_bytes = 2 * kbs * kBoxBytes;              // v_hi boxes, then v_lo boxes
     uint8_t* vbufs = align1024(smem_raw);                    // VB x [v_hi | v_lo]
@@ -790,6 +792,7 @@ bool configure_once(const void* fn, size_t smem, int& configured_device, size_t&
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
         return false;
+    if (prefer_max_shared(fn) != cudaSuccess) return false;
     configured_device = dev;
     configured_bytes = smem;
     return true;
@@ -930,8 +933,18 @@ cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const b
     p.stall_tx = test_stall_bytes(kStallExpandTc);
     p.status = status;
     const int kbs = r_pad64 / kKB;
-    const int stages = kbs == 1 ? kStagesE : 2;
-    const int vbufs = kbs == 1 ? 2 : 1;
+    // r_pad64 = 64: four ring stages and one v slice buffer (225 KB), or
+    // three stages and two buffers (209 KB); r_pad64 = 128: two stages, one
+    // buffer.
+    // Large work items (8 or more tiles) pay the v-slice load of one buffer
+    // rarely and gain from the deeper ring; small ones keep the second
+    // buffer (Mistral-7B prefill: 1.469 against 1.509 ms per step; the
+    // mixed batch's 4-tile items: 4.18 against 4.03 ms).
+    const int st_env = env_int("LORA_TC_EXPAND_STAGES", p.chunk >= 8 ? kStagesE : 3);
+    const int stages = kbs == 1 ? (st_env == 3 ? 3 : kStagesE) : 2;
+    const int vbufs = kbs == 1 && stages == 3 ? 2 : 1;
+    p.stages = stages;
+    p.vbufs = vbufs;
     const size_t smem = static_cast<size_t>(vbufs * 2 * kbs + stages * (kbs + 2)) * kBoxBytes + 1024;
     static int configured = -1;
     static size_t configured_bytes = 0;
