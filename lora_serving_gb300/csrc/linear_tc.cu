@@ -204,15 +204,6 @@ struct Plan {
     }
 };
 
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-        "[%5];\n" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
-        : "memory");
-}
-
 // L2 prefetches of a box (no shared memory, no completion to wait for).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1)
 {
@@ -700,6 +691,8 @@ cudaError_t launch_linear_tc(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int
     if (configured_device != dev) {
         e = cudaFuncSetAttribute(linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(linear_tc_smem()));
+        if (e != cudaSuccess) return e;
+        e = prefer_max_shared(reinterpret_cast<const void*>(linear_tc_kernel));
         if (e != cudaSuccess) return e;
         e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;

@@ -246,3 +246,80 @@ def test_linear_split_k_bad_row_id_flagged():
     ids_ref = ids.copy()
     ids_ref[bad] = -1
     check_bf16(got, _oracle(ids_ref, x, W, ads, st), np.zeros_like(ids), got, "split K with a bad id")
+
+
+# ---- decode-sized batches (at most 64 rows): the tile turned around ----------
+
+SWAP_CASES = {
+    "one_row": dict(h_in=256, widths=(256,), ranks=(16, 8), r_slot=16, ids=np.array([1]), n_prefill=0),
+    "five_rows_ragged": dict(h_in=200, widths=(136, 520), ranks=(8, 16, 16), r_slot=16,
+                             ids=np.array([2, -1, 0, 2, 1]), n_prefill=0),
+    "sixteen_all_base": dict(h_in=128, widths=(128,), ranks=(16,), r_slot=16, ids=np.full(16, -1), n_prefill=0),
+    "rank8_k_tail": dict(h_in=328, widths=(392, 64), ranks=(8, 4, 8), r_slot=8,
+                         ids=np.array([(i * 3) % 4 - 1 for i in range(37)]), n_prefill=0),
+    "rank64": dict(h_in=512, widths=(256, 128), ranks=(64, 40, 64, 8), r_slot=64,
+                   ids=np.array([(i * 5) % 5 - 1 for i in range(48)]), n_prefill=0),
+    "four_proj": dict(h_in=320, widths=(200, 72, 72, 264), ranks=(16, 8, 12), r_slot=16,
+                      ids=np.array([i % 4 - 1 for i in range(33)]), n_prefill=0),
+    "many_adapters": dict(h_in=256, widths=(384,), ranks=tuple([16] * 40), r_slot=16,
+                          ids=np.array([i % 41 - 1 for i in range(64)]), n_prefill=0),
+    "prefill_and_decode": dict(h_in=256, widths=(256, 128), ranks=(16, 16, 16), r_slot=16,
+                               ids=np.concatenate([_segments([20, 12], [1, 0]), np.array([2, 0, -1, 1, 2])]),
+                               n_prefill=32),
+}
+
+
+@pytest.mark.parametrize("split", [None, "1", "2", "8"])
+@pytest.mark.parametrize("name", list(SWAP_CASES))
+def test_linear_decode_sized_vs_oracle(name, split, monkeypatch):
+    """Batches of at most 64 rows take the turned-around tile (128 output
+    columns as the MMA's M, the rows as its N, K split over a cluster, one K
+    extension per adapter present): every element against the oracle, for
+    each cluster split the launcher may choose."""
+    if split is not None:
+        if name not in ("five_rows_ragged", "rank64", "many_adapters"):
+            pytest.skip("splits are exercised on three shapes")
+        monkeypatch.setenv("LORA_SWAP_SPLIT", split)
+    st, x, W, ads, ids, meta = _case(**SWAP_CASES[name], seed=11)
+    got, status = _run(st, x, W, meta)
+    assert status == 0
+    ref = _oracle(ids, x, W, ads, st)
+    check_bf16(got, ref, np.zeros_like(ids), got, f"linear decode-sized {name} split={split}")
+
+
+def test_linear_decode_sized_llama3b_layer():
+    """The Llama-3.2-3B-shaped decode layer (64 tokens, 8 adapters of rank
+    16, q/k/v 3072 -> 5120 and o 3072 -> 3072) through the turned-around
+    tile, every element against the oracle."""
+    wl = synth.get("llama3b_decode").materialise("delta")
+    for g in wl.groups:
+        st = store.GroupStore.from_workload(wl, g.name)
+        W = wl.base_weight(g.name)
+        meta = store.BatchMeta(wl.ids, 0, wl.n_slots)
+        got, status = _run(st, wl.x[g.name], W, meta)
+        assert status == 0
+        ref = np.zeros((wl.n_rows, st.ld_y), np.uint16)
+        for p, (pname, w) in enumerate(g.projs):
+            off = st.offsets[p]
+            ad = O.Adapters([wl.A[(g.name, pname, k)] for k in range(wl.n_slots)],
+                            [wl.B[(g.name, pname, k)] for k in range(wl.n_slots)],
+                            [O.scale(float(wl.alphas[k]), int(wl.ranks[k]), bool(wl.rslora[k]))
+                             for k in range(wl.n_slots)])
+            ref = O.linear_projection(wl.ids, wl.x[g.name], W[off:off + w], ref, off, ad)
+        check_bf16(got, ref, np.zeros_like(wl.ids), got, f"linear 3B decode {g.name}")
+
+
+def test_linear_decode_sized_bad_id_keeps_base():
+    """A row naming a slot outside [-1, n_slots) keeps the base product and
+    sets LORA_DEV_SLOT_OUT_OF_RANGE; the other rows are unaffected."""
+    st, x, W, ads, ids, meta = _case(h_in=256, widths=(256,), ranks=(16, 8), r_slot=16,
+                                     ids=np.array([0, 1, 1, 0, -1, 1]), n_prefill=0, seed=3)
+    bad = ids.copy()
+    bad[2] = 7
+    meta.ids.copy_(torch.from_numpy(bad.astype(np.int32)))
+    got, status = _run(st, x, W, meta)
+    assert status & abi.LORA_DEV_SLOT_OUT_OF_RANGE
+    ids_base = ids.copy()
+    ids_base[2] = -1
+    ref = _oracle(ids_base, x, W, ads, st)
+    check_bf16(got, ref, np.zeros_like(ids), got, "bad id keeps the base product")
