@@ -102,6 +102,8 @@ lora_status_t check_disjoint(const lora_proj_t* projs, int n_proj)
 
 inline lora_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? LORA_OK : LORA_ERR_CUDA; }
 
+inline int env_int_abi(const char* name, int dflt) { return lora::env_int(name, dflt); }
+
 RowMap ids_map(const int32_t* ids, int row_base, int n_pos, int n_rows, int n_slots)
 {
     RowMap m{};
@@ -293,9 +295,18 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
         }
     }
 
-    // Decode rows first: their kernel is short and latency-bound, and the
-    // prefill shrink that follows (programmatic dependent launch) can run
-    // beside it -- the two touch disjoint rows of y and of the workspace.
+    // A mixed batch whose prefill rows take the tensor cores launches the
+    // prefill shrink first (one CTA per SM), then the decode rows' kernel,
+    // which fills the SMs' remaining room beside it (programmatic dependent
+    // launch), then the prefill expand: the shrink and the decode kernel
+    // touch disjoint rows of y and of the workspace.  Otherwise the decode
+    // rows' kernel comes first and the prefill kernels follow.
+    const bool tc_prefill = P > 0 && meta->max_seg_len >= kTcMinSegment && lora::sgmv_tc_supported(n_proj, r_slot, h_in);
+    const bool shrink_first = tc_prefill && D > 0 && env_int_abi("LORA_APPLY_SHRINK_FIRST", 1) != 0;
+    if (shrink_first)
+        LORA_TRY(cuda_status(lora::launch_sgmv_shrink_tc(nullptr, 0, vh, vl, x, ld_x, h_in, ps, meta->seg_starts,
+                                                         meta->seg_slot, meta->n_segs, P, T, n_slots, flags,
+                                                         dev_status, s)));
     if (D > 0) {
         const bool gathered = meta->perm && meta->gseg_starts && meta->gseg_slot && meta->n_gsegs > 0;
         const bool fused_ok = gathered && lora::fused_decode_supported(n_proj, r_slot);
@@ -323,11 +334,12 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
         }
     }
     if (P > 0) {
-        if (meta->max_seg_len >= kTcMinSegment && lora::sgmv_tc_supported(n_proj, r_slot, h_in)) {
+        if (tc_prefill) {
             // long segments: tensor-core shrink into the hi/lo planes, then expand
-            LORA_TRY(cuda_status(lora::launch_sgmv_shrink_tc(nullptr, 0, vh, vl, x, ld_x, h_in, ps,
-                                                             meta->seg_starts, meta->seg_slot, meta->n_segs, P,
-                                                             T, n_slots, flags, dev_status, s)));
+            if (!shrink_first)
+                LORA_TRY(cuda_status(lora::launch_sgmv_shrink_tc(nullptr, 0, vh, vl, x, ld_x, h_in, ps,
+                                                                 meta->seg_starts, meta->seg_slot, meta->n_segs, P,
+                                                                 T, n_slots, flags, dev_status, s)));
             LORA_TRY(cuda_status(lora::launch_sgmv_expand_tc(y, ld_y, vh, vl, ps, meta->seg_starts,
                                                              meta->seg_slot, meta->n_segs, P, T, n_slots, flags,
                                                              dev_status, s)));
@@ -408,7 +420,12 @@ lora_status_t lora_linear(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld
                                                               meta->gseg_slot, meta->n_gsegs, D, meta->max_gseg_len,
                                                               T, n_slots, LORA_APPLY_NO_PDL, vh, vl, dev_status,
                                                               s)));
-    // base product with the delta in the same accumulator
+    // base product with the delta in the same accumulator: decode-sized
+    // batches turn the tile around (the weights are the bytes), larger ones
+    // take the persistent tile kernel
+    if (lora::linear_swap_supported(T, r_slot) && env_int_abi("LORA_LINEAR_SWAP", 1) != 0)
+        return cuda_status(lora::launch_linear_swap(y, ld_y, x, ld_x, h_in, W, ld_w, n_out, ps, vh, vl,
+                                                    meta->lora_ids, T, n_slots, dev_status, s));
     return cuda_status(lora::launch_linear_tc(y, ld_y, x, ld_x, h_in, W, ld_w, n_out, ps, vh, vl, meta->lora_ids, T,
                                               n_slots, dev_status, s));
 }

@@ -558,6 +558,8 @@ cudaError_t launch_bgmv_fused(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, in
         for (auto fn : {bgmv_fused_kernel<128, 2>, bgmv_fused_kernel<256, 2>, bgmv_fused_kernel<256, 3>}) {
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
             if (e != cudaSuccess) return e;
+            e = prefer_max_shared(reinterpret_cast<const void*>(fn));
+            if (e != cudaSuccess) return e;
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             if (e != cudaSuccess) return e;
         }

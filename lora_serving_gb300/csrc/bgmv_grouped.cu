@@ -600,6 +600,10 @@ cudaError_t grouped_plan(const ProjSet& ps, int n_groups, int n_pos, int max_gro
         e = cudaFuncSetAttribute(bgmv_group_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(sizeof(bf16_t) * kGxCols * 64));
         if (e != cudaSuccess) return e;
+        e = prefer_max_shared(reinterpret_cast<const void*>(bgmv_group_shrink_kernel));
+        if (e != cudaSuccess) return e;
+        e = prefer_max_shared(reinterpret_cast<const void*>(bgmv_group_expand_kernel));
+        if (e != cudaSuccess) return e;
         e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         configured_device = dev;

@@ -209,6 +209,10 @@ cudaError_t configure_merge(int& n_sms)
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(merge_batch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
         if (e != cudaSuccess) return e;
+        e = prefer_max_shared(reinterpret_cast<const void*>(merge_kernel));
+        if (e != cudaSuccess) return e;
+        e = prefer_max_shared(reinterpret_cast<const void*>(merge_batch_kernel));
+        if (e != cudaSuccess) return e;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         configured_device = dev;

@@ -112,6 +112,10 @@ cudaError_t launch_shrink_rowwise(float* v, int ld_v, const bf16_t* x, int ld_x,
         cudaError_t e = cudaFuncSetAttribute(shrink_rowwise_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
         if (e != cudaSuccess) return e;
+        e = prefer_max_shared(reinterpret_cast<const void*>(shrink_rowwise_kernel));
+        if (e != cudaSuccess) return e;
+        e = prefer_max_shared(reinterpret_cast<const void*>(expand_rowwise_kernel));
+        if (e != cudaSuccess) return e;
         attr_set = true;
     }
     // Rank blocks of at least 8 ranks (one per warp), enough of them that
