@@ -723,6 +723,123 @@ def run_linear(args, rank, local, ws):
     return out
 
 
+# ------------------------------------------- linear layer, decode ----
+# The LoRA linear layer on the Llama-3.2-3B-shaped decode batch (64 tokens,
+# 8 adapters of rank 16): 28 layer instances x (q/k/v, o) lora_linear calls
+# per step, each layer's base weights its own (1.4 GB, beyond L2).  Context
+# in the same run: the base products alone through cuBLAS, and cuBLAS then
+# lora_apply (the unfused layer, two roundings).
+
+LINEAR_DECODE_WORKLOAD = "linear_llama3b_decode"
+
+
+def linear_decode_bytes(wl, group) -> int:
+    """Algorithmic (compulsory) bytes of one decode-sized lora_linear call:
+    the group's base weight, the adapters the batch uses (A and B' once),
+    x read once and y written once (every row: base rows get the base
+    product)."""
+    act = wl.ids >= 0
+    n_adapters = int(np.unique(wl.ids[act]).size)
+    w_lora = sum(wl.r_slot * (group.h_in + w) * 2 for _, w in group.projs)
+    return (group.ld_y * group.h_in * 2 + n_adapters * w_lora + wl.n_rows * group.h_in * 2
+            + wl.n_rows * group.ld_y * 2)
+
+
+def run_linear_decode(args, rank, local, ws):
+    import torch
+    from lora_serving_gb300 import abi, build, store, synth
+    torch.cuda.set_device(local)
+    build()
+    abi.load()
+    dev = torch.device("cuda", local)
+    name = "llama3b_decode"
+    layers = args.layers or LAYERS[name]
+    base = synth.get(name)
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    meta = store.BatchMeta(base.ids, 0, base.n_slots, device=dev)
+    ws_buf = {g.name: store.workspace_for(base.n_rows, len(g.projs), base.r_slot, device=dev) for g in base.groups}
+    inst = []
+    for l in range(layers):
+        wl = synth.get(name)
+        wl.materialise("delta", layer=l)
+        inst.append({g.name: {"st": store.GroupStore.from_workload(wl, g.name, device=dev),
+                              "x": to_dev(wl.x[g.name]), "W": to_dev(wl.base_weight(g.name, layer=l)),
+                              "y": torch.empty(base.n_rows, g.ld_y, dtype=torch.bfloat16, device=dev)}
+                     for g in base.groups})
+
+    def fused():
+        for it in inst:
+            for g in base.groups:
+                d = it[g.name]
+                store.linear(d["y"], d["x"], d["W"], d["st"], meta, ws_buf[g.name])
+
+    def cublas_base():
+        for it in inst:
+            for g in base.groups:
+                d = it[g.name]
+                torch.matmul(d["x"], d["W"].t(), out=d["y"])
+
+    def unfused():
+        for it in inst:
+            for g in base.groups:
+                d = it[g.name]
+                torch.matmul(d["x"], d["W"].t(), out=d["y"])
+                store.apply(d["y"], d["x"], d["st"], meta, ws_buf[g.name], flags=abi.LORA_APPLY_X_READY)
+
+    stream = torch.cuda.Stream(device=dev)
+    graphs = {}
+    launches = 0
+    for name_v, fn in (("fused", fused), ("cublas_base", cublas_base), ("unfused", unfused)):
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        l0 = abi.lora_kernel_launch_count()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            fn()
+        if name_v == "fused":
+            launches = abi.lora_kernel_launch_count() - l0
+        graphs[name_v] = gr
+    torch.cuda.synchronize()
+    other = {}
+    for name_v in ("cublas_base", "unfused"):
+        _, per = time_replays(lambda i: graphs[name_v].replay(), max(10, args.steps // 2), args.warmup, ws)
+        other[name_v] = round(statistics.median(per), 5)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    _, per = time_replays(lambda i: graphs["fused"].replay(), args.steps, args.warmup, ws)
+    clk = clocks.stop()
+    med_local = statistics.median(per)
+    med = max_over_ranks(med_local, ws, device=dev if ws > 1 else "cpu")
+    units = sum_over_ranks(float(base.n_rows * layers), ws, device=dev if ws > 1 else "cpu")
+    bytes_step = layers * sum(linear_decode_bytes(base, g) for g in base.groups)
+    achieved = bytes_step / (med_local / 1e3) / 1e9
+    peak, peak_kind = peaks()
+    out = {
+        "metric": "LoRA linear layer tokens/s (base product + per-row delta, decode batch)",
+        "value": round(units / (med / 1e3), 1), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(med, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": LINEAR_DECODE_WORKLOAD, "tokens": base.n_rows, "layers": layers,
+                   "groups": {g.name: [g.h_in, g.ld_y] for g in base.groups}, "n_slots": base.n_slots,
+                   "r_slot": base.r_slot, "us_per_layer": round(med / layers * 1e3, 3),
+                   "l2": "every layer's base weights its own (1.4 GB per step)",
+                   "timing": "CUDA graph of the step's lora_linear calls; median replay",
+                   "us_per_layer_context": {"cublas_base_only": round(other["cublas_base"] / layers * 1e3, 3),
+                                            "cublas_base_then_lora_apply": round(other["unfused"] / layers * 1e3, 3)},
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": {"kernel": "linear_swap_kernel (+ bgmv_group_shrink_kernel per call)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} hbm_gbs", "per": "step", "bytes_per_step": bytes_step,
+                     "traffic": None},
+        "clocks": clk,
+        "gpu_launches": int(launches * args.steps),
+        "e2e": None,
+    }
+    return out
+
+
 # ---------------------------------------------------------- slots ----
 # Adapter slot manager: loading adapters into GPU slots.  Llama-3.2-3B q/k/v/o
 # adapters of rank 16 (640 KiB prepared), SLOTS_N slots, a pool of SLOTS_POOL
@@ -1351,6 +1468,9 @@ def run_reference(args, rank, ws):
     name = HEADLINE if args.workload == "all" else args.workload
     if name == STANDALONE_WORKLOAD:   # the same delta, through the oracle's per-row path
         name = "llama3b_decode"
+    if name == LINEAR_DECODE_WORKLOAD:
+        return {"impl": "reference", "unavailable": "the oracle's linear layer is timed on the prefill workload "
+                                                    "(--workload linear_mistral7b_prefill)"}
     layers = args.layers or LAYERS.get(name, 1)
     per_step = max(1.0, args.cpu_seconds / max(1, args.steps))
     if name == SLOTS_WORKLOAD:
@@ -1462,6 +1582,8 @@ def main(argv=None):
         out = run_slots(args, rank, local, ws)
     elif args.workload == STANDALONE_WORKLOAD:
         out = run_standalone(args, rank, local, ws)
+    elif args.workload == LINEAR_DECODE_WORKLOAD:
+        out = run_linear_decode(args, rank, local, ws)
     elif args.workload == "all":
         out = run_all(args, rank, local, ws)
     else:
