@@ -26,6 +26,9 @@
 // the cluster in rank order, rounds, and writes whole 16-byte pieces of y.
 //   warp 0: TMA producer   warp 1: masks v and issues the MMAs
 //   warps 2..5: read the accumulator out
+// Under programmatic dependent launch the base steps (x, W) run while the
+// shrink that produces v finishes; the adapter steps, y and the status word
+// follow the grid dependency.
 // Every wait is bounded (0.2 s); a timeout sets LORA_DEV_TIMEOUT, the CTA
 // writes nothing, its producer lets every copy it issued land, and the
 // tensor memory is freed.
@@ -45,13 +48,14 @@ using namespace tc;
 constexpr int kSwM = 128;                    // output columns per tile (tensor-memory lanes)
 constexpr int kSwK = 64;                     // K elements per step (one 128-byte swizzled row)
 constexpr int kSwMaxN = 64;                  // batch rows, at most
-constexpr int kSwStages = 3;
+constexpr int kSwStages = 3;                 // 97 KB: two CTAs per SM
 constexpr int kSwABytes = kSwM * 128;        // W or B' box
 constexpr int kSwBBytes = kSwMaxN * 128;     // x, v_hi or v_lo box (room for 64 rows)
 constexpr int kSwStageBytes = kSwABytes + 2 * kSwBBytes;
 constexpr int kSwThreads = 192;              // 6 warps
 constexpr int kSwMaxSplit = 8;
 constexpr int kSwRedPitch = kSwM + 4;        // fp32 pitch of the transposed partial
+constexpr int kScanBar = 1;                  // named barrier: warp 1's group scan -> the producer's adapter steps
 
 struct SwapParams {
     int n_proj, r_slot, n_slots, n_rows, n_pad;   // n_pad: rows rounded up to 16 (the MMA N)
@@ -96,6 +100,10 @@ linear_swap_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant
     __shared__ int s_slot[kSwMaxN];                 // this CTA's adapter slots (LoRA steps)
     __shared__ unsigned long long s_mask[kSwMaxN];  // rows of each of them
     __shared__ int s_ngroups, s_badid;
+    // Programmatic dependent launch: x, W, B' and the ids are read at once
+    // (none is written by the shrink before this kernel), the base steps
+    // run while the shrink finishes; v, y and the status word wait for it.
+    grid_dep_launch();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int crank = P.cs > 1 ? static_cast<int>(cluster_rank()) : 0;
     const int tile = blockIdx.x / P.cs;
@@ -120,60 +128,21 @@ linear_swap_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant
         mbar_init_fence();
         s_fail = 0;
     }
-    __syncthreads();
-    if (warp == 1) {
-        // Warp 1 (lanes own rows lane and lane + 32): a row opens a group if
-        // its slot is valid and no earlier row names it; group g (in order
-        // of first appearance) goes to cluster rank g % cs, with the mask of
-        // every row that names its slot.
-        bool first[2], bad = false;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int t = lane + 32 * h, id = s_ids[t];
-            bad |= t < P.n_rows && (id < -1 || id >= P.n_slots);
-            bool f = id >= 0 && id < P.n_slots;
-            for (int u = 0; u < t && f; ++u)
-                if (s_ids[u] == id) f = false;
-            first[h] = f;
-        }
-        const unsigned long long F = static_cast<unsigned long long>(__ballot_sync(0xFFFFFFFFu, first[0])) |
-                                     (static_cast<unsigned long long>(__ballot_sync(0xFFFFFFFFu, first[1])) << 32);
-        const bool any_bad = __any_sync(0xFFFFFFFFu, bad);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int t = lane + 32 * h;
-            if (!first[h]) continue;
-            const int g = __popcll(F & ((1ull << t) - 1ull));
-            if (g % P.cs != crank) continue;
-            unsigned long long m = 0;
-            for (int u = t; u < P.n_rows; ++u)
-                if (s_ids[u] == s_ids[t]) m |= 1ull << u;
-            s_slot[g / P.cs] = s_ids[t];
-            s_mask[g / P.cs] = m;
-        }
-        if (lane == 0) {
-            const int G = __popcll(F);
-            s_ngroups = G > crank ? (G - crank + P.cs - 1) / P.cs : 0;
-            s_badid = any_bad ? 1 : 0;
-        }
-    }
     if (warp == 0) tmem_alloc(&s_tmem, kSwMaxN);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    const int n_steps = n_base + s_ngroups;
     const uint32_t b_bytes = static_cast<uint32_t>(P.n_pad) * 128;
 
-    if (warp == 0 && lane == 0) {
-        // ---- producer: base steps (W box + x box), then LoRA steps (B' box + v boxes) ----
+    if (warp == 0) {
+        // ---- producer (lane 0): the base steps (W box + x box) at once;
+        // then, once warp 1 has scanned the groups, the LoRA steps (B' box +
+        // v boxes) ----
         int issued = 0;
-        for (int i = 0; i < n_steps && !s_fail; ++i) {
+        auto issue = [&](int i) -> bool {
             const int s = i % kSwStages;
-            if (i >= kSwStages && !mbar_wait(&empty[s], ((i / kSwStages) - 1) & 1)) {
-                s_fail = 1;
-                break;
-            }
+            if (i >= kSwStages && !mbar_wait_spin(&empty[s], ((i / kSwStages) - 1) & 1)) return false;
             uint8_t* st = ring + s * kSwStageBytes;
             if (i < n_base) {
                 const int k = (kb0 + i) * kSwK;
@@ -181,6 +150,7 @@ linear_swap_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant
                 tma_load_2d(st, &mw, k, P.w_row[p] + col0, &full[s]);
                 tma_load_2d(st + kSwABytes, &mx, k, 0, &full[s]);
             } else {
+                if (i == n_base) grid_dep_wait();   // v is the preceding kernel's output
                 const int g = i - n_base;
                 mbar_expect_tx(&full[s], kSwABytes + 2 * b_bytes);
                 tma_load_2d(st, bmap, 0, s_slot[g] * P.width[p] + col0, &full[s]);
@@ -188,19 +158,88 @@ linear_swap_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant
                 tma_load_3d(st + kSwABytes + kSwBBytes, &mvl, 0, p, 0, &full[s]);
             }
             issued = i + 1;
+            return true;
+        };
+        bool ok = true;
+        if (lane == 0)
+            for (int i = 0; i < n_base && ok && !s_fail; ++i) ok = issue(i);
+        __syncwarp();
+        // warp 1 has arrived after its group scan (it does not wait here: it
+        // goes on to consume the base steps)
+        named_barrier(kScanBar, 64);
+        if (lane == 0) {
+            const int n_steps = n_base + s_ngroups;
+            for (int i = n_base; i < n_steps && ok && !s_fail; ++i) ok = issue(i);
+            if (!ok) s_fail = 1;
+            // every copy issued lands before the CTA moves on
+            for (int i = issued > kSwStages ? issued - kSwStages : 0; i < issued; ++i)
+                if (!mbar_wait(&full[i % kSwStages], (i / kSwStages) & 1)) s_fail = 1;
         }
-        // every copy issued lands before the CTA moves on
-        for (int i = issued > kSwStages ? issued - kSwStages : 0; i < issued; ++i)
-            if (!mbar_wait(&full[i % kSwStages], (i / kSwStages) & 1)) s_fail = 1;
+        __syncwarp();
     } else if (warp == 1) {
+        // ---- group scan: lanes own rows lane and lane + 32; a row opens a
+        // group if its slot is valid and no earlier row names it; group g
+        // (in order of first appearance) goes to cluster rank g % cs, with
+        // the mask of every row that names its slot ----
+        {
+            int idv[2];
+            bool first[2], bad = false;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int t = lane + 32 * h;
+                idv[h] = s_ids[t];
+                bad |= t < P.n_rows && (idv[h] < -1 || idv[h] >= P.n_slots);
+            }
+            // rows of each half naming the same slot as this lane's row
+            unsigned same[2][2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    unsigned m = 0;
+                    for (int u = 0; u < 32; ++u) m |= (__shfl_sync(0xFFFFFFFFu, idv[hh], u) == idv[h]) ? (1u << u) : 0u;
+                    same[h][hh] = m;
+                }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const bool valid = idv[h] >= 0 && idv[h] < P.n_slots;
+                const unsigned long long m = static_cast<unsigned long long>(same[h][0]) |
+                                             (static_cast<unsigned long long>(same[h][1]) << 32);
+                const int t = lane + 32 * h;
+                first[h] = valid && (m & ((1ull << t) - 1ull)) == 0;
+            }
+            const unsigned long long F = static_cast<unsigned long long>(__ballot_sync(0xFFFFFFFFu, first[0])) |
+                                         (static_cast<unsigned long long>(__ballot_sync(0xFFFFFFFFu, first[1])) << 32);
+            const bool any_bad = __any_sync(0xFFFFFFFFu, bad);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int t = lane + 32 * h;
+                if (!first[h]) continue;
+                const int g = __popcll(F & ((1ull << t) - 1ull));
+                if (g % P.cs != crank) continue;
+                const unsigned long long rows_mask = (static_cast<unsigned long long>(same[h][0]) |
+                                                      (static_cast<unsigned long long>(same[h][1]) << 32)) &
+                                                     (P.n_rows >= 64 ? ~0ull : ((1ull << P.n_rows) - 1ull));
+                s_slot[g / P.cs] = idv[h];
+                s_mask[g / P.cs] = rows_mask;
+            }
+            if (lane == 0) {
+                const int G = __popcll(F);
+                s_ngroups = G > crank ? (G - crank + P.cs - 1) / P.cs : 0;
+                s_badid = any_bad ? 1 : 0;
+            }
+            __syncwarp();
+        }
+        named_barrier_arrive(kScanBar, 64);   // the producer may issue the adapter steps
         // ---- MMA warp: masks the v boxes of a LoRA step, lane 0 issues ----
         const uint32_t idesc = idesc_bf16_f32(kSwM, P.n_pad);
+        const int n_steps = n_base + s_ngroups;
         bool ok = true, acc = false;
         for (int i = 0; i < n_steps && ok; ++i) {
             const int s = i % kSwStages;
             // lane 0 waits for the stage; the warp follows its verdict together
             int landed = 1;
-            if (lane == 0) landed = mbar_wait(&full[s], (i / kSwStages) & 1) ? 1 : 0;
+            if (lane == 0) landed = mbar_wait_spin(&full[s], (i / kSwStages) & 1) ? 1 : 0;
             landed = __shfl_sync(0xFFFFFFFFu, landed, 0);
             __syncwarp();
             if (!landed) {
@@ -250,6 +289,7 @@ linear_swap_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant
     bool ok = mbar_wait(&done, 0);
     tc_fence_after();
     ok = __syncthreads_and(ok && !s_fail);
+    const bool has_steps = n_base + s_ngroups > 0;   // an accumulator with no MMA is left unwritten
     float* red = reinterpret_cast<float*>(ring);   // [n_pad][kSwRedPitch]; the ring is consumed
     if (warp >= 2) {
         const int quarter = warp & 3;               // the tensor-memory lanes this warp may read
@@ -258,7 +298,7 @@ linear_swap_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant
             float d[16];
             tmem_ld16(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + j0, d);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) red[(j0 + j) * kSwRedPitch + c] = (n_steps > 0 && ok) ? d[j] : 0.f;
+            for (int j = 0; j < 16; ++j) red[(j0 + j) * kSwRedPitch + c] = (has_steps && ok) ? d[j] : 0.f;
         }
     }
     if (tid == 0 && !ok) s_fail = 1;
@@ -267,6 +307,7 @@ linear_swap_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant
         cluster_arrive();
         cluster_wait();
     }
+    grid_dep_wait();   // y and the status word are touched only after the preceding grid has completed
     // a failed peer has no valid partial: then nothing of the tile is written
     bool all_ok = true;
     for (int r = 0; r < P.cs; ++r) {
@@ -279,25 +320,35 @@ linear_swap_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant
     }
     // CTA crank sums columns [crank * 128 / cs, (crank + 1) * 128 / cs) of
     // every row over the cluster, 8 columns (one 16-byte piece of y) per item
-    const int c_lo = crank * kSwM / P.cs, c_hi = (crank + 1) * kSwM / P.cs;
+    // (in 8-column pieces: 16 pieces per tile shared out as evenly as cs allows)
+    const int c_lo = crank * (kSwM / 8) / P.cs * 8, c_hi = (crank + 1) * (kSwM / 8) / P.cs * 8;
     const int per_row = (c_hi - c_lo) / 8;
     const uint32_t red_s = smem_u32(red);
     for (int it = tid; it < P.n_rows * per_row; it += kSwThreads) {
         const int t = it / per_row, c = c_lo + (it - t * per_row) * 8;
+        // every peer's two pieces requested at once, then summed in rank order
+        const uint32_t src = red_s + 4u * static_cast<uint32_t>(t * kSwRedPitch + c);
+        float4 f0[kSwMaxSplit], f1[kSwMaxSplit];
+#pragma unroll
+        for (int r = 0; r < kSwMaxSplit; ++r)
+            if (r < P.cs) {
+                const uint32_t at = P.cs > 1 ? map_rank(src, r) : src;
+                f0[r] = ld_dsmem_f4(at);
+                f1[r] = ld_dsmem_f4(at + 16);
+            }
         float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int r = 0; r < P.cs; ++r) {
-            const uint32_t src = red_s + 4u * static_cast<uint32_t>(t * kSwRedPitch + c);
-            const uint32_t at = P.cs > 1 ? map_rank(src, r) : src;
-            const float4 f0 = ld_dsmem_f4(at), f1 = ld_dsmem_f4(at + 16);
-            v[0] += f0.x;
-            v[1] += f0.y;
-            v[2] += f0.z;
-            v[3] += f0.w;
-            v[4] += f1.x;
-            v[5] += f1.y;
-            v[6] += f1.z;
-            v[7] += f1.w;
-        }
+#pragma unroll
+        for (int r = 0; r < kSwMaxSplit; ++r)
+            if (r < P.cs) {
+                v[0] += f0[r].x;
+                v[1] += f0[r].y;
+                v[2] += f0[r].z;
+                v[3] += f0[r].w;
+                v[4] += f1[r].x;
+                v[5] += f1[r].y;
+                v[6] += f1[r].z;
+                v[7] += f1[r].w;
+            }
         if (all_ok && c < ncols) {
             uint4 o;
             o.x = pack_bf16x2(v[0], v[1]);
@@ -384,7 +435,9 @@ cudaError_t launch_linear_swap(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, i
         configured_device = dev;
     }
     // Split K so the column tiles' clusters cover the SMs (two CTAs fit on
-    // an SM), each CTA keeping at least two K blocks.
+    // an SM), each CTA keeping at least two K blocks.  (One CTA per SM with
+    // a six-stage ring, splits of 3 and 6 filling the SMs once, was slower:
+    // 57 against 43 us per Llama-3.2-3B decode layer.)
     int cs = 1;
     while (cs < kSwMaxSplit && static_cast<long long>(n_ct) * cs < n_sms && P.n_kb >= 4 * cs) cs *= 2;
     cs = std::max(1, std::min({env_int("LORA_SWAP_SPLIT", cs), kSwMaxSplit, P.n_kb}));
@@ -394,13 +447,15 @@ cudaError_t launch_linear_swap(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, i
     cfg.blockDim = dim3(kSwThreads);
     cfg.dynamicSmemBytes = swap_smem();
     cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = cs;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, linear_swap_kernel, mx, mw, mvh, mvl, mb[0], mb[1], mb[2], mb[3], P);
     note_launch();
     return e;

@@ -162,6 +162,12 @@ __device__ __forceinline__ void named_barrier(int id, int count)
 {
     asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
 }
+// Arrival on such a barrier without waiting (the producer side of a
+// hand-off: the waiting side calls named_barrier with the same count).
+__device__ __forceinline__ void named_barrier_arrive(int id, int count)
+{
+    asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
 
 // ---- tensor memory --------------------------------------------------------
 

@@ -226,8 +226,11 @@ SPLIT_CASES = {
 @pytest.mark.parametrize("name", list(SPLIT_CASES))
 def test_linear_split_k_small_batches(name, split, monkeypatch):
     """Batches of at most 128 rows with K split over a cluster of 2-8 CTAs
-    (partials summed through distributed shared memory) and without."""
+    (partials summed through distributed shared memory) and without, in the
+    persistent tile kernel (batches of at most 64 rows would otherwise take
+    the turned-around tile, tested below)."""
     monkeypatch.setenv("LORA_LINEAR_SPLIT", str(split))
+    monkeypatch.setenv("LORA_LINEAR_SWAP", "0")
     st, x, W, ads, ids, meta = _case(**SPLIT_CASES[name], seed=40 + split)
     got, status = _run(st, x, W, meta)
     assert status == 0
@@ -269,13 +272,14 @@ SWAP_CASES = {
 }
 
 
-@pytest.mark.parametrize("split", [None, "1", "2", "8"])
+@pytest.mark.parametrize("split", [None, "1", "2", "3", "6", "8"])
 @pytest.mark.parametrize("name", list(SWAP_CASES))
 def test_linear_decode_sized_vs_oracle(name, split, monkeypatch):
     """Batches of at most 64 rows take the turned-around tile (128 output
     columns as the MMA's M, the rows as its N, K split over a cluster, one K
     extension per adapter present): every element against the oracle, for
-    each cluster split the launcher may choose."""
+    each cluster split the launcher may choose (sizes 3 and 6 leave the
+    tile's 16 column pieces shared out unevenly)."""
     if split is not None:
         if name not in ("five_rows_ragged", "rank64", "many_adapters"):
             pytest.skip("splits are exercised on three shapes")
