@@ -148,18 +148,21 @@ ROUTE_KERNELS = {
 # only for the linear layer); valid only while the listed kernel sources
 # hash to `src`.
 NCU_TRAFFIC = {
-    "llama3b_decode": {"files": ['bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "010059f8745e9b90",
-             "bytes_per_call": 3438272},
-    "stress70b": {"files": ['bgmv_grouped.cu', 'decode_common.cuh', 'common.cuh'], "src": "0d1b3c3b8322d136",
-             "bytes_per_call": 988209024},
-    "mistral7b_prefill": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "e1e55b430f7ab83b",
-             "bytes_per_call": 2060608192},
+    "llama3b_decode": {"files": ['bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "b264cebf48604b0c",
+             "bytes_per_call": 3442880},
+    "stress70b": {"files": ['bgmv_grouped.cu', 'decode_common.cuh', 'common.cuh'], "src": "ba1c9ca552bedd58",
+             "bytes_per_call": 988152576},
+    "mistral7b_prefill": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "19155bd8848086dc",
+             "bytes_per_call": 2061788096},
     "merge_mistral7b": {"files": ['merge.cu', 'decode_common.cuh', 'common.cuh'], "src": "64c410c3e24d8148",
              "bytes_per_step": 6994841856},
-    "linear_mistral7b_prefill": {"files": ['linear_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "f502730f1fa519ab",
-             "bytes_per_step": 19274225664},
-    "mixed": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "304df0d5fa9a8122",
-             "bytes_per_call": 113018240},
+    "linear_mistral7b_prefill": {"files": ['linear_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "2967019a7ab0382c",
+             "bytes_per_step": 19454782208},
+    "mixed": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "b16a389cb54688e0",
+             "bytes_per_call": 113133120},
+    # captured on 2 layers, scaled to the 28 of a step (every layer has the same shapes)
+    "linear_llama3b_decode": {"files": ['linear_swap.cu', 'bgmv_grouped.cu', 'tc_common.cuh', 'tmap.cpp', 'decode_common.cuh', 'common.cuh'],
+             "src": "329bae22d97a6d8b", "bytes_per_step": 1602936832},
 }
 
 
@@ -832,7 +835,7 @@ def run_linear_decode(args, rank, local, ws):
         "roofline": {"kernel": "linear_swap_kernel (+ bgmv_group_shrink_kernel per call)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} hbm_gbs", "per": "step", "bytes_per_step": bytes_step,
-                     "traffic": None},
+                     "traffic": recorded_traffic(LINEAR_DECODE_WORKLOAD) if layers == LAYERS[name] else None},
         "clocks": clk,
         "gpu_launches": int(launches * args.steps),
         "e2e": None,
