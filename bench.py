@@ -154,8 +154,8 @@ NCU_TRAFFIC = {
              "bytes_per_call": 988152576},
     "mistral7b_prefill": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "19155bd8848086dc",
              "bytes_per_call": 2061788096},
-    "merge_mistral7b": {"files": ['merge.cu', 'decode_common.cuh', 'common.cuh'], "src": "64c410c3e24d8148",
-             "bytes_per_step": 6994841856},
+    "merge_mistral7b": {"files": ['merge.cu', 'merge_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "a42607bd1f8823b7",
+             "bytes_per_step": 6934879914},
     "linear_mistral7b_prefill": {"files": ['linear_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "2967019a7ab0382c",
              "bytes_per_step": 19454782208},
     "mixed": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "b16a389cb54688e0",
@@ -438,7 +438,7 @@ def run_merge(args, rank, local, ws):
                          f"{torch.cuda.get_device_properties(dev).L2_cache_size / 1e6:.0f} MB)",
                    "timing": "CUDA graph of one batched merge then one batched unmerge of every weight; CUDA events",
                    "parallelism": f"replicas x{ws}"},
-        "roofline": {"kernel": "merge_batch_kernel", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+        "roofline": {"kernel": "merge_tc_kernel", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
                      "per": "step", "bytes_per_step": bytes_step, "traffic": recorded_traffic(MERGE_WORKLOAD, layers)},
         "clocks": clk,
@@ -1352,8 +1352,24 @@ def run_all(args, rank, local, ws):
         d["config"] = line["config"]
         per[name] = d
     out["per_config"] = per
-    out["gpu_launches"] = out["gpu_launches"] + sum(d["gpu_launches"] for d in per.values())
-    out["gpu_launches_note"] = "timed launches of the headline and of every per_config line"
+    # The rows beyond the delta itself (merge / unmerge, adapter slot loads,
+    # the standalone calls, the LoRA linear layer in both forms), each with
+    # its own metric, trimmed: no e2e and no oracle leg.
+    extra = {}
+    trimmed = argparse.Namespace(**{**vars(args), "no_e2e": True, "no_cpu_baseline": True, "layers": None,
+                                    "seqs": None})
+    for wname, fn in ((MERGE_WORKLOAD, run_merge), (SLOTS_WORKLOAD, run_slots),
+                      (STANDALONE_WORKLOAD, run_standalone), (LINEAR_DECODE_WORKLOAD, run_linear_decode),
+                      (LINEAR_WORKLOAD, run_linear)):
+        line = fn(trimmed, rank, local, ws)
+        extra[wname] = {k: line[k] for k in ("metric", "value", "unit", "ms_per_step", "roofline", "clocks",
+                                             "gpu_launches", "config") if k in line}
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    out["extra_workloads"] = extra
+    out["gpu_launches"] = (out["gpu_launches"] + sum(d["gpu_launches"] for d in per.values())
+                           + sum(d.get("gpu_launches", 0) for d in extra.values()))
+    out["gpu_launches_note"] = "timed launches of the headline, of every per_config line and of extra_workloads"
     return out
 
 

@@ -129,5 +129,9 @@ cudaError_t launch_merge(bf16_t* W, int ld_w, int out, int h_in, const bf16_t* A
 cudaError_t launch_merge_batch(int n, bf16_t* const* W, const int* ld_w, const int* out, const int* h_in,
                                const bf16_t* const* A, const bf16_t* const* B, int r_slot, int sign,
                                cudaStream_t stream);
+// The tensor-memory form of both (slot ranks up to 64).
+bool merge_tc_supported(int r_slot);
+cudaError_t launch_merge_tc(int n, bf16_t* const* W, const int* ld_w, const int* out, const int* h_in,
+                            const bf16_t* const* A, const bf16_t* const* B, int r_slot, int sign, cudaStream_t stream);
 
 }  // namespace lora

@@ -7,6 +7,9 @@
 // sign = +1 (merge) or -1 (unmerge), B' the folded store (scale applied),
 // the sum in fp32 over the slot rank (padding ranks are zero).
 //
+// Slot ranks up to 64 take the tensor-memory kernel of merge_tc.cu; the
+// kernels here serve larger ranks (and LORA_MERGE_TC=0).
+//
 // One CTA per 128 x 128 tile of W: its 128 rows of B' and 128 columns of A
 // arrive by 16-byte cp.async, then the tile itself (a second group, needed
 // only by the epilogue, so it lands while the MMAs run); warp w forms rows
@@ -223,9 +226,14 @@ cudaError_t configure_merge(int& n_sms)
 
 }  // namespace
 
+// Slot ranks up to 64 take the tensor-memory kernel (merge_tc.cu) unless
+// LORA_MERGE_TC=0; larger ranks take the kernels above.
+static bool use_merge_tc(int r_slot) { return merge_tc_supported(r_slot) && env_int("LORA_MERGE_TC", 1) != 0; }
+
 cudaError_t launch_merge(bf16_t* W, int ld_w, int out, int h_in, const bf16_t* A, const bf16_t* B, int r_slot,
                          int sign, cudaStream_t stream)
 {
+    if (use_merge_tc(r_slot)) return launch_merge_tc(1, &W, &ld_w, &out, &h_in, &A, &B, r_slot, sign, stream);
     MergeParams p{};
     p.n = 1;
     p.w[0] = MergeWeight{W, A, B, ld_w, out, h_in, (h_in + kMCols - 1) / kMCols, 0};
@@ -245,6 +253,7 @@ cudaError_t launch_merge_batch(int n, bf16_t* const* W, const int* ld_w, const i
                                const bf16_t* const* A, const bf16_t* const* B, int r_slot, int sign,
                                cudaStream_t stream)
 {
+    if (use_merge_tc(r_slot)) return launch_merge_tc(n, W, ld_w, out, h_in, A, B, r_slot, sign, stream);
     int n_sms = 0;
     cudaError_t e = configure_merge(n_sms);
     if (e != cudaSuccess) return e;
