@@ -31,6 +31,23 @@ __device__ __forceinline__ float2 ld_dsmem_f2(uint32_t remote)
     asm("ld.shared::cluster.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "r"(remote));
     return v;
 }
+// A 32-bit store into a peer CTA's shared memory (published to it by the
+// next cluster barrier).
+__device__ __forceinline__ void st_dsmem_u32(uint32_t remote, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;\n" ::"r"(remote), "r"(v) : "memory");
+}
+
+// Four fp32 values into a peer CTA's shared memory, completing 16 bytes of
+// the transaction count of the peer's mbarrier at remote_bar.
+__device__ __forceinline__ void st_async_f4(uint32_t remote, float a, float b, float c, float d, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];\n" ::"r"(
+                     remote),
+                 "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t remote)
 {
     float4 v;

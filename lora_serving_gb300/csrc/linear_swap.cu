@@ -94,12 +94,13 @@ linear_swap_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant
                    const __grid_constant__ CUtensorMap mb2, const __grid_constant__ CUtensorMap mb3, SwapParams P)
 {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full[kSwStages], empty[kSwStages], done;
+    __shared__ __align__(8) uint64_t full[kSwStages], empty[kSwStages], done, recv_bar;
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_fail;
     __shared__ int s_slot[kSwMaxN];                 // this CTA's adapter slots (LoRA steps)
     __shared__ unsigned long long s_mask[kSwMaxN];  // rows of each of them
     __shared__ int s_ngroups, s_badid;
+    __shared__ int s_peer_fail[kSwMaxSplit];        // the cluster's failure flags, written by each CTA
     // Programmatic dependent launch: x, W, B' and the ids are read at once
     // (none is written by the shrink before this kernel), the base steps
     // run while the shrink finishes; v, y and the status word wait for it.
@@ -117,52 +118,61 @@ linear_swap_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant
     // first appearance, the g-th taken by cluster rank g % cs
     const int kb0 = crank * P.n_kb / P.cs;
     const int n_base = (crank + 1) * P.n_kb / P.cs - kb0;
-    __shared__ int s_ids[kSwMaxN];
-    if (tid < kSwMaxN) s_ids[tid] = tid < P.n_rows ? __ldg(P.ids + tid) : -1;
+    // tile columns [c_lo, c_hi) are summed over the cluster by this CTA: 8
+    // columns (one 16-byte piece of y) at a time, the 16 pieces shared out
+    // as evenly as cs allows
+    const int c_lo = crank * (kSwM / 8) / P.cs * 8, c_hi = (crank + 1) * (kSwM / 8) / P.cs * 8;
+    const int n_own = c_hi - c_lo;
+    const uint32_t b_bytes = static_cast<uint32_t>(P.n_pad) * 128;
+
+    // ---- producer (warp 0, lane 0): the base steps (W box + x box) at
+    // once, the first ring's worth before the tensor memory is allocated;
+    // then, once warp 1 has scanned the groups, the LoRA steps (B' box + v
+    // boxes) ----
+    int issued = 0;
+    auto issue = [&](int i) -> bool {
+        const int s = i % kSwStages;
+        if (i >= kSwStages && !mbar_wait_spin(&empty[s], ((i / kSwStages) - 1) & 1)) return false;
+        uint8_t* st = ring + s * kSwStageBytes;
+        if (i < n_base) {
+            const int k = (kb0 + i) * kSwK;
+            mbar_expect_tx(&full[s], kSwABytes + b_bytes);
+            tma_load_2d(st, &mw, k, P.w_row[p] + col0, &full[s]);
+            tma_load_2d(st + kSwABytes, &mx, k, 0, &full[s]);
+        } else {
+            if (i == n_base) grid_dep_wait();   // v is the preceding kernel's output
+            const int g = i - n_base;
+            mbar_expect_tx(&full[s], kSwABytes + 2 * b_bytes);
+            tma_load_2d(st, bmap, 0, s_slot[g] * P.width[p] + col0, &full[s]);
+            tma_load_3d(st + kSwABytes, &mvh, 0, p, 0, &full[s]);
+            tma_load_3d(st + kSwABytes + kSwBBytes, &mvl, 0, p, 0, &full[s]);
+        }
+        issued = i + 1;
+        return true;
+    };
     if (tid == 0) {
         for (int s = 0; s < kSwStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         mbar_init(&done, 1);
+        mbar_init(&recv_bar, 1);
         mbar_init_fence();
+        // the partials of this CTA's columns, from every CTA of the cluster
+        if (P.cs > 1) mbar_expect_tx(&recv_bar, static_cast<unsigned>(P.cs * n_own * P.n_pad) * 4u);
         s_fail = 0;
+        for (int i = 0; i < min(n_base, kSwStages); ++i) issue(i);   // no wait: the ring is empty
     }
     if (warp == 0) tmem_alloc(&s_tmem, kSwMaxN);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    const uint32_t b_bytes = static_cast<uint32_t>(P.n_pad) * 128;
 
     if (warp == 0) {
-        // ---- producer (lane 0): the base steps (W box + x box) at once;
-        // then, once warp 1 has scanned the groups, the LoRA steps (B' box +
-        // v boxes) ----
-        int issued = 0;
-        auto issue = [&](int i) -> bool {
-            const int s = i % kSwStages;
-            if (i >= kSwStages && !mbar_wait_spin(&empty[s], ((i / kSwStages) - 1) & 1)) return false;
-            uint8_t* st = ring + s * kSwStageBytes;
-            if (i < n_base) {
-                const int k = (kb0 + i) * kSwK;
-                mbar_expect_tx(&full[s], kSwABytes + b_bytes);
-                tma_load_2d(st, &mw, k, P.w_row[p] + col0, &full[s]);
-                tma_load_2d(st + kSwABytes, &mx, k, 0, &full[s]);
-            } else {
-                if (i == n_base) grid_dep_wait();   // v is the preceding kernel's output
-                const int g = i - n_base;
-                mbar_expect_tx(&full[s], kSwABytes + 2 * b_bytes);
-                tma_load_2d(st, bmap, 0, s_slot[g] * P.width[p] + col0, &full[s]);
-                tma_load_3d(st + kSwABytes, &mvh, 0, p, 0, &full[s]);
-                tma_load_3d(st + kSwABytes + kSwBBytes, &mvl, 0, p, 0, &full[s]);
-            }
-            issued = i + 1;
-            return true;
-        };
         bool ok = true;
         if (lane == 0)
-            for (int i = 0; i < n_base && ok && !s_fail; ++i) ok = issue(i);
+            for (int i = issued; i < n_base && ok && !s_fail; ++i) ok = issue(i);
         __syncwarp();
         // warp 1 has arrived after its group scan (it does not wait here: it
         // goes on to consume the base steps)
@@ -187,7 +197,7 @@ linear_swap_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int t = lane + 32 * h;
-                idv[h] = s_ids[t];
+                idv[h] = t < P.n_rows ? __ldg(P.ids + t) : -1;
                 bad |= t < P.n_rows && (idv[h] < -1 || idv[h] >= P.n_slots);
             }
             // rows of each half naming the same slot as this lane's row
@@ -285,88 +295,94 @@ linear_swap_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant
         __syncwarp();
     }
 
-    // ---- epilogue: accumulator (lane = column, column j = row) -> transposed partial ----
+    // ---- epilogue: each column's fp32 partial (accumulator lane = column,
+    // accumulator column = row) goes to the CTA that sums that column over
+    // the cluster; it lands in that CTA's ring, idle once the cluster
+    // barrier below has passed ----
     bool ok = mbar_wait(&done, 0);
     tc_fence_after();
     ok = __syncthreads_and(ok && !s_fail);
     const bool has_steps = n_base + s_ngroups > 0;   // an accumulator with no MMA is left unwritten
-    float* red = reinterpret_cast<float*>(ring);   // [n_pad][kSwRedPitch]; the ring is consumed
-    if (warp >= 2) {
-        const int quarter = warp & 3;               // the tensor-memory lanes this warp may read
-        const int c = quarter * 32 + lane;          // tile column
-        for (int j0 = 0; j0 < P.n_pad; j0 += 16) {
-            float d[16];
-            tmem_ld16(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + j0, d);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) red[(j0 + j) * kSwRedPitch + c] = (has_steps && ok) ? d[j] : 0.f;
-        }
-    }
     if (tid == 0 && !ok) s_fail = 1;
     __syncthreads();
+    // this CTA's failure flag into every peer's s_peer_fail[crank]: the
+    // cluster barrier publishes them, so the check below reads local memory
+    if (tid < P.cs) {
+        if (P.cs > 1)
+            st_dsmem_u32(map_rank(smem_u32(&s_peer_fail[crank]), tid), s_fail);
+        else
+            s_peer_fail[0] = s_fail;
+    }
     if (P.cs > 1) {
         cluster_arrive();
         cluster_wait();
     }
-    grid_dep_wait();   // y and the status word are touched only after the preceding grid has completed
-    // a failed peer has no valid partial: then nothing of the tile is written
-    bool all_ok = true;
-    for (int r = 0; r < P.cs; ++r) {
-        int f;
-        asm volatile("ld.shared::cluster.b32 %0, [%1];\n"
-                     : "=r"(f)
-                     : "r"(P.cs > 1 ? map_rank(smem_u32(const_cast<int*>(&s_fail)), r) : smem_u32(const_cast<int*>(&s_fail)))
-                     : "memory");
-        if (f) all_ok = false;
+    // receive buffer of every CTA: [source rank][own column][row] fp32
+    float* recv = reinterpret_cast<float*>(ring);
+    if (warp >= 2) {
+        const int quarter = warp & 3;               // the tensor-memory lanes this warp may read
+        const int c = quarter * 32 + lane;          // tile column
+        int r = 0;                                  // the CTA that sums column c
+        while (r + 1 < P.cs && c >= (r + 1) * (kSwM / 8) / P.cs * 8) ++r;
+        const int lo_r = r * (kSwM / 8) / P.cs * 8, n_r = (r + 1) * (kSwM / 8) / P.cs * 8 - lo_r;
+        const int off = (crank * n_r + (c - lo_r)) * P.n_pad;
+        const uint32_t dst = P.cs > 1 ? map_rank(smem_u32(recv + off), r) : 0u;
+        const uint32_t bar = P.cs > 1 ? map_rank(smem_u32(&recv_bar), r) : 0u;
+        for (int j0 = 0; j0 < P.n_pad; j0 += 16) {
+            float d[16];
+            tmem_ld16(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + j0, d);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) d[j] = (has_steps && ok) ? d[j] : 0.f;
+            if (P.cs > 1) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    st_async_f4(dst + 4u * static_cast<uint32_t>(j0 + 4 * q4), d[4 * q4], d[4 * q4 + 1], d[4 * q4 + 2],
+                                d[4 * q4 + 3], bar);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) recv[off + j0 + j] = d[j];
+            }
+        }
     }
-    // CTA crank sums columns [crank * 128 / cs, (crank + 1) * 128 / cs) of
-    // every row over the cluster, 8 columns (one 16-byte piece of y) per item
-    // (in 8-column pieces: 16 pieces per tile shared out as evenly as cs allows)
-    const int c_lo = crank * (kSwM / 8) / P.cs * 8, c_hi = (crank + 1) * (kSwM / 8) / P.cs * 8;
-    const int per_row = (c_hi - c_lo) / 8;
-    const uint32_t red_s = smem_u32(red);
+    grid_dep_wait();   // y and the status word are touched only after the preceding grid has completed
+    bool got = true;
+    if (P.cs > 1)
+        got = mbar_wait(&recv_bar, 0);
+    else
+        __syncthreads();
+    // a failed peer has no valid partial: then nothing of the tile is written
+    bool all_ok = got;
+    for (int r = 0; r < P.cs; ++r)
+        if (s_peer_fail[r]) all_ok = false;
+    // rows fastest across the threads (conflict-free reads of recv); the
+    // sources are summed in rank order
+    const int per_row = n_own / 8;
     for (int it = tid; it < P.n_rows * per_row; it += kSwThreads) {
-        const int t = it / per_row, c = c_lo + (it - t * per_row) * 8;
-        // every peer's two pieces requested at once, then summed in rank order
-        const uint32_t src = red_s + 4u * static_cast<uint32_t>(t * kSwRedPitch + c);
-        float4 f0[kSwMaxSplit], f1[kSwMaxSplit];
-#pragma unroll
-        for (int r = 0; r < kSwMaxSplit; ++r)
-            if (r < P.cs) {
-                const uint32_t at = P.cs > 1 ? map_rank(src, r) : src;
-                f0[r] = ld_dsmem_f4(at);
-                f1[r] = ld_dsmem_f4(at + 16);
-            }
+        const int piece = it / P.n_rows, t = it - piece * P.n_rows;
+        const int lc = piece * 8;
         float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int src = 0; src < P.cs; ++src) {
+            const float* rp = recv + (src * n_own + lc) * P.n_pad + t;
 #pragma unroll
-        for (int r = 0; r < kSwMaxSplit; ++r)
-            if (r < P.cs) {
-                v[0] += f0[r].x;
-                v[1] += f0[r].y;
-                v[2] += f0[r].z;
-                v[3] += f0[r].w;
-                v[4] += f1[r].x;
-                v[5] += f1[r].y;
-                v[6] += f1[r].z;
-                v[7] += f1[r].w;
-            }
-        if (all_ok && c < ncols) {
+            for (int e = 0; e < 8; ++e) v[e] += rp[e * P.n_pad];
+        }
+        if (all_ok && c_lo + lc < ncols) {
             uint4 o;
             o.x = pack_bf16x2(v[0], v[1]);
             o.y = pack_bf16x2(v[2], v[3]);
             o.z = pack_bf16x2(v[4], v[5]);
             o.w = pack_bf16x2(v[6], v[7]);
-            *reinterpret_cast<uint4*>(P.y + static_cast<size_t>(t) * P.ld_y + P.out_off[p] + col0 + c) = o;
+            *reinterpret_cast<uint4*>(P.y + static_cast<size_t>(t) * P.ld_y + P.out_off[p] + col0 + c_lo + lc) = o;
         }
     }
-    if (P.cs > 1) {
-        cluster_arrive();   // peers may leave once everyone has read their partials
-        cluster_wait();
-    }
+    // no peer reads this CTA's memory, and every write into it has landed
+    // (the receive barrier): the CTA may leave without a second cluster barrier
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kSwMaxN);
     if (tid == 0) {
         if (!all_ok && s_fail) flag(P.status, LORA_DEV_TIMEOUT);
+        if (!got) flag(P.status, LORA_DEV_TIMEOUT);
         if (s_badid && tile == 0 && crank == 0) flag(P.status, LORA_DEV_SLOT_OUT_OF_RANGE);
     }
 }
