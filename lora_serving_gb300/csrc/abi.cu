@@ -415,10 +415,18 @@ lora_status_t lora_linear(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld
                                                                   meta->max_seg_len, T, n_slots, LORA_APPLY_NO_PDL,
                                                                   vh, vl, dev_status, s)));
     }
+    // The decode rows' shrink, when it is the call's first kernel, starts
+    // early (its adapter rows load while the kernel before it finishes) and
+    // lets the linear kernel launch once everything before the call has
+    // completed, since that kernel reads x at once.
+    const bool first_kernel = !(P > 0 && meta->n_segs > 0);
+    const unsigned dshrink_flags = first_kernel && env_int_abi("LORA_LINEAR_SHRINK_PDL", 1) != 0
+                                       ? lora::kShrinkTriggerLate
+                                       : LORA_APPLY_NO_PDL;
     if (D > 0 && meta->n_gsegs > 0)
         LORA_TRY(cuda_status(lora::launch_bgmv_grouped_shrink(x, ld_x, h_in, ps, meta->perm, meta->gseg_starts,
                                                               meta->gseg_slot, meta->n_gsegs, D, meta->max_gseg_len,
-                                                              T, n_slots, LORA_APPLY_NO_PDL, vh, vl, dev_status,
+                                                              T, n_slots, dshrink_flags, vh, vl, dev_status,
                                                               s)));
     // base product with the delta in the same accumulator: decode-sized
     // batches turn the tile around (the weights are the bytes), larger ones

@@ -132,6 +132,7 @@ struct GsParams {
     int kc;                   // K elements per cluster rank (multiple of kGsKT)
     int ks;                   // cluster size (CTAs splitting K)
     int x_ready;
+    int late_trigger;         // dependents launch only once x may be read (see kShrinkTriggerLate)
     int32_t* status;
 };
 
@@ -150,7 +151,7 @@ bgmv_group_shrink_kernel(GsParams p)
     __shared__ __align__(16) float s_vp[kRB * kGsRanks];
     __shared__ int s_rows[kRB];
 
-    grid_dep_launch();
+    if (!p.late_trigger) grid_dep_launch();
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int crank = p.ks > 1 ? static_cast<int>(cluster_rank()) : 0;
@@ -252,6 +253,7 @@ bgmv_group_shrink_kernel(GsParams p)
         grid_dep_wait();
         waited = true;
     }
+    if (p.late_trigger) grid_dep_launch();   // everything before this kernel is complete: x may be read
 #pragma unroll
     for (int st = 0; st < kGsStages; ++st) {
         if (st < n_kt) issue_X(st, st);
@@ -660,6 +662,7 @@ cudaError_t grouped_shrink(const GroupedPlan& g, const bf16_t* x, int ld_x, int 
     sp.ks = ks;
     sp.kc = ((h_in + ks - 1) / ks + kGsKT - 1) / kGsKT * kGsKT;
     sp.x_ready = (flags & LORA_APPLY_X_READY) ? 1 : 0;
+    sp.late_trigger = (flags & kShrinkTriggerLate) ? 1 : 0;
     sp.status = status;
     const long long n_shrink = g.units * sp.n_rb * ks;
     if (n_shrink > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;

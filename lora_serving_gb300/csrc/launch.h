@@ -117,6 +117,13 @@ cudaError_t launch_linear_tc(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int
 // The same layer for decode-sized batches (n_rows <= 64, r_slot <= 64): the
 // tile turned around (128 output columns as the MMA's M, the rows as its N),
 // K split over a cluster, the delta a K extension per adapter slot present.
+// Internal launch flag (beside the public LORA_APPLY_* bits) for the grouped
+// shrink: its dependents may launch only once its grid dependency has
+// resolved, i.e. once everything enqueued before it has completed.  A
+// following kernel that reads x (or anything else written earlier) at
+// once may then start early behind a shrink that itself starts early.
+constexpr unsigned kShrinkTriggerLate = 0x100u;
+
 bool linear_swap_supported(int n_rows, int r_slot);
 cudaError_t launch_linear_swap(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int h_in, const bf16_t* W, int ld_w,
                                int n_out, const ProjSet& ps, const bf16_t* vh, const bf16_t* vl, const int32_t* ids,
