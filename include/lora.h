@@ -78,10 +78,11 @@ typedef enum {
 #define LORA_DEV_BAD_SEGMENT 0x2       /* a segment/perm entry fell outside its rows, or a
                                           group outgrew meta->max_gseg_len; rows skipped */
 #define LORA_DEV_TIMEOUT 0x4           /* an asynchronous copy did not land within 0.2 s (never
-                                          expected): the kernel that waited leaves its rows of y
-                                          unwritten, or, if it was a shrink, stores a zero
-                                          intermediate for them so the expand adds nothing; the
-                                          call returns and later calls are unaffected */
+                                          expected): the kernel that waited stops; rows of y it
+                                          had not finished keep their previous values (a shrink
+                                          stores a zero intermediate for its unfinished rows, so
+                                          the expand adds nothing); the call returns and later
+                                          calls are unaffected */
 
 /* Largest r_slot (rank of one projection's slot) the kernels accept. */
 #define LORA_MAX_RANK 128

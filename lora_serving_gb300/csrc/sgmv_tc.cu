@@ -394,16 +394,22 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
 // The row tiles of a CTA's items are resolved once, at its start, into a
 // shared-memory table.  The v_hi / v_lo slice of an item (row tile,
 // projection) is loaded once into one of two buffers (one when r_pad64 > 64),
-// so the next item's slice loads while the current one's tiles finish; B'
-// and y tiles stream through a TMA ring of up to kStagesE stages; the fp32 accumulator
-// is double-buffered in tensor memory, so the epilogue of tile i (TMEM ->
-// registers, + y from shared memory, round, store) overlaps the loads and
-// MMAs of tile i+1.
-//   warp 0: TMA producer      warp 1: MMA issuer      warps 2..17: epilogue
+// so the next item's slice loads while the current one's tiles finish.  A
+// tile's B' boxes (from L2) go through a two-stage ring that the MMA's
+// completion frees; its y tile (from HBM) through a ring of up to kStagesY
+// stages, each held from its load until the store has read it back, which
+// is why the two do not share stages.  The fp32 accumulator is
+// double-buffered in tensor memory, so the epilogue of tile i (TMEM ->
+// registers, + y from shared memory, round) overlaps the loads and MMAs of
+// tile i+1, and a store warp writes finished tiles back, so that no
+// epilogue warp waits on a store.
+//   warp 0: TMA producer   warp 1: MMA issuer   warps 2..17: epilogue
+//   warp 18: TMA store
 
-constexpr int kStagesE = 4;        // ring stages, at most (the launcher picks 3 or 4, or 2 for r_pad64 = 128)
+constexpr int kStagesY = 5;        // y ring stages, at most (the launcher picks 3 to 5)
 constexpr int kEpiWarps = 16;       // 4 per TMEM lane quarter, 32 columns each
-constexpr int kExpandThreadsP = 32 * (2 + kEpiWarps);
+constexpr int kStoreWarpE = 2 + kEpiWarps;
+constexpr int kExpandThreadsP = 32 * (kStoreWarpE + 1);
 constexpr int kChunkMax = 16;       // output tiles per work item, at most
 constexpr int kMaxItems = 64;       // work items per CTA (the launcher sizes the grid)
 
@@ -420,9 +426,9 @@ struct ExpandTcParams {
     int n_segs, n_pos, n_rows;
     bf16_t* y;
     int ld_y;
-    int stages;                     // ring stages (<= kStagesE)
+    int stages;                     // y ring stages (<= kStagesY)
     int vbufs;                      // v slice buffers (1 or 2)
-    unsigned stall_tx;              // test hook: extra bytes expected on the first ring stage (0 normally)
+    unsigned stall_tx;              // test hook: extra bytes expected on the first B' stage (0 normally)
     int32_t* status;
 };
 
@@ -524,8 +530,8 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
                       const __grid_constant__ CUtensorMap mb3, ExpandTcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full[kStagesE], empty[kStagesE], acc_full[2], acc_empty[2];
-    __shared__ __align__(8) uint64_t v_full[2], v_empty[2];
+    __shared__ __align__(8) uint64_t yfull[kStagesY], yempty[kStagesY], epi_done[kStagesY];
+    __shared__ __align__(8) uint64_t bfull[2], bempty[2], acc_full[2], acc_empty[2], v_full[2], v_empty[2], mma_done;
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_fail;
     __shared__ RowTile s_rt[kMaxItems];
@@ -562,25 +568,31 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
 
     const CUtensorMap* bmap[4] = {&mb0, &mb1, &mb2, &mb3};
     const int kbs = p.r_pad64 / kKB;                         // K blocks per plane
-    const int S = p.stages;                                  // ring depth (shared memory permitting)
+    const int S = p.stages;                                  // y ring depth (shared memory permitting)
     const int VB = p.vbufs;                                  // v slice buffers
-    const int stage_bytes = (kbs + 2) * kBoxBytes;           // B' (kbs boxes) + y (2 boxes)
+    const int bstage_bytes = kbs * kBoxBytes;                // B' of one tile
+    const int ystage_bytes = 2 * kBoxBytes;                  // one y tile: two 64-column boxes
     const int vbuf_bytes = 2 * kbs * kBoxBytes;              // v_hi boxes, then v_lo boxes
     uint8_t* vbufs = align1024(smem_raw);                    // VB x [v_hi | v_lo]
-    uint8_t* ring = vbufs + VB * vbuf_bytes;                 // S x [B' | y]
+    uint8_t* bring = vbufs + VB * vbuf_bytes;                // 2 x B'
+    uint8_t* yring = bring + 2 * bstage_bytes;               // S x y
 
     if (warp == 0) tmem_alloc(&s_tmem, 2 * kExpandN);
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kEpiWarps / 2);   // released by the team that took the tile
+            mbar_init(&yfull[s], 1);
+            mbar_init(&yempty[s], 1);                 // the store warp
+            mbar_init(&epi_done[s], kEpiWarps / 2);   // the team that took the tile
         }
         for (int a = 0; a < 2; ++a) {
+            mbar_init(&bfull[a], 1);
+            mbar_init(&bempty[a], 1);                 // the MMA thread's commit
             mbar_init(&acc_full[a], 1);
             mbar_init(&acc_empty[a], kEpiWarps / 2);
             mbar_init(&v_full[a], 1);
             mbar_init(&v_empty[a], 1);
         }
+        mbar_init(&mma_done, 1);
         mbar_init_fence();
         s_fail = 0;
     }
@@ -594,7 +606,7 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
             TileIter tr;
             tr.init(p, n_rt);
             int k_prev = -1;
-            int issued = 0, v_issued = 0;   // ring stages and v slices armed so far
+            int y_issued = 0, b_issued = 0, v_issued = 0;   // stages and v slices armed so far
             for (int i = 0; !s_fail; ++i) {
                 const RowTile rt = s_rt[tr.k];
                 if (tr.k != k_prev) {   // a new item: its v slice into buffer k % VB
@@ -613,8 +625,10 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
                     }
                     v_issued = tr.k + 1;
                 }
-                const int s = i % S;
-                if (i >= S && !mbar_wait(&empty[s], ((i / S) - 1) & 1)) {
+                const int col0 = tr.ct * kExpandN;
+                // B' of the tile into B' stage i % 2
+                const int b = i & 1;
+                if (i >= 2 && !mbar_wait(&bempty[b], ((i >> 1) - 1) & 1)) {
                     s_fail = 1;
                     break;
                 }
@@ -622,21 +636,32 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
                 // s_fail first): re-arm it only while nothing has failed, so a
                 // stage whose previous phase never completed is never armed again.
                 if (s_fail) break;
-                uint8_t* st = ring + s * stage_bytes;
-                const int col0 = tr.ct * kExpandN;
-                mbar_expect_tx(&full[s], stage_bytes + (i == 0 ? p.stall_tx : 0u));
+                uint8_t* bs = bring + b * bstage_bytes;
+                mbar_expect_tx(&bfull[b], bstage_bytes + (i == 0 ? p.stall_tx : 0u));
                 for (int kb = 0; kb < kbs; ++kb)
-                    tma_load_2d(st + kb * kBoxBytes, bmap[tr.q], kb * kKB, rt.slot * p.width[tr.q] + col0, &full[s]);
+                    tma_load_2d(bs + kb * kBoxBytes, bmap[tr.q], kb * kKB, rt.slot * p.width[tr.q] + col0, &bfull[b]);
+                b_issued = i + 1;
+                // the y tile into y stage i % S
+                const int s = i % S;
+                if (i >= S && !mbar_wait(&yempty[s], ((i / S) - 1) & 1)) {
+                    s_fail = 1;
+                    break;
+                }
+                if (s_fail) break;
+                uint8_t* ys = yring + s * ystage_bytes;
+                mbar_expect_tx(&yfull[s], ystage_bytes);
                 const int ycol = p.out_off[tr.q] + col0;
-                tma_load_2d(st + kbs * kBoxBytes, &my, ycol, rt.row0, &full[s]);
-                tma_load_2d(st + (kbs + 1) * kBoxBytes, &my, ycol + kKB, rt.row0, &full[s]);
-                issued = i + 1;
+                tma_load_2d(ys, &my, ycol, rt.row0, &yfull[s]);
+                tma_load_2d(ys + kBoxBytes, &my, ycol + kKB, rt.row0, &yfull[s]);
+                y_issued = i + 1;
                 if (!tr.next(p, n_rt, n_items)) break;
             }
             // Every copy issued has landed before the CTA moves on (after a
-            // normal run the MMA thread has seen each of these phases complete).
-            for (int i = issued > S ? issued - S : 0; i < issued; ++i)
-                if (!mbar_wait(&full[i % S], (i / S) & 1)) s_fail = 1;
+            // normal run the consumers have seen each of these phases complete).
+            for (int i = y_issued > S ? y_issued - S : 0; i < y_issued; ++i)
+                if (!mbar_wait(&yfull[i % S], (i / S) & 1)) s_fail = 1;
+            for (int i = b_issued > 2 ? b_issued - 2 : 0; i < b_issued; ++i)
+                if (!mbar_wait(&bfull[i & 1], (i >> 1) & 1)) s_fail = 1;
             for (int k = v_issued > VB ? v_issued - VB : 0; k < v_issued; ++k)
                 if (!mbar_wait(&v_full[k % VB], (k / VB) & 1)) s_fail = 1;
         }
@@ -653,11 +678,11 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
                     k_prev = k;
                     if (!mbar_wait(&v_full[k % VB], (k / VB) & 1)) { ok = false; break; }
                 }
-                const int s = i % S, a = i & 1;
+                const int b = i & 1, a = i & 1;
                 if (i >= 2 && !mbar_wait(&acc_empty[a], ((i >> 1) - 1) & 1)) { ok = false; break; }
-                if (!mbar_wait(&full[s], (i / S) & 1)) { ok = false; break; }
+                if (!mbar_wait(&bfull[b], (i >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t bs = smem_u32(ring + s * stage_bytes);
+                const uint32_t bs = smem_u32(bring + b * bstage_bytes);
                 const uint32_t vs = smem_u32(vbufs + (k % VB) * vbuf_bytes);
                 const uint32_t d = tmem + a * kExpandN;
                 int n = 0;
@@ -670,13 +695,17 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
                                      idesc, n != 0);
                     }
                 mma_commit(&acc_full[a]);
+                mma_commit(&bempty[b]);   // B' stage b is free once these MMAs are done
                 const bool more = tr.next(p, n_rt, n_items);
                 if (!more || tr.k != k) mma_commit(&v_empty[k % VB]);   // the item's slice is free after these
                 if (!more) break;
             }
             if (!ok) s_fail = 1;
+            // the tensor memory is freed only after every MMA issued has completed
+            mma_commit(&mma_done);
+            if (!mbar_wait(&mma_done, 0)) s_fail = 1;
         }
-    } else {   // ---- epilogue warps ----
+    } else if (warp < kStoreWarpE) {   // ---- epilogue warps ----
         // Two teams of 8 warps take alternate tiles (team t: tiles i = t, t+2,
         // ..., accumulator t), so two tiles' epilogues are in flight at once.
         // Within a team, 2 warps per TMEM lane quarter, 64 columns each.
@@ -686,8 +715,8 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
         const int hc = w8 >> 2;             // which 64-column half of the tile (one y box)
         const int r = quarter * 32 + lane;  // tile row
         // Every warp of a team runs every one of the team's iterations and
-        // meets both named barriers whatever happened (after a timeout it
-        // only skips work), so a barrier never waits for a warp that has left.
+        // arrives on its barriers whatever happened (after a timeout it only
+        // skips work), so no wait is left without its arrivals.
         TileIter tr;
         tr.init(p, n_rt);
         bool more = true;
@@ -695,11 +724,12 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
         for (int i = team; more; i += 2) {
             const RowTile rt = s_rt[tr.k];
             const int s = i % S, a = team;
-            const bool ok = !s_fail && mbar_wait(&acc_full[a], (i >> 1) & 1);
+            bool ok = !s_fail && mbar_wait(&acc_full[a], (i >> 1) & 1);
+            ok = ok && mbar_wait(&yfull[s], (i / S) & 1);   // the staged y tile (TMA-written) is visible here
             if (!ok) s_fail = 1;
             tc_fence_after();
             const uint32_t tcol = tmem + a * kExpandN + (static_cast<uint32_t>(quarter * 32) << 16) + hc * kKB;
-            uint8_t* ybox = ring + s * stage_bytes + (kbs + hc) * kBoxBytes;
+            uint8_t* ybox = yring + s * ystage_bytes + hc * kBoxBytes;
             uint8_t* sy = ybox + r * 128;
             const int tile_col0 = tr.ct * kExpandN;
             const int col0 = tile_col0 + hc * kKB;
@@ -732,25 +762,31 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
                     }
                 }
             }
-            if (whole) {
-                fence_async_smem();
-                named_barrier(1 + team, 256);
-                if (w8 == 0 && lane == 0) {
-                    if (!s_fail) {
-                        uint8_t* y0 = ring + s * stage_bytes + kbs * kBoxBytes;
-                        tma_store_2d(&my, p.out_off[tr.q] + tile_col0, rt.row0, y0);
-                        tma_store_2d(&my, p.out_off[tr.q] + tile_col0 + kKB, rt.row0, y0 + kBoxBytes);
-                        bulk_commit();
-                    }
-                    bulk_wait_read();   // the stage may be refilled once the stores have read it
-                }
-                named_barrier(1 + team, 256);
-            }
+            fence_async_smem();   // the TMA store reads what these threads wrote
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);   // this warp is done with stage s
+            if (lane == 0) mbar_arrive(&epi_done[s]);   // this warp is done with y stage s
             more = tr.next(p, n_rt, n_items) && tr.next(p, n_rt, n_items);
         }
-        if (w8 == 0 && lane == 0) bulk_wait_all();
+    } else if (lane == 0) {   // ---- store: finished whole tiles back to y, then the stage is free ----
+        TileIter tr;
+        tr.init(p, n_rt);
+        for (int i = 0;; ++i) {
+            const RowTile rt = s_rt[tr.k];
+            const int s = i % S;
+            if (!s_fail && !mbar_wait(&epi_done[s], (i / S) & 1)) s_fail = 1;
+            const int tile_col0 = tr.ct * kExpandN;
+            const bool whole = rt.nrows == kTileM && tile_col0 + kExpandN <= p.width[tr.q];
+            if (whole && !s_fail) {
+                uint8_t* y0 = yring + s * ystage_bytes;
+                tma_store_2d(&my, p.out_off[tr.q] + tile_col0, rt.row0, y0);
+                tma_store_2d(&my, p.out_off[tr.q] + tile_col0 + kKB, rt.row0, y0 + kBoxBytes);
+                bulk_commit();
+                bulk_wait_read();   // the stage may be refilled once the stores have read it
+            }
+            mbar_arrive(&yempty[s]);
+            if (!tr.next(p, n_rt, n_items)) break;
+        }
+        bulk_wait_all();
     }
     __syncthreads();
     tc_fence_after();
@@ -933,19 +969,17 @@ cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const b
     p.stall_tx = test_stall_bytes(kStallExpandTc);
     p.status = status;
     const int kbs = r_pad64 / kKB;
-    // r_pad64 = 64: four ring stages and one v slice buffer (225 KB), or
-    // three stages and two buffers (209 KB); r_pad64 = 128: two stages, one
-    // buffer.
-    // Large work items (8 or more tiles) pay the v-slice load of one buffer
-    // rarely and gain from the deeper ring; small ones keep the second
-    // buffer (Mistral-7B prefill: 1.469 against 1.509 ms per step; the
-    // mixed batch's 4-tile items: 4.18 against 4.03 ms).
-    const int st_env = env_int("LORA_TC_EXPAND_STAGES", p.chunk >= 8 ? kStagesE : 3);
-    const int stages = kbs == 1 ? (st_env == 3 ? 3 : kStagesE) : 2;
-    const int vbufs = kbs == 1 && stages == 3 ? 2 : 1;
+    // r_pad64 = 64: five y stages and one v slice buffer, or four stages and
+    // two buffers; r_pad64 = 128: three stages and one buffer (each 225 KB
+    // with the two B' stages).  Large work items (8 or more tiles) pay the
+    // v-slice load of one buffer rarely and gain from the deeper ring; small
+    // ones keep the second buffer.
+    const int st_env = env_int("LORA_TC_EXPAND_STAGES", p.chunk >= 8 ? kStagesY : 4);
+    const int stages = kbs == 1 ? std::max(3, std::min(kStagesY, st_env)) : 3;
+    const int vbufs = kbs == 1 && stages < kStagesY ? 2 : 1;
     p.stages = stages;
     p.vbufs = vbufs;
-    const size_t smem = static_cast<size_t>(vbufs * 2 * kbs + stages * (kbs + 2)) * kBoxBytes + 1024;
+    const size_t smem = static_cast<size_t>(vbufs * 2 * kbs + 2 * kbs + 2 * stages) * kBoxBytes + 1024;
     static int configured = -1;
     static size_t configured_bytes = 0;
     if (!configure_once(reinterpret_cast<const void*>(sgmv_expand_tc_kernel), smem, configured, configured_bytes))
