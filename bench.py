@@ -148,21 +148,21 @@ ROUTE_KERNELS = {
 # only for the linear layer); valid only while the listed kernel sources
 # hash to `src`.
 NCU_TRAFFIC = {
-    "llama3b_decode": {"files": ['bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "b264cebf48604b0c",
-             "bytes_per_call": 3442880},
-    "stress70b": {"files": ['bgmv_grouped.cu', 'decode_common.cuh', 'common.cuh'], "src": "ba1c9ca552bedd58",
-             "bytes_per_call": 988152576},
-    "mistral7b_prefill": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "19155bd8848086dc",
-             "bytes_per_call": 2061788096},
-    "merge_mistral7b": {"files": ['merge.cu', 'merge_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "a42607bd1f8823b7",
-             "bytes_per_step": 6934879914},
-    "linear_mistral7b_prefill": {"files": ['linear_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh'], "src": "2967019a7ab0382c",
-             "bytes_per_step": 19454782208},
-    "mixed": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'bgmv_fused.cu', 'decode_common.cuh', 'common.cuh'], "src": "b16a389cb54688e0",
-             "bytes_per_call": 113133120},
+    "llama3b_decode": {"files": ['bgmv_fused.cu', 'decode_common.cuh', 'common.cuh', 'cluster.cuh'], "src": "c3d91c968f69f3f4",
+             "bytes_per_call": 3442240},
+    "stress70b": {"files": ['bgmv_grouped.cu', 'decode_common.cuh', 'common.cuh', 'cluster.cuh'], "src": "d394e5f3b5e71d17",
+             "bytes_per_call": 988095360},
+    "mistral7b_prefill": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh', 'cluster.cuh'], "src": "f804e56e8793a4e6",
+             "bytes_per_call": 2062889408},
+    "merge_mistral7b": {"files": ['merge.cu', 'merge_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh', 'cluster.cuh'], "src": "868105680b61064e",
+             "bytes_per_step": 6934772736},
+    "linear_mistral7b_prefill": {"files": ['linear_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh', 'cluster.cuh'], "src": "fcb8237452adf5e9",
+             "bytes_per_step": 19563948288},
+    "mixed": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'bgmv_fused.cu', 'decode_common.cuh', 'common.cuh', 'cluster.cuh'], "src": "5f85d28ffafe0d47",
+             "bytes_per_call": 113182144},
     # captured on 2 layers, scaled to the 28 of a step (every layer has the same shapes)
-    "linear_llama3b_decode": {"files": ['linear_swap.cu', 'bgmv_grouped.cu', 'tc_common.cuh', 'tmap.cpp', 'decode_common.cuh', 'common.cuh'],
-             "src": "329bae22d97a6d8b", "bytes_per_step": 1602936832},
+    "linear_llama3b_decode": {"files": ['linear_swap.cu', 'bgmv_grouped.cu', 'tc_common.cuh', 'tmap.cpp', 'decode_common.cuh', 'common.cuh', 'cluster.cuh'],
+             "src": "5798ea1c8569984d", "bytes_per_step": 1603055104},
 }
 
 
