@@ -258,7 +258,7 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
             const int s = kb % S;
             // a stage is re-armed only once the MMAs have consumed it (its
             // previous phase complete)
-            if (kb >= S && !mbar_wait(&empty[s], ((kb / S) - 1) & 1)) {
+            if (kb >= S && !mbar_wait_spin(&empty[s], ((kb / S) - 1) & 1)) {
                 s_fail = 1;
                 break;
             }
@@ -280,7 +280,7 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
         bool ok = true;
         for (int kb = 0; kb < n_kb && ok; ++kb) {
             const int s = kb % S;
-            if (!mbar_wait(&full[s], (kb / S) & 1)) {
+            if (!mbar_wait_spin(&full[s], (kb / S) & 1)) {
                 ok = false;
                 break;
             }
@@ -612,7 +612,7 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
                 if (tr.k != k_prev) {   // a new item: its v slice into buffer k % VB
                     k_prev = tr.k;
                     const int vb = tr.k % VB;
-                    if (tr.k >= VB && !mbar_wait(&v_empty[vb], ((tr.k / VB) - 1) & 1)) {
+                    if (tr.k >= VB && !mbar_wait_spin(&v_empty[vb], ((tr.k / VB) - 1) & 1)) {
                         s_fail = 1;
                         break;
                     }
@@ -628,7 +628,7 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
                 const int col0 = tr.ct * kExpandN;
                 // B' of the tile into B' stage i % 2
                 const int b = i & 1;
-                if (i >= 2 && !mbar_wait(&bempty[b], ((i >> 1) - 1) & 1)) {
+                if (i >= 2 && !mbar_wait_spin(&bempty[b], ((i >> 1) - 1) & 1)) {
                     s_fail = 1;
                     break;
                 }
@@ -643,7 +643,7 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
                 b_issued = i + 1;
                 // the y tile into y stage i % S
                 const int s = i % S;
-                if (i >= S && !mbar_wait(&yempty[s], ((i / S) - 1) & 1)) {
+                if (i >= S && !mbar_wait_spin(&yempty[s], ((i / S) - 1) & 1)) {
                     s_fail = 1;
                     break;
                 }
@@ -676,11 +676,11 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
                 const int k = tr.k;
                 if (k != k_prev) {
                     k_prev = k;
-                    if (!mbar_wait(&v_full[k % VB], (k / VB) & 1)) { ok = false; break; }
+                    if (!mbar_wait_spin(&v_full[k % VB], (k / VB) & 1)) { ok = false; break; }
                 }
                 const int b = i & 1, a = i & 1;
-                if (i >= 2 && !mbar_wait(&acc_empty[a], ((i >> 1) - 1) & 1)) { ok = false; break; }
-                if (!mbar_wait(&bfull[b], (i >> 1) & 1)) { ok = false; break; }
+                if (i >= 2 && !mbar_wait_spin(&acc_empty[a], ((i >> 1) - 1) & 1)) { ok = false; break; }
+                if (!mbar_wait_spin(&bfull[b], (i >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t bs = smem_u32(bring + b * bstage_bytes);
                 const uint32_t vs = smem_u32(vbufs + (k % VB) * vbuf_bytes);
@@ -811,11 +811,19 @@ namespace {
 
 size_t shrink_smem(int stages, int R) { return static_cast<size_t>(stages) * (kBoxBytes + R * 128) + 1024; }
 
+// Four stages, two CTAs per SM where they fit in shared memory; where one
+// CTA is alone on its SM anyway (wide rank stacks), as many stages as that
+// SM holds, since the CTA's bytes in flight are then all the SM has.
 int shrink_stages(int R)
 {
+    constexpr size_t kTwoPerSm = 113 * 1024, kOnePerSm = 225 * 1024;
     int s = 4;
-    while (s > 2 && shrink_smem(s, R) > 200 * 1024) --s;
-    return s;
+    if (shrink_smem(4, R) > kTwoPerSm)
+        while (s < 8 && shrink_smem(s + 1, R) <= kOnePerSm) ++s;
+    while (s > 2 && shrink_smem(s, R) > kOnePerSm) --s;
+    int e = std::max(2, std::min(8, env_int("LORA_TC_SHRINK_STAGES", s)));
+    while (e > 2 && shrink_smem(e, R) > kOnePerSm) --e;
+    return e;
 }
 
 // Raises the kernel's dynamic shared-memory limit to at least smem on the
