@@ -139,6 +139,7 @@ struct ShrinkTcParams {
     const int32_t* seg_slot;
     int n_segs, n_pos, n_rows;
     int stages;
+    int kps;             // K blocks per ring stage (1 or 2: a row's adjacent 128-byte pieces fetched together)
     int mode;            // 0: fp32 v [n_rows][ld_v]; 1: bf16 hi/lo planes [n_rows][ld_p]
     float* v;
     int ld_v;
@@ -225,12 +226,14 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
         return;
     }
     const CUtensorMap* amap[4] = {&ma0, &ma1, &ma2, &ma3};
-    const int S = p.stages;
-    const int stage_bytes = kBoxBytes + p.R * 128;
+    const int S = p.stages, KPS = p.kps;
+    const int sub_bytes = kBoxBytes + p.R * 128;   // one K block: the x box, then one A box per projection
+    const int stage_bytes = KPS * sub_bytes;
     uint8_t* base = align1024(smem_raw);
     const int n_kb_all = (p.h_in + kKB - 1) / kKB;
     const int kb0 = crank * n_kb_all / p.ks;
     const int n_kb = (crank + 1) * n_kb_all / p.ks - kb0;   // >= 1: the launcher keeps ks <= n_kb_all
+    const int n_st = (n_kb + KPS - 1) / KPS;                 // ring stages this CTA fills
 
     uint32_t ncols = 32;   // accumulator columns: a power of two >= R
     while (ncols < static_cast<uint32_t>(p.R)) ncols <<= 1;
@@ -252,44 +255,52 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
     if (!p.x_ready) grid_dep_wait();   // x may be the preceding kernel's output
 
     if (warp == 0 && lane == 0) {
-        // producer: X box + one A box per projection per 64-element K block
+        // producer: per K block an X box + one A box per projection, KPS
+        // K blocks to a stage
         int issued = 0;
-        for (int kb = 0; kb < n_kb; ++kb) {
-            const int s = kb % S;
+        for (int i = 0; i < n_st; ++i) {
+            const int s = i % S;
             // a stage is re-armed only once the MMAs have consumed it (its
             // previous phase complete)
-            if (kb >= S && !mbar_wait_spin(&empty[s], ((kb / S) - 1) & 1)) {
+            if (i >= S && !mbar_wait_spin(&empty[s], ((i / S) - 1) & 1)) {
                 s_fail = 1;
                 break;
             }
             uint8_t* st = base + s * stage_bytes;
-            mbar_expect_tx(&full[s], stage_bytes + (kb == 0 ? p.stall_tx : 0u));
-            tma_load_2d(st, &mx, (kb0 + kb) * kKB, ti.row0, &full[s]);
-            for (int q = 0; q < p.n_proj; ++q)
-                tma_load_2d(st + kBoxBytes + q * p.r_slot * 128, amap[q], (kb0 + kb) * kKB, ti.slot * p.r_slot,
-                            &full[s]);
-            issued = kb + 1;
+            const int nkb = min(KPS, n_kb - i * KPS);
+            mbar_expect_tx(&full[s], nkb * sub_bytes + (i == 0 ? p.stall_tx : 0u));
+            for (int j = 0; j < nkb; ++j) {
+                const int k = (kb0 + i * KPS + j) * kKB;
+                uint8_t* sb = st + j * sub_bytes;
+                tma_load_2d(sb, &mx, k, ti.row0, &full[s]);
+                for (int q = 0; q < p.n_proj; ++q)
+                    tma_load_2d(sb + kBoxBytes + q * p.r_slot * 128, amap[q], k, ti.slot * p.r_slot, &full[s]);
+            }
+            issued = i + 1;
         }
         // Every copy issued has landed before the CTA moves on (after a normal
         // run the MMA thread has already seen each of these phases complete).
-        for (int kb = issued > S ? issued - S : 0; kb < issued; ++kb)
-            if (!mbar_wait(&full[kb % S], (kb / S) & 1)) s_fail = 1;
+        for (int i = issued > S ? issued - S : 0; i < issued; ++i)
+            if (!mbar_wait(&full[i % S], (i / S) & 1)) s_fail = 1;
     } else if (warp == 1 && lane == 0) {
         // MMA issuer: 4 x (128 x R x 16) per K block, accumulating in TMEM
         const uint32_t idesc = idesc_bf16_f32(kTileM, p.R);
         bool ok = true;
-        for (int kb = 0; kb < n_kb && ok; ++kb) {
-            const int s = kb % S;
-            if (!mbar_wait_spin(&full[s], (kb / S) & 1)) {
+        for (int i = 0; i < n_st && ok; ++i) {
+            const int s = i % S;
+            if (!mbar_wait_spin(&full[s], (i / S) & 1)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t st = smem_u32(base + s * stage_bytes);
+            const int nkb = min(KPS, n_kb - i * KPS);
+            for (int j = 0; j < nkb; ++j) {
+                const uint32_t sb = smem_u32(base + s * stage_bytes + j * sub_bytes);
 #pragma unroll
-            for (int ks = 0; ks < kKB / 16; ++ks)
-                mma_bf16(tmem, sdesc_sw128(st + ks * 32), sdesc_sw128(st + kBoxBytes + ks * 32), idesc,
-                         (kb | ks) != 0);
+                for (int ks = 0; ks < kKB / 16; ++ks)
+                    mma_bf16(tmem, sdesc_sw128(sb + ks * 32), sdesc_sw128(sb + kBoxBytes + ks * 32), idesc,
+                             (i | j | ks) != 0);
+            }
             mma_commit(&empty[s]);   // frees the stage once these MMAs have read it
         }
         if (!ok) s_fail = 1;
@@ -809,20 +820,25 @@ size_t sgmv_tc_plane_bytes(int n_rows, int n_proj, int r_slot)
 
 namespace {
 
-size_t shrink_smem(int stages, int R) { return static_cast<size_t>(stages) * (kBoxBytes + R * 128) + 1024; }
+size_t shrink_smem(int stages, int R, int kps = 1)
+{
+    return static_cast<size_t>(stages) * kps * (kBoxBytes + R * 128) + 1024;
+}
 
 // Four stages, two CTAs per SM where they fit in shared memory; where one
 // CTA is alone on its SM anyway (wide rank stacks), as many stages as that
 // SM holds, since the CTA's bytes in flight are then all the SM has.
-int shrink_stages(int R)
+int shrink_stages(int R, int kps)
 {
     constexpr size_t kTwoPerSm = 113 * 1024, kOnePerSm = 225 * 1024;
     int s = 4;
     if (shrink_smem(4, R) > kTwoPerSm)
         while (s < 8 && shrink_smem(s + 1, R) <= kOnePerSm) ++s;
-    while (s > 2 && shrink_smem(s, R) > kOnePerSm) --s;
+    // the same bytes in flight when a stage holds kps K blocks
+    s = std::max(2, (s + kps - 1) / kps);
+    while (s > 2 && shrink_smem(s, R, kps) > kOnePerSm) --s;
     int e = std::max(2, std::min(8, env_int("LORA_TC_SHRINK_STAGES", s)));
-    while (e > 2 && shrink_smem(e, R) > kOnePerSm) --e;
+    while (e > 2 && shrink_smem(e, R, kps) > kOnePerSm) --e;
     return e;
 }
 
@@ -872,7 +888,11 @@ cudaError_t launch_sgmv_shrink_tc(float* v, int ld_v, bf16_t* vh, bf16_t* vl, co
     p.n_segs = n_segs;
     p.n_pos = n_pos;
     p.n_rows = n_rows;
-    p.stages = shrink_stages(R);
+    // Two K blocks to a stage: each x row's two adjacent 128-byte pieces are
+    // requested together (Mistral-7B prefill: 1.432 against 1.444 ms per
+    // step on one box; the mixed batch 3.678 against 3.706 ms).
+    p.kps = std::max(1, std::min(2, env_int("LORA_TC_SHRINK_KPS", 2)));
+    p.stages = shrink_stages(R, p.kps);
     p.mode = v ? 0 : 1;
     p.v = v;
     p.ld_v = ld_v;
@@ -899,7 +919,7 @@ cudaError_t launch_sgmv_shrink_tc(float* v, int ld_v, bf16_t* vh, bf16_t* vl, co
     p.ks = std::max(1, std::min(env_int("LORA_TC_SHRINK_KS", ks), n_kb));
     // the cluster's partials reuse the ring: 128 rows x (R + 4) fp32
     const size_t red = p.ks > 1 ? static_cast<size_t>(kTileM) * (R + 4) * sizeof(float) + 1024 : 0;
-    const size_t smem = std::max(shrink_smem(p.stages, R), red);
+    const size_t smem = std::max(shrink_smem(p.stages, R, p.kps), red);
     static int configured = -1;
     static size_t configured_bytes = 0;
     if (!configure_once(reinterpret_cast<const void*>(sgmv_shrink_tc_kernel), smem, configured, configured_bytes))
