@@ -2,6 +2,8 @@
 same seeded inputs (tolerances in helpers.py), on all five workloads, plus
 the edge cases the method has (empty batch, all-base batch, prefill-only,
 decode-only, ranks above the BGMV cap, malformed ids and segments)."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -605,6 +607,44 @@ def test_merge_vs_oracle(out, h_in, r, r_slot, sign):
     E = (r + 1) * 2.0 ** -24 * (np.abs(O.bf16_to_f64(Bb)) @ np.abs(O.bf16_to_f64(Ab)) + np.abs(O.bf16_to_f64(Wb)))
     assert np.all(np.abs(got - ref) <= 2.0 ** -7 * (np.abs(ref) + E) + E)
     assert (got != ref).mean() < 1e-3
+
+
+def test_merge_full_size_gate_shape():
+    """The benchmark's largest merge launch shape, every element: a
+    Mistral-7B gate weight (14336 x 4096) with a rank-64 adapter, merged and
+    then unmerged on the GPU, each against the fp64 oracle applied to the
+    same input (row blocks over the host cores).  Bound as in
+    test_merge_vs_oracle."""
+    import concurrent.futures as cf
+    out, h_in, r = 14336, 4096, 64
+    W, A, Bp, Wb, Ab, Bb = _merge_case(out, h_in, r, r, seed=14336)
+    Wd = W.cuda()
+    Ad, Bd = A.cuda(), Bp.cuda()
+    absA = np.abs(O.bf16_to_f64(Ab))
+
+    def check(before_bits, after_bits, sign, what):
+        def block(i0):
+            i1 = min(out, i0 + 512)
+            ref = O.bf16_to_f64(O.merge(before_bits[i0:i1], Ab, Bb[i0:i1], sign))
+            got = O.bf16_to_f64(after_bits[i0:i1])
+            E = (r + 1) * 2.0 ** -24 * (np.abs(O.bf16_to_f64(Bb[i0:i1])) @ absA +
+                                        np.abs(O.bf16_to_f64(before_bits[i0:i1])))
+            bad = int(np.sum(np.abs(got - ref) > 2.0 ** -7 * (np.abs(ref) + E) + E))
+            return bad, int(np.sum(got != ref))
+        with cf.ThreadPoolExecutor(max_workers=os.cpu_count() or 1) as ex:
+            res = list(ex.map(block, range(0, out, 512)))
+        bad = sum(b for b, _ in res)
+        diff = sum(d for _, d in res)
+        assert bad == 0, f"{what}: {bad} elements outside the bound"
+        assert diff < 1e-3 * out * h_in, f"{what}: {diff} elements differ from the oracle"
+
+    abi.lora_merge(Wd, Ad, Bd, 1)
+    torch.cuda.synchronize()
+    merged = to_host(Wd)
+    check(Wb, merged, 1, "merge")
+    abi.lora_merge(Wd, Ad, Bd, -1)
+    torch.cuda.synchronize()
+    check(merged, to_host(Wd), -1, "unmerge")
 
 
 def test_merge_unmerge_round_trip_exact():
