@@ -227,8 +227,10 @@ typedef struct {
  * workspace [dev] at least lora_apply_workspace_bytes(n_rows, n_proj, r_slot)
  *           bytes, 256-byte aligned; its contents are scratch (the
  *           intermediate v: fp32, and bf16 hi/lo planes for the kernels
- *           whose expand runs on tensor cores), written only after the
- *           kernel enqueued just before the call has completed.
+ *           whose expand runs on tensor cores; and the tensor-core
+ *           expand's work-item counter), written only after the kernel
+ *           enqueued just before the call has completed.  Calls that may
+ *           run at the same time on the GPU need separate workspaces.
  * flags     LORA_APPLY_* above (0 = default ordering).
  * Errors (before anything is enqueued): LORA_ERR_INVALID_ARG (NULL projs,
  * meta, x or lora_ids; n_proj outside 1..LORA_MAX_PROJ), LORA_ERR_SHAPE (a

@@ -240,17 +240,23 @@ lora_status_t lora_sgmv_expand(lora_bf16_t* y, int ld_y, int y_off, int width,
 }
 
 // Workspace layout: [bf16 hi/lo planes of v for the tensor-core SGMV route]
-// [fp32 v for the other routes], each part 256-byte aligned.
+// [fp32 v for the other routes][the tensor-core expand's work-item counter],
+// each part 256-byte aligned.
 static size_t plane_region_bytes(int n_rows, int n_proj, int r_slot)
 {
     return (lora::sgmv_tc_plane_bytes(n_rows, n_proj, r_slot) + 255) / 256 * 256;
 }
+static size_t fp32_region_bytes(int n_rows, int n_proj, int r_slot)
+{
+    return (static_cast<size_t>(n_rows) * n_proj * r_slot * sizeof(float) + 255) / 256 * 256;
+}
+constexpr size_t kTicketRegionBytes = 256;
 
 size_t lora_apply_workspace_bytes(int n_rows, int n_proj, int r_slot)
 {
     if (n_rows <= 0 || n_proj <= 0 || r_slot <= 0) return 0;
     if (n_proj > LORA_MAX_PROJ || r_slot > LORA_MAX_RANK) return 0;   // lora_apply rejects these
-    return plane_region_bytes(n_rows, n_proj, r_slot) + static_cast<size_t>(n_rows) * n_proj * r_slot * sizeof(float);
+    return plane_region_bytes(n_rows, n_proj, r_slot) + fp32_region_bytes(n_rows, n_proj, r_slot) + kTicketRegionBytes;
 }
 
 lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_x, int h_in,
@@ -284,6 +290,8 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
     bf16_t* vh = static_cast<bf16_t*>(workspace);
     bf16_t* vl = vh + plane_region_bytes(T, n_proj, r_slot) / 2 / sizeof(bf16_t);
     float* v = reinterpret_cast<float*>(static_cast<char*>(workspace) + plane_region_bytes(T, n_proj, r_slot));
+    unsigned* tickets = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + plane_region_bytes(T, n_proj, r_slot) +
+                                                    fp32_region_bytes(T, n_proj, r_slot));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int D = T - P;
     if (P > 0) LORA_TRY(check_segments(meta->seg_starts, meta->seg_slot, meta->n_segs, P, T, nullptr));
@@ -306,7 +314,7 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
     if (shrink_first)
         LORA_TRY(cuda_status(lora::launch_sgmv_shrink_tc(nullptr, 0, vh, vl, x, ld_x, h_in, ps, meta->seg_starts,
                                                          meta->seg_slot, meta->n_segs, P, T, n_slots, flags,
-                                                         dev_status, s)));
+                                                         dev_status, s, tickets)));
     if (D > 0) {
         const bool gathered = meta->perm && meta->gseg_starts && meta->gseg_slot && meta->n_gsegs > 0;
         const bool fused_ok = gathered && lora::fused_decode_supported(n_proj, r_slot);
@@ -339,10 +347,10 @@ lora_status_t lora_apply(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld_
             if (!shrink_first)
                 LORA_TRY(cuda_status(lora::launch_sgmv_shrink_tc(nullptr, 0, vh, vl, x, ld_x, h_in, ps,
                                                                  meta->seg_starts, meta->seg_slot, meta->n_segs, P,
-                                                                 T, n_slots, flags, dev_status, s)));
+                                                                 T, n_slots, flags, dev_status, s, tickets)));
             LORA_TRY(cuda_status(lora::launch_sgmv_expand_tc(y, ld_y, vh, vl, ps, meta->seg_starts,
                                                              meta->seg_slot, meta->n_segs, P, T, n_slots, flags,
-                                                             dev_status, s)));
+                                                             dev_status, s, tickets)));
         } else if (r_slot <= 64) {
             // short segments: the segments as groups of the grouped pair (no
             // permutation: a segment's positions are its rows)

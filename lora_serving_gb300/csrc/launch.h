@@ -59,13 +59,17 @@ bool sgmv_tc_supported(int n_proj, int r_slot, int h_in);
 size_t sgmv_tc_plane_bytes(int n_rows, int n_proj, int r_slot);
 // Both take lora_apply's ordering flags (programmatic dependent launch unless
 // LORA_APPLY_NO_PDL; the shrink reads x before the wait with X_READY).
+// tickets (device, or null): a work-item counter the shrink zeroes and the
+// expand that follows it in the same call draws its items from (null: the
+// expand's static item order).  Calls that may overlap need their own.
 cudaError_t launch_sgmv_shrink_tc(float* v, int ld_v, bf16_t* vh, bf16_t* vl, const bf16_t* x, int ld_x, int h_in,
                                   const ProjSet& ps, const int32_t* seg_starts, const int32_t* seg_slot, int n_segs,
                                   int n_pos, int n_rows, int n_slots, unsigned flags, int32_t* status,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, unsigned* tickets = nullptr);
 cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const bf16_t* vl, const ProjSet& ps,
                                   const int32_t* seg_starts, const int32_t* seg_slot, int n_segs, int n_pos,
-                                  int n_rows, int n_slots, unsigned flags, int32_t* status, cudaStream_t stream);
+                                  int n_rows, int n_slots, unsigned flags, int32_t* status, cudaStream_t stream,
+                                  unsigned* tickets = nullptr);
 
 // Whether the fused decode kernel handles this projection set.
 bool fused_decode_supported(int n_proj, int r_slot);

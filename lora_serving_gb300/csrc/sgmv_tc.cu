@@ -150,6 +150,7 @@ struct ShrinkTcParams {
     int ks;              // CTAs per row tile (a cluster), each a slice of K
     int x_ready;         // x is not written by the preceding kernel: read it before the wait
     unsigned stall_tx;   // test hook: extra bytes expected on the first stage (0 normally)
+    unsigned* tickets;   // the following expand's work-item counter, zeroed here (or null)
     int32_t* status;
 };
 
@@ -317,6 +318,9 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
     tc_fence_after();
     ok = __syncthreads_and(ok && !s_fail);
     grid_dep_wait();   // the preceding kernel may still read the buffers written below
+    // The expand that follows in the same call takes its work items from this
+    // counter; no kernel before this one still uses it.
+    if (p.tickets != nullptr && blockIdx.x == 0 && tid == 0) *p.tickets = 0u;
     const int r = warp * 32 + lane;   // tile row = TMEM lane
     if (p.ks == 1) {
         const bool row_ok = r < ti.nrows;
@@ -417,12 +421,14 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
 //   warp 0: TMA producer   warp 1: MMA issuer   warps 2..17: epilogue
 //   warp 18: TMA store
 
-constexpr int kStagesY = 5;        // y ring stages, at most (the launcher picks 3 to 5)
+constexpr int kStagesY = 5;        // y ring stages, at most (the launcher picks 2 to 5)
 constexpr int kEpiWarps = 16;       // 4 per TMEM lane quarter, 32 columns each
 constexpr int kStoreWarpE = 2 + kEpiWarps;
 constexpr int kExpandThreadsP = 32 * (kStoreWarpE + 1);
 constexpr int kChunkMax = 16;       // output tiles per work item, at most
-constexpr int kMaxItems = 64;       // work items per CTA (the launcher sizes the grid)
+constexpr int kMaxItems = 64;       // work items per CTA in the static order (the launcher sizes the grid)
+constexpr int kMaxRt = 1024;        // row tiles a CTA can table (the dynamic order needs all of them)
+constexpr int kQD = 8;              // work-item queue depth (dynamic order)
 
 struct ExpandTcParams {
     int n_proj, r_slot, r_pad64, n_slots;
@@ -440,6 +446,9 @@ struct ExpandTcParams {
     int stages;                     // y ring stages (<= kStagesY)
     int vbufs;                      // v slice buffers (1 or 2)
     unsigned stall_tx;              // test hook: extra bytes expected on the first B' stage (0 normally)
+    unsigned* tickets;              // dynamic order: the call's work-item counter (zeroed by the shrink)
+    int dyn;                        // 1: items taken from tickets; 0: item c + k G for CTA c
+    int table_bytes;                // the row-tile table at the start of dynamic shared memory
     int32_t* status;
 };
 
@@ -447,14 +456,81 @@ struct RowTile {
     int slot, row0, nrows;
 };
 
-// Walks this CTA's tiles: item k (global item c + k * G), tile ct of the
-// item's projection.  Divides once per item, never per tile.
+// Work items in the dynamic order: the producer takes each item's number
+// from the call's counter (one atomic per item) and passes it through a
+// queue of kQD slots; the MMA thread, every epilogue warp and the store
+// thread read the items in the same order.  An item number past the last
+// item ends the sequence.
+struct ItemQueue {
+    long long* item;
+    uint64_t* full;    // the producer's arrival
+    uint64_t* empty;   // one arrival per reader
+};
+constexpr int kItemReaders = 2 + kEpiWarps;   // MMA thread, epilogue warps, store thread
+enum ItemRole { kRoleProducer, kRoleThread, kRoleWarp };
+
+// Walks this CTA's tiles: item k (static order: global item c + k * G;
+// dynamic order: the k-th item taken), tile ct of the item's projection.
+// Divides once per item, never per tile.  kDyn and kRole are compile-time,
+// so the static order carries none of the queue's state.
+template <bool kDyn, int kRole>
 struct TileIter {
-    int k, q, ct, ct_end;
-    __device__ __forceinline__ void item(const ExpandTcParams& p, int n_rt)
+    int k, q, ct, ct_end, rix;   // rix: the item's entry of the row-tile table
+    unsigned ahead;              // producer, dynamic order: the next item's ticket, taken one item early
+    const ExpandTcParams& p;
+    int n_rt;
+    long long n_all;
+    ItemQueue Q;
+    volatile int* fail;
+    __device__ __forceinline__ TileIter(const ExpandTcParams& pp, int nrt, long long nall, const ItemQueue& qq,
+                                        volatile int* f)
+        : k(0), q(0), ct(0), ct_end(0), rix(0), ahead(0), p(pp), n_rt(nrt), n_all(nall), Q(qq), fail(f)
     {
-        const long long it = blockIdx.x + static_cast<long long>(k) * gridDim.x;
+    }
+    // item k's number, or -1 past the end (or on a timeout, with *fail set)
+    __device__ __forceinline__ long long take()
+    {
+        if constexpr (!kDyn) {
+            const long long it = blockIdx.x + static_cast<long long>(k) * gridDim.x;
+            return it < n_all ? it : -1;
+        } else {
+            const int slot = k % kQD;
+            long long it;
+            if constexpr (kRole == kRoleProducer) {
+                if (k >= kQD && !mbar_wait_spin(&Q.empty[slot], ((k / kQD) - 1) & 1)) {
+                    *fail = 1;
+                    return -1;
+                }
+                // this item's ticket was taken one item earlier, so the atomic's
+                // round trip overlaps the previous item's loads; the next one is
+                // requested now
+                const unsigned t = *fail ? 0xFFFFFFFFu : (k == 0 ? atomicAdd(p.tickets, 1u) : ahead);
+                it = static_cast<long long>(t) < n_all ? static_cast<long long>(t) : -1;
+                if (it >= 0) ahead = atomicAdd(p.tickets, 1u);
+                Q.item[slot] = it;
+                mbar_arrive(&Q.full[slot]);
+                return it;
+            } else {
+                const bool ok = kRole == kRoleThread ? mbar_wait_spin(&Q.full[slot], (k / kQD) & 1)
+                                                     : mbar_wait(&Q.full[slot], (k / kQD) & 1);
+                if (!ok) {
+                    *fail = 1;
+                    return -1;
+                }
+                it = Q.item[slot];
+                if constexpr (kRole == kRoleWarp) __syncwarp();   // every lane has read the slot before it is freed
+                if (kRole == kRoleThread || (threadIdx.x & 31) == 0) mbar_arrive(&Q.empty[slot]);
+                return it;
+            }
+        }
+    }
+    __device__ __forceinline__ bool item()
+    {
+        const long long it = take();
+        if (it < 0) return false;
         int ch = static_cast<int>(it / n_rt);   // chunk index over all projections
+        if constexpr (kDyn) rix = static_cast<int>(it - static_cast<long long>(ch) * n_rt);
+        else rix = k;
         q = 0;
         while (q < p.n_proj - 1 && ch >= p.chunks[q]) {
             ch -= p.chunks[q];
@@ -462,19 +538,19 @@ struct TileIter {
         }
         ct = ch * p.chunk;
         ct_end = min(ct + p.chunk, p.col_tiles[q]);
+        return true;
     }
-    __device__ __forceinline__ void init(const ExpandTcParams& p, int n_rt)
+    __device__ __forceinline__ bool init()
     {
         k = 0;
-        item(p, n_rt);
+        return item();
     }
     // false once past the CTA's last item
-    __device__ __forceinline__ bool next(const ExpandTcParams& p, int n_rt, int n_items)
+    __device__ __forceinline__ bool next()
     {
         if (++ct < ct_end) return true;
-        if (++k >= n_items) return false;
-        item(p, n_rt);
-        return true;
+        ++k;
+        return item();
     }
 };
 
@@ -484,8 +560,10 @@ __device__ __forceinline__ int item_row_tile(long long it, int n_rt) { return st
 // One block-wide pass over the segment table, kExpandThreadsP segments per
 // round: row tiles per segment (slot -1 and malformed segments have none)
 // and their prefix sums.  With fill, the segment holding the row tile of
-// each of this CTA's n_items items writes s_rt[item].  Returns the total
-// number of row tiles.  Every thread of the block takes part.
+// each of this CTA's n_items items writes s_rt[item] (static order), or
+// every segment writes s_rt[u] for each of its row tiles u (dynamic order).
+// Returns the total number of row tiles.  Every thread of the block takes
+// part.
 __device__ int scan_row_tiles(const ExpandTcParams& p, bool fill, int n_rt, int n_items, RowTile* s_rt, int* s_warp,
                               int* s_bad)
 {
@@ -515,7 +593,17 @@ __device__ int scan_row_tiles(const ExpandTcParams& p, bool fill, int n_rt, int 
             if (w < warp) before += s_warp[w];
             total += s_warp[w];
         }
-        if (fill && n > 0) {
+        if (fill && n > 0 && p.dyn) {
+            const int excl = base + before + (incl - n);   // row tiles before this segment
+            const int cap = p.table_bytes / static_cast<int>(sizeof(RowTile));   // entries the table holds
+            for (int j = 0; j < n && excl + j < cap; ++j) {
+                RowTile rt;
+                rt.slot = sl;
+                rt.row0 = s + j * kTileM;
+                rt.nrows = min(kTileM, e - rt.row0);
+                s_rt[excl + j] = rt;
+            }
+        } else if (fill && n > 0) {
             const int excl = base + before + (incl - n);   // row tiles before this segment
             for (int kk = 0; kk < n_items; ++kk) {
                 const int u = item_row_tile(blockIdx.x + static_cast<long long>(kk) * gridDim.x, n_rt);
@@ -534,6 +622,7 @@ __device__ int scan_row_tiles(const ExpandTcParams& p, bool fill, int n_rt, int 
     return base;
 }
 
+template <bool kDyn>
 __global__ void __launch_bounds__(kExpandThreadsP, 1)
 sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_constant__ CUtensorMap mvl,
                       const __grid_constant__ CUtensorMap my, const __grid_constant__ CUtensorMap mb0,
@@ -543,12 +632,15 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t yfull[kStagesY], yempty[kStagesY], epi_done[kStagesY];
     __shared__ __align__(8) uint64_t bfull[2], bempty[2], acc_full[2], acc_empty[2], v_full[2], v_empty[2], mma_done;
+    __shared__ __align__(8) uint64_t q_full[kQD], q_empty[kQD];
+    __shared__ long long q_item[kQD];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_fail;
-    __shared__ RowTile s_rt[kMaxItems];
     __shared__ int s_warp[kExpandThreadsP / 32];
     __shared__ int s_bad;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // row tiles: of this CTA's items (static order) or all of them (dynamic)
+    RowTile* s_rt = reinterpret_cast<RowTile*>(smem_raw);
 
     // ---- this CTA's items and their row tiles ----
     // Under programmatic dependent launch the segment table is read at once;
@@ -560,14 +652,20 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
     __syncthreads();
     const int n_rt = scan_row_tiles(p, false, 1, 0, s_rt, s_warp, &s_bad);
     const long long n_all = static_cast<long long>(n_rt) * p.n_chunks;
-    const int n_items = n_all > blockIdx.x ? static_cast<int>((n_all - 1 - blockIdx.x) / gridDim.x + 1) : 0;
-    if (n_items <= 0 || n_items > kMaxItems) {   // the launcher sizes the grid so the second cannot happen
+    // static order: this CTA's item count; dynamic order: every CTA takes part
+    // while the row tiles fit the table (the launcher's bound makes sure)
+    const int n_items = p.dyn ? (n_all > 0 ? 1 : 0)
+                              : (n_all > blockIdx.x ? static_cast<int>((n_all - 1 - blockIdx.x) / gridDim.x + 1) : 0);
+    // (a segment table whose tiles outnumber the launcher's bound, possible
+    // only for overlapping segments, is flagged and left alone)
+    if (n_items <= 0 || n_items > kMaxItems || (p.dyn && n_rt > p.table_bytes / static_cast<int>(sizeof(RowTile)))) {
         grid_dep_wait();
         if (tid == 0 && (n_items > 0 || (blockIdx.x == 0 && s_bad))) flag(p.status, LORA_DEV_BAD_SEGMENT);
         return;
     }
     scan_row_tiles(p, true, n_rt, n_items, s_rt, s_warp, &s_bad);
-    for (int i = tid; i < n_items; i += kExpandThreadsP)
+    const int n_table = p.dyn ? n_rt : n_items;
+    for (int i = tid; i < n_table; i += kExpandThreadsP)
         if (s_rt[i].slot >= p.n_slots || s_rt[i].slot < -1) atomicOr(&s_bad, 2);
     __syncthreads();
     grid_dep_wait();
@@ -584,7 +682,7 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
     const int bstage_bytes = kbs * kBoxBytes;                // B' of one tile
     const int ystage_bytes = 2 * kBoxBytes;                  // one y tile: two 64-column boxes
     const int vbuf_bytes = 2 * kbs * kBoxBytes;              // v_hi boxes, then v_lo boxes
-    uint8_t* vbufs = align1024(smem_raw);                    // VB x [v_hi | v_lo]
+    uint8_t* vbufs = align1024(smem_raw + p.table_bytes);    // VB x [v_hi | v_lo]
     uint8_t* bring = vbufs + VB * vbuf_bytes;                // 2 x B'
     uint8_t* yring = bring + 2 * bstage_bytes;               // S x y
 
@@ -604,6 +702,10 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
             mbar_init(&v_empty[a], 1);
         }
         mbar_init(&mma_done, 1);
+        for (int j = 0; j < kQD; ++j) {
+            mbar_init(&q_full[j], 1);
+            mbar_init(&q_empty[j], kItemReaders);
+        }
         mbar_init_fence();
         s_fail = 0;
     }
@@ -611,15 +713,16 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
+    const ItemQueue Q{q_item, q_full, q_empty};
 
     if (warp == 0) {
         if (lane == 0) {   // ---- producer ----
-            TileIter tr;
-            tr.init(p, n_rt);
+            TileIter<kDyn, kRoleProducer> tr(p, n_rt, n_all, Q, &s_fail);
+            bool more = tr.init();
             int k_prev = -1;
             int y_issued = 0, b_issued = 0, v_issued = 0;   // stages and v slices armed so far
-            for (int i = 0; !s_fail; ++i) {
-                const RowTile rt = s_rt[tr.k];
+            for (int i = 0; more && !s_fail; ++i) {
+                const RowTile rt = s_rt[tr.rix];
                 if (tr.k != k_prev) {   // a new item: its v slice into buffer k % VB
                     k_prev = tr.k;
                     const int vb = tr.k % VB;
@@ -665,7 +768,7 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
                 tma_load_2d(ys, &my, ycol, rt.row0, &yfull[s]);
                 tma_load_2d(ys + kBoxBytes, &my, ycol + kKB, rt.row0, &yfull[s]);
                 y_issued = i + 1;
-                if (!tr.next(p, n_rt, n_items)) break;
+                more = tr.next();
             }
             // Every copy issued has landed before the CTA moves on (after a
             // normal run the consumers have seen each of these phases complete).
@@ -680,10 +783,10 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
         if (lane == 0) {   // ---- MMA issuer ----
             const uint32_t idesc = idesc_bf16_f32(kTileM, kExpandN);
             bool ok = true;
-            TileIter tr;
-            tr.init(p, n_rt);
+            TileIter<kDyn, kRoleThread> tr(p, n_rt, n_all, Q, &s_fail);
+            bool more = tr.init();
             int k_prev = -1;
-            for (int i = 0; ok && !s_fail; ++i) {
+            for (int i = 0; more && ok && !s_fail; ++i) {
                 const int k = tr.k;
                 if (k != k_prev) {
                     k_prev = k;
@@ -707,9 +810,8 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
                     }
                 mma_commit(&acc_full[a]);
                 mma_commit(&bempty[b]);   // B' stage b is free once these MMAs are done
-                const bool more = tr.next(p, n_rt, n_items);
+                more = tr.next();
                 if (!more || tr.k != k) mma_commit(&v_empty[k % VB]);   // the item's slice is free after these
-                if (!more) break;
             }
             if (!ok) s_fail = 1;
             // the tensor memory is freed only after every MMA issued has completed
@@ -728,12 +830,11 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
         // Every warp of a team runs every one of the team's iterations and
         // arrives on its barriers whatever happened (after a timeout it only
         // skips work), so no wait is left without its arrivals.
-        TileIter tr;
-        tr.init(p, n_rt);
-        bool more = true;
-        if (team == 1) more = tr.next(p, n_rt, n_items);
+        TileIter<kDyn, kRoleWarp> tr(p, n_rt, n_all, Q, &s_fail);
+        bool more = tr.init();
+        if (team == 1 && more) more = tr.next();
         for (int i = team; more; i += 2) {
-            const RowTile rt = s_rt[tr.k];
+            const RowTile rt = s_rt[tr.rix];
             const int s = i % S, a = team;
             bool ok = !s_fail && mbar_wait(&acc_full[a], (i >> 1) & 1);
             ok = ok && mbar_wait(&yfull[s], (i / S) & 1);   // the staged y tile (TMA-written) is visible here
@@ -776,13 +877,13 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
             fence_async_smem();   // the TMA store reads what these threads wrote
             __syncwarp();
             if (lane == 0) mbar_arrive(&epi_done[s]);   // this warp is done with y stage s
-            more = tr.next(p, n_rt, n_items) && tr.next(p, n_rt, n_items);
+            more = tr.next() && tr.next();
         }
     } else if (lane == 0) {   // ---- store: finished whole tiles back to y, then the stage is free ----
-        TileIter tr;
-        tr.init(p, n_rt);
-        for (int i = 0;; ++i) {
-            const RowTile rt = s_rt[tr.k];
+        TileIter<kDyn, kRoleThread> tr(p, n_rt, n_all, Q, &s_fail);
+        bool more = tr.init();
+        for (int i = 0; more; ++i) {
+            const RowTile rt = s_rt[tr.rix];
             const int s = i % S;
             if (!s_fail && !mbar_wait(&epi_done[s], (i / S) & 1)) s_fail = 1;
             const int tile_col0 = tr.ct * kExpandN;
@@ -795,7 +896,7 @@ sgmv_expand_tc_kernel(const __grid_constant__ CUtensorMap mvh, const __grid_cons
                 bulk_wait_read();   // the stage may be refilled once the stores have read it
             }
             mbar_arrive(&yempty[s]);
-            if (!tr.next(p, n_rt, n_items)) break;
+            more = tr.next();
         }
         bulk_wait_all();
     }
@@ -865,7 +966,7 @@ bool configure_once(const void* fn, size_t smem, int& configured_device, size_t&
 cudaError_t launch_sgmv_shrink_tc(float* v, int ld_v, bf16_t* vh, bf16_t* vl, const bf16_t* x, int ld_x, int h_in,
                                   const ProjSet& ps, const int32_t* seg_starts, const int32_t* seg_slot, int n_segs,
                                   int n_pos, int n_rows, int n_slots, unsigned flags, int32_t* status,
-                                  cudaStream_t stream)
+                                  cudaStream_t stream, unsigned* tickets)
 {
     if (n_pos <= 0 || n_segs <= 0) return cudaSuccess;
     const int R = ps.n_proj * ps.r_slot;
@@ -902,6 +1003,7 @@ cudaError_t launch_sgmv_shrink_tc(float* v, int ld_v, bf16_t* vh, bf16_t* vl, co
     p.ld_p = ps.n_proj * p.r_pad64;
     p.x_ready = (flags & LORA_APPLY_X_READY) ? 1 : 0;
     p.stall_tx = test_stall_bytes(kStallShrinkTc);
+    p.tickets = tickets;
     p.status = status;
     // Few row tiles: split K over a cluster of ks CTAs per tile so that the
     // grid covers the SMs (each CTA keeps at least two K blocks).
@@ -945,7 +1047,8 @@ cudaError_t launch_sgmv_shrink_tc(float* v, int ld_v, bf16_t* vh, bf16_t* vl, co
 
 cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const bf16_t* vl, const ProjSet& ps,
                                   const int32_t* seg_starts, const int32_t* seg_slot, int n_segs, int n_pos,
-                                  int n_rows, int n_slots, unsigned flags, int32_t* status, cudaStream_t stream)
+                                  int n_rows, int n_slots, unsigned flags, int32_t* status, cudaStream_t stream,
+                                  unsigned* tickets)
 {
     if (n_pos <= 0 || n_segs <= 0) return cudaSuccess;
     const int r_pad64 = (ps.r_slot + kKB - 1) / kKB * kKB;
@@ -996,27 +1099,76 @@ cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const b
     p.ld_y = ld_y;
     p.stall_tx = test_stall_bytes(kStallExpandTc);
     p.status = status;
+    // Dynamic order (work items taken from the call's counter, so that CTAs
+    // that start late or run slow take fewer) for large work items, while
+    // every row tile fits the table; the static round-robin order otherwise.
+    // Measured on one box: Mistral-7B prefill (16-tile items) 1.427 ->
+    // 1.409 ms per step; the mixed batch (4-tile items) 3.70 -> 3.81 ms, where
+    // each item's hand-off costs more than the balance gains.
+    // LORA_TC_EXPAND_DYNAMIC: 0 never, 2 for every size the table allows.
+    const int dyn_env = env_int("LORA_TC_EXPAND_DYNAMIC", 1);
+    p.tickets = tickets;
+    p.dyn = tickets != nullptr && rt_bound <= kMaxRt && dyn_env != 0 && (dyn_env == 2 || p.chunk >= 8);
     const int kbs = r_pad64 / kKB;
-    // r_pad64 = 64: five y stages and one v slice buffer, or four stages and
-    // two buffers; r_pad64 = 128: three stages and one buffer (each 225 KB
-    // with the two B' stages).  Large work items (8 or more tiles) pay the
-    // v-slice load of one buffer rarely and gain from the deeper ring; small
-    // ones keep the second buffer.
-    const int st_env = env_int("LORA_TC_EXPAND_STAGES", p.chunk >= 8 ? kStagesY : 4);
-    const int stages = kbs == 1 ? std::max(3, std::min(kStagesY, st_env)) : 3;
-    const int vbufs = kbs == 1 && stages < kStagesY ? 2 : 1;
+    // The row-tile table, then the rings: r_pad64 = 64: five y stages and one
+    // v slice buffer, or four and two; r_pad64 = 128: fewer.  Large work items
+    // (8 or more tiles) pay the v-slice load of one buffer rarely and gain
+    // from the deeper ring; small ones keep the second buffer.  The deepest
+    // form that fits beside the table and the kernel's own shared memory.
+    const int table_entries = p.dyn ? static_cast<int>(rt_bound) : kMaxItems;
+    p.table_bytes = (table_entries * static_cast<int>(sizeof(RowTile)) + 15) / 16 * 16;
+    auto* kernel = p.dyn ? sgmv_expand_tc_kernel<true> : sgmv_expand_tc_kernel<false>;
+    static size_t static_smem[2] = {0, 0}, smem_optin = 0;
+    static int smem_device = -1;
+    if (smem_device != dev) {
+        cudaFuncAttributes fa0{}, fa1{};
+        int optin = 0;
+        if (cudaFuncGetAttributes(&fa0, sgmv_expand_tc_kernel<false>) != cudaSuccess ||
+            cudaFuncGetAttributes(&fa1, sgmv_expand_tc_kernel<true>) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return cudaErrorInvalidValue;
+        static_smem[0] = fa0.sharedSizeBytes;
+        static_smem[1] = fa1.sharedSizeBytes;
+        smem_optin = static_cast<size_t>(optin);
+        smem_device = dev;
+    }
+    const size_t own_smem = static_smem[p.dyn ? 1 : 0];
+    auto smem_of = [&](int st, int vb) {
+        return static_cast<size_t>(p.table_bytes) + 1024 +
+               static_cast<size_t>(vb * 2 * kbs + 2 * kbs + 2 * st) * kBoxBytes;
+    };
+    static const int kBig[][2] = {{5, 1}, {4, 1}, {3, 1}, {2, 1}};
+    static const int kSmall[][2] = {{4, 2}, {3, 2}, {4, 1}, {3, 1}, {2, 1}};
+    const bool big = p.chunk >= 8;
+    const int n_forms = big ? 4 : 5;
+    int stages = 2, vbufs = 1;
+    const int st_env = env_int("LORA_TC_EXPAND_STAGES", 0);
+    for (int f = 0; f < n_forms; ++f) {
+        const int st = big ? kBig[f][0] : kSmall[f][0], vb = big ? kBig[f][1] : kSmall[f][1];
+        if (kbs != 1 && vb != 1) continue;
+        if (st_env > 0 && st != st_env) continue;
+        if (own_smem + smem_of(st, vb) <= smem_optin) {
+            stages = st;
+            vbufs = vb;
+            break;
+        }
+    }
     p.stages = stages;
     p.vbufs = vbufs;
-    const size_t smem = static_cast<size_t>(vbufs * 2 * kbs + 2 * kbs + 2 * stages) * kBoxBytes + 1024;
+    const size_t smem = smem_of(stages, vbufs);
+    if (own_smem + smem > smem_optin) return cudaErrorInvalidValue;
     static int configured = -1;
     static size_t configured_bytes = 0;
-    if (!configure_once(reinterpret_cast<const void*>(sgmv_expand_tc_kernel), smem, configured, configured_bytes))
+    static int configured_dyn = -1;
+    static size_t configured_bytes_dyn = 0;
+    if (!(p.dyn ? configure_once(reinterpret_cast<const void*>(kernel), smem, configured_dyn, configured_bytes_dyn)
+                : configure_once(reinterpret_cast<const void*>(kernel), smem, configured, configured_bytes)))
         return cudaErrorInvalidValue;
     // One CTA per SM (the shared memory allows no more), and enough CTAs that
     // none takes more than kMaxItems items.
     const long long items_bound = rt_bound * p.n_chunks;
     long long grid = env_int("LORA_TC_EXPAND_GRID", n_sms);
-    grid = std::max(grid, (items_bound + kMaxItems - 1) / kMaxItems);   // at most kMaxItems items per CTA
+    if (!p.dyn) grid = std::max(grid, (items_bound + kMaxItems - 1) / kMaxItems);   // at most kMaxItems items per CTA
     grid = std::min(grid, items_bound);
     if (grid > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
@@ -1029,7 +1181,7 @@ cudaError_t launch_sgmv_expand_tc(bf16_t* y, int ld_y, const bf16_t* vh, const b
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = (flags & LORA_APPLY_NO_PDL) ? 0 : 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, sgmv_expand_tc_kernel, mvh, mvl, my, mb[0], mb[1], mb[2], mb[3], p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, mvh, mvl, my, mb[0], mb[1], mb[2], mb[3], p);
     note_launch();
     return e;
 }

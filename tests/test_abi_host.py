@@ -190,9 +190,11 @@ def test_kernel_entry_points_validate_before_launch():
     assert st == 2
     # a slice whose end overflows int is past the row, not wrapped around
     assert lib.lora_bgmv_expand(base, 64, 2**31 - 8, 64, base, 16, base, ids, 4, 16, 2, 0, 0) == 2
-    # bf16 hi/lo planes (rank padded to 64, region rounded to 256 B) + fp32 v
+    # bf16 hi/lo planes (rank padded to 64) + fp32 v + the expand's work-item
+    # counter, each region rounded to 256 B
     planes = (2 * 10 * 3 * 64 * 2 + 255) // 256 * 256
-    assert lib.lora_apply_workspace_bytes(10, 3, 16) == planes + 10 * 3 * 16 * 4
+    fp32 = (10 * 3 * 16 * 4 + 255) // 256 * 256
+    assert lib.lora_apply_workspace_bytes(10, 3, 16) == planes + fp32 + 256
 
 
 def test_linear_and_merge_batch_validate_before_launch():

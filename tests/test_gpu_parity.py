@@ -506,8 +506,13 @@ def _segments(lens, slots):
     (8200, (4096,), 16, [200], [2]),                                     # h_in not a multiple of 64
 ])
 @pytest.mark.parametrize("mode", ["delta", "accumulate"])
-def test_apply_prefill_tensor_core(h_in, widths, rank, lens, slots, mode):
-    """Prefill segments of >= 64 rows take the tcgen05 shrink/expand route."""
+@pytest.mark.parametrize("order", ["default", "dynamic"])
+def test_apply_prefill_tensor_core(h_in, widths, rank, lens, slots, mode, order, monkeypatch):
+    """Prefill segments of >= 64 rows take the tcgen05 shrink/expand route;
+    "dynamic": the expand takes its work items from the call's counter even
+    for these small items (the order it uses for large ones)."""
+    if order == "dynamic":
+        monkeypatch.setenv("LORA_TC_EXPAND_DYNAMIC", "2")
     ids = _segments(lens, slots)
     rng = np.random.default_rng(h_in)
     ids = np.concatenate([ids, rng.integers(-1, 4, 9).astype(np.int32)])   # plus some decode rows

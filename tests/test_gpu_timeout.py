@@ -50,13 +50,17 @@ def _call(wl, st, meta, ws, stream):
     return to_host(y), abi.lora_read_device_status(status), time.perf_counter() - t0
 
 
-@pytest.mark.parametrize("shrink_ks", [None, "1"])
+@pytest.mark.parametrize("variant", [None, "shrink_ks_1", "expand_dynamic"])
 @pytest.mark.parametrize("kernel", list(STALL))
-def test_stalled_copy_reports_timeout_and_returns(kernel, shrink_ks, monkeypatch):
-    if shrink_ks is not None and kernel != "shrink_tc":
+def test_stalled_copy_reports_timeout_and_returns(kernel, variant, monkeypatch):
+    if variant == "shrink_ks_1" and kernel != "shrink_tc":
         pytest.skip("the cluster split only concerns the shrink")
-    if shrink_ks is not None:
-        monkeypatch.setenv("LORA_TC_SHRINK_KS", shrink_ks)   # one CTA per row tile (no cluster)
+    if variant == "expand_dynamic" and kernel != "expand_tc":
+        pytest.skip("the work-item order only concerns the expand")
+    if variant == "shrink_ks_1":
+        monkeypatch.setenv("LORA_TC_SHRINK_KS", "1")   # one CTA per row tile (no cluster)
+    if variant == "expand_dynamic":
+        monkeypatch.setenv("LORA_TC_EXPAND_DYNAMIC", "2")   # items from the call's counter
     wl = _case(h_in=1024)   # 16 K blocks: the shrink splits K over a cluster unless told not to
     st = store.GroupStore.from_workload(wl, "g")
     meta = store.BatchMeta(wl.ids, wl.n_prefill, wl.n_slots)
