@@ -162,7 +162,7 @@ NCU_TRAFFIC = {
              "bytes_per_call": 113216512},
     # captured on 2 layers, scaled to the 28 of a step (every layer has the same shapes)
     "linear_llama3b_decode": {"files": ['linear_swap.cu', 'bgmv_grouped.cu', 'tc_common.cuh', 'tmap.cpp', 'decode_common.cuh', 'common.cuh', 'cluster.cuh'],
-             "src": "5798ea1c8569984d", "bytes_per_step": 1603055104},
+             "src": "3a6bf76587f4524e", "bytes_per_step": 1603055104},
 }
 
 

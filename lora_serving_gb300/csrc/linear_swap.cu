@@ -247,7 +247,7 @@ linear_swap_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant
         bool ok = true, acc = false;
         for (int i = 0; i < n_steps && ok; ++i) {
             const int s = i % kSwStages;
-            // lane 0 waits for the stage; the warp follows its verdict together
+            // lane 0 waits for the stage; the warp follows its answer together
             int landed = 1;
             if (lane == 0) landed = mbar_wait_spin(&full[s], (i / kSwStages) & 1) ? 1 : 0;
             landed = __shfl_sync(0xFFFFFFFFu, landed, 0);
