@@ -407,16 +407,21 @@ lora_status_t lora_linear(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld
     }
     bf16_t* vh = static_cast<bf16_t*>(workspace);
     bf16_t* vl = vh + plane_region_bytes(T, n_proj, r_slot) / 2 / sizeof(bf16_t);
+    unsigned* tickets = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + plane_region_bytes(T, n_proj, r_slot) +
+                                                    fp32_region_bytes(T, n_proj, r_slot));
+    bool tickets_zeroed = false;   // the tensor-core shrink zeroes the linear kernel's tile counter
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     // v = A x into the hi/lo planes: tensor-core shrink over the prefill
     // segments (grouped shrink over them where the tensor-core form does not
     // apply), grouped shrink over the decode groups
     if (P > 0 && meta->n_segs > 0) {
-        if (tc_shrink)
+        if (tc_shrink) {
             LORA_TRY(cuda_status(lora::launch_sgmv_shrink_tc(nullptr, 0, vh, vl, x, ld_x, h_in, ps, meta->seg_starts,
                                                              meta->seg_slot, meta->n_segs, P, T, n_slots,
-                                                             LORA_APPLY_NO_PDL, dev_status, s)));
+                                                             LORA_APPLY_NO_PDL, dev_status, s, tickets)));
+            tickets_zeroed = true;
+        }
         else
             LORA_TRY(cuda_status(lora::launch_bgmv_grouped_shrink(x, ld_x, h_in, ps, nullptr, meta->seg_starts,
                                                                   meta->seg_slot, meta->n_segs, P,
@@ -443,7 +448,7 @@ lora_status_t lora_linear(lora_bf16_t* y, int ld_y, const lora_bf16_t* x, int ld
         return cuda_status(lora::launch_linear_swap(y, ld_y, x, ld_x, h_in, W, ld_w, n_out, ps, vh, vl,
                                                     meta->lora_ids, T, n_slots, dev_status, s));
     return cuda_status(lora::launch_linear_tc(y, ld_y, x, ld_x, h_in, W, ld_w, n_out, ps, vh, vl, meta->lora_ids, T,
-                                              n_slots, dev_status, s));
+                                              n_slots, dev_status, s, tickets_zeroed ? tickets : nullptr));
 }
 
 lora_status_t lora_merge(lora_bf16_t* W, int ld_w, int out, int h_in, const lora_bf16_t* A,

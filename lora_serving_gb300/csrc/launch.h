@@ -116,7 +116,8 @@ cudaError_t launch_group_expand_f32(bf16_t* y, int ld_y, const float* v, int ld_
 // projections' base weights, v from the bf16 hi/lo planes.
 cudaError_t launch_linear_tc(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int h_in, const bf16_t* W, int ld_w,
                              int n_out, const ProjSet& ps, const bf16_t* vh, const bf16_t* vl,
-                             const int32_t* ids, int n_rows, int n_slots, int32_t* status, cudaStream_t stream);
+                             const int32_t* ids, int n_rows, int n_slots, int32_t* status, cudaStream_t stream,
+                             unsigned* tickets = nullptr);
 
 // The same layer for decode-sized batches (n_rows <= 64, r_slot <= 64): the
 // tile turned around (128 output columns as the MMA's M, the rows as its N),

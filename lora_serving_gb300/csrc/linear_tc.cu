@@ -79,6 +79,8 @@ struct LinearParams {
     const bf16_t* B[LORA_MAX_PROJ];
     int n_tm, n_tn, n_tiles, n_kb, kbs;
     int cs;                      // split-K cluster size (1: persistent tiles)
+    unsigned* tickets;           // persistent tiles in the dynamic order: the call's tile counter (zeroed
+                                 // by the shrink before this kernel), or null for tiles c, c + G, ...
     int x_box_bytes;             // bytes of one x box (fewer rows when the batch is one short tile)
     const int32_t* ids;
     const bf16_t* vh;
@@ -345,6 +347,65 @@ __device__ __noinline__ void splitk_reduce(const LinearParams& P, int t, int cra
     }
 }
 
+// The tiles a CTA takes: tiles c, c + G, ... (static order), or in the
+// dynamic order the tiles numbered by the call's counter, so that CTAs that
+// start late or run slow take fewer.  In the dynamic order the producer
+// warp's lane 0 takes each tile's ticket one tile early and hands the tile
+// numbers to the MMA, mask and epilogue warps through a queue of kLQD slots.
+constexpr int kLQD = 8;
+constexpr int kLTileReaders = 2 + kLEpiWarps;   // MMA warp, mask warp, epilogue warps
+template <bool kDyn>
+struct LTileSeq {
+    int t_first, t_step, n_tiles;
+    const LinearParams& P;
+    long long* q_item;
+    uint64_t* q_full;
+    uint64_t* q_empty;
+    volatile int* fail;
+    unsigned ahead;   // producer lane 0: the next tile's ticket
+    __device__ __forceinline__ LTileSeq(int tf, int ts, const LinearParams& pp, long long* qi, uint64_t* qf, uint64_t* qe,
+                                        volatile int* f)
+        : t_first(tf), t_step(ts), n_tiles(pp.n_tiles), P(pp), q_item(qi), q_full(qf), q_empty(qe), fail(f), ahead(0)
+    {
+    }
+    // The warp's k-th tile, or -1 past the last (or on a timeout, with *fail
+    // set).  Every lane of the warp calls it.
+    __device__ __forceinline__ int get(int k, bool producer)
+    {
+        if constexpr (!kDyn) {
+            const long long t = t_first + static_cast<long long>(k) * t_step;
+            return t < n_tiles ? static_cast<int>(t) : -1;
+        } else {
+            const int lane = threadIdx.x & 31, slot = k % kLQD;
+            int t = -1;
+            if (producer) {
+                if (lane == 0) {
+                    if (k >= kLQD && !mbar_wait_spin(&q_empty[slot], ((k / kLQD) - 1) & 1)) {
+                        *fail = 1;   // the tile numbers stop here: every reader's wait runs out
+                    } else {
+                        const unsigned tk = *fail ? 0xFFFFFFFFu : (k == 0 ? atomicAdd(P.tickets, 1u) : ahead);
+                        t = static_cast<long long>(tk) < n_tiles ? static_cast<int>(tk) : -1;
+                        if (t >= 0) ahead = atomicAdd(P.tickets, 1u);
+                        q_item[slot] = t;
+                        mbar_arrive(&q_full[slot]);
+                    }
+                }
+                return __shfl_sync(0xFFFFFFFFu, t, 0);
+            }
+            const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&q_full[slot], (k / kLQD) & 1));
+            if (!ok) {
+                *fail = 1;
+                return -1;
+            }
+            t = static_cast<int>(q_item[slot]);
+            __syncwarp();   // every lane has read the slot before it is freed
+            if (lane == 0) mbar_arrive(&q_empty[slot]);
+            return t;
+        }
+    }
+};
+
+template <bool kDyn>
 __global__ void __launch_bounds__(kLThreads, 1)
 linear_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mw,
                  const __grid_constant__ CUtensorMap mvh, const __grid_constant__ CUtensorMap mvl,
@@ -354,6 +415,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full[kLStages], empty[kLStages], mask_req[kLStages], masked[kLStages];
     __shared__ __align__(8) uint64_t acc_full, acc_empty;
+    __shared__ __align__(8) uint64_t q_full[kLQD], q_empty[kLQD];
+    __shared__ long long q_item[kLQD];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_fail;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -370,6 +433,10 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
         }
         mbar_init(&acc_full, 1);
         mbar_init(&acc_empty, kLEpiWarps);
+        for (int j = 0; j < kLQD; ++j) {
+            mbar_init(&q_full[j], 1);
+            mbar_init(&q_empty[j], kLTileReaders);
+        }
         mbar_init_fence();
         s_fail = 0;
     }
@@ -381,11 +448,14 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
     const int crank = P.cs > 1 ? static_cast<int>(cluster_rank()) : 0;
     const int t_first = P.cs > 1 ? static_cast<int>(blockIdx.x) / P.cs : static_cast<int>(blockIdx.x);
     const int t_step = P.cs > 1 ? P.n_tiles : static_cast<int>(gridDim.x);
+    LTileSeq<kDyn> seq(t_first, t_step, P, q_item, q_full, q_empty, &s_fail);
     float* part = reinterpret_cast<float*>(ring);   // split K: this CTA's partial sums, after its K loop
 
     if (warp == 0) {   // ---- producer (lane 0 issues; the warp plans each tile) ----
         int it = 0;
-        for (int t = t_first; t < P.n_tiles && !s_fail; t += t_step) {
+        for (int kk = 0; !s_fail; ++kk) {
+            const int t = seq.get(kk, true);
+            if (t < 0) break;
             const LTile T = tile_of(P, t);
             Plan pl;
             pl.make(P, T.m, crank);
@@ -428,7 +498,9 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
     } else if (warp == 1) {   // ---- MMA issuer ----
         int it = 0, ti = 0, ok = 1;
         int mc[kLStages] = {};   // masked steps seen per stage (the phase of masked[s])
-        for (int t = t_first; ok && t < P.n_tiles && !s_fail; t += t_step, ++ti) {
+        for (int kk = 0; ok && !s_fail; ++kk, ++ti) {
+            const int t = seq.get(kk, false);
+            if (t < 0) break;
             const LTile T = tile_of(P, t);
             Plan pl;
             pl.make(P, T.m, crank);
@@ -486,7 +558,9 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
     } else if (warp == kLMaskWarp) {   // ---- v masking for halves that mix adapters ----
         int it = 0, ok = 1;
         int mr[kLStages] = {};   // requests served per stage (the phase of mask_req[s])
-        for (int t = t_first; ok && t < P.n_tiles && !s_fail; t += t_step) {
+        for (int kk = 0; ok && !s_fail; ++kk) {
+            const int t = seq.get(kk, false);
+            if (t < 0) break;
             const LTile T = tile_of(P, t);
             Plan pl;
             pl.make(P, T.m, crank);
@@ -526,7 +600,9 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
         const int quarter = warp & 3;        // tensor-memory lanes this warp may read
         const int cs = (e >> 2) * 64;        // its 64 columns of the tile
         int ti = 0;
-        for (int t = t_first; t < P.n_tiles; t += t_step, ++ti) {
+        for (int kk = 0;; ++kk, ++ti) {
+            const int t = seq.get(kk, false);
+            if (t < 0) break;
             const LTile T = tile_of(P, t);
             Plan pl;
             pl.make(P, T.m, crank);
@@ -637,7 +713,8 @@ size_t linear_tc_smem() { return static_cast<size_t>(kLStages) * kStageBytes + 1
 
 cudaError_t launch_linear_tc(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int h_in, const bf16_t* W, int ld_w,
                              int n_out, const ProjSet& ps, const bf16_t* vh, const bf16_t* vl,
-                             const int32_t* ids, int n_rows, int n_slots, int32_t* status, cudaStream_t stream)
+                             const int32_t* ids, int n_rows, int n_slots, int32_t* status, cudaStream_t stream,
+                             unsigned* tickets)
 {
     if (n_rows <= 0) return cudaSuccess;
     LinearParams P{};
@@ -689,11 +766,13 @@ cudaError_t launch_linear_tc(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(linear_tc_smem()));
-        if (e != cudaSuccess) return e;
-        e = prefer_max_shared(reinterpret_cast<const void*>(linear_tc_kernel));
-        if (e != cudaSuccess) return e;
+        for (const void* fn : {reinterpret_cast<const void*>(linear_tc_kernel<false>),
+                               reinterpret_cast<const void*>(linear_tc_kernel<true>)}) {
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(linear_tc_smem()));
+            if (e != cudaSuccess) return e;
+            e = prefer_max_shared(fn);
+            if (e != cudaSuccess) return e;
+        }
         e = cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         configured_device = dev;
@@ -732,7 +811,7 @@ cudaError_t launch_linear_tc(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int
                 cfg.attrs = &attr;
                 cfg.numAttrs = 1;
                 int active = 0;
-                if (cudaOccupancyMaxActiveClusters(&active, linear_tc_kernel, &cfg) == cudaSuccess &&
+                if (cudaOccupancyMaxActiveClusters(&active, linear_tc_kernel<false>, &cfg) == cudaSuccess &&
                     active >= P.n_tiles)
                     cs = c;
             }
@@ -743,12 +822,17 @@ cudaError_t launch_linear_tc(bf16_t* y, int ld_y, const bf16_t* x, int ld_x, int
     cs = std::max(1, std::min({env_int("LORA_LINEAR_SPLIT", cs), kMaxSplit, P.n_kb}));
     if (n_rows > kLH || P.n_tm != 1) cs = 1;
     P.cs = cs;
+    // persistent tiles in the dynamic order when the call's counter is given
+    // (its shrink zeroes it); split K keeps one tile per cluster
+    P.tickets = cs == 1 && env_int("LORA_LINEAR_DYNAMIC", 1) != 0 ? tickets : nullptr;
     cfg.gridDim = dim3(static_cast<unsigned>(cs > 1 ? P.n_tiles * cs
                                                     : std::min<long long>(env_int("LORA_LINEAR_GRID", n_sms), n_tiles)));
     attr.val.clusterDim.x = cs;
     cfg.attrs = &attr;
     cfg.numAttrs = cs > 1 ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, linear_tc_kernel, mx, mw, mvh, mvl, mb[0], mb[1], mb[2], mb[3], P);
+    e = P.tickets != nullptr
+            ? cudaLaunchKernelEx(&cfg, linear_tc_kernel<true>, mx, mw, mvh, mvl, mb[0], mb[1], mb[2], mb[3], P)
+            : cudaLaunchKernelEx(&cfg, linear_tc_kernel<false>, mx, mw, mvh, mvl, mb[0], mb[1], mb[2], mb[3], P);
     note_launch();
     return e;
 }

@@ -150,7 +150,7 @@ struct ShrinkTcParams {
     int ks;              // CTAs per row tile (a cluster), each a slice of K
     int x_ready;         // x is not written by the preceding kernel: read it before the wait
     unsigned stall_tx;   // test hook: extra bytes expected on the first stage (0 normally)
-    unsigned* tickets;   // the following expand's work-item counter, zeroed here (or null)
+    unsigned* tickets;   // the work counter of the kernel that follows in the call (expand or linear), zeroed here (or null)
     int32_t* status;
 };
 
@@ -216,13 +216,18 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
     grid_dep_launch();
     const int crank = p.ks > 1 ? static_cast<int>(cluster_rank()) : 0;
     const TileInfo ti = find_tile<kShrinkThreads>(p.seg_starts, p.seg_slot, p.n_segs, p.n_pos, blockIdx.x / p.ks);
+    // Block 0 zeroes the counter the kernel after this one takes its work
+    // from (after the grid dependency: no kernel before this one still uses
+    // it), on every path, also when the call has no adapter tile at all.
     if (!ti.found) {
         grid_dep_wait();
+        if (p.tickets != nullptr && blockIdx.x == 0 && tid == 0) *p.tickets = 0u;
         if (ti.bad && blockIdx.x == 0 && tid == 0) flag(p.status, LORA_DEV_BAD_SEGMENT);
         return;
     }
     if (ti.slot >= p.n_slots || ti.slot < -1) {
         grid_dep_wait();
+        if (p.tickets != nullptr && blockIdx.x == 0 && tid == 0) *p.tickets = 0u;
         if (tid == 0 && crank == 0) flag(p.status, LORA_DEV_SLOT_OUT_OF_RANGE);
         return;
     }
@@ -318,9 +323,7 @@ sgmv_shrink_tc_kernel(const __grid_constant__ CUtensorMap mx, const __grid_const
     tc_fence_after();
     ok = __syncthreads_and(ok && !s_fail);
     grid_dep_wait();   // the preceding kernel may still read the buffers written below
-    // The expand that follows in the same call takes its work items from this
-    // counter; no kernel before this one still uses it.
-    if (p.tickets != nullptr && blockIdx.x == 0 && tid == 0) *p.tickets = 0u;
+    if (p.tickets != nullptr && blockIdx.x == 0 && tid == 0) *p.tickets = 0u;   // (as above)
     const int r = warp * 32 + lane;   // tile row = TMEM lane
     if (p.ks == 1) {
         const bool row_ok = r < ti.nrows;
