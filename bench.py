@@ -152,14 +152,14 @@ NCU_TRAFFIC = {
              "bytes_per_call": 3442240},
     "stress70b": {"files": ['bgmv_grouped.cu', 'decode_common.cuh', 'common.cuh', 'cluster.cuh'], "src": "d394e5f3b5e71d17",
              "bytes_per_call": 988095360},
-    "mistral7b_prefill": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh', 'cluster.cuh'], "src": "bbfc40ef82ee164b",
-             "bytes_per_call": 2061107968},
+    "mistral7b_prefill": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh', 'cluster.cuh'], "src": "8bc12fda24a1f2bd",
+             "bytes_per_call": 2061036160},
     "merge_mistral7b": {"files": ['merge.cu', 'merge_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh', 'cluster.cuh'], "src": "868105680b61064e",
              "bytes_per_step": 6934772736},
-    "linear_mistral7b_prefill": {"files": ['linear_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh', 'cluster.cuh'], "src": "fcb8237452adf5e9",
-             "bytes_per_step": 19563948288},
-    "mixed": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'bgmv_fused.cu', 'decode_common.cuh', 'common.cuh', 'cluster.cuh'], "src": "9b2d6574b12f3d7a",
-             "bytes_per_call": 113216512},
+    "linear_mistral7b_prefill": {"files": ['linear_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh', 'cluster.cuh'], "src": "f30119a4aaa30b0e",
+             "bytes_per_step": 13868097280},
+    "mixed": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'bgmv_fused.cu', 'decode_common.cuh', 'common.cuh', 'cluster.cuh'], "src": "cf39137e5cbe5700",
+             "bytes_per_call": 113187840},
     # captured on 2 layers, scaled to the 28 of a step (every layer has the same shapes)
     "linear_llama3b_decode": {"files": ['linear_swap.cu', 'bgmv_grouped.cu', 'tc_common.cuh', 'tmap.cpp', 'decode_common.cuh', 'common.cuh', 'cluster.cuh'],
              "src": "3a6bf76587f4524e", "bytes_per_step": 1603055104},
