@@ -7,6 +7,15 @@ relative L2 error of the written outputs is <= 1e-3 and the max abs error is
 the spacing is 2^-5 = 0.03125): such an element may differ from the oracle by
 at most one bf16 step; the count of such elements is returned.  Rows whose
 id is -1 must be bit-identical to y_in.
+
+One more figure, stricter than the stated bar: at least MIN_EXACT of the
+adapter rows' elements must equal the oracle's value bit for bit.  A
+kernel that forms y + delta in fp32 and rounds once agrees with the
+correctly rounded fp64 result except where y lies within the fp32 error of
+a rounding boundary (about 1e-4 of the elements).  The rel-L2 figure
+alone is weak in accumulate mode, where y_in ~ N(0,1) dominates the norm:
+a delta 0.1 % too large moves rel-L2 to only 8.5e-4 there, but leaves 10 %
+of the elements one step off.
 """
 from __future__ import annotations
 
@@ -17,6 +26,7 @@ import oracle as O
 
 REL_L2 = 1e-3
 MAX_ABS = 3e-2
+MIN_EXACT = 0.95
 
 
 def to_dev(bits: np.ndarray, device="cuda") -> torch.Tensor:
@@ -86,7 +96,7 @@ def check_bf16(got_bits, ref_bits, ids, yin_bits, what=""):
                                       err_msg=f"{what}: base-only rows changed")
     act = ~base
     if not act.any():
-        return {"rel_l2": 0.0, "max_abs": 0.0, "n_big_step": 0, "n": 0}
+        return {"rel_l2": 0.0, "max_abs": 0.0, "n_big_step": 0, "n": 0, "exact": 1.0}
     got = O.bf16_to_f64(got_bits[act])
     ref = O.bf16_to_f64(ref_bits[act])
     err = np.abs(got - ref)
@@ -100,7 +110,10 @@ def check_bf16(got_bits, ref_bits, ids, yin_bits, what=""):
     assert not bad.any(), (f"{what}: {int(bad.sum())} elements off by more than "
                            f"max(3e-2, one bf16 step); worst {float(err.max()):.4g}; "
                            f"{n_big} elements one bf16 step off where the step exceeds 3e-2")
-    return {"rel_l2": rel, "max_abs": float(err.max()), "n_big_step": n_big, "n": int(err.size)}
+    exact = float(np.mean(got_bits[act] == ref_bits[act]))
+    assert exact >= MIN_EXACT, (f"{what}: only {exact:.4f} of the adapter rows' elements equal the "
+                                f"oracle's rounded value (at least {MIN_EXACT}); rel-L2 {rel:.3e}")
+    return {"rel_l2": rel, "max_abs": float(err.max()), "n_big_step": n_big, "n": int(err.size), "exact": exact}
 
 
 def shrink_bound(ids, x_bits, A_list, h_in):
