@@ -161,6 +161,11 @@ lora_status_t lora_bgmv_shrink(float* v, int ld_v, const lora_bf16_t* x, int ld_
     LORA_TRY(check_store(A));
     LORA_TRY(check_v(v, ld_v, r_slot));
     ProjSet ps = single_proj(A, nullptr, 0, 0, r_slot);
+    // Rows grouped by their ids on the device (each adapter's A streamed once
+    // per 16 rows) where the grouped kernels take the rank; per row otherwise.
+    if (lora::bgmv_ids_supported(r_slot, n_rows, n_slots))
+        return cuda_status(lora::launch_bgmv_ids_shrink_f32(v, ld_v, x, ld_x, h_in, ps, lora_ids, n_rows, n_slots,
+                                                            dev_status, reinterpret_cast<cudaStream_t>(stream)));
     RowMap m = ids_map(lora_ids, 0, n_rows, n_rows, n_slots);
     return cuda_status(lora::launch_shrink_rowwise(v, ld_v, x, ld_x, h_in, ps, m, dev_status,
                                                    reinterpret_cast<cudaStream_t>(stream)));
@@ -178,6 +183,9 @@ lora_status_t lora_bgmv_expand(lora_bf16_t* y, int ld_y, int y_off, int width,
     LORA_TRY(check_store(B));
     LORA_TRY(check_v(v, ld_v, r_slot));
     ProjSet ps = single_proj(nullptr, B, y_off, width, r_slot);
+    if (lora::bgmv_ids_supported(r_slot, n_rows, n_slots))
+        return cuda_status(lora::launch_bgmv_ids_expand_f32(y, ld_y, v, ld_v, ps, lora_ids, n_rows, n_slots,
+                                                            dev_status, reinterpret_cast<cudaStream_t>(stream)));
     RowMap m = ids_map(lora_ids, 0, n_rows, n_rows, n_slots);
     return cuda_status(lora::launch_expand_rowwise(y, ld_y, v, ld_v, ps, m, dev_status,
                                                    reinterpret_cast<cudaStream_t>(stream)));

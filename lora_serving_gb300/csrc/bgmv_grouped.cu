@@ -99,6 +99,52 @@ __device__ __forceinline__ bool unit_rows(const int32_t* perm, int pos0, int nro
     return bad;
 }
 
+// Ids form (per-row adapter ids, no gather metadata: the standalone BGMV
+// calls).  Unit u is the (u % subs)-th run of up to 16 rows, in row order,
+// among the rows whose id is slot u / subs; its rows land in s_rows (rows
+// past the unit's read 0).  One block-wide ordered compaction per NT ids,
+// stopping once the run is complete.  Unit 0 reads every id and reports one
+// outside [-1, n_slots) in bad (such a row matches no slot and is skipped).
+// Every thread takes part; the answer is uniform across the CTA.
+template <int NT>
+__device__ UnitInfo ids_unit(const int32_t* ids, int n_pos, int n_slots, int u, int subs, int* s_rows)
+{
+    __shared__ int s_cnt[NT / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    UnitInfo ui;
+    ui.slot = u / subs;
+    ui.g = ui.slot;
+    ui.pos0 = 0;
+    const int lo = (u - ui.slot * subs) * kRB;
+    int base = 0;   // matching rows in earlier rounds
+    bool bad = false;
+    for (int r0 = 0; r0 < n_pos && (u == 0 || base < lo + kRB); r0 += NT) {
+        const int i = r0 + tid;
+        const int id = i < n_pos ? __ldg(ids + i) : -1;
+        bad |= id < -1 || id >= n_slots;
+        const bool m = i < n_pos && id == ui.slot;
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, m);
+        if (lane == 0) s_cnt[warp] = __popc(bal);
+        __syncthreads();
+        int before = 0, total = 0;
+#pragma unroll
+        for (int w = 0; w < NT / 32; ++w) {
+            const int c = s_cnt[w];
+            if (w < warp) before += c;
+            total += c;
+        }
+        const int rank = base + before + __popc(bal & ((1u << lane) - 1u));
+        if (m && rank >= lo && rank < lo + kRB) s_rows[rank - lo] = i;
+        base += total;
+        __syncthreads();   // s_cnt is rewritten by the next round
+    }
+    ui.nrows = max(0, min(kRB, base - lo));
+    ui.found = ui.nrows > 0;
+    if (tid < kRB && tid >= ui.nrows) s_rows[tid] = 0;
+    ui.bad = __syncthreads_or(bad) && u == 0;
+    return ui;
+}
+
 // ---- grouped shrink ----------------------------------------------------------
 
 constexpr int kGsThreads = 256;
@@ -133,6 +179,8 @@ struct GsParams {
     int ks;                   // cluster size (CTAs splitting K)
     int x_ready;
     int late_trigger;         // dependents launch only once x may be read (see kShrinkTriggerLate)
+    const int32_t* ids;       // ids form: per-row adapter ids instead of the gather metadata (or null)
+    int id_subs;              // ids form: units per slot, ceil(n_pos / 16)
     int32_t* status;
 };
 
@@ -158,12 +206,14 @@ bgmv_group_shrink_kernel(GsParams p)
     const int cl = blockIdx.x / p.ks;
     const int unit = cl / p.n_rb, rb = cl - unit * p.n_rb;
     const int grid_units = static_cast<int>(gridDim.x) / (p.ks * p.n_rb);
-    const UnitInfo ui = grouped_unit<kGsThreads>(p, unit, grid_units);   // uniform across the cluster
+    // uniform across the cluster
+    const UnitInfo ui = p.ids ? ids_unit<kGsThreads>(p.ids, p.n_pos, p.n_slots, unit, p.id_subs, s_rows)
+                              : grouped_unit<kGsThreads>(p, unit, grid_units);
     const int pos0 = ui.pos0, nrows = ui.nrows, slot = ui.slot;
     const bool flagger = rb == 0 && crank == 0 && tid == 0;
     if (ui.bad) {   // flagged, and a unit that was found is still done
         grid_dep_wait();
-        if (flagger) flag(p.status, LORA_DEV_BAD_SEGMENT);
+        if (flagger) flag(p.status, p.ids ? LORA_DEV_SLOT_OUT_OF_RANGE : LORA_DEV_BAD_SEGMENT);
     }
     if (nrows <= 0 || slot == -1) {
         if (blockIdx.x == 0) grid_dep_wait();
@@ -223,7 +273,7 @@ bgmv_group_shrink_kernel(GsParams p)
         cp_async_commit();
     }
 
-    if (__syncthreads_or(unit_rows(p.perm, pos0, nrows, p.n_rows, s_rows))) {
+    if (__syncthreads_or(p.ids ? false : unit_rows(p.perm, pos0, nrows, p.n_rows, s_rows))) {
         cp_async_wait<0>();   // no copy may land after the CTA has left
         grid_dep_wait();      // same rows in every CTA of the cluster: all leave here
         if (flagger) flag(p.status, LORA_DEV_BAD_SEGMENT);
@@ -383,6 +433,8 @@ struct GexParams {
     int n_rows;
     int n_blocks;             // column blocks per unit, over all projections
     int upg;                  // direct unit form (units per group) or 0
+    const int32_t* ids;       // ids form: per-row adapter ids instead of the gather metadata (or null)
+    int id_subs;              // ids form: units per slot, ceil(n_pos / 16)
     int32_t* status;
 };
 
@@ -418,13 +470,15 @@ bgmv_group_expand_kernel(GexParams p)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int unit = blockIdx.x / p.n_blocks;
     const int blk = blockIdx.x - unit * p.n_blocks;
-    const UnitInfo ui = grouped_unit<kGxThreads>(p, unit, INT_MAX);   // unit count: checked by the shrink
+    const UnitInfo ui = p.ids ? ids_unit<kGxThreads>(p.ids, p.n_pos, p.n_slots, unit, p.id_subs, s_rows)
+                              : grouped_unit<kGxThreads>(p, unit, INT_MAX);   // unit count: checked by the shrink
     const int pos0 = ui.pos0, nrows = ui.nrows, slot = ui.slot;
     const bool bad = ui.bad;
+    const int32_t bad_bit = p.ids ? LORA_DEV_SLOT_OUT_OF_RANGE : LORA_DEV_BAD_SEGMENT;
     const bool flagger = blk == 0 && tid == 0;   // one CTA per unit reports
     if (nrows <= 0 || slot == -1) {
         if (blockIdx.x == 0 || bad) grid_dep_wait();
-        if (bad && flagger) flag(p.status, LORA_DEV_BAD_SEGMENT);
+        if (bad && flagger) flag(p.status, bad_bit);
         return;
     }
     if (slot < -1 || slot >= p.n_slots) {
@@ -450,7 +504,7 @@ bgmv_group_expand_kernel(GexParams p)
                  p.ps.B[pj] + (static_cast<size_t>(slot) * width + col0 + wc0) * r_slot, bytes, &s_bar[warp]);
     }
     __syncwarp();
-    if (__syncthreads_or(unit_rows(p.perm, pos0, nrows, p.n_rows, s_rows))) {
+    if (__syncthreads_or(p.ids ? false : unit_rows(p.perm, pos0, nrows, p.n_rows, s_rows))) {
         if (wcols > 0 && lane == 0) mbar_wait(&s_bar[warp], 0);   // let the block land before leaving (bounded)
         grid_dep_wait();
         if (flagger) flag(p.status, LORA_DEV_BAD_SEGMENT);
@@ -574,7 +628,7 @@ bgmv_group_expand_kernel(GexParams p)
         }
         __syncwarp();
     }
-    if (bad && flagger) flag(p.status, LORA_DEV_BAD_SEGMENT);
+    if (bad && flagger) flag(p.status, bad_bit);
 }
 
 }  // namespace
@@ -585,6 +639,8 @@ namespace {
 struct GroupedPlan {
     int r_pad64, ld_p, form_upg, xr, pdl, n_sms;
     long long units;
+    const int32_t* ids;   // ids form (per-row adapter ids), or null
+    int id_subs;
 };
 
 cudaError_t grouped_plan(const ProjSet& ps, int n_groups, int n_pos, int max_group_len, unsigned flags,
@@ -626,6 +682,21 @@ cudaError_t grouped_plan(const ProjSet& ps, int n_groups, int n_pos, int max_gro
     return cudaSuccess;
 }
 
+// The ids form's plan: units are (slot, run of 16 rows), as many as the
+// worst case (every row on one slot) needs.
+cudaError_t grouped_plan_ids(const ProjSet& ps, const int32_t* ids, int n_rows, int n_slots, GroupedPlan& g)
+{
+    const int subs = (n_rows + kRB - 1) / kRB;
+    const cudaError_t e = grouped_plan(ps, 1, n_rows, kRB, LORA_APPLY_NO_PDL, g);
+    if (e != cudaSuccess) return e;
+    g.form_upg = 0;
+    g.units = static_cast<long long>(n_slots) * subs;
+    g.xr = kRB;
+    g.ids = ids;
+    g.id_subs = subs;
+    return cudaSuccess;
+}
+
 // v goes to the planes vh/vl, or as fp32 to v (ld_v) when v is not null.
 cudaError_t grouped_shrink(const GroupedPlan& g, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
                            const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
@@ -663,6 +734,8 @@ cudaError_t grouped_shrink(const GroupedPlan& g, const bf16_t* x, int ld_x, int 
     sp.kc = ((h_in + ks - 1) / ks + kGsKT - 1) / kGsKT * kGsKT;
     sp.x_ready = (flags & LORA_APPLY_X_READY) ? 1 : 0;
     sp.late_trigger = (flags & kShrinkTriggerLate) ? 1 : 0;
+    sp.ids = g.ids;
+    sp.id_subs = g.id_subs;
     sp.status = status;
     const long long n_shrink = g.units * sp.n_rb * ks;
     if (n_shrink > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
@@ -717,6 +790,8 @@ cudaError_t grouped_expand(const GroupedPlan& g, bf16_t* y, int ld_y, const Proj
     gp.n_rows = n_rows;
     for (int q = 0; q < ps.n_proj; ++q) gp.n_blocks += (ps.width[q] + kGxCols - 1) / kGxCols;
     gp.upg = g.form_upg;
+    gp.ids = g.ids;
+    gp.id_subs = g.id_subs;
     gp.status = status;
     const long long n_expand = g.units * gp.n_blocks;
     if (n_expand > 0x7FFFFFFFll) return cudaErrorInvalidConfiguration;
@@ -780,6 +855,43 @@ cudaError_t launch_group_shrink_f32(float* v, int ld_v, const bf16_t* x, int ld_
     if (e != cudaSuccess) return e;
     return grouped_shrink(g, x, ld_x, h_in, ps, perm, gstarts, gslot, n_groups, n_pos, n_rows, n_slots,
                           LORA_APPLY_NO_PDL, nullptr, nullptr, v, ld_v, status, stream);
+}
+
+// The ids form launches n_slots * ceil(n_rows / 16) units, most of them
+// empty when the rows spread over the slots; past this many per call the
+// per-row kernels serve instead.
+constexpr long long kIdsMaxUnits = 1 << 16;
+
+bool bgmv_ids_supported(int r_slot, int n_rows, int n_slots)
+{
+    const long long units = static_cast<long long>(n_slots) * ((n_rows + kRB - 1) / kRB);
+    return r_slot <= 64 && r_slot % 8 == 0 && n_rows > 0 && units <= kIdsMaxUnits;
+}
+
+cudaError_t launch_bgmv_ids_shrink_f32(float* v, int ld_v, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
+                                       const int32_t* ids, int n_rows, int n_slots, int32_t* status,
+                                       cudaStream_t stream)
+{
+    if (n_rows <= 0) return cudaSuccess;
+    if (!v || !bgmv_ids_supported(ps.n_proj * ps.r_slot, n_rows, n_slots)) return cudaErrorInvalidValue;
+    GroupedPlan g{};
+    const cudaError_t e = grouped_plan_ids(ps, ids, n_rows, n_slots, g);
+    if (e != cudaSuccess) return e;
+    return grouped_shrink(g, x, ld_x, h_in, ps, nullptr, nullptr, nullptr, 0, n_rows, n_rows, n_slots,
+                          LORA_APPLY_NO_PDL, nullptr, nullptr, v, ld_v, status, stream);
+}
+
+cudaError_t launch_bgmv_ids_expand_f32(bf16_t* y, int ld_y, const float* v, int ld_v, const ProjSet& ps,
+                                       const int32_t* ids, int n_rows, int n_slots, int32_t* status,
+                                       cudaStream_t stream)
+{
+    if (n_rows <= 0) return cudaSuccess;
+    if (!v || !bgmv_ids_supported(ps.r_slot, n_rows, n_slots)) return cudaErrorInvalidValue;
+    GroupedPlan g{};
+    const cudaError_t e = grouped_plan_ids(ps, ids, n_rows, n_slots, g);
+    if (e != cudaSuccess) return e;
+    return grouped_expand(g, y, ld_y, ps, nullptr, nullptr, nullptr, 0, n_rows, n_rows, n_slots, nullptr, nullptr,
+                          v, ld_v, status, stream);
 }
 
 cudaError_t launch_group_expand_f32(bf16_t* y, int ld_y, const float* v, int ld_v, const ProjSet& ps,

@@ -111,6 +111,19 @@ cudaError_t launch_group_expand_f32(bf16_t* y, int ld_y, const float* v, int ld_
                                     int n_pos, int max_group_len, int n_rows, int n_slots, int32_t* status,
                                     cudaStream_t stream);
 
+// The grouped pair driven by per-row adapter ids (the standalone BGMV calls,
+// no gather metadata): unit = (slot, run of 16 rows with that id, in row
+// order), found by each CTA with a block-wide scan of the ids.  fp32 v;
+// r_slot <= 64 and at most 65536 units (bgmv_ids_supported).  Plain stream
+// order.
+bool bgmv_ids_supported(int r_slot, int n_rows, int n_slots);
+cudaError_t launch_bgmv_ids_shrink_f32(float* v, int ld_v, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
+                                       const int32_t* ids, int n_rows, int n_slots, int32_t* status,
+                                       cudaStream_t stream);
+cudaError_t launch_bgmv_ids_expand_f32(bf16_t* y, int ld_y, const float* v, int ld_v, const ProjSet& ps,
+                                       const int32_t* ids, int n_rows, int n_slots, int32_t* status,
+                                       cudaStream_t stream);
+
 // The LoRA linear layer: y[:, off_p + c] = bf16(x W^T + B'_p v_p) for every
 // row (ids per row, -1 = base only), W [n_out][ld_w] stacking the
 // projections' base weights, v from the bf16 hi/lo planes.
