@@ -269,6 +269,36 @@ def test_bad_slot_in_gather_groups_flagged_and_rows_skipped():
     check_bf16(got[ok], oracle_group(wl, "g", ok), ids[ok], wl.y["g"][ok], "bad group slot")
 
 
+@pytest.mark.parametrize("n_rows", [300, 1000])
+def test_bgmv_per_row_ids_over_several_scan_rounds(n_rows):
+    """The per-row-id calls group their rows on the device, each CTA scanning
+    the ids 256 (shrink) or 128 (expand) at a time.  Batches longer than one
+    round, with slot 0 holding more than 16 rows in every round: its runs of
+    16 span rounds.  Shrink and expand against the oracle; base rows keep
+    their v and y."""
+    rng = np.random.default_rng(n_rows)
+    ids = rng.integers(-1, 5, n_rows).astype(np.int32)
+    ids[rng.random(n_rows) < 0.3] = 0
+    wl = _small(ids, 0, n_slots=5, rank=16, h_in=512, widths=(320,), mode="accumulate")
+    st = store.GroupStore.from_workload(wl, "g")
+    d_ids = torch.from_numpy(wl.ids).cuda()
+    v = torch.full((n_rows, wl.r_slot), -7.0, device="cuda")
+    y = to_dev(wl.y["g"])
+    s = _status()
+    abi.lora_bgmv_shrink(v, to_dev(wl.x["g"]), st.A[0], d_ids, h_in=512, r_slot=wl.r_slot, n_slots=5, dev_status=s)
+    abi.lora_bgmv_expand(y, 0, 320, v, st.B[0], d_ids, r_slot=wl.r_slot, n_slots=5, dev_status=s)
+    torch.cuda.synchronize()
+    assert abi.lora_read_device_status(s) == 0
+    act = wl.ids >= 0
+    got_v = v.cpu().numpy().astype(np.float64)
+    ad = oracle_adapters(wl, "g", "p0")
+    ref_v = O.shrink(wl.ids, wl.x["g"], ad, v_cols=wl.r_slot)
+    bound = shrink_bound(wl.ids, wl.x["g"], [wl.A[("g", "p0", k)] for k in range(5)], 512)
+    assert np.all(np.abs(got_v[act] - ref_v[act]) <= bound[act])
+    assert np.all(got_v[~act] == -7.0), "base rows must not be written"
+    check_bf16(to_host(y), oracle_group(wl, "g"), wl.ids, wl.y["g"], f"bgmv ids n_rows={n_rows}")
+
+
 def test_bad_row_id_flagged_in_per_token_kernels():
     """The per-token BGMV entry points read lora_ids: ids outside [-1, n_slots)
     are flagged and those rows skipped."""
