@@ -104,7 +104,11 @@ typedef enum {
  *                pass the stacked store and r_slot = n_proj * slot rank)
  * lora_ids [dev] int32 [n_rows], -1 = base (v row not written)
  * v        [dev] fp32 [n_rows][ld_v], ld_v >= r_slot; fp32 accumulation
- * n_rows == 0 is a no-op.
+ * n_rows == 0 is a no-op.  For r_slot <= 64 (and n_slots * ceil(n_rows/16)
+ * <= 65536) the rows are grouped by id on the device, each adapter's A read
+ * once per run of 16 of its rows; otherwise row by row.  The form does not
+ * change the result.  An id outside [-1, n_slots) sets
+ * LORA_DEV_SLOT_OUT_OF_RANGE and its row is skipped.
  */
 lora_status_t lora_bgmv_shrink(float* v, int ld_v, const lora_bf16_t* x, int ld_x,
                                const lora_bf16_t* A, const int32_t* lora_ids, int n_rows,
@@ -119,6 +123,7 @@ lora_status_t lora_bgmv_shrink(float* v, int ld_v, const lora_bf16_t* x, int ld_
  * v        [dev] fp32 [n_rows][ld_v] (pass v + p*r_slot for projection p of
  *                a stacked shrink), ld_v >= r_slot
  * B        [dev] bf16 [n_slots][width][r_slot], already scaled (B')
+ * Kernel form and id checks as in lora_bgmv_shrink.
  */
 lora_status_t lora_bgmv_expand(lora_bf16_t* y, int ld_y, int y_off, int width,
                                const float* v, int ld_v, const lora_bf16_t* B,
