@@ -97,6 +97,17 @@ typedef enum {
  * ------------------------------------------------------------------ */
 
 /*
+ * Ordering of the four standalone calls below: as lora_apply with flags 0.
+ * Their kernels use programmatic dependent launch and may start while the
+ * kernel enqueued before them is still running.  They read the adapter store,
+ * lora_ids and the segment tables at once, so these must not be written by
+ * that kernel (copies made with cudaMemcpyAsync are ordered as usual).  They
+ * read x and v, and write v, y and dev_status, only once that kernel has
+ * completed.  None completes before the kernel before it.  The row-by-row
+ * form (slot ranks above 64) runs in plain stream order.
+ */
+
+/*
  * BGMV shrink [TGI 4, decode, token by token]:
  *   v[t][j] = sum_i A[id_t][j][i] * x[t][i]      for j < r_slot, id_t >= 0
  * x        [dev] bf16 [n_rows][ld_x], ld_x >= h_in

@@ -208,8 +208,8 @@ lora_status_t lora_sgmv_shrink(float* v, int ld_v, const lora_bf16_t* x, int ld_
     ProjSet ps = single_proj(A, nullptr, 0, 0, r_slot);
     if (!row_perm && max_seg_len >= kTcMinSegment && lora::sgmv_tc_supported(1, r_slot, h_in))
         return cuda_status(lora::launch_sgmv_shrink_tc(v, ld_v, nullptr, nullptr, x, ld_x, h_in, ps, seg_starts,
-                                                       seg_slot, n_segs, n_pos, n_rows, n_slots, LORA_APPLY_NO_PDL,
-                                                       dev_status, reinterpret_cast<cudaStream_t>(stream)));
+                                                       seg_slot, n_segs, n_pos, n_rows, n_slots, 0u, dev_status,
+                                                       reinterpret_cast<cudaStream_t>(stream)));
     // Short segments and gathered rows: the segments as groups of the
     // grouped shrink (units of 16 rows, each adapter's A streamed once per
     // unit), for ranks the grouped kernels take.

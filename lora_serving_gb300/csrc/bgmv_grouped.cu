@@ -687,7 +687,7 @@ cudaError_t grouped_plan(const ProjSet& ps, int n_groups, int n_pos, int max_gro
 cudaError_t grouped_plan_ids(const ProjSet& ps, const int32_t* ids, int n_rows, int n_slots, GroupedPlan& g)
 {
     const int subs = (n_rows + kRB - 1) / kRB;
-    const cudaError_t e = grouped_plan(ps, 1, n_rows, kRB, LORA_APPLY_NO_PDL, g);
+    const cudaError_t e = grouped_plan(ps, 1, n_rows, kRB, 0u, g);
     if (e != cudaSuccess) return e;
     g.form_upg = 0;
     g.units = static_cast<long long>(n_slots) * subs;
@@ -851,10 +851,10 @@ cudaError_t launch_group_shrink_f32(float* v, int ld_v, const bf16_t* x, int ld_
     if (n_pos <= 0 || n_groups <= 0) return cudaSuccess;
     if (!v || ps.r_slot > 64 || ps.r_slot % 8 != 0) return cudaErrorInvalidValue;
     GroupedPlan g{};
-    const cudaError_t e = grouped_plan(ps, n_groups, n_pos, max_group_len, LORA_APPLY_NO_PDL, g);
+    const cudaError_t e = grouped_plan(ps, n_groups, n_pos, max_group_len, 0u, g);
     if (e != cudaSuccess) return e;
-    return grouped_shrink(g, x, ld_x, h_in, ps, perm, gstarts, gslot, n_groups, n_pos, n_rows, n_slots,
-                          LORA_APPLY_NO_PDL, nullptr, nullptr, v, ld_v, status, stream);
+    return grouped_shrink(g, x, ld_x, h_in, ps, perm, gstarts, gslot, n_groups, n_pos, n_rows, n_slots, 0u, nullptr,
+                          nullptr, v, ld_v, status, stream);
 }
 
 // The ids form launches n_slots * ceil(n_rows / 16) units, most of them
@@ -877,8 +877,8 @@ cudaError_t launch_bgmv_ids_shrink_f32(float* v, int ld_v, const bf16_t* x, int 
     GroupedPlan g{};
     const cudaError_t e = grouped_plan_ids(ps, ids, n_rows, n_slots, g);
     if (e != cudaSuccess) return e;
-    return grouped_shrink(g, x, ld_x, h_in, ps, nullptr, nullptr, nullptr, 0, n_rows, n_rows, n_slots,
-                          LORA_APPLY_NO_PDL, nullptr, nullptr, v, ld_v, status, stream);
+    return grouped_shrink(g, x, ld_x, h_in, ps, nullptr, nullptr, nullptr, 0, n_rows, n_rows, n_slots, 0u, nullptr,
+                          nullptr, v, ld_v, status, stream);
 }
 
 cudaError_t launch_bgmv_ids_expand_f32(bf16_t* y, int ld_y, const float* v, int ld_v, const ProjSet& ps,
@@ -902,7 +902,7 @@ cudaError_t launch_group_expand_f32(bf16_t* y, int ld_y, const float* v, int ld_
     if (n_pos <= 0 || n_groups <= 0) return cudaSuccess;
     if (!v || ps.r_slot > 64 || ps.r_slot % 8 != 0) return cudaErrorInvalidValue;
     GroupedPlan g{};
-    const cudaError_t e = grouped_plan(ps, n_groups, n_pos, max_group_len, LORA_APPLY_NO_PDL, g);
+    const cudaError_t e = grouped_plan(ps, n_groups, n_pos, max_group_len, 0u, g);
     if (e != cudaSuccess) return e;
     return grouped_expand(g, y, ld_y, ps, perm, gstarts, gslot, n_groups, n_pos, n_rows, n_slots, nullptr, nullptr,
                           v, ld_v, status, stream);

@@ -101,7 +101,8 @@ cudaError_t launch_bgmv_grouped_shrink(const bf16_t* x, int ld_x, int h_in, cons
                                        bf16_t* vl, int32_t* status, cudaStream_t stream);
 
 // The grouped pair with an fp32 intermediate (the standalone SGMV calls):
-// v[row][j] (ld_v) instead of the planes; r_slot <= 64.  Plain stream order.
+// v[row][j] (ld_v) instead of the planes; r_slot <= 64.  Programmatic
+// dependent launch, as lora_apply's default ordering.
 cudaError_t launch_group_shrink_f32(float* v, int ld_v, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
                                     const int32_t* perm, const int32_t* gstarts, const int32_t* gslot, int n_groups,
                                     int n_pos, int max_group_len, int n_rows, int n_slots, int32_t* status,
@@ -114,8 +115,8 @@ cudaError_t launch_group_expand_f32(bf16_t* y, int ld_y, const float* v, int ld_
 // The grouped pair driven by per-row adapter ids (the standalone BGMV calls,
 // no gather metadata): unit = (slot, run of 16 rows with that id, in row
 // order), found by each CTA with a block-wide scan of the ids.  fp32 v;
-// r_slot <= 64 and at most 65536 units (bgmv_ids_supported).  Plain stream
-// order.
+// r_slot <= 64 and at most 65536 units (bgmv_ids_supported).  Programmatic
+// dependent launch, as lora_apply's default ordering.
 bool bgmv_ids_supported(int r_slot, int n_rows, int n_slots);
 cudaError_t launch_bgmv_ids_shrink_f32(float* v, int ld_v, const bf16_t* x, int ld_x, int h_in, const ProjSet& ps,
                                        const int32_t* ids, int n_rows, int n_slots, int32_t* status,
