@@ -150,8 +150,8 @@ ROUTE_KERNELS = {
 NCU_TRAFFIC = {
     "llama3b_decode": {"files": ['bgmv_fused.cu', 'decode_common.cuh', 'common.cuh', 'cluster.cuh'], "src": "c3d91c968f69f3f4",
              "bytes_per_call": 3442240},
-    "stress70b": {"files": ['bgmv_grouped.cu', 'decode_common.cuh', 'common.cuh', 'cluster.cuh'], "src": "e5e51dcc0ff9a405",
-             "bytes_per_call": 988068096},
+    "stress70b": {"files": ['bgmv_grouped.cu', 'decode_common.cuh', 'common.cuh', 'cluster.cuh'], "src": "5d6b34e0b472f189",
+             "bytes_per_call": 987991680},
     "mistral7b_prefill": {"files": ['sgmv_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh', 'cluster.cuh'], "src": "8bc12fda24a1f2bd",
              "bytes_per_call": 2061036160},
     "merge_mistral7b": {"files": ['merge.cu', 'merge_tc.cu', 'tc_common.cuh', 'tmap.cpp', 'common.cuh', 'cluster.cuh'], "src": "868105680b61064e",
@@ -162,7 +162,7 @@ NCU_TRAFFIC = {
              "bytes_per_call": 113187840},
     # captured on 2 layers, scaled to the 28 of a step (every layer has the same shapes)
     "linear_llama3b_decode": {"files": ['linear_swap.cu', 'bgmv_grouped.cu', 'tc_common.cuh', 'tmap.cpp', 'decode_common.cuh', 'common.cuh', 'cluster.cuh'],
-             "src": "2811350d3e51a100", "bytes_per_step": 1603073024},
+             "src": "eda5c99cc28c95a4", "bytes_per_step": 1603022848},
 }
 
 
